@@ -1,0 +1,222 @@
+"""CPU oracle for the mixed-precision optimizer step - TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never does, and
+this package imports nothing from the product: the two sides share only the
+seeded input generators in ``workloads/``.
+
+The arithmetic lives in ``oracle.c`` (plain C, single-threaded, its own
+number-format converters); this module only marshals numpy arrays into it.
+16-bit and 8-bit floating-point buffers travel as raw bit patterns
+(``uint16`` / ``uint8`` arrays); fp32 buffers as ``float32``.
+
+Dtype names: ``"f32"``, ``"f16"``, ``"bf16"``, ``"e4m3fn"``, ``"e5m2"``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_CODES = {"f32": 0, "f16": 1, "bf16": 2, "e4m3fn": 3, "e5m2": 4}
+_lock = threading.Lock()
+_lib = None
+
+P = ctypes.c_void_p
+I64P = ctypes.POINTER(ctypes.c_int64)
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so next to it (gcc, no CUDA)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC",
+                               "-shared", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = ctypes.CDLL(build())
+            L.orc_fmt_max.restype = ctypes.c_double
+            L.orc_fmt_max.argtypes = [ctypes.c_int]
+            L.orc_decode.argtypes = [ctypes.c_int, P, P, ctypes.c_int64]
+            L.orc_encode.argtypes = [ctypes.c_int, P, P, ctypes.c_int64]
+            L.orc_unscale_check.argtypes = [ctypes.c_int, P, I64P, ctypes.c_int,
+                                            ctypes.c_float, P, ctypes.c_int]
+            L.orc_update_scale.argtypes = [P, P, P, ctypes.c_float, ctypes.c_float,
+                                           ctypes.c_int32, P, ctypes.c_int]
+            L.orc_adamw_master_step.argtypes = (
+                [ctypes.c_int, P, P, P, P, ctypes.c_int, P, I64P, P, ctypes.c_int32, P]
+                + [ctypes.c_double] * 5 + [P, P])
+            L.orc_fp8_quant_tensorwise.argtypes = [P, ctypes.c_int, ctypes.c_int64,
+                                                   ctypes.c_int64, ctypes.c_int,
+                                                   ctypes.c_double, P, P, P, P, ctypes.c_int]
+            _lib = L
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"], "oracle buffers must be C-contiguous"
+    return a.ctypes.data_as(P)
+
+
+def _ptr_array(arrs):
+    return (P * max(1, len(arrs)))(*[(_ptr(a) if a is not None else None) for a in arrs])
+
+
+def _numels(arrs):
+    return (ctypes.c_int64 * max(1, len(arrs)))(*[a.size for a in arrs])
+
+
+def _bits_dtype(dt: str):
+    return {"f32": np.float32, "f16": np.uint16, "bf16": np.uint16,
+            "e4m3fn": np.uint8, "e5m2": np.uint8}[dt]
+
+
+# ---------------------------------------------------------------- converters
+def fmt_max(dt: str) -> float:
+    """Largest finite magnitude of a format, from its bit-layout definition."""
+    return lib().orc_fmt_max(_CODES[dt])
+
+
+def decode(dt: str, bits: np.ndarray) -> np.ndarray:
+    """Raw bit patterns of format ``dt`` -> float32 values."""
+    bits = np.ascontiguousarray(bits, dtype=_bits_dtype(dt))
+    out = np.empty(bits.shape, np.float32)
+    lib().orc_decode(_CODES[dt], _ptr(bits), _ptr(out), bits.size)
+    return out
+
+
+def encode(dt: str, x: np.ndarray) -> np.ndarray:
+    """float32 values -> round-to-nearest-even bit patterns of format ``dt``
+    (overflow: infinity, or NaN for e4m3fn; NaN: positive canonical NaN)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, _bits_dtype(dt))
+    lib().orc_encode(_CODES[dt], _ptr(x), _ptr(out), x.size)
+    return out
+
+
+# ------------------------------------------------------------------ the step
+def unscale_check(grads, dt: str, scale: float, found_inf: int = 0, inplace: bool = False) -> int:
+    """OR of !isfinite(g * (1/S)) over every element of every tensor."""
+    fi = np.array([found_inf], np.int32)
+    lib().orc_unscale_check(len(grads), _ptr_array(grads), _numels(grads), _CODES[dt],
+                            ctypes.c_float(scale), _ptr(fi), int(inplace))
+    return int(fi[0])
+
+
+def update_scale(scale: float, tracker: int, found_inf: int, growth: float, backoff: float,
+                 interval: int, amax: np.ndarray | None = None):
+    """One pass of the dynamic scale state machine. Returns (scale, tracker, found_inf)
+    and zeroes ``amax`` in place when given."""
+    s = np.array([scale], np.float32)
+    t = np.array([tracker], np.int32)
+    f = np.array([found_inf], np.int32)
+    n = 0 if amax is None else amax.size
+    lib().orc_update_scale(_ptr(s), _ptr(t), _ptr(f), ctypes.c_float(growth),
+                           ctypes.c_float(backoff), int(interval),
+                           _ptr(amax) if n else None, n)
+    return float(s[0]), int(t[0]), int(f[0])
+
+
+def adamw_master_step(master, exp_avg, exp_avg_sq, grads, gdt: str, bf16_out, scale,
+                      found_inf: int, step: int, lr, beta1, beta2, eps, wd,
+                      amax_slot=None, amax: np.ndarray | None = None) -> int:
+    """FP32-master AdamW over a tensor list (in place); returns the new step count.
+    ``scale`` None means S = 1. ``bf16_out`` is a list of uint16 arrays or None."""
+    n = len(master)
+    sc = None if scale is None else np.array([scale], np.float32)
+    st = np.array([step], np.int32)
+    slots = None if amax_slot is None else np.ascontiguousarray(amax_slot, np.int32)
+    lib().orc_adamw_master_step(
+        n, _ptr_array(master), _ptr_array(exp_avg), _ptr_array(exp_avg_sq),
+        _ptr_array(grads), _CODES[gdt], _ptr_array(bf16_out) if bf16_out else None,
+        _numels(master), _ptr(sc) if sc is not None else None, int(found_inf), _ptr(st),
+        lr, beta1, beta2, eps, wd,
+        _ptr(slots) if slots is not None else None,
+        _ptr(amax) if amax is not None else None)
+    return int(st[0])
+
+
+def fp8_quant_tensorwise(x: np.ndarray, xdt: str, rows: int, cols: int, fp8: str,
+                         eps: float = 1e-12, transposed: bool = True, amax: float | None = None):
+    """Returns (q [rows*cols] uint8, q_t [cols*rows] uint8 or None, inv_scale, amax)."""
+    x = np.ascontiguousarray(x)
+    assert x.size == rows * cols
+    out = np.empty(rows * cols, np.uint8)
+    out_t = np.empty(rows * cols, np.uint8) if transposed else None
+    inv = np.zeros(1, np.float32)
+    am = np.array([0.0 if amax is None else amax], np.float32)
+    lib().orc_fp8_quant_tensorwise(_ptr(x), _CODES[xdt], rows, cols, _CODES[fp8], eps,
+                                   _ptr(out), _ptr(out_t) if out_t is not None else None,
+                                   _ptr(inv), _ptr(am), int(amax is not None))
+    return out, out_t, float(inv[0]), float(am[0])
+
+
+class AmpStepOracle:
+    """One optimizer step in the pages' order, composed from the functions above:
+
+    1. unscale + non-finite check of the scaled gradients (found_inf),
+    2. skip-or-step: FP32-master AdamW emitting the bf16 working copy,
+    3. for FP8 weights, tensorwise e4m3fn quantization of the bf16 copy
+       (row-major + transposed) from the amax folded in step 2,
+    4. the scale state machine, which also clears found_inf and amax.
+    """
+
+    def __init__(self, master, grad_dtype, lr, beta1, beta2, eps, weight_decay,
+                 init_scale, growth_factor, backoff_factor, growth_interval,
+                 emit_bf16=True, fp8_shapes=None, fp8_eps=1e-12):
+        self.master = [np.array(m, np.float32, copy=True) for m in master]
+        self.exp_avg = [np.zeros_like(m) for m in self.master]
+        self.exp_avg_sq = [np.zeros_like(m) for m in self.master]
+        self.bf16 = [np.zeros(m.size, np.uint16) for m in self.master] if emit_bf16 else None
+        self.gdt = grad_dtype
+        self.hyper = (lr, beta1, beta2, eps, weight_decay)
+        self.scale, self.tracker, self.step, self.found_inf = float(init_scale), 0, 0, 0
+        self.growth, self.backoff, self.interval = growth_factor, backoff_factor, growth_interval
+        # fp8_shapes: per tensor (rows, cols) or None; FP8 slots numbered in order
+        self.fp8_shapes = fp8_shapes
+        self.slots = None
+        self.fp8_eps = fp8_eps
+        if fp8_shapes is not None:
+            self.slots, k = [], 0
+            for sh in fp8_shapes:
+                self.slots.append(k if sh is not None else -1)
+                k += sh is not None
+            self.amax = np.zeros(max(k, 1), np.float32)
+            self.fp8 = [None] * len(master)
+            self.fp8_t = [None] * len(master)
+            self.inv_scale = np.zeros(max(k, 1), np.float32)
+        else:
+            self.amax = None
+
+    def run(self, grads):
+        """Apply one step with the given scaled gradients; returns found_inf."""
+        fi = unscale_check(grads, self.gdt, self.scale, found_inf=self.found_inf)
+        self.found_inf = fi
+        self.step = adamw_master_step(self.master, self.exp_avg, self.exp_avg_sq, grads,
+                                      self.gdt, self.bf16, self.scale, fi, self.step,
+                                      *self.hyper, amax_slot=self.slots, amax=self.amax)
+        if self.fp8_shapes is not None and not fi:
+            for i, sh in enumerate(self.fp8_shapes):
+                if sh is None:
+                    continue
+                s = self.slots[i]
+                q, qt, inv, _ = fp8_quant_tensorwise(self.bf16[i], "bf16", sh[0], sh[1],
+                                                     "e4m3fn", self.fp8_eps, True,
+                                                     amax=float(self.amax[s]))
+                self.fp8[i], self.fp8_t[i], self.inv_scale[s] = q, qt, inv
+        self.scale, self.tracker, self.found_inf = update_scale(
+            self.scale, self.tracker, self.found_inf, self.growth, self.backoff,
+            self.interval, self.amax)
+        return fi

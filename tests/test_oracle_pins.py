@@ -1,0 +1,401 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Nothing here compares the oracle with itself: every expected value is either
+printed on the pages (fixtures under tests/golden/, each with its citation),
+a closed form, an independent library routine (numpy / torch CPU casts,
+torch.optim.AdamW), an invariant, or brute force on tiny inputs.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from workloads import amp_config, host_grads, host_master
+
+F32 = np.float32
+
+
+def f32(x):
+    return np.float32(x)
+
+
+# ------------------------------------------------------------------ formats
+def test_format_constants(golden):
+    g = golden("format_constants.json")
+    assert O.fmt_max("f16") == g["max"]["f16"]
+    assert O.fmt_max("e4m3fn") == g["max"]["e4m3fn"]
+    assert O.fmt_max("e5m2") == g["max"]["e5m2"]
+    def two_digits(v):            # the pages print these to two significant digits
+        return float(f"{v:.1e}")
+    assert two_digits(O.fmt_max("bf16")) == g["max"]["bf16_approx"]
+    # smallest positive normal: exponent field 1, fraction 0
+    assert two_digits(O.decode("f16", np.array([0x0400]))[0]) == g["min_normal_approx"]["f16"]
+    assert two_digits(O.decode("bf16", np.array([0x0080]))[0]) == g["min_normal_approx"]["bf16"]
+    # bit layouts: the fraction width sets the spacing just above 1.0
+    for dt, (s, e, m) in g["layouts"].items():
+        one = {"f16": 0x3C00, "bf16": 0x3F80}[dt]
+        assert O.decode(dt, np.array([one + 1]))[0] - 1.0 == 2.0 ** -m
+        # exponent width: max exponent field gives inf (IEEE specials)
+        assert np.isinf(O.decode(dt, np.array([((1 << e) - 1) << m]))[0])
+
+
+def test_decode_f16_exhaustive_vs_numpy():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ours = O.decode("f16", bits)
+    ref = bits.view(np.float16).astype(np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+@pytest.mark.parametrize("dt,tdt", [("bf16", torch.bfloat16), ("e4m3fn", torch.float8_e4m3fn),
+                                     ("e5m2", torch.float8_e5m2)])
+def test_decode_exhaustive_vs_torch(dt, tdt):
+    n = 1 << (16 if dt == "bf16" else 8)
+    bits = np.arange(n, dtype=np.uint32).astype(np.uint16 if dt == "bf16" else np.uint8)
+    ours = O.decode(dt, bits)
+    tb = torch.from_numpy(bits.view(np.int16) if dt == "bf16" else bits.view(np.int8))
+    ref = tb.view(tdt).to(torch.float32).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+def _rounding_class_sweep():
+    """All 2^20 values of the top 20 bits of an fp32 pattern, each with the
+    low 12 bits in {0, 1, 0x7FF, 0x800, 0x801, 0xFFF}: every sign, exponent and
+    kept-fraction combination of the 8/16-bit formats, with the round bit and
+    the sticky bits below it both clear, set and at the tie."""
+    hi = (np.arange(1 << 20, dtype=np.uint64) << 12)
+    lows = np.array([0, 1, 0x7FF, 0x800, 0x801, 0xFFF], np.uint64)
+    return (hi[:, None] | lows[None, :]).astype(np.uint32).ravel().view(np.float32)
+
+
+@pytest.fixture(scope="module")
+def sweep():
+    return _rounding_class_sweep()
+
+
+def test_encode_f16_vs_numpy(sweep):
+    ours = O.encode("f16", sweep)
+    with np.errstate(over="ignore", invalid="ignore"):
+        ref = sweep.astype(np.float16)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours.view(np.float16)), nan)
+    assert np.all(ours[nan] == 0x7E00)            # canonical NaN reading
+    assert np.array_equal(ours[~nan], ref[~nan].view(np.uint16))
+
+
+def test_encode_bf16_vs_torch(sweep):
+    ours = O.encode("bf16", sweep)
+    ref = torch.from_numpy(sweep).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    nan = np.isnan(sweep)
+    assert np.all(ours[nan] == 0x7FC0)
+    assert np.array_equal(ours[~nan], ref[~nan])
+
+
+@pytest.mark.parametrize("dt,tdt", [("e4m3fn", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)])
+def test_encode_fp8_vs_torch_in_range(sweep, dt, tdt):
+    """On the range the quantizer feeds the encoder (|y| <= fp8_max after the
+    clamp) the oracle's RNE encoder agrees bit for bit with torch's cast."""
+    m = O.fmt_max(dt)
+    x = sweep[np.abs(sweep) <= m]
+    ours = O.encode(dt, x)
+    ref = torch.from_numpy(x).to(tdt).view(torch.int8).numpy().view(np.uint8)
+    assert np.array_equal(ours, ref)
+
+
+def test_encode_fp8_overflow_and_specials():
+    # e4m3fn has no infinity: beyond the largest finite value rounding overflows to NaN
+    assert O.encode("e4m3fn", np.array([448.0, 464.0, 465.0, np.inf, np.nan], F32)).tolist() == \
+        [0x7E, 0x7E, 0x7F, 0x7F, 0x7F]
+    # e5m2: IEEE-like; 61440 is the tie between 57344 and 2^16 -> even -> inf
+    assert O.encode("e5m2", np.array([57344.0, 61439.0, 61440.0, -np.inf, np.nan], F32)).tolist() == \
+        [0x7B, 0x7B, 0x7C, 0xFC, 0x7E]
+    # signed zeros and the smallest subnormals
+    assert O.encode("e4m3fn", np.array([-0.0, 2.0 ** -9, -2.0 ** -10, 2.0 ** -10 * 1.0001], F32)).tolist() == \
+        [0x80, 0x01, 0x80, 0x01]
+
+
+# -------------------------------------------------------- worked examples
+def test_fp16_small_update_lost(golden):
+    g = golden("fp16_small_update_example.json")
+    w = O.encode("f16", np.array([g["w0"]], F32))
+    u = O.decode("f16", O.encode("f16", np.array([g["update"]], F32)))
+    s = O.decode("f16", w)[0] + u[0]            # fp32 sum of the two fp16 values
+    res = O.decode("f16", O.encode("f16", np.array([s], F32)))[0]
+    assert res == g["fp16_result"]
+    spacing = O.decode("f16", w + 1)[0] - O.decode("f16", w)[0]
+    assert abs(spacing - g["fp16_spacing_at_w0_approx"]) < 0.1 * g["fp16_spacing_at_w0_approx"]
+    # the fp32 master keeps it
+    assert f32(g["w0"]) + f32(g["update"]) != f32(g["w0"])
+
+
+def test_bf16_master_copy_example(golden):
+    g = golden("master_weight_bf16_example.json")
+    w0, d = f32(g["w0"]), f32(g["delta"])
+    w_bits = O.encode("bf16", np.array([w0], F32))
+    assert O.decode("bf16", w_bits)[0] - O.decode("bf16", w_bits - 1)[0] == g["bf16_spacing_at_w0"]
+    assert O.decode("bf16", w_bits - 1)[0] == g["bf16_next_below_w0"]
+    master, bf_only = w0, O.decode("bf16", w_bits)[0]
+    copies, only = [], []
+    for _ in range(g["steps"]):
+        master = F32(master + d)                     # fp32 master update
+        copies.append(float(O.decode("bf16", O.encode("bf16", np.array([master], F32)))[0]))
+        bf_only = O.decode("bf16", O.encode("bf16", np.array([F32(bf_only + d)], F32)))[0]
+        only.append(float(bf_only))
+    assert copies == g["bf16_copy_of_fp32_master"]
+    assert only == g["bf16_only_parameter"]
+
+
+def test_bf16_master_copy_example_through_adamw(golden):
+    """Same example driven by the oracle's AdamW: a constant gradient with
+    wd = 0 gives the bias-corrected update lr * g / (|g| + eps) = lr every
+    step, so lr = 0.001 reproduces the page's -0.001 per step."""
+    g = golden("master_weight_bf16_example.json")
+    master = [np.array([g["w0"]], F32)]
+    m, v = [np.zeros(1, F32)], [np.zeros(1, F32)]
+    bf = [np.zeros(1, np.uint16)]
+    step, copies, masters = 0, [], []
+    for _ in range(g["steps"]):
+        grads = [np.array([1.0], F32)]
+        step = O.adamw_master_step(master, m, v, grads, "f32", bf, None, 0, step,
+                                   -g["delta"], 0.9, 0.999, 1e-12, 0.0)
+        copies.append(float(O.decode("bf16", bf[0])[0]))
+        masters.append(float(master[0][0]))
+    assert copies == g["bf16_copy_of_fp32_master"]
+    for k, mv in enumerate(masters, 1):   # closed form 1.25 - 0.001 k, to fp32 rounding
+        assert abs(mv - (g["w0"] + k * g["delta"])) <= 4 * 2.0 ** -23 * 1.25
+    assert step == g["steps"]
+
+
+# ---------------------------------------------------------- scale machine
+def _run_trace(init, interval, inf_steps, steps):
+    s, t, opt = init, 0, 0
+    rows = []
+    for k in range(1, steps + 1):
+        fi = int(k in inf_steps)
+        opt += 0 if fi else 1
+        s, t, fi_after = O.update_scale(s, t, fi, 2.0, 0.5, interval)
+        assert fi_after == 0
+        rows.append((s, t, opt, bool(fi)))
+    return rows
+
+
+def test_scaler_trace_tiny(golden):
+    tr = golden("scaler_traces.json")["traces"]["tiny_interval2_inf_at_2"]
+    rows = _run_trace(tr["init_scale"], tr["growth_interval"], tr["inf_steps"], tr["steps"])
+    assert [r[0] for r in rows] == tr["scale"]
+    assert [r[1] for r in rows] == tr["tracker"]
+    assert [r[3] for r in rows] == tr["skipped"]
+
+
+def test_scaler_trace_interval10(golden):
+    tr = golden("scaler_traces.json")["traces"]["interval10_inf_at_7_27_47"]
+    rows = _run_trace(tr["init_scale"], tr["growth_interval"], tr["inf_steps"], tr["steps"])
+    grew = [k for k in range(2, tr["steps"] + 1) if rows[k - 1][0] > rows[k - 2][0]]
+    assert grew == tr["growth_at"]
+    assert rows[-1][0] == tr["final_scale"] and rows[-1][1] == tr["final_tracker"]
+
+
+def test_scaler_growth_overflow_keeps_scale_and_clears_amax():
+    big = float(np.finfo(np.float32).max)
+    amax = np.array([3.0, 5.0], F32)
+    s, t, fi = O.update_scale(big, 0, 0, 2.0, 0.5, 1, amax)
+    assert s == big and t == 0 and fi == 0 and np.all(amax == 0)
+
+
+# --------------------------------------------------------- unscale / check
+def test_unscale_check_detects_and_unscales():
+    S = 65536.0
+    g = [np.array([1.0, -2.0, 0.5], np.float16).view(np.uint16).copy(),
+         (np.arange(257, dtype=np.float16) * np.float16(0.25)).view(np.uint16).copy()]
+    assert O.unscale_check([a.copy() for a in g], "f16", S) == 0
+    for val in (np.inf, -np.inf, np.nan):
+        h = [a.copy() for a in g]
+        h[1][256] = np.array([val], np.float16).view(np.uint16)[0]     # tail element
+        assert O.unscale_check(h, "f16", S) == 1
+    # never cleared: an incoming flag survives a clean list
+    assert O.unscale_check([a.copy() for a in g], "f16", S, found_inf=1) == 1
+    # S = 0: 1/S = inf, so even 0 * inf = NaN is non-finite
+    assert O.unscale_check([np.zeros(4, np.uint16)], "f16", 0.0) == 1
+    # finite fp16 times a huge 1/S overflows fp32
+    assert O.unscale_check([np.array([65504.0], np.float16).view(np.uint16)], "f16", 1e-35) == 1
+    # in place: the stored value becomes fp16(g / S)
+    h = [a.copy() for a in g]
+    O.unscale_check(h, "f16", S, inplace=True)
+    np.testing.assert_array_equal(h[0].view(np.float16).astype(np.float64),
+                                  (g[0].view(np.float16).astype(np.float64) / S)
+                                  .astype(np.float16).astype(np.float64))
+
+
+# ------------------------------------------------------------------ AdamW
+def _adamw_oracle(p0, grads_seq, lr, b1, b2, eps, wd, gdt="f32", scale=None):
+    master = [p.copy() for p in p0]
+    m = [np.zeros_like(p) for p in p0]
+    v = [np.zeros_like(p) for p in p0]
+    step = 0
+    for g in grads_seq:
+        step = O.adamw_master_step(master, m, v, g, gdt, None, scale, 0, step, lr, b1, b2, eps, wd)
+    return master, m, v, step
+
+
+def test_adamw_first_step_closed_form():
+    """t = 1 from m = v = 0: m_hat = g and v_hat = g^2 exactly, so
+    p1 = p0 (1 - lr wd) - lr g / (|g| + eps)."""
+    rng = np.random.default_rng(1)
+    p0 = [rng.standard_normal(1000).astype(F32)]
+    g = [rng.standard_normal(1000).astype(F32) * F32(1e-3)]
+    lr, wd, eps = 1e-3, 0.01, 1e-8
+    p, m, v, step = _adamw_oracle(p0, [g], lr, 0.9, 0.999, eps, wd)
+    p0d, gd = p0[0].astype(np.float64), g[0].astype(np.float64)
+    exact = p0d * (1 - lr * wd) - lr * gd / (np.abs(gd) + eps)
+    # fp32 rounding of each term: relative to the size of the terms, not of
+    # their difference (p0 (1 - lr wd) and lr can nearly cancel)
+    assert np.all(np.abs(p[0] - exact) <= 1e-6 * (np.abs(p0d) + lr))
+    np.testing.assert_allclose(m[0], 0.1 * gd, rtol=1e-6)
+    np.testing.assert_allclose(v[0], 0.001 * gd * gd, rtol=1e-6)
+    assert step == 1
+
+
+def test_adamw_pure_decay_closed_form():
+    """g = 0: both moments stay 0, the Adam term vanishes and each step only
+    multiplies by the fp32 factor (1 - lr wd): p_t = p0 * decay^t in fp32."""
+    p0 = [np.array([1.0, -0.5, 3.0e-3, 0.0], F32)]
+    lr, wd, T = 1e-2, 0.1, 25
+    p, m, v, _ = _adamw_oracle(p0, [[np.zeros(4, F32)]] * T, lr, 0.9, 0.95, 1e-8, wd)
+    expect = p0[0].copy()
+    decay = F32(1.0 - lr * wd)
+    for _ in range(T):
+        expect = (expect * decay).astype(F32)
+    assert np.array_equal(p[0], expect)
+    assert not m[0].any() and not v[0].any()
+
+
+def test_adamw_matches_torch_optim():
+    """Independent library: torch.optim.AdamW on CPU fp32, 10 steps."""
+    rng = np.random.default_rng(7)
+    sizes = [1000, 4096, 257]
+    p0 = [rng.standard_normal(n).astype(F32) * F32(0.02) for n in sizes]
+    gseq = [[rng.standard_normal(n).astype(F32) * F32(1e-3) for n in sizes] for _ in range(10)]
+    hp = dict(lr=3e-4, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.1)
+    p, m, v, _ = _adamw_oracle(p0, gseq, hp["lr"], *hp["betas"], hp["eps"], hp["weight_decay"])
+    tp = [torch.nn.Parameter(torch.from_numpy(x.copy())) for x in p0]
+    opt = torch.optim.AdamW(tp, foreach=False, fused=False, **hp)
+    for gs in gseq:
+        for t, g in zip(tp, gs):
+            t.grad = torch.from_numpy(g.copy())
+        opt.step()
+    for i, t in enumerate(tp):
+        st = opt.state[t]
+        for ours, ref in ((p[i], t.detach().numpy()), (m[i], st["exp_avg"].numpy()),
+                          (v[i], st["exp_avg_sq"].numpy())):
+            floor = 1e-6 * np.sqrt(np.mean(ref.astype(np.float64) ** 2))
+            err = np.abs(ours.astype(np.float64) - ref)
+            assert np.all(err <= 1e-6 * np.maximum(np.abs(ours), np.abs(ref)) + floor)
+
+
+def test_adamw_skip_changes_nothing():
+    rng = np.random.default_rng(3)
+    master = [rng.standard_normal(300).astype(F32)]
+    m, v = [rng.standard_normal(300).astype(F32)], [rng.random(300).astype(F32)]
+    bf = [np.full(300, 0x1234, np.uint16)]
+    snap = [a[0].copy() for a in (master, m, v, bf)]
+    amax = np.array([7.0], F32)
+    st = O.adamw_master_step(master, m, v, [np.full(300, 0x3C00, np.uint16)], "f16", bf, 65536.0,
+                             1, 5, 1e-3, 0.9, 0.999, 1e-8, 0.01, amax_slot=[0], amax=amax)
+    assert st == 5 and amax[0] == 7.0
+    for a, s in zip((master, m, v, bf), snap):
+        assert np.array_equal(a[0], s)
+
+
+def test_adamw_bf16_emit_and_amax():
+    rng = np.random.default_rng(4)
+    master = [rng.standard_normal(n).astype(F32) for n in (100, 37)]
+    m = [np.zeros_like(x) for x in master]
+    v = [np.zeros_like(x) for x in master]
+    bf = [np.zeros(x.size, np.uint16) for x in master]
+    amax = np.zeros(1, F32)
+    O.adamw_master_step(master, m, v, [np.zeros(x.size, F32) for x in master], "f32", bf, None,
+                        0, 0, 1e-3, 0.9, 0.999, 1e-8, 0.0, amax_slot=[-1, 0], amax=amax)
+    ref = [torch.from_numpy(x).to(torch.bfloat16) for x in master]
+    for b, r in zip(bf, ref):
+        assert np.array_equal(b, r.view(torch.int16).numpy().view(np.uint16))
+    assert amax[0] == ref[1].abs().max().float().item()
+
+
+# ----------------------------------------------------------- FP8 quantizer
+@pytest.mark.parametrize("fmt,top", [("e4m3fn", 0x7E), ("e5m2", 0x7B)])
+def test_quant_amax_maps_to_fp8_max(fmt, top):
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((33, 70)).astype(F32)
+    x[5, 7] = -np.abs(x).max() * 3          # unique largest magnitude, negative
+    x[20, 69] = -x[5, 7]                    # and its positive twin
+    q, qt, inv, amax = O.fp8_quant_tensorwise(x.ravel(), "f32", 33, 70, fmt)
+    q = q.reshape(33, 70)
+    assert amax == np.abs(x).max()
+    assert q[5, 7] == (top | 0x80) and q[20, 69] == top
+    deq = O.decode(fmt, q) * inv
+    assert np.max(np.abs(deq)) == pytest.approx(amax, rel=1e-6)
+    assert np.array_equal(qt.reshape(70, 33), q.T)       # the column-major copy
+
+
+@pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
+def test_quant_zero_tensor_uses_eps(fmt):
+    q, qt, inv, amax = O.fp8_quant_tensorwise(np.zeros(64 * 32, np.uint16), "bf16", 64, 32, fmt,
+                                              eps=1e-12)
+    assert amax == 0.0 and not q.any() and not qt.any()
+    assert inv == F32(1e-12 / O.fmt_max(fmt))
+
+
+@pytest.mark.parametrize("fmt,tdt", [("e4m3fn", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)])
+@pytest.mark.parametrize("shape", [(1, 1), (3, 5), (17, 31), (64, 130)])
+def test_quant_vs_torch_ops(fmt, tdt, shape):
+    """Tiny tensors: torch CPU ops (abs-max, fp64 scale, fp32 multiply,
+    clamp, library fp8 cast) give the same bytes and inv_scale."""
+    rng = np.random.default_rng(shape[0] * 100 + shape[1])
+    x = (rng.standard_normal(shape) * 10 ** rng.uniform(-3, 3)).astype(F32)
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    bits = xb.view(torch.int16).numpy().view(np.uint16).ravel()
+    q, qt, inv, amax = O.fp8_quant_tensorwise(bits, "bf16", *shape, fmt)
+    mx = float(torch.finfo(tdt).max)
+    am = xb.float().abs().max()
+    sc = mx / am.double().clamp(min=1e-12)
+    ref = (xb.float() * sc).clamp(-mx, mx).to(tdt).view(torch.int8).numpy().view(np.uint8)
+    assert amax == am.item()
+    assert np.array_equal(q, ref.ravel())
+    assert inv == sc.reciprocal().float().item()
+    assert np.array_equal(qt.reshape(shape[1], shape[0]), ref.T)
+
+
+def test_quant_dequant_error_bound():
+    """RNE error: |deq - x| <= half the fp8 spacing at |x*scale|, mapped back."""
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal(4096).astype(F32)
+    q, _, inv, amax = O.fp8_quant_tensorwise(x, "f32", 64, 64, "e4m3fn", transposed=False)
+    y = np.abs(x.astype(np.float64) * F32(448.0 / amax))
+    e = np.floor(np.log2(np.maximum(y, 2.0 ** -6)))
+    half_spacing = 0.5 * 2.0 ** (e - 3)
+    err = np.abs(O.decode("e4m3fn", q).astype(np.float64) - x.astype(np.float64) * F32(448.0 / amax))
+    assert np.all(err <= half_spacing * (1 + 1e-6))
+
+
+# ------------------------------------------------------------ composition
+def test_tiny_config_trace_through_oracle_step(golden):
+    """Config 'tiny': the composed step reproduces the hand-derived scaler
+    trace, skips exactly step 2 and leaves the state untouched there."""
+    cfg = amp_config("tiny")
+    tr = golden("scaler_traces.json")["traces"]["tiny_interval2_inf_at_2"]
+    orc = O.AmpStepOracle(host_master(cfg), cfg.grad_dtype, cfg.lr, cfg.beta1, cfg.beta2, cfg.eps,
+                          cfg.weight_decay, cfg.init_scale, cfg.growth_factor, cfg.backoff_factor,
+                          cfg.growth_interval)
+    for k in range(1, cfg.steps + 1):
+        before = [x.copy() for x in orc.master]
+        fi = orc.run(host_grads(cfg, k, orc.scale))
+        assert bool(fi) == tr["skipped"][k - 1]
+        if fi:
+            assert all(np.array_equal(a, b) for a, b in zip(before, orc.master))
+        assert orc.scale == tr["scale"][k - 1] and orc.tracker == tr["tracker"][k - 1]
+        assert orc.step == tr["optimizer_step"][k - 1]
