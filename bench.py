@@ -1,0 +1,460 @@
+"""Benchmark of the fused mixed-precision optimizer step on GB300.
+
+Default workload: the 8B Llama-3-shaped parameter set (8,030,261,248 params in
+291 tensors; hidden 4096, 32 layers, GQA 32q/8kv, ffn 14336, vocab 128256),
+fp32 master + m + v, fp16 gradients scaled by a dynamic loss scale, AdamW
+emitting the bf16 working copy and, for the 224 linear weights, e4m3fn copies
+with their transposed (column-major) copies.  One step = unscale/check ->
+AdamW (+bf16, +amax) -> FP8 quantization -> scale update, all resident in HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload llama3_8b|llama_1b|gpt2_small|fp8_sweep] [--no-e2e]
+
+Prints one JSON line.  Under torchrun (N > 1) every rank holds its own
+parameter shard of the same size (weak scaling) and the per-step non-finite
+flag is combined across ranks with an all-reduce(MAX) before the update.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HBM_FALLBACK_GBS = 6800.0
+BF16_FALLBACK_TFLOPS = 1900.0
+L2_BYTES = 129 * 2 ** 20
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return HBM_FALLBACK_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling while the timed region runs."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc = index, None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 8:
+                try:
+                    rows.append((float(f[0]), float(f[1]), f[4:8]))
+                except ValueError:
+                    pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, fl in rows for i, v in enumerate(fl)
+                          if v.lower() == "active"})
+        load = [r[0] for r in rows]
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- workloads
+def build_step(workload: str, device, seed: int):
+    """Allocate a workload's device state; returns (step_obj, info)."""
+    import torch
+
+    from loss_scaling_master_gb300 import AmpOptimizerStep
+    from workloads import amp_config, device_fill_normal, device_generator, tensor_sigmas
+
+    cfg = amp_config(workload)
+    gdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[cfg.grad_dtype]
+    gen = device_generator(device, seed, 1)
+    master = [device_fill_normal(torch.empty(s.numel, device=device), cfg.master_sigma, gen)
+              for s in cfg.specs]
+    sig = tensor_sigmas(cfg, seed)
+    grads = [device_fill_normal(torch.empty(s.numel, dtype=gdt, device=device),
+                                float(sig[i] * cfg.init_scale), gen)
+             for i, s in enumerate(cfg.specs)]
+    fp8_shapes = [(s.rows, s.cols) if s.fp8 else None for s in cfg.specs] \
+        if cfg.fp8_weights else None
+    step = AmpOptimizerStep(master, grads, lr=cfg.lr, beta1=cfg.beta1, beta2=cfg.beta2,
+                            eps=cfg.eps, weight_decay=cfg.weight_decay,
+                            init_scale=cfg.init_scale, growth_factor=cfg.growth_factor,
+                            backoff_factor=cfg.backoff_factor,
+                            growth_interval=cfg.growth_interval, fp8_shapes=fp8_shapes)
+    n = sum(s.numel for s in cfg.specs)
+    n8 = sum(s.numel for s in cfg.specs if s.fp8) if cfg.fp8_weights else 0
+    gbytes = {"f16": 2, "bf16": 2, "f32": 4}[cfg.grad_dtype]
+    info = {"cfg": cfg, "params": n, "fp8_params": n8, "tensors": len(cfg.specs),
+            # algorithmic bytes per step, per kernel
+            "bytes_check": gbytes * n,
+            "bytes_adamw": (gbytes + 12) * n + 12 * n + 2 * n,
+            "bytes_quant": 4 * n8,
+            "grad_bytes": gbytes * n}
+    return step, info
+
+
+def run_ours(args, rank, world, device):
+    import torch
+    import torch.distributed as dist
+
+    import loss_scaling_master_gb300 as A
+
+    torch.cuda.set_device(device)
+    if args.workload == "fp8_sweep":
+        return run_fp8_sweep(args, rank, world, device)
+    step, info = build_step(args.workload, device, seed=1234 + rank)
+    n_params = info["params"]
+    stream = torch.cuda.Stream(device=device)
+    comb = None
+    if world > 1:
+        def comb():
+            dist.all_reduce(step.found_inf, op=dist.ReduceOp.MAX)
+
+    def one_step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        A.amp_unscale_check(step.L_g, step.scale, step.found_inf, stream=stream)
+        if comb is not None:
+            with torch.cuda.stream(stream):
+                comb()
+        if ev is not None:
+            ev[1].record(stream)
+        A.amp_adamw_master_step(step.L_master, step.L_m, step.L_v, step.L_g, step.L_b,
+                                step.scale, step.found_inf, step.step_count, *step.hyper,
+                                amax=step.amax if step.n_fp8 else None, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        if step.n_fp8:
+            A.fp8_quant_tensorwise_list(step.L_x8, step.L_q, step.L_qt, "e4m3fn", step.amax,
+                                        step.inv_scale, eps=step.fp8_eps,
+                                        skip_if=step.found_inf, stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+        A.amp_update_scale(step.scale, step.growth_tracker, step.found_inf, step.growth,
+                           step.backoff, step.interval, amax=step.amax if step.n_fp8 else None,
+                           n_amax=step.n_fp8, stream=stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    st0 = step.state()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t_begin = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_begin.record(stream)
+        for k in range(args.steps):
+            one_step(evs[k])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    ms_total = t_begin.elapsed_time(t_end)
+    st1 = step.state()
+    assert st1["step"] - st0["step"] == args.steps, "a timed step was skipped"
+    k_check = [e[0].elapsed_time(e[1]) for e in evs]
+    k_adamw = [e[1].elapsed_time(e[2]) for e in evs]
+    k_quant = [e[2].elapsed_time(e[3]) for e in evs]
+    ms_t = torch.tensor([ms_total], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_total = float(ms_t.item())
+    ms_step = ms_total / args.steps
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, step, info, stream, world)
+
+    if rank != 0:
+        step.close()
+        return None
+    peak, peak_kind = measured_peaks()
+    adamw_ms = statistics.mean(k_adamw)
+    achieved = info["bytes_adamw"] / (adamw_ms * 1e-3) / 1e9
+    total_bytes = info["bytes_check"] + info["bytes_adamw"] + info["bytes_quant"]
+    line = {
+        "metric": "fused AMP step params/s (unscale/check + FP32-master AdamW + bf16 emit "
+                  "+ tensorwise FP8 e4m3fn with transposed copy)",
+        "value": n_params * args.steps * world / (ms_total * 1e-3),
+        "unit": "params/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32 (master/m/v), f16 grads, bf16 + e4m3fn outputs",
+        "data": "synthetic (seeded N(0,0.02) masters, N(0,sigma*S) fp16 grads; no trained weights)",
+        "config": {"workload": f"{args.workload}: {info['params']:,} params in {info['tensors']} "
+                               f"tensors, {info['fp8_params']:,} FP8-emitted",
+                   "grad_dtype": info["cfg"].grad_dtype, "parallelism": f"dp{world} (sharded, weak)",
+                   "l2": "inputs larger than L2 (no flush needed)",
+                   "per_step_bytes": total_bytes},
+        "hbm_gbs_step": total_bytes / (ms_step * 1e-3) / 1e9,
+        "kernels_ms": {"unscale_check": statistics.mean(k_check),
+                       "adamw_master_step": adamw_ms,
+                       "fp8_quant_list": statistics.mean(k_quant)},
+        "fp8_quant_gbs": (info["bytes_quant"] / (statistics.mean(k_quant) * 1e-3) / 1e9)
+        if info["bytes_quant"] else None,
+        "roofline": {"bound": "hbm", "kernel": "amp_adamw_master_step",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "bytes_per_param": info["bytes_adamw"] / n_params,
+                     "traffic": None},
+        "clocks": clk.summary(),
+        "gpu_launches": args.steps * step.launches_per_step,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
+    step.close()
+    return line
+
+
+def run_e2e(args, step, info, stream, world):
+    """Same step through the public API, with each step's gradients copied
+    from pinned host memory and the scaler state read back, both timed."""
+    import torch
+    import torch.distributed as dist
+
+    nbytes = info["grad_bytes"]
+    host = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    dev_views, off = [], 0
+    for g in step.grads:
+        b = g.numel() * g.element_size()
+        dev_views.append((g.view(torch.uint8).view(-1), host[off:off + b]))
+        off += b
+    state_host = torch.empty(4, dtype=torch.int32, pin_memory=True)
+    # keep the gradients finite: copy the device grads to the host once
+    for d, h in dev_views:
+        h.copy_(d)
+    torch.cuda.synchronize()
+    packed = torch.empty(4, dtype=torch.int32, device=step.scale.device)
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for d, h in dev_views:
+                d.copy_(h, non_blocking=True)
+        step.step(stream=stream)
+        with torch.cuda.stream(stream):
+            packed[0:1].copy_(step.scale.view(torch.int32))
+            packed[1:2].copy_(step.growth_tracker)
+            packed[2:3].copy_(step.step_count)
+            packed[3:4].copy_(step.found_inf)
+            state_host.copy_(packed, non_blocking=True)
+
+    for _ in range(max(1, args.warmup // 2)):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    del host
+    return {"value": info["params"] * args.steps * world / (ms * 1e-3), "unit": "params/s",
+            "ms_per_step": ms / args.steps, "h2d_bytes_per_step": nbytes,
+            "d2h_bytes_per_step": 16,
+            "api": "AmpOptimizerStep.step() (C-ABI calls) + pinned H2D of the grads + D2H of "
+                   "{scale, tracker, step, found_inf}"}
+
+
+def run_fp8_sweep(args, rank, world, device):
+    """Standalone quantizer on the sweep matrices (bf16, row-major + transposed)."""
+    import torch
+
+    import loss_scaling_master_gb300 as A
+    from workloads import FP8_SWEEP_SHAPES, FP8_SWEEP_ZERO_SHAPE, device_generator
+
+    gen = device_generator(device, 99 + rank, 4)
+    mats = []
+    for (r, c) in FP8_SWEEP_SHAPES + [FP8_SWEEP_ZERO_SHAPE]:
+        x = torch.empty((r, c), dtype=torch.bfloat16, device=device)
+        if (r, c) == FP8_SWEEP_ZERO_SHAPE and len(mats) == len(FP8_SWEEP_SHAPES):
+            x.zero_()
+        else:
+            x.normal_(0.0, 1.0, generator=gen)
+        mats.append(x)
+    outs = [(torch.empty(x.shape, dtype=torch.uint8, device=device),
+             torch.empty((x.shape[1], x.shape[0]), dtype=torch.uint8, device=device))
+            for x in mats]
+    inv = torch.zeros(len(mats), device=device)
+    amax = torch.zeros(len(mats), device=device)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.Stream(device=device)
+    fmts = ["e4m3fn", "e5m2"]
+
+    def one(ev=None):
+        for f in fmts:
+            for i, x in enumerate(mats):
+                A.fp8_quant_tensorwise(x, f, outs[i][0], outs[i][1], inv[i:i + 1],
+                                       amax[i:i + 1], stream=stream)
+
+    for _ in range(args.warmup):
+        one()
+    torch.cuda.synchronize()
+    times = []
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for _ in range(args.steps):
+            with torch.cuda.stream(stream):
+                flush.fill_(1)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            one()
+            b.record(stream)
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+    ms = statistics.mean(times)
+    elems = sum(x.numel() for x in mats) * len(fmts)
+    peak, kind = measured_peaks()
+    gbs = 6 * elems / (ms * 1e-3) / 1e9
+    if rank != 0:
+        return None
+    return {"metric": "FP8 tensorwise quant GB/s (amax + e4m3fn/e5m2 cast + transposed copy)",
+            "value": gbs * world, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, fp8 out",
+            "data": "synthetic N(0,1) bf16 + one all-zero matrix",
+            "config": {"workload": "fp8_sweep [4096,4096],[8192,8192],[16384,5120],zero[4096,4096] "
+                                   "x {e4m3fn,e5m2}", "l2": "flushed between steps"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                         "frac": gbs / peak, "peak_kind": kind, "traffic": None},
+            "clocks": clk.summary(), "gpu_launches": args.steps * len(mats) * len(fmts) * 2}
+
+
+# ------------------------------------------------------------ CPU baseline
+def cpu_baseline(workload: str, seconds: float):
+    """The CPU oracle as it stands, single-threaded, on a bounded sample of
+    the workload: layer 0 of the parameter set (all of its tensors, FP8
+    copies included), timed for whole steps until ~`seconds` have passed."""
+    import numpy as np
+
+    import oracle as O
+    from workloads import AmpConfig, amp_config
+
+    cfg = amp_config(workload if workload != "fp8_sweep" else "llama3_8b")
+    specs = [s for s in cfg.specs if s.name.startswith(("l0.", "h0."))] or cfg.specs[:3]
+    sub = AmpConfig(cfg.name + "-layer0", specs, cfg.grad_dtype, cfg.steps, cfg.lr, cfg.beta1,
+                    cfg.beta2, cfg.eps, cfg.weight_decay, cfg.init_scale, cfg.growth_factor,
+                    cfg.backoff_factor, cfg.growth_interval, cfg.grad_sigma,
+                    fp8_weights=cfg.fp8_weights)
+    rng = np.random.default_rng(5)
+    master = [(rng.standard_normal(s.numel, dtype=np.float32) * np.float32(0.02)) for s in specs]
+    sig = 1e-4 if isinstance(cfg.grad_sigma, str) else float(cfg.grad_sigma)
+    grads = [(rng.standard_normal(s.numel, dtype=np.float32) * np.float32(sig * cfg.init_scale))
+             .astype(np.float16).view(np.uint16) for s in specs]
+    fp8_shapes = [(s.rows, s.cols) if s.fp8 else None for s in specs] if cfg.fp8_weights else None
+    orc = O.AmpStepOracle(master, "f16", cfg.lr, cfg.beta1, cfg.beta2, cfg.eps, cfg.weight_decay,
+                          cfg.init_scale, cfg.growth_factor, cfg.backoff_factor,
+                          cfg.growth_interval, fp8_shapes=fp8_shapes)
+    n = sum(s.numel for s in specs)
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        orc.run(grads)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or steps >= 50:
+            break
+    return {"value": n * steps / el, "unit": "params/s", "cores": 1, "kind": "oracle",
+            "sample": f"{len(specs)} tensors of {cfg.name} layer 0 ({n:,} params, "
+                      f"{sum(s.numel for s in specs if s.fp8):,} FP8-emitted), {steps} full steps "
+                      f"in {el:.1f} s, single-threaded C oracle"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    t0 = time.perf_counter()
+    cb = cpu_baseline(args.workload, args.cpu_seconds)
+    el = time.perf_counter() - t0
+    return {"impl": "reference", "metric": "fused AMP step params/s", "value": cb["value"],
+            "unit": "params/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32 (master/m/v), f16 grads",
+            "data": "synthetic", "config": {"workload": args.workload},
+            "cpu_baseline": cb,
+            "e2e": {"value": cb["value"], "unit": "params/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "note": f"the pages ship no runnable code; the reference arm is the CPU oracle "
+                    f"({el:.1f} s wall)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama3_8b",
+                    choices=["llama3_8b", "llama_1b", "gpt2_small", "fp8_sweep"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        import torch
+        if world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        line = run_ours(args, rank, world, torch.device("cuda", local))
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

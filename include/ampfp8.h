@@ -1,0 +1,236 @@
+/*
+ * ampfp8.h - C ABI of libampfp8.so: the per-step mixed-precision optimizer
+ * pipeline on one GPU (sm_103a).
+ *
+ *   amp_unscale_check        scaled low-precision gradients -> found_inf flag
+ *   amp_adamw_master_step    skip-on-inf + unscale + FP32-master AdamW
+ *                            + BF16 working copy (+ per-tensor amax fold)
+ *   fp8_quant_tensorwise     tensorwise dynamic FP8 cast (+ transposed copy)
+ *   fp8_quant_tensorwise_list  the same over a list of 2-D tensors
+ *   amp_update_scale         dynamic loss-scale state machine
+ *
+ * Sources the operations follow (page title, section):
+ *   [CH20]  "第20章 量化与混合精度训练": §20.2.2 GradScaler, §20.5.13 Master
+ *           Weights, §20.5.33 GradScaler 的 _growth_tracker 状态机细节.
+ *   [MP]    "从 AMP 到 Mixed Precision：训练和推理为什么不使用同一种精度":
+ *           "Gradient 和 Loss Scaling", "为什么需要 FP32 Master Weights",
+ *           "PyTorch AMP 与 FP32 Master Weights" (mode B: bf16 params + fp32 master).
+ *   [FP8]   "FP8训练：量化、自动微分、Torchao": §2 量化数学, §3 格式选择,
+ *           §4 _scaled_mm 布局要求.
+ *   [NOTES] "AMP：Automatic Mixed Precision 技术笔记": §4 GradScaler.
+ *   [MP06]  "06 · 混合精度": §三 (12 bytes/param of fp32 master + m + v),
+ *           §四 Loss Scaling.
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer named *_dev, and every tensor a list refers to, is device
+ *     memory owned by the caller.  Tensors are contiguous; 16-bit and 8-bit
+ *     floating-point data are raw bit patterns.
+ *   - Every call is asynchronous: it validates its arguments on the host,
+ *     enqueues kernels on `stream` (NULL = the legacy default stream) and
+ *     returns.  No per-step call synchronises the host with the device or
+ *     allocates device memory; only the set-up calls on tensor lists do.
+ *   - A negative status means nothing was enqueued (argument errors), or
+ *     that a launch failed (AMP_ECUDA).  amp_last_error() then returns a
+ *     message for the calling thread.  Faults inside kernels surface at the
+ *     caller's next synchronisation, as for any CUDA work.
+ *   - Calls that touch the same buffers must be ordered on one stream (or
+ *     by events); the library takes no locks.
+ *   - Pointers need no particular alignment: tensors whose addresses allow
+ *     16-byte vector access take the vector path, others a scalar path that
+ *     gives the same bits.
+ */
+#ifndef AMPFP8_H
+#define AMPFP8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; declared here so the header needs
+ * no CUDA include. */
+typedef struct CUstream_st *amp_stream_t;
+
+typedef enum {
+    AMP_OK = 0,
+    AMP_EINVAL = -1,  /* null pointer, negative size, mismatched list shapes */
+    AMP_EDTYPE = -2,  /* element type not accepted by this entry point */
+    AMP_ECUDA = -4,   /* a CUDA runtime call or kernel launch failed */
+    AMP_ENOMEM = -5   /* device allocation in amp_tensor_list_create failed */
+} amp_status;
+
+typedef enum {
+    AMP_DT_F32 = 1,
+    AMP_DT_F16 = 2,     /* IEEE binary16 */
+    AMP_DT_BF16 = 3,    /* bfloat16 */
+    AMP_DT_E4M3FN = 4,  /* OCP FP8 E4M3, finite + NaN (max 448) */
+    AMP_DT_E5M2 = 5     /* OCP FP8 E5M2, IEEE-like (max 57344) */
+} amp_dtype;
+
+/* ------------------------------------------------------------------------ */
+/* Tensor lists                                                              */
+/* ------------------------------------------------------------------------ */
+
+/* Opaque handle describing a ragged list of n contiguous device tensors of
+ * one dtype.  It owns only one device block with its copies of the pointer
+ * and size arrays, the chunk table the list kernels walk (and, for 2-D
+ * lists, the tile table of the FP8 kernels); it never owns tensor data. */
+typedef struct amp_tensor_list_s *amp_tensor_list;
+
+/* Create a list handle.
+ *   n        number of tensors, >= 0
+ *   dev_ptrs host array[n] of device pointers (a pointer may be NULL only
+ *            when its tensor is empty)
+ *   rows     host array[n]: element counts of 1-D tensors, or row counts
+ *            when `cols` is given
+ *   cols     host array[n] of column counts (2-D, row-major), or NULL
+ *   dtype    element type of every tensor
+ *   stream   the device block is filled with cudaMemcpyAsync on it
+ * Allocates the device block with cudaMalloc (the only allocating call of
+ * the library) and waits for the upload on `stream` (a one-time set-up
+ * call, unlike the per-step entry points below).  Returns AMP_EINVAL for n < 0, a null array, a negative
+ * size or a NULL pointer of a non-empty tensor; AMP_ENOMEM if allocation
+ * fails.  *out is set only on success. */
+amp_status amp_tensor_list_create(int n, void *const *dev_ptrs, const int64_t *rows,
+                                  const int64_t *cols, amp_dtype dtype,
+                                  amp_stream_t stream, amp_tensor_list *out);
+
+/* Per-tensor amax slots of a list used as the bf16 output of
+ * amp_adamw_master_step: slots[i] >= 0 folds max|bf16| of tensor i into
+ * amax_dev[slots[i]]; -1 (the default) does not.  Host array[n], copied to
+ * the handle's device block on `stream` (waits for the copy: set-up call). */
+amp_status amp_tensor_list_set_amax_slots(amp_tensor_list list, const int32_t *slots,
+                                          amp_stream_t stream);
+
+/* Release the handle and its device block (cudaFree; synchronises the
+ * device like any cudaFree).  NULL is accepted. */
+amp_status amp_tensor_list_destroy(amp_tensor_list list);
+
+/* ------------------------------------------------------------------------ */
+/* A1: unscale + non-finite check.  [CH20] §20.2.2, [MP] "Gradient 和 Loss    */
+/* Scaling", [NOTES] §4 steps 3-4: before the optimizer the scaled gradients  */
+/* are divided by S and inspected for inf/NaN.                                */
+/* ------------------------------------------------------------------------ */
+
+/* found_inf_dev |= OR over all elements of !isfinite(float(g) * (1/S)),
+ * where 1/S is the correctly rounded fp32 reciprocal of *scale_dev (S = 1
+ * when scale_dev is NULL).  The flag (int32, 0/1) is never cleared here, so
+ * several lists can be checked into one flag; amp_update_scale clears it.
+ *   grads    list of AMP_DT_F16, AMP_DT_BF16 or AMP_DT_F32 tensors
+ *   inplace  0: read-only check (2 bytes/elt for 16-bit grads);
+ *            1: also store g * (1/S) back, rounded to nearest-even in the
+ *               gradient dtype (NaN as the canonical quiet NaN).
+ * Errors: AMP_EINVAL (null list / flag), AMP_EDTYPE (fp8 list). */
+amp_status amp_unscale_check(amp_tensor_list grads, const float *scale_dev,
+                             int32_t *found_inf_dev, int inplace, amp_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* A2-A6: skip decision + FP32-master AdamW + BF16 emission + amax fold.     */
+/* [CH20] §20.5.13, [MP] "为什么需要 FP32 Master Weights" / "PyTorch AMP 与   */
+/* FP32 Master Weights" mode B, [MP06] §三 12 bytes/param.                    */
+/* ------------------------------------------------------------------------ */
+
+/* AdamW hyper-parameters, as the user states them (fp64). */
+typedef struct {
+    double lr, beta1, beta2, eps, weight_decay;
+} amp_adamw_hyper;
+
+/* If found_inf_dev is non-NULL and *found_inf_dev != 0 the step is skipped:
+ * nothing below is written and *step_dev is unchanged.  Otherwise, with
+ * t = *step_dev + 1 and per-step scalars computed once in fp64 and rounded
+ * to fp32 (step_size = lr / (1 - beta1^t), c2 = sqrt(1 - beta2^t)), every
+ * element does in fp32, each operation rounded to nearest-even and none
+ * fused:
+ *     g = float(grad) * (1/S)
+ *     p = p * (1 - lr*wd)
+ *     m = beta1*m + (1-beta1)*g
+ *     v = beta2*v + (1-beta2)*(g*g)
+ *     p = p - step_size * (m / (sqrt(v)/c2 + eps))
+ * then bf16_out = RNE(p), and *step_dev = t.  The constants (1 - lr*wd),
+ * (1-beta1), (1-beta2) are formed in fp64 and rounded once to fp32.
+ *   master, exp_avg, exp_avg_sq  AMP_DT_F32 lists, updated in place
+ *   grads      AMP_DT_F16 / AMP_DT_BF16 / AMP_DT_F32 list (scaled by S)
+ *   bf16_out   AMP_DT_BF16 list or NULL; tensors with an amax slot also do
+ *              amax_dev[slot] = max(amax_dev[slot], |bf16|) (fp32 bits,
+ *              NaN-propagating), which the caller must have zeroed
+ *              (amp_update_scale does at the end of each step)
+ *   scale_dev  fp32 S, or NULL for S = 1
+ *   step_dev   int32 count of completed (non-skipped) steps
+ * All lists must have the same tensor count and element counts.
+ * Errors: AMP_EINVAL (null / mismatched lists, null step or hyper, slots
+ * without amax_dev), AMP_EDTYPE (wrong list dtypes). */
+amp_status amp_adamw_master_step(amp_tensor_list master, amp_tensor_list exp_avg,
+                                 amp_tensor_list exp_avg_sq, amp_tensor_list grads,
+                                 amp_tensor_list bf16_out, const float *scale_dev,
+                                 const int32_t *found_inf_dev, int32_t *step_dev,
+                                 const amp_adamw_hyper *hyper, float *amax_dev,
+                                 amp_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* A6-A9: tensorwise dynamic FP8 quantization.  [FP8] §2 (quant math), §3     */
+/* (e4m3fn for weights/activations, e5m2 for gradients), §4 (column-major     */
+/* copies for the backward GEMMs).                                            */
+/* ------------------------------------------------------------------------ */
+
+/* x is [rows, cols] row-major (AMP_DT_BF16, AMP_DT_F16 or AMP_DT_F32).
+ *   amax      = max |x| in fp32 (NaN-propagating); written to *amax_dev
+ *               unless amax_given != 0, in which case *amax_dev is read
+ *   scale_d   = fp8_max / max(double(amax), eps)                  (fp64)
+ *   out[i,j]  = fp8(clamp(float(x[i,j]) * float(scale_d), -fp8_max, fp8_max))
+ *               round-to-nearest-even; NaN -> 0x7F (e4m3fn) / 0x7E (e5m2)
+ *   out_t[j,i] = out[i,j]   ([cols, rows] row-major = column-major out), if
+ *               out_t is non-NULL
+ *   *inv_scale_dev = float(1 / scale_d)
+ * fp8_dtype is AMP_DT_E4M3FN (max 448) or AMP_DT_E5M2 (max 57344); eps > 0
+ * (1e-12 is the usual value).  If skip_if_dev is non-NULL and
+ * *skip_if_dev != 0 nothing is written.  Empty tensors (rows*cols == 0)
+ * write amax 0 and the matching inv_scale.
+ * Errors: AMP_EINVAL (null out / inv_scale / amax, negative size,
+ * eps <= 0), AMP_EDTYPE. */
+amp_status fp8_quant_tensorwise(const void *x, amp_dtype x_dtype, int64_t rows, int64_t cols,
+                                amp_dtype fp8_dtype, double eps, void *out, void *out_t,
+                                float *inv_scale_dev, float *amax_dev, int amax_given,
+                                const int32_t *skip_if_dev, amp_stream_t stream);
+
+/* The same over a list of 2-D tensors in one launch, with amax given per
+ * tensor: tensor i uses amax_dev[i] (e.g. folded by amp_adamw_master_step
+ * with slot i) and writes inv_scale_dev[i].
+ *   x      2-D list, AMP_DT_BF16 / AMP_DT_F16 / AMP_DT_F32
+ *   out    2-D list of fp8_dtype with the shapes of x
+ *   out_t  2-D list of fp8_dtype with the transposed shapes, or NULL
+ * Errors: AMP_EINVAL (null / mismatched lists, 1-D list, eps <= 0),
+ * AMP_EDTYPE. */
+amp_status fp8_quant_tensorwise_list(amp_tensor_list x, amp_tensor_list out,
+                                     amp_tensor_list out_t, amp_dtype fp8_dtype, double eps,
+                                     const float *amax_dev, float *inv_scale_dev,
+                                     const int32_t *skip_if_dev, amp_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* A3: dynamic loss-scale state machine.  [CH20] §20.5.33, [MP06] §四.        */
+/* ------------------------------------------------------------------------ */
+
+/* One thread on the device:
+ *   if *found_inf_dev: *scale_dev *= backoff_factor; *growth_tracker_dev = 0
+ *   else: *growth_tracker_dev += 1; if it reaches growth_interval:
+ *         *scale_dev *= growth_factor (kept unchanged if the product is not
+ *         finite); *growth_tracker_dev = 0
+ * then clears *found_inf_dev and amax_dev[0 .. n_amax) for the next step.
+ * Errors: AMP_EINVAL (null state pointers, growth_interval < 1, n_amax < 0,
+ * n_amax > 0 with amax_dev NULL). */
+amp_status amp_update_scale(float *scale_dev, int32_t *growth_tracker_dev,
+                            int32_t *found_inf_dev, float growth_factor, float backoff_factor,
+                            int32_t growth_interval, float *amax_dev, int n_amax,
+                            amp_stream_t stream);
+
+/* Message describing the last non-OK status returned on this thread. */
+const char *amp_last_error(void);
+
+/* ABI version of this header (incremented on incompatible changes). */
+int amp_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* AMPFP8_H */

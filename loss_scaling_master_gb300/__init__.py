@@ -1,0 +1,17 @@
+"""GB300-native mixed-precision optimizer step: loss-scale unscale/check,
+dynamic scale state machine, FP32-master AdamW with bf16 emission, and
+tensorwise dynamic FP8 quantization with transposed copies.
+
+The compute lives in libampfp8.so (hand-written CUDA for sm_103a, C ABI in
+include/ampfp8.h); this package is its thin ctypes binding.
+"""
+from ._lib import (AmpError, TensorList, amp_abi_version, amp_adamw_master_step,
+                   amp_last_error, amp_tensor_list_create, amp_tensor_list_destroy,
+                   amp_tensor_list_set_amax_slots, amp_unscale_check, amp_update_scale,
+                   fp8_quant_tensorwise, fp8_quant_tensorwise_list, load)
+from .step import AmpOptimizerStep
+
+__all__ = ["AmpError", "TensorList", "AmpOptimizerStep", "load", "amp_abi_version",
+           "amp_last_error", "amp_tensor_list_create", "amp_tensor_list_destroy",
+           "amp_tensor_list_set_amax_slots", "amp_unscale_check", "amp_adamw_master_step",
+           "fp8_quant_tensorwise", "fp8_quant_tensorwise_list", "amp_update_scale"]

@@ -1,0 +1,211 @@
+"""ctypes binding of libampfp8.so (declared in include/ampfp8.h).
+
+Argument marshalling only: every function here passes device pointers,
+sizes and a stream handle straight to the C entry point of the same name and
+raises ``AmpError`` on a non-OK status.  PyTorch supplies device memory and
+streams; no computation of the step happens in Python.  There is no fallback:
+if the shared library is missing, loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libampfp8.so")
+
+AMP_OK = 0
+STATUS = {0: "AMP_OK", -1: "AMP_EINVAL", -2: "AMP_EDTYPE", -4: "AMP_ECUDA", -5: "AMP_ENOMEM"}
+DT = {"f32": 1, "f16": 2, "bf16": 3, "e4m3fn": 4, "e5m2": 5}
+_TORCH_DT = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16",
+             torch.float8_e4m3fn: "e4m3fn", torch.float8_e5m2: "e5m2"}
+
+# every symbol include/ampfp8.h declares
+EXPORTS = ("amp_tensor_list_create", "amp_tensor_list_set_amax_slots", "amp_tensor_list_destroy",
+           "amp_unscale_check", "amp_adamw_master_step", "fp8_quant_tensorwise",
+           "fp8_quant_tensorwise_list", "amp_update_scale", "amp_last_error", "amp_abi_version")
+
+
+class AmpError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} -> {STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+class amp_adamw_hyper(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
+                ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double)]
+
+
+_lock = threading.Lock()
+_lib = None
+P = ctypes.c_void_p
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libampfp8.so and declare its prototypes (raises if not built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(path)
+        i32, i64, dbl, flt = ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_float
+        L.amp_tensor_list_create.argtypes = [i32, P, P, P, i32, P, ctypes.POINTER(P)]
+        L.amp_tensor_list_set_amax_slots.argtypes = [P, P, P]
+        L.amp_tensor_list_destroy.argtypes = [P]
+        L.amp_unscale_check.argtypes = [P, P, P, i32, P]
+        L.amp_adamw_master_step.argtypes = [P, P, P, P, P, P, P, P,
+                                            ctypes.POINTER(amp_adamw_hyper), P, P]
+        L.fp8_quant_tensorwise.argtypes = [P, i32, i64, i64, i32, dbl, P, P, P, P, i32, P, P]
+        L.fp8_quant_tensorwise_list.argtypes = [P, P, P, i32, dbl, P, P, P, P]
+        L.amp_update_scale.argtypes = [P, P, P, flt, flt, ctypes.c_int32, P, i32, P]
+        for name in EXPORTS[:-2]:
+            getattr(L, name).restype = ctypes.c_int
+        L.amp_last_error.restype = ctypes.c_char_p
+        L.amp_last_error.argtypes = []
+        L.amp_abi_version.restype = ctypes.c_int
+        L.amp_abi_version.argtypes = []
+        _lib = L
+        return L
+
+
+def _check(fn: str, st: int):
+    if st != AMP_OK:
+        raise AmpError(fn, st, load().amp_last_error().decode(errors="replace"))
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return P(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dptr(t):
+    return None if t is None else P(t.data_ptr())
+
+
+def dtype_name(t: torch.Tensor) -> str:
+    return _TORCH_DT[t.dtype]
+
+
+class TensorList:
+    """Owner of an ``amp_tensor_list`` handle; keeps its tensors alive."""
+
+    def __init__(self, handle, tensors, dtype: str, two_d: bool):
+        self.handle, self.tensors, self.dtype, self.two_d = handle, tensors, dtype, two_d
+
+    def __len__(self):
+        return len(self.tensors)
+
+    def close(self):
+        if self.handle:
+            h, self.handle = self.handle, None
+            _check("amp_tensor_list_destroy", load().amp_tensor_list_destroy(h))
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def amp_tensor_list_create(tensors, two_d: bool = False, dtype: str | None = None,
+                           stream=None) -> TensorList:
+    """Describe contiguous device tensors as one list (2-D lists keep their
+    [rows, cols] shapes for the FP8 kernels)."""
+    tensors = list(tensors)
+    if dtype is None:
+        if not tensors:
+            raise ValueError("empty list needs an explicit dtype")
+        dtype = dtype_name(tensors[0])
+    n = len(tensors)
+    for t in tensors:
+        if not t.is_contiguous() or dtype_name(t) != dtype:
+            raise ValueError("every tensor must be contiguous and of the list dtype")
+        if two_d and t.dim() != 2:
+            raise ValueError("2-D list needs 2-D tensors")
+    ptrs = (P * max(n, 1))(*[t.data_ptr() for t in tensors])
+    if two_d:
+        rows = (ctypes.c_int64 * max(n, 1))(*[t.shape[0] for t in tensors])
+        cols = (ctypes.c_int64 * max(n, 1))(*[t.shape[1] for t in tensors])
+    else:
+        rows = (ctypes.c_int64 * max(n, 1))(*[t.numel() for t in tensors])
+        cols = None
+    h = P()
+    _check("amp_tensor_list_create",
+           load().amp_tensor_list_create(n, ptrs, rows, cols, DT[dtype], _stream(stream),
+                                         ctypes.byref(h)))
+    return TensorList(h, tensors, dtype, two_d)
+
+
+def amp_tensor_list_set_amax_slots(lst: TensorList, slots, stream=None):
+    arr = (ctypes.c_int32 * max(len(lst), 1))(*[int(s) for s in slots])
+    _check("amp_tensor_list_set_amax_slots",
+           load().amp_tensor_list_set_amax_slots(lst.handle, arr, _stream(stream)))
+
+
+def amp_tensor_list_destroy(lst: TensorList):
+    lst.close()
+
+
+def amp_unscale_check(grads: TensorList, scale, found_inf, inplace: bool = False, stream=None):
+    _check("amp_unscale_check",
+           load().amp_unscale_check(grads.handle, _dptr(scale), _dptr(found_inf), int(inplace),
+                                    _stream(stream)))
+
+
+def amp_adamw_master_step(master: TensorList, exp_avg: TensorList, exp_avg_sq: TensorList,
+                          grads: TensorList, bf16_out: TensorList | None, scale, found_inf, step,
+                          lr: float, beta1: float, beta2: float, eps: float,
+                          weight_decay: float, amax=None, stream=None):
+    h = amp_adamw_hyper(lr, beta1, beta2, eps, weight_decay)
+    _check("amp_adamw_master_step",
+           load().amp_adamw_master_step(master.handle, exp_avg.handle, exp_avg_sq.handle,
+                                        grads.handle, bf16_out.handle if bf16_out else None,
+                                        _dptr(scale), _dptr(found_inf), _dptr(step),
+                                        ctypes.byref(h), _dptr(amax), _stream(stream)))
+
+
+def fp8_quant_tensorwise(x: torch.Tensor, fp8_dtype: str, out: torch.Tensor, out_t, inv_scale,
+                         amax, amax_given: bool = False, eps: float = 1e-12, skip_if=None,
+                         stream=None, rows: int | None = None, cols: int | None = None):
+    """x is [rows, cols] row-major (a 1-D tensor is one row unless rows/cols say otherwise)."""
+    if rows is None:
+        rows, cols = (x.shape[0], x.shape[1]) if x.dim() == 2 else (1, x.numel())
+    _check("fp8_quant_tensorwise",
+           load().fp8_quant_tensorwise(_dptr(x), DT[dtype_name(x)], rows, cols, DT[fp8_dtype],
+                                       eps, _dptr(out), _dptr(out_t), _dptr(inv_scale),
+                                       _dptr(amax), int(amax_given), _dptr(skip_if),
+                                       _stream(stream)))
+
+
+def fp8_quant_tensorwise_list(x: TensorList, out: TensorList, out_t: TensorList | None,
+                              fp8_dtype: str, amax, inv_scale, eps: float = 1e-12, skip_if=None,
+                              stream=None):
+    _check("fp8_quant_tensorwise_list",
+           load().fp8_quant_tensorwise_list(x.handle, out.handle, out_t.handle if out_t else None,
+                                            DT[fp8_dtype], eps, _dptr(amax), _dptr(inv_scale),
+                                            _dptr(skip_if), _stream(stream)))
+
+
+def amp_update_scale(scale, growth_tracker, found_inf, growth_factor: float,
+                     backoff_factor: float, growth_interval: int, amax=None, n_amax: int = 0,
+                     stream=None):
+    _check("amp_update_scale",
+           load().amp_update_scale(_dptr(scale), _dptr(growth_tracker), _dptr(found_inf),
+                                   growth_factor, backoff_factor, int(growth_interval),
+                                   _dptr(amax), int(n_amax), _stream(stream)))
+
+
+def amp_last_error() -> str:
+    return load().amp_last_error().decode(errors="replace")
+
+
+def amp_abi_version() -> int:
+    return load().amp_abi_version()

@@ -1,0 +1,272 @@
+// adamw_master.cu - A2..A6: skip-on-inf, unscale, FP32-master AdamW, BF16
+// working-copy emission and the per-tensor amax fold for FP8 weights.
+//
+//   "第20章 量化与混合精度训练" §20.5.13 Master Weights and "从 AMP 到 Mixed
+//   Precision" sections "为什么需要 FP32 Master Weights" / "PyTorch AMP 与 FP32
+//   Master Weights" (mode B): the optimizer updates an fp32 master and casts
+//   it to the bf16 copy the forward pass uses; "06 · 混合精度" §三: master,
+//   m and v are fp32, 12 bytes per parameter.
+//
+// Two launches per step:
+//   prologue  one thread: reads found_inf and the step counter, forms the
+//             bias-corrected scalars in fp64 once, advances the counter when
+//             the step is not skipped, and leaves {skip, step_size, c2} in a
+//             16-byte block of the master list's device block;
+//   main      one CTA per chunk of 16384 elements; a skipped step returns at
+//             once, otherwise every thread streams groups of 8 elements with
+//             16-byte loads/stores: 14 bytes read + 14 bytes written per
+//             parameter (fp16/bf16 grads, bf16 emission).
+#include "internal.h"
+
+namespace amp {
+namespace {
+
+struct AdamwParams {
+    ListView p, m, v, g, b;
+    const float *scale;
+    const AdamwStepScalars *scal;
+    float *amax;
+    float decay, b1, omb1, b2, omb2, eps;
+    int use_slots;
+};
+
+struct Scal {
+    float r, decay, b1, omb1, b2, omb2, eps, step_size, c2;
+};
+
+// One element of the update; each operation rounded on its own (no fma).
+__device__ __forceinline__ void adamw_elem(float &p, float &m, float &v, float graw,
+                                           const Scal &s) {
+    const float g = __fmul_rn(graw, s.r);
+    p = __fmul_rn(p, s.decay);
+    m = __fadd_rn(__fmul_rn(s.b1, m), __fmul_rn(s.omb1, g));
+    v = __fadd_rn(__fmul_rn(s.b2, v), __fmul_rn(s.omb2, __fmul_rn(g, g)));
+    const float denom = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), s.c2), s.eps);
+    p = __fsub_rn(p, __fmul_rn(s.step_size, __fdiv_rn(m, denom)));
+}
+
+template <int GT>
+__device__ __forceinline__ float grad_at(const void *gp, int64_t k) {
+    if (GT == kF32) return static_cast<const float *>(gp)[k];
+    return lowp_to_f32<GT>(static_cast<const uint16_t *>(gp)[k]);
+}
+
+// Registers of one group of 8 consecutive elements.
+template <int GT>
+struct Group {
+    uint4 p[2], m[2], v[2];
+    uint4 g[GT == kF32 ? 2 : 1];
+};
+
+template <int GT>
+__device__ __forceinline__ void load_group(Group<GT> &r, const float *pp, const float *mp,
+                                           const float *vp, const void *gp, int64_t e) {
+    r.p[0] = ld_cs(pp + e);
+    r.p[1] = ld_cs(pp + e + 4);
+    r.m[0] = ld_cs(mp + e);
+    r.m[1] = ld_cs(mp + e + 4);
+    r.v[0] = ld_cs(vp + e);
+    r.v[1] = ld_cs(vp + e + 4);
+    if constexpr (GT == kF32) {
+        r.g[0] = ld_cs(static_cast<const float *>(gp) + e);
+        r.g[1] = ld_cs(static_cast<const float *>(gp) + e + 4);
+    } else {
+        r.g[0] = ld_cs(static_cast<const uint16_t *>(gp) + e);
+    }
+}
+
+__device__ __forceinline__ float u4_get(const uint4 &w, int j) {
+    return __uint_as_float(j == 0 ? w.x : j == 1 ? w.y : j == 2 ? w.z : w.w);
+}
+__device__ __forceinline__ void u4_set(uint4 &w, int j, float f) {
+    const uint32_t b = __float_as_uint(f);
+    if (j == 0) w.x = b; else if (j == 1) w.y = b; else if (j == 2) w.z = b; else w.w = b;
+}
+
+template <int GT, bool BF16>
+__device__ __forceinline__ void compute_store_group(Group<GT> &r, float *pp, float *mp, float *vp,
+                                                    uint16_t *bp, int64_t e, const Scal &s,
+                                                    uint32_t &amax2) {
+    float p[8], m[8], v[8], g[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        p[j] = u4_get(r.p[j >> 2], j & 3);
+        m[j] = u4_get(r.m[j >> 2], j & 3);
+        v[j] = u4_get(r.v[j >> 2], j & 3);
+    }
+    if constexpr (GT == kF32) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) g[j] = u4_get(r.g[j >> 2], j & 3);
+    } else {
+        const uint32_t w[4] = {r.g[0].x, r.g[0].y, r.g[0].z, r.g[0].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            g[2 * j] = lowp_to_f32<GT>(w[j] & 0xFFFFu);
+            g[2 * j + 1] = lowp_to_f32<GT>(w[j] >> 16);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) adamw_elem(p[j], m[j], v[j], g[j], s);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        u4_set(r.p[j >> 2], j & 3, p[j]);
+        u4_set(r.m[j >> 2], j & 3, m[j]);
+        u4_set(r.v[j >> 2], j & 3, v[j]);
+    }
+    st_cs(pp + e, r.p[0]);
+    st_cs(pp + e + 4, r.p[1]);
+    st_cs(mp + e, r.m[0]);
+    st_cs(mp + e + 4, r.m[1]);
+    st_cs(vp + e, r.v[0]);
+    st_cs(vp + e + 4, r.v[1]);
+    if (BF16) {
+        uint4 o;
+        o.x = f32x2_to_bf16x2(p[0], p[1]);
+        o.y = f32x2_to_bf16x2(p[2], p[3]);
+        o.z = f32x2_to_bf16x2(p[4], p[5]);
+        o.w = f32x2_to_bf16x2(p[6], p[7]);
+        st_g(bp + e, o);
+        amax2 = __vmaxu2(amax2, __vmaxu2(__vmaxu2(o.x & 0x7FFF7FFFu, o.y & 0x7FFF7FFFu),
+                                         __vmaxu2(o.z & 0x7FFF7FFFu, o.w & 0x7FFF7FFFu)));
+    }
+}
+
+template <int GT, bool BF16>
+__device__ __forceinline__ void scalar_elem(float *pp, float *mp, float *vp, const void *gp,
+                                            uint16_t *bp, int64_t k, const Scal &s,
+                                            uint32_t &amax1) {
+    float p = pp[k], m = mp[k], v = vp[k];
+    adamw_elem(p, m, v, grad_at<GT>(gp, k), s);
+    pp[k] = p;
+    mp[k] = m;
+    vp[k] = v;
+    if (BF16) {
+        const uint16_t b = f32_to_bf16(p);
+        bp[k] = b;
+        amax1 = max(amax1, uint32_t(b & 0x7FFFu));
+    }
+}
+
+template <int GT, bool BF16>
+__global__ void __launch_bounds__(kThreads) adamw_main_kernel(AdamwParams P) {
+    const AdamwStepScalars sc = *P.scal;
+    if (sc.skip) return;  // A2: nothing is written on a skipped step
+    const uint2 ch = P.p.chunks[blockIdx.x];
+    const int t = int(ch.x);
+    const int64_t start = int64_t(ch.y) * kChunk;
+    const int64_t n = min(int64_t(kChunk), P.p.numel[t] - start);
+    constexpr int gsz = GT == kF32 ? 4 : 2;
+    float *pp = static_cast<float *>(P.p.ptrs[t]) + start;
+    float *mp = static_cast<float *>(P.m.ptrs[t]) + start;
+    float *vp = static_cast<float *>(P.v.ptrs[t]) + start;
+    const void *gp = static_cast<const char *>(P.g.ptrs[t]) + start * gsz;
+    uint16_t *bp = BF16 ? static_cast<uint16_t *>(P.b.ptrs[t]) + start : nullptr;
+
+    Scal s;
+    s.r = P.scale ? __fdiv_rn(1.0f, *P.scale) : 1.0f;
+    s.decay = P.decay;
+    s.b1 = P.b1;
+    s.omb1 = P.omb1;
+    s.b2 = P.b2;
+    s.omb2 = P.omb2;
+    s.eps = P.eps;
+    s.step_size = sc.step_size;
+    s.c2 = sc.bc2_sqrt;
+
+    uint32_t amax2 = 0;  // packed bf16x2 maxima of |bf16|
+    uint32_t amax1 = 0;
+    const bool vec = aligned16(pp) && aligned16(mp) && aligned16(vp) && aligned16(gp) &&
+                     (!BF16 || aligned16(bp));
+    if (vec) {
+        const int64_t ng = n >> 3;
+        int64_t i = threadIdx.x;
+        for (; i + kThreads < ng; i += 2 * kThreads) {
+            Group<GT> a, b;
+            load_group<GT>(a, pp, mp, vp, gp, i * 8);
+            load_group<GT>(b, pp, mp, vp, gp, (i + kThreads) * 8);
+            compute_store_group<GT, BF16>(a, pp, mp, vp, bp, i * 8, s, amax2);
+            compute_store_group<GT, BF16>(b, pp, mp, vp, bp, (i + kThreads) * 8, s, amax2);
+        }
+        if (i < ng) {
+            Group<GT> a;
+            load_group<GT>(a, pp, mp, vp, gp, i * 8);
+            compute_store_group<GT, BF16>(a, pp, mp, vp, bp, i * 8, s, amax2);
+        }
+        const int64_t k = ng * 8 + threadIdx.x;
+        if (k < n) scalar_elem<GT, BF16>(pp, mp, vp, gp, bp, k, s, amax1);
+    } else {
+        for (int64_t k = threadIdx.x; k < n; k += kThreads)
+            scalar_elem<GT, BF16>(pp, mp, vp, gp, bp, k, s, amax1);
+    }
+    if (BF16 && P.use_slots) {
+        const int slot = P.b.slots[t];
+        if (slot >= 0) {
+            // |bf16| bit patterns order like magnitudes (NaN above inf), and
+            // bf16 bits << 16 are the fp32 bits of the same value.
+            uint32_t a = max(max(amax2 & 0xFFFFu, amax2 >> 16), amax1);
+            a = warp_max_u32(a);
+            if ((threadIdx.x & 31) == 0 && a != 0)
+                atomicMax(reinterpret_cast<unsigned int *>(P.amax) + slot, a << 16);
+        }
+    }
+}
+
+__global__ void adamw_prologue_kernel(const int32_t *found_inf, int32_t *step, double lr,
+                                      double beta1, double beta2, AdamwStepScalars *out) {
+    AdamwStepScalars s;
+    s.skip = found_inf ? (*found_inf != 0) : 0;
+    s.step_size = 0.0f;
+    s.bc2_sqrt = 1.0f;
+    s.pad = 0.0f;
+    if (!s.skip) {
+        const int32_t t = *step + 1;
+        const double bc1 = 1.0 - pow(beta1, double(t));
+        const double bc2 = 1.0 - pow(beta2, double(t));
+        s.step_size = float(lr / bc1);
+        s.bc2_sqrt = float(sqrt(bc2));
+        *step = t;
+    }
+    *out = s;
+}
+
+}  // namespace
+
+cudaError_t launch_adamw(const ListView &p, const ListView &m, const ListView &v,
+                         const ListView &g, const ListView *b, int64_t n_chunks, int gelem,
+                         const float *scale, const int32_t *found_inf, int32_t *step,
+                         const AdamwConsts &c, AdamwStepScalars *scal, float *amax,
+                         bool use_slots, cudaStream_t s) {
+    adamw_prologue_kernel<<<1, 1, 0, s>>>(found_inf, step, c.lr, c.beta1, c.beta2, scal);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || n_chunks == 0) return e;
+    AdamwParams P;
+    P.p = p;
+    P.m = m;
+    P.v = v;
+    P.g = g;
+    P.b = b ? *b : ListView{};
+    P.scale = scale;
+    P.scal = scal;
+    P.amax = amax;
+    P.decay = c.decay;
+    P.b1 = c.b1;
+    P.omb1 = c.omb1;
+    P.b2 = c.b2;
+    P.omb2 = c.omb2;
+    P.eps = c.eps;
+    P.use_slots = use_slots ? 1 : 0;
+    const dim3 grid((unsigned)n_chunks), block(kThreads);
+    const bool bf = b != nullptr;
+#define AMP_ADAMW_LAUNCH(GT)                                                         \
+    do {                                                                             \
+        if (bf) adamw_main_kernel<GT, true><<<grid, block, 0, s>>>(P);               \
+        else adamw_main_kernel<GT, false><<<grid, block, 0, s>>>(P);                 \
+    } while (0)
+    if (gelem == kF32) AMP_ADAMW_LAUNCH(kF32);
+    else if (gelem == kF16) AMP_ADAMW_LAUNCH(kF16);
+    else AMP_ADAMW_LAUNCH(kBF16);
+#undef AMP_ADAMW_LAUNCH
+    return cudaGetLastError();
+}
+
+}  // namespace amp

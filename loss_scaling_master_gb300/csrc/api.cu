@@ -1,0 +1,322 @@
+// api.cu - the extern "C" boundary of libampfp8.so: argument validation,
+// tensor-list handles and kernel launches.  Every entry point is declared and
+// documented in include/ampfp8.h.
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+amp_status fail(amp_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+amp_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(AMP_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int elem_code(amp_dtype d) {
+    switch (d) {
+    case AMP_DT_F32: return amp::kF32;
+    case AMP_DT_F16: return amp::kF16;
+    case AMP_DT_BF16: return amp::kBF16;
+    default: return -1;
+    }
+}
+
+int fp8_code(amp_dtype d) {
+    return d == AMP_DT_E4M3FN ? amp::kE4M3 : d == AMP_DT_E5M2 ? amp::kE5M2 : -1;
+}
+
+size_t elem_size(amp_dtype d) {
+    switch (d) {
+    case AMP_DT_F32: return 4;
+    case AMP_DT_F16:
+    case AMP_DT_BF16: return 2;
+    case AMP_DT_E4M3FN:
+    case AMP_DT_E5M2: return 1;
+    }
+    return 0;
+}
+
+size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool same_shapes(const amp_tensor_list_s *a, const amp_tensor_list_s *b) {
+    return a->n == b->n && a->numel == b->numel;
+}
+
+}  // namespace
+
+namespace amp {
+int sm_count(int device) {
+    static std::mutex mu;
+    static std::vector<int> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    if (device >= int(cache.size())) cache.resize(device + 1, 0);
+    if (cache[device] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || v <= 0)
+            v = 148;
+        cache[device] = v;
+    }
+    return cache[device];
+}
+}  // namespace amp
+
+extern "C" {
+
+const char *amp_last_error(void) { return g_err; }
+
+int amp_abi_version(void) { return 1; }
+
+amp_status amp_tensor_list_create(int n, void *const *dev_ptrs, const int64_t *rows,
+                                  const int64_t *cols, amp_dtype dtype, amp_stream_t stream,
+                                  amp_tensor_list *out) {
+    if (!out) return fail(AMP_EINVAL, "amp_tensor_list_create: out is NULL");
+    if (n < 0) return fail(AMP_EINVAL, "amp_tensor_list_create: n < 0");
+    if (n > 0 && (!dev_ptrs || !rows))
+        return fail(AMP_EINVAL, "amp_tensor_list_create: dev_ptrs / rows is NULL");
+    if (elem_size(dtype) == 0) return fail(AMP_EDTYPE, "amp_tensor_list_create: unknown dtype");
+    auto *L = new amp_tensor_list_s();
+    L->n = n;
+    L->dtype = dtype;
+    L->two_d = cols != nullptr;
+    L->ptrs.resize(n);
+    L->numel.resize(n);
+    L->rows.resize(n);
+    L->cols.resize(n);
+    std::vector<uint2> chunks, tiles;
+    for (int i = 0; i < n; ++i) {
+        const int64_t r = rows[i], c = cols ? cols[i] : 1;
+        if (r < 0 || c < 0) {
+            delete L;
+            return fail(AMP_EINVAL, "amp_tensor_list_create: negative size at tensor %d", i);
+        }
+        const int64_t ne = r * c;
+        if (ne > 0 && dev_ptrs[i] == nullptr) {
+            delete L;
+            return fail(AMP_EINVAL, "amp_tensor_list_create: NULL pointer of non-empty tensor %d", i);
+        }
+        if ((ne + amp::kChunk - 1) / amp::kChunk > int64_t(UINT32_MAX)) {
+            delete L;
+            return fail(AMP_EINVAL, "amp_tensor_list_create: tensor %d too large", i);
+        }
+        L->ptrs[i] = dev_ptrs[i];
+        L->numel[i] = ne;
+        L->rows[i] = r;
+        L->cols[i] = c;
+        for (int64_t k = 0; k * amp::kChunk < ne; ++k) chunks.push_back(make_uint2(i, uint32_t(k)));
+        if (cols) {
+            const int64_t nt = ((r + amp::kTile - 1) / amp::kTile) * ((c + amp::kTile - 1) / amp::kTile);
+            for (int64_t k = 0; k < nt; ++k) tiles.push_back(make_uint2(i, uint32_t(k)));
+        }
+    }
+    if (chunks.size() > size_t(INT32_MAX) || tiles.size() > size_t(INT32_MAX)) {
+        delete L;
+        return fail(AMP_EINVAL, "amp_tensor_list_create: list too large");
+    }
+    L->n_chunks = int64_t(chunks.size());
+    L->n_tiles = int64_t(tiles.size());
+
+    // one device block: ptrs | numel | rows | cols | slots | chunks | tiles | scratch
+    const size_t nn = size_t(n > 0 ? n : 1);
+    const size_t o_ptrs = 0;
+    const size_t o_numel = align_up(o_ptrs + nn * sizeof(void *));
+    const size_t o_rows = align_up(o_numel + nn * sizeof(int64_t));
+    const size_t o_cols = align_up(o_rows + nn * sizeof(int64_t));
+    const size_t o_slots = align_up(o_cols + nn * sizeof(int64_t));
+    const size_t o_chunks = align_up(o_slots + nn * sizeof(int32_t));
+    const size_t o_tiles = align_up(o_chunks + std::max<size_t>(1, chunks.size()) * sizeof(uint2));
+    const size_t o_scratch = align_up(o_tiles + std::max<size_t>(1, tiles.size()) * sizeof(uint2));
+    const size_t total = align_up(o_scratch + 256);
+    std::vector<char> host(total, 0);
+    std::memcpy(host.data() + o_ptrs, L->ptrs.data(), n * sizeof(void *));
+    std::memcpy(host.data() + o_numel, L->numel.data(), n * sizeof(int64_t));
+    std::memcpy(host.data() + o_rows, L->rows.data(), n * sizeof(int64_t));
+    std::memcpy(host.data() + o_cols, L->cols.data(), n * sizeof(int64_t));
+    std::vector<int32_t> slots(nn, -1);
+    std::memcpy(host.data() + o_slots, slots.data(), nn * sizeof(int32_t));
+    std::memcpy(host.data() + o_chunks, chunks.data(), chunks.size() * sizeof(uint2));
+    std::memcpy(host.data() + o_tiles, tiles.data(), tiles.size() * sizeof(uint2));
+
+    cudaError_t e = cudaGetDevice(&L->device);
+    if (e != cudaSuccess) {
+        delete L;
+        return cuda_fail(e, "amp_tensor_list_create: cudaGetDevice");
+    }
+    e = cudaMalloc(&L->block, total);
+    if (e != cudaSuccess) {
+        delete L;
+        return fail(AMP_ENOMEM, "amp_tensor_list_create: cudaMalloc(%zu): %s", total,
+                    cudaGetErrorString(e));
+    }
+    // The host staging buffer must outlive the asynchronous copy.
+    e = cudaMemcpyAsync(L->block, host.data(), total, cudaMemcpyHostToDevice,
+                        reinterpret_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaFree(L->block);
+        delete L;
+        return cuda_fail(e, "amp_tensor_list_create: upload");
+    }
+    char *b = static_cast<char *>(L->block);
+    L->view.ptrs = reinterpret_cast<void *const *>(b + o_ptrs);
+    L->view.numel = reinterpret_cast<const int64_t *>(b + o_numel);
+    L->view.rows = reinterpret_cast<const int64_t *>(b + o_rows);
+    L->view.cols = reinterpret_cast<const int64_t *>(b + o_cols);
+    L->view.slots = reinterpret_cast<const int32_t *>(b + o_slots);
+    L->view.chunks = reinterpret_cast<const uint2 *>(b + o_chunks);
+    L->view.tiles = reinterpret_cast<const uint2 *>(b + o_tiles);
+    L->view.n = n;
+    L->scratch = b + o_scratch;
+    *out = L;
+    return AMP_OK;
+}
+
+amp_status amp_tensor_list_set_amax_slots(amp_tensor_list list, const int32_t *slots,
+                                          amp_stream_t stream) {
+    if (!list || (list->n > 0 && !slots))
+        return fail(AMP_EINVAL, "amp_tensor_list_set_amax_slots: NULL argument");
+    if (list->n == 0) return AMP_OK;
+    std::vector<int32_t> h(slots, slots + list->n);
+    bool any = false;
+    for (int32_t s : h) any |= s >= 0;
+    cudaError_t e = cudaMemcpyAsync(const_cast<int32_t *>(list->view.slots), h.data(),
+                                    h.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
+                                    reinterpret_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "amp_tensor_list_set_amax_slots");
+    list->has_slots = any;
+    return AMP_OK;
+}
+
+amp_status amp_tensor_list_destroy(amp_tensor_list list) {
+    if (!list) return AMP_OK;
+    cudaError_t e = list->block ? cudaFree(list->block) : cudaSuccess;
+    delete list;
+    return e == cudaSuccess ? AMP_OK : cuda_fail(e, "amp_tensor_list_destroy");
+}
+
+amp_status amp_unscale_check(amp_tensor_list grads, const float *scale_dev, int32_t *found_inf_dev,
+                             int inplace, amp_stream_t stream) {
+    if (!grads || !found_inf_dev) return fail(AMP_EINVAL, "amp_unscale_check: NULL argument");
+    const int ec = elem_code(grads->dtype);
+    if (ec < 0) return fail(AMP_EDTYPE, "amp_unscale_check: gradients must be f32/f16/bf16");
+    cudaError_t e = amp::launch_unscale_check(grads->view, grads->n_chunks, ec, scale_dev,
+                                              found_inf_dev, inplace ? 1 : 0,
+                                              reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AMP_OK : cuda_fail(e, "amp_unscale_check");
+}
+
+amp_status amp_adamw_master_step(amp_tensor_list master, amp_tensor_list exp_avg,
+                                 amp_tensor_list exp_avg_sq, amp_tensor_list grads,
+                                 amp_tensor_list bf16_out, const float *scale_dev,
+                                 const int32_t *found_inf_dev, int32_t *step_dev,
+                                 const amp_adamw_hyper *hyper, float *amax_dev,
+                                 amp_stream_t stream) {
+    if (!master || !exp_avg || !exp_avg_sq || !grads || !step_dev || !hyper)
+        return fail(AMP_EINVAL, "amp_adamw_master_step: NULL argument");
+    if (master->dtype != AMP_DT_F32 || exp_avg->dtype != AMP_DT_F32 ||
+        exp_avg_sq->dtype != AMP_DT_F32)
+        return fail(AMP_EDTYPE, "amp_adamw_master_step: master/exp_avg/exp_avg_sq must be f32");
+    const int gc = elem_code(grads->dtype);
+    if (gc < 0) return fail(AMP_EDTYPE, "amp_adamw_master_step: gradients must be f32/f16/bf16");
+    if (bf16_out && bf16_out->dtype != AMP_DT_BF16)
+        return fail(AMP_EDTYPE, "amp_adamw_master_step: bf16_out must be bf16");
+    if (!same_shapes(master, exp_avg) || !same_shapes(master, exp_avg_sq) ||
+        !same_shapes(master, grads) || (bf16_out && !same_shapes(master, bf16_out)))
+        return fail(AMP_EINVAL, "amp_adamw_master_step: lists differ in tensor count or sizes");
+    const bool slots = bf16_out && bf16_out->has_slots;
+    if (slots && !amax_dev)
+        return fail(AMP_EINVAL, "amp_adamw_master_step: bf16_out has amax slots but amax_dev is NULL");
+    const amp_adamw_hyper &h = *hyper;
+    amp::AdamwConsts c;
+    c.lr = h.lr;
+    c.beta1 = h.beta1;
+    c.beta2 = h.beta2;
+    c.decay = float(1.0 - h.lr * h.weight_decay);
+    c.b1 = float(h.beta1);
+    c.omb1 = float(1.0 - h.beta1);
+    c.b2 = float(h.beta2);
+    c.omb2 = float(1.0 - h.beta2);
+    c.eps = float(h.eps);
+    cudaError_t e = amp::launch_adamw(
+        master->view, exp_avg->view, exp_avg_sq->view, grads->view,
+        bf16_out ? &bf16_out->view : nullptr, master->n_chunks, gc, scale_dev, found_inf_dev,
+        step_dev, c, reinterpret_cast<amp::AdamwStepScalars *>(master->scratch), amax_dev, slots,
+        reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AMP_OK : cuda_fail(e, "amp_adamw_master_step");
+}
+
+amp_status fp8_quant_tensorwise(const void *x, amp_dtype x_dtype, int64_t rows, int64_t cols,
+                                amp_dtype fp8_dtype, double eps, void *out, void *out_t,
+                                float *inv_scale_dev, float *amax_dev, int amax_given,
+                                const int32_t *skip_if_dev, amp_stream_t stream) {
+    if (rows < 0 || cols < 0) return fail(AMP_EINVAL, "fp8_quant_tensorwise: negative size");
+    if (!inv_scale_dev || !amax_dev) return fail(AMP_EINVAL, "fp8_quant_tensorwise: NULL inv_scale/amax");
+    if (rows * cols > 0 && (!x || !out)) return fail(AMP_EINVAL, "fp8_quant_tensorwise: NULL x/out");
+    if (!(eps > 0.0)) return fail(AMP_EINVAL, "fp8_quant_tensorwise: eps must be > 0");
+    const int xc = elem_code(x_dtype), fc = fp8_code(fp8_dtype);
+    if (xc < 0 || fc < 0) return fail(AMP_EDTYPE, "fp8_quant_tensorwise: unsupported dtype");
+    const int64_t tiles = ((rows + amp::kTile - 1) / amp::kTile) * ((cols + amp::kTile - 1) / amp::kTile);
+    if (tiles > int64_t(INT32_MAX)) return fail(AMP_EINVAL, "fp8_quant_tensorwise: tensor too large");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "fp8_quant_tensorwise: cudaGetDevice");
+    e = amp::launch_fp8_quant(x, xc, rows, cols, fc, eps, static_cast<uint8_t *>(out),
+                              static_cast<uint8_t *>(out_t), inv_scale_dev, amax_dev,
+                              amax_given ? 1 : 0, skip_if_dev, dev,
+                              reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AMP_OK : cuda_fail(e, "fp8_quant_tensorwise");
+}
+
+amp_status fp8_quant_tensorwise_list(amp_tensor_list x, amp_tensor_list out, amp_tensor_list out_t,
+                                     amp_dtype fp8_dtype, double eps, const float *amax_dev,
+                                     float *inv_scale_dev, const int32_t *skip_if_dev,
+                                     amp_stream_t stream) {
+    if (!x || !out || !amax_dev || !inv_scale_dev)
+        return fail(AMP_EINVAL, "fp8_quant_tensorwise_list: NULL argument");
+    if (!x->two_d || !out->two_d || (out_t && !out_t->two_d))
+        return fail(AMP_EINVAL, "fp8_quant_tensorwise_list: lists must be 2-D");
+    if (!(eps > 0.0)) return fail(AMP_EINVAL, "fp8_quant_tensorwise_list: eps must be > 0");
+    const int xc = elem_code(x->dtype), fc = fp8_code(fp8_dtype);
+    if (xc < 0 || fc < 0 || out->dtype != fp8_dtype || (out_t && out_t->dtype != fp8_dtype))
+        return fail(AMP_EDTYPE, "fp8_quant_tensorwise_list: unsupported or mismatched dtype");
+    if (out->n != x->n || out->rows != x->rows || out->cols != x->cols)
+        return fail(AMP_EINVAL, "fp8_quant_tensorwise_list: out shapes differ from x");
+    if (out_t && (out_t->n != x->n || out_t->rows != x->cols || out_t->cols != x->rows))
+        return fail(AMP_EINVAL, "fp8_quant_tensorwise_list: out_t shapes are not x transposed");
+    cudaError_t e = amp::launch_fp8_quant_list(x->view, x->n_tiles, xc, out->view,
+                                               out_t ? &out_t->view : nullptr, fc, eps, amax_dev,
+                                               inv_scale_dev, skip_if_dev,
+                                               reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AMP_OK : cuda_fail(e, "fp8_quant_tensorwise_list");
+}
+
+amp_status amp_update_scale(float *scale_dev, int32_t *growth_tracker_dev, int32_t *found_inf_dev,
+                            float growth_factor, float backoff_factor, int32_t growth_interval,
+                            float *amax_dev, int n_amax, amp_stream_t stream) {
+    if (!scale_dev || !growth_tracker_dev || !found_inf_dev)
+        return fail(AMP_EINVAL, "amp_update_scale: NULL state pointer");
+    if (growth_interval < 1) return fail(AMP_EINVAL, "amp_update_scale: growth_interval < 1");
+    if (n_amax < 0 || (n_amax > 0 && !amax_dev))
+        return fail(AMP_EINVAL, "amp_update_scale: bad amax arguments");
+    cudaError_t e = amp::launch_update_scale(scale_dev, growth_tracker_dev, found_inf_dev,
+                                             growth_factor, backoff_factor, growth_interval,
+                                             amax_dev, n_amax,
+                                             reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AMP_OK : cuda_fail(e, "amp_update_scale");
+}
+
+}  // extern "C"

@@ -1,0 +1,118 @@
+// common.cuh - device-side building blocks shared by the libampfp8 kernels:
+// list views, vector memory access, exact format conversions.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace amp {
+
+// Elements per chunk of a 1-D tensor list.  One CTA walks one chunk.
+constexpr int kChunk = 16384;
+// Threads per CTA of the streaming list kernels.
+constexpr int kThreads = 256;
+// Square tile edge of the FP8 quantization kernels (bytes of fp8 output).
+constexpr int kTile = 128;
+
+// Device view of a tensor list handle (all arrays live in the handle's
+// device block).  chunks[c] = {tensor, chunk index within the tensor};
+// tiles[k] = {tensor, tile index within the tensor, row-major over tiles}.
+struct ListView {
+    void *const *ptrs;
+    const int64_t *numel;
+    const int64_t *rows;
+    const int64_t *cols;
+    const int32_t *slots;
+    const uint2 *chunks;
+    const uint2 *tiles;
+    int n;
+};
+
+enum ElemType : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
+enum Fp8Type : int { kE4M3 = 0, kE5M2 = 1 };
+
+// Canonical positive NaN codes written by the encoders.
+constexpr uint16_t kBf16NaN = 0x7FC0u;
+constexpr uint16_t kF16NaN = 0x7E00u;
+constexpr uint8_t kE4M3NaN = 0x7Fu;
+constexpr uint8_t kE5M2NaN = 0x7Eu;
+
+__device__ __forceinline__ bool aligned16(const void *p) {
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+// 16-byte loads/stores.  "cs" = streaming (evict-first) for data touched
+// once per step, plain for data another kernel of the step re-reads.
+__device__ __forceinline__ uint4 ld_cs(const void *p) {
+    return __ldcs(reinterpret_cast<const uint4 *>(p));
+}
+__device__ __forceinline__ uint4 ld_g(const void *p) {
+    return __ldg(reinterpret_cast<const uint4 *>(p));
+}
+__device__ __forceinline__ void st_cs(void *p, uint4 v) {
+    __stcs(reinterpret_cast<uint4 *>(p), v);
+}
+__device__ __forceinline__ void st_g(void *p, uint4 v) {
+    *reinterpret_cast<uint4 *>(p) = v;
+}
+
+// ---- exact widening conversions -----------------------------------------
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) {
+    return __uint_as_float(b << 16);
+}
+__device__ __forceinline__ float f16_bits_to_f32(uint32_t h) {
+    float f;
+    asm("{ .reg .b16 t; mov.b16 t, %1; cvt.f32.f16 %0, t; }" : "=f"(f) : "h"((unsigned short)h));
+    return f;
+}
+template <int ET>
+__device__ __forceinline__ float lowp_to_f32(uint32_t bits) {
+    return ET == kBF16 ? bf16_bits_to_f32(bits) : f16_bits_to_f32(bits);
+}
+
+// ---- round-to-nearest-even narrowing conversions ------------------------
+// Two fp32 -> packed bf16x2 (lo in bits 0..15), NaN -> canonical 0x7FC0.
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    if (lo != lo) r = (r & 0xFFFF0000u) | kBf16NaN;
+    if (hi != hi) r = (r & 0x0000FFFFu) | (uint32_t(kBf16NaN) << 16);
+    return r;
+}
+__device__ __forceinline__ uint16_t f32_to_bf16(float x) {
+    return (uint16_t)(f32x2_to_bf16x2(x, 0.0f) & 0xFFFFu);
+}
+__device__ __forceinline__ uint16_t f32_to_f16(float x) {
+    unsigned short h;
+    asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(x));
+    return x != x ? kF16NaN : (uint16_t)h;
+}
+
+// Two fp32 -> packed fp8x2 (lo in bits 0..7), round-to-nearest-even with
+// saturation to the largest finite value (the same bytes as clamping to
+// +-fp8_max first), NaN -> canonical code.
+template <int FT>
+__device__ __forceinline__ uint32_t f32x2_to_fp8x2(float lo, float hi) {
+    unsigned short r;
+    if (FT == kE4M3)
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    else
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    uint32_t v = r;
+    const uint32_t nan = FT == kE4M3 ? kE4M3NaN : kE5M2NaN;
+    if (lo != lo) v = (v & 0xFF00u) | nan;
+    if (hi != hi) v = (v & 0x00FFu) | (nan << 8);
+    return v;
+}
+
+template <int FT>
+__host__ __device__ constexpr float fp8_max() {
+    return FT == kE4M3 ? 448.0f : 57344.0f;
+}
+
+// Warp-wide unsigned max.
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
+    return __reduce_max_sync(0xFFFFFFFFu, v);
+}
+
+}  // namespace amp

@@ -1,0 +1,309 @@
+// fp8_quant.cu - A6..A9: tensorwise dynamic FP8 quantization with the
+// transposed (column-major) copy.
+//
+//   "FP8训练：量化、自动微分、Torchao" §2: amax = max|x| (fp32), scale =
+//   fp8_max / max(double(amax), EPS) in fp64, q = clamp(x*scale, +-fp8_max)
+//   cast to fp8, inv_scale = 1/scale; §3: e4m3fn (448) for weights and
+//   activations, e5m2 (57344) for gradients; §4: the backward GEMMs need
+//   column-major copies, i.e. the same bytes laid out [cols, rows].
+//
+// amax pass (single tensor, when not given): grid-stride 16-byte loads, SIMD
+//   integer max of |x| bit patterns, one atomicMax per warp - 2 bytes read
+//   per bf16 element.
+// quant pass: one CTA per 128x128 tile.  Each thread loads 8 rows x 8
+//   columns with 16-byte coalesced loads, converts pairs with the hardware
+//   RNE+satfinite cvt, stores its 8 row-major bytes, and parks them in a
+//   16 KB shared tile whose 4-byte words are XOR-swizzled by row band.  The
+//   transposed copy is then read back 16 words per thread (conflict-free),
+//   transposed 4x4 bytes at a time with byte permutes, and written as 16-byte
+//   stores in which 8 lanes cover one 128-byte segment of a transposed row.
+//   Bytes: 2 read + 1 + 1 written per element.
+// Tiles on a ragged edge, or with sizes/addresses that break 16-byte access,
+// take an element-wise path with the same arithmetic.
+#include <algorithm>
+
+#include "internal.h"
+
+namespace amp {
+namespace {
+
+template <int XT>
+__device__ __forceinline__ float x_at(const void *x, int64_t k) {
+    if (XT == kF32) return static_cast<const float *>(x)[k];
+    return lowp_to_f32<XT>(static_cast<const uint16_t *>(x)[k]);
+}
+
+// scale_d = fp8_max / max(double(amax), eps) with NaN propagating.
+__device__ __forceinline__ void tensor_scale(float amax, double eps, float fmax, float &s32,
+                                             float &inv) {
+    const double a = double(amax);
+    const double cl = (a != a) ? a : (a < eps ? eps : a);
+    const double sd = double(fmax) / cl;
+    s32 = float(sd);
+    inv = float(1.0 / sd);
+}
+
+template <int FT>
+__device__ __forceinline__ uint8_t quant1(float x, float s32) {
+    return uint8_t(f32x2_to_fp8x2<FT>(__fmul_rn(x, s32), 0.0f) & 0xFFu);
+}
+
+// 4-byte word (row r, word w) of the 128x128 byte tile, XOR-swizzled so that
+// the transposed read pattern hits 32 distinct banks.
+__device__ __forceinline__ int swz(int r, int w) { return r * 32 + (w ^ (((r >> 4) & 7) << 2)); }
+
+template <int XT, int FT>
+__device__ __forceinline__ void quant_tile(const void *x, int64_t rows, int64_t cols, uint8_t *out,
+                                           uint8_t *out_t, int64_t r0, int64_t c0,
+                                           const float *s_scale, uint32_t *sm) {
+    constexpr int esz = XT == kF32 ? 4 : 2;
+    constexpr int nv = XT == kF32 ? 2 : 1;  // 16-byte loads per 8 elements
+    const bool fast = r0 + kTile <= rows && c0 + kTile <= cols && (cols & 7) == 0 &&
+                      aligned16(x) && (reinterpret_cast<uintptr_t>(out) & 7) == 0 &&
+                      (out_t == nullptr || ((rows & 15) == 0 && aligned16(out_t)));
+    if (fast) {
+        const int c8 = threadIdx.x & 15, rb = threadIdx.x >> 4;
+        uint4 raw[8][nv];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int64_t e = (r0 + rb + 16 * k) * cols + c0 + 8 * c8;
+            const char *src = static_cast<const char *>(x) + e * esz;
+#pragma unroll
+            for (int u = 0; u < nv; ++u) raw[k][u] = ld_cs(src + 16 * u);
+        }
+        __syncthreads();  // s_scale is ready
+        const float s32 = *s_scale;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            float y[8];
+            if constexpr (XT == kF32) {
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    y[4 * u + 0] = __uint_as_float(raw[k][u].x);
+                    y[4 * u + 1] = __uint_as_float(raw[k][u].y);
+                    y[4 * u + 2] = __uint_as_float(raw[k][u].z);
+                    y[4 * u + 3] = __uint_as_float(raw[k][u].w);
+                }
+            } else {
+                const uint32_t w[4] = {raw[k][0].x, raw[k][0].y, raw[k][0].z, raw[k][0].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    y[2 * j] = lowp_to_f32<XT>(w[j] & 0xFFFFu);
+                    y[2 * j + 1] = lowp_to_f32<XT>(w[j] >> 16);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) y[j] = __fmul_rn(y[j], s32);
+            uint2 q;
+            q.x = f32x2_to_fp8x2<FT>(y[0], y[1]) | (f32x2_to_fp8x2<FT>(y[2], y[3]) << 16);
+            q.y = f32x2_to_fp8x2<FT>(y[4], y[5]) | (f32x2_to_fp8x2<FT>(y[6], y[7]) << 16);
+            const int r = rb + 16 * k;
+            *reinterpret_cast<uint2 *>(out + (r0 + r) * cols + c0 + 8 * c8) = q;
+            if (out_t) *reinterpret_cast<uint2 *>(sm + swz(r, 2 * c8)) = q;
+        }
+        if (out_t == nullptr) return;
+        __syncthreads();
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        const int rg = lane & 7, wq = (lane >> 3) + 4 * warp;
+        uint32_t wv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) wv[i] = sm[(16 * rg + i) * 32 + (wq ^ (rg << 2))];
+        uint32_t col[4][4];  // col[j][blk]: rows 4blk..4blk+3 of column 4wq+j
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk) {
+            const uint32_t a = wv[4 * blk], b = wv[4 * blk + 1], c = wv[4 * blk + 2],
+                           d = wv[4 * blk + 3];
+            const uint32_t t0 = __byte_perm(a, b, 0x5140), t1 = __byte_perm(a, b, 0x7362);
+            const uint32_t t2 = __byte_perm(c, d, 0x5140), t3 = __byte_perm(c, d, 0x7362);
+            col[0][blk] = __byte_perm(t0, t2, 0x5410);
+            col[1][blk] = __byte_perm(t0, t2, 0x7632);
+            col[2][blk] = __byte_perm(t1, t3, 0x5410);
+            col[3][blk] = __byte_perm(t1, t3, 0x7632);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t dst = (c0 + 4 * wq + j) * rows + r0 + 16 * rg;
+            st_g(out_t + dst, make_uint4(col[j][0], col[j][1], col[j][2], col[j][3]));
+        }
+    } else {
+        __syncthreads();
+        const float s32 = *s_scale;
+        for (int idx = threadIdx.x; idx < kTile * kTile; idx += kThreads) {
+            const int64_t i = r0 + (idx >> 7), j = c0 + (idx & (kTile - 1));
+            if (i < rows && j < cols) {
+                const uint8_t q = quant1<FT>(x_at<XT>(x, i * cols + j), s32);
+                out[i * cols + j] = q;
+                if (out_t) out_t[j * rows + i] = q;
+            }
+        }
+    }
+}
+
+template <int XT, int FT>
+__global__ void __launch_bounds__(kThreads) quant_single_kernel(const void *x, int64_t rows,
+                                                                int64_t cols, uint8_t *out,
+                                                                uint8_t *out_t, const float *amax,
+                                                                float *inv_scale, double eps,
+                                                                const int32_t *skip_if) {
+    if (skip_if && *skip_if) return;
+    __shared__ __align__(16) uint32_t sm[kTile * 32];
+    __shared__ float s_scale;
+    const int64_t tiles_c = (cols + kTile - 1) / kTile;
+    const int64_t tr = blockIdx.x / tiles_c, tc = blockIdx.x % tiles_c;
+    if (threadIdx.x == 0) {
+        float s32, inv;
+        tensor_scale(*amax, eps, fp8_max<FT>(), s32, inv);
+        s_scale = s32;
+        if (blockIdx.x == 0) *inv_scale = inv;
+    }
+    quant_tile<XT, FT>(x, rows, cols, out, out_t, tr * kTile, tc * kTile, &s_scale, sm);
+}
+
+template <int XT, int FT>
+__global__ void __launch_bounds__(kThreads) quant_list_kernel(ListView X, ListView O, ListView OT,
+                                                              int has_t, const float *amax,
+                                                              float *inv_scale, double eps,
+                                                              const int32_t *skip_if) {
+    if (skip_if && *skip_if) return;
+    __shared__ __align__(16) uint32_t sm[kTile * 32];
+    __shared__ float s_scale;
+    const uint2 tl = X.tiles[blockIdx.x];
+    const int t = int(tl.x);
+    const int64_t rows = X.rows[t], cols = X.cols[t];
+    const int64_t tiles_c = (cols + kTile - 1) / kTile;
+    const int64_t tr = tl.y / tiles_c, tc = tl.y % tiles_c;
+    if (threadIdx.x == 0) {
+        float s32, inv;
+        tensor_scale(amax[t], eps, fp8_max<FT>(), s32, inv);
+        s_scale = s32;
+        if (tl.y == 0) inv_scale[t] = inv;
+    }
+    uint8_t *ot = has_t ? static_cast<uint8_t *>(OT.ptrs[t]) : nullptr;
+    quant_tile<XT, FT>(X.ptrs[t], rows, cols, static_cast<uint8_t *>(O.ptrs[t]), ot,
+                       tr * kTile, tc * kTile, &s_scale, sm);
+}
+
+template <int XT>
+__global__ void __launch_bounds__(kThreads) amax_kernel(const void *x, int64_t n,
+                                                        unsigned int *amax_bits) {
+    const int64_t gtid = int64_t(blockIdx.x) * kThreads + threadIdx.x;
+    const int64_t gstride = int64_t(gridDim.x) * kThreads;
+    uint32_t mx = 0;
+    if (aligned16(x)) {
+        constexpr int per = XT == kF32 ? 4 : 8;
+        const int64_t nv = n / per;
+        const char *b = static_cast<const char *>(x);
+        for (int64_t i = gtid; i < nv; i += gstride) {
+            const uint4 w = ld_cs(b + i * 16);
+            if (XT == kF32) {
+                mx = max(mx, max(max(w.x & 0x7FFFFFFFu, w.y & 0x7FFFFFFFu),
+                                 max(w.z & 0x7FFFFFFFu, w.w & 0x7FFFFFFFu)));
+            } else {
+                mx = __vmaxu2(mx, __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
+                                           __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu)));
+            }
+        }
+        if (XT != kF32) mx = max(mx & 0xFFFFu, mx >> 16);
+        for (int64_t k = nv * per + gtid; k < n; k += gstride) {
+            mx = max(mx, XT == kF32 ? (static_cast<const uint32_t *>(x)[k] & 0x7FFFFFFFu)
+                                    : uint32_t(static_cast<const uint16_t *>(x)[k] & 0x7FFFu));
+        }
+    } else {
+        for (int64_t k = gtid; k < n; k += gstride) {
+            mx = max(mx, XT == kF32 ? (static_cast<const uint32_t *>(x)[k] & 0x7FFFFFFFu)
+                                    : uint32_t(static_cast<const uint16_t *>(x)[k] & 0x7FFFu));
+        }
+    }
+    // |x| bit patterns -> fp32 bit patterns of the same magnitude (monotone,
+    // NaN above inf), so an unsigned max is the NaN-propagating fp32 max.
+    uint32_t f;
+    if (XT == kF32) f = mx;
+    else if (XT == kBF16) f = mx << 16;
+    else f = __float_as_uint(f16_bits_to_f32(mx));
+    f = warp_max_u32(f);
+    if ((threadIdx.x & 31) == 0 && f != 0) atomicMax(amax_bits, f);
+}
+
+__global__ void quant_empty_kernel(float *amax, int amax_given, float *inv_scale, double eps,
+                                   float fmax, const int32_t *skip_if) {
+    if (skip_if && *skip_if) return;
+    if (!amax_given) *amax = 0.0f;
+    float s32, inv;
+    tensor_scale(*amax, eps, fmax, s32, inv);
+    *inv_scale = inv;
+}
+
+template <int XT, int FT>
+cudaError_t launch_single(const void *x, int64_t rows, int64_t cols, uint8_t *out, uint8_t *out_t,
+                          float *inv_scale, float *amax, int amax_given, double eps,
+                          const int32_t *skip_if, int device, cudaStream_t s) {
+    const int64_t n = rows * cols;
+    if (!amax_given) {
+        // amax is an output here: it starts from +0 and is max-reduced.
+        cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), s);
+        if (e != cudaSuccess) return e;
+        const int64_t per = XT == kF32 ? 4 : 8;
+        const int64_t want = (n / per + kThreads - 1) / kThreads;
+        const int64_t cap = int64_t(sm_count(device)) * 8;
+        const unsigned grid = (unsigned)std::max<int64_t>(1, std::min(want, cap));
+        amax_kernel<XT><<<grid, kThreads, 0, s>>>(x, n, reinterpret_cast<unsigned int *>(amax));
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    const int64_t tiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
+    quant_single_kernel<XT, FT><<<unsigned(tiles), kThreads, 0, s>>>(x, rows, cols, out, out_t,
+                                                                      amax, inv_scale, eps,
+                                                                      skip_if);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fp8_quant(const void *x, int xelem, int64_t rows, int64_t cols, int fp8,
+                             double eps, uint8_t *out, uint8_t *out_t, float *inv_scale,
+                             float *amax, int amax_given, const int32_t *skip_if, int device,
+                             cudaStream_t s) {
+    if (rows * cols == 0) {
+        quant_empty_kernel<<<1, 1, 0, s>>>(amax, amax_given, inv_scale, eps,
+                                           fp8 == kE4M3 ? fp8_max<kE4M3>() : fp8_max<kE5M2>(),
+                                           skip_if);
+        return cudaGetLastError();
+    }
+#define AMP_Q1(XT, FT) \
+    launch_single<XT, FT>(x, rows, cols, out, out_t, inv_scale, amax, amax_given, eps, skip_if, \
+                          device, s)
+    if (fp8 == kE4M3) {
+        if (xelem == kBF16) return AMP_Q1(kBF16, kE4M3);
+        if (xelem == kF16) return AMP_Q1(kF16, kE4M3);
+        return AMP_Q1(kF32, kE4M3);
+    }
+    if (xelem == kBF16) return AMP_Q1(kBF16, kE5M2);
+    if (xelem == kF16) return AMP_Q1(kF16, kE5M2);
+    return AMP_Q1(kF32, kE5M2);
+#undef AMP_Q1
+}
+
+cudaError_t launch_fp8_quant_list(const ListView &x, int64_t n_tiles, int xelem,
+                                  const ListView &out, const ListView *out_t, int fp8,
+                                  double eps, const float *amax, float *inv_scale,
+                                  const int32_t *skip_if, cudaStream_t s) {
+    if (n_tiles == 0) return cudaSuccess;
+    const ListView ot = out_t ? *out_t : ListView{};
+    const int has_t = out_t != nullptr;
+    const dim3 grid((unsigned)n_tiles), block(kThreads);
+#define AMP_QL(XT, FT) \
+    quant_list_kernel<XT, FT><<<grid, block, 0, s>>>(x, out, ot, has_t, amax, inv_scale, eps, skip_if)
+    if (fp8 == kE4M3) {
+        if (xelem == kBF16) AMP_QL(kBF16, kE4M3);
+        else if (xelem == kF16) AMP_QL(kF16, kE4M3);
+        else AMP_QL(kF32, kE4M3);
+    } else {
+        if (xelem == kBF16) AMP_QL(kBF16, kE5M2);
+        else if (xelem == kF16) AMP_QL(kF16, kE5M2);
+        else AMP_QL(kF32, kE5M2);
+    }
+#undef AMP_QL
+    return cudaGetLastError();
+}
+
+}  // namespace amp

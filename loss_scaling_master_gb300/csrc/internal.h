@@ -1,0 +1,69 @@
+// internal.h - host-side pieces shared by the C-ABI layer (api.cu) and the
+// kernel translation units: the list handle and the launch functions.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "ampfp8.h"
+#include "common.cuh"
+
+struct amp_tensor_list_s {
+    int n = 0;
+    amp_dtype dtype = AMP_DT_F32;
+    bool two_d = false;
+    int device = 0;
+    std::vector<void *> ptrs;
+    std::vector<int64_t> numel, rows, cols;
+    int64_t n_chunks = 0;
+    int64_t n_tiles = 0;
+    bool has_slots = false;
+    void *block = nullptr;   // the single device allocation
+    void *scratch = nullptr; // 256 bytes of it for per-call kernel scalars
+    amp::ListView view{};    // pointers into `block`
+};
+
+namespace amp {
+
+// Per-step AdamW constants prepared on the host (fp64 -> fp32 once).
+struct AdamwConsts {
+    double lr, beta1, beta2;          // per-step scalars are formed on device
+    float decay, b1, omb1, b2, omb2, eps;
+};
+
+// Device scalars of one AdamW step, written by the prologue kernel.
+struct AdamwStepScalars {
+    int32_t skip;
+    float step_size;
+    float bc2_sqrt;
+    float pad;
+};
+
+int sm_count(int device);
+
+cudaError_t launch_unscale_check(const ListView &g, int64_t n_chunks, int elem, const float *scale,
+                                 int32_t *found_inf, int inplace, cudaStream_t s);
+
+cudaError_t launch_adamw(const ListView &p, const ListView &m, const ListView &v,
+                         const ListView &g, const ListView *b, int64_t n_chunks, int gelem,
+                         const float *scale, const int32_t *found_inf, int32_t *step,
+                         const AdamwConsts &c, AdamwStepScalars *scal, float *amax,
+                         bool use_slots, cudaStream_t s);
+
+cudaError_t launch_update_scale(float *scale, int32_t *tracker, int32_t *found_inf, float growth,
+                                float backoff, int32_t interval, float *amax, int n_amax,
+                                cudaStream_t s);
+
+cudaError_t launch_fp8_quant(const void *x, int xelem, int64_t rows, int64_t cols, int fp8,
+                             double eps, uint8_t *out, uint8_t *out_t, float *inv_scale,
+                             float *amax, int amax_given, const int32_t *skip_if, int device,
+                             cudaStream_t s);
+
+cudaError_t launch_fp8_quant_list(const ListView &x, int64_t n_tiles, int xelem,
+                                  const ListView &out, const ListView *out_t, int fp8,
+                                  double eps, const float *amax, float *inv_scale,
+                                  const int32_t *skip_if, cudaStream_t s);
+
+}  // namespace amp

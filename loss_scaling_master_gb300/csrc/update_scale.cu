@@ -1,0 +1,47 @@
+// update_scale.cu - A3: the dynamic loss-scale state machine
+// ("第20章 量化与混合精度训练" §20.5.33 GradScaler 的 _growth_tracker 状态机细节;
+// "06 · 混合精度" §四: skip and halve on inf/NaN, double after N clean steps).
+// One thread updates {scale, tracker} in place from found_inf; the block then
+// clears found_inf and the per-tensor amax slots for the next step, so the
+// host never reads the state back.
+#include "internal.h"
+
+namespace amp {
+namespace {
+
+__global__ void update_scale_kernel(float *scale, int32_t *tracker, int32_t *found_inf,
+                                    float growth, float backoff, int32_t interval, float *amax,
+                                    int n_amax) {
+    if (threadIdx.x == 0) {
+        const int32_t fi = *found_inf;
+        float s = *scale;
+        int32_t t = *tracker;
+        if (fi) {
+            s = __fmul_rn(s, backoff);
+            t = 0;
+        } else {
+            t = t + 1;
+            if (t >= interval) {
+                const float grown = __fmul_rn(s, growth);
+                if (isfinite(grown)) s = grown;
+                t = 0;
+            }
+        }
+        *scale = s;
+        *tracker = t;
+        *found_inf = 0;
+    }
+    for (int i = threadIdx.x; i < n_amax; i += blockDim.x) amax[i] = 0.0f;
+}
+
+}  // namespace
+
+cudaError_t launch_update_scale(float *scale, int32_t *tracker, int32_t *found_inf, float growth,
+                                float backoff, int32_t interval, float *amax, int n_amax,
+                                cudaStream_t s) {
+    update_scale_kernel<<<1, 256, 0, s>>>(scale, tracker, found_inf, growth, backoff, interval,
+                                          amax, n_amax);
+    return cudaGetLastError();
+}
+
+}  // namespace amp

@@ -1,0 +1,72 @@
+"""The C-ABI library loads, exports every symbol include/ampfp8.h declares,
+and rejects invalid arguments with a status before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from loss_scaling_master_gb300 import build as B
+    B.build()
+    import loss_scaling_master_gb300 as pkg
+    return pkg.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "ampfp8.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:amp_status|const char \*|int)\s*\*?\s*(\w+)\s*\(",
+                                 src, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) == 10, names
+    from loss_scaling_master_gb300._lib import EXPORTS
+    assert sorted(EXPORTS) == names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_abi_version(lib):
+    assert lib.amp_abi_version() == 1
+
+
+def test_invalid_arguments_return_status(lib):
+    from loss_scaling_master_gb300._lib import DT, amp_adamw_hyper
+    EINVAL, EDTYPE = -1, -2
+    P = ctypes.c_void_p
+    assert lib.amp_unscale_check(None, None, None, 0, None) == EINVAL
+    assert b"NULL" in lib.amp_last_error()
+    h = amp_adamw_hyper(1e-3, 0.9, 0.999, 1e-8, 0.0)
+    assert lib.amp_adamw_master_step(None, None, None, None, None, None, None, None,
+                                     ctypes.byref(h), None, None) == EINVAL
+    assert lib.amp_update_scale(None, None, None, 2.0, 0.5, 10, None, 0, None) == EINVAL
+    dummy = P(16)
+    assert lib.amp_update_scale(dummy, dummy, dummy, 2.0, 0.5, 0, None, 0, None) == EINVAL
+    assert lib.amp_update_scale(dummy, dummy, dummy, 2.0, 0.5, 1, None, 3, None) == EINVAL
+    # fp8 quant: negative size, bad eps, unsupported dtypes
+    assert lib.fp8_quant_tensorwise(dummy, DT["bf16"], -1, 4, DT["e4m3fn"], 1e-12, dummy, None,
+                                    dummy, dummy, 0, None, None) == EINVAL
+    assert lib.fp8_quant_tensorwise(dummy, DT["bf16"], 4, 4, DT["e4m3fn"], 0.0, dummy, None,
+                                    dummy, dummy, 0, None, None) == EINVAL
+    assert lib.fp8_quant_tensorwise(dummy, DT["e4m3fn"], 4, 4, DT["e4m3fn"], 1e-12, dummy, None,
+                                    dummy, dummy, 0, None, None) == EDTYPE
+    assert lib.fp8_quant_tensorwise(dummy, DT["bf16"], 4, 4, DT["f16"], 1e-12, dummy, None,
+                                    dummy, dummy, 0, None, None) == EDTYPE
+    # list creation: negative n, NULL arrays, negative size, NULL pointer of a non-empty tensor
+    out = P()
+    assert lib.amp_tensor_list_create(-1, None, None, None, DT["f32"], None, ctypes.byref(out)) == EINVAL
+    assert lib.amp_tensor_list_create(1, None, None, None, DT["f32"], None, ctypes.byref(out)) == EINVAL
+    ptrs = (P * 1)(None)
+    neg = (ctypes.c_int64 * 1)(-5)
+    one = (ctypes.c_int64 * 1)(7)
+    assert lib.amp_tensor_list_create(1, ptrs, neg, None, DT["f32"], None, ctypes.byref(out)) == EINVAL
+    assert lib.amp_tensor_list_create(1, ptrs, one, None, DT["f32"], None, ctypes.byref(out)) == EINVAL
+    assert lib.amp_tensor_list_create(1, ptrs, one, None, 99, None, ctypes.byref(out)) == EDTYPE
+    assert not out.value

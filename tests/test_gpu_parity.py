@@ -1,0 +1,416 @@
+"""CUDA path (through the C ABI) vs the CPU oracle, element by element, on
+seeded inputs that span several chunks/tiles, ragged tails, misaligned
+tensors and the method's degenerate cases."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from parity_helpers import (assert_bf16_close, assert_state_close, bit_identical_fraction,
+                            to_device, to_host_bits)
+
+pytestmark = pytest.mark.gpu
+
+RAGGED = [1, 7, 8, 9, 63, 64, 67, 255, 256, 257, 1000, 4096, 16383, 16384, 16385, 40000]
+
+
+@pytest.fixture(scope="module")
+def A():
+    from loss_scaling_master_gb300 import build as B
+    B.build()
+    import loss_scaling_master_gb300 as pkg
+    pkg.load()
+    assert torch.cuda.is_available()
+    return pkg
+
+
+@pytest.fixture(scope="module")
+def dev(A):
+    return torch.device("cuda:0")
+
+
+def _grads_host(rng, sizes, dt, sigma=1.0):
+    out = []
+    for n in sizes:
+        x = (rng.standard_normal(n) * sigma).astype(np.float32)
+        if dt == "f32":
+            out.append(x)
+        elif dt == "f16":
+            out.append(x.astype(np.float16).view(np.uint16))
+        else:
+            out.append(O.encode("bf16", x))
+    return out
+
+
+def _device_views(host_list, dt, device, misalign: bool):
+    """Device tensors holding host_list; with misalign, packed back to back
+    in one buffer with a 1-element lead, so most bases are not 16-byte aligned."""
+    if not misalign:
+        return [to_device(h, dt, device) for h in host_list]
+    flat = np.concatenate([np.zeros(1, host_list[0].dtype)] + list(host_list))
+    buf = to_device(flat, dt, device)
+    views, off = [], 1
+    for h in host_list:
+        views.append(buf[off:off + h.size])
+        off += h.size
+    return views
+
+
+def _inf_bits(dt, val):
+    if dt == "f32":
+        return np.float32(val)
+    if dt == "f16":
+        return np.array([val], np.float16).view(np.uint16)[0]
+    return O.encode("bf16", np.array([val], np.float32))[0]
+
+
+# ------------------------------------------------------------ unscale / check
+@pytest.mark.parametrize("dt", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("misalign", [False, True])
+def test_unscale_check_parity(A, dev, dt, misalign):
+    rng = np.random.default_rng(10)
+    sizes = RAGGED
+    base = _grads_host(rng, sizes, dt, sigma=3.0)
+    cases = []
+    for scale in (65536.0, 1.0, 2.0 ** -20, 1e-35, 0.0, np.inf, np.nan, -4.0):
+        cases.append((scale, None))
+    for site in ((len(sizes) - 1, sizes[-1] - 1, np.inf), (5, 0, np.nan), (9, 256, -np.inf),
+                 (13, 16383, np.inf), (14, 16384, np.nan)):
+        cases.append((65536.0, site))
+    for scale, site in cases:
+        hl = [h.copy() for h in base]
+        if site is not None:
+            hl[site[0]][site[1]] = _inf_bits(dt, site[2])
+        tensors = _device_views(hl, dt, dev, misalign)
+        L = A.amp_tensor_list_create(tensors)
+        for start in (0, 1):
+            fi = torch.tensor([start], dtype=torch.int32, device=dev)
+            s = torch.tensor([scale], dtype=torch.float32, device=dev)
+            A.amp_unscale_check(L, s, fi)
+            expect = O.unscale_check([h.copy() for h in hl], dt, float(np.float32(scale)),
+                                     found_inf=start)
+            assert int(fi.item()) == expect, (dt, misalign, scale, site, start)
+        L.close()
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16", "f32"])
+def test_unscale_inplace_parity(A, dev, dt):
+    rng = np.random.default_rng(11)
+    hl = _grads_host(rng, RAGGED, dt, sigma=1e3)
+    hl[3][2] = _inf_bits(dt, np.nan)
+    for scale in (65536.0, 3.0, 1e-3):
+        tensors = _device_views(hl, dt, dev, misalign=True)
+        L = A.amp_tensor_list_create(tensors)
+        fi = torch.zeros(1, dtype=torch.int32, device=dev)
+        A.amp_unscale_check(L, torch.tensor([scale], device=dev), fi, inplace=True)
+        ref = [h.copy() for h in hl]
+        expect = O.unscale_check(ref, dt, scale, inplace=True)
+        assert int(fi.item()) == expect == 1
+        for t, r in zip(tensors, ref):
+            got = to_host_bits(t)
+            assert np.array_equal(got.view(r.dtype) if dt != "f32" else got.view(np.uint32),
+                                  r if dt != "f32" else r.view(np.uint32))
+        L.close()
+
+
+# ------------------------------------------------------------ scale machine
+def test_update_scale_parity(A, dev):
+    rng = np.random.default_rng(12)
+    for interval, growth, backoff, init in ((2, 2.0, 0.5, 65536.0), (10, 2.0, 0.5, 65536.0),
+                                            (1, 2.0, 0.5, 2.0 ** 126), (3, 1.0, 1.0, 1.0),
+                                            (5, 3.0, 0.25, 1000.0)):
+        s = torch.tensor([init], dtype=torch.float32, device=dev)
+        t = torch.zeros(1, dtype=torch.int32, device=dev)
+        fi = torch.zeros(1, dtype=torch.int32, device=dev)
+        amax = torch.full((5,), 7.0, device=dev)
+        rs, rt = float(np.float32(init)), 0
+        for k in range(60):
+            flag = int(rng.random() < 0.15)
+            fi.fill_(flag)
+            A.amp_update_scale(s, t, fi, growth, backoff, interval, amax=amax, n_amax=5)
+            ram = np.full(5, 7.0, np.float32)
+            rs, rt, rfi = O.update_scale(rs, rt, flag, growth, backoff, interval, ram)
+            assert float(s.item()) == rs and int(t.item()) == rt and int(fi.item()) == rfi == 0
+            assert not amax.any()
+            amax.fill_(7.0)
+
+
+# ------------------------------------------------------------------- AdamW
+def _adamw_case(A, dev, gdt, misalign, sizes, steps, hyper, scales, skip_at, slots, seed):
+    rng = np.random.default_rng(seed)
+    n = len(sizes)
+    master_h = [(rng.standard_normal(k) * 0.02).astype(np.float32) for k in sizes]
+    mk = lambda hs, dt: _device_views(hs, dt, dev, misalign)
+    P = mk(master_h, "f32")
+    M = mk([np.zeros(k, np.float32) for k in sizes], "f32")
+    V = mk([np.zeros(k, np.float32) for k in sizes], "f32")
+    G = mk(_grads_host(rng, sizes, gdt), gdt)
+    Bf = mk([np.zeros(k, np.uint16) for k in sizes], "bf16")
+    LP, LM, LV, LG, LB = (A.amp_tensor_list_create(x) for x in (P, M, V, G, Bf))
+    n_slots = max(slots) + 1 if slots else 0
+    if slots:
+        A.amp_tensor_list_set_amax_slots(LB, slots)
+    amax = torch.zeros(max(n_slots, 1), device=dev)
+    step = torch.zeros(1, dtype=torch.int32, device=dev)
+    fi = torch.zeros(1, dtype=torch.int32, device=dev)
+    s_dev = torch.zeros(1, device=dev)
+    rp = [x.copy() for x in master_h]
+    rm = [np.zeros(k, np.float32) for k in sizes]
+    rv = [np.zeros(k, np.float32) for k in sizes]
+    rb = [np.zeros(k, np.uint16) for k in sizes]
+    rstep = 0
+    for k in range(steps):
+        S = scales[k % len(scales)]
+        gh = _grads_host(rng, sizes, gdt, sigma=1e-3 * S)
+        for t, h in zip(G, gh):
+            t.copy_(to_device(h, gdt, dev))
+        skip = int(k in skip_at)
+        fi.fill_(skip)
+        s_dev.fill_(S)
+        amax.zero_()
+        A.amp_adamw_master_step(LP, LM, LV, LG, LB, s_dev, fi, step, *hyper,
+                                amax=amax if slots else None)
+        ram = np.zeros(max(n_slots, 1), np.float32)
+        rstep = O.adamw_master_step(rp, rm, rv, gh, gdt, rb, float(np.float32(S)), skip, rstep,
+                                    *hyper, amax_slot=slots, amax=ram)
+        assert int(step.item()) == rstep
+        if slots:
+            assert np.array_equal(to_host_bits(amax)[:n_slots].view(np.uint32),
+                                  ram[:n_slots].view(np.uint32))
+    ident = []
+    for i in range(n):
+        gp, gm, gv = to_host_bits(P[i]), to_host_bits(M[i]), to_host_bits(V[i])
+        assert_state_close(gp, rp[i], f"master[{i}]")
+        assert_state_close(gm, rm[i], f"exp_avg[{i}]")
+        assert_state_close(gv, rv[i], f"exp_avg_sq[{i}]")
+        assert_bf16_close(to_host_bits(Bf[i]), rb[i], f"bf16[{i}]")
+        ident += [bit_identical_fraction(gp, rp[i]), bit_identical_fraction(gm, rm[i]),
+                  bit_identical_fraction(gv, rv[i])]
+    for L in (LP, LM, LV, LG, LB):
+        L.close()
+    return min(ident)
+
+
+@pytest.mark.parametrize("gdt", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("misalign", [False, True])
+def test_adamw_parity(A, dev, gdt, misalign):
+    sizes = RAGGED + [3 * 16384 + 5]
+    slots = [-1] * len(sizes)
+    slots[4], slots[13], slots[-1] = 0, 1, 2
+    ident = _adamw_case(A, dev, gdt, misalign, sizes, steps=6,
+                        hyper=(1e-3, 0.9, 0.999, 1e-8, 0.01), scales=[65536.0, 1024.0, 3.0],
+                        skip_at={2}, slots=slots, seed=20)
+    # same operation order on both sides: expect bit-identical fp32 state
+    assert ident == 1.0, f"fp32 state not bit-identical (min fraction {ident})"
+
+
+def test_adamw_gpt2_hyper_no_scale(A, dev):
+    """bf16 grads, S fixed 1.0, lr 3e-4, betas (0.9, 0.95), wd 0.1."""
+    ident = _adamw_case(A, dev, "bf16", False, [768, 50257, 3 * 768 * 10], steps=10,
+                        hyper=(3e-4, 0.9, 0.95, 1e-8, 0.1), scales=[1.0], skip_at=set(),
+                        slots=None, seed=21)
+    assert ident == 1.0
+
+
+def test_adamw_bf16_emission_exhaustive_rounding_classes(A, dev):
+    """lr = 0 and wd = 0 leave p unchanged, so the bf16 copy is RNE(p) for
+    every fp32 p of the rounding-class sweep (ties, near-ties, subnormals,
+    inf, NaN, signed zeros)."""
+    hi = np.arange(1 << 20, dtype=np.uint64) << 12
+    lows = np.array([0, 1, 0x7FF, 0x800, 0x801, 0xFFF], np.uint64)
+    p = (hi[:, None] | lows[None, :]).astype(np.uint32).ravel().view(np.float32)
+    P = [to_device(p, "f32", dev)]
+    M = [torch.zeros(p.size, device=dev)]
+    V = [torch.zeros(p.size, device=dev)]
+    G = [torch.zeros(p.size, dtype=torch.float16, device=dev)]
+    B = [torch.empty(p.size, dtype=torch.bfloat16, device=dev)]
+    Ls = [A.amp_tensor_list_create(x) for x in (P, M, V, G, B)]
+    step = torch.zeros(1, dtype=torch.int32, device=dev)
+    A.amp_adamw_master_step(*Ls, None, None, step, 0.0, 0.9, 0.999, 1e-8, 0.0)
+    got = to_host_bits(B[0])
+    ref = O.encode("bf16", p)
+    assert np.array_equal(got, ref)
+    gp = to_host_bits(P[0])
+    nan = np.isnan(p)
+    assert np.array_equal(gp[~nan].view(np.uint32), p[~nan].view(np.uint32))
+    for L in Ls:
+        L.close()
+
+
+# -------------------------------------------------------------------- FP8
+FP8_SHAPES = [(1, 1), (3, 5), (17, 31), (128, 128), (127, 129), (256, 384), (129, 136),
+              (300, 520), (64, 4096), (384, 256)]
+
+
+def _x_host(rng, rows, cols, xdt, outliers=True):
+    x = rng.standard_normal(rows * cols).astype(np.float32)
+    if outliers and x.size > 10:
+        idx = rng.choice(x.size, size=max(1, x.size // 1000), replace=False)
+        x[idx] *= 100
+    if xdt == "f32":
+        return x
+    if xdt == "f16":
+        return x.astype(np.float16).view(np.uint16)
+    return O.encode("bf16", x)
+
+
+def _run_quant(A, dev, xh, xdt, rows, cols, fmt, with_t, amax_given=None, skip=None,
+               misalign=False):
+    x = _device_views([xh], xdt, dev, misalign)[0]
+    out = torch.full((rows * cols,), 0xA5, dtype=torch.uint8, device=dev)
+    out_t = torch.full((rows * cols,), 0x5A, dtype=torch.uint8, device=dev) if with_t else None
+    inv = torch.zeros(1, device=dev)
+    amax = torch.tensor([amax_given if amax_given is not None else -1.0], device=dev)
+    sk = None if skip is None else torch.tensor([skip], dtype=torch.int32, device=dev)
+    A.fp8_quant_tensorwise(x, fmt, out, out_t, inv, amax, amax_given=amax_given is not None,
+                           skip_if=sk, rows=rows, cols=cols)
+    return (to_host_bits(out), None if out_t is None else to_host_bits(out_t),
+            to_host_bits(inv)[0], to_host_bits(amax)[0])
+
+
+@pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
+@pytest.mark.parametrize("xdt", ["bf16", "f16", "f32"])
+def test_fp8_quant_parity(A, dev, fmt, xdt):
+    rng = np.random.default_rng(30)
+    for rows, cols in FP8_SHAPES:
+        xh = _x_host(rng, rows, cols, xdt)
+        for with_t in (True, False):
+            for misalign in ((False, True) if rows * cols > 8 else (False,)):
+                q, qt, inv, am = _run_quant(A, dev, xh, xdt, rows, cols, fmt, with_t,
+                                            misalign=misalign)
+                rq, rqt, rinv, ram = O.fp8_quant_tensorwise(xh, xdt, rows, cols, fmt,
+                                                            transposed=with_t)
+                key = (rows, cols, with_t, misalign)
+                assert am == np.float32(ram), key
+                assert np.float32(inv).view(np.uint32) == np.float32(rinv).view(np.uint32), key
+                assert np.array_equal(q, rq), key
+                if with_t:
+                    assert np.array_equal(qt, rqt), key
+
+
+@pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
+def test_fp8_quant_degenerate_cases(A, dev, fmt):
+    rng = np.random.default_rng(31)
+    # all-zero tensor: amax clamps to EPS, all bytes zero
+    z = np.zeros(256 * 128, np.uint16)
+    q, qt, inv, am = _run_quant(A, dev, z, "bf16", 256, 128, fmt, True)
+    rq, rqt, rinv, _ = O.fp8_quant_tensorwise(z, "bf16", 256, 128, fmt)
+    assert am == 0.0 and not q.any() and not qt.any() and inv == np.float32(rinv)
+    # given amax (delayed-style): values beyond it saturate; inf saturates
+    xh = _x_host(rng, 128, 256, "f32")
+    xh[5] = np.inf
+    xh[77] = -np.inf
+    for given in (0.5, 3.0, 1e-20):
+        q, qt, inv, _ = _run_quant(A, dev, xh, "f32", 128, 256, fmt, True, amax_given=given)
+        rq, rqt, rinv, _ = O.fp8_quant_tensorwise(xh, "f32", 128, 256, fmt, amax=given)
+        assert np.array_equal(q, rq) and np.array_equal(qt, rqt) and inv == np.float32(rinv)
+    # a NaN input: amax is NaN, every byte is the NaN code
+    xn = _x_host(rng, 128, 128, "bf16")
+    xn[1000] = 0x7FC1
+    q, qt, inv, am = _run_quant(A, dev, xn, "bf16", 128, 128, fmt, True)
+    rq, rqt, rinv, ram = O.fp8_quant_tensorwise(xn, "bf16", 128, 128, fmt)
+    assert np.isnan(am) and np.isnan(ram) and np.isnan(inv) and np.isnan(rinv)
+    assert np.array_equal(q, rq) and np.array_equal(qt, rqt)
+    # amax = inf: finite values go to signed zero, the infinite one to NaN
+    xi = _x_host(rng, 128, 128, "f32")
+    xi[3] = -np.inf
+    q, qt, inv, am = _run_quant(A, dev, xi, "f32", 128, 128, fmt, True)
+    rq, rqt, rinv, ram = O.fp8_quant_tensorwise(xi, "f32", 128, 128, fmt)
+    assert np.isinf(am) and np.array_equal(q, rq) and np.array_equal(qt, rqt)
+    # empty tensor
+    q, qt, inv, am = _run_quant(A, dev, np.zeros(0, np.uint16), "bf16", 0, 7, fmt, True)
+    assert am == 0.0 and inv == np.float32(O.fp8_quant_tensorwise(np.zeros(0, np.uint16), "bf16",
+                                                                  0, 7, fmt)[2])
+    # skip flag set: nothing written
+    q, qt, inv, am = _run_quant(A, dev, xh, "f32", 128, 256, fmt, True, amax_given=1.0, skip=1)
+    assert np.all(q == 0xA5) and np.all(qt == 0x5A) and inv == 0.0
+
+
+@pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
+def test_fp8_cast_rounding_classes(A, dev, fmt):
+    """With amax = fp8_max the scale is exactly 1, so each byte is the
+    saturating RNE cast of the fp32 input itself: every sign / exponent /
+    kept-fraction combination with round and sticky bits clear, set and tied."""
+    hi = np.arange(1 << 20, dtype=np.uint64) << 12
+    lows = np.array([0, 1, 0x7FF, 0x800, 0x801, 0xFFF], np.uint64)
+    x = (hi[:, None] | lows[None, :]).astype(np.uint32).ravel().view(np.float32)
+    cols = 4096
+    rows = x.size // cols
+    x = x[:rows * cols]
+    fmax = O.fmt_max(fmt)
+    q, qt, inv, _ = _run_quant(A, dev, x, "f32", rows, cols, fmt, True, amax_given=fmax)
+    rq, rqt, rinv, _ = O.fp8_quant_tensorwise(x, "f32", rows, cols, fmt, amax=fmax)
+    assert inv == 1.0 == rinv
+    assert np.array_equal(q, rq)
+    assert np.array_equal(qt, rqt)
+
+
+def test_fp8_quant_list_parity(A, dev):
+    rng = np.random.default_rng(32)
+    shapes = [(128, 256), (1024, 512), (127, 129), (384, 128), (64, 4096)]
+    xs_h = [_x_host(rng, r, c, "bf16") for r, c in shapes]
+    X = [to_device(h, "bf16", dev).view(r, c) for h, (r, c) in zip(xs_h, shapes)]
+    Q = [torch.empty((r, c), dtype=torch.float8_e4m3fn, device=dev) for r, c in shapes]
+    QT = [torch.empty((c, r), dtype=torch.float8_e4m3fn, device=dev) for r, c in shapes]
+    LX, LQ, LQT = (A.amp_tensor_list_create(t, two_d=True) for t in (X, Q, QT))
+    amax_h = np.array([np.abs(O.decode("bf16", h)).max() for h in xs_h], np.float32)
+    amax_h[1] *= 0.5     # a given amax below the data: saturation path
+    amax = torch.from_numpy(amax_h).to(dev)
+    inv = torch.zeros(len(shapes), device=dev)
+    for skip in (1, 0):
+        fi = torch.tensor([skip], dtype=torch.int32, device=dev)
+        A.fp8_quant_tensorwise_list(LX, LQ, LQT, "e4m3fn", amax, inv, skip_if=fi)
+        if skip:
+            assert not inv.any()
+    for i, (r, c) in enumerate(shapes):
+        rq, rqt, rinv, _ = O.fp8_quant_tensorwise(xs_h[i], "bf16", r, c, "e4m3fn",
+                                                  amax=float(amax_h[i]))
+        assert np.array_equal(to_host_bits(Q[i].view(torch.uint8)).ravel(), rq), i
+        assert np.array_equal(to_host_bits(QT[i].view(torch.uint8)).ravel(), rqt), i
+        assert to_host_bits(inv)[i] == np.float32(rinv)
+    for L in (LX, LQ, LQT):
+        L.close()
+
+
+# ------------------------------------------------------------ composition
+def test_amp_step_composition_with_fp8(A, dev):
+    """The four calls of a step, with FP8 weights and an inf at step 3,
+    against the oracle's step in the pages' order."""
+    from loss_scaling_master_gb300 import AmpOptimizerStep
+    rng = np.random.default_rng(40)
+    shapes = [(96, 256), (300,), (128, 136), (1000,), (256, 512)]
+    fp8_shapes = [s if len(s) == 2 else None for s in shapes]
+    sizes = [int(np.prod(s)) for s in shapes]
+    master = [(rng.standard_normal(n) * 0.02).astype(np.float32) for n in sizes]
+    G = [torch.empty(n, dtype=torch.float16, device=dev) for n in sizes]
+    hyper = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+    st = AmpOptimizerStep([torch.from_numpy(m.copy()).to(dev) for m in master], G,
+                          init_scale=65536.0, growth_interval=2, fp8_shapes=fp8_shapes, **hyper)
+    orc = O.AmpStepOracle(master, "f16", hyper["lr"], hyper["beta1"], hyper["beta2"],
+                          hyper["eps"], hyper["weight_decay"], 65536.0, 2.0, 0.5, 2,
+                          fp8_shapes=fp8_shapes)
+    for k in range(1, 8):
+        gh = [(rng.standard_normal(n) * 1e-4 * orc.scale).astype(np.float16).view(np.uint16)
+              for n in sizes]
+        if k == 3:
+            gh[2][135] = 0x7C00
+        for t, h in zip(G, gh):
+            t.copy_(to_device(h, "f16", dev))
+        st.step()
+        orc.run(gh)
+        s = st.state()
+        assert (s["scale"], s["growth_tracker"], s["step"], s["found_inf"]) == \
+            (orc.scale, orc.tracker, orc.step, 0), k
+    for i in range(len(shapes)):
+        assert np.array_equal(to_host_bits(st.master[i]).view(np.uint32),
+                              orc.master[i].view(np.uint32))
+        assert np.array_equal(to_host_bits(st.bf16[i]), orc.bf16[i])
+    j = 0
+    for i, sh in enumerate(fp8_shapes):
+        if sh is None:
+            continue
+        assert np.array_equal(to_host_bits(st.fp8[j].view(torch.uint8)).ravel(), orc.fp8[i])
+        assert np.array_equal(to_host_bits(st.fp8_t[j].view(torch.uint8)).ravel(), orc.fp8_t[i])
+        assert to_host_bits(st.inv_scale)[j] == orc.inv_scale[orc.slots[i]]
+        j += 1
+    st.close()
