@@ -32,6 +32,24 @@ BF16_FALLBACK_TFLOPS = 1900.0
 L2_BYTES = 129 * 2 ** 20
 
 
+def profiled_traffic(kernel: str, units: int):
+    """DRAM bytes per launch of `kernel` from its committed ncu capture, scaled
+    by units processed; None when the kernel source changed since the capture."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)[kernel]
+        m = hashlib.sha256()
+        for src in rec["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                m.update(f.read())
+        if m.hexdigest() != rec["source_sha256"]:
+            return None
+        return rec["dram_bytes_per_param"] * units
+    except Exception:
+        return None
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -102,12 +120,19 @@ def build_step(workload: str, device, seed: int):
     cfg = amp_config(workload)
     gdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[cfg.grad_dtype]
     gen = device_generator(device, seed, 1)
-    master = [device_fill_normal(torch.empty(s.numel, device=device), cfg.master_sigma, gen)
-              for s in cfg.specs]
+    # flat master and gradient buffers with one view per tensor, as sharded
+    # data-parallel optimizers keep them (every offset is a multiple of 8
+    # elements, so every view stays 16-byte aligned)
+    n_all = sum(s.numel for s in cfg.specs)
+    master_flat = torch.empty(n_all, device=device)
+    grads_flat = torch.empty(n_all, dtype=gdt, device=device)
+    master, grads, off = [], [], 0
     sig = tensor_sigmas(cfg, seed)
-    grads = [device_fill_normal(torch.empty(s.numel, dtype=gdt, device=device),
-                                float(sig[i] * cfg.init_scale), gen)
-             for i, s in enumerate(cfg.specs)]
+    for i, s in enumerate(cfg.specs):
+        master.append(device_fill_normal(master_flat[off:off + s.numel], cfg.master_sigma, gen))
+        grads.append(device_fill_normal(grads_flat[off:off + s.numel],
+                                        float(sig[i] * cfg.init_scale), gen))
+        off += s.numel
     fp8_shapes = [(s.rows, s.cols) if s.fp8 else None for s in cfg.specs] \
         if cfg.fp8_weights else None
     step = AmpOptimizerStep(master, grads, lr=cfg.lr, beta1=cfg.beta1, beta2=cfg.beta2,
@@ -123,7 +148,7 @@ def build_step(workload: str, device, seed: int):
             "bytes_check": gbytes * n,
             "bytes_adamw": (gbytes + 12) * n + 12 * n + 2 * n,
             "bytes_quant": 4 * n8,
-            "grad_bytes": gbytes * n}
+            "grad_bytes": gbytes * n, "grads_flat": grads_flat}
     return step, info
 
 
@@ -238,7 +263,9 @@ def run_ours(args, rank, world, device):
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "bytes_per_param": info["bytes_adamw"] / n_params,
-                     "traffic": None},
+                     "traffic": profiled_traffic("adamw_main_kernel", n_params),
+                     "traffic_note": "ncu dram read+write of a 124M-param launch scaled by "
+                                     "params (profiles/adamw_main_gpt2_small.md)"},
         "clocks": clk.summary(),
         "gpu_launches": args.steps * step.launches_per_step,
     }
@@ -257,23 +284,16 @@ def run_e2e(args, step, info, stream, world):
     import torch.distributed as dist
 
     nbytes = info["grad_bytes"]
-    host = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
-    dev_views, off = [], 0
-    for g in step.grads:
-        b = g.numel() * g.element_size()
-        dev_views.append((g.view(torch.uint8).view(-1), host[off:off + b]))
-        off += b
+    dev_flat = info["grads_flat"]
+    host = torch.empty(dev_flat.shape, dtype=dev_flat.dtype, pin_memory=True)
     state_host = torch.empty(4, dtype=torch.int32, pin_memory=True)
-    # keep the gradients finite: copy the device grads to the host once
-    for d, h in dev_views:
-        h.copy_(d)
+    host.copy_(dev_flat)     # finite gradients of the workload's recipe
     torch.cuda.synchronize()
     packed = torch.empty(4, dtype=torch.int32, device=step.scale.device)
 
     def e2e_step():
         with torch.cuda.stream(stream):
-            for d, h in dev_views:
-                d.copy_(h, non_blocking=True)
+            dev_flat.copy_(host, non_blocking=True)
         step.step(stream=stream)
         with torch.cuda.stream(stream):
             packed[0:1].copy_(step.scale.view(torch.int32))
