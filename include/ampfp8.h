@@ -168,6 +168,32 @@ amp_status amp_adamw_master_step(amp_tensor_list master, amp_tensor_list exp_avg
                                  const amp_adamw_hyper *hyper, float *amax_dev,
                                  amp_stream_t stream);
 
+/* Allocation-free form of amp_adamw_master_step.  The pages have no
+ * counterpart: it exists for callers that cannot allocate device memory -
+ * runtimes that serve all device memory from their own arena, loops that must
+ * not take the device-wide synchronisation of cudaMalloc/cudaFree, processes
+ * running with the GPU nearly full, and plain-C callers that cannot keep a
+ * list handle alive.  The same arithmetic and kernels as
+ * amp_adamw_master_step; the tensors come as host arrays of n device
+ * pointers (bf16_out and amax_slots may be NULL) plus numel[n], and the
+ * tables the kernels walk are copied on `stream` into one fixed device array
+ * of about 4.1 MB built into the library (held on every GPU that loads it
+ * until exit).  Limits: n <= 1024 tensors and at most 524,288 chunks of 16384
+ * elements in total; larger calls return AMP_EINVAL with a message.
+ *   - No cudaMalloc/cudaFree or other allocating routine is called.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call shares the array: calls whose work can overlap on the GPU
+ *     (unordered streams) race; order them on one stream. */
+amp_status amp_adamw_master_step_noalloc(int n, float *const *master, float *const *exp_avg,
+                                         float *const *exp_avg_sq, const void *const *grads,
+                                         amp_dtype grad_dtype, uint16_t *const *bf16_out,
+                                         const int64_t *numel, const int32_t *amax_slots,
+                                         const float *scale_dev, const int32_t *found_inf_dev,
+                                         int32_t *step_dev, const amp_adamw_hyper *hyper,
+                                         float *amax_dev, amp_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* A6-A9: tensorwise dynamic FP8 quantization.  [FP8] §2 (quant math), §3     */
 /* (e4m3fn for weights/activations, e5m2 for gradients), §4 (column-major     */

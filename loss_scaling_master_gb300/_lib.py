@@ -25,8 +25,9 @@ _TORCH_DT = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16",
 
 # every symbol include/ampfp8.h declares
 EXPORTS = ("amp_tensor_list_create", "amp_tensor_list_set_amax_slots", "amp_tensor_list_destroy",
-           "amp_unscale_check", "amp_adamw_master_step", "fp8_quant_tensorwise",
-           "fp8_quant_tensorwise_list", "amp_update_scale", "amp_last_error", "amp_abi_version")
+           "amp_unscale_check", "amp_adamw_master_step", "amp_adamw_master_step_noalloc",
+           "fp8_quant_tensorwise", "fp8_quant_tensorwise_list", "amp_update_scale",
+           "amp_last_error", "amp_abi_version")
 
 
 class AmpError(RuntimeError):
@@ -62,6 +63,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.amp_unscale_check.argtypes = [P, P, P, i32, P]
         L.amp_adamw_master_step.argtypes = [P, P, P, P, P, P, P, P,
                                             ctypes.POINTER(amp_adamw_hyper), P, P]
+        L.amp_adamw_master_step_noalloc.argtypes = [i32, P, P, P, P, i32, P, P, P, P, P, P,
+                                                    ctypes.POINTER(amp_adamw_hyper), P, P]
         L.fp8_quant_tensorwise.argtypes = [P, i32, i64, i64, i32, dbl, P, P, P, P, i32, P, P]
         L.fp8_quant_tensorwise_list.argtypes = [P, P, P, i32, dbl, P, P, P, P]
         L.amp_update_scale.argtypes = [P, P, P, flt, flt, ctypes.c_int32, P, i32, P]
@@ -170,6 +173,25 @@ def amp_adamw_master_step(master: TensorList, exp_avg: TensorList, exp_avg_sq: T
                                         grads.handle, bf16_out.handle if bf16_out else None,
                                         _dptr(scale), _dptr(found_inf), _dptr(step),
                                         ctypes.byref(h), _dptr(amax), _stream(stream)))
+
+
+def amp_adamw_master_step_noalloc(master, exp_avg, exp_avg_sq, grads, bf16_out, scale,
+                                  found_inf, step, lr: float, beta1: float, beta2: float,
+                                  eps: float, weight_decay: float, amax_slots=None, amax=None,
+                                  stream=None):
+    """Allocation-free AdamW step over plain lists of contiguous device tensors
+    (no list handles); see include/ampfp8.h for its limits."""
+    n = len(master)
+    arr = lambda ts: (P * max(n, 1))(*[t.data_ptr() for t in ts])
+    numel = (ctypes.c_int64 * max(n, 1))(*[t.numel() for t in master])
+    slots = None if amax_slots is None else (ctypes.c_int32 * max(n, 1))(*amax_slots)
+    h = amp_adamw_hyper(lr, beta1, beta2, eps, weight_decay)
+    _check("amp_adamw_master_step_noalloc",
+           load().amp_adamw_master_step_noalloc(
+               n, arr(master), arr(exp_avg), arr(exp_avg_sq), arr(grads),
+               DT[dtype_name(grads[0])] if n else DT["f32"],
+               arr(bf16_out) if bf16_out is not None else None, numel, slots, _dptr(scale),
+               _dptr(found_inf), _dptr(step), ctypes.byref(h), _dptr(amax), _stream(stream)))
 
 
 def fp8_quant_tensorwise(x: torch.Tensor, fp8_dtype: str, out: torch.Tensor, out_t, inv_scale,

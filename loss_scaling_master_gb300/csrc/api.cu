@@ -59,6 +59,8 @@ bool same_shapes(const amp_tensor_list_s *a, const amp_tensor_list_s *b) {
 }  // namespace
 
 namespace amp {
+void set_last_error(const char *msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
+
 int sm_count(int device) {
     static std::mutex mu;
     static std::vector<int> cache;

@@ -43,6 +43,9 @@ struct AdamwStepScalars {
 
 int sm_count(int device);
 
+// Set the calling thread's amp_last_error() message.
+void set_last_error(const char *msg);
+
 cudaError_t launch_unscale_check(const ListView &g, int64_t n_chunks, int elem, const float *scale,
                                  int32_t *found_inf, int inplace, cudaStream_t s);
 
