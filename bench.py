@@ -166,8 +166,10 @@ def run_ours(args, rank, world, device):
     stream = torch.cuda.Stream(device=device)
     comb = None
     if world > 1:
+        from loss_scaling_master_gb300.sharded import combine_found_inf
+
         def comb():
-            dist.all_reduce(step.found_inf, op=dist.ReduceOp.MAX)
+            combine_found_inf(step.found_inf)
 
     def one_step(ev=None):
         if ev is not None:
@@ -195,15 +197,16 @@ def run_ours(args, rank, world, device):
         if ev is not None:
             ev[4].record(stream)
 
-    for _ in range(args.warmup):
-        one_step()
-    torch.cuda.synchronize()
-    st0 = step.state()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
+    st0 = step.state()
+    # the clock sampler starts first, so the timed steps follow the warm-up
+    # steps without an idle gap
     with ClockSampler(torch.cuda.current_device()) as clk:
+        for _ in range(args.warmup):
+            one_step()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
         t_begin = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_begin.record(stream)
@@ -215,7 +218,7 @@ def run_ours(args, rank, world, device):
             dist.barrier()
     ms_total = t_begin.elapsed_time(t_end)
     st1 = step.state()
-    assert st1["step"] - st0["step"] == args.steps, "a timed step was skipped"
+    assert st1["step"] - st0["step"] == args.steps + args.warmup, "a step was skipped"
     k_check = [e[0].elapsed_time(e[1]) for e in evs]
     k_adamw = [e[1].elapsed_time(e[2]) for e in evs]
     k_quant = [e[2].elapsed_time(e[3]) for e in evs]
@@ -278,23 +281,45 @@ def run_ours(args, rank, world, device):
 
 
 def run_e2e(args, step, info, stream, world):
-    """Same step through the public API, with each step's gradients copied
-    from pinned host memory and the scaler state read back, both timed."""
+    """The same step through the public API (AmpOptimizerStep.step), with
+    every step's gradients copied from pinned host memory and the scaler state
+    read back, all inside the timed region.  Two device gradient buffers let
+    the copy of step k+1 (on its own stream, in 1 GiB pieces) overlap the
+    update of step k."""
     import torch
     import torch.distributed as dist
 
     nbytes = info["grad_bytes"]
-    dev_flat = info["grads_flat"]
-    host = torch.empty(dev_flat.shape, dtype=dev_flat.dtype, pin_memory=True)
+    bufs = [info["grads_flat"], torch.empty_like(info["grads_flat"])]
+    views, off = [], 0
+    for g in step.grads:
+        views.append(bufs[1][off:off + g.numel()])
+        off += g.numel()
+    b1 = step.add_grad_buffer(views)
+    from loss_scaling_master_gb300.hostmem import pinned_empty
+    hbuf = pinned_empty(bufs[0].numel(), bufs[0].dtype)
+    host = hbuf.tensor
+    host.copy_(bufs[0])      # finite gradients of the workload's recipe
     state_host = torch.empty(4, dtype=torch.int32, pin_memory=True)
-    host.copy_(dev_flat)     # finite gradients of the workload's recipe
-    torch.cuda.synchronize()
     packed = torch.empty(4, dtype=torch.int32, device=step.scale.device)
+    copy_stream = torch.cuda.Stream(device=step.scale.device)
+    ready = [torch.cuda.Event(), torch.cuda.Event()]
+    free = [torch.cuda.Event(), torch.cuda.Event()]
+    for e in free:
+        e.record(stream)
+    piece = (1 << 30) // host.element_size()
+    torch.cuda.synchronize()
 
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            dev_flat.copy_(host, non_blocking=True)
-        step.step(stream=stream)
+    def e2e_step(k):
+        b = k % 2
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(free[b])
+            for o in range(0, host.numel(), piece):
+                bufs[b][o:o + piece].copy_(host[o:o + piece], non_blocking=True)
+            ready[b].record(copy_stream)
+        stream.wait_event(ready[b])
+        step.step(stream=stream, grad_buffer=(0 if b == 0 else b1))
+        free[b].record(stream)
         with torch.cuda.stream(stream):
             packed[0:1].copy_(step.scale.view(torch.int32))
             packed[1:2].copy_(step.growth_tracker)
@@ -302,25 +327,29 @@ def run_e2e(args, step, info, stream, world):
             packed[3:4].copy_(step.found_inf)
             state_host.copy_(packed, non_blocking=True)
 
-    for _ in range(max(1, args.warmup // 2)):
-        e2e_step()
+    for k in range(max(2, args.warmup // 2)):
+        e2e_step(k)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    copy_stream.wait_event(t0)
+    for k in range(args.steps):
+        e2e_step(k)
     t1.record(stream)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
-    del host
+    del host, bufs
+    hbuf.close()
     return {"value": info["params"] * args.steps * world / (ms * 1e-3), "unit": "params/s",
             "ms_per_step": ms / args.steps, "h2d_bytes_per_step": nbytes,
             "d2h_bytes_per_step": 16,
-            "api": "AmpOptimizerStep.step() (C-ABI calls) + pinned H2D of the grads + D2H of "
-                   "{scale, tracker, step, found_inf}"}
+            "api": "AmpOptimizerStep.step() (C-ABI calls), pinned (huge-page, cudaHostRegister) "
+                   "H2D of each step's grads (1 GiB pieces on a copy stream, double-buffered) + "
+                   "D2H of {scale, tracker, step, found_inf}",
+            "host_huge_pages": hbuf.huge_pages}
 
 
 def run_fp8_sweep(args, rank, world, device):

@@ -47,6 +47,8 @@ class AmpOptimizerStep:
         mk = lambda ts, two_d=False: A.amp_tensor_list_create(ts, two_d=two_d, stream=stream)
         self.L_master, self.L_m, self.L_v = mk(self.master), mk(self.exp_avg), mk(self.exp_avg_sq)
         self.L_g = mk(self.grads)
+        self.grad_lists = [self.L_g]
+        self.graphs = {}
         self.L_b = mk(self.bf16) if emit_bf16 else None
         self.n_fp8 = 0
         self.fp8, self.fp8_t = [], []
@@ -75,10 +77,45 @@ class AmpOptimizerStep:
         """Kernels one step enqueues (check, AdamW prologue + main, [quant], update)."""
         return 4 + (1 if self.n_fp8 else 0)
 
-    def step(self, stream=None):
-        s = stream if stream is not None else self.stream
-        A.amp_unscale_check(self.L_g, self.scale, self.found_inf, stream=s)
-        A.amp_adamw_master_step(self.L_master, self.L_m, self.L_v, self.L_g, self.L_b, self.scale,
+    def add_grad_buffer(self, grads) -> int:
+        """Register another set of gradient buffers (same shapes and dtype) and
+        return its index for step(grad_buffer=...): with two buffers the host
+        can fill one while the GPU steps on the other."""
+        grads = list(grads)
+        if [g.numel() for g in grads] != [g.numel() for g in self.grads] or \
+                any(a.dtype != b.dtype for a, b in zip(grads, self.grads)):
+            raise ValueError("gradient buffers must match the first set in sizes and dtype")
+        self.grad_lists.append(A.amp_tensor_list_create(grads, stream=self.stream))
+        return len(self.grad_lists) - 1
+
+    def capture_graph(self, stream=None, grad_buffer: int = 0):
+        """Record one step into a CUDA graph; later step() calls on the same
+        gradient buffer replay it.  Every call of the step is stream-ordered
+        and allocation-free, so the graph is the same calls with the same
+        device pointers; the caller keeps writing each step's gradients into
+        the same buffers."""
+        s = stream if stream is not None else (self.stream or torch.cuda.Stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            self._enqueue(None, grad_buffer)
+        self.graphs[grad_buffer] = g
+        return g
+
+    def step(self, stream=None, grad_buffer: int = 0):
+        g = self.graphs.get(grad_buffer)
+        if g is not None:
+            if stream is not None:
+                with torch.cuda.stream(stream):
+                    g.replay()
+            else:
+                g.replay()
+            return
+        self._enqueue(stream if stream is not None else self.stream, grad_buffer)
+
+    def _enqueue(self, s, grad_buffer: int = 0):
+        L_g = self.grad_lists[grad_buffer]
+        A.amp_unscale_check(L_g, self.scale, self.found_inf, stream=s)
+        A.amp_adamw_master_step(self.L_master, self.L_m, self.L_v, L_g, self.L_b, self.scale,
                                 self.found_inf, self.step_count, *self.hyper,
                                 amax=self.amax if self.n_fp8 else None, stream=s)
         if self.n_fp8:
@@ -95,7 +132,9 @@ class AmpOptimizerStep:
                 "step": int(self.step_count.item()), "found_inf": int(self.found_inf.item())}
 
     def close(self):
-        for name in ("L_master", "L_m", "L_v", "L_g", "L_b", "L_x8", "L_q", "L_qt"):
+        for name in ("L_master", "L_m", "L_v", "L_b", "L_x8", "L_q", "L_qt"):
             lst = getattr(self, name, None)
             if lst is not None:
                 lst.close()
+        for lst in self.grad_lists:
+            lst.close()

@@ -1,0 +1,198 @@
+"""Parity at the workloads' full sizes, in the launch configuration bench.py
+times (AmpOptimizerStep over the whole parameter set).
+
+* GPT-2-small set (124,356,864 params, bf16 grads, S = 1): every element,
+  all 10 steps.
+* 1B Llama set (1,235,814,400 params, fp16 grads, dynamic S, inf/-inf/NaN at
+  steps 7/27/47): the scaler trace every step, and master/m/v/bf16 on sampled
+  elements (each tensor's ends, chunk boundaries, random positions and the
+  planted non-finite sites), which the oracle computes one by one - the update
+  is element-wise once found_inf is known.
+* FP8 sweep (bf16 [4096,4096], [8192,8192], [16384,5120] and an all-zero
+  [4096,4096], e4m3fn and e5m2): every byte of both layouts.
+* 8B Llama-3 set, the bench's own state (flat buffers, FP8 weights): 3 steps;
+  two FP8 weights and a norm vector in full through the oracle (bf16, amax,
+  inv_scale, row-major and transposed bytes), sampled elements elsewhere.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from parity_helpers import (assert_bf16_close, assert_state_close, bit_identical_fraction,
+                            to_device, to_host_bits)
+from workloads import (FP8_SWEEP_SHAPES, FP8_SWEEP_ZERO_SHAPE, amp_config, device_fill_normal,
+                       device_generator, fp8_sweep_host, host_grads, host_master, injection_site,
+                       tensor_sigmas)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def A():
+    from loss_scaling_master_gb300 import build as B
+    B.build()
+    import loss_scaling_master_gb300 as pkg
+    pkg.load()
+    assert torch.cuda.is_available()
+    return pkg
+
+
+def _step_obj(A, cfg, master_dev, grads_dev, fp8_shapes=None):
+    return A.AmpOptimizerStep(master_dev, grads_dev, lr=cfg.lr, beta1=cfg.beta1, beta2=cfg.beta2,
+                              eps=cfg.eps, weight_decay=cfg.weight_decay,
+                              init_scale=cfg.init_scale, growth_factor=cfg.growth_factor,
+                              backoff_factor=cfg.backoff_factor,
+                              growth_interval=cfg.growth_interval, fp8_shapes=fp8_shapes)
+
+
+def _oracle(cfg, master_host, fp8_shapes=None):
+    return O.AmpStepOracle(master_host, cfg.grad_dtype, cfg.lr, cfg.beta1, cfg.beta2, cfg.eps,
+                           cfg.weight_decay, cfg.init_scale, cfg.growth_factor,
+                           cfg.backoff_factor, cfg.growth_interval, fp8_shapes=fp8_shapes)
+
+
+def test_gpt2_small_full_parity(A):
+    dev = torch.device("cuda:0")
+    cfg = amp_config("gpt2_small")
+    mh = host_master(cfg)
+    st = _step_obj(A, cfg, [torch.from_numpy(m).to(dev) for m in mh],
+                   [torch.empty(s.numel, dtype=torch.bfloat16, device=dev) for s in cfg.specs])
+    orc = _oracle(cfg, mh)
+    for k in range(1, cfg.steps + 1):
+        gh = host_grads(cfg, k, orc.scale)
+        for t, h in zip(st.grads, gh):
+            t.copy_(to_device(h, "bf16", dev))
+        st.step()
+        orc.run(gh)
+        s = st.state()
+        assert (s["scale"], s["growth_tracker"], s["step"]) == (orc.scale, orc.tracker, orc.step)
+    ident = []
+    for i in range(len(cfg.specs)):
+        for got, ref, nm in ((st.master[i], orc.master[i], "master"),
+                             (st.exp_avg[i], orc.exp_avg[i], "exp_avg"),
+                             (st.exp_avg_sq[i], orc.exp_avg_sq[i], "exp_avg_sq")):
+            g = to_host_bits(got)
+            assert_state_close(g, ref, f"{nm}[{cfg.specs[i].name}]")
+            ident.append(bit_identical_fraction(g, ref))
+        assert_bf16_close(to_host_bits(st.bf16[i]), orc.bf16[i], f"bf16[{cfg.specs[i].name}]")
+    assert min(ident) == 1.0
+    st.close()
+
+
+def _sample_indices(n, rng, k=48):
+    idx = {0, n - 1, n // 2}
+    for b in range(16384, n, 16384 * 97):
+        idx.update((b - 1, b))
+    idx.update(rng.integers(0, n, size=min(k, n)).tolist())
+    return np.array(sorted(i for i in idx if 0 <= i < n), np.int64)
+
+
+def test_llama_1b_sampled_parity(A):
+    dev = torch.device("cuda:0")
+    cfg = amp_config("llama_1b")
+    sig = tensor_sigmas(cfg, 0)
+    gen = device_generator(dev, 0, 3)
+    master = [device_fill_normal(torch.empty(s.numel, device=dev), cfg.master_sigma, gen)
+              for s in cfg.specs]
+    grads = [torch.empty(s.numel, dtype=torch.float16, device=dev) for s in cfg.specs]
+    rng = np.random.default_rng(77)
+    sites = {k: injection_site(cfg, k, 0) for k in cfg.inject}
+    samples = []
+    for i, s in enumerate(cfg.specs):
+        ix = set(_sample_indices(s.numel, rng).tolist())
+        ix.update(e for (t, e, _) in sites.values() if t == i)
+        samples.append(torch.tensor(sorted(ix), dtype=torch.int64, device=dev))
+    take = lambda ts: [to_host_bits(t.index_select(0, ix)) for t, ix in zip(ts, samples)]
+    orc = _oracle(cfg, take(master))
+    st = _step_obj(A, cfg, master, grads)
+    gen_g = device_generator(dev, 0, 4)
+    for k in range(1, cfg.steps + 1):
+        for i, g in enumerate(grads):
+            device_fill_normal(g, float(sig[i] * orc.scale), gen_g)
+        if k in sites:
+            t, e, val = sites[k]
+            grads[t][e] = val
+        gh = take(grads)
+        st.step()
+        fi = orc.run(gh)
+        assert fi == int(k in sites)
+        s = st.state()
+        assert (s["scale"], s["growth_tracker"], s["step"]) == (orc.scale, orc.tracker, orc.step), k
+    assert orc.step == cfg.steps - len(sites)
+    for nm, got, ref in (("master", st.master, orc.master), ("exp_avg", st.exp_avg, orc.exp_avg),
+                         ("exp_avg_sq", st.exp_avg_sq, orc.exp_avg_sq)):
+        for i, g in enumerate(take(got)):
+            assert_state_close(g, ref[i], f"{nm}[{cfg.specs[i].name}]")
+            assert bit_identical_fraction(g, ref[i]) == 1.0
+    for i, b in enumerate(take(st.bf16)):
+        assert_bf16_close(b, orc.bf16[i], f"bf16[{cfg.specs[i].name}]")
+    st.close()
+
+
+@pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
+def test_fp8_sweep_full_parity(A, fmt):
+    dev = torch.device("cuda:0")
+    shapes = FP8_SWEEP_SHAPES + [FP8_SWEEP_ZERO_SHAPE]
+    for j, (r, c) in enumerate(shapes):
+        xh = fp8_sweep_host(r, c, seed=0, zero=(j == len(FP8_SWEEP_SHAPES)))
+        x = to_device(xh, "bf16", dev).view(r, c)
+        out = torch.empty((r, c), dtype=torch.uint8, device=dev)
+        out_t = torch.empty((c, r), dtype=torch.uint8, device=dev)
+        inv = torch.zeros(1, device=dev)
+        amax = torch.zeros(1, device=dev)
+        A.fp8_quant_tensorwise(x, fmt, out, out_t, inv, amax)
+        rq, rqt, rinv, ramax = O.fp8_quant_tensorwise(xh, "bf16", r, c, fmt)
+        assert to_host_bits(amax)[0] == np.float32(ramax)
+        assert to_host_bits(inv)[0] == np.float32(rinv)
+        assert np.array_equal(to_host_bits(out).ravel(), rq), (r, c)
+        assert np.array_equal(to_host_bits(out_t).ravel(), rqt), (r, c)
+        del x, out, out_t
+
+
+def test_llama3_8b_bench_state_parity(A):
+    import bench
+    dev = torch.device("cuda:0")
+    st, info = bench.build_step("llama3_8b", dev, seed=1234)
+    cfg = info["cfg"]
+    names = [s.name for s in cfg.specs]
+    full = [names.index(n) for n in ("l0.k", "l31.gate", "l5.ffn_norm")]
+    rng = np.random.default_rng(88)
+    samples = {i: torch.tensor(_sample_indices(s.numel, rng), dtype=torch.int64, device=dev)
+               for i, s in enumerate(cfg.specs) if i not in full}
+    order = full + sorted(samples)
+    init = [to_host_bits(st.master[i]) if i in full
+            else to_host_bits(st.master[i].index_select(0, samples[i])) for i in order]
+    gh = [to_host_bits(st.grads[i]) if i in full
+          else to_host_bits(st.grads[i].index_select(0, samples[i])) for i in order]
+    fp8_shapes = [(cfg.specs[i].rows, cfg.specs[i].cols) if (i in full and cfg.specs[i].fp8)
+                  else None for i in order]
+    orc = _oracle(cfg, init, fp8_shapes=fp8_shapes)
+    for k in range(3):
+        st.step()
+        assert orc.run(gh) == 0
+        s = st.state()
+        assert (s["scale"], s["growth_tracker"], s["step"]) == (orc.scale, orc.tracker, orc.step)
+    fp8_index = {}
+    j = 0
+    for i, s in enumerate(cfg.specs):
+        if s.fp8:
+            fp8_index[i] = j
+            j += 1
+    for pos, i in enumerate(order):
+        sel = (lambda t: to_host_bits(t)) if i in full else \
+            (lambda t, ix=samples[i]: to_host_bits(t.index_select(0, ix)))
+        for nm, got, ref in (("master", st.master[i], orc.master[pos]),
+                             ("exp_avg", st.exp_avg[i], orc.exp_avg[pos]),
+                             ("exp_avg_sq", st.exp_avg_sq[i], orc.exp_avg_sq[pos])):
+            g = sel(got)
+            assert_state_close(g, ref, f"{nm}[{names[i]}]")
+            assert bit_identical_fraction(g, ref) == 1.0
+        assert_bf16_close(sel(st.bf16[i]), orc.bf16[pos], f"bf16[{names[i]}]")
+        if fp8_shapes[pos] is not None:
+            q = st.fp8[fp8_index[i]].view(torch.uint8)
+            qt = st.fp8_t[fp8_index[i]].view(torch.uint8)
+            assert np.array_equal(to_host_bits(q).ravel(), orc.fp8[pos]), names[i]
+            assert np.array_equal(to_host_bits(qt).ravel(), orc.fp8_t[pos]), names[i]
+            assert to_host_bits(st.inv_scale)[fp8_index[i]] == orc.inv_scale[orc.slots[pos]]
+    st.close()
