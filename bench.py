@@ -50,6 +50,20 @@ def profiled_traffic(kernel: str, units: int):
         return None
 
 
+METRIC = ("fused AMP step params/s (unscale/check + FP32-master AdamW + bf16 emit "
+          "+ tensorwise FP8 e4m3fn with transposed copy)")
+
+
+def workload_config(workload: str, world: int) -> dict:
+    from workloads import amp_config
+    cfg = amp_config(workload)
+    n = sum(s.numel for s in cfg.specs)
+    n8 = sum(s.numel for s in cfg.specs if s.fp8) if cfg.fp8_weights else 0
+    return {"workload": f"{workload}: {n:,} params in {len(cfg.specs)} tensors, {n8:,} FP8-emitted",
+            "grad_dtype": cfg.grad_dtype, "parallelism": f"dp{world} (sharded, weak)",
+            "l2": "inputs larger than L2 (no flush needed)"}
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -240,8 +254,7 @@ def run_ours(args, rank, world, device):
     achieved = info["bytes_adamw"] / (adamw_ms * 1e-3) / 1e9
     total_bytes = info["bytes_check"] + info["bytes_adamw"] + info["bytes_quant"]
     line = {
-        "metric": "fused AMP step params/s (unscale/check + FP32-master AdamW + bf16 emit "
-                  "+ tensorwise FP8 e4m3fn with transposed copy)",
+        "metric": METRIC,
         "value": n_params * args.steps * world / (ms_total * 1e-3),
         "unit": "params/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -251,11 +264,7 @@ def run_ours(args, rank, world, device):
         "vs_baseline": None,
         "dtype": "f32 (master/m/v), f16 grads, bf16 + e4m3fn outputs",
         "data": "synthetic (seeded N(0,0.02) masters, N(0,sigma*S) fp16 grads; no trained weights)",
-        "config": {"workload": f"{args.workload}: {info['params']:,} params in {info['tensors']} "
-                               f"tensors, {info['fp8_params']:,} FP8-emitted",
-                   "grad_dtype": info["cfg"].grad_dtype, "parallelism": f"dp{world} (sharded, weak)",
-                   "l2": "inputs larger than L2 (no flush needed)",
-                   "per_step_bytes": total_bytes},
+        "config": dict(workload_config(args.workload, world), per_step_bytes=total_bytes),
         "hbm_gbs_step": total_bytes / (ms_step * 1e-3) / 1e9,
         "kernels_ms": {"unscale_check": statistics.mean(k_check),
                        "adamw_master_step": adamw_ms,
@@ -417,31 +426,36 @@ def run_fp8_sweep(args, rank, world, device):
 
 
 # ------------------------------------------------------------ CPU baseline
-def cpu_baseline(workload: str, seconds: float):
-    """The CPU oracle as it stands, single-threaded, on a bounded sample of
-    the workload: layer 0 of the parameter set (all of its tensors, FP8
-    copies included), timed for whole steps until ~`seconds` have passed."""
+def _oracle_sample(workload: str, names):
+    """Oracle state for a named subset of the workload's tensors."""
     import numpy as np
 
     import oracle as O
-    from workloads import AmpConfig, amp_config
+    from workloads import amp_config
 
     cfg = amp_config(workload if workload != "fp8_sweep" else "llama3_8b")
-    specs = [s for s in cfg.specs if s.name.startswith(("l0.", "h0."))] or cfg.specs[:3]
-    sub = AmpConfig(cfg.name + "-layer0", specs, cfg.grad_dtype, cfg.steps, cfg.lr, cfg.beta1,
-                    cfg.beta2, cfg.eps, cfg.weight_decay, cfg.init_scale, cfg.growth_factor,
-                    cfg.backoff_factor, cfg.growth_interval, cfg.grad_sigma,
-                    fp8_weights=cfg.fp8_weights)
+    specs = [s for s in cfg.specs if names(s.name)] or cfg.specs[:3]
     rng = np.random.default_rng(5)
     master = [(rng.standard_normal(s.numel, dtype=np.float32) * np.float32(0.02)) for s in specs]
     sig = 1e-4 if isinstance(cfg.grad_sigma, str) else float(cfg.grad_sigma)
     grads = [(rng.standard_normal(s.numel, dtype=np.float32) * np.float32(sig * cfg.init_scale))
              .astype(np.float16).view(np.uint16) for s in specs]
+    if cfg.grad_dtype == "bf16":
+        grads = [O.encode("bf16", O.decode("f16", g)) for g in grads]
     fp8_shapes = [(s.rows, s.cols) if s.fp8 else None for s in specs] if cfg.fp8_weights else None
-    orc = O.AmpStepOracle(master, "f16", cfg.lr, cfg.beta1, cfg.beta2, cfg.eps, cfg.weight_decay,
-                          cfg.init_scale, cfg.growth_factor, cfg.backoff_factor,
+    orc = O.AmpStepOracle(master, cfg.grad_dtype, cfg.lr, cfg.beta1, cfg.beta2, cfg.eps,
+                          cfg.weight_decay, cfg.init_scale, cfg.growth_factor, cfg.backoff_factor,
                           cfg.growth_interval, fp8_shapes=fp8_shapes)
     n = sum(s.numel for s in specs)
+    n8 = sum(s.numel for s in specs if s.fp8) if cfg.fp8_weights else 0
+    return cfg, specs, orc, grads, n, n8
+
+
+def cpu_baseline(workload: str, seconds: float):
+    """The CPU oracle as it stands, single-threaded, on a bounded sample of
+    the workload: layer 0 of the parameter set (all of its tensors, FP8
+    copies included), timed for whole steps until ~`seconds` have passed."""
+    cfg, specs, orc, grads, n, n8 = _oracle_sample(workload, lambda nm: nm.startswith(("l0.", "h0.")))
     steps, t0 = 0, time.perf_counter()
     while True:
         orc.run(grads)
@@ -450,27 +464,38 @@ def cpu_baseline(workload: str, seconds: float):
         if el >= seconds or steps >= 50:
             break
     return {"value": n * steps / el, "unit": "params/s", "cores": 1, "kind": "oracle",
-            "sample": f"{len(specs)} tensors of {cfg.name} layer 0 ({n:,} params, "
-                      f"{sum(s.numel for s in specs if s.fp8):,} FP8-emitted), {steps} full steps "
-                      f"in {el:.1f} s, single-threaded C oracle"}
+            "sample": f"{len(specs)} tensors of {cfg.name} layer 0 ({n:,} params, {n8:,} "
+                      f"FP8-emitted), {steps} full step(s) in {el:.1f} s, single-threaded C oracle"}
 
 
 def run_reference(args, rank, world):
+    """The reference arm: the pages ship no runnable code, so it is the CPU
+    oracle, timed for W untimed + K timed steps on a bounded sample of the
+    workload (the attention block of layer 0), on one host core."""
     if rank != 0:
         return None
+    attn = ("l0.attn_norm", "l0.q", "l0.k", "l0.v", "l0.o", "l0.ffn_norm",
+            "h0.ln_1.w", "h0.ln_1.b", "h0.attn.c_attn.w", "h0.attn.c_proj.w")
+    cfg, specs, orc, grads, n, n8 = _oracle_sample(args.workload, lambda nm: nm in attn)
+    for _ in range(args.warmup):
+        orc.run(grads)
     t0 = time.perf_counter()
-    cb = cpu_baseline(args.workload, args.cpu_seconds)
+    for _ in range(args.steps):
+        orc.run(grads)
     el = time.perf_counter() - t0
-    return {"impl": "reference", "metric": "fused AMP step params/s", "value": cb["value"],
-            "unit": "params/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32 (master/m/v), f16 grads",
-            "data": "synthetic", "config": {"workload": args.workload},
-            "cpu_baseline": cb,
-            "e2e": {"value": cb["value"], "unit": "params/s", "h2d_bytes_per_step": 0,
+    value = n * args.steps / el
+    sample = (f"{len(specs)} tensors of {cfg.name} layer 0 attention ({n:,} params, {n8:,} "
+              f"FP8-emitted) per step, single-threaded C oracle")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "params/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32 (master/m/v), f16 grads, bf16 + e4m3fn outputs",
+            "data": "synthetic", "config": workload_config(args.workload, world),
+            "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
-            "note": f"the pages ship no runnable code; the reference arm is the CPU oracle "
-                    f"({el:.1f} s wall)"}
+            "note": "the pages ship no runnable code; the reference arm is the CPU oracle"}
 
 
 def main():
