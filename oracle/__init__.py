@@ -58,6 +58,13 @@ def lib():
             L.orc_adamw_master_step.argtypes = (
                 [ctypes.c_int, P, P, P, P, ctypes.c_int, P, I64P, P, ctypes.c_int32, P]
                 + [ctypes.c_double] * 5 + [P, P])
+            L.orc_grad_sumsq.restype = ctypes.c_double
+            L.orc_grad_sumsq.argtypes = [ctypes.c_int, P, I64P, ctypes.c_int, ctypes.c_float]
+            L.orc_clip_coef.restype = ctypes.c_float
+            L.orc_clip_coef.argtypes = [ctypes.c_double, ctypes.c_double]
+            L.orc_adamw_master_step_clip.argtypes = (
+                [ctypes.c_int, P, P, P, P, ctypes.c_int, P, I64P, P, ctypes.c_int32, P]
+                + [ctypes.c_double] * 5 + [P, P, ctypes.c_float])
             L.orc_fp8_quant_tensorwise.argtypes = [P, ctypes.c_int, ctypes.c_int64,
                                                    ctypes.c_int64, ctypes.c_int,
                                                    ctypes.c_double, P, P, P, P, ctypes.c_int]
@@ -129,22 +136,38 @@ def update_scale(scale: float, tracker: int, found_inf: int, growth: float, back
     return float(s[0]), int(t[0]), int(f[0])
 
 
+def grad_sumsq(grads, dt: str, scale: float) -> float:
+    """fp64 sum over all elements of (g * (1/S))^2, in element order."""
+    return float(lib().orc_grad_sumsq(len(grads), _ptr_array(grads), _numels(grads), _CODES[dt],
+                                      ctypes.c_float(scale)))
+
+
+def clip_coef(sumsq: float, max_norm: float) -> float:
+    """fp32 min(1, max_norm / (sqrt(sumsq) + 1e-6))."""
+    return float(lib().orc_clip_coef(sumsq, max_norm))
+
+
 def adamw_master_step(master, exp_avg, exp_avg_sq, grads, gdt: str, bf16_out, scale,
                       found_inf: int, step: int, lr, beta1, beta2, eps, wd,
-                      amax_slot=None, amax: np.ndarray | None = None) -> int:
+                      amax_slot=None, amax: np.ndarray | None = None,
+                      clip: float | None = None) -> int:
     """FP32-master AdamW over a tensor list (in place); returns the new step count.
-    ``scale`` None means S = 1. ``bf16_out`` is a list of uint16 arrays or None."""
+    ``scale`` None means S = 1. ``bf16_out`` is a list of uint16 arrays or None.
+    ``clip`` is the fp32 gradient clipping factor (None: no clipping)."""
     n = len(master)
     sc = None if scale is None else np.array([scale], np.float32)
     st = np.array([step], np.int32)
     slots = None if amax_slot is None else np.ascontiguousarray(amax_slot, np.int32)
-    lib().orc_adamw_master_step(
-        n, _ptr_array(master), _ptr_array(exp_avg), _ptr_array(exp_avg_sq),
-        _ptr_array(grads), _CODES[gdt], _ptr_array(bf16_out) if bf16_out else None,
-        _numels(master), _ptr(sc) if sc is not None else None, int(found_inf), _ptr(st),
-        lr, beta1, beta2, eps, wd,
-        _ptr(slots) if slots is not None else None,
-        _ptr(amax) if amax is not None else None)
+    args = [n, _ptr_array(master), _ptr_array(exp_avg), _ptr_array(exp_avg_sq),
+            _ptr_array(grads), _CODES[gdt], _ptr_array(bf16_out) if bf16_out else None,
+            _numels(master), _ptr(sc) if sc is not None else None, int(found_inf), _ptr(st),
+            lr, beta1, beta2, eps, wd,
+            _ptr(slots) if slots is not None else None,
+            _ptr(amax) if amax is not None else None]
+    if clip is None:
+        lib().orc_adamw_master_step(*args)
+    else:
+        lib().orc_adamw_master_step_clip(*args, ctypes.c_float(clip))
     return int(st[0])
 
 
@@ -175,7 +198,7 @@ class AmpStepOracle:
 
     def __init__(self, master, grad_dtype, lr, beta1, beta2, eps, weight_decay,
                  init_scale, growth_factor, backoff_factor, growth_interval,
-                 emit_bf16=True, fp8_shapes=None, fp8_eps=1e-12):
+                 emit_bf16=True, fp8_shapes=None, fp8_eps=1e-12, max_norm=None):
         self.master = [np.array(m, np.float32, copy=True) for m in master]
         self.exp_avg = [np.zeros_like(m) for m in self.master]
         self.exp_avg_sq = [np.zeros_like(m) for m in self.master]
@@ -188,6 +211,8 @@ class AmpStepOracle:
         self.fp8_shapes = fp8_shapes
         self.slots = None
         self.fp8_eps = fp8_eps
+        self.max_norm = max_norm
+        self.grad_norm = None
         if fp8_shapes is not None:
             self.slots, k = [], 0
             for sh in fp8_shapes:
@@ -204,9 +229,15 @@ class AmpStepOracle:
         """Apply one step with the given scaled gradients; returns found_inf."""
         fi = unscale_check(grads, self.gdt, self.scale, found_inf=self.found_inf)
         self.found_inf = fi
+        clip = None
+        if self.max_norm is not None:
+            ss = grad_sumsq(grads, self.gdt, self.scale)
+            self.grad_norm = float(np.sqrt(ss))
+            clip = clip_coef(ss, self.max_norm)
         self.step = adamw_master_step(self.master, self.exp_avg, self.exp_avg_sq, grads,
                                       self.gdt, self.bf16, self.scale, fi, self.step,
-                                      *self.hyper, amax_slot=self.slots, amax=self.amax)
+                                      *self.hyper, amax_slot=self.slots, amax=self.amax,
+                                      clip=clip)
         if self.fp8_shapes is not None and not fi:
             for i, sh in enumerate(self.fp8_shapes):
                 if sh is None:

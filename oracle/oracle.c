@@ -210,6 +210,36 @@ void orc_unscale_check(int n_tensors, void *const *ptrs, const int64_t *numel,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Gradient-norm clipping after unscale.  "AMP：Automatic Mixed Precision 技术 */
+/* 笔记" §6 and "06 · 混合精度" §四: with a loss scaler the gradients are       */
+/* unscaled first and clipped afterwards (clip_grad_norm_(params, max_norm)),  */
+/* otherwise the threshold would apply to the scaled values.  The pages call   */
+/* the library routine without writing it out; the plain reading is the global */
+/* L2 norm over every element of every gradient, and the factor               */
+/* min(1, max_norm / (norm + 1e-6)) applied to each unscaled gradient.         */
+/* ------------------------------------------------------------------------ */
+double orc_grad_sumsq(int n_tensors, void *const *ptrs, const int64_t *numel, int dtype,
+                      float scale)
+{
+    float inv_s = 1.0f / scale;
+    double acc = 0.0;
+    for (int t = 0; t < n_tensors; ++t)
+        for (int64_t k = 0; k < numel[t]; ++k) {
+            double g = (double)(load_as_f32(dtype, ptrs[t], k) * inv_s);
+            acc += g * g;
+        }
+    return acc;
+}
+
+float orc_clip_coef(double sumsq, double max_norm)
+{
+    double c = max_norm / (sqrt(sumsq) + 1e-6);
+    if (isnan(c))
+        return (float)c; /* NaN propagates (the step is skipped anyway) */
+    return (float)(c < 1.0 ? c : 1.0);
+}
+
+/* ------------------------------------------------------------------------ */
 /* Dynamic loss-scale state machine, [CH20] §20.5.33: on inf/NaN multiply    */
 /* the scale by backoff and reset the tracker; otherwise count the clean     */
 /* step and multiply by growth once the count reaches the interval.          */
@@ -248,12 +278,33 @@ void orc_update_scale(float *scale, int32_t *tracker, int32_t *found_inf,
 /* amax_slot[t] >= 0 also folds max|bf16| of tensor t into amax[slot]        */
 /* (NaN-propagating), the input of the FP8 weight quantizer.                 */
 /* ------------------------------------------------------------------------ */
+void orc_adamw_master_step_clip(int n_tensors, float *const *master, float *const *exp_avg,
+                                float *const *exp_avg_sq, void *const *grads, int gdtype,
+                                uint16_t *const *bf16_out, const int64_t *numel,
+                                const float *scale, int32_t found_inf, int32_t *step,
+                                double lr, double beta1, double beta2, double eps, double wd,
+                                const int32_t *amax_slot, float *amax, float clip_coef);
+
 void orc_adamw_master_step(int n_tensors, float *const *master, float *const *exp_avg,
                            float *const *exp_avg_sq, void *const *grads, int gdtype,
                            uint16_t *const *bf16_out, const int64_t *numel,
                            const float *scale, int32_t found_inf, int32_t *step,
                            double lr, double beta1, double beta2, double eps, double wd,
                            const int32_t *amax_slot, float *amax)
+{
+    orc_adamw_master_step_clip(n_tensors, master, exp_avg, exp_avg_sq, grads, gdtype, bf16_out,
+                               numel, scale, found_inf, step, lr, beta1, beta2, eps, wd,
+                               amax_slot, amax, 1.0f);
+}
+
+/* As above; every unscaled gradient is first multiplied by clip_coef (fp32),
+ * the clipping factor of orc_clip_coef (1.0 leaves it unchanged). */
+void orc_adamw_master_step_clip(int n_tensors, float *const *master, float *const *exp_avg,
+                                float *const *exp_avg_sq, void *const *grads, int gdtype,
+                                uint16_t *const *bf16_out, const int64_t *numel,
+                                const float *scale, int32_t found_inf, int32_t *step,
+                                double lr, double beta1, double beta2, double eps, double wd,
+                                const int32_t *amax_slot, float *amax, float clip_coef)
 {
     if (found_inf)
         return; /* skipped step: no state, output or counter changes */
@@ -273,7 +324,7 @@ void orc_adamw_master_step(int n_tensors, float *const *master, float *const *ex
     for (int i = 0; i < n_tensors; ++i) {
         int slot = amax_slot ? amax_slot[i] : -1;
         for (int64_t k = 0; k < numel[i]; ++k) {
-            float g = load_as_f32(gdtype, grads[i], k) * inv_s;
+            float g = (load_as_f32(gdtype, grads[i], k) * inv_s) * clip_coef;
             float p = master[i][k], m = exp_avg[i][k], v = exp_avg_sq[i][k];
             p = p * decay;
             m = b1 * m + omb1 * g;

@@ -399,3 +399,64 @@ def test_tiny_config_trace_through_oracle_step(golden):
             assert all(np.array_equal(a, b) for a, b in zip(before, orc.master))
         assert orc.scale == tr["scale"][k - 1] and orc.tracker == tr["tracker"][k - 1]
         assert orc.step == tr["optimizer_step"][k - 1]
+
+
+# --------------------------------------------------- grad-norm clipping
+def test_grad_norm_closed_form():
+    """Constant gradients c (fp16, scaled by S = 2^k): norm = |c| sqrt(N)."""
+    S = 1024.0
+    sizes = [100, 300, 24]
+    c = np.float16(3.0)
+    grads = [np.full(n, c, np.float16).view(np.uint16) for n in sizes]
+    ss = O.grad_sumsq(grads, "f16", S)
+    assert ss == (3.0 / S) ** 2 * sum(sizes)
+    assert O.clip_coef(ss, 1e9) == 1.0
+    assert O.clip_coef(0.0, 1.0) == 1.0
+    assert np.isnan(O.clip_coef(float("nan"), 1.0))
+
+
+def test_clip_matches_torch_clip_grad_norm():
+    """Independent library: unscale, torch.nn.utils.clip_grad_norm_, then
+    torch.optim.AdamW, vs the oracle's fused clip + AdamW over 5 steps."""
+    rng = np.random.default_rng(9)
+    sizes = [1000, 4096, 257]
+    S = 4096.0
+    p0 = [rng.standard_normal(n).astype(F32) * F32(0.02) for n in sizes]
+    hp = dict(lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.01)
+    max_norm = 0.05
+    gseq = [[(rng.standard_normal(n) * 1e-3 * S).astype(np.float16).view(np.uint16) for n in sizes]
+            for _ in range(5)]
+    master = [x.copy() for x in p0]
+    m = [np.zeros_like(x) for x in p0]
+    v = [np.zeros_like(x) for x in p0]
+    step = 0
+    tp = [torch.nn.Parameter(torch.from_numpy(x.copy())) for x in p0]
+    opt = torch.optim.AdamW(tp, foreach=False, fused=False, **hp)
+    for gs in gseq:
+        ss = O.grad_sumsq(gs, "f16", S)
+        coef = O.clip_coef(ss, max_norm)
+        assert coef < 1.0
+        step = O.adamw_master_step(master, m, v, gs, "f16", None, S, 0, step, hp["lr"],
+                                   *hp["betas"], hp["eps"], hp["weight_decay"], clip=coef)
+        for t, g in zip(tp, gs):
+            t.grad = torch.from_numpy(g.view(np.float16).astype(np.float32) / np.float32(S))
+        tn = torch.nn.utils.clip_grad_norm_(tp, max_norm, foreach=False)
+        assert abs(float(tn) - np.sqrt(ss)) <= 1e-6 * np.sqrt(ss)
+        opt.step()
+    for i, t in enumerate(tp):
+        ref = t.detach().numpy()
+        floor = 1e-6 * np.sqrt(np.mean(ref.astype(np.float64) ** 2))
+        assert np.all(np.abs(master[i].astype(np.float64) - ref)
+                      <= 1e-6 * np.maximum(np.abs(master[i]), np.abs(ref)) + floor)
+
+
+def test_clip_factor_one_is_the_unclipped_step():
+    rng = np.random.default_rng(10)
+    p0 = [rng.standard_normal(500).astype(F32)]
+    g = [rng.standard_normal(500).astype(F32)]
+    a = _adamw_oracle(p0, [g], 1e-3, 0.9, 0.999, 1e-8, 0.01)
+    master = [p0[0].copy()]
+    m, v = [np.zeros(500, F32)], [np.zeros(500, F32)]
+    O.adamw_master_step(master, m, v, g, "f32", None, None, 0, 0, 1e-3, 0.9, 0.999, 1e-8, 0.01,
+                        clip=1.0)
+    assert np.array_equal(master[0], a[0][0]) and np.array_equal(m[0], a[1][0])
