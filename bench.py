@@ -176,6 +176,7 @@ def run_ours(args, rank, world, device):
     if args.workload == "fp8_sweep":
         return run_fp8_sweep(args, rank, world, device)
     step, info = build_step(args.workload, device, seed=1234 + rank)
+    step.max_norm = args.clip
     n_params = info["params"]
     stream = torch.cuda.Stream(device=device)
     comb = None
@@ -188,15 +189,26 @@ def run_ours(args, rank, world, device):
     def one_step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        A.amp_unscale_check(step.L_g, step.scale, step.found_inf, stream=stream)
+        if args.clip is None:
+            A.amp_unscale_check(step.L_g, step.scale, step.found_inf, stream=stream)
+        else:
+            A.amp_unscale_check_norm(step.L_g, step.scale, step.found_inf, step.grad_sumsq,
+                                     stream=stream)
         if comb is not None:
             with torch.cuda.stream(stream):
                 comb()
         if ev is not None:
             ev[1].record(stream)
-        A.amp_adamw_master_step(step.L_master, step.L_m, step.L_v, step.L_g, step.L_b,
-                                step.scale, step.found_inf, step.step_count, *step.hyper,
-                                amax=step.amax if step.n_fp8 else None, stream=stream)
+        amax = step.amax if step.n_fp8 else None
+        if args.clip is None:
+            A.amp_adamw_master_step(step.L_master, step.L_m, step.L_v, step.L_g, step.L_b,
+                                    step.scale, step.found_inf, step.step_count, *step.hyper,
+                                    amax=amax, stream=stream)
+        else:
+            A.amp_adamw_master_step_clip(step.L_master, step.L_m, step.L_v, step.L_g, step.L_b,
+                                         step.scale, step.found_inf, step.step_count,
+                                         *step.hyper, step.grad_sumsq, args.clip, amax=amax,
+                                         stream=stream)
         if ev is not None:
             ev[2].record(stream)
         if step.n_fp8:
@@ -266,6 +278,7 @@ def run_ours(args, rank, world, device):
         "data": "synthetic (seeded N(0,0.02) masters, N(0,sigma*S) fp16 grads; no trained weights)",
         "config": dict(workload_config(args.workload, world), per_step_bytes=total_bytes),
         "hbm_gbs_step": total_bytes / (ms_step * 1e-3) / 1e9,
+        "grad_clip": args.clip,
         "kernels_ms": {"unscale_check": statistics.mean(k_check),
                        "adamw_master_step": adamw_ms,
                        "fp8_quant_list": statistics.mean(k_quant)},
@@ -509,6 +522,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--clip", type=float, default=None,
+                    help="also clip the unscaled gradients to this global L2 norm")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -126,6 +126,25 @@ amp_status amp_tensor_list_destroy(amp_tensor_list list);
 amp_status amp_unscale_check(amp_tensor_list grads, const float *scale_dev,
                              int32_t *found_inf_dev, int inplace, amp_stream_t stream);
 
+/* Gradient-norm clipping input ("AMP：Automatic Mixed Precision 技术笔记" §6,
+ * "06 · 混合精度" §四: unscale first, then clip_grad_norm_).  Does everything
+ * amp_unscale_check does (inplace = 0) and also writes
+ *     *grad_sumsq_dev = sum over all elements of (float(g) * (1/S))^2   (fp64)
+ * for amp_adamw_master_step_clip.  Each thread squares the stored values
+ * (exact in fp32 for 16-bit gradients) in fused multiply-add chains of four,
+ * adds the chain sums in compensated fp32, and chunks and the final total are
+ * added in fp64 in a fixed order, so the value does not depend on scheduling;
+ * (1/S)^2 is applied per chunk in fp64, which equals squaring the unscaled
+ * fp32 gradient while 1/S is a power of two.  Relative error <= 6 ulp of
+ * fp32 (3.6e-7).  A non-finite gradient makes the sum NaN (found_inf is set
+ * and the step is skipped); squared fp32 gradients above 3.4e38 overflow the
+ * per-thread sums.  The list handle's per-chunk scratch holds the partial
+ * sums: calls on one list must not overlap on the GPU.
+ * Errors: AMP_EINVAL (NULL argument), AMP_EDTYPE (fp8 list). */
+amp_status amp_unscale_check_norm(amp_tensor_list grads, const float *scale_dev,
+                                  int32_t *found_inf_dev, double *grad_sumsq_dev,
+                                  amp_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* A2-A6: skip decision + FP32-master AdamW + BF16 emission + amax fold.     */
 /* [CH20] §20.5.13, [MP] "为什么需要 FP32 Master Weights" / "PyTorch AMP 与   */
@@ -167,6 +186,21 @@ amp_status amp_adamw_master_step(amp_tensor_list master, amp_tensor_list exp_avg
                                  const int32_t *found_inf_dev, int32_t *step_dev,
                                  const amp_adamw_hyper *hyper, float *amax_dev,
                                  amp_stream_t stream);
+
+/* amp_adamw_master_step with gradient-norm clipping: the per-step scalar
+ *     clip = min(1, max_norm / (sqrt(*grad_sumsq_dev) + 1e-6))
+ * is formed once in fp64 (NaN propagates) and rounded to fp32, and every
+ * element uses g = (float(grad) * (1/S)) * clip in place of float(grad) * (1/S).
+ * grad_sumsq_dev is the output of amp_unscale_check_norm for the same step.
+ * Errors: as amp_adamw_master_step, plus AMP_EINVAL for a NULL
+ * grad_sumsq_dev or a max_norm that is not finite and > 0. */
+amp_status amp_adamw_master_step_clip(amp_tensor_list master, amp_tensor_list exp_avg,
+                                      amp_tensor_list exp_avg_sq, amp_tensor_list grads,
+                                      amp_tensor_list bf16_out, const float *scale_dev,
+                                      const int32_t *found_inf_dev, int32_t *step_dev,
+                                      const amp_adamw_hyper *hyper, float *amax_dev,
+                                      const double *grad_sumsq_dev, double max_norm,
+                                      amp_stream_t stream);
 
 /* Allocation-free form of amp_adamw_master_step.  The pages have no
  * counterpart: it exists for callers that cannot allocate device memory -

@@ -25,7 +25,8 @@ _TORCH_DT = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16",
 
 # every symbol include/ampfp8.h declares
 EXPORTS = ("amp_tensor_list_create", "amp_tensor_list_set_amax_slots", "amp_tensor_list_destroy",
-           "amp_unscale_check", "amp_adamw_master_step", "amp_adamw_master_step_noalloc",
+           "amp_unscale_check", "amp_unscale_check_norm", "amp_adamw_master_step",
+           "amp_adamw_master_step_clip", "amp_adamw_master_step_noalloc",
            "fp8_quant_tensorwise", "fp8_quant_tensorwise_list", "amp_update_scale",
            "amp_last_error", "amp_abi_version")
 
@@ -63,6 +64,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.amp_unscale_check.argtypes = [P, P, P, i32, P]
         L.amp_adamw_master_step.argtypes = [P, P, P, P, P, P, P, P,
                                             ctypes.POINTER(amp_adamw_hyper), P, P]
+        L.amp_unscale_check_norm.argtypes = [P, P, P, P, P]
+        L.amp_adamw_master_step_clip.argtypes = [P, P, P, P, P, P, P, P,
+                                                 ctypes.POINTER(amp_adamw_hyper), P, P, dbl, P]
         L.amp_adamw_master_step_noalloc.argtypes = [i32, P, P, P, P, i32, P, P, P, P, P, P,
                                                     ctypes.POINTER(amp_adamw_hyper), P, P]
         L.fp8_quant_tensorwise.argtypes = [P, i32, i64, i64, i32, dbl, P, P, P, P, i32, P, P]
@@ -161,6 +165,28 @@ def amp_unscale_check(grads: TensorList, scale, found_inf, inplace: bool = False
     _check("amp_unscale_check",
            load().amp_unscale_check(grads.handle, _dptr(scale), _dptr(found_inf), int(inplace),
                                     _stream(stream)))
+
+
+def amp_unscale_check_norm(grads: TensorList, scale, found_inf, grad_sumsq, stream=None):
+    """As amp_unscale_check, and grad_sumsq (fp64 device scalar) = sum of
+    squared unscaled gradients."""
+    _check("amp_unscale_check_norm",
+           load().amp_unscale_check_norm(grads.handle, _dptr(scale), _dptr(found_inf),
+                                         _dptr(grad_sumsq), _stream(stream)))
+
+
+def amp_adamw_master_step_clip(master: TensorList, exp_avg: TensorList, exp_avg_sq: TensorList,
+                               grads: TensorList, bf16_out: TensorList | None, scale, found_inf,
+                               step, lr: float, beta1: float, beta2: float, eps: float,
+                               weight_decay: float, grad_sumsq, max_norm: float, amax=None,
+                               stream=None):
+    h = amp_adamw_hyper(lr, beta1, beta2, eps, weight_decay)
+    _check("amp_adamw_master_step_clip",
+           load().amp_adamw_master_step_clip(master.handle, exp_avg.handle, exp_avg_sq.handle,
+                                             grads.handle, bf16_out.handle if bf16_out else None,
+                                             _dptr(scale), _dptr(found_inf), _dptr(step),
+                                             ctypes.byref(h), _dptr(amax), _dptr(grad_sumsq),
+                                             float(max_norm), _stream(stream)))
 
 
 def amp_adamw_master_step(master: TensorList, exp_avg: TensorList, exp_avg_sq: TensorList,

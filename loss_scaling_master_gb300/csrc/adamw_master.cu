@@ -31,13 +31,15 @@ struct AdamwParams {
 };
 
 struct Scal {
-    float r, decay, b1, omb1, b2, omb2, eps, step_size, c2;
+    float r, clip, decay, b1, omb1, b2, omb2, eps, step_size, c2;
 };
 
 // One element of the update; each operation rounded on its own (no fma).
+// g = (float(grad) * (1/S)) * clip, where clip is exactly 1.0 unless the
+// gradients are being norm-clipped (x * 1.0f == x, so that path is unchanged).
 __device__ __forceinline__ void adamw_elem(float &p, float &m, float &v, float graw,
                                            const Scal &s) {
-    const float g = __fmul_rn(graw, s.r);
+    const float g = __fmul_rn(__fmul_rn(graw, s.r), s.clip);
     p = __fmul_rn(p, s.decay);
     m = __fadd_rn(__fmul_rn(s.b1, m), __fmul_rn(s.omb1, g));
     v = __fadd_rn(__fmul_rn(s.b2, v), __fmul_rn(s.omb2, __fmul_rn(g, g)));
@@ -164,6 +166,7 @@ __global__ void __launch_bounds__(kThreads) adamw_main_kernel(AdamwParams P) {
 
     Scal s;
     s.r = P.scale ? __fdiv_rn(1.0f, *P.scale) : 1.0f;
+    s.clip = sc.clip;
     s.decay = P.decay;
     s.b1 = P.b1;
     s.omb1 = P.omb1;
@@ -212,12 +215,18 @@ __global__ void __launch_bounds__(kThreads) adamw_main_kernel(AdamwParams P) {
 }
 
 __global__ void adamw_prologue_kernel(const int32_t *found_inf, int32_t *step, double lr,
-                                      double beta1, double beta2, AdamwStepScalars *out) {
+                                      double beta1, double beta2, const double *clip_sumsq,
+                                      double max_norm, AdamwStepScalars *out) {
     AdamwStepScalars s;
     s.skip = found_inf ? (*found_inf != 0) : 0;
     s.step_size = 0.0f;
     s.bc2_sqrt = 1.0f;
-    s.pad = 0.0f;
+    s.clip = 1.0f;
+    if (clip_sumsq) {
+        // min(1, max_norm / (||g|| + 1e-6)), NaN propagating
+        const double c = max_norm / (sqrt(*clip_sumsq) + 1e-6);
+        s.clip = float(c != c ? c : (c < 1.0 ? c : 1.0));
+    }
     if (!s.skip) {
         const int32_t t = *step + 1;
         const double bc1 = 1.0 - pow(beta1, double(t));
@@ -235,8 +244,10 @@ cudaError_t launch_adamw(const ListView &p, const ListView &m, const ListView &v
                          const ListView &g, const ListView *b, int64_t n_chunks, int gelem,
                          const float *scale, const int32_t *found_inf, int32_t *step,
                          const AdamwConsts &c, AdamwStepScalars *scal, float *amax,
-                         bool use_slots, cudaStream_t s) {
-    adamw_prologue_kernel<<<1, 1, 0, s>>>(found_inf, step, c.lr, c.beta1, c.beta2, scal);
+                         bool use_slots, cudaStream_t s, const double *clip_sumsq,
+                         double max_norm) {
+    adamw_prologue_kernel<<<1, 1, 0, s>>>(found_inf, step, c.lr, c.beta1, c.beta2, clip_sumsq,
+                                          max_norm, scal);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || n_chunks == 0) return e;
     AdamwParams P;

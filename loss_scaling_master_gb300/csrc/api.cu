@@ -80,7 +80,7 @@ extern "C" {
 
 const char *amp_last_error(void) { return g_err; }
 
-int amp_abi_version(void) { return 1; }
+int amp_abi_version(void) { return 2; }
 
 amp_status amp_tensor_list_create(int n, void *const *dev_ptrs, const int64_t *rows,
                                   const int64_t *cols, amp_dtype dtype, amp_stream_t stream,
@@ -140,7 +140,8 @@ amp_status amp_tensor_list_create(int n, void *const *dev_ptrs, const int64_t *r
     const size_t o_slots = align_up(o_cols + nn * sizeof(int64_t));
     const size_t o_chunks = align_up(o_slots + nn * sizeof(int32_t));
     const size_t o_tiles = align_up(o_chunks + std::max<size_t>(1, chunks.size()) * sizeof(uint2));
-    const size_t o_scratch = align_up(o_tiles + std::max<size_t>(1, tiles.size()) * sizeof(uint2));
+    const size_t o_partials = align_up(o_tiles + std::max<size_t>(1, tiles.size()) * sizeof(uint2));
+    const size_t o_scratch = align_up(o_partials + std::max<size_t>(1, chunks.size()) * sizeof(double));
     const size_t total = align_up(o_scratch + 256);
     std::vector<char> host(total, 0);
     std::memcpy(host.data() + o_ptrs, L->ptrs.data(), n * sizeof(void *));
@@ -180,6 +181,7 @@ amp_status amp_tensor_list_create(int n, void *const *dev_ptrs, const int64_t *r
     L->view.slots = reinterpret_cast<const int32_t *>(b + o_slots);
     L->view.chunks = reinterpret_cast<const uint2 *>(b + o_chunks);
     L->view.tiles = reinterpret_cast<const uint2 *>(b + o_tiles);
+    L->view.partials = reinterpret_cast<double *>(b + o_partials);
     L->view.n = n;
     L->scratch = b + o_scratch;
     *out = L;
@@ -221,12 +223,12 @@ amp_status amp_unscale_check(amp_tensor_list grads, const float *scale_dev, int3
     return e == cudaSuccess ? AMP_OK : cuda_fail(e, "amp_unscale_check");
 }
 
-amp_status amp_adamw_master_step(amp_tensor_list master, amp_tensor_list exp_avg,
-                                 amp_tensor_list exp_avg_sq, amp_tensor_list grads,
-                                 amp_tensor_list bf16_out, const float *scale_dev,
-                                 const int32_t *found_inf_dev, int32_t *step_dev,
-                                 const amp_adamw_hyper *hyper, float *amax_dev,
-                                 amp_stream_t stream) {
+static amp_status adamw_entry(amp_tensor_list master, amp_tensor_list exp_avg,
+                              amp_tensor_list exp_avg_sq, amp_tensor_list grads,
+                              amp_tensor_list bf16_out, const float *scale_dev,
+                              const int32_t *found_inf_dev, int32_t *step_dev,
+                              const amp_adamw_hyper *hyper, float *amax_dev,
+                              const double *clip_sumsq, double max_norm, amp_stream_t stream) {
     if (!master || !exp_avg || !exp_avg_sq || !grads || !step_dev || !hyper)
         return fail(AMP_EINVAL, "amp_adamw_master_step: NULL argument");
     if (master->dtype != AMP_DT_F32 || exp_avg->dtype != AMP_DT_F32 ||
@@ -257,8 +259,45 @@ amp_status amp_adamw_master_step(amp_tensor_list master, amp_tensor_list exp_avg
         master->view, exp_avg->view, exp_avg_sq->view, grads->view,
         bf16_out ? &bf16_out->view : nullptr, master->n_chunks, gc, scale_dev, found_inf_dev,
         step_dev, c, reinterpret_cast<amp::AdamwStepScalars *>(master->scratch), amax_dev, slots,
-        reinterpret_cast<cudaStream_t>(stream));
+        reinterpret_cast<cudaStream_t>(stream), clip_sumsq, max_norm);
     return e == cudaSuccess ? AMP_OK : cuda_fail(e, "amp_adamw_master_step");
+}
+
+amp_status amp_adamw_master_step(amp_tensor_list master, amp_tensor_list exp_avg,
+                                 amp_tensor_list exp_avg_sq, amp_tensor_list grads,
+                                 amp_tensor_list bf16_out, const float *scale_dev,
+                                 const int32_t *found_inf_dev, int32_t *step_dev,
+                                 const amp_adamw_hyper *hyper, float *amax_dev,
+                                 amp_stream_t stream) {
+    return adamw_entry(master, exp_avg, exp_avg_sq, grads, bf16_out, scale_dev, found_inf_dev,
+                       step_dev, hyper, amax_dev, nullptr, 0.0, stream);
+}
+
+amp_status amp_adamw_master_step_clip(amp_tensor_list master, amp_tensor_list exp_avg,
+                                      amp_tensor_list exp_avg_sq, amp_tensor_list grads,
+                                      amp_tensor_list bf16_out, const float *scale_dev,
+                                      const int32_t *found_inf_dev, int32_t *step_dev,
+                                      const amp_adamw_hyper *hyper, float *amax_dev,
+                                      const double *grad_sumsq_dev, double max_norm,
+                                      amp_stream_t stream) {
+    if (!grad_sumsq_dev) return fail(AMP_EINVAL, "amp_adamw_master_step_clip: grad_sumsq_dev is NULL");
+    if (!(max_norm > 0.0) || max_norm > 1e300)
+        return fail(AMP_EINVAL, "amp_adamw_master_step_clip: max_norm must be finite and > 0");
+    return adamw_entry(master, exp_avg, exp_avg_sq, grads, bf16_out, scale_dev, found_inf_dev,
+                       step_dev, hyper, amax_dev, grad_sumsq_dev, max_norm, stream);
+}
+
+amp_status amp_unscale_check_norm(amp_tensor_list grads, const float *scale_dev,
+                                  int32_t *found_inf_dev, double *grad_sumsq_dev,
+                                  amp_stream_t stream) {
+    if (!grads || !found_inf_dev || !grad_sumsq_dev)
+        return fail(AMP_EINVAL, "amp_unscale_check_norm: NULL argument");
+    const int ec = elem_code(grads->dtype);
+    if (ec < 0) return fail(AMP_EDTYPE, "amp_unscale_check_norm: gradients must be f32/f16/bf16");
+    cudaError_t e = amp::launch_check_norm(grads->view, grads->n_chunks, ec, scale_dev,
+                                           found_inf_dev, grad_sumsq_dev,
+                                           reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AMP_OK : cuda_fail(e, "amp_unscale_check_norm");
 }
 
 amp_status fp8_quant_tensorwise(const void *x, amp_dtype x_dtype, int64_t rows, int64_t cols,

@@ -25,6 +25,7 @@ struct ListView {
     const int32_t *slots;
     const uint2 *chunks;
     const uint2 *tiles;
+    double *partials;  // one fp64 slot per chunk (scratch of the norm pass)
     int n;
 };
 

@@ -38,7 +38,7 @@ struct AdamwStepScalars {
     int32_t skip;
     float step_size;
     float bc2_sqrt;
-    float pad;
+    float clip;  // gradient clipping factor, exactly 1.0 when not clipping
 };
 
 int sm_count(int device);
@@ -49,11 +49,15 @@ void set_last_error(const char *msg);
 cudaError_t launch_unscale_check(const ListView &g, int64_t n_chunks, int elem, const float *scale,
                                  int32_t *found_inf, int inplace, cudaStream_t s);
 
+cudaError_t launch_check_norm(const ListView &g, int64_t n_chunks, int elem, const float *scale,
+                              int32_t *found_inf, double *sumsq, cudaStream_t s);
+
 cudaError_t launch_adamw(const ListView &p, const ListView &m, const ListView &v,
                          const ListView &g, const ListView *b, int64_t n_chunks, int gelem,
                          const float *scale, const int32_t *found_inf, int32_t *step,
                          const AdamwConsts &c, AdamwStepScalars *scal, float *amax,
-                         bool use_slots, cudaStream_t s);
+                         bool use_slots, cudaStream_t s, const double *clip_sumsq = nullptr,
+                         double max_norm = 0.0);
 
 cudaError_t launch_update_scale(float *scale, int32_t *tracker, int32_t *found_inf, float growth,
                                 float backoff, int32_t interval, float *amax, int n_amax,

@@ -24,11 +24,12 @@ class AmpOptimizerStep:
     def __init__(self, master, grads, *, lr, beta1, beta2, eps, weight_decay,
                  init_scale=65536.0, growth_factor=2.0, backoff_factor=0.5,
                  growth_interval=2000, emit_bf16=True, fp8_shapes=None, fp8_eps=1e-12,
-                 stream=None):
+                 max_norm=None, stream=None):
         """master: fp32 device tensors (updated in place); grads: device
         tensors (f16/bf16/f32) the caller fills with scaled gradients before
         each step.  fp8_shapes: per tensor (rows, cols) for weights that get
-        e4m3fn copies, None for the others (requires emit_bf16)."""
+        e4m3fn copies, None for the others (requires emit_bf16).  max_norm:
+        clip the unscaled gradients to this global L2 norm (None: no clipping)."""
         dev = master[0].device
         self.stream = stream
         self.master = list(master)
@@ -43,6 +44,8 @@ class AmpOptimizerStep:
         self.growth_tracker = torch.zeros(1, dtype=torch.int32, device=dev)
         self.step_count = torch.zeros(1, dtype=torch.int32, device=dev)
         self.found_inf = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.max_norm = max_norm
+        self.grad_sumsq = torch.zeros(1, dtype=torch.float64, device=dev)
         self.fp8_eps = fp8_eps
         mk = lambda ts, two_d=False: A.amp_tensor_list_create(ts, two_d=two_d, stream=stream)
         self.L_master, self.L_m, self.L_v = mk(self.master), mk(self.exp_avg), mk(self.exp_avg_sq)
@@ -74,8 +77,9 @@ class AmpOptimizerStep:
 
     @property
     def launches_per_step(self) -> int:
-        """Kernels one step enqueues (check, AdamW prologue + main, [quant], update)."""
-        return 4 + (1 if self.n_fp8 else 0)
+        """Kernels one step enqueues (check [+ norm reduce], AdamW prologue + main,
+        [quant], update)."""
+        return 4 + (1 if self.n_fp8 else 0) + (1 if self.max_norm is not None else 0)
 
     def add_grad_buffer(self, grads) -> int:
         """Register another set of gradient buffers (same shapes and dtype) and
@@ -114,10 +118,17 @@ class AmpOptimizerStep:
 
     def _enqueue(self, s, grad_buffer: int = 0):
         L_g = self.grad_lists[grad_buffer]
-        A.amp_unscale_check(L_g, self.scale, self.found_inf, stream=s)
-        A.amp_adamw_master_step(self.L_master, self.L_m, self.L_v, L_g, self.L_b, self.scale,
-                                self.found_inf, self.step_count, *self.hyper,
-                                amax=self.amax if self.n_fp8 else None, stream=s)
+        amax = self.amax if self.n_fp8 else None
+        if self.max_norm is None:
+            A.amp_unscale_check(L_g, self.scale, self.found_inf, stream=s)
+            A.amp_adamw_master_step(self.L_master, self.L_m, self.L_v, L_g, self.L_b, self.scale,
+                                    self.found_inf, self.step_count, *self.hyper, amax=amax,
+                                    stream=s)
+        else:
+            A.amp_unscale_check_norm(L_g, self.scale, self.found_inf, self.grad_sumsq, stream=s)
+            A.amp_adamw_master_step_clip(self.L_master, self.L_m, self.L_v, L_g, self.L_b,
+                                         self.scale, self.found_inf, self.step_count, *self.hyper,
+                                         self.grad_sumsq, self.max_norm, amax=amax, stream=s)
         if self.n_fp8:
             A.fp8_quant_tensorwise_list(self.L_x8, self.L_q, self.L_qt, "e4m3fn", self.amax,
                                         self.inv_scale, eps=self.fp8_eps, skip_if=self.found_inf,

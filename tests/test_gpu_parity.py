@@ -458,3 +458,70 @@ def test_graph_replay_matches_eager(A, dev):
     assert torch.equal(eager.inv_scale, graphed.inv_scale)
     eager.close()
     graphed.close()
+
+
+# ------------------------------------------------------ grad-norm clipping
+@pytest.mark.parametrize("dt", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("misalign", [False, True])
+def test_grad_norm_parity_and_determinism(A, dev, dt, misalign):
+    """Sum of squared unscaled gradients vs the oracle's fp64 sequential sum.
+    Tolerance: squares of 16-bit values are exact in fp32; a chain of four
+    fused multiply-adds plus the pair add costs <= 4 ulp, the compensated
+    per-thread sum <= 2 ulp, every later addition is fp64 (6 ulp of fp32 =
+    3.6e-7, plus 2 ulp when 1/S is not a power of two); rel 1e-6 bounds it.
+    Repeated calls are bit-identical."""
+    rng = np.random.default_rng(50)
+    for scale in (65536.0, 1.0, 1000.0):
+        hl = _grads_host(rng, RAGGED + [3 * 16384 + 5], dt, sigma=0.01 * scale)
+        tensors = _device_views(hl, dt, dev, misalign)
+        L = A.amp_tensor_list_create(tensors)
+        fi = torch.zeros(1, dtype=torch.int32, device=dev)
+        ss = torch.zeros(1, dtype=torch.float64, device=dev)
+        A.amp_unscale_check_norm(L, torch.tensor([scale], device=dev), fi, ss)
+        first = ss.item()
+        A.amp_unscale_check_norm(L, torch.tensor([scale], device=dev), fi, ss)
+        assert ss.item() == first
+        ref = O.grad_sumsq(hl, dt, scale)
+        assert abs(first - ref) <= 1e-6 * ref, (scale, first, ref)
+        assert int(fi.item()) == 0
+        hl[3][1] = _inf_bits(dt, np.inf)
+        bad = _device_views(hl, dt, dev, misalign)
+        Lb = A.amp_tensor_list_create(bad)
+        A.amp_unscale_check_norm(Lb, torch.tensor([scale], device=dev), fi, ss)
+        assert int(fi.item()) == 1 and not np.isfinite(ss.item())
+        L.close()
+        Lb.close()
+
+
+def test_clipped_step_composition(A, dev):
+    """AmpOptimizerStep with max_norm vs the oracle's step with clipping, over
+    steps where the factor is < 1, = 1 and a skipped step."""
+    from loss_scaling_master_gb300 import AmpOptimizerStep
+    rng = np.random.default_rng(51)
+    sizes = [1000, 4096, 257, 40000]
+    master = [(rng.standard_normal(n) * 0.02).astype(np.float32) for n in sizes]
+    hyper = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+    st = AmpOptimizerStep([torch.from_numpy(m.copy()).to(dev) for m in master],
+                          [torch.empty(n, dtype=torch.float16, device=dev) for n in sizes],
+                          init_scale=65536.0, growth_interval=3, max_norm=0.5, **hyper)
+    orc = O.AmpStepOracle(master, "f16", hyper["lr"], hyper["beta1"], hyper["beta2"], hyper["eps"],
+                          hyper["weight_decay"], 65536.0, 2.0, 0.5, 3, max_norm=0.5)
+    for k in range(6):
+        sigma = (1e-2 if k % 2 == 0 else 1e-5) * orc.scale      # clipped, then unclipped
+        gh = [(rng.standard_normal(n) * sigma).astype(np.float16).view(np.uint16) for n in sizes]
+        if k == 3:
+            gh[2][100] = 0x7C00
+        for t, h in zip(st.grads, gh):
+            t.copy_(to_device(h, "f16", dev))
+        st.step()
+        orc.run(gh)
+        s = st.state()
+        assert (s["scale"], s["growth_tracker"], s["step"]) == (orc.scale, orc.tracker, orc.step)
+        if k != 3:
+            assert abs(np.sqrt(st.grad_sumsq.item()) - orc.grad_norm) <= 1e-6 * orc.grad_norm
+    for i in range(len(sizes)):
+        assert_state_close(to_host_bits(st.master[i]), orc.master[i], f"master[{i}]")
+        assert_state_close(to_host_bits(st.exp_avg[i]), orc.exp_avg[i], f"exp_avg[{i}]")
+        assert_state_close(to_host_bits(st.exp_avg_sq[i]), orc.exp_avg_sq[i], f"exp_avg_sq[{i}]")
+        assert_bf16_close(to_host_bits(st.bf16[i]), orc.bf16[i], f"bf16[{i}]")
+    st.close()
