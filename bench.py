@@ -124,7 +124,7 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- workloads
-def build_step(workload: str, device, seed: int):
+def build_step(workload: str, device, seed: int, fp8_scaling: str = "dynamic"):
     """Allocate a workload's device state; returns (step_obj, info)."""
     import torch
 
@@ -153,7 +153,8 @@ def build_step(workload: str, device, seed: int):
                             eps=cfg.eps, weight_decay=cfg.weight_decay,
                             init_scale=cfg.init_scale, growth_factor=cfg.growth_factor,
                             backoff_factor=cfg.backoff_factor,
-                            growth_interval=cfg.growth_interval, fp8_shapes=fp8_shapes)
+                            growth_interval=cfg.growth_interval, fp8_shapes=fp8_shapes,
+                            fp8_scaling=fp8_scaling if fp8_shapes is not None else "dynamic")
     n = sum(s.numel for s in cfg.specs)
     n8 = sum(s.numel for s in cfg.specs if s.fp8) if cfg.fp8_weights else 0
     gbytes = {"f16": 2, "bf16": 2, "f32": 4}[cfg.grad_dtype]
@@ -175,8 +176,14 @@ def run_ours(args, rank, world, device):
     torch.cuda.set_device(device)
     if args.workload == "fp8_sweep":
         return run_fp8_sweep(args, rank, world, device)
-    step, info = build_step(args.workload, device, seed=1234 + rank)
+    step, info = build_step(args.workload, device, seed=1234 + rank, fp8_scaling=args.fp8_scaling)
     step.max_norm = args.clip
+    delayed = step.fp8_scaling == "delayed"
+    if delayed and args.clip is not None:
+        raise SystemExit("--clip with --fp8-scaling delayed is not supported")
+    if delayed:
+        info["bytes_adamw"] += 2 * info["fp8_params"]       # fp8 + fp8T written in the same pass
+        info["bytes_quant"] = 0
     n_params = info["params"]
     stream = torch.cuda.Stream(device=device)
     comb = None
@@ -200,7 +207,14 @@ def run_ours(args, rank, world, device):
         if ev is not None:
             ev[1].record(stream)
         amax = step.amax if step.n_fp8 else None
-        if args.clip is None:
+        if delayed:
+            P, F = step.delayed_groups[0]
+            A.amp_adamw_master_step_fp8_delayed(P, F, step.L_q, step.L_qt, "e4m3fn",
+                                                step.amax_history, step.hist_len, step.amax,
+                                                step.inv_scale, step.scale, step.found_inf,
+                                                step.step_count, *step.hyper,
+                                                fp8_eps=step.fp8_eps, stream=stream)
+        elif args.clip is None:
             A.amp_adamw_master_step(step.L_master, step.L_m, step.L_v, step.L_g, step.L_b,
                                     step.scale, step.found_inf, step.step_count, *step.hyper,
                                     amax=amax, stream=stream)
@@ -211,15 +225,22 @@ def run_ours(args, rank, world, device):
                                          stream=stream)
         if ev is not None:
             ev[2].record(stream)
-        if step.n_fp8:
+        if step.n_fp8 and not delayed:
             A.fp8_quant_tensorwise_list(step.L_x8, step.L_q, step.L_qt, "e4m3fn", step.amax,
                                         step.inv_scale, eps=step.fp8_eps,
                                         skip_if=step.found_inf, stream=stream)
         if ev is not None:
             ev[3].record(stream)
-        A.amp_update_scale(step.scale, step.growth_tracker, step.found_inf, step.growth,
-                           step.backoff, step.interval, amax=step.amax if step.n_fp8 else None,
-                           n_amax=step.n_fp8, stream=stream)
+        if delayed:
+            A.amp_update_scale_fp8_history(step.scale, step.growth_tracker, step.found_inf,
+                                           step.growth, step.backoff, step.interval, step.amax,
+                                           step.amax_history, step.n_fp8, step.hist_len,
+                                           stream=stream)
+        else:
+            A.amp_update_scale(step.scale, step.growth_tracker, step.found_inf, step.growth,
+                               step.backoff, step.interval,
+                               amax=step.amax if step.n_fp8 else None, n_amax=step.n_fp8,
+                               stream=stream)
         if ev is not None:
             ev[4].record(stream)
 
@@ -279,11 +300,13 @@ def run_ours(args, rank, world, device):
         "config": dict(workload_config(args.workload, world), per_step_bytes=total_bytes),
         "hbm_gbs_step": total_bytes / (ms_step * 1e-3) / 1e9,
         "grad_clip": args.clip,
+        "fp8_scaling": step.fp8_scaling,
         "kernels_ms": {"unscale_check": statistics.mean(k_check),
                        "adamw_master_step": adamw_ms,
                        "fp8_quant_list": statistics.mean(k_quant)},
         "fp8_quant_gbs": (info["bytes_quant"] / (statistics.mean(k_quant) * 1e-3) / 1e9)
         if info["bytes_quant"] else None,
+        "adamw_gbs": info["bytes_adamw"] / (statistics.mean(k_adamw) * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "kernel": "amp_adamw_master_step",
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
@@ -522,6 +545,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--fp8-scaling", default="dynamic", choices=["dynamic", "delayed"],
+                    help="FP8 weight scaling: this step's amax (a separate cast pass) or the "
+                         "previous step's (cast fused into the AdamW pass)")
     ap.add_argument("--clip", type=float, default=None,
                     help="also clip the unscaled gradients to this global L2 norm")
     args = ap.parse_args()

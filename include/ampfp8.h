@@ -267,6 +267,44 @@ amp_status fp8_quant_tensorwise_list(amp_tensor_list x, amp_tensor_list out,
                                      const float *amax_dev, float *inv_scale_dev,
                                      const int32_t *skip_if_dev, amp_stream_t stream);
 
+/* Delayed FP8 scaling fused into the update ("第20章 量化与混合精度训练"
+ * §20.5.9: each FP8 op keeps an amax history and casts with the scale of the
+ * previous steps' amax; §20.5.31 ScalingStrategy.DELAYED).  The pages have no
+ * fused form: with the scale known before the pass, the FP8 weights' update,
+ * bf16 copy, FP8 bytes and transposed FP8 bytes come out of one pass (30
+ * bytes per parameter instead of 28 + 4 over two passes).
+ * One optimizer step over two groups of tensors that share the step counter:
+ *   plain group  - 1-D lists master, exp_avg, exp_avg_sq, grads, bf16_out:
+ *                  exactly amp_adamw_master_step (no amax slots);
+ *   FP8 group    - 2-D lists master8, exp_avg8, exp_avg_sq8, grads8, bf16_out8
+ *                  and fp8_out (all with one shape set), fp8_t_out (the
+ *                  transposed shapes, or NULL): the same update and bf16
+ *                  copy, and per tensor j, in the same pass,
+ *        amax_h  = max over amax_history[j*hist_len .. j*hist_len+hist_len)
+ *                  (NaN propagating; newest first, see below)
+ *        scale_d = fp8_max / max(double(amax_h), eps)              (fp64)
+ *        fp8_out[j] = fp8(clamp(float(bf16) * float(scale_d), +-fp8_max)),
+ *                  fp8_t_out[j] its [cols, rows] copy, RNE, NaN -> 0x7F/0x7E
+ *        inv_scale_dev[j] = float(1 / scale_d)
+ *        amax_dev[j] = max(amax_dev[j], max |bf16 of tensor j|)  (the caller
+ *                  zeroes amax_dev; amp_update_scale_fp8_history does)
+ * On a skipped step (*found_inf_dev != 0) nothing is written, inv_scale
+ * included, and *step_dev is unchanged.  Either group may be empty (n = 0).
+ * grads and grads8 share one dtype (f16, bf16 or f32); fp8_dtype is
+ * AMP_DT_E4M3FN or AMP_DT_E5M2; eps > 0; hist_len >= 1.  The per-tensor scales
+ * live in fp8_out's device block between the two launches of the call: calls
+ * on one fp8_out list must not overlap on the GPU.
+ * Errors: AMP_EINVAL (NULL / mismatched lists, hist_len < 1, eps <= 0),
+ * AMP_EDTYPE. */
+amp_status amp_adamw_master_step_fp8_delayed(
+    amp_tensor_list master, amp_tensor_list exp_avg, amp_tensor_list exp_avg_sq,
+    amp_tensor_list grads, amp_tensor_list bf16_out, amp_tensor_list master8,
+    amp_tensor_list exp_avg8, amp_tensor_list exp_avg_sq8, amp_tensor_list grads8,
+    amp_tensor_list bf16_out8, amp_tensor_list fp8_out, amp_tensor_list fp8_t_out,
+    amp_dtype fp8_dtype, double eps, const float *amax_history, int hist_len, float *amax_dev,
+    float *inv_scale_dev, const float *scale_dev, const int32_t *found_inf_dev,
+    int32_t *step_dev, const amp_adamw_hyper *hyper, amp_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* A3: dynamic loss-scale state machine.  [CH20] §20.5.33, [MP06] §四.        */
 /* ------------------------------------------------------------------------ */
@@ -283,6 +321,19 @@ amp_status amp_update_scale(float *scale_dev, int32_t *growth_tracker_dev,
                             int32_t *found_inf_dev, float growth_factor, float backoff_factor,
                             int32_t growth_interval, float *amax_dev, int n_amax,
                             amp_stream_t stream);
+
+/* amp_update_scale for the delayed-scaling step: the same state machine, and
+ * when the step was not skipped (*found_inf_dev == 0 on entry) each FP8
+ * tensor's amax of this step enters its history row of hist_len floats at
+ * position 0, the older entries moving up by one and the oldest dropped.
+ * amax_dev[0 .. n_fp8) and *found_inf_dev are cleared in every case.
+ * Errors: as amp_update_scale, plus AMP_EINVAL for hist_len < 1 or NULL
+ * amax / history with n_fp8 > 0. */
+amp_status amp_update_scale_fp8_history(float *scale_dev, int32_t *growth_tracker_dev,
+                                        int32_t *found_inf_dev, float growth_factor,
+                                        float backoff_factor, int32_t growth_interval,
+                                        float *amax_dev, float *amax_history, int n_fp8,
+                                        int hist_len, amp_stream_t stream);
 
 /* Message describing the last non-OK status returned on this thread. */
 const char *amp_last_error(void);

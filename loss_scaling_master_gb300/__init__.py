@@ -6,7 +6,8 @@ The compute lives in libampfp8.so (hand-written CUDA for sm_103a, C ABI in
 include/ampfp8.h); this package is its thin ctypes binding.
 """
 from ._lib import (AmpError, TensorList, amp_abi_version, amp_adamw_master_step,
-                   amp_adamw_master_step_clip, amp_adamw_master_step_noalloc, amp_last_error,
+                   amp_adamw_master_step_clip, amp_adamw_master_step_fp8_delayed,
+                   amp_adamw_master_step_noalloc, amp_last_error, amp_update_scale_fp8_history,
                    amp_unscale_check_norm, amp_tensor_list_create, amp_tensor_list_destroy,
                    amp_tensor_list_set_amax_slots, amp_unscale_check, amp_update_scale,
                    fp8_quant_tensorwise, fp8_quant_tensorwise_list, load)
@@ -16,5 +17,6 @@ __all__ = ["AmpError", "TensorList", "AmpOptimizerStep", "load", "amp_abi_versio
            "amp_last_error", "amp_tensor_list_create", "amp_tensor_list_destroy",
            "amp_tensor_list_set_amax_slots", "amp_unscale_check", "amp_adamw_master_step",
            "amp_adamw_master_step_noalloc", "amp_adamw_master_step_clip",
-           "amp_unscale_check_norm",
+           "amp_unscale_check_norm", "amp_adamw_master_step_fp8_delayed",
+           "amp_update_scale_fp8_history",
            "fp8_quant_tensorwise", "fp8_quant_tensorwise_list", "amp_update_scale"]

@@ -27,6 +27,7 @@ _TORCH_DT = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16",
 EXPORTS = ("amp_tensor_list_create", "amp_tensor_list_set_amax_slots", "amp_tensor_list_destroy",
            "amp_unscale_check", "amp_unscale_check_norm", "amp_adamw_master_step",
            "amp_adamw_master_step_clip", "amp_adamw_master_step_noalloc",
+           "amp_adamw_master_step_fp8_delayed", "amp_update_scale_fp8_history",
            "fp8_quant_tensorwise", "fp8_quant_tensorwise_list", "amp_update_scale",
            "amp_last_error", "amp_abi_version")
 
@@ -69,6 +70,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                                  ctypes.POINTER(amp_adamw_hyper), P, P, dbl, P]
         L.amp_adamw_master_step_noalloc.argtypes = [i32, P, P, P, P, i32, P, P, P, P, P, P,
                                                     ctypes.POINTER(amp_adamw_hyper), P, P]
+        L.amp_adamw_master_step_fp8_delayed.argtypes = [P] * 12 + [i32, dbl, P, i32, P, P, P, P,
+                                                                  P, ctypes.POINTER(amp_adamw_hyper),
+                                                                  P]
+        L.amp_update_scale_fp8_history.argtypes = [P, P, P, flt, flt, ctypes.c_int32, P, P, i32,
+                                                   i32, P]
         L.fp8_quant_tensorwise.argtypes = [P, i32, i64, i64, i32, dbl, P, P, P, P, i32, P, P]
         L.fp8_quant_tensorwise_list.argtypes = [P, P, P, i32, dbl, P, P, P, P]
         L.amp_update_scale.argtypes = [P, P, P, flt, flt, ctypes.c_int32, P, i32, P]
@@ -218,6 +224,34 @@ def amp_adamw_master_step_noalloc(master, exp_avg, exp_avg_sq, grads, bf16_out, 
                DT[dtype_name(grads[0])] if n else DT["f32"],
                arr(bf16_out) if bf16_out is not None else None, numel, slots, _dptr(scale),
                _dptr(found_inf), _dptr(step), ctypes.byref(h), _dptr(amax), _stream(stream)))
+
+
+def amp_adamw_master_step_fp8_delayed(plain, fp8_group, fp8_out: TensorList,
+                                      fp8_t_out: TensorList | None, fp8_dtype: str,
+                                      amax_history, hist_len: int, amax, inv_scale, scale,
+                                      found_inf, step, lr: float, beta1: float, beta2: float,
+                                      eps: float, weight_decay: float, fp8_eps: float = 1e-12,
+                                      stream=None):
+    """plain / fp8_group: (master, exp_avg, exp_avg_sq, grads, bf16_out) TensorLists;
+    the FP8 group's lists are 2-D."""
+    h = amp_adamw_hyper(lr, beta1, beta2, eps, weight_decay)
+    _check("amp_adamw_master_step_fp8_delayed",
+           load().amp_adamw_master_step_fp8_delayed(
+               *[x.handle for x in plain], *[x.handle for x in fp8_group], fp8_out.handle,
+               fp8_t_out.handle if fp8_t_out else None, DT[fp8_dtype], fp8_eps,
+               _dptr(amax_history), int(hist_len), _dptr(amax), _dptr(inv_scale), _dptr(scale),
+               _dptr(found_inf), _dptr(step), ctypes.byref(h), _stream(stream)))
+
+
+def amp_update_scale_fp8_history(scale, growth_tracker, found_inf, growth_factor: float,
+                                 backoff_factor: float, growth_interval: int, amax,
+                                 amax_history, n_fp8: int, hist_len: int, stream=None):
+    _check("amp_update_scale_fp8_history",
+           load().amp_update_scale_fp8_history(_dptr(scale), _dptr(growth_tracker),
+                                               _dptr(found_inf), growth_factor, backoff_factor,
+                                               int(growth_interval), _dptr(amax),
+                                               _dptr(amax_history), int(n_fp8), int(hist_len),
+                                               _stream(stream)))
 
 
 def fp8_quant_tensorwise(x: torch.Tensor, fp8_dtype: str, out: torch.Tensor, out_t, inv_scale,

@@ -16,6 +16,7 @@
 //             once, otherwise every thread streams groups of 8 elements with
 //             16-byte loads/stores: 14 bytes read + 14 bytes written per
 //             parameter (fp16/bf16 grads, bf16 emission).
+#include "fp8_tile.cuh"
 #include "internal.h"
 
 namespace amp {
@@ -86,9 +87,9 @@ __device__ __forceinline__ void u4_set(uint4 &w, int j, float f) {
 }
 
 template <int GT, bool BF16>
-__device__ __forceinline__ void compute_store_group(Group<GT> &r, float *pp, float *mp, float *vp,
-                                                    uint16_t *bp, int64_t e, const Scal &s,
-                                                    uint32_t &amax2) {
+__device__ __forceinline__ uint4 compute_store_group(Group<GT> &r, float *pp, float *mp, float *vp,
+                                                     uint16_t *bp, int64_t e, const Scal &s,
+                                                     uint32_t &amax2) {
     float p[8], m[8], v[8], g[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -130,13 +131,15 @@ __device__ __forceinline__ void compute_store_group(Group<GT> &r, float *pp, flo
         st_g(bp + e, o);
         amax2 = __vmaxu2(amax2, __vmaxu2(__vmaxu2(o.x & 0x7FFF7FFFu, o.y & 0x7FFF7FFFu),
                                          __vmaxu2(o.z & 0x7FFF7FFFu, o.w & 0x7FFF7FFFu)));
+        return o;
     }
+    return make_uint4(0u, 0u, 0u, 0u);
 }
 
 template <int GT, bool BF16>
-__device__ __forceinline__ void scalar_elem(float *pp, float *mp, float *vp, const void *gp,
-                                            uint16_t *bp, int64_t k, const Scal &s,
-                                            uint32_t &amax1) {
+__device__ __forceinline__ uint16_t scalar_elem(float *pp, float *mp, float *vp, const void *gp,
+                                                uint16_t *bp, int64_t k, const Scal &s,
+                                                uint32_t &amax1) {
     float p = pp[k], m = mp[k], v = vp[k];
     adamw_elem(p, m, v, grad_at<GT>(gp, k), s);
     pp[k] = p;
@@ -146,7 +149,9 @@ __device__ __forceinline__ void scalar_elem(float *pp, float *mp, float *vp, con
         const uint16_t b = f32_to_bf16(p);
         bp[k] = b;
         amax1 = max(amax1, uint32_t(b & 0x7FFFu));
+        return b;
     }
+    return 0;
 }
 
 template <int GT, bool BF16>
@@ -214,9 +219,12 @@ __global__ void __launch_bounds__(kThreads) adamw_main_kernel(AdamwParams P) {
     }
 }
 
-__global__ void adamw_prologue_kernel(const int32_t *found_inf, int32_t *step, double lr,
-                                      double beta1, double beta2, const double *clip_sumsq,
-                                      double max_norm, AdamwStepScalars *out) {
+// Per-step scalars: skip flag, bias corrections (fp64, rounded once), clip
+// factor; advances the step counter when the step is not skipped.
+__device__ __forceinline__ AdamwStepScalars step_scalars(const int32_t *found_inf, int32_t *step,
+                                                         double lr, double beta1, double beta2,
+                                                         const double *clip_sumsq,
+                                                         double max_norm) {
     AdamwStepScalars s;
     s.skip = found_inf ? (*found_inf != 0) : 0;
     s.step_size = 0.0f;
@@ -235,7 +243,130 @@ __global__ void adamw_prologue_kernel(const int32_t *found_inf, int32_t *step, d
         s.bc2_sqrt = float(sqrt(bc2));
         *step = t;
     }
-    *out = s;
+    return s;
+}
+
+__global__ void adamw_prologue_kernel(const int32_t *found_inf, int32_t *step, double lr,
+                                      double beta1, double beta2, const double *clip_sumsq,
+                                      double max_norm, AdamwStepScalars *out) {
+    *out = step_scalars(found_inf, step, lr, beta1, beta2, clip_sumsq, max_norm);
+}
+
+// ---------------------------------------------------------------------------
+// AdamW + BF16 + FP8 with delayed scaling ("第20章 量化与混合精度训练" §20.5.9:
+// each FP8 op keeps an amax history and casts with the scale of the previous
+// steps' amax).  The scale is known before the pass, so the FP8 bytes and
+// their transposed copy come out of the same pass as the update: 30 bytes per
+// parameter for the FP8 weights instead of 28 + 4 in two passes.
+// ---------------------------------------------------------------------------
+struct Fp8StepParams {
+    ListView p, m, v, g, b, q, qt;
+    int has_t;
+    const float *scale;
+    const AdamwStepScalars *scal;
+    const float *tscale;  // per tensor: the fp32 cast scale from the history
+    float *amax;          // per tensor: max|bf16| of this step, for the history
+    float decay, b1, omb1, b2, omb2, eps;
+};
+
+// One CTA: thread 0 the step scalars; every thread a strided share of the
+// FP8 tensors' scales from their amax histories (NaN propagating max).
+__global__ void adamw_fp8_prologue_kernel(const int32_t *found_inf, int32_t *step, double lr,
+                                          double beta1, double beta2, AdamwStepScalars *out,
+                                          const float *hist, int hist_len, int n8, double eps,
+                                          float fmax, float *tscale, float *inv_scale) {
+    const int skip = found_inf ? (*found_inf != 0) : 0;
+    __syncthreads();  // every thread has read found_inf before thread 0 goes on
+    if (threadIdx.x == 0) *out = step_scalars(found_inf, step, lr, beta1, beta2, nullptr, 0.0);
+    if (skip) return;
+    for (int j = threadIdx.x; j < n8; j += blockDim.x) {
+        const float *h = hist + int64_t(j) * hist_len;
+        float a = h[0];
+        for (int k = 1; k < hist_len; ++k) a = (a != a || h[k] != h[k]) ? __int_as_float(0x7FC00000) : fmaxf(a, h[k]);
+        float s32, inv;
+        tensor_scale(a, eps, fmax, s32, inv);
+        tscale[j] = s32;
+        inv_scale[j] = inv;
+    }
+}
+
+template <int GT, int FT>
+__global__ void __launch_bounds__(kThreads) adamw_fp8_tile_kernel(Fp8StepParams P) {
+    const AdamwStepScalars sc = *P.scal;
+    if (sc.skip) return;
+    __shared__ __align__(16) uint32_t sm[kTile * 32];
+    const uint2 tl = P.p.tiles[blockIdx.x];
+    const int t = int(tl.x);
+    const int64_t rows = P.p.rows[t], cols = P.p.cols[t];
+    const int64_t tiles_c = (cols + kTile - 1) / kTile;
+    const int64_t r0 = int64_t(tl.y / tiles_c) * kTile, c0 = int64_t(tl.y % tiles_c) * kTile;
+    float *pp = static_cast<float *>(P.p.ptrs[t]);
+    float *mp = static_cast<float *>(P.m.ptrs[t]);
+    float *vp = static_cast<float *>(P.v.ptrs[t]);
+    const void *gp = P.g.ptrs[t];
+    uint16_t *bp = static_cast<uint16_t *>(P.b.ptrs[t]);
+    uint8_t *qp = static_cast<uint8_t *>(P.q.ptrs[t]);
+    uint8_t *qtp = P.has_t ? static_cast<uint8_t *>(P.qt.ptrs[t]) : nullptr;
+
+    Scal s;
+    s.r = P.scale ? __fdiv_rn(1.0f, *P.scale) : 1.0f;
+    s.clip = sc.clip;
+    s.decay = P.decay;
+    s.b1 = P.b1;
+    s.omb1 = P.omb1;
+    s.b2 = P.b2;
+    s.omb2 = P.omb2;
+    s.eps = P.eps;
+    s.step_size = sc.step_size;
+    s.c2 = sc.bc2_sqrt;
+    const float s32 = P.tscale[t];
+
+    uint32_t amax2 = 0, amax1 = 0;
+    const bool fast = r0 + kTile <= rows && c0 + kTile <= cols && (cols & 7) == 0 &&
+                      aligned16(pp) && aligned16(mp) && aligned16(vp) && aligned16(gp) &&
+                      aligned16(bp) && (reinterpret_cast<uintptr_t>(qp) & 7) == 0 &&
+                      (qtp == nullptr || ((rows & 15) == 0 && aligned16(qtp)));
+    if (fast) {
+        const int c8 = threadIdx.x & 15, rb = threadIdx.x >> 4;
+#pragma unroll 1
+        for (int k = 0; k < 8; k += 2) {
+            const int ra = rb + 16 * k, rbb = rb + 16 * (k + 1);
+            const int64_t ea = (r0 + ra) * cols + c0 + 8 * c8;
+            const int64_t eb = (r0 + rbb) * cols + c0 + 8 * c8;
+            Group<GT> a, b;
+            load_group<GT>(a, pp, mp, vp, gp, ea);
+            load_group<GT>(b, pp, mp, vp, gp, eb);
+            const uint4 oa = compute_store_group<GT, true>(a, pp, mp, vp, bp, ea, s, amax2);
+            const uint4 ob = compute_store_group<GT, true>(b, pp, mp, vp, bp, eb, s, amax2);
+            const uint2 qa = bf16x8_to_fp8x8<FT>(oa, s32);
+            const uint2 qb = bf16x8_to_fp8x8<FT>(ob, s32);
+            *reinterpret_cast<uint2 *>(qp + ea) = qa;
+            *reinterpret_cast<uint2 *>(qp + eb) = qb;
+            if (qtp) {
+                *reinterpret_cast<uint2 *>(sm + swz(ra, 2 * c8)) = qa;
+                *reinterpret_cast<uint2 *>(sm + swz(rbb, 2 * c8)) = qb;
+            }
+        }
+        if (qtp) {
+            __syncthreads();
+            store_transposed_tile(sm, qtp, rows, r0, c0);
+        }
+    } else {
+        for (int idx = threadIdx.x; idx < kTile * kTile; idx += kThreads) {
+            const int64_t i = r0 + (idx >> 7), j = c0 + (idx & (kTile - 1));
+            if (i < rows && j < cols) {
+                const int64_t e = i * cols + j;
+                const uint16_t bv = scalar_elem<GT, true>(pp, mp, vp, gp, bp, e, s, amax1);
+                const uint8_t q8 = quant1<FT>(bf16_bits_to_f32(bv), s32);
+                qp[e] = q8;
+                if (qtp) qtp[j * rows + i] = q8;
+            }
+        }
+    }
+    uint32_t a = max(max(amax2 & 0xFFFFu, amax2 >> 16), amax1);
+    a = warp_max_u32(a);
+    if ((threadIdx.x & 31) == 0 && a != 0)
+        atomicMax(reinterpret_cast<unsigned int *>(P.amax) + t, a << 16);
 }
 
 }  // namespace
@@ -249,7 +380,16 @@ cudaError_t launch_adamw(const ListView &p, const ListView &m, const ListView &v
     adamw_prologue_kernel<<<1, 1, 0, s>>>(found_inf, step, c.lr, c.beta1, c.beta2, clip_sumsq,
                                           max_norm, scal);
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || n_chunks == 0) return e;
+    if (e != cudaSuccess) return e;
+    return launch_adamw_main(p, m, v, g, b, n_chunks, gelem, scale, c, scal, amax, use_slots, s);
+}
+
+cudaError_t launch_adamw_main(const ListView &p, const ListView &m, const ListView &v,
+                              const ListView &g, const ListView *b, int64_t n_chunks, int gelem,
+                              const float *scale, const AdamwConsts &c,
+                              const AdamwStepScalars *scal, float *amax, bool use_slots,
+                              cudaStream_t s) {
+    if (n_chunks == 0) return cudaSuccess;
     AdamwParams P;
     P.p = p;
     P.m = m;
@@ -277,6 +417,55 @@ cudaError_t launch_adamw(const ListView &p, const ListView &m, const ListView &v
     else if (gelem == kF16) AMP_ADAMW_LAUNCH(kF16);
     else AMP_ADAMW_LAUNCH(kBF16);
 #undef AMP_ADAMW_LAUNCH
+    return cudaGetLastError();
+}
+
+cudaError_t launch_adamw_fp8_delayed(const Fp8DelayedLists &L, int gelem, int fp8,
+                                     const float *scale, const int32_t *found_inf, int32_t *step,
+                                     const AdamwConsts &c, AdamwStepScalars *scal,
+                                     const float *hist, int hist_len, double eps, float *amax,
+                                     float *inv_scale, cudaStream_t s) {
+    const float fmax = fp8 == kE4M3 ? fp8_max<kE4M3>() : fp8_max<kE5M2>();
+    adamw_fp8_prologue_kernel<<<1, 256, 0, s>>>(found_inf, step, c.lr, c.beta1, c.beta2, scal,
+                                                hist, hist_len, L.n8, eps, fmax, L.tscale,
+                                                inv_scale);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (L.n_plain_chunks > 0) {
+        e = launch_adamw_main(L.p, L.m, L.v, L.g, &L.b, L.n_plain_chunks, gelem, scale, c, scal,
+                              nullptr, false, s);
+        if (e != cudaSuccess) return e;
+    }
+    if (L.n_tiles == 0) return cudaSuccess;
+    Fp8StepParams P;
+    P.p = L.p8;
+    P.m = L.m8;
+    P.v = L.v8;
+    P.g = L.g8;
+    P.b = L.b8;
+    P.q = L.q;
+    P.qt = L.qt ? *L.qt : ListView{};
+    P.has_t = L.qt != nullptr;
+    P.scale = scale;
+    P.scal = scal;
+    P.tscale = L.tscale;
+    P.amax = amax;
+    P.decay = c.decay;
+    P.b1 = c.b1;
+    P.omb1 = c.omb1;
+    P.b2 = c.b2;
+    P.omb2 = c.omb2;
+    P.eps = c.eps;
+    const dim3 grid((unsigned)L.n_tiles), block(kThreads);
+#define AMP_FP8_LAUNCH(GT)                                                            \
+    do {                                                                              \
+        if (fp8 == kE4M3) adamw_fp8_tile_kernel<GT, kE4M3><<<grid, block, 0, s>>>(P); \
+        else adamw_fp8_tile_kernel<GT, kE5M2><<<grid, block, 0, s>>>(P);              \
+    } while (0)
+    if (gelem == kF32) AMP_FP8_LAUNCH(kF32);
+    else if (gelem == kF16) AMP_FP8_LAUNCH(kF16);
+    else AMP_FP8_LAUNCH(kBF16);
+#undef AMP_FP8_LAUNCH
     return cudaGetLastError();
 }
 

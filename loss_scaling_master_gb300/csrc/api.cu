@@ -80,7 +80,7 @@ extern "C" {
 
 const char *amp_last_error(void) { return g_err; }
 
-int amp_abi_version(void) { return 2; }
+int amp_abi_version(void) { return 3; }
 
 amp_status amp_tensor_list_create(int n, void *const *dev_ptrs, const int64_t *rows,
                                   const int64_t *cols, amp_dtype dtype, amp_stream_t stream,
@@ -141,7 +141,8 @@ amp_status amp_tensor_list_create(int n, void *const *dev_ptrs, const int64_t *r
     const size_t o_chunks = align_up(o_slots + nn * sizeof(int32_t));
     const size_t o_tiles = align_up(o_chunks + std::max<size_t>(1, chunks.size()) * sizeof(uint2));
     const size_t o_partials = align_up(o_tiles + std::max<size_t>(1, tiles.size()) * sizeof(uint2));
-    const size_t o_scratch = align_up(o_partials + std::max<size_t>(1, chunks.size()) * sizeof(double));
+    const size_t o_tscale = align_up(o_partials + std::max<size_t>(1, chunks.size()) * sizeof(double));
+    const size_t o_scratch = align_up(o_tscale + nn * sizeof(float));
     const size_t total = align_up(o_scratch + 256);
     std::vector<char> host(total, 0);
     std::memcpy(host.data() + o_ptrs, L->ptrs.data(), n * sizeof(void *));
@@ -184,6 +185,7 @@ amp_status amp_tensor_list_create(int n, void *const *dev_ptrs, const int64_t *r
     L->view.partials = reinterpret_cast<double *>(b + o_partials);
     L->view.n = n;
     L->scratch = b + o_scratch;
+    L->tscale = reinterpret_cast<float *>(b + o_tscale);
     *out = L;
     return AMP_OK;
 }
@@ -285,6 +287,92 @@ amp_status amp_adamw_master_step_clip(amp_tensor_list master, amp_tensor_list ex
         return fail(AMP_EINVAL, "amp_adamw_master_step_clip: max_norm must be finite and > 0");
     return adamw_entry(master, exp_avg, exp_avg_sq, grads, bf16_out, scale_dev, found_inf_dev,
                        step_dev, hyper, amax_dev, grad_sumsq_dev, max_norm, stream);
+}
+
+amp_status amp_adamw_master_step_fp8_delayed(
+    amp_tensor_list master, amp_tensor_list exp_avg, amp_tensor_list exp_avg_sq,
+    amp_tensor_list grads, amp_tensor_list bf16_out, amp_tensor_list master8,
+    amp_tensor_list exp_avg8, amp_tensor_list exp_avg_sq8, amp_tensor_list grads8,
+    amp_tensor_list bf16_out8, amp_tensor_list fp8_out, amp_tensor_list fp8_t_out,
+    amp_dtype fp8_dtype, double eps, const float *amax_history, int hist_len, float *amax_dev,
+    float *inv_scale_dev, const float *scale_dev, const int32_t *found_inf_dev, int32_t *step_dev,
+    const amp_adamw_hyper *hyper, amp_stream_t stream) {
+    const char *fn = "amp_adamw_master_step_fp8_delayed";
+    if (!master || !exp_avg || !exp_avg_sq || !grads || !bf16_out || !master8 || !exp_avg8 ||
+        !exp_avg_sq8 || !grads8 || !bf16_out8 || !fp8_out || !amax_history || !amax_dev ||
+        !inv_scale_dev || !step_dev || !hyper)
+        return fail(AMP_EINVAL, "%s: NULL argument", fn);
+    if (hist_len < 1) return fail(AMP_EINVAL, "%s: hist_len < 1", fn);
+    if (!(eps > 0.0)) return fail(AMP_EINVAL, "%s: eps must be > 0", fn);
+    const int fc = fp8_code(fp8_dtype);
+    const int gc = elem_code(grads->dtype);
+    if (fc < 0 || gc < 0 || grads8->dtype != grads->dtype)
+        return fail(AMP_EDTYPE, "%s: unsupported or mixed gradient / fp8 dtype", fn);
+    for (amp_tensor_list l : {master, exp_avg, exp_avg_sq, master8, exp_avg8, exp_avg_sq8})
+        if (l->dtype != AMP_DT_F32) return fail(AMP_EDTYPE, "%s: master/m/v must be f32", fn);
+    if (bf16_out->dtype != AMP_DT_BF16 || bf16_out8->dtype != AMP_DT_BF16 ||
+        fp8_out->dtype != fp8_dtype || (fp8_t_out && fp8_t_out->dtype != fp8_dtype))
+        return fail(AMP_EDTYPE, "%s: bf16 / fp8 output dtypes", fn);
+    if (!same_shapes(master, exp_avg) || !same_shapes(master, exp_avg_sq) ||
+        !same_shapes(master, grads) || !same_shapes(master, bf16_out))
+        return fail(AMP_EINVAL, "%s: plain lists differ in tensor count or sizes", fn);
+    for (amp_tensor_list l : {master8, exp_avg8, exp_avg_sq8, grads8, bf16_out8, fp8_out})
+        if (!l->two_d || l->n != fp8_out->n || l->rows != fp8_out->rows || l->cols != fp8_out->cols)
+            return fail(AMP_EINVAL, "%s: FP8-weight lists must be 2-D with one shape set", fn);
+    if (fp8_t_out && (!fp8_t_out->two_d || fp8_t_out->n != fp8_out->n ||
+                      fp8_t_out->rows != fp8_out->cols || fp8_t_out->cols != fp8_out->rows))
+        return fail(AMP_EINVAL, "%s: fp8_t_out shapes are not the FP8 weights transposed", fn);
+    const amp_adamw_hyper &h = *hyper;
+    amp::AdamwConsts c;
+    c.lr = h.lr;
+    c.beta1 = h.beta1;
+    c.beta2 = h.beta2;
+    c.decay = float(1.0 - h.lr * h.weight_decay);
+    c.b1 = float(h.beta1);
+    c.omb1 = float(1.0 - h.beta1);
+    c.b2 = float(h.beta2);
+    c.omb2 = float(1.0 - h.beta2);
+    c.eps = float(h.eps);
+    amp::Fp8DelayedLists L;
+    L.p = master->view;
+    L.m = exp_avg->view;
+    L.v = exp_avg_sq->view;
+    L.g = grads->view;
+    L.b = bf16_out->view;
+    L.n_plain_chunks = master->n_chunks;
+    L.p8 = master8->view;
+    L.m8 = exp_avg8->view;
+    L.v8 = exp_avg_sq8->view;
+    L.g8 = grads8->view;
+    L.b8 = bf16_out8->view;
+    L.q = fp8_out->view;
+    L.qt = fp8_t_out ? &fp8_t_out->view : nullptr;
+    L.n_tiles = master8->n_tiles;
+    L.n8 = fp8_out->n;
+    L.tscale = fp8_out->tscale;
+    cudaError_t e = amp::launch_adamw_fp8_delayed(
+        L, gc, fc, scale_dev, found_inf_dev, step_dev, c,
+        reinterpret_cast<amp::AdamwStepScalars *>(fp8_out->scratch), amax_history, hist_len, eps,
+        amax_dev, inv_scale_dev, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AMP_OK : cuda_fail(e, fn);
+}
+
+amp_status amp_update_scale_fp8_history(float *scale_dev, int32_t *growth_tracker_dev,
+                                        int32_t *found_inf_dev, float growth_factor,
+                                        float backoff_factor, int32_t growth_interval,
+                                        float *amax_dev, float *amax_history, int n_fp8,
+                                        int hist_len, amp_stream_t stream) {
+    const char *fn = "amp_update_scale_fp8_history";
+    if (!scale_dev || !growth_tracker_dev || !found_inf_dev)
+        return fail(AMP_EINVAL, "%s: NULL state pointer", fn);
+    if (growth_interval < 1) return fail(AMP_EINVAL, "%s: growth_interval < 1", fn);
+    if (n_fp8 < 0 || hist_len < 1 || (n_fp8 > 0 && (!amax_dev || !amax_history)))
+        return fail(AMP_EINVAL, "%s: bad amax / history arguments", fn);
+    cudaError_t e = amp::launch_update_scale_hist(scale_dev, growth_tracker_dev, found_inf_dev,
+                                                  growth_factor, backoff_factor, growth_interval,
+                                                  amax_dev, amax_history, n_fp8, hist_len,
+                                                  reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AMP_OK : cuda_fail(e, fn);
 }
 
 amp_status amp_unscale_check_norm(amp_tensor_list grads, const float *scale_dev,

@@ -22,6 +22,7 @@
 // take an element-wise path with the same arithmetic.
 #include <algorithm>
 
+#include "fp8_tile.cuh"
 #include "internal.h"
 
 namespace amp {
@@ -32,25 +33,6 @@ __device__ __forceinline__ float x_at(const void *x, int64_t k) {
     if (XT == kF32) return static_cast<const float *>(x)[k];
     return lowp_to_f32<XT>(static_cast<const uint16_t *>(x)[k]);
 }
-
-// scale_d = fp8_max / max(double(amax), eps) with NaN propagating.
-__device__ __forceinline__ void tensor_scale(float amax, double eps, float fmax, float &s32,
-                                             float &inv) {
-    const double a = double(amax);
-    const double cl = (a != a) ? a : (a < eps ? eps : a);
-    const double sd = double(fmax) / cl;
-    s32 = float(sd);
-    inv = float(1.0 / sd);
-}
-
-template <int FT>
-__device__ __forceinline__ uint8_t quant1(float x, float s32) {
-    return uint8_t(f32x2_to_fp8x2<FT>(__fmul_rn(x, s32), 0.0f) & 0xFFu);
-}
-
-// 4-byte word (row r, word w) of the 128x128 byte tile, XOR-swizzled so that
-// the transposed read pattern hits 32 distinct banks.
-__device__ __forceinline__ int swz(int r, int w) { return r * 32 + (w ^ (((r >> 4) & 7) << 2)); }
 
 template <int XT, int FT>
 __device__ __forceinline__ void quant_tile(const void *x, int64_t rows, int64_t cols, uint8_t *out,
@@ -103,28 +85,7 @@ __device__ __forceinline__ void quant_tile(const void *x, int64_t rows, int64_t 
         }
         if (out_t == nullptr) return;
         __syncthreads();
-        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-        const int rg = lane & 7, wq = (lane >> 3) + 4 * warp;
-        uint32_t wv[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) wv[i] = sm[(16 * rg + i) * 32 + (wq ^ (rg << 2))];
-        uint32_t col[4][4];  // col[j][blk]: rows 4blk..4blk+3 of column 4wq+j
-#pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {
-            const uint32_t a = wv[4 * blk], b = wv[4 * blk + 1], c = wv[4 * blk + 2],
-                           d = wv[4 * blk + 3];
-            const uint32_t t0 = __byte_perm(a, b, 0x5140), t1 = __byte_perm(a, b, 0x7362);
-            const uint32_t t2 = __byte_perm(c, d, 0x5140), t3 = __byte_perm(c, d, 0x7362);
-            col[0][blk] = __byte_perm(t0, t2, 0x5410);
-            col[1][blk] = __byte_perm(t0, t2, 0x7632);
-            col[2][blk] = __byte_perm(t1, t3, 0x5410);
-            col[3][blk] = __byte_perm(t1, t3, 0x7632);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int64_t dst = (c0 + 4 * wq + j) * rows + r0 + 16 * rg;
-            st_g(out_t + dst, make_uint4(col[j][0], col[j][1], col[j][2], col[j][3]));
-        }
+        store_transposed_tile(sm, out_t, rows, r0, c0);
     } else {
         __syncthreads();
         const float s32 = *s_scale;

@@ -1,0 +1,77 @@
+// fp8_tile.cuh - pieces of the tensorwise FP8 cast shared by the standalone
+// quantizer and the fused AdamW + FP8 step ("FP8训练：量化、自动微分、Torchao"
+// §2 scale and cast, §4 column-major copy).
+#pragma once
+
+#include "common.cuh"
+
+namespace amp {
+
+// scale_d = fp8_max / max(double(amax), eps), NaN propagating; the cast uses
+// scale_d rounded to fp32, inv_scale is 1/scale_d rounded to fp32.
+__device__ __forceinline__ void tensor_scale(float amax, double eps, float fmax, float &s32,
+                                             float &inv) {
+    const double a = double(amax);
+    const double cl = (a != a) ? a : (a < eps ? eps : a);
+    const double sd = double(fmax) / cl;
+    s32 = float(sd);
+    inv = float(1.0 / sd);
+}
+
+template <int FT>
+__device__ __forceinline__ uint8_t quant1(float x, float s32) {
+    return uint8_t(f32x2_to_fp8x2<FT>(__fmul_rn(x, s32), 0.0f) & 0xFFu);
+}
+
+// Eight bf16 values (a 16-byte word group) -> eight fp8 bytes of x * s32.
+template <int FT>
+__device__ __forceinline__ uint2 bf16x8_to_fp8x8(const uint4 &b, float s32) {
+    const uint32_t w[4] = {b.x, b.y, b.z, b.w};
+    uint32_t h[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float lo = __fmul_rn(bf16_bits_to_f32(w[j] & 0xFFFFu), s32);
+        const float hi = __fmul_rn(bf16_bits_to_f32(w[j] >> 16), s32);
+        h[j] = f32x2_to_fp8x2<FT>(lo, hi);
+    }
+    return make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+}
+
+// 4-byte word (row r, word w) of a 128x128 byte tile in shared memory,
+// XOR-swizzled by 16-row band so the transposed read hits 32 distinct banks.
+__device__ __forceinline__ int swz(int r, int w) { return r * 32 + (w ^ (((r >> 4) & 7) << 2)); }
+
+// Write the transposed copy of a full 128x128 byte tile held in `sm` (filled
+// through swz) to out_t, which is [cols, rows] row-major: tile element
+// (i, j) goes to out_t[(c0 + j) * rows + r0 + i].  256 threads; each reads 16
+// words of one word-column (conflict-free), transposes 4x4 byte blocks with
+// byte permutes and writes four 16-byte stores; 8 lanes cover one 128-byte
+// segment of a transposed row.  Requires rows % 16 == 0 and a 16-byte aligned
+// out_t.
+__device__ __forceinline__ void store_transposed_tile(const uint32_t *sm, uint8_t *out_t,
+                                                      int64_t rows, int64_t r0, int64_t c0) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int rg = lane & 7, wq = (lane >> 3) + 4 * warp;
+    uint32_t wv[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) wv[i] = sm[(16 * rg + i) * 32 + (wq ^ (rg << 2))];
+    uint32_t col[4][4];  // col[j][blk]: rows 4blk..4blk+3 of column 4wq+j
+#pragma unroll
+    for (int blk = 0; blk < 4; ++blk) {
+        const uint32_t a = wv[4 * blk], b = wv[4 * blk + 1], c = wv[4 * blk + 2],
+                       d = wv[4 * blk + 3];
+        const uint32_t t0 = __byte_perm(a, b, 0x5140), t1 = __byte_perm(a, b, 0x7362);
+        const uint32_t t2 = __byte_perm(c, d, 0x5140), t3 = __byte_perm(c, d, 0x7362);
+        col[0][blk] = __byte_perm(t0, t2, 0x5410);
+        col[1][blk] = __byte_perm(t0, t2, 0x7632);
+        col[2][blk] = __byte_perm(t1, t3, 0x5410);
+        col[3][blk] = __byte_perm(t1, t3, 0x7632);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int64_t dst = (c0 + 4 * wq + j) * rows + r0 + 16 * rg;
+        st_g(out_t + dst, make_uint4(col[j][0], col[j][1], col[j][2], col[j][3]));
+    }
+}
+
+}  // namespace amp

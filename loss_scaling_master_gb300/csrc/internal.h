@@ -22,6 +22,7 @@ struct amp_tensor_list_s {
     bool has_slots = false;
     void *block = nullptr;   // the single device allocation
     void *scratch = nullptr; // 256 bytes of it for per-call kernel scalars
+    float *tscale = nullptr; // one float per tensor of it (per-call scratch)
     amp::ListView view{};    // pointers into `block`
 };
 
@@ -58,6 +59,34 @@ cudaError_t launch_adamw(const ListView &p, const ListView &m, const ListView &v
                          const AdamwConsts &c, AdamwStepScalars *scal, float *amax,
                          bool use_slots, cudaStream_t s, const double *clip_sumsq = nullptr,
                          double max_norm = 0.0);
+
+cudaError_t launch_adamw_main(const ListView &p, const ListView &m, const ListView &v,
+                              const ListView &g, const ListView *b, int64_t n_chunks, int gelem,
+                              const float *scale, const AdamwConsts &c,
+                              const AdamwStepScalars *scal, float *amax, bool use_slots,
+                              cudaStream_t s);
+
+// The lists of one delayed-scaling FP8 step: the tensors without FP8 copies
+// (1-D, walked by chunks) and the FP8 weights (2-D, walked by 128x128 tiles).
+struct Fp8DelayedLists {
+    ListView p, m, v, g, b;          // plain tensors
+    int64_t n_plain_chunks;
+    ListView p8, m8, v8, g8, b8, q;  // FP8 weights (2-D) and their fp8 copies
+    const ListView *qt;              // transposed copies or nullptr
+    int64_t n_tiles;
+    int n8;
+    float *tscale;                   // per FP8 weight: fp32 cast scale (scratch)
+};
+
+cudaError_t launch_adamw_fp8_delayed(const Fp8DelayedLists &L, int gelem, int fp8,
+                                     const float *scale, const int32_t *found_inf, int32_t *step,
+                                     const AdamwConsts &c, AdamwStepScalars *scal,
+                                     const float *hist, int hist_len, double eps, float *amax,
+                                     float *inv_scale, cudaStream_t s);
+
+cudaError_t launch_update_scale_hist(float *scale, int32_t *tracker, int32_t *found_inf,
+                                     float growth, float backoff, int32_t interval, float *amax,
+                                     float *hist, int n, int hist_len, cudaStream_t s);
 
 cudaError_t launch_update_scale(float *scale, int32_t *tracker, int32_t *found_inf, float growth,
                                 float backoff, int32_t interval, float *amax, int n_amax,

@@ -34,7 +34,51 @@ __global__ void update_scale_kernel(float *scale, int32_t *tracker, int32_t *fou
     for (int i = threadIdx.x; i < n_amax; i += blockDim.x) amax[i] = 0.0f;
 }
 
+// As update_scale_kernel, and on a step that was not skipped each FP8
+// tensor's amax of this step is pushed into its history (newest first, the
+// oldest dropped); amax is cleared either way.
+__global__ void update_scale_hist_kernel(float *scale, int32_t *tracker, int32_t *found_inf,
+                                         float growth, float backoff, int32_t interval,
+                                         float *amax, float *hist, int n, int hist_len) {
+    const int32_t fi = *found_inf;
+    __syncthreads();  // every thread has read the flag before thread 0 clears it
+    if (threadIdx.x == 0) {
+        float s = *scale;
+        int32_t t = *tracker;
+        if (fi) {
+            s = __fmul_rn(s, backoff);
+            t = 0;
+        } else {
+            t = t + 1;
+            if (t >= interval) {
+                const float grown = __fmul_rn(s, growth);
+                if (isfinite(grown)) s = grown;
+                t = 0;
+            }
+        }
+        *scale = s;
+        *tracker = t;
+        *found_inf = 0;
+    }
+    for (int j = threadIdx.x; j < n; j += blockDim.x) {
+        if (!fi) {
+            float *h = hist + int64_t(j) * hist_len;
+            for (int k = hist_len - 1; k > 0; --k) h[k] = h[k - 1];
+            h[0] = amax[j];
+        }
+        amax[j] = 0.0f;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_update_scale_hist(float *scale, int32_t *tracker, int32_t *found_inf,
+                                     float growth, float backoff, int32_t interval, float *amax,
+                                     float *hist, int n, int hist_len, cudaStream_t s) {
+    update_scale_hist_kernel<<<1, 256, 0, s>>>(scale, tracker, found_inf, growth, backoff,
+                                               interval, amax, hist, n, hist_len);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_update_scale(float *scale, int32_t *tracker, int32_t *found_inf, float growth,
                                 float backoff, int32_t interval, float *amax, int n_amax,

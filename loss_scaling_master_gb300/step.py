@@ -15,21 +15,28 @@ No call reads anything back to the host; ``state()`` does, for monitoring.
 """
 from __future__ import annotations
 
+import contextlib
+
 import torch
 
 from . import _lib as A
+
+_nullctx = contextlib.nullcontext
 
 
 class AmpOptimizerStep:
     def __init__(self, master, grads, *, lr, beta1, beta2, eps, weight_decay,
                  init_scale=65536.0, growth_factor=2.0, backoff_factor=0.5,
                  growth_interval=2000, emit_bf16=True, fp8_shapes=None, fp8_eps=1e-12,
-                 max_norm=None, stream=None):
+                 max_norm=None, fp8_scaling="dynamic", amax_history_len=1, stream=None):
         """master: fp32 device tensors (updated in place); grads: device
         tensors (f16/bf16/f32) the caller fills with scaled gradients before
         each step.  fp8_shapes: per tensor (rows, cols) for weights that get
         e4m3fn copies, None for the others (requires emit_bf16).  max_norm:
-        clip the unscaled gradients to this global L2 norm (None: no clipping)."""
+        clip the unscaled gradients to this global L2 norm (None: no clipping).
+        fp8_scaling: "dynamic" (this step's amax, a separate cast pass) or
+        "delayed" (the max of the last amax_history_len steps' amax, cast in
+        the update pass; the history starts from the initial bf16 copy)."""
         dev = master[0].device
         self.stream = stream
         self.master = list(master)
@@ -74,11 +81,56 @@ class AmpOptimizerStep:
             self.L_qt = mk(self.fp8_t, True)
         self.amax = torch.zeros(max(self.n_fp8, 1), dtype=torch.float32, device=dev)
         self.inv_scale = torch.zeros(max(self.n_fp8, 1), dtype=torch.float32, device=dev)
+        self.fp8_scaling = fp8_scaling
+        self.hist_len = amax_history_len
+        if fp8_scaling == "delayed":
+            if not self.n_fp8 or max_norm is not None:
+                raise ValueError("delayed FP8 scaling needs FP8 weights and no clipping")
+            self._setup_delayed(fp8_shapes, stream)
+        elif fp8_scaling != "dynamic":
+            raise ValueError(fp8_scaling)
+
+    def _groups(self, grads):
+        """1-D lists of the plain tensors and 2-D lists of the FP8 weights."""
+        mk = lambda ts, two_d=False, dt=None: A.amp_tensor_list_create(ts, two_d=two_d, dtype=dt,
+                                                                        stream=self.stream)
+        plain = [i for i, sh in enumerate(self.fp8_shapes) if sh is None]
+        fp8 = [i for i, sh in enumerate(self.fp8_shapes) if sh is not None]
+        v2 = lambda ts: [ts[i].view(*self.fp8_shapes[i]) for i in fp8]
+        gdt = A.dtype_name(grads[0])
+        P = (mk([self.master[i] for i in plain], dt="f32"), mk([self.exp_avg[i] for i in plain], dt="f32"),
+             mk([self.exp_avg_sq[i] for i in plain], dt="f32"), mk([grads[i] for i in plain], dt=gdt),
+             mk([self.bf16[i] for i in plain], dt="bf16"))
+        F = (mk(v2(self.master), True), mk(v2(self.exp_avg), True), mk(v2(self.exp_avg_sq), True),
+             mk(v2(grads), True), mk(v2(self.bf16), True))
+        return P, F
+
+    def _setup_delayed(self, fp8_shapes, stream):
+        self.fp8_shapes = list(fp8_shapes)
+        dev = self.scale.device
+        self.amax_history = torch.zeros((self.n_fp8, self.hist_len), dtype=torch.float32,
+                                        device=dev)
+        self.delayed_groups = [self._groups(self.grads)]
+        # seed: bf16 = RNE(master), then one dynamic cast whose amax opens the history
+        j = 0
+        for i, sh in enumerate(self.fp8_shapes):
+            if sh is None:
+                continue
+            self.bf16[i].copy_(self.master[i])
+            A.fp8_quant_tensorwise(self.bf16[i].view(*sh), "e4m3fn", self.fp8[j], self.fp8_t[j],
+                                   self.inv_scale[j:j + 1], self.amax[j:j + 1],
+                                   eps=self.fp8_eps, stream=stream)
+            j += 1
+        with torch.cuda.stream(stream) if stream is not None else _nullctx():
+            self.amax_history[:, 0].copy_(self.amax[:self.n_fp8])
+            self.amax.zero_()
 
     @property
     def launches_per_step(self) -> int:
         """Kernels one step enqueues (check [+ norm reduce], AdamW prologue + main,
-        [quant], update)."""
+        [quant], update; delayed FP8: check, prologue, plain + FP8 mains, update)."""
+        if self.fp8_scaling == "delayed":
+            return 5
         return 4 + (1 if self.n_fp8 else 0) + (1 if self.max_norm is not None else 0)
 
     def add_grad_buffer(self, grads) -> int:
@@ -90,6 +142,8 @@ class AmpOptimizerStep:
                 any(a.dtype != b.dtype for a, b in zip(grads, self.grads)):
             raise ValueError("gradient buffers must match the first set in sizes and dtype")
         self.grad_lists.append(A.amp_tensor_list_create(grads, stream=self.stream))
+        if self.fp8_scaling == "delayed":
+            self.delayed_groups.append(self._groups(grads))
         return len(self.grad_lists) - 1
 
     def capture_graph(self, stream=None, grad_buffer: int = 0):
@@ -119,6 +173,19 @@ class AmpOptimizerStep:
     def _enqueue(self, s, grad_buffer: int = 0):
         L_g = self.grad_lists[grad_buffer]
         amax = self.amax if self.n_fp8 else None
+        if self.fp8_scaling == "delayed":
+            P, F = self.delayed_groups[grad_buffer]
+            A.amp_unscale_check(L_g, self.scale, self.found_inf, stream=s)
+            A.amp_adamw_master_step_fp8_delayed(P, F, self.L_q, self.L_qt, "e4m3fn",
+                                                self.amax_history, self.hist_len, self.amax,
+                                                self.inv_scale, self.scale, self.found_inf,
+                                                self.step_count, *self.hyper,
+                                                fp8_eps=self.fp8_eps, stream=s)
+            A.amp_update_scale_fp8_history(self.scale, self.growth_tracker, self.found_inf,
+                                           self.growth, self.backoff, self.interval, self.amax,
+                                           self.amax_history, self.n_fp8, self.hist_len,
+                                           stream=s)
+            return
         if self.max_norm is None:
             A.amp_unscale_check(L_g, self.scale, self.found_inf, stream=s)
             A.amp_adamw_master_step(self.L_master, self.L_m, self.L_v, L_g, self.L_b, self.scale,
@@ -142,6 +209,13 @@ class AmpOptimizerStep:
         return {"scale": float(self.scale.item()), "growth_tracker": int(self.growth_tracker.item()),
                 "step": int(self.step_count.item()), "found_inf": int(self.found_inf.item())}
 
+    def state_fp8(self) -> dict:
+        """Host copies of the FP8 scaling state (synchronises)."""
+        d = {"amax": self.amax[:self.n_fp8].cpu(), "inv_scale": self.inv_scale[:self.n_fp8].cpu()}
+        if self.fp8_scaling == "delayed":
+            d["amax_history"] = self.amax_history.cpu()
+        return d
+
     def close(self):
         for name in ("L_master", "L_m", "L_v", "L_b", "L_x8", "L_q", "L_qt"):
             lst = getattr(self, name, None)
@@ -149,3 +223,6 @@ class AmpOptimizerStep:
                 lst.close()
         for lst in self.grad_lists:
             lst.close()
+        for P, F in getattr(self, "delayed_groups", []):
+            for lst in P + F:
+                lst.close()

@@ -198,7 +198,8 @@ class AmpStepOracle:
 
     def __init__(self, master, grad_dtype, lr, beta1, beta2, eps, weight_decay,
                  init_scale, growth_factor, backoff_factor, growth_interval,
-                 emit_bf16=True, fp8_shapes=None, fp8_eps=1e-12, max_norm=None):
+                 emit_bf16=True, fp8_shapes=None, fp8_eps=1e-12, max_norm=None,
+                 fp8_scaling="dynamic", hist_len=1):
         self.master = [np.array(m, np.float32, copy=True) for m in master]
         self.exp_avg = [np.zeros_like(m) for m in self.master]
         self.exp_avg_sq = [np.zeros_like(m) for m in self.master]
@@ -224,6 +225,25 @@ class AmpStepOracle:
             self.inv_scale = np.zeros(max(k, 1), np.float32)
         else:
             self.amax = None
+        # Delayed scaling ("第20章 量化与混合精度训练" §20.5.9): each FP8 weight
+        # keeps the amax of its last hist_len steps (newest first) and is cast
+        # with the scale of their maximum.  At construction there is no
+        # previous step, so the history starts from the amax of the initial
+        # bf16 copy, cast dynamically.
+        self.fp8_scaling = fp8_scaling
+        self.hist_len = hist_len
+        if fp8_scaling == "delayed":
+            assert fp8_shapes is not None and emit_bf16
+            self.hist = np.zeros((max(k, 1), hist_len), np.float32)
+            for i, sh in enumerate(fp8_shapes):
+                if sh is None:
+                    continue
+                self.bf16[i] = encode("bf16", self.master[i])
+                q, qt, inv, am = fp8_quant_tensorwise(self.bf16[i], "bf16", sh[0], sh[1],
+                                                      "e4m3fn", self.fp8_eps, True)
+                s_ = self.slots[i]
+                self.fp8[i], self.fp8_t[i], self.inv_scale[s_] = q, qt, inv
+                self.hist[s_, 0] = am
 
     def run(self, grads):
         """Apply one step with the given scaled gradients; returns found_inf."""
@@ -243,10 +263,17 @@ class AmpStepOracle:
                 if sh is None:
                     continue
                 s = self.slots[i]
+                if self.fp8_scaling == "delayed":
+                    h = self.hist[s]
+                    a = float("nan") if np.isnan(h).any() else float(h.max())
+                else:
+                    a = float(self.amax[s])
                 q, qt, inv, _ = fp8_quant_tensorwise(self.bf16[i], "bf16", sh[0], sh[1],
-                                                     "e4m3fn", self.fp8_eps, True,
-                                                     amax=float(self.amax[s]))
+                                                     "e4m3fn", self.fp8_eps, True, amax=a)
                 self.fp8[i], self.fp8_t[i], self.inv_scale[s] = q, qt, inv
+        if self.fp8_scaling == "delayed" and not fi:
+            self.hist[:, 1:] = self.hist[:, :-1].copy()
+            self.hist[:, 0] = self.amax[:self.hist.shape[0]]
         self.scale, self.tracker, self.found_inf = update_scale(
             self.scale, self.tracker, self.found_inf, self.growth, self.backoff,
             self.interval, self.amax)

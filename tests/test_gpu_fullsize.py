@@ -10,9 +10,10 @@ times (AmpOptimizerStep over the whole parameter set).
   is element-wise once found_inf is known.
 * FP8 sweep (bf16 [4096,4096], [8192,8192], [16384,5120] and an all-zero
   [4096,4096], e4m3fn and e5m2): every byte of both layouts.
-* 8B Llama-3 set, the bench's own state (flat buffers, FP8 weights): 3 steps;
-  two FP8 weights and a norm vector in full through the oracle (bf16, amax,
-  inv_scale, row-major and transposed bytes), sampled elements elsewhere.
+* 8B Llama-3 set, the bench's own state (flat buffers, FP8 weights), with
+  dynamic and with delayed FP8 scaling: 3 steps; two FP8 weights and a norm
+  vector in full through the oracle (bf16, amax or amax history, inv_scale,
+  row-major and transposed bytes), sampled elements elsewhere.
 """
 import numpy as np
 import pytest
@@ -150,10 +151,12 @@ def test_fp8_sweep_full_parity(A, fmt):
         del x, out, out_t
 
 
-def test_llama3_8b_bench_state_parity(A):
+@pytest.mark.parametrize("fp8_scaling", ["dynamic", "delayed"])
+def test_llama3_8b_bench_state_parity(A, fp8_scaling):
     import bench
     dev = torch.device("cuda:0")
-    st, info = bench.build_step("llama3_8b", dev, seed=1234)
+    torch.cuda.empty_cache()
+    st, info = bench.build_step("llama3_8b", dev, seed=1234, fp8_scaling=fp8_scaling)
     cfg = info["cfg"]
     names = [s.name for s in cfg.specs]
     full = [names.index(n) for n in ("l0.k", "l31.gate", "l5.ffn_norm")]
@@ -167,7 +170,9 @@ def test_llama3_8b_bench_state_parity(A):
           else to_host_bits(st.grads[i].index_select(0, samples[i])) for i in order]
     fp8_shapes = [(cfg.specs[i].rows, cfg.specs[i].cols) if (i in full and cfg.specs[i].fp8)
                   else None for i in order]
-    orc = _oracle(cfg, init, fp8_shapes=fp8_shapes)
+    orc = O.AmpStepOracle(init, cfg.grad_dtype, cfg.lr, cfg.beta1, cfg.beta2, cfg.eps,
+                          cfg.weight_decay, cfg.init_scale, cfg.growth_factor, cfg.backoff_factor,
+                          cfg.growth_interval, fp8_shapes=fp8_shapes, fp8_scaling=fp8_scaling)
     for k in range(3):
         st.step()
         assert orc.run(gh) == 0
@@ -195,4 +200,9 @@ def test_llama3_8b_bench_state_parity(A):
             assert np.array_equal(to_host_bits(q).ravel(), orc.fp8[pos]), names[i]
             assert np.array_equal(to_host_bits(qt).ravel(), orc.fp8_t[pos]), names[i]
             assert to_host_bits(st.inv_scale)[fp8_index[i]] == orc.inv_scale[orc.slots[pos]]
+            if fp8_scaling == "delayed":
+                assert np.array_equal(to_host_bits(st.amax_history)[fp8_index[i]],
+                                      orc.hist[orc.slots[pos]])
     st.close()
+    del st, info
+    torch.cuda.empty_cache()

@@ -525,3 +525,60 @@ def test_clipped_step_composition(A, dev):
         assert_state_close(to_host_bits(st.exp_avg_sq[i]), orc.exp_avg_sq[i], f"exp_avg_sq[{i}]")
         assert_bf16_close(to_host_bits(st.bf16[i]), orc.bf16[i], f"bf16[{i}]")
     st.close()
+
+
+# ------------------------------------------------------ delayed FP8 scaling
+@pytest.mark.parametrize("hist_len", [1, 3])
+@pytest.mark.parametrize("gdt", ["f16", "bf16"])
+def test_delayed_fp8_step_composition(A, dev, hist_len, gdt):
+    """AdamW + bf16 + FP8 in one pass with the delayed scale vs the oracle's
+    step: full tiles (vector path), ragged edge tiles and a tensor whose
+    column count breaks 16-byte rows (element path), a skipped step."""
+    from loss_scaling_master_gb300 import AmpOptimizerStep
+    rng = np.random.default_rng(70 + hist_len)
+    shapes = [(256, 512), (300,), (96, 256), (128, 136), (1000,), (130, 52), (384, 128)]
+    fp8_shapes = [s if len(s) == 2 else None for s in shapes]
+    sizes = [int(np.prod(s)) for s in shapes]
+    master = [(rng.standard_normal(n) * 0.02).astype(np.float32) for n in sizes]
+    hyper = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+    tdt = torch.float16 if gdt == "f16" else torch.bfloat16
+    st = AmpOptimizerStep([torch.from_numpy(m.copy()).to(dev) for m in master],
+                          [torch.empty(n, dtype=tdt, device=dev) for n in sizes],
+                          init_scale=4096.0, growth_interval=3, fp8_shapes=fp8_shapes,
+                          fp8_scaling="delayed", amax_history_len=hist_len, **hyper)
+    orc = O.AmpStepOracle(master, gdt, hyper["lr"], hyper["beta1"], hyper["beta2"], hyper["eps"],
+                          hyper["weight_decay"], 4096.0, 2.0, 0.5, 3, fp8_shapes=fp8_shapes,
+                          fp8_scaling="delayed", hist_len=hist_len)
+
+    def check_fp8():
+        j = 0
+        for i, sh in enumerate(fp8_shapes):
+            if sh is None:
+                continue
+            assert np.array_equal(to_host_bits(st.fp8[j].view(torch.uint8)).ravel(), orc.fp8[i]), i
+            assert np.array_equal(to_host_bits(st.fp8_t[j].view(torch.uint8)).ravel(), orc.fp8_t[i]), i
+            assert to_host_bits(st.inv_scale)[j] == orc.inv_scale[orc.slots[i]], i
+            j += 1
+        assert np.array_equal(to_host_bits(st.amax_history), orc.hist)
+
+    torch.cuda.synchronize()
+    check_fp8()                                      # the seeding cast
+    for k in range(6):
+        sigma = 1e-3 * orc.scale
+        gh = [(rng.standard_normal(n) * sigma).astype(np.float32) for n in sizes]
+        gh = [g.astype(np.float16).view(np.uint16) if gdt == "f16" else O.encode("bf16", g)
+              for g in gh]
+        if k == 3:
+            gh[3][17] = _inf_bits(gdt, np.inf)
+        for t, h in zip(st.grads, gh):
+            t.copy_(to_device(h, gdt, dev))
+        st.step()
+        orc.run(gh)
+        s = st.state()
+        assert (s["scale"], s["growth_tracker"], s["step"]) == (orc.scale, orc.tracker, orc.step)
+        check_fp8()
+    for i in range(len(shapes)):
+        assert np.array_equal(to_host_bits(st.master[i]).view(np.uint32), orc.master[i].view(np.uint32))
+        assert np.array_equal(to_host_bits(st.exp_avg[i]).view(np.uint32), orc.exp_avg[i].view(np.uint32))
+        assert np.array_equal(to_host_bits(st.bf16[i]), orc.bf16[i])
+    st.close()

@@ -460,3 +460,38 @@ def test_clip_factor_one_is_the_unclipped_step():
     O.adamw_master_step(master, m, v, g, "f32", None, None, 0, 0, 1e-3, 0.9, 0.999, 1e-8, 0.01,
                         clip=1.0)
     assert np.array_equal(master[0], a[0][0]) and np.array_equal(m[0], a[1][0])
+
+
+# ------------------------------------------------------ delayed FP8 scaling
+@pytest.mark.parametrize("hist_len", [1, 3])
+def test_delayed_scaling_uses_previous_amax(hist_len):
+    """'第20章 量化与混合精度训练' §20.5.9: the scale of a step comes from the
+    amax of earlier steps.  With history length H the cast of step t uses the
+    max of the amaxes of the last H non-skipped steps' bf16 copies (the
+    initial copy counting as the first); a skipped step leaves it unchanged."""
+    rng = np.random.default_rng(60)
+    shapes = [(64, 96), None, (32, 40)]
+    sizes = [64 * 96, 300, 32 * 40]
+    master = [(rng.standard_normal(n) * 0.02).astype(F32) for n in sizes]
+    orc = O.AmpStepOracle(master, "f16", 1e-2, 0.9, 0.999, 1e-8, 0.0, 1024.0, 2.0, 0.5, 100,
+                          fp8_shapes=shapes, fp8_scaling="delayed", hist_len=hist_len)
+    amaxes = {0: [np.abs(O.decode("bf16", orc.bf16[0])).max()],
+              2: [np.abs(O.decode("bf16", orc.bf16[2])).max()]}
+    for k in range(5):
+        g = [(rng.standard_normal(n) * 1e-3 * 1024).astype(np.float16).view(np.uint16) for n in sizes]
+        if k == 2:
+            g[1][5] = 0x7C00
+        inv_before = orc.inv_scale.copy()
+        fi = orc.run(g)
+        for i, slot in ((0, 0), (2, 1)):
+            if fi:
+                assert orc.inv_scale[slot] == inv_before[slot]
+                continue
+            used = max(amaxes[i][-hist_len:])
+            assert orc.inv_scale[slot] == np.float32(1.0 / (448.0 / max(float(used), 1e-12)))
+            amaxes[i].append(np.abs(O.decode("bf16", orc.bf16[i])).max())
+        assert fi == (k == 2)
+    for i, slot in ((0, 0), (2, 1)):
+        want = list(reversed(amaxes[i][-hist_len:]))
+        want += [0.0] * (hist_len - len(want))
+        assert np.array_equal(orc.hist[slot], np.array(want, F32))
