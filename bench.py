@@ -64,6 +64,17 @@ def workload_config(workload: str, world: int) -> dict:
             "l2": "inputs larger than L2 (no flush needed)"}
 
 
+def adamw_traffic(delayed: bool, n_params: int, n_fp8: int):
+    """DRAM bytes of the AdamW call from the committed captures: the chunked
+    kernel for every parameter, or (delayed FP8) the chunked kernel for the
+    plain parameters plus the tile kernel for the FP8 weights."""
+    if not delayed:
+        return profiled_traffic("adamw_main_kernel", n_params)
+    a = profiled_traffic("adamw_main_kernel", n_params - n_fp8)
+    b = profiled_traffic("adamw_fp8_tile_kernel", n_fp8)
+    return None if a is None or b is None else a + b
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -311,9 +322,9 @@ def run_ours(args, rank, world, device):
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "bytes_per_param": info["bytes_adamw"] / n_params,
-                     "traffic": profiled_traffic("adamw_main_kernel", n_params),
-                     "traffic_note": "ncu dram read+write of a 124M-param launch scaled by "
-                                     "params (profiles/adamw_main_gpt2_small.md)"},
+                     "traffic": adamw_traffic(delayed, n_params, info["fp8_params"]),
+                     "traffic_note": "ncu dram read+write per param of a smaller launch of the "
+                                     "same kernel(s), scaled by params (profiles/traffic.json)"},
         "clocks": clk.summary(),
         "gpu_launches": args.steps * step.launches_per_step,
     }
@@ -541,7 +552,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama3_8b",
-                    choices=["llama3_8b", "llama_1b", "gpt2_small", "fp8_sweep"])
+                    choices=["llama3_8b", "llama_1b", "gpt2_small", "fp8_sweep",
+                             "llama3_8b_2layers"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

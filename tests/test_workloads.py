@@ -16,6 +16,8 @@ def test_param_set_sizes():
     assert _count(llama3_8b_specs()) == (8_030_261_248, 291)
     fp8 = [s for s in llama3_8b_specs() if s.fp8]
     assert len(fp8) == 224 and sum(s.numel for s in fp8) == 6_979_321_856
+    two = amp_config("llama3_8b_2layers").specs
+    assert _count(two) == (436_224_000, 18) and sum(s.numel for s in two if s.fp8) == 436_207_616
 
 
 def test_injection_sites_are_seeded_and_in_range():

@@ -124,6 +124,12 @@ def amp_config(name: str) -> AmpConfig:
     if name == "llama3_8b":
         return AmpConfig("llama3_8b", llama3_8b_specs(), "f16", 20, 1e-3, 0.9, 0.999, 1e-8, 0.01,
                          65536.0, 2.0, 0.5, 2000, 1e-4, fp8_weights=True)
+    if name == "llama3_8b_2layers":
+        # two decoder layers of the 8B set (no embedding / head): a profiling-size
+        # case of the same kernels (436,224,000 params, all linear weights FP8)
+        specs = [s for s in llama3_8b_specs() if s.name.startswith(("l0.", "l1."))]
+        return AmpConfig("llama3_8b_2layers", specs, "f16", 20, 1e-3, 0.9, 0.999, 1e-8, 0.01,
+                         65536.0, 2.0, 0.5, 2000, 1e-4, fp8_weights=True)
     raise KeyError(name)
 
 
