@@ -144,9 +144,16 @@ __global__ void __launch_bounds__(kThreads) quant_list_kernel(ListView X, ListVi
                        tr * kTile, tc * kTile, &s_scale, sm);
 }
 
+// amax is an output: it starts from +0 (unless the call is skipped).
+__global__ void amax_zero_kernel(float *amax, const int32_t *skip_if) {
+    if (!(skip_if && *skip_if)) *amax = 0.0f;
+}
+
 template <int XT>
 __global__ void __launch_bounds__(kThreads) amax_kernel(const void *x, int64_t n,
-                                                        unsigned int *amax_bits) {
+                                                        unsigned int *amax_bits,
+                                                        const int32_t *skip_if) {
+    if (skip_if && *skip_if) return;
     const int64_t gtid = int64_t(blockIdx.x) * kThreads + threadIdx.x;
     const int64_t gstride = int64_t(gridDim.x) * kThreads;
     uint32_t mx = 0;
@@ -200,14 +207,15 @@ cudaError_t launch_single(const void *x, int64_t rows, int64_t cols, uint8_t *ou
                           const int32_t *skip_if, int device, cudaStream_t s) {
     const int64_t n = rows * cols;
     if (!amax_given) {
-        // amax is an output here: it starts from +0 and is max-reduced.
-        cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), s);
+        amax_zero_kernel<<<1, 1, 0, s>>>(amax, skip_if);
+        cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         const int64_t per = XT == kF32 ? 4 : 8;
         const int64_t want = (n / per + kThreads - 1) / kThreads;
         const int64_t cap = int64_t(sm_count(device)) * 8;
         const unsigned grid = (unsigned)std::max<int64_t>(1, std::min(want, cap));
-        amax_kernel<XT><<<grid, kThreads, 0, s>>>(x, n, reinterpret_cast<unsigned int *>(amax));
+        amax_kernel<XT><<<grid, kThreads, 0, s>>>(x, n, reinterpret_cast<unsigned int *>(amax),
+                                                   skip_if);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -65,6 +65,8 @@ def lib():
             L.orc_adamw_master_step_clip.argtypes = (
                 [ctypes.c_int, P, P, P, P, ctypes.c_int, P, I64P, P, ctypes.c_int32, P]
                 + [ctypes.c_double] * 5 + [P, P, ctypes.c_float])
+            L.orc_fp8_quant_rowwise.argtypes = [P, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                                ctypes.c_int, ctypes.c_double] + [P] * 8
             L.orc_fp8_quant_tensorwise.argtypes = [P, ctypes.c_int, ctypes.c_int64,
                                                    ctypes.c_int64, ctypes.c_int,
                                                    ctypes.c_double, P, P, P, P, ctypes.c_int]
@@ -184,6 +186,25 @@ def fp8_quant_tensorwise(x: np.ndarray, xdt: str, rows: int, cols: int, fp8: str
                                    _ptr(out), _ptr(out_t) if out_t is not None else None,
                                    _ptr(inv), _ptr(am), int(amax is not None))
     return out, out_t, float(inv[0]), float(am[0])
+
+
+def fp8_quant_rowwise(x: np.ndarray, xdt: str, rows: int, cols: int, fp8: str,
+                      eps: float = 1e-12, transposed: bool = True):
+    """Per-row scales for the row-major bytes, per-column scales for the
+    transposed copy.  Returns a dict of q, q_t, amax/scale/inv per row and col."""
+    x = np.ascontiguousarray(x)
+    assert x.size == rows * cols
+    r = {"q": np.empty(rows * cols, np.uint8),
+         "amax_row": np.empty(rows, np.float32), "scale_row": np.empty(rows, np.float32),
+         "inv_row": np.empty(rows, np.float32)}
+    if transposed:
+        r.update(q_t=np.empty(rows * cols, np.uint8), amax_col=np.empty(cols, np.float32),
+                 scale_col=np.empty(cols, np.float32), inv_col=np.empty(cols, np.float32))
+    g = lambda k: _ptr(r[k]) if k in r else None
+    lib().orc_fp8_quant_rowwise(_ptr(x), _CODES[xdt], rows, cols, _CODES[fp8], eps, g("q"),
+                                g("q_t"), g("amax_row"), g("scale_row"), g("inv_row"),
+                                g("amax_col"), g("scale_col"), g("inv_col"))
+    return r
 
 
 class AmpStepOracle:

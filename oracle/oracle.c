@@ -400,3 +400,69 @@ void orc_fp8_quant_tensorwise(const void *x, int xdtype, int64_t rows, int64_t c
         }
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Rowwise FP8 scaling.  "FP8训练：量化、自动微分、Torchao" §1: instead of one   */
+/* scale per tensor, every row gets its own scale (§2's formula per row).     */
+/* §4: the backward GEMMs consume the column-major copy, whose reduction runs */
+/* along the rows of x - so that copy carries one scale per column of x (a    */
+/* per-row scale would vary along its reduction dimension).  Reading: out has */
+/* per-row scales, out_t (= [cols, rows] row-major) per-column scales.         */
+/* Each scale is §2's scale_d = fp8_max / max(double(amax), EPS) of its own   */
+/* row or column; the cast is §2's clamp and RNE.                              */
+/* ------------------------------------------------------------------------ */
+static double nan_max_abs_update(double acc, float v)
+{
+    float a = fabsf(v);
+    if (isnan(a) || isnan(acc))
+        return NAN;
+    return a > acc ? a : acc;
+}
+
+static uint8_t cast_scaled(const orc_fmt *f, float x, float s32)
+{
+    double fmax = fmt_max(f);
+    float lo = (float)-fmax, hi = (float)fmax;
+    float y = x * s32;
+    if (!isnan(y))
+        y = y < lo ? lo : (y > hi ? hi : y);
+    return (uint8_t)fmt_encode(f, (double)y);
+}
+
+static void scale_of(double fmax, double eps, float amax, float *s32, float *inv)
+{
+    double ad = (double)amax;
+    double cl = isnan(ad) ? ad : (ad < eps ? eps : ad);
+    double sd = fmax / cl;
+    *s32 = (float)sd;
+    *inv = (float)(1.0 / sd);
+}
+
+void orc_fp8_quant_rowwise(const void *x, int xdtype, int64_t rows, int64_t cols, int fp8_dtype,
+                           double eps, uint8_t *out, uint8_t *out_t, float *amax_row,
+                           float *scale_row, float *inv_row, float *amax_col, float *scale_col,
+                           float *inv_col)
+{
+    const orc_fmt *f = fmt_of(fp8_dtype);
+    double fmax = fmt_max(f);
+    for (int64_t i = 0; i < rows; ++i) {
+        double a = 0.0;
+        for (int64_t j = 0; j < cols; ++j)
+            a = nan_max_abs_update(a, load_as_f32(xdtype, x, i * cols + j));
+        amax_row[i] = (float)a;
+        scale_of(fmax, eps, amax_row[i], &scale_row[i], &inv_row[i]);
+        for (int64_t j = 0; j < cols; ++j)
+            out[i * cols + j] = cast_scaled(f, load_as_f32(xdtype, x, i * cols + j), scale_row[i]);
+    }
+    if (!out_t)
+        return;
+    for (int64_t j = 0; j < cols; ++j) {
+        double a = 0.0;
+        for (int64_t i = 0; i < rows; ++i)
+            a = nan_max_abs_update(a, load_as_f32(xdtype, x, i * cols + j));
+        amax_col[j] = (float)a;
+        scale_of(fmax, eps, amax_col[j], &scale_col[j], &inv_col[j]);
+        for (int64_t i = 0; i < rows; ++i)
+            out_t[j * rows + i] = cast_scaled(f, load_as_f32(xdtype, x, i * cols + j), scale_col[j]);
+    }
+}

@@ -327,9 +327,11 @@ def test_fp8_quant_degenerate_cases(A, dev, fmt):
     q, qt, inv, am = _run_quant(A, dev, np.zeros(0, np.uint16), "bf16", 0, 7, fmt, True)
     assert am == 0.0 and inv == np.float32(O.fp8_quant_tensorwise(np.zeros(0, np.uint16), "bf16",
                                                                   0, 7, fmt)[2])
-    # skip flag set: nothing written
+    # skip flag set: nothing written, the amax output included
     q, qt, inv, am = _run_quant(A, dev, xh, "f32", 128, 256, fmt, True, amax_given=1.0, skip=1)
     assert np.all(q == 0xA5) and np.all(qt == 0x5A) and inv == 0.0
+    q, qt, inv, am = _run_quant(A, dev, xh, "f32", 128, 256, fmt, True, skip=1)
+    assert np.all(q == 0xA5) and np.all(qt == 0x5A) and inv == 0.0 and am == -1.0
 
 
 @pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])

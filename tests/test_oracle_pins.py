@@ -495,3 +495,57 @@ def test_delayed_scaling_uses_previous_amax(hist_len):
         want = list(reversed(amaxes[i][-hist_len:]))
         want += [0.0] * (hist_len - len(want))
         assert np.array_equal(orc.hist[slot], np.array(want, F32))
+
+
+# ----------------------------------------------------------- rowwise FP8
+@pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
+def test_rowwise_reduces_to_tensorwise(fmt):
+    """One row: the row scale is the tensor scale; one column: the column
+    scale of the transposed copy is the tensor scale (the pinned quantizer)."""
+    rng = np.random.default_rng(80)
+    x = (rng.standard_normal(333) * 7).astype(F32)
+    r = O.fp8_quant_rowwise(x, "f32", 1, 333, fmt)
+    q, qt, inv, amax = O.fp8_quant_tensorwise(x, "f32", 1, 333, fmt)
+    assert np.array_equal(r["q"], q) and r["inv_row"][0] == np.float32(inv) and r["amax_row"][0] == amax
+    c = O.fp8_quant_rowwise(x, "f32", 333, 1, fmt)
+    assert np.array_equal(c["q_t"], qt) and c["inv_col"][0] == np.float32(inv)
+
+
+@pytest.mark.parametrize("fmt,top", [("e4m3fn", 0x7E), ("e5m2", 0x7B)])
+def test_rowwise_each_row_and_column_reaches_fp8_max(fmt, top):
+    rng = np.random.default_rng(81)
+    rows, cols = 37, 53
+    x = (rng.standard_normal((rows, cols)) * 10 ** rng.uniform(-3, 3, size=(rows, 1))).astype(F32)
+    r = O.fp8_quant_rowwise(x.ravel(), "f32", rows, cols, fmt)
+    q = r["q"].reshape(rows, cols)
+    qt = r["q_t"].reshape(cols, rows)
+    for i in range(rows):
+        j = int(np.argmax(np.abs(x[i])))
+        assert q[i, j] & 0x7F == top
+    for j in range(cols):
+        i = int(np.argmax(np.abs(x[:, j])))
+        assert qt[j, i] & 0x7F == top
+    # a row scaled by a power of two keeps its bytes (its scale follows it)
+    y = x.copy()
+    y[4] *= 8.0
+    r2 = O.fp8_quant_rowwise(y.ravel(), "f32", rows, cols, fmt)
+    assert np.array_equal(r2["q"].reshape(rows, cols)[4], q[4])
+
+
+@pytest.mark.parametrize("fmt,tdt", [("e4m3fn", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)])
+def test_rowwise_vs_torch_ops(fmt, tdt):
+    rng = np.random.default_rng(82)
+    rows, cols = 24, 40
+    xb = torch.from_numpy((rng.standard_normal((rows, cols)) * 3).astype(F32)).to(torch.bfloat16)
+    bits = xb.view(torch.int16).numpy().view(np.uint16).ravel()
+    r = O.fp8_quant_rowwise(bits, "bf16", rows, cols, fmt)
+    mx = float(torch.finfo(tdt).max)
+    for dim, key, qk in ((1, "row", "q"), (0, "col", "q_t")):
+        am = xb.float().abs().amax(dim=dim, keepdim=True)
+        sc = mx / am.double().clamp(min=1e-12)
+        ref = (xb.float() * sc).clamp(-mx, mx).to(tdt).view(torch.int8).numpy().view(np.uint8)
+        if dim == 0:
+            ref = ref.T
+        assert np.array_equal(r[qk], ref.ravel())
+        assert np.array_equal(r["inv_" + key], sc.reciprocal().float().numpy().ravel())
+        assert np.array_equal(r["amax_" + key], am.numpy().ravel())
