@@ -432,12 +432,22 @@ def run_fp8_sweep(args, rank, world, device):
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.Stream(device=device)
     fmts = ["e4m3fn", "e5m2"]
+    rowwise = args.fp8_granularity == "rowwise"
+    if rowwise:
+        rc = [{k: torch.empty(n, device=device) for k, n in
+               (("ar", x.shape[0]), ("sr", x.shape[0]), ("ir", x.shape[0]),
+                ("ac", x.shape[1]), ("sc", x.shape[1]), ("ic", x.shape[1]))} for x in mats]
 
     def one(ev=None):
         for f in fmts:
             for i, x in enumerate(mats):
-                A.fp8_quant_tensorwise(x, f, outs[i][0], outs[i][1], inv[i:i + 1],
-                                       amax[i:i + 1], stream=stream)
+                if rowwise:
+                    d = rc[i]
+                    A.fp8_quant_rowwise(x, f, outs[i][0], outs[i][1], d["ar"], d["sr"], d["ir"],
+                                        d["ac"], d["sc"], d["ic"], stream=stream)
+                else:
+                    A.fp8_quant_tensorwise(x, f, outs[i][0], outs[i][1], inv[i:i + 1],
+                                           amax[i:i + 1], stream=stream)
 
     for _ in range(args.warmup):
         one()
@@ -460,7 +470,8 @@ def run_fp8_sweep(args, rank, world, device):
     gbs = 6 * elems / (ms * 1e-3) / 1e9
     if rank != 0:
         return None
-    return {"metric": "FP8 tensorwise quant GB/s (amax + e4m3fn/e5m2 cast + transposed copy)",
+    gran = "rowwise (per-row / per-column scales)" if rowwise else "tensorwise"
+    return {"metric": f"FP8 {gran} quant GB/s (amax + e4m3fn/e5m2 cast + transposed copy)",
             "value": gbs * world, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, fp8 out",
@@ -469,7 +480,8 @@ def run_fp8_sweep(args, rank, world, device):
                                    "x {e4m3fn,e5m2}", "l2": "flushed between steps"},
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                          "frac": gbs / peak, "peak_kind": kind, "traffic": None},
-            "clocks": clk.summary(), "gpu_launches": args.steps * len(mats) * len(fmts) * 2}
+            "clocks": clk.summary(),
+            "gpu_launches": args.steps * len(mats) * len(fmts) * (4 if rowwise else 3)}
 
 
 # ------------------------------------------------------------ CPU baseline
@@ -560,6 +572,8 @@ def main():
     ap.add_argument("--fp8-scaling", default="dynamic", choices=["dynamic", "delayed"],
                     help="FP8 weight scaling: this step's amax (a separate cast pass) or the "
                          "previous step's (cast fused into the AdamW pass)")
+    ap.add_argument("--fp8-granularity", default="tensorwise", choices=["tensorwise", "rowwise"],
+                    help="scale granularity of the fp8_sweep workload")
     ap.add_argument("--clip", type=float, default=None,
                     help="also clip the unscaled gradients to this global L2 norm")
     args = ap.parse_args()

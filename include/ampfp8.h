@@ -254,6 +254,26 @@ amp_status fp8_quant_tensorwise(const void *x, amp_dtype x_dtype, int64_t rows, 
                                 float *inv_scale_dev, float *amax_dev, int amax_given,
                                 const int32_t *skip_if_dev, amp_stream_t stream);
 
+/* Rowwise scaling ("FP8训练：量化、自动微分、Torchao" §1: one scale per row
+ * instead of one per tensor).  x is [rows, cols] row-major (bf16, f16, f32).
+ * For every row i, §2's recipe on that row alone:
+ *     amax_row[i]  = max_j |x[i,j]|  (fp32, NaN propagating)
+ *     scale_d      = fp8_max / max(double(amax_row[i]), eps)          (fp64)
+ *     scale_row[i] = float(scale_d), inv_scale_row[i] = float(1/scale_d)
+ *     out[i,j]     = fp8(clamp(float(x[i,j]) * scale_row[i], +-fp8_max)), RNE
+ * If out_t is non-NULL it is the column-major copy for the GEMMs that reduce
+ * along the rows of x (§4), so it takes one scale per column j, the same
+ * recipe on column j: amax_col[j], scale_col[j], inv_scale_col[j], and
+ * out_t[j,i] = fp8(clamp(float(x[i,j]) * scale_col[j], +-fp8_max)).
+ * Four launches (zero, amax, scales, cast), 6 bytes per element.  A set
+ * *skip_if_dev writes nothing.  Empty tensors return at once.
+ * Errors: AMP_EINVAL (NULL outputs, negative size, eps <= 0), AMP_EDTYPE. */
+amp_status fp8_quant_rowwise(const void *x, amp_dtype x_dtype, int64_t rows, int64_t cols,
+                             amp_dtype fp8_dtype, double eps, void *out, void *out_t,
+                             float *amax_row, float *scale_row, float *inv_scale_row,
+                             float *amax_col, float *scale_col, float *inv_scale_col,
+                             const int32_t *skip_if_dev, amp_stream_t stream);
+
 /* The same over a list of 2-D tensors in one launch, with amax given per
  * tensor: tensor i uses amax_dev[i] (e.g. folded by amp_adamw_master_step
  * with slot i) and writes inv_scale_dev[i].

@@ -28,7 +28,8 @@ EXPORTS = ("amp_tensor_list_create", "amp_tensor_list_set_amax_slots", "amp_tens
            "amp_unscale_check", "amp_unscale_check_norm", "amp_adamw_master_step",
            "amp_adamw_master_step_clip", "amp_adamw_master_step_noalloc",
            "amp_adamw_master_step_fp8_delayed", "amp_update_scale_fp8_history",
-           "fp8_quant_tensorwise", "fp8_quant_tensorwise_list", "amp_update_scale",
+           "fp8_quant_tensorwise", "fp8_quant_tensorwise_list", "fp8_quant_rowwise",
+           "amp_update_scale",
            "amp_last_error", "amp_abi_version")
 
 
@@ -76,6 +77,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.amp_update_scale_fp8_history.argtypes = [P, P, P, flt, flt, ctypes.c_int32, P, P, i32,
                                                    i32, P]
         L.fp8_quant_tensorwise.argtypes = [P, i32, i64, i64, i32, dbl, P, P, P, P, i32, P, P]
+        L.fp8_quant_rowwise.argtypes = [P, i32, i64, i64, i32, dbl] + [P] * 10
         L.fp8_quant_tensorwise_list.argtypes = [P, P, P, i32, dbl, P, P, P, P]
         L.amp_update_scale.argtypes = [P, P, P, flt, flt, ctypes.c_int32, P, i32, P]
         for name in EXPORTS[:-2]:
@@ -265,6 +267,18 @@ def fp8_quant_tensorwise(x: torch.Tensor, fp8_dtype: str, out: torch.Tensor, out
                                        eps, _dptr(out), _dptr(out_t), _dptr(inv_scale),
                                        _dptr(amax), int(amax_given), _dptr(skip_if),
                                        _stream(stream)))
+
+
+def fp8_quant_rowwise(x: torch.Tensor, fp8_dtype: str, out, out_t, amax_row, scale_row,
+                      inv_scale_row, amax_col=None, scale_col=None, inv_scale_col=None,
+                      eps: float = 1e-12, skip_if=None, stream=None):
+    """x is [rows, cols]; per-row scales for out, per-column scales for out_t."""
+    rows, cols = x.shape
+    _check("fp8_quant_rowwise",
+           load().fp8_quant_rowwise(_dptr(x), DT[dtype_name(x)], rows, cols, DT[fp8_dtype], eps,
+                                    _dptr(out), _dptr(out_t), _dptr(amax_row), _dptr(scale_row),
+                                    _dptr(inv_scale_row), _dptr(amax_col), _dptr(scale_col),
+                                    _dptr(inv_scale_col), _dptr(skip_if), _stream(stream)))
 
 
 def fp8_quant_tensorwise_list(x: TensorList, out: TensorList, out_t: TensorList | None,

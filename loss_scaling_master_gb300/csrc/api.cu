@@ -80,7 +80,7 @@ extern "C" {
 
 const char *amp_last_error(void) { return g_err; }
 
-int amp_abi_version(void) { return 3; }
+int amp_abi_version(void) { return 4; }
 
 amp_status amp_tensor_list_create(int n, void *const *dev_ptrs, const int64_t *rows,
                                   const int64_t *cols, amp_dtype dtype, amp_stream_t stream,
@@ -408,6 +408,33 @@ amp_status fp8_quant_tensorwise(const void *x, amp_dtype x_dtype, int64_t rows, 
                               amax_given ? 1 : 0, skip_if_dev, dev,
                               reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? AMP_OK : cuda_fail(e, "fp8_quant_tensorwise");
+}
+
+amp_status fp8_quant_rowwise(const void *x, amp_dtype x_dtype, int64_t rows, int64_t cols,
+                             amp_dtype fp8_dtype, double eps, void *out, void *out_t,
+                             float *amax_row, float *scale_row, float *inv_scale_row,
+                             float *amax_col, float *scale_col, float *inv_scale_col,
+                             const int32_t *skip_if_dev, amp_stream_t stream) {
+    const char *fn = "fp8_quant_rowwise";
+    if (rows < 0 || cols < 0) return fail(AMP_EINVAL, "%s: negative size", fn);
+    if (rows * cols > 0 && (!x || !out || !amax_row || !scale_row || !inv_scale_row))
+        return fail(AMP_EINVAL, "%s: NULL x / out / row outputs", fn);
+    if (out_t && rows * cols > 0 && (!amax_col || !scale_col || !inv_scale_col))
+        return fail(AMP_EINVAL, "%s: out_t needs the column outputs", fn);
+    if (!(eps > 0.0)) return fail(AMP_EINVAL, "%s: eps must be > 0", fn);
+    const int xc = elem_code(x_dtype), fc = fp8_code(fp8_dtype);
+    if (xc < 0 || fc < 0) return fail(AMP_EDTYPE, "%s: unsupported dtype", fn);
+    const int64_t tiles = ((rows + amp::kTile - 1) / amp::kTile) * ((cols + amp::kTile - 1) / amp::kTile);
+    if (tiles > int64_t(INT32_MAX)) return fail(AMP_EINVAL, "%s: tensor too large", fn);
+    if (rows * cols == 0) return AMP_OK;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    e = amp::launch_fp8_quant_rowwise(x, xc, rows, cols, fc, eps, static_cast<uint8_t *>(out),
+                                      static_cast<uint8_t *>(out_t), amax_row, scale_row,
+                                      inv_scale_row, amax_col, scale_col, inv_scale_col,
+                                      skip_if_dev, dev, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AMP_OK : cuda_fail(e, fn);
 }
 
 amp_status fp8_quant_tensorwise_list(amp_tensor_list x, amp_tensor_list out, amp_tensor_list out_t,

@@ -1,0 +1,274 @@
+// fp8_rowwise.cu - rowwise FP8 scaling ("FP8训练：量化、自动微分、Torchao" §1:
+// one scale per row instead of one per tensor, §2's formula per row; §4: the
+// column-major copy for the backward GEMMs, whose reduction runs along the
+// rows, carries one scale per column).
+//
+// Four launches, 6 bytes per element as for the tensorwise cast:
+//   zero   amax_row[rows], amax_col[cols] <- +0 (skipped calls write nothing)
+//   amax   one CTA per 128x128 tile reads it once (2 B/elt): every thread holds
+//          8 rows x 8 columns; row maxima are combined across the 16 lanes
+//          sharing a row, column maxima through 8 KB of shared memory; one
+//          atomicMax per row and per column of the tile (fp32 bit patterns of
+//          |x|: an unsigned max that propagates NaN)
+//   scale  per row and per column, scale_d in fp64, fp32 multiplier and
+//          inverse written once
+//   cast   one CTA per tile reads it again (2 B/elt), casts each element twice
+//          (row multiplier for the row-major bytes, column multiplier for the
+//          transposed bytes) and writes both (1 + 1 B/elt), the transposed
+//          tile through the swizzled shared-memory transpose.
+#include <algorithm>
+
+#include "fp8_tile.cuh"
+#include "internal.h"
+
+namespace amp {
+namespace {
+
+// |x| of element k as the bit pattern of an fp32 magnitude (monotone in |x|,
+// NaN above inf).
+template <int XT>
+__device__ __forceinline__ uint32_t abs_f32_bits(const void *x, int64_t k) {
+    if (XT == kF32) return static_cast<const uint32_t *>(x)[k] & 0x7FFFFFFFu;
+    const uint32_t h = static_cast<const uint16_t *>(x)[k] & 0x7FFFu;
+    return XT == kBF16 ? (h << 16) : __float_as_uint(f16_bits_to_f32(h));
+}
+
+template <int XT>
+__device__ __forceinline__ void load8_abs(const void *x, int64_t e, uint32_t (&a)[8]) {
+    if (XT == kF32) {
+        const char *p = static_cast<const char *>(x) + e * 4;
+        const uint4 u = ld_cs(p), v = ld_cs(p + 16);
+        const uint32_t w[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a[j] = w[j] & 0x7FFFFFFFu;
+    } else {
+        const uint4 u = ld_cs(static_cast<const char *>(x) + e * 2);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t lo = w[j] & 0x7FFFu, hi = (w[j] >> 16) & 0x7FFFu;
+            if (XT == kBF16) {
+                a[2 * j] = lo << 16;
+                a[2 * j + 1] = hi << 16;
+            } else {
+                a[2 * j] = __float_as_uint(f16_bits_to_f32(lo));
+                a[2 * j + 1] = __float_as_uint(f16_bits_to_f32(hi));
+            }
+        }
+    }
+}
+
+template <int XT>
+__device__ __forceinline__ void load8_f32(const void *x, int64_t e, float (&y)[8]) {
+    if (XT == kF32) {
+        const char *p = static_cast<const char *>(x) + e * 4;
+        const uint4 u = ld_cs(p), v = ld_cs(p + 16);
+        const uint32_t w[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) y[j] = __uint_as_float(w[j]);
+    } else {
+        const uint4 u = ld_cs(static_cast<const char *>(x) + e * 2);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            y[2 * j] = lowp_to_f32<XT>(w[j] & 0xFFFFu);
+            y[2 * j + 1] = lowp_to_f32<XT>(w[j] >> 16);
+        }
+    }
+}
+
+__device__ __forceinline__ bool tile_fast(const void *x, int64_t rows, int64_t cols, int64_t r0,
+                                          int64_t c0) {
+    return r0 + kTile <= rows && c0 + kTile <= cols && (cols & 7) == 0 && aligned16(x);
+}
+
+__global__ void rowcol_zero_kernel(float *amax_row, int64_t rows, float *amax_col, int64_t cols,
+                                   const int32_t *skip_if) {
+    if (skip_if && *skip_if) return;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < rows + cols;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        if (i < rows) amax_row[i] = 0.0f;
+        else if (amax_col) amax_col[i - rows] = 0.0f;
+    }
+}
+
+template <int XT>
+__global__ void __launch_bounds__(kThreads) rowcol_amax_kernel(const void *x, int64_t rows,
+                                                               int64_t cols, unsigned *amax_row,
+                                                               unsigned *amax_col,
+                                                               const int32_t *skip_if) {
+    if (skip_if && *skip_if) return;
+    __shared__ uint32_t colmax[16][kTile];
+    __shared__ uint32_t s_row[kTile], s_col[kTile];
+    const int64_t tiles_c = (cols + kTile - 1) / kTile;
+    const int64_t r0 = int64_t(blockIdx.x / tiles_c) * kTile;
+    const int64_t c0 = int64_t(blockIdx.x % tiles_c) * kTile;
+    if (tile_fast(x, rows, cols, r0, c0)) {
+        const int c8 = threadIdx.x & 15, rb = threadIdx.x >> 4;
+        uint32_t cm[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        uint32_t a[8][8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) load8_abs<XT>(x, (r0 + rb + 16 * k) * cols + c0 + 8 * c8, a[k]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            uint32_t rm = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                rm = max(rm, a[k][j]);
+                cm[j] = max(cm[j], a[k][j]);
+            }
+            // the 16 lanes holding this row: lanes 0-15 or 16-31 of the warp
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) rm = max(rm, __shfl_xor_sync(0xFFFFFFFFu, rm, off));
+            if (c8 == 0 && rm != 0) atomicMax(amax_row + r0 + rb + 16 * k, rm);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) colmax[rb][8 * c8 + j] = cm[j];
+        __syncthreads();
+        if (threadIdx.x < kTile) {
+            uint32_t m = 0;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) m = max(m, colmax[r][threadIdx.x]);
+            if (amax_col && m != 0) atomicMax(amax_col + c0 + threadIdx.x, m);
+        }
+    } else {
+        if (threadIdx.x < kTile) s_row[threadIdx.x] = s_col[threadIdx.x] = 0u;
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < kTile * kTile; idx += kThreads) {
+            const int64_t i = r0 + (idx >> 7), j = c0 + (idx & (kTile - 1));
+            if (i < rows && j < cols) {
+                const uint32_t v = abs_f32_bits<XT>(x, i * cols + j);
+                atomicMax(&s_row[idx >> 7], v);
+                atomicMax(&s_col[idx & (kTile - 1)], v);
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x < kTile) {
+            const int t = threadIdx.x;
+            if (r0 + t < rows && s_row[t] != 0) atomicMax(amax_row + r0 + t, s_row[t]);
+            if (amax_col && c0 + t < cols && s_col[t] != 0) atomicMax(amax_col + c0 + t, s_col[t]);
+        }
+    }
+}
+
+__global__ void rowcol_scale_kernel(const float *amax_row, float *scale_row, float *inv_row,
+                                    int64_t rows, const float *amax_col, float *scale_col,
+                                    float *inv_col, int64_t cols, double eps, float fmax,
+                                    const int32_t *skip_if) {
+    if (skip_if && *skip_if) return;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < rows + cols;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        if (i < rows) {
+            tensor_scale(amax_row[i], eps, fmax, scale_row[i], inv_row[i]);
+        } else if (amax_col) {
+            const int64_t j = i - rows;
+            tensor_scale(amax_col[j], eps, fmax, scale_col[j], inv_col[j]);
+        }
+    }
+}
+
+template <int XT, int FT>
+__global__ void __launch_bounds__(kThreads) rowcol_cast_kernel(const void *x, int64_t rows,
+                                                               int64_t cols, uint8_t *out,
+                                                               uint8_t *out_t,
+                                                               const float *scale_row,
+                                                               const float *scale_col,
+                                                               const int32_t *skip_if) {
+    if (skip_if && *skip_if) return;
+    __shared__ __align__(16) uint32_t sm[kTile * 32];
+    const int64_t tiles_c = (cols + kTile - 1) / kTile;
+    const int64_t r0 = int64_t(blockIdx.x / tiles_c) * kTile;
+    const int64_t c0 = int64_t(blockIdx.x % tiles_c) * kTile;
+    const bool fast = tile_fast(x, rows, cols, r0, c0) &&
+                      (reinterpret_cast<uintptr_t>(out) & 7) == 0 &&
+                      (out_t == nullptr || ((rows & 15) == 0 && aligned16(out_t)));
+    if (fast) {
+        const int c8 = threadIdx.x & 15, rb = threadIdx.x >> 4;
+        float sc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) sc[j] = out_t ? scale_col[c0 + 8 * c8 + j] : 0.0f;
+#pragma unroll 2
+        for (int k = 0; k < 8; ++k) {
+            const int r = rb + 16 * k;
+            const int64_t e = (r0 + r) * cols + c0 + 8 * c8;
+            float y[8];
+            load8_f32<XT>(x, e, y);
+            const float sr = scale_row[r0 + r];
+            uint32_t h[4], g[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                h[j] = f32x2_to_fp8x2<FT>(__fmul_rn(y[2 * j], sr), __fmul_rn(y[2 * j + 1], sr));
+                g[j] = f32x2_to_fp8x2<FT>(__fmul_rn(y[2 * j], sc[2 * j]),
+                                          __fmul_rn(y[2 * j + 1], sc[2 * j + 1]));
+            }
+            *reinterpret_cast<uint2 *>(out + e) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+            if (out_t)
+                *reinterpret_cast<uint2 *>(sm + swz(r, 2 * c8)) =
+                    make_uint2(g[0] | (g[1] << 16), g[2] | (g[3] << 16));
+        }
+        if (out_t) {
+            __syncthreads();
+            store_transposed_tile(sm, out_t, rows, r0, c0);
+        }
+    } else {
+        for (int idx = threadIdx.x; idx < kTile * kTile; idx += kThreads) {
+            const int64_t i = r0 + (idx >> 7), j = c0 + (idx & (kTile - 1));
+            if (i < rows && j < cols) {
+                const float v = XT == kF32 ? static_cast<const float *>(x)[i * cols + j]
+                                           : lowp_to_f32<XT>(static_cast<const uint16_t *>(x)[i * cols + j]);
+                out[i * cols + j] = quant1<FT>(v, scale_row[i]);
+                if (out_t) out_t[j * rows + i] = quant1<FT>(v, scale_col[j]);
+            }
+        }
+    }
+}
+
+template <int XT, int FT>
+cudaError_t launch_rowwise_t(const void *x, int64_t rows, int64_t cols, uint8_t *out,
+                             uint8_t *out_t, float *amax_row, float *scale_row, float *inv_row,
+                             float *amax_col, float *scale_col, float *inv_col, double eps,
+                             const int32_t *skip_if, int device, cudaStream_t s) {
+    const int64_t n_rc = rows + (out_t ? cols : 0);
+    const unsigned small_grid =
+        (unsigned)std::max<int64_t>(1, std::min<int64_t>((n_rc + 255) / 256, sm_count(device) * 4));
+    float *acol = out_t ? amax_col : nullptr;
+    rowcol_zero_kernel<<<small_grid, 256, 0, s>>>(amax_row, rows, acol, out_t ? cols : 0, skip_if);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
+    if (tiles == 0) return cudaSuccess;
+    rowcol_amax_kernel<XT><<<(unsigned)tiles, kThreads, 0, s>>>(
+        x, rows, cols, reinterpret_cast<unsigned *>(amax_row), reinterpret_cast<unsigned *>(acol),
+        skip_if);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    rowcol_scale_kernel<<<small_grid, 256, 0, s>>>(amax_row, scale_row, inv_row, rows, acol,
+                                                   scale_col, inv_col, out_t ? cols : 0, eps,
+                                                   fp8_max<FT>(), skip_if);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    rowcol_cast_kernel<XT, FT><<<(unsigned)tiles, kThreads, 0, s>>>(x, rows, cols, out, out_t,
+                                                                     scale_row, scale_col, skip_if);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fp8_quant_rowwise(const void *x, int xelem, int64_t rows, int64_t cols, int fp8,
+                                     double eps, uint8_t *out, uint8_t *out_t, float *amax_row,
+                                     float *scale_row, float *inv_row, float *amax_col,
+                                     float *scale_col, float *inv_col, const int32_t *skip_if,
+                                     int device, cudaStream_t s) {
+#define AMP_RW(XT, FT)                                                                           \
+    return launch_rowwise_t<XT, FT>(x, rows, cols, out, out_t, amax_row, scale_row, inv_row,     \
+                                    amax_col, scale_col, inv_col, eps, skip_if, device, s)
+    if (fp8 == kE4M3) {
+        if (xelem == kBF16) AMP_RW(kBF16, kE4M3);
+        if (xelem == kF16) AMP_RW(kF16, kE4M3);
+        AMP_RW(kF32, kE4M3);
+    }
+    if (xelem == kBF16) AMP_RW(kBF16, kE5M2);
+    if (xelem == kF16) AMP_RW(kF16, kE5M2);
+    AMP_RW(kF32, kE5M2);
+#undef AMP_RW
+}
+
+}  // namespace amp

@@ -97,6 +97,12 @@ cudaError_t launch_fp8_quant(const void *x, int xelem, int64_t rows, int64_t col
                              float *amax, int amax_given, const int32_t *skip_if, int device,
                              cudaStream_t s);
 
+cudaError_t launch_fp8_quant_rowwise(const void *x, int xelem, int64_t rows, int64_t cols, int fp8,
+                                     double eps, uint8_t *out, uint8_t *out_t, float *amax_row,
+                                     float *scale_row, float *inv_row, float *amax_col,
+                                     float *scale_col, float *inv_col, const int32_t *skip_if,
+                                     int device, cudaStream_t s);
+
 cudaError_t launch_fp8_quant_list(const ListView &x, int64_t n_tiles, int xelem,
                                   const ListView &out, const ListView *out_t, int fp8,
                                   double eps, const float *amax, float *inv_scale,

@@ -206,3 +206,23 @@ def test_llama3_8b_bench_state_parity(A, fp8_scaling):
     st.close()
     del st, info
     torch.cuda.empty_cache()
+
+
+def test_fp8_sweep_rowwise_full_parity(A):
+    """The sweep matrices with per-row / per-column scales, every byte and scale."""
+    dev = torch.device("cuda:0")
+    for j, (r, c) in enumerate(FP8_SWEEP_SHAPES + [FP8_SWEEP_ZERO_SHAPE]):
+        xh = fp8_sweep_host(r, c, seed=0, zero=(j == len(FP8_SWEEP_SHAPES)))
+        x = to_device(xh, "bf16", dev).view(r, c)
+        o = {"q": torch.empty(r * c, dtype=torch.uint8, device=dev),
+             "q_t": torch.empty(r * c, dtype=torch.uint8, device=dev)}
+        o.update({k: torch.empty(r, device=dev) for k in ("amax_row", "scale_row", "inv_row")})
+        o.update({k: torch.empty(c, device=dev) for k in ("amax_col", "scale_col", "inv_col")})
+        A.fp8_quant_rowwise(x, "e4m3fn", o["q"], o["q_t"], o["amax_row"], o["scale_row"],
+                            o["inv_row"], o["amax_col"], o["scale_col"], o["inv_col"])
+        ref = O.fp8_quant_rowwise(xh, "bf16", r, c, "e4m3fn")
+        for k in ref:
+            g = to_host_bits(o[k])
+            assert np.array_equal(g.view(np.uint8) if g.dtype == np.uint8 else g.view(np.uint32),
+                                  ref[k] if ref[k].dtype == np.uint8 else ref[k].view(np.uint32)), (k, r, c)
+        del x, o

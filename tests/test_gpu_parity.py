@@ -584,3 +584,59 @@ def test_delayed_fp8_step_composition(A, dev, hist_len, gdt):
         assert np.array_equal(to_host_bits(st.exp_avg[i]).view(np.uint32), orc.exp_avg[i].view(np.uint32))
         assert np.array_equal(to_host_bits(st.bf16[i]), orc.bf16[i])
     st.close()
+
+
+# ----------------------------------------------------------- rowwise FP8
+def _run_rowwise(A, dev, xh, xdt, rows, cols, fmt, with_t, skip=None, misalign=False):
+    x = _device_views([xh], xdt, dev, misalign)[0].view(rows, cols)
+    o = {"q": torch.full((rows * cols,), 0xA5, dtype=torch.uint8, device=dev)}
+    o.update({k: torch.full((rows,), -1.0, device=dev) for k in ("amax_row", "scale_row", "inv_row")})
+    if with_t:
+        o["q_t"] = torch.full((rows * cols,), 0x5A, dtype=torch.uint8, device=dev)
+        o.update({k: torch.full((cols,), -1.0, device=dev) for k in ("amax_col", "scale_col", "inv_col")})
+    sk = None if skip is None else torch.tensor([skip], dtype=torch.int32, device=dev)
+    A.fp8_quant_rowwise(x, fmt, o["q"], o.get("q_t"), o["amax_row"], o["scale_row"], o["inv_row"],
+                        o.get("amax_col"), o.get("scale_col"), o.get("inv_col"), skip_if=sk)
+    return {k: to_host_bits(v) for k, v in o.items()}
+
+
+@pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
+@pytest.mark.parametrize("xdt", ["bf16", "f16", "f32"])
+def test_fp8_rowwise_parity(A, dev, fmt, xdt):
+    rng = np.random.default_rng(90)
+    for rows, cols in FP8_SHAPES:
+        xh = _x_host(rng, rows, cols, xdt)
+        if rows > 3:                       # a zero row: its scale clamps to EPS
+            if xdt == "f32":
+                xh.reshape(rows, cols)[2] = 0
+            else:
+                xh.reshape(rows, cols)[2] = 0
+        for with_t in (True, False):
+            for misalign in ((False, True) if rows * cols > 8 else (False,)):
+                got = _run_rowwise(A, dev, xh, xdt, rows, cols, fmt, with_t, misalign=misalign)
+                ref = O.fp8_quant_rowwise(xh, xdt, rows, cols, fmt, transposed=with_t)
+                key = (rows, cols, with_t, misalign)
+                for k in ref:
+                    if ref[k].dtype == np.float32:
+                        assert np.array_equal(got[k].view(np.uint32), ref[k].view(np.uint32)), (k, key)
+                    else:
+                        assert np.array_equal(got[k], ref[k]), (k, key)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
+def test_fp8_rowwise_degenerate(A, dev, fmt):
+    rng = np.random.default_rng(91)
+    rows, cols = 256, 384
+    xh = _x_host(rng, rows, cols, "f32")
+    xh[5 * cols + 7] = np.nan            # row 5 and column 7 become NaN; others unaffected
+    xh[9 * cols + 100] = -np.inf         # row 9 and column 100: amax inf
+    got = _run_rowwise(A, dev, xh, "f32", rows, cols, fmt, True)
+    ref = O.fp8_quant_rowwise(xh, "f32", rows, cols, fmt)
+    assert np.array_equal(got["q"], ref["q"]) and np.array_equal(got["q_t"], ref["q_t"])
+    for k in ("amax_row", "scale_row", "inv_row", "amax_col", "scale_col", "inv_col"):
+        g, r = got[k], ref[k]
+        assert np.array_equal(np.isnan(g), np.isnan(r)), k
+        assert np.array_equal(g[~np.isnan(r)], r[~np.isnan(r)]), k
+    skipped = _run_rowwise(A, dev, xh, "f32", rows, cols, fmt, True, skip=1)
+    assert np.all(skipped["q"] == 0xA5) and np.all(skipped["q_t"] == 0x5A)
+    assert np.all(skipped["amax_row"] == -1.0) and np.all(skipped["inv_col"] == -1.0)
