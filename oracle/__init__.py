@@ -65,6 +65,14 @@ def lib():
             L.orc_adamw_master_step_clip.argtypes = (
                 [ctypes.c_int, P, P, P, P, ctypes.c_int, P, I64P, P, ctypes.c_int32, P]
                 + [ctypes.c_double] * 5 + [P, P, ctypes.c_float])
+            L.orc_adamw_master_step_ex.argtypes = (
+                [ctypes.c_int, P, P, P, P, ctypes.c_int, P, I64P, P, ctypes.c_int32, P]
+                + [ctypes.c_double] * 5 + [P, P, ctypes.c_float, ctypes.c_int, ctypes.c_uint64])
+            L.orc_philox4x32_10.argtypes = [P, P, P]
+            L.orc_bf16_stochastic.restype = ctypes.c_uint16
+            L.orc_bf16_stochastic.argtypes = [ctypes.c_float, ctypes.c_uint32]
+            L.orc_bf16_stochastic_list.argtypes = [P, P, ctypes.c_int64, ctypes.c_uint64,
+                                                   ctypes.c_int32, ctypes.c_int32]
             L.orc_fp8_quant_rowwise.argtypes = [P, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                                                 ctypes.c_int, ctypes.c_double] + [P] * 8
             L.orc_fp8_quant_tensorwise.argtypes = [P, ctypes.c_int, ctypes.c_int64,
@@ -152,7 +160,7 @@ def clip_coef(sumsq: float, max_norm: float) -> float:
 def adamw_master_step(master, exp_avg, exp_avg_sq, grads, gdt: str, bf16_out, scale,
                       found_inf: int, step: int, lr, beta1, beta2, eps, wd,
                       amax_slot=None, amax: np.ndarray | None = None,
-                      clip: float | None = None) -> int:
+                      clip: float | None = None, sr_seed: int | None = None) -> int:
     """FP32-master AdamW over a tensor list (in place); returns the new step count.
     ``scale`` None means S = 1. ``bf16_out`` is a list of uint16 arrays or None.
     ``clip`` is the fp32 gradient clipping factor (None: no clipping)."""
@@ -166,11 +174,31 @@ def adamw_master_step(master, exp_avg, exp_avg_sq, grads, gdt: str, bf16_out, sc
             lr, beta1, beta2, eps, wd,
             _ptr(slots) if slots is not None else None,
             _ptr(amax) if amax is not None else None]
-    if clip is None:
+    if sr_seed is not None:
+        lib().orc_adamw_master_step_ex(*args, ctypes.c_float(1.0 if clip is None else clip), 1,
+                                       ctypes.c_uint64(sr_seed))
+    elif clip is None:
         lib().orc_adamw_master_step(*args)
     else:
         lib().orc_adamw_master_step_clip(*args, ctypes.c_float(clip))
     return int(st[0])
+
+
+def philox4x32_10(ctr, key):
+    c = np.ascontiguousarray(ctr, np.uint32)
+    k = np.ascontiguousarray(key, np.uint32)
+    o = np.zeros(4, np.uint32)
+    lib().orc_philox4x32_10(_ptr(c), _ptr(k), _ptr(o))
+    return o
+
+
+def bf16_stochastic(p: np.ndarray, seed: int, step: int, tensor: int) -> np.ndarray:
+    """Stochastically rounded bf16 bits of fp32 p, random bits from the counter
+    {element group, step, tensor} and key seed."""
+    p = np.ascontiguousarray(p, np.float32)
+    out = np.empty(p.size, np.uint16)
+    lib().orc_bf16_stochastic_list(_ptr(p), _ptr(out), p.size, seed, step, tensor)
+    return out
 
 
 def fp8_quant_tensorwise(x: np.ndarray, xdt: str, rows: int, cols: int, fp8: str,

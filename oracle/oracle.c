@@ -284,6 +284,15 @@ void orc_adamw_master_step_clip(int n_tensors, float *const *master, float *cons
                                 const float *scale, int32_t found_inf, int32_t *step,
                                 double lr, double beta1, double beta2, double eps, double wd,
                                 const int32_t *amax_slot, float *amax, float clip_coef);
+void orc_adamw_master_step_ex(int n_tensors, float *const *master, float *const *exp_avg,
+                              float *const *exp_avg_sq, void *const *grads, int gdtype,
+                              uint16_t *const *bf16_out, const int64_t *numel,
+                              const float *scale, int32_t found_inf, int32_t *step,
+                              double lr, double beta1, double beta2, double eps, double wd,
+                              const int32_t *amax_slot, float *amax, float clip_coef,
+                              int stochastic, uint64_t seed);
+static uint32_t sr_bits(uint64_t seed, int32_t step, int32_t tensor, int64_t k);
+uint16_t orc_bf16_stochastic(float p, uint32_t u);
 
 void orc_adamw_master_step(int n_tensors, float *const *master, float *const *exp_avg,
                            float *const *exp_avg_sq, void *const *grads, int gdtype,
@@ -305,6 +314,22 @@ void orc_adamw_master_step_clip(int n_tensors, float *const *master, float *cons
                                 const float *scale, int32_t found_inf, int32_t *step,
                                 double lr, double beta1, double beta2, double eps, double wd,
                                 const int32_t *amax_slot, float *amax, float clip_coef)
+{
+    orc_adamw_master_step_ex(n_tensors, master, exp_avg, exp_avg_sq, grads, gdtype, bf16_out,
+                             numel, scale, found_inf, step, lr, beta1, beta2, eps, wd, amax_slot,
+                             amax, clip_coef, 0, 0);
+}
+
+/* As above; with stochastic != 0 the bf16 copy is rounded stochastically
+ * (orc_bf16_stochastic, random bits of element k of tensor i at the new step
+ * count t from sr_bits(seed, t, i, k)) instead of to nearest-even. */
+void orc_adamw_master_step_ex(int n_tensors, float *const *master, float *const *exp_avg,
+                              float *const *exp_avg_sq, void *const *grads, int gdtype,
+                              uint16_t *const *bf16_out, const int64_t *numel,
+                              const float *scale, int32_t found_inf, int32_t *step,
+                              double lr, double beta1, double beta2, double eps, double wd,
+                              const int32_t *amax_slot, float *amax, float clip_coef,
+                              int stochastic, uint64_t seed)
 {
     if (found_inf)
         return; /* skipped step: no state, output or counter changes */
@@ -335,7 +360,8 @@ void orc_adamw_master_step_clip(int n_tensors, float *const *master, float *cons
             exp_avg[i][k] = m;
             exp_avg_sq[i][k] = v;
             if (bf16_out && bf16_out[i]) {
-                uint16_t b = (uint16_t)fmt_encode(&FMT_BF16, (double)p);
+                uint16_t b = stochastic ? orc_bf16_stochastic(p, sr_bits(seed, t, i, k))
+                                        : (uint16_t)fmt_encode(&FMT_BF16, (double)p);
                 bf16_out[i][k] = b;
                 if (slot >= 0) {
                     float a = fabsf((float)fmt_decode(&FMT_BF16, b));
@@ -465,4 +491,74 @@ void orc_fp8_quant_rowwise(const void *x, int xdtype, int64_t rows, int64_t cols
         for (int64_t i = 0; i < rows; ++i)
             out_t[j * rows + i] = cast_scaled(f, load_as_f32(xdtype, x, i * cols + j), scale_col[j]);
     }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Stochastic rounding of the bf16 working copy.  "第20章 量化与混合精度训练"  */
+/* §20.5.14: instead of round-to-nearest, round down or up with probability   */
+/* proportional to the distance, so the expected value is the input.  For a  */
+/* finite fp32 p between two neighbouring bf16 values lo (toward zero) and hi */
+/* (away from zero, inf beyond the largest finite), the result is hi with     */
+/* probability (|p| - |lo|) / (|hi| - |lo|): with 16 uniform random bits u,    */
+/* hi exactly when u < the 16 low bits of p's magnitude pattern.  NaN gives   */
+/* the canonical NaN, values already on the grid stay.                        */
+/*                                                                            */
+/* Random bits: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random   */
+/* numbers: as easy as 1, 2, 3", SC 2011): a 4x32-bit counter, a 2x32-bit key, */
+/* ten rounds of two 32x32->64 multiplies and xors, key bumped by the golden-  */
+/* ratio and sqrt(3)-1 Weyl constants between rounds.                          */
+/* Counter of element k of tensor t at optimizer step s: {k/8 low, k/8 high,   */
+/* s, t}; key = the 64-bit seed {low, high}; element k takes the 16-bit half    */
+/* (k%8)%2 (low half first) of output word (k%8)/2.                            */
+/* ------------------------------------------------------------------------ */
+void orc_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4])
+{
+    uint32_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+    uint32_t k0 = key_in[0], k1 = key_in[1];
+    for (int r = 0; r < 10; ++r) {
+        uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+        uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+        uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+        uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+        c0 = hi1 ^ c1 ^ k0;
+        c1 = lo1;
+        c2 = hi0 ^ c3 ^ k1;
+        c3 = lo0;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* the 16 random bits of element k */
+static uint32_t sr_bits(uint64_t seed, int32_t step, int32_t tensor, int64_t k)
+{
+    uint64_t grp = (uint64_t)k >> 3;
+    uint32_t ctr[4] = {(uint32_t)grp, (uint32_t)(grp >> 32), (uint32_t)step, (uint32_t)tensor};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t o[4];
+    orc_philox4x32_10(ctr, key, o);
+    int lane = (int)(k & 7);
+    uint32_t w = o[lane >> 1];
+    return (lane & 1) ? (w >> 16) : (w & 0xFFFFu);
+}
+
+/* stochastic rounding of p to bf16 with the random 16 bits u */
+uint16_t orc_bf16_stochastic(float p, uint32_t u)
+{
+    if (isnan(p))
+        return (uint16_t)FMT_BF16.nan_code;
+    uint32_t bits;
+    memcpy(&bits, &p, 4);
+    uint32_t sign = bits & 0x80000000u, mag = bits & 0x7FFFFFFFu;
+    uint32_t lo = mag >> 16, frac = mag & 0xFFFFu;
+    uint32_t r = lo + ((u & 0xFFFFu) < frac ? 1u : 0u);  /* P(up) = frac / 2^16 */
+    return (uint16_t)((sign >> 16) | r);
+}
+
+void orc_bf16_stochastic_list(const float *p, uint16_t *out, int64_t n, uint64_t seed,
+                              int32_t step, int32_t tensor)
+{
+    for (int64_t k = 0; k < n; ++k)
+        out[k] = orc_bf16_stochastic(p[k], sr_bits(seed, step, tensor, k));
 }

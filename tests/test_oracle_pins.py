@@ -549,3 +549,57 @@ def test_rowwise_vs_torch_ops(fmt, tdt):
         assert np.array_equal(r[qk], ref.ravel())
         assert np.array_equal(r["inv_" + key], sc.reciprocal().float().numpy().ravel())
         assert np.array_equal(r["amax_" + key], am.numpy().ravel())
+
+
+# ---------------------------------------------------- stochastic rounding
+def test_philox_known_answers():
+    """Philox4x32-10 known-answer vectors of its authors' reference release
+    (Salmon et al., 'Parallel random numbers: as easy as 1, 2, 3', SC 2011)."""
+    kat = [([0, 0, 0, 0], [0, 0], [0x6627e8d5, 0xe169c58d, 0xbc57ac4c, 0x9b00dbd8]),
+           ([0xffffffff] * 4, [0xffffffff] * 2, [0x408f276d, 0x41c83b0e, 0xa20bc7c6, 0x6d5451fd]),
+           ([0x243f6a88, 0x85a308d3, 0x13198a2e, 0x03707344], [0xa4093822, 0x299f31d0],
+            [0xd16cfe09, 0x94fdcceb, 0x5001e420, 0x24126ea1])]
+    for ctr, key, want in kat:
+        assert O.philox4x32_10(ctr, key).tolist() == want
+
+
+def test_stochastic_rounding_is_unbiased_and_on_grid():
+    """'第20章 量化与混合精度训练' §20.5.14: round down or up with probability
+    proportional to the distance; the expected value is the input."""
+    p = np.full(200000, np.float32(1.0 + 1e-3), np.float32)        # between two bf16 values
+    lo, hi = 1.0, 1.0 + 2.0 ** -7
+    b = O.bf16_stochastic(p, seed=1234, step=1, tensor=0)
+    vals = O.decode("bf16", b).astype(np.float64)
+    assert set(np.unique(vals)) <= {lo, hi}
+    frac_up = np.mean(vals == hi)
+    want = (float(p[0]) - lo) / (hi - lo)
+    assert abs(frac_up - want) < 5 * np.sqrt(want * (1 - want) / p.size)
+    assert abs(vals.mean() - float(p[0])) < 5 * (hi - lo) * np.sqrt(want * (1 - want) / p.size)
+    # exact grid values, zeros, inf and NaN are left as RNE leaves them
+    special = np.array([1.25, -0.0, 0.0, np.inf, -np.inf, np.nan, 65536.0], np.float32)
+    assert np.array_equal(O.bf16_stochastic(special, 7, 3, 1), O.encode("bf16", special))
+    # negative values mirror positive ones (rounding away from zero is "up")
+    q = O.bf16_stochastic(-p[:1000], 1234, 1, 0)
+    assert np.array_equal(q & 0x7FFF, b[:1000])
+
+
+def test_adamw_with_stochastic_rounding_keeps_master_and_rounds_copy():
+    rng = np.random.default_rng(62)
+    p0 = [rng.standard_normal(5000).astype(F32) * F32(0.02)]
+    g = [rng.standard_normal(5000).astype(F32) * F32(1e-3)]
+    m1, v1 = [np.zeros(5000, F32)], [np.zeros(5000, F32)]
+    m2, v2 = [np.zeros(5000, F32)], [np.zeros(5000, F32)]
+    a, b = [p0[0].copy()], [p0[0].copy()]
+    ba, bb = [np.zeros(5000, np.uint16)], [np.zeros(5000, np.uint16)]
+    O.adamw_master_step(a, m1, v1, g, "f32", ba, None, 0, 0, 1e-3, 0.9, 0.999, 1e-8, 0.01)
+    O.adamw_master_step(b, m2, v2, g, "f32", bb, None, 0, 0, 1e-3, 0.9, 0.999, 1e-8, 0.01,
+                        sr_seed=99)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(m1[0], m2[0])      # state unchanged
+    assert np.array_equal(bb[0], O.bf16_stochastic(b[0], 99, 1, 0))         # step t = 1, tensor 0
+    d = bf16_ulp_steps(ba[0], bb[0])
+    assert d.max() <= 1 and 0 < np.mean(d) < 1
+
+
+def bf16_ulp_steps(a, b):
+    key = lambda x: np.where(x & 0x8000, -(x.astype(np.int64) & 0x7FFF), x.astype(np.int64) & 0x7FFF)
+    return np.abs(key(a) - key(b))
