@@ -192,6 +192,8 @@ def run_ours(args, rank, world, device):
     delayed = step.fp8_scaling == "delayed"
     if delayed and args.clip is not None:
         raise SystemExit("--clip with --fp8-scaling delayed is not supported")
+    if args.sr_seed is not None and (delayed or args.clip is not None):
+        raise SystemExit("--sr-seed goes with the plain dynamic step")
     if delayed:
         info["bytes_adamw"] += 2 * info["fp8_params"]       # fp8 + fp8T written in the same pass
         info["bytes_quant"] = 0
@@ -225,6 +227,10 @@ def run_ours(args, rank, world, device):
                                                 step.inv_scale, step.scale, step.found_inf,
                                                 step.step_count, *step.hyper,
                                                 fp8_eps=step.fp8_eps, stream=stream)
+        elif args.sr_seed is not None:
+            A.amp_adamw_master_step_sr(step.L_master, step.L_m, step.L_v, step.L_g, step.L_b,
+                                       step.scale, step.found_inf, step.step_count, *step.hyper,
+                                       args.sr_seed, amax=amax, stream=stream)
         elif args.clip is None:
             A.amp_adamw_master_step(step.L_master, step.L_m, step.L_v, step.L_g, step.L_b,
                                     step.scale, step.found_inf, step.step_count, *step.hyper,
@@ -311,6 +317,7 @@ def run_ours(args, rank, world, device):
         "config": dict(workload_config(args.workload, world), per_step_bytes=total_bytes),
         "hbm_gbs_step": total_bytes / (ms_step * 1e-3) / 1e9,
         "grad_clip": args.clip,
+        "bf16_rounding": "stochastic" if args.sr_seed is not None else "nearest-even",
         "fp8_scaling": step.fp8_scaling,
         "kernels_ms": {"unscale_check": statistics.mean(k_check),
                        "adamw_master_step": adamw_ms,
@@ -574,6 +581,8 @@ def main():
                          "previous step's (cast fused into the AdamW pass)")
     ap.add_argument("--fp8-granularity", default="tensorwise", choices=["tensorwise", "rowwise"],
                     help="scale granularity of the fp8_sweep workload")
+    ap.add_argument("--sr-seed", type=int, default=None,
+                    help="round the bf16 copy stochastically (Philox4x32-10 with this seed)")
     ap.add_argument("--clip", type=float, default=None,
                     help="also clip the unscaled gradients to this global L2 norm")
     args = ap.parse_args()

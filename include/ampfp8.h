@@ -202,6 +202,26 @@ amp_status amp_adamw_master_step_clip(amp_tensor_list master, amp_tensor_list ex
                                       const double *grad_sumsq_dev, double max_norm,
                                       amp_stream_t stream);
 
+/* amp_adamw_master_step with the bf16 working copy rounded stochastically
+ * ("第20章 量化与混合精度训练" §20.5.14: round down or up with probability
+ * proportional to the distance, so the expected value is the input) instead
+ * of to nearest-even; master, m, v and the amax fold are as in
+ * amp_adamw_master_step.  For a finite fp32 p the result is the bf16 value
+ * away from zero (inf beyond the largest finite) with probability
+ * (16 dropped bits of |p|) / 2^16, else the one toward zero; values on the
+ * bf16 grid and infinities are kept, NaN gives 0x7FC0.  Random bits:
+ * Philox4x32-10 (Salmon et al., SC 2011) with key = seed and counter
+ * {k/8 (low, high 32 bits), t, i} for element k of tensor i at step t (the
+ * step counter after this step); element k uses 16-bit half (k%8)%2 (low
+ * first) of output word (k%8)/2.  Deterministic for a given seed and step.
+ * Errors: as amp_adamw_master_step, and AMP_EINVAL for a NULL bf16_out. */
+amp_status amp_adamw_master_step_sr(amp_tensor_list master, amp_tensor_list exp_avg,
+                                    amp_tensor_list exp_avg_sq, amp_tensor_list grads,
+                                    amp_tensor_list bf16_out, const float *scale_dev,
+                                    const int32_t *found_inf_dev, int32_t *step_dev,
+                                    const amp_adamw_hyper *hyper, float *amax_dev, uint64_t seed,
+                                    amp_stream_t stream);
+
 /* Allocation-free form of amp_adamw_master_step.  The pages have no
  * counterpart: it exists for callers that cannot allocate device memory -
  * runtimes that serve all device memory from their own arena, loops that must

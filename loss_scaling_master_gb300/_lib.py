@@ -26,7 +26,8 @@ _TORCH_DT = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16",
 # every symbol include/ampfp8.h declares
 EXPORTS = ("amp_tensor_list_create", "amp_tensor_list_set_amax_slots", "amp_tensor_list_destroy",
            "amp_unscale_check", "amp_unscale_check_norm", "amp_adamw_master_step",
-           "amp_adamw_master_step_clip", "amp_adamw_master_step_noalloc",
+           "amp_adamw_master_step_clip", "amp_adamw_master_step_sr",
+           "amp_adamw_master_step_noalloc",
            "amp_adamw_master_step_fp8_delayed", "amp_update_scale_fp8_history",
            "fp8_quant_tensorwise", "fp8_quant_tensorwise_list", "fp8_quant_rowwise",
            "amp_update_scale",
@@ -69,6 +70,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.amp_unscale_check_norm.argtypes = [P, P, P, P, P]
         L.amp_adamw_master_step_clip.argtypes = [P, P, P, P, P, P, P, P,
                                                  ctypes.POINTER(amp_adamw_hyper), P, P, dbl, P]
+        L.amp_adamw_master_step_sr.argtypes = [P, P, P, P, P, P, P, P,
+                                               ctypes.POINTER(amp_adamw_hyper), P,
+                                               ctypes.c_uint64, P]
         L.amp_adamw_master_step_noalloc.argtypes = [i32, P, P, P, P, i32, P, P, P, P, P, P,
                                                     ctypes.POINTER(amp_adamw_hyper), P, P]
         L.amp_adamw_master_step_fp8_delayed.argtypes = [P] * 12 + [i32, dbl, P, i32, P, P, P, P,
@@ -195,6 +199,18 @@ def amp_adamw_master_step_clip(master: TensorList, exp_avg: TensorList, exp_avg_
                                              _dptr(scale), _dptr(found_inf), _dptr(step),
                                              ctypes.byref(h), _dptr(amax), _dptr(grad_sumsq),
                                              float(max_norm), _stream(stream)))
+
+
+def amp_adamw_master_step_sr(master: TensorList, exp_avg: TensorList, exp_avg_sq: TensorList,
+                             grads: TensorList, bf16_out: TensorList, scale, found_inf, step,
+                             lr: float, beta1: float, beta2: float, eps: float,
+                             weight_decay: float, seed: int, amax=None, stream=None):
+    h = amp_adamw_hyper(lr, beta1, beta2, eps, weight_decay)
+    _check("amp_adamw_master_step_sr",
+           load().amp_adamw_master_step_sr(master.handle, exp_avg.handle, exp_avg_sq.handle,
+                                           grads.handle, bf16_out.handle, _dptr(scale),
+                                           _dptr(found_inf), _dptr(step), ctypes.byref(h),
+                                           _dptr(amax), ctypes.c_uint64(seed), _stream(stream)))
 
 
 def amp_adamw_master_step(master: TensorList, exp_avg: TensorList, exp_avg_sq: TensorList,

@@ -18,6 +18,7 @@
 //             parameter (fp16/bf16 grads, bf16 emission).
 #include "fp8_tile.cuh"
 #include "internal.h"
+#include "philox.cuh"
 
 namespace amp {
 namespace {
@@ -29,6 +30,7 @@ struct AdamwParams {
     float *amax;
     float decay, b1, omb1, b2, omb2, eps;
     int use_slots;
+    uint64_t sr_seed;  // stochastic bf16 rounding key
 };
 
 struct Scal {
@@ -86,10 +88,10 @@ __device__ __forceinline__ void u4_set(uint4 &w, int j, float f) {
     if (j == 0) w.x = b; else if (j == 1) w.y = b; else if (j == 2) w.z = b; else w.w = b;
 }
 
-template <int GT, bool BF16>
+template <int GT, bool BF16, bool SR = false>
 __device__ __forceinline__ uint4 compute_store_group(Group<GT> &r, float *pp, float *mp, float *vp,
                                                      uint16_t *bp, int64_t e, const Scal &s,
-                                                     uint32_t &amax2) {
+                                                     uint32_t &amax2, const uint4 *rnd = nullptr) {
     float p[8], m[8], v[8], g[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -124,10 +126,20 @@ __device__ __forceinline__ uint4 compute_store_group(Group<GT> &r, float *pp, fl
     st_cs(vp + e + 4, r.v[1]);
     if (BF16) {
         uint4 o;
-        o.x = f32x2_to_bf16x2(p[0], p[1]);
-        o.y = f32x2_to_bf16x2(p[2], p[3]);
-        o.z = f32x2_to_bf16x2(p[4], p[5]);
-        o.w = f32x2_to_bf16x2(p[6], p[7]);
+        if constexpr (SR) {
+            const uint32_t w[4] = {rnd->x, rnd->y, rnd->z, rnd->w};
+            uint32_t h[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                h[j] = bf16_stochastic(p[2 * j], w[j] & 0xFFFFu) |
+                       (bf16_stochastic(p[2 * j + 1], w[j] >> 16) << 16);
+            o = make_uint4(h[0], h[1], h[2], h[3]);
+        } else {
+            o.x = f32x2_to_bf16x2(p[0], p[1]);
+            o.y = f32x2_to_bf16x2(p[2], p[3]);
+            o.z = f32x2_to_bf16x2(p[4], p[5]);
+            o.w = f32x2_to_bf16x2(p[6], p[7]);
+        }
         st_g(bp + e, o);
         amax2 = __vmaxu2(amax2, __vmaxu2(__vmaxu2(o.x & 0x7FFF7FFFu, o.y & 0x7FFF7FFFu),
                                          __vmaxu2(o.z & 0x7FFF7FFFu, o.w & 0x7FFF7FFFu)));
@@ -136,17 +148,17 @@ __device__ __forceinline__ uint4 compute_store_group(Group<GT> &r, float *pp, fl
     return make_uint4(0u, 0u, 0u, 0u);
 }
 
-template <int GT, bool BF16>
+template <int GT, bool BF16, bool SR = false>
 __device__ __forceinline__ uint16_t scalar_elem(float *pp, float *mp, float *vp, const void *gp,
                                                 uint16_t *bp, int64_t k, const Scal &s,
-                                                uint32_t &amax1) {
+                                                uint32_t &amax1, uint32_t u16 = 0) {
     float p = pp[k], m = mp[k], v = vp[k];
     adamw_elem(p, m, v, grad_at<GT>(gp, k), s);
     pp[k] = p;
     mp[k] = m;
     vp[k] = v;
     if (BF16) {
-        const uint16_t b = f32_to_bf16(p);
+        const uint16_t b = SR ? uint16_t(bf16_stochastic(p, u16)) : f32_to_bf16(p);
         bp[k] = b;
         amax1 = max(amax1, uint32_t(b & 0x7FFFu));
         return b;
@@ -154,7 +166,15 @@ __device__ __forceinline__ uint16_t scalar_elem(float *pp, float *mp, float *vp,
     return 0;
 }
 
-template <int GT, bool BF16>
+// 16 random bits of element k (an index within its tensor) for the SR path.
+__device__ __forceinline__ uint32_t sr_u16(uint64_t seed, int32_t t, int tensor, int64_t k) {
+    const uint4 r = sr_random8(seed, t, tensor, k >> 3);
+    const int lane = int(k & 7);
+    const uint32_t w = (lane >> 1) == 0 ? r.x : (lane >> 1) == 1 ? r.y : (lane >> 1) == 2 ? r.z : r.w;
+    return (lane & 1) ? (w >> 16) : (w & 0xFFFFu);
+}
+
+template <int GT, bool BF16, bool SR = false>
 __global__ void __launch_bounds__(kThreads) adamw_main_kernel(AdamwParams P) {
     const AdamwStepScalars sc = *P.scal;
     if (sc.skip) return;  // A2: nothing is written on a skipped step
@@ -192,19 +212,30 @@ __global__ void __launch_bounds__(kThreads) adamw_main_kernel(AdamwParams P) {
             Group<GT> a, b;
             load_group<GT>(a, pp, mp, vp, gp, i * 8);
             load_group<GT>(b, pp, mp, vp, gp, (i + kThreads) * 8);
-            compute_store_group<GT, BF16>(a, pp, mp, vp, bp, i * 8, s, amax2);
-            compute_store_group<GT, BF16>(b, pp, mp, vp, bp, (i + kThreads) * 8, s, amax2);
+            uint4 ra, rb;
+            if constexpr (SR) {
+                // group index within the tensor: (start + 8 i) / 8
+                ra = sr_random8(P.sr_seed, sc.t, t, (start >> 3) + i);
+                rb = sr_random8(P.sr_seed, sc.t, t, (start >> 3) + i + kThreads);
+            }
+            compute_store_group<GT, BF16, SR>(a, pp, mp, vp, bp, i * 8, s, amax2, &ra);
+            compute_store_group<GT, BF16, SR>(b, pp, mp, vp, bp, (i + kThreads) * 8, s, amax2, &rb);
         }
         if (i < ng) {
             Group<GT> a;
             load_group<GT>(a, pp, mp, vp, gp, i * 8);
-            compute_store_group<GT, BF16>(a, pp, mp, vp, bp, i * 8, s, amax2);
+            uint4 ra;
+            if constexpr (SR) ra = sr_random8(P.sr_seed, sc.t, t, (start >> 3) + i);
+            compute_store_group<GT, BF16, SR>(a, pp, mp, vp, bp, i * 8, s, amax2, &ra);
         }
         const int64_t k = ng * 8 + threadIdx.x;
-        if (k < n) scalar_elem<GT, BF16>(pp, mp, vp, gp, bp, k, s, amax1);
+        if (k < n)
+            scalar_elem<GT, BF16, SR>(pp, mp, vp, gp, bp, k, s, amax1,
+                                      SR ? sr_u16(P.sr_seed, sc.t, t, start + k) : 0u);
     } else {
         for (int64_t k = threadIdx.x; k < n; k += kThreads)
-            scalar_elem<GT, BF16>(pp, mp, vp, gp, bp, k, s, amax1);
+            scalar_elem<GT, BF16, SR>(pp, mp, vp, gp, bp, k, s, amax1,
+                                      SR ? sr_u16(P.sr_seed, sc.t, t, start + k) : 0u);
     }
     if (BF16 && P.use_slots) {
         const int slot = P.b.slots[t];
@@ -230,6 +261,8 @@ __device__ __forceinline__ AdamwStepScalars step_scalars(const int32_t *found_in
     s.step_size = 0.0f;
     s.bc2_sqrt = 1.0f;
     s.clip = 1.0f;
+    s.t = *step;
+    s.pad[0] = s.pad[1] = s.pad[2] = 0;
     if (clip_sumsq) {
         // min(1, max_norm / (||g|| + 1e-6)), NaN propagating
         const double c = max_norm / (sqrt(*clip_sumsq) + 1e-6);
@@ -241,6 +274,7 @@ __device__ __forceinline__ AdamwStepScalars step_scalars(const int32_t *found_in
         const double bc2 = 1.0 - pow(beta2, double(t));
         s.step_size = float(lr / bc1);
         s.bc2_sqrt = float(sqrt(bc2));
+        s.t = t;
         *step = t;
     }
     return s;
@@ -376,19 +410,20 @@ cudaError_t launch_adamw(const ListView &p, const ListView &m, const ListView &v
                          const float *scale, const int32_t *found_inf, int32_t *step,
                          const AdamwConsts &c, AdamwStepScalars *scal, float *amax,
                          bool use_slots, cudaStream_t s, const double *clip_sumsq,
-                         double max_norm) {
+                         double max_norm, bool stochastic, uint64_t seed) {
     adamw_prologue_kernel<<<1, 1, 0, s>>>(found_inf, step, c.lr, c.beta1, c.beta2, clip_sumsq,
                                           max_norm, scal);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return launch_adamw_main(p, m, v, g, b, n_chunks, gelem, scale, c, scal, amax, use_slots, s);
+    return launch_adamw_main(p, m, v, g, b, n_chunks, gelem, scale, c, scal, amax, use_slots, s,
+                             stochastic, seed);
 }
 
 cudaError_t launch_adamw_main(const ListView &p, const ListView &m, const ListView &v,
                               const ListView &g, const ListView *b, int64_t n_chunks, int gelem,
                               const float *scale, const AdamwConsts &c,
                               const AdamwStepScalars *scal, float *amax, bool use_slots,
-                              cudaStream_t s) {
+                              cudaStream_t s, bool stochastic, uint64_t seed) {
     if (n_chunks == 0) return cudaSuccess;
     AdamwParams P;
     P.p = p;
@@ -406,11 +441,13 @@ cudaError_t launch_adamw_main(const ListView &p, const ListView &m, const ListVi
     P.omb2 = c.omb2;
     P.eps = c.eps;
     P.use_slots = use_slots ? 1 : 0;
+    P.sr_seed = seed;
     const dim3 grid((unsigned)n_chunks), block(kThreads);
     const bool bf = b != nullptr;
 #define AMP_ADAMW_LAUNCH(GT)                                                         \
     do {                                                                             \
-        if (bf) adamw_main_kernel<GT, true><<<grid, block, 0, s>>>(P);               \
+        if (bf && stochastic) adamw_main_kernel<GT, true, true><<<grid, block, 0, s>>>(P); \
+        else if (bf) adamw_main_kernel<GT, true><<<grid, block, 0, s>>>(P);          \
         else adamw_main_kernel<GT, false><<<grid, block, 0, s>>>(P);                 \
     } while (0)
     if (gelem == kF32) AMP_ADAMW_LAUNCH(kF32);

@@ -80,7 +80,7 @@ extern "C" {
 
 const char *amp_last_error(void) { return g_err; }
 
-int amp_abi_version(void) { return 4; }
+int amp_abi_version(void) { return 5; }
 
 amp_status amp_tensor_list_create(int n, void *const *dev_ptrs, const int64_t *rows,
                                   const int64_t *cols, amp_dtype dtype, amp_stream_t stream,
@@ -230,7 +230,8 @@ static amp_status adamw_entry(amp_tensor_list master, amp_tensor_list exp_avg,
                               amp_tensor_list bf16_out, const float *scale_dev,
                               const int32_t *found_inf_dev, int32_t *step_dev,
                               const amp_adamw_hyper *hyper, float *amax_dev,
-                              const double *clip_sumsq, double max_norm, amp_stream_t stream) {
+                              const double *clip_sumsq, double max_norm, amp_stream_t stream,
+                              bool stochastic = false, uint64_t seed = 0) {
     if (!master || !exp_avg || !exp_avg_sq || !grads || !step_dev || !hyper)
         return fail(AMP_EINVAL, "amp_adamw_master_step: NULL argument");
     if (master->dtype != AMP_DT_F32 || exp_avg->dtype != AMP_DT_F32 ||
@@ -261,8 +262,19 @@ static amp_status adamw_entry(amp_tensor_list master, amp_tensor_list exp_avg,
         master->view, exp_avg->view, exp_avg_sq->view, grads->view,
         bf16_out ? &bf16_out->view : nullptr, master->n_chunks, gc, scale_dev, found_inf_dev,
         step_dev, c, reinterpret_cast<amp::AdamwStepScalars *>(master->scratch), amax_dev, slots,
-        reinterpret_cast<cudaStream_t>(stream), clip_sumsq, max_norm);
+        reinterpret_cast<cudaStream_t>(stream), clip_sumsq, max_norm, stochastic, seed);
     return e == cudaSuccess ? AMP_OK : cuda_fail(e, "amp_adamw_master_step");
+}
+
+amp_status amp_adamw_master_step_sr(amp_tensor_list master, amp_tensor_list exp_avg,
+                                    amp_tensor_list exp_avg_sq, amp_tensor_list grads,
+                                    amp_tensor_list bf16_out, const float *scale_dev,
+                                    const int32_t *found_inf_dev, int32_t *step_dev,
+                                    const amp_adamw_hyper *hyper, float *amax_dev, uint64_t seed,
+                                    amp_stream_t stream) {
+    if (!bf16_out) return fail(AMP_EINVAL, "amp_adamw_master_step_sr: bf16_out is NULL");
+    return adamw_entry(master, exp_avg, exp_avg_sq, grads, bf16_out, scale_dev, found_inf_dev,
+                       step_dev, hyper, amax_dev, nullptr, 0.0, stream, true, seed);
 }
 
 amp_status amp_adamw_master_step(amp_tensor_list master, amp_tensor_list exp_avg,

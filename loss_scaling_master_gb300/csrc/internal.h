@@ -40,6 +40,8 @@ struct AdamwStepScalars {
     float step_size;
     float bc2_sqrt;
     float clip;  // gradient clipping factor, exactly 1.0 when not clipping
+    int32_t t;   // the step being taken (step counter after it)
+    int32_t pad[3];
 };
 
 int sm_count(int device);
@@ -58,13 +60,13 @@ cudaError_t launch_adamw(const ListView &p, const ListView &m, const ListView &v
                          const float *scale, const int32_t *found_inf, int32_t *step,
                          const AdamwConsts &c, AdamwStepScalars *scal, float *amax,
                          bool use_slots, cudaStream_t s, const double *clip_sumsq = nullptr,
-                         double max_norm = 0.0);
+                         double max_norm = 0.0, bool stochastic = false, uint64_t seed = 0);
 
 cudaError_t launch_adamw_main(const ListView &p, const ListView &m, const ListView &v,
                               const ListView &g, const ListView *b, int64_t n_chunks, int gelem,
                               const float *scale, const AdamwConsts &c,
                               const AdamwStepScalars *scal, float *amax, bool use_slots,
-                              cudaStream_t s);
+                              cudaStream_t s, bool stochastic = false, uint64_t seed = 0);
 
 // The lists of one delayed-scaling FP8 step: the tensors without FP8 copies
 // (1-D, walked by chunks) and the FP8 weights (2-D, walked by 128x128 tiles).

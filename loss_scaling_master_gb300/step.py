@@ -28,7 +28,8 @@ class AmpOptimizerStep:
     def __init__(self, master, grads, *, lr, beta1, beta2, eps, weight_decay,
                  init_scale=65536.0, growth_factor=2.0, backoff_factor=0.5,
                  growth_interval=2000, emit_bf16=True, fp8_shapes=None, fp8_eps=1e-12,
-                 max_norm=None, fp8_scaling="dynamic", amax_history_len=1, stream=None):
+                 max_norm=None, fp8_scaling="dynamic", amax_history_len=1, sr_seed=None,
+                 stream=None):
         """master: fp32 device tensors (updated in place); grads: device
         tensors (f16/bf16/f32) the caller fills with scaled gradients before
         each step.  fp8_shapes: per tensor (rows, cols) for weights that get
@@ -36,7 +37,9 @@ class AmpOptimizerStep:
         clip the unscaled gradients to this global L2 norm (None: no clipping).
         fp8_scaling: "dynamic" (this step's amax, a separate cast pass) or
         "delayed" (the max of the last amax_history_len steps' amax, cast in
-        the update pass; the history starts from the initial bf16 copy)."""
+        the update pass; the history starts from the initial bf16 copy).
+        sr_seed: round the bf16 copy stochastically with this 64-bit seed
+        (None: round to nearest-even)."""
         dev = master[0].device
         self.stream = stream
         self.master = list(master)
@@ -83,6 +86,10 @@ class AmpOptimizerStep:
         self.inv_scale = torch.zeros(max(self.n_fp8, 1), dtype=torch.float32, device=dev)
         self.fp8_scaling = fp8_scaling
         self.hist_len = amax_history_len
+        self.sr_seed = sr_seed
+        if sr_seed is not None and (max_norm is not None or fp8_scaling != "dynamic"
+                                    or not emit_bf16):
+            raise ValueError("stochastic rounding is offered with the plain AdamW step")
         if fp8_scaling == "delayed":
             if not self.n_fp8 or max_norm is not None:
                 raise ValueError("delayed FP8 scaling needs FP8 weights and no clipping")
@@ -186,7 +193,12 @@ class AmpOptimizerStep:
                                            self.amax_history, self.n_fp8, self.hist_len,
                                            stream=s)
             return
-        if self.max_norm is None:
+        if self.sr_seed is not None:
+            A.amp_unscale_check(L_g, self.scale, self.found_inf, stream=s)
+            A.amp_adamw_master_step_sr(self.L_master, self.L_m, self.L_v, L_g, self.L_b,
+                                       self.scale, self.found_inf, self.step_count, *self.hyper,
+                                       self.sr_seed, amax=amax, stream=s)
+        elif self.max_norm is None:
             A.amp_unscale_check(L_g, self.scale, self.found_inf, stream=s)
             A.amp_adamw_master_step(self.L_master, self.L_m, self.L_v, L_g, self.L_b, self.scale,
                                     self.found_inf, self.step_count, *self.hyper, amax=amax,

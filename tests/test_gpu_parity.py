@@ -640,3 +640,72 @@ def test_fp8_rowwise_degenerate(A, dev, fmt):
     skipped = _run_rowwise(A, dev, xh, "f32", rows, cols, fmt, True, skip=1)
     assert np.all(skipped["q"] == 0xA5) and np.all(skipped["q_t"] == 0x5A)
     assert np.all(skipped["amax_row"] == -1.0) and np.all(skipped["inv_col"] == -1.0)
+
+
+# ------------------------------------------------------ stochastic rounding
+@pytest.mark.parametrize("misalign", [False, True])
+def test_adamw_stochastic_rounding_parity(A, dev, misalign):
+    """The bf16 copy rounded stochastically with the Philox4x32-10 stream of
+    each element: bit-identical to the oracle's (same published generator,
+    written separately) over several steps with a skip; the master state is
+    the RNE step's."""
+    rng = np.random.default_rng(95)
+    sizes = [1, 7, 257, 4096, 16385, 40000]
+    seed = 0x1234_5678_9ABC_DEF0
+    master_h = [(rng.standard_normal(k) * 0.02).astype(np.float32) for k in sizes]
+    P = _device_views(master_h, "f32", dev, misalign)
+    M = _device_views([np.zeros(k, np.float32) for k in sizes], "f32", dev, misalign)
+    V = _device_views([np.zeros(k, np.float32) for k in sizes], "f32", dev, misalign)
+    G = _device_views(_grads_host(rng, sizes, "f16"), "f16", dev, misalign)
+    B = _device_views([np.zeros(k, np.uint16) for k in sizes], "bf16", dev, misalign)
+    Ls = [A.amp_tensor_list_create(x) for x in (P, M, V, G, B)]
+    A.amp_tensor_list_set_amax_slots(Ls[4], [0, -1, -1, 1, -1, 2])
+    amax = torch.zeros(3, device=dev)
+    step = torch.zeros(1, dtype=torch.int32, device=dev)
+    fi = torch.zeros(1, dtype=torch.int32, device=dev)
+    rp, rm, rv = [x.copy() for x in master_h], [np.zeros(k, np.float32) for k in sizes], \
+        [np.zeros(k, np.float32) for k in sizes]
+    rb = [np.zeros(k, np.uint16) for k in sizes]
+    rstep = 0
+    for k in range(4):
+        gh = _grads_host(rng, sizes, "f16", sigma=1e-3 * 1024)
+        for t, h in zip(G, gh):
+            t.copy_(to_device(h, "f16", dev))
+        skip = int(k == 2)
+        fi.fill_(skip)
+        amax.zero_()
+        A.amp_adamw_master_step_sr(*Ls, torch.tensor([1024.0], device=dev), fi, step,
+                                   1e-3, 0.9, 0.999, 1e-8, 0.01, seed, amax=amax)
+        ram = np.zeros(3, np.float32)
+        rstep = O.adamw_master_step(rp, rm, rv, gh, "f16", rb, 1024.0, skip, rstep, 1e-3, 0.9,
+                                    0.999, 1e-8, 0.01, amax_slot=[0, -1, -1, 1, -1, 2], amax=ram,
+                                    sr_seed=seed)
+        assert int(step.item()) == rstep
+        assert np.array_equal(to_host_bits(amax).view(np.uint32), ram.view(np.uint32))
+    for i in range(len(sizes)):
+        assert np.array_equal(to_host_bits(P[i]).view(np.uint32), rp[i].view(np.uint32))
+        assert np.array_equal(to_host_bits(B[i]), rb[i]), i
+    for L in Ls:
+        L.close()
+
+
+def test_stochastic_rounding_unbiased_on_gpu(A, dev):
+    """E[bf16_sr(p)] = p: the mean of the stochastically rounded copy of a
+    constant master over 4M elements sits within 5 sigma of the master."""
+    n = 1 << 22
+    p = torch.full((n,), 1.0 + 1e-3, device=dev)
+    Ls = [A.amp_tensor_list_create([t]) for t in
+          (p, torch.zeros(n, device=dev), torch.zeros(n, device=dev),
+           torch.zeros(n, dtype=torch.float16, device=dev),
+           torch.empty(n, dtype=torch.bfloat16, device=dev))]
+    step = torch.zeros(1, dtype=torch.int32, device=dev)
+    # lr = 0, wd = 0: p stays, the copy is SR(p)
+    A.amp_adamw_master_step_sr(*Ls, None, None, step, 0.0, 0.9, 0.999, 1e-8, 0.0, 42)
+    b = Ls[4].tensors[0].float().double()
+    lo, hi = 1.0, 1.0 + 2.0 ** -7
+    frac = (float(np.float32(1.0 + 1e-3)) - lo) / (hi - lo)
+    assert set(torch.unique(b).tolist()) <= {lo, hi}
+    sigma = (hi - lo) * np.sqrt(frac * (1 - frac) / n)
+    assert abs(b.mean().item() - float(np.float32(1.0 + 1e-3))) < 5 * sigma
+    for L in Ls:
+        L.close()
