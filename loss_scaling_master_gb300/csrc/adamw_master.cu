@@ -66,17 +66,17 @@ struct Group {
 template <int GT>
 __device__ __forceinline__ void load_group(Group<GT> &r, const float *pp, const float *mp,
                                            const float *vp, const void *gp, int64_t e) {
-    r.p[0] = ld_cs(pp + e);
-    r.p[1] = ld_cs(pp + e + 4);
-    r.m[0] = ld_cs(mp + e);
-    r.m[1] = ld_cs(mp + e + 4);
-    r.v[0] = ld_cs(vp + e);
-    r.v[1] = ld_cs(vp + e + 4);
+    r.p[0] = ld16(pp + e);
+    r.p[1] = ld16(pp + e + 4);
+    r.m[0] = ld16(mp + e);
+    r.m[1] = ld16(mp + e + 4);
+    r.v[0] = ld16(vp + e);
+    r.v[1] = ld16(vp + e + 4);
     if constexpr (GT == kF32) {
-        r.g[0] = ld_cs(static_cast<const float *>(gp) + e);
-        r.g[1] = ld_cs(static_cast<const float *>(gp) + e + 4);
+        r.g[0] = ld16(static_cast<const float *>(gp) + e);
+        r.g[1] = ld16(static_cast<const float *>(gp) + e + 4);
     } else {
-        r.g[0] = ld_cs(static_cast<const uint16_t *>(gp) + e);
+        r.g[0] = ld16(static_cast<const uint16_t *>(gp) + e);
     }
 }
 
@@ -118,12 +118,12 @@ __device__ __forceinline__ uint4 compute_store_group(Group<GT> &r, float *pp, fl
         u4_set(r.m[j >> 2], j & 3, m[j]);
         u4_set(r.v[j >> 2], j & 3, v[j]);
     }
-    st_cs(pp + e, r.p[0]);
-    st_cs(pp + e + 4, r.p[1]);
-    st_cs(mp + e, r.m[0]);
-    st_cs(mp + e + 4, r.m[1]);
-    st_cs(vp + e, r.v[0]);
-    st_cs(vp + e + 4, r.v[1]);
+    st16(pp + e, r.p[0]);
+    st16(pp + e + 4, r.p[1]);
+    st16(mp + e, r.m[0]);
+    st16(mp + e + 4, r.m[1]);
+    st16(vp + e, r.v[0]);
+    st16(vp + e + 4, r.v[1]);
     if (BF16) {
         uint4 o;
         if constexpr (SR) {
@@ -140,7 +140,7 @@ __device__ __forceinline__ uint4 compute_store_group(Group<GT> &r, float *pp, fl
             o.z = f32x2_to_bf16x2(p[4], p[5]);
             o.w = f32x2_to_bf16x2(p[6], p[7]);
         }
-        st_g(bp + e, o);
+        st16(bp + e, o);
         amax2 = __vmaxu2(amax2, __vmaxu2(__vmaxu2(o.x & 0x7FFF7FFFu, o.y & 0x7FFF7FFFu),
                                          __vmaxu2(o.z & 0x7FFF7FFFu, o.w & 0x7FFF7FFFu)));
         return o;

@@ -51,7 +51,7 @@ __device__ __forceinline__ void quant_tile(const void *x, int64_t rows, int64_t 
             const int64_t e = (r0 + rb + 16 * k) * cols + c0 + 8 * c8;
             const char *src = static_cast<const char *>(x) + e * esz;
 #pragma unroll
-            for (int u = 0; u < nv; ++u) raw[k][u] = ld_cs(src + 16 * u);
+            for (int u = 0; u < nv; ++u) raw[k][u] = ld16(src + 16 * u);
         }
         __syncthreads();  // s_scale is ready
         const float s32 = *s_scale;
@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const void *x, int64_t n
         const int64_t nv = n / per;
         const char *b = static_cast<const char *>(x);
         for (int64_t i = gtid; i < nv; i += gstride) {
-            const uint4 w = ld_cs(b + i * 16);
+            const uint4 w = ld16(b + i * 16);
             if (XT == kF32) {
                 mx = max(mx, max(max(w.x & 0x7FFFFFFFu, w.y & 0x7FFFFFFFu),
                                  max(w.z & 0x7FFFFFFFu, w.w & 0x7FFFFFFFu)));

@@ -37,12 +37,12 @@ template <int XT>
 __device__ __forceinline__ void load8_abs(const void *x, int64_t e, uint32_t (&a)[8]) {
     if (XT == kF32) {
         const char *p = static_cast<const char *>(x) + e * 4;
-        const uint4 u = ld_cs(p), v = ld_cs(p + 16);
+        const uint4 u = ld16(p), v = ld16(p + 16);
         const uint32_t w[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int j = 0; j < 8; ++j) a[j] = w[j] & 0x7FFFFFFFu;
     } else {
-        const uint4 u = ld_cs(static_cast<const char *>(x) + e * 2);
+        const uint4 u = ld16(static_cast<const char *>(x) + e * 2);
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -62,12 +62,12 @@ template <int XT>
 __device__ __forceinline__ void load8_f32(const void *x, int64_t e, float (&y)[8]) {
     if (XT == kF32) {
         const char *p = static_cast<const char *>(x) + e * 4;
-        const uint4 u = ld_cs(p), v = ld_cs(p + 16);
+        const uint4 u = ld16(p), v = ld16(p + 16);
         const uint32_t w[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int j = 0; j < 8; ++j) y[j] = __uint_as_float(w[j]);
     } else {
-        const uint4 u = ld_cs(static_cast<const char *>(x) + e * 2);
+        const uint4 u = ld16(static_cast<const char *>(x) + e * 2);
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {

@@ -70,7 +70,7 @@ __device__ __forceinline__ void store_transposed_tile(const uint32_t *sm, uint8_
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int64_t dst = (c0 + 4 * wq + j) * rows + r0 + 16 * rg;
-        st_g(out_t + dst, make_uint4(col[j][0], col[j][1], col[j][2], col[j][3]));
+        st16(out_t + dst, make_uint4(col[j][0], col[j][1], col[j][2], col[j][3]));
     }
 }
 

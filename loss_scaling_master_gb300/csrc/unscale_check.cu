@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kThreads) check_kernel(ListView g, const float
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int64_t j = i + int64_t(u) * kThreads;
-                w[u] = j < nv ? ld_cs(base + j * 16) : make_uint4(0u, 0u, 0u, 0u);
+                w[u] = j < nv ? ld16(base + j * 16) : make_uint4(0u, 0u, 0u, 0u);
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
