@@ -226,3 +226,55 @@ def test_fp8_sweep_rowwise_full_parity(A):
             assert np.array_equal(g.view(np.uint8) if g.dtype == np.uint8 else g.view(np.uint32),
                                   ref[k] if ref[k].dtype == np.uint8 else ref[k].view(np.uint32)), (k, r, c)
         del x, o
+
+
+def test_over_2g_element_tensors(A):
+    """Largest sizes: one tensor of 2^31 + 12,345 elements through AdamW, and a
+    [2^16 + 128, 2^15 + 64] matrix (over 2^31 elements) through the FP8 cast
+    with its transposed copy - byte offsets past 2^31 and 2^32.  Checked at
+    sampled elements around and beyond the 32-bit boundaries."""
+    dev = torch.device("cuda:0")
+    torch.cuda.empty_cache()
+    n = (1 << 31) + 12345
+    gen = device_generator(dev, 5, 9)
+    p = device_fill_normal(torch.empty(n, device=dev), 0.02, gen)
+    g = device_fill_normal(torch.empty(n, dtype=torch.float16, device=dev), 10.0, gen)
+    m = torch.zeros(n, device=dev)
+    v = torch.zeros(n, device=dev)
+    b = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    idx = torch.tensor([0, 1, (1 << 31) - 1, 1 << 31, (1 << 31) + 1, n - 8, n - 1] +
+                       torch.randint(0, n, (64,), generator=torch.Generator().manual_seed(3)).tolist(),
+                       dtype=torch.int64, device=dev)
+    p0, g0 = to_host_bits(p[idx]), to_host_bits(g[idx])
+    Ls = [A.amp_tensor_list_create([t]) for t in (p, m, v, g, b)]
+    step = torch.zeros(1, dtype=torch.int32, device=dev)
+    A.amp_adamw_master_step(*Ls, torch.tensor([1024.0], device=dev), None, step,
+                            1e-3, 0.9, 0.999, 1e-8, 0.01)
+    rp, rm, rv, rb = [p0.copy()], [np.zeros(idx.numel(), np.float32)], [np.zeros(idx.numel(), np.float32)], \
+        [np.zeros(idx.numel(), np.uint16)]
+    O.adamw_master_step(rp, rm, rv, [g0], "f16", rb, 1024.0, 0, 0, 1e-3, 0.9, 0.999, 1e-8, 0.01)
+    assert np.array_equal(to_host_bits(p[idx]).view(np.uint32), rp[0].view(np.uint32))
+    assert np.array_equal(to_host_bits(v[idx]).view(np.uint32), rv[0].view(np.uint32))
+    assert np.array_equal(to_host_bits(b[idx]), rb[0])
+    for L in Ls:
+        L.close()
+    del p, g, m, v, b, Ls
+    torch.cuda.empty_cache()
+
+    rows, cols = (1 << 16) + 128, (1 << 15) + 64
+    x = device_fill_normal(torch.empty((rows, cols), dtype=torch.bfloat16, device=dev), 1.0, gen)
+    q = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+    qt = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
+    inv = torch.zeros(1, device=dev)
+    amax = torch.zeros(1, device=dev)
+    A.fp8_quant_tensorwise(x, "e4m3fn", q, qt, inv, amax)
+    am = float(to_host_bits(amax)[0])
+    assert am == float(x.abs().max().float().item())
+    rsel = torch.tensor([0, 1, rows // 2, rows - 2, rows - 1], device=dev)
+    csel = torch.tensor([0, 7, cols // 2, cols - 65, cols - 1], device=dev)
+    xs = x[rsel][:, csel].contiguous()
+    rq, _, rinv, _ = O.fp8_quant_tensorwise(to_host_bits(xs).ravel(), "bf16", 5, 5, "e4m3fn",
+                                            transposed=False, amax=am)
+    assert np.array_equal(to_host_bits(q[rsel][:, csel]).ravel(), rq)
+    assert np.array_equal(to_host_bits(qt[csel][:, rsel]).T.ravel(), rq)
+    assert to_host_bits(inv)[0] == np.float32(rinv)
