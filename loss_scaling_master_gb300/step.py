@@ -221,6 +221,41 @@ class AmpOptimizerStep:
         return {"scale": float(self.scale.item()), "growth_tracker": int(self.growth_tracker.item()),
                 "step": int(self.step_count.item()), "found_inf": int(self.found_inf.item())}
 
+    def state_dict(self) -> dict:
+        """Host copies of everything a resumed run needs: master, m, v, the
+        bf16 and FP8 copies, the scaler and step counters, FP8 scales and the
+        amax history.  Synchronises."""
+        cpu = lambda ts: [t.detach().cpu().clone() for t in ts]
+        d = {"master": cpu(self.master), "exp_avg": cpu(self.exp_avg),
+             "exp_avg_sq": cpu(self.exp_avg_sq),
+             "bf16": cpu(self.bf16) if self.bf16 is not None else None,
+             "fp8": cpu(self.fp8), "fp8_t": cpu(self.fp8_t),
+             "scale": self.scale.cpu().clone(), "growth_tracker": self.growth_tracker.cpu().clone(),
+             "step": self.step_count.cpu().clone(), "found_inf": self.found_inf.cpu().clone(),
+             "amax": self.amax.cpu().clone(), "inv_scale": self.inv_scale.cpu().clone()}
+        if self.fp8_scaling == "delayed":
+            d["amax_history"] = self.amax_history.cpu().clone()
+        return d
+
+    def load_state_dict(self, d: dict):
+        """Copy a state_dict() back into this step's device buffers (same
+        parameter set and options); the list handles keep pointing at them."""
+        def put(dst, src):
+            for a, b in zip(dst, src):
+                a.copy_(b)
+        put(self.master, d["master"])
+        put(self.exp_avg, d["exp_avg"])
+        put(self.exp_avg_sq, d["exp_avg_sq"])
+        if self.bf16 is not None and d["bf16"] is not None:
+            put(self.bf16, d["bf16"])
+        put(self.fp8, d["fp8"])
+        put(self.fp8_t, d["fp8_t"])
+        for name in ("scale", "growth_tracker", "step_count", "found_inf", "amax", "inv_scale"):
+            getattr(self, name).copy_(d["step" if name == "step_count" else name])
+        if self.fp8_scaling == "delayed":
+            self.amax_history.copy_(d["amax_history"])
+        torch.cuda.synchronize(self.scale.device)
+
     def state_fp8(self) -> dict:
         """Host copies of the FP8 scaling state (synchronises)."""
         d = {"amax": self.amax[:self.n_fp8].cpu(), "inv_scale": self.inv_scale[:self.n_fp8].cpu()}

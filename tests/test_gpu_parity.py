@@ -709,3 +709,51 @@ def test_stochastic_rounding_unbiased_on_gpu(A, dev):
     assert abs(b.mean().item() - float(np.float32(1.0 + 1e-3))) < 5 * sigma
     for L in Ls:
         L.close()
+
+
+# --------------------------------------------------------- checkpoint / resume
+@pytest.mark.parametrize("fp8_scaling", ["dynamic", "delayed"])
+def test_checkpoint_resume_is_bit_identical(A, dev, fp8_scaling):
+    """Save the state after 3 steps, restore it into a fresh step object and
+    continue: the resumed run equals the uninterrupted one bit for bit."""
+    from loss_scaling_master_gb300 import AmpOptimizerStep
+    rng = np.random.default_rng(101)
+    shapes = [(128, 256), (300,), (256, 384)]
+    fp8_shapes = [s if len(s) == 2 else None for s in shapes]
+    sizes = [int(np.prod(s)) for s in shapes]
+    master = [(rng.standard_normal(n) * 0.02).astype(np.float32) for n in sizes]
+    grads = [[(rng.standard_normal(n) * 1e-3 * 1024).astype(np.float16).view(np.uint16) for n in sizes]
+             for _ in range(6)]
+    grads[4][1][7] = 0x7C00                                        # a skipped step after resume
+    hyper = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+
+    def make():
+        return AmpOptimizerStep([torch.from_numpy(m.copy()).to(dev) for m in master],
+                                [torch.empty(n, dtype=torch.float16, device=dev) for n in sizes],
+                                init_scale=1024.0, growth_interval=2, fp8_shapes=fp8_shapes,
+                                fp8_scaling=fp8_scaling, amax_history_len=2, **hyper)
+
+    def run(st, gs):
+        for g in gs:
+            for t, h in zip(st.grads, g):
+                t.copy_(to_device(h, "f16", dev))
+            st.step()
+
+    whole = make()
+    run(whole, grads)
+    first = make()
+    run(first, grads[:3])
+    ckpt = first.state_dict()
+    first.close()
+    resumed = make()
+    resumed.load_state_dict(ckpt)
+    run(resumed, grads[3:])
+    a, b = whole.state_dict(), resumed.state_dict()
+    for k in a:
+        if a[k] is None:
+            continue
+        xs, ys = (a[k], b[k]) if isinstance(a[k], list) else ([a[k]], [b[k]])
+        for x, y in zip(xs, ys):
+            assert torch.equal(x.view(torch.uint8), y.view(torch.uint8)), k
+    whole.close()
+    resumed.close()
