@@ -69,8 +69,8 @@ def adamw_traffic(delayed: bool, n_params: int, n_fp8: int):
     kernel for every parameter, or (delayed FP8) the chunked kernel for the
     plain parameters plus the tile kernel for the FP8 weights."""
     if not delayed:
-        return profiled_traffic("adamw_main_kernel", n_params)
-    a = profiled_traffic("adamw_main_kernel", n_params - n_fp8)
+        return profiled_traffic("adamw_bulk_kernel", n_params)
+    a = profiled_traffic("adamw_bulk_kernel", n_params - n_fp8)
     b = profiled_traffic("adamw_fp8_tile_kernel", n_fp8)
     return None if a is None or b is None else a + b
 

@@ -58,7 +58,8 @@ typedef enum {
     AMP_EINVAL = -1,  /* null pointer, negative size, mismatched list shapes */
     AMP_EDTYPE = -2,  /* element type not accepted by this entry point */
     AMP_ECUDA = -4,   /* a CUDA runtime call or kernel launch failed */
-    AMP_ENOMEM = -5   /* device allocation in amp_tensor_list_create failed */
+    AMP_ENOMEM = -5,  /* device allocation in amp_tensor_list_create failed */
+    AMP_ETIMEOUT = -6 /* a kernel's bounded wait gave up (see amp_tensor_list_check) */
 } amp_status;
 
 typedef enum {
@@ -103,6 +104,22 @@ amp_status amp_tensor_list_create(int n, void *const *dev_ptrs, const int64_t *r
  * the handle's device block on `stream` (waits for the copy: set-up call). */
 amp_status amp_tensor_list_set_amax_slots(amp_tensor_list list, const int32_t *slots,
                                           amp_stream_t stream);
+
+/* Health check.  The AdamW kernels stream through shared memory with
+ * asynchronous bulk copies whose completion they wait for with a time limit
+ * (one second of GPU time) instead of forever; a wait that gives up leaves
+ * its chunk not updated and sets a sticky error word in the device block of
+ * the list that holds the step scalars: `master` for amp_adamw_master_step
+ * and its _clip / _sr forms, `fp8_out` for amp_adamw_master_step_fp8_delayed.
+ * This call waits for `stream`, reads and clears that word, and returns
+ * AMP_ETIMEOUT if it was set, AMP_OK otherwise. */
+amp_status amp_tensor_list_check(amp_tensor_list list, amp_stream_t stream);
+
+/* Self-test of the bounded wait: one CTA waits on a barrier that nothing
+ * completes, gives up after limit_seconds (0 < limit <= 10) of GPU time and
+ * writes *err_dev = 1 (0 would mean the barrier completed).  No fault, no
+ * hang; the context stays usable.  The pages have no counterpart. */
+amp_status amp_selftest_bounded_wait(int32_t *err_dev, double limit_seconds, amp_stream_t stream);
 
 /* Release the handle and its device block (cudaFree; synchronises the
  * device like any cudaFree).  NULL is accepted. */
@@ -247,6 +264,12 @@ amp_status amp_adamw_master_step_noalloc(int n, float *const *master, float *con
                                          const float *scale_dev, const int32_t *found_inf_dev,
                                          int32_t *step_dev, const amp_adamw_hyper *hyper,
                                          float *amax_dev, amp_stream_t stream);
+
+/* amp_tensor_list_check for amp_adamw_master_step_noalloc: waits for
+ * `stream`, reads and clears the sticky error word of the current device's
+ * fixed array; AMP_ETIMEOUT if a bounded wait gave up since the last check.
+ * Allocates nothing. */
+amp_status amp_noalloc_check(amp_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* A6-A9: tensorwise dynamic FP8 quantization.  [FP8] §2 (quant math), §3     */

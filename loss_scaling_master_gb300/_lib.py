@@ -18,16 +18,18 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libampfp8.so")
 
 AMP_OK = 0
-STATUS = {0: "AMP_OK", -1: "AMP_EINVAL", -2: "AMP_EDTYPE", -4: "AMP_ECUDA", -5: "AMP_ENOMEM"}
+STATUS = {0: "AMP_OK", -1: "AMP_EINVAL", -2: "AMP_EDTYPE", -4: "AMP_ECUDA", -5: "AMP_ENOMEM",
+          -6: "AMP_ETIMEOUT"}
 DT = {"f32": 1, "f16": 2, "bf16": 3, "e4m3fn": 4, "e5m2": 5}
 _TORCH_DT = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16",
              torch.float8_e4m3fn: "e4m3fn", torch.float8_e5m2: "e5m2"}
 
 # every symbol include/ampfp8.h declares
 EXPORTS = ("amp_tensor_list_create", "amp_tensor_list_set_amax_slots", "amp_tensor_list_destroy",
+           "amp_tensor_list_check", "amp_selftest_bounded_wait",
            "amp_unscale_check", "amp_unscale_check_norm", "amp_adamw_master_step",
            "amp_adamw_master_step_clip", "amp_adamw_master_step_sr",
-           "amp_adamw_master_step_noalloc",
+           "amp_adamw_master_step_noalloc", "amp_noalloc_check",
            "amp_adamw_master_step_fp8_delayed", "amp_update_scale_fp8_history",
            "fp8_quant_tensorwise", "fp8_quant_tensorwise_list", "fp8_quant_rowwise",
            "amp_update_scale",
@@ -65,6 +67,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.amp_tensor_list_set_amax_slots.argtypes = [P, P, P]
         L.amp_tensor_list_destroy.argtypes = [P]
         L.amp_unscale_check.argtypes = [P, P, P, i32, P]
+        L.amp_tensor_list_check.argtypes = [P, P]
+        L.amp_noalloc_check.argtypes = [P]
+        L.amp_selftest_bounded_wait.argtypes = [P, dbl, P]
         L.amp_adamw_master_step.argtypes = [P, P, P, P, P, P, P, P,
                                             ctypes.POINTER(amp_adamw_hyper), P, P]
         L.amp_unscale_check_norm.argtypes = [P, P, P, P, P]
@@ -171,6 +176,21 @@ def amp_tensor_list_set_amax_slots(lst: TensorList, slots, stream=None):
 
 def amp_tensor_list_destroy(lst: TensorList):
     lst.close()
+
+
+def amp_tensor_list_check(lst: TensorList, stream=None):
+    """Raise AmpError(AMP_ETIMEOUT) if a kernel's bounded wait gave up (synchronises)."""
+    _check("amp_tensor_list_check", load().amp_tensor_list_check(lst.handle, _stream(stream)))
+
+
+def amp_noalloc_check(stream=None):
+    """amp_tensor_list_check for the allocation-free AdamW entry point (synchronises)."""
+    _check("amp_noalloc_check", load().amp_noalloc_check(_stream(stream)))
+
+
+def amp_selftest_bounded_wait(err, limit_seconds: float = 0.05, stream=None):
+    _check("amp_selftest_bounded_wait",
+           load().amp_selftest_bounded_wait(_dptr(err), float(limit_seconds), _stream(stream)))
 
 
 def amp_unscale_check(grads: TensorList, scale, found_inf, inplace: bool = False, stream=None):

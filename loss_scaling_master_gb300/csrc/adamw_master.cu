@@ -16,6 +16,7 @@
 //             once, otherwise every thread streams groups of 8 elements with
 //             16-byte loads/stores: 14 bytes read + 14 bytes written per
 //             parameter (fp16/bf16 grads, bf16 emission).
+#include "bulk_copy.cuh"
 #include "fp8_tile.cuh"
 #include "internal.h"
 #include "philox.cuh"
@@ -31,6 +32,7 @@ struct AdamwParams {
     float decay, b1, omb1, b2, omb2, eps;
     int use_slots;
     uint64_t sr_seed;  // stochastic bf16 rounding key
+    int32_t *err;      // sticky error word (a bounded wait gave up)
 };
 
 struct Scal {
@@ -174,10 +176,34 @@ __device__ __forceinline__ uint32_t sr_u16(uint64_t seed, int32_t t, int tensor,
     return (lane & 1) ? (w >> 16) : (w & 0xFFFFu);
 }
 
-template <int GT, bool BF16, bool SR = false>
-__global__ void __launch_bounds__(kThreads) adamw_main_kernel(AdamwParams P) {
+// ---------------------------------------------------------------------------
+// The update pass over the plain (non-FP8-tiled) tensors, one CTA per chunk,
+// streamed with TMA bulk copies: the chunk goes through kStages shared-memory
+// stages of kSub elements.  One thread issues the cp.async.bulk loads of the
+// p, m, v and g runs into a stage (completion counted by bytes on the stage's
+// mbarrier) kStages sub-blocks ahead; every thread updates groups of 8
+// elements in shared memory; the results go back with cp.async.bulk stores,
+// whose reads of the stage are awaited before it is refilled.  On GB300 a
+// plain copy streams ~5 % faster this way than with per-thread 16-byte
+// loads/stores, and this kernel ~0.5 % faster than its per-thread form; 2
+// stages of 2048 elements measured best (1024 x 2..4, 2048 x 3 and smaller
+// stages were 0.6-50 % slower).  Every wait is bounded in time: one that
+// gives up sets the sticky error word, lets its own loads land and returns.
+// Chunks whose addresses do not allow 16-byte bulk copies, and the last
+// (n mod 8) elements of a tensor, take the per-element path.
+// ---------------------------------------------------------------------------
+constexpr int kSub = 2048;    // elements per stage
+constexpr int kStages = 2;    // stages in flight per CTA
+
+template <int GT>
+__host__ __device__ constexpr int bulk_stage_bytes() { return kSub * (12 + (GT == kF32 ? 4 : 2) + 2); }
+
+template <int GT, bool BF16, bool SR>
+__global__ void __launch_bounds__(kThreads) adamw_bulk_kernel(AdamwParams P) {
     const AdamwStepScalars sc = *P.scal;
     if (sc.skip) return;  // A2: nothing is written on a skipped step
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(8) uint64_t bar[kStages];
     const uint2 ch = P.p.chunks[blockIdx.x];
     const int t = int(ch.x);
     const int64_t start = int64_t(ch.y) * kChunk;
@@ -186,7 +212,7 @@ __global__ void __launch_bounds__(kThreads) adamw_main_kernel(AdamwParams P) {
     float *pp = static_cast<float *>(P.p.ptrs[t]) + start;
     float *mp = static_cast<float *>(P.m.ptrs[t]) + start;
     float *vp = static_cast<float *>(P.v.ptrs[t]) + start;
-    const void *gp = static_cast<const char *>(P.g.ptrs[t]) + start * gsz;
+    const char *gp = static_cast<const char *>(P.g.ptrs[t]) + start * gsz;
     uint16_t *bp = BF16 ? static_cast<uint16_t *>(P.b.ptrs[t]) + start : nullptr;
 
     Scal s;
@@ -201,47 +227,110 @@ __global__ void __launch_bounds__(kThreads) adamw_main_kernel(AdamwParams P) {
     s.step_size = sc.step_size;
     s.c2 = sc.bc2_sqrt;
 
-    uint32_t amax2 = 0;  // packed bf16x2 maxima of |bf16|
-    uint32_t amax1 = 0;
+    uint32_t amax2 = 0, amax1 = 0;
     const bool vec = aligned16(pp) && aligned16(mp) && aligned16(vp) && aligned16(gp) &&
                      (!BF16 || aligned16(bp));
+    int64_t done = 0;  // elements handled by the bulk pipeline
     if (vec) {
-        const int64_t ng = n >> 3;
-        int64_t i = threadIdx.x;
-        for (; i + kThreads < ng; i += 2 * kThreads) {
-            Group<GT> a, b;
-            load_group<GT>(a, pp, mp, vp, gp, i * 8);
-            load_group<GT>(b, pp, mp, vp, gp, (i + kThreads) * 8);
-            uint4 ra, rb;
-            if constexpr (SR) {
-                // group index within the tensor: (start + 8 i) / 8
-                ra = sr_random8(P.sr_seed, sc.t, t, (start >> 3) + i);
-                rb = sr_random8(P.sr_seed, sc.t, t, (start >> 3) + i + kThreads);
+        constexpr int kStage = bulk_stage_bytes<GT>();
+        const int64_t nb = n & ~int64_t(7);
+        const int nsub = int((nb + kSub - 1) / kSub);
+        if (threadIdx.x == 0) {
+            for (int q = 0; q < kStages; ++q) mbar_init(&bar[q], 1);
+            mbar_fence_init();
+        }
+        __syncthreads();
+        // stage layout: p | m | v (fp32) | g | bf16
+        auto stage_p = [&](int k) { return reinterpret_cast<float *>(smem + (k % kStages) * kStage); };
+        auto issue = [&](int k) {
+            const int64_t off = int64_t(k) * kSub;
+            const uint32_t cnt = uint32_t(min(int64_t(kSub), nb - off));
+            float *sp = stage_p(k);
+            uint64_t *b = &bar[k % kStages];
+            mbar_arrive_expect_tx(b, cnt * (12u + gsz));
+            bulk_g2s(sp, pp + off, cnt * 4u, b);
+            bulk_g2s(sp + kSub, mp + off, cnt * 4u, b);
+            bulk_g2s(sp + 2 * kSub, vp + off, cnt * 4u, b);
+            bulk_g2s(sp + 3 * kSub, gp + off * gsz, cnt * gsz, b);
+        };
+        if (threadIdx.x == 0)
+            for (int q = 0; q < kStages && q < nsub; ++q) issue(q);
+        uint32_t phases = 0;  // bit q: parity of stage q's next completion
+        int failed_at = -1;   // sub-block whose wait gave up
+        for (int k = 0; k < nsub; ++k) {
+            const int64_t off = int64_t(k) * kSub;
+            const int cnt = int(min(int64_t(kSub), nb - off));
+            const int q = k % kStages;
+            const bool w = mbar_wait(&bar[q], (phases >> q) & 1u);
+            if (!__syncthreads_and(w)) {
+                failed_at = k;
+                break;
             }
-            compute_store_group<GT, BF16, SR>(a, pp, mp, vp, bp, i * 8, s, amax2, &ra);
-            compute_store_group<GT, BF16, SR>(b, pp, mp, vp, bp, (i + kThreads) * 8, s, amax2, &rb);
+            phases ^= 1u << q;
+            float *sp = stage_p(k);
+            for (int j = threadIdx.x; 8 * j < cnt; j += kThreads) {
+                Group<GT> r;
+                const uint4 *p4 = reinterpret_cast<const uint4 *>(sp) + 2 * j;
+                const uint4 *m4 = reinterpret_cast<const uint4 *>(sp + kSub) + 2 * j;
+                const uint4 *v4 = reinterpret_cast<const uint4 *>(sp + 2 * kSub) + 2 * j;
+                r.p[0] = p4[0];
+                r.p[1] = p4[1];
+                r.m[0] = m4[0];
+                r.m[1] = m4[1];
+                r.v[0] = v4[0];
+                r.v[1] = v4[1];
+                const uint4 *g4 = reinterpret_cast<const uint4 *>(sp + 3 * kSub);
+                if constexpr (GT == kF32) {
+                    r.g[0] = g4[2 * j];
+                    r.g[1] = g4[2 * j + 1];
+                } else {
+                    r.g[0] = g4[j];
+                }
+                uint4 rnd;
+                if constexpr (SR) rnd = sr_random8(P.sr_seed, sc.t, t, ((start + off) >> 3) + j);
+                // compute_store_group writes to p/m/v/b at the given element
+                // offset: point it at this stage's shared buffers
+                uint16_t *sb = reinterpret_cast<uint16_t *>(
+                    reinterpret_cast<unsigned char *>(sp + 3 * kSub) + kSub * gsz);
+                compute_store_group<GT, BF16, SR>(r, sp, sp + kSub, sp + 2 * kSub, sb,
+                                                  int64_t(8) * j, s, amax2, &rnd);
+            }
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                bulk_s2g(pp + off, sp, uint32_t(cnt) * 4u);
+                bulk_s2g(mp + off, sp + kSub, uint32_t(cnt) * 4u);
+                bulk_s2g(vp + off, sp + 2 * kSub, uint32_t(cnt) * 4u);
+                if (BF16)
+                    bulk_s2g(bp + off,
+                             reinterpret_cast<unsigned char *>(sp + 3 * kSub) + kSub * gsz,
+                             uint32_t(cnt) * 2u);
+                bulk_commit();
+                if (k + kStages < nsub) {
+                    bulk_wait_read_all();  // this stage's stores have read it
+                    issue(k + kStages);
+                }
+            }
         }
-        if (i < ng) {
-            Group<GT> a;
-            load_group<GT>(a, pp, mp, vp, gp, i * 8);
-            uint4 ra;
-            if constexpr (SR) ra = sr_random8(P.sr_seed, sc.t, t, (start >> 3) + i);
-            compute_store_group<GT, BF16, SR>(a, pp, mp, vp, bp, i * 8, s, amax2, &ra);
+        if (threadIdx.x == 0) {
+            if (failed_at >= 0) {
+                atomicExch(P.err, 1);
+                // let the loads issued for sub-blocks failed_at .. failed_at+kStages-1
+                // finish landing in this CTA's shared memory before it exits
+                for (int k = failed_at; k < failed_at + kStages && k < nsub; ++k)
+                    mbar_wait(&bar[k % kStages], (phases >> (k % kStages)) & 1u);
+            }
+            bulk_wait_all();
         }
-        const int64_t k = ng * 8 + threadIdx.x;
-        if (k < n)
-            scalar_elem<GT, BF16, SR>(pp, mp, vp, gp, bp, k, s, amax1,
-                                      SR ? sr_u16(P.sr_seed, sc.t, t, start + k) : 0u);
-    } else {
-        for (int64_t k = threadIdx.x; k < n; k += kThreads)
-            scalar_elem<GT, BF16, SR>(pp, mp, vp, gp, bp, k, s, amax1,
-                                      SR ? sr_u16(P.sr_seed, sc.t, t, start + k) : 0u);
+        if (failed_at >= 0) return;
+        done = nb;
     }
+    for (int64_t k = done + threadIdx.x; k < n; k += kThreads)
+        scalar_elem<GT, BF16, SR>(pp, mp, vp, gp, bp, k, s, amax1,
+                                  SR ? sr_u16(P.sr_seed, sc.t, t, start + k) : 0u);
     if (BF16 && P.use_slots) {
         const int slot = P.b.slots[t];
         if (slot >= 0) {
-            // |bf16| bit patterns order like magnitudes (NaN above inf), and
-            // bf16 bits << 16 are the fp32 bits of the same value.
             uint32_t a = max(max(amax2 & 0xFFFFu, amax2 >> 16), amax1);
             a = warp_max_u32(a);
             if ((threadIdx.x & 31) == 0 && a != 0)
@@ -403,6 +492,28 @@ __global__ void __launch_bounds__(kThreads) adamw_fp8_tile_kernel(Fp8StepParams 
         atomicMax(reinterpret_cast<unsigned int *>(P.amax) + t, a << 16);
 }
 
+// Self-test of the bounded wait: a barrier that nothing completes (one
+// expected arrival, none made); the wait must give up after limit_ns and
+// report through *err, leaving the context usable.
+__global__ void bounded_wait_selftest_kernel(int32_t *err, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        mbar_fence_init();
+        const bool done = mbar_wait(&bar, 0, limit_ns);
+        *err = done ? 0 : 1;
+    }
+}
+
+template <int GT, bool BF16, bool SR>
+void bulk_launch(dim3 grid, dim3 block, cudaStream_t s, const AdamwParams &P) {
+    constexpr int smem = kStages * bulk_stage_bytes<GT>();
+    // above the 48 KB default: opt in (cheap, and valid for whichever device is current)
+    cudaFuncSetAttribute(adamw_bulk_kernel<GT, BF16, SR>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    adamw_bulk_kernel<GT, BF16, SR><<<grid, block, smem, s>>>(P);
+}
+
 }  // namespace
 
 cudaError_t launch_adamw(const ListView &p, const ListView &m, const ListView &v,
@@ -424,6 +535,8 @@ cudaError_t launch_adamw_main(const ListView &p, const ListView &m, const ListVi
                               const float *scale, const AdamwConsts &c,
                               const AdamwStepScalars *scal, float *amax, bool use_slots,
                               cudaStream_t s, bool stochastic, uint64_t seed) {
+    // the sticky error word sits next to the step scalars in the same scratch block
+    int32_t *err = reinterpret_cast<int32_t *>(const_cast<AdamwStepScalars *>(scal)) + kErrWordOffset;
     if (n_chunks == 0) return cudaSuccess;
     AdamwParams P;
     P.p = p;
@@ -442,13 +555,14 @@ cudaError_t launch_adamw_main(const ListView &p, const ListView &m, const ListVi
     P.eps = c.eps;
     P.use_slots = use_slots ? 1 : 0;
     P.sr_seed = seed;
+    P.err = err;
     const dim3 grid((unsigned)n_chunks), block(kThreads);
     const bool bf = b != nullptr;
 #define AMP_ADAMW_LAUNCH(GT)                                                         \
     do {                                                                             \
-        if (bf && stochastic) adamw_main_kernel<GT, true, true><<<grid, block, 0, s>>>(P); \
-        else if (bf) adamw_main_kernel<GT, true><<<grid, block, 0, s>>>(P);          \
-        else adamw_main_kernel<GT, false><<<grid, block, 0, s>>>(P);                 \
+        if (bf && stochastic) bulk_launch<GT, true, true>(grid, block, s, P);         \
+        else if (bf) bulk_launch<GT, true, false>(grid, block, s, P);                \
+        else bulk_launch<GT, false, false>(grid, block, s, P);                       \
     } while (0)
     if (gelem == kF32) AMP_ADAMW_LAUNCH(kF32);
     else if (gelem == kF16) AMP_ADAMW_LAUNCH(kF16);
@@ -503,6 +617,11 @@ cudaError_t launch_adamw_fp8_delayed(const Fp8DelayedLists &L, int gelem, int fp
     else if (gelem == kF16) AMP_FP8_LAUNCH(kF16);
     else AMP_FP8_LAUNCH(kBF16);
 #undef AMP_FP8_LAUNCH
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bounded_wait_selftest(int32_t *err, double limit_s, cudaStream_t s) {
+    bounded_wait_selftest_kernel<<<1, 32, 0, s>>>(err, (unsigned long long)(limit_s * 1e9));
     return cudaGetLastError();
 }
 

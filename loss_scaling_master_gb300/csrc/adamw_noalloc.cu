@@ -183,3 +183,25 @@ extern "C" amp_status amp_adamw_master_step_noalloc(
     if (e != cudaSuccess) return noalloc_fail(AMP_ECUDA, "%s: %s", fn, cudaGetErrorString(e));
     return AMP_OK;
 }
+
+extern "C" amp_status amp_noalloc_check(amp_stream_t stream) {
+    const char *fn = "amp_noalloc_check";
+    unsigned char *base = nullptr;
+    cudaError_t e = scratch_on_current_device(&base);
+    if (e != cudaSuccess)
+        return noalloc_fail(AMP_ECUDA, "%s: cudaGetSymbolAddress: %s", fn, cudaGetErrorString(e));
+    int32_t *word = reinterpret_cast<int32_t *>(base) + amp::kErrWordOffset;
+    int32_t v = 0;
+    e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) e = cudaMemcpy(&v, word, sizeof v, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && v != 0) {
+        const int32_t zero = 0;
+        e = cudaMemcpy(word, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        if (e == cudaSuccess)
+            return noalloc_fail(AMP_ETIMEOUT,
+                                "%s: a kernel's bounded wait for its asynchronous copies gave up; "
+                                "the chunks it held were not updated", fn);
+    }
+    if (e != cudaSuccess) return noalloc_fail(AMP_ECUDA, "%s: %s", fn, cudaGetErrorString(e));
+    return AMP_OK;
+}

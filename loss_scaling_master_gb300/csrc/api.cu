@@ -80,7 +80,7 @@ extern "C" {
 
 const char *amp_last_error(void) { return g_err; }
 
-int amp_abi_version(void) { return 5; }
+int amp_abi_version(void) { return 6; }
 
 amp_status amp_tensor_list_create(int n, void *const *dev_ptrs, const int64_t *rows,
                                   const int64_t *cols, amp_dtype dtype, amp_stream_t stream,
@@ -212,6 +212,33 @@ amp_status amp_tensor_list_destroy(amp_tensor_list list) {
     cudaError_t e = list->block ? cudaFree(list->block) : cudaSuccess;
     delete list;
     return e == cudaSuccess ? AMP_OK : cuda_fail(e, "amp_tensor_list_destroy");
+}
+
+amp_status amp_tensor_list_check(amp_tensor_list list, amp_stream_t stream) {
+    if (!list) return fail(AMP_EINVAL, "amp_tensor_list_check: NULL list");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int32_t *word = reinterpret_cast<int32_t *>(list->scratch) + amp::kErrWordOffset;
+    int32_t v = 0;
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemcpy(&v, word, sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "amp_tensor_list_check");
+    if (v != 0) {
+        const int32_t zero = 0;
+        e = cudaMemcpy(word, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, "amp_tensor_list_check");
+        return fail(AMP_ETIMEOUT,
+                    "amp_tensor_list_check: a kernel's bounded wait for its asynchronous copies "
+                    "gave up; the chunks it held were not updated");
+    }
+    return AMP_OK;
+}
+
+amp_status amp_selftest_bounded_wait(int32_t *err_dev, double limit_seconds, amp_stream_t stream) {
+    if (!err_dev || !(limit_seconds > 0.0) || limit_seconds > 10.0)
+        return fail(AMP_EINVAL, "amp_selftest_bounded_wait: err_dev NULL or limit not in (0, 10] s");
+    cudaError_t e = amp::launch_bounded_wait_selftest(err_dev, limit_seconds,
+                                                      reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AMP_OK : cuda_fail(e, "amp_selftest_bounded_wait");
 }
 
 amp_status amp_unscale_check(amp_tensor_list grads, const float *scale_dev, int32_t *found_inf_dev,

@@ -34,6 +34,11 @@ struct AdamwConsts {
     float decay, b1, omb1, b2, omb2, eps;
 };
 
+// Offset, in int32 words from the step-scalar block, of the sticky error word
+// the bulk-copy kernels set when a bounded wait gives up (within the 256-byte
+// per-list scratch; the step scalars take the first 32 bytes).
+constexpr int kErrWordOffset = 32;
+
 // Device scalars of one AdamW step, written by the prologue kernel.
 struct AdamwStepScalars {
     int32_t skip;
@@ -85,6 +90,8 @@ cudaError_t launch_adamw_fp8_delayed(const Fp8DelayedLists &L, int gelem, int fp
                                      const AdamwConsts &c, AdamwStepScalars *scal,
                                      const float *hist, int hist_len, double eps, float *amax,
                                      float *inv_scale, cudaStream_t s);
+
+cudaError_t launch_bounded_wait_selftest(int32_t *err, double limit_s, cudaStream_t s);
 
 cudaError_t launch_update_scale_hist(float *scale, int32_t *tracker, int32_t *found_inf,
                                      float growth, float backoff, int32_t interval, float *amax,

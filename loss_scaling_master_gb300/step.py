@@ -216,6 +216,12 @@ class AmpOptimizerStep:
                            self.backoff, self.interval, amax=self.amax if self.n_fp8 else None,
                            n_amax=self.n_fp8, stream=s)
 
+    def check(self, stream=None):
+        """Raise AmpError(AMP_ETIMEOUT) if an AdamW kernel's bounded wait on its
+        bulk copies gave up since the last check (synchronises)."""
+        holder = self.L_q if self.fp8_scaling == "delayed" else self.L_master
+        A.amp_tensor_list_check(holder, stream=stream if stream is not None else self.stream)
+
     def state(self) -> dict:
         """Host copy of the scaler/optimizer counters (synchronises)."""
         return {"scale": float(self.scale.item()), "growth_tracker": int(self.growth_tracker.item()),

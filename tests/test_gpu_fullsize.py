@@ -78,6 +78,7 @@ def test_gpt2_small_full_parity(A):
             ident.append(bit_identical_fraction(g, ref))
         assert_bf16_close(to_host_bits(st.bf16[i]), orc.bf16[i], f"bf16[{cfg.specs[i].name}]")
     assert min(ident) == 1.0
+    st.check()                      # no bounded wait gave up
     st.close()
 
 
@@ -128,6 +129,7 @@ def test_llama_1b_sampled_parity(A):
             assert bit_identical_fraction(g, ref[i]) == 1.0
     for i, b in enumerate(take(st.bf16)):
         assert_bf16_close(b, orc.bf16[i], f"bf16[{cfg.specs[i].name}]")
+    st.check()                      # no bounded wait gave up
     st.close()
 
 
@@ -203,6 +205,7 @@ def test_llama3_8b_bench_state_parity(A, fp8_scaling):
             if fp8_scaling == "delayed":
                 assert np.array_equal(to_host_bits(st.amax_history)[fp8_index[i]],
                                       orc.hist[orc.slots[pos]])
+    st.check()                      # no bounded wait gave up
     st.close()
     del st, info
     torch.cuda.empty_cache()

@@ -757,3 +757,29 @@ def test_checkpoint_resume_is_bit_identical(A, dev, fp8_scaling):
             assert torch.equal(x.view(torch.uint8), y.view(torch.uint8)), k
     whole.close()
     resumed.close()
+
+
+# ------------------------------------------------------ bounded waits
+def test_bounded_wait_gives_up_and_context_survives(A, dev):
+    """A wait on a barrier that nothing completes ends after its time limit
+    with an error status instead of hanging; the GPU keeps working."""
+    import time
+    err = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    t0 = time.perf_counter()
+    A.amp_selftest_bounded_wait(err, 0.05)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 1
+    assert time.perf_counter() - t0 < 5.0
+    x = torch.arange(1000, device=dev, dtype=torch.float32)
+    assert float(x.sum().item()) == 499500.0               # the context is fine
+
+
+def test_list_check_ok_after_steps(A, dev):
+    from loss_scaling_master_gb300 import AmpOptimizerStep
+    st = AmpOptimizerStep([torch.zeros(5000, device=dev)], [torch.zeros(5000, dtype=torch.float16, device=dev)],
+                          lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
+    for _ in range(3):
+        st.step()
+    A.amp_tensor_list_check(st.L_master)
+    st.check()
+    st.close()

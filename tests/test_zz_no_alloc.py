@@ -61,6 +61,8 @@ def test_noalloc_matches_handle_path_two_calls(A):
         A.amp_adamw_master_step_noalloc(pb, mb, vb, grads, bb, scale, fi, step_b, *hyper,
                                         amax_slots=slots, amax=amax_b)
         torch.cuda.synchronize()
+        A.amp_noalloc_check()
+        A.amp_tensor_list_check(LP)
         LG.close()
         assert int(step_a.item()) == int(step_b.item()) == call + 1
         assert np.array_equal(to_host_bits(amax_a).view(np.uint32), to_host_bits(amax_b).view(np.uint32))
