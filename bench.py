@@ -373,12 +373,20 @@ def run_e2e(args, step, info, stream, world):
     piece = (1 << 30) // host.element_size()
     torch.cuda.synchronize()
 
-    def e2e_step(k):
+    copy_ev = []   # (start, end) of each timed step's host->device copy
+
+    def e2e_step(k, timed=False):
         b = k % 2
         with torch.cuda.stream(copy_stream):
             copy_stream.wait_event(free[b])
+            if timed:
+                ce = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                ce[0].record(copy_stream)
             for o in range(0, host.numel(), piece):
                 bufs[b][o:o + piece].copy_(host[o:o + piece], non_blocking=True)
+            if timed:
+                ce[1].record(copy_stream)
+                copy_ev.append(ce)
             ready[b].record(copy_stream)
         stream.wait_event(ready[b])
         step.step(stream=stream, grad_buffer=(0 if b == 0 else b1))
@@ -400,15 +408,19 @@ def run_e2e(args, step, info, stream, world):
     t0.record(stream)
     copy_stream.wait_event(t0)
     for k in range(args.steps):
-        e2e_step(k)
+        e2e_step(k, timed=True)
     t1.record(stream)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
+    copy_ms = sorted(a.elapsed_time(b) for a, b in copy_ev)
     del host, bufs
     hbuf.close()
     return {"value": info["params"] * args.steps * world / (ms * 1e-3), "unit": "params/s",
             "ms_per_step": ms / args.steps, "h2d_bytes_per_step": nbytes,
             "d2h_bytes_per_step": 16,
+            "h2d_copy_ms": {"min": copy_ms[0], "median": copy_ms[len(copy_ms) // 2],
+                            "max": copy_ms[-1]},
+            "h2d_gbs_best": nbytes / copy_ms[0] / 1e6,
             "api": "AmpOptimizerStep.step() (C-ABI calls), pinned (huge-page, cudaHostRegister) "
                    "H2D of each step's grads (1 GiB pieces on a copy stream, double-buffered) + "
                    "D2H of {scale, tracker, step, found_inf}",

@@ -55,7 +55,7 @@ typedef struct CUstream_st *amp_stream_t;
 
 typedef enum {
     AMP_OK = 0,
-    AMP_EINVAL = -1,  /* null pointer, negative size, mismatched list shapes */
+    AMP_EINVAL = -1,  /* null pointer, negative or too large size (a side >= 2^48 or rows*cols past int64), mismatched list shapes */
     AMP_EDTYPE = -2,  /* element type not accepted by this entry point */
     AMP_ECUDA = -4,   /* a CUDA runtime call or kernel launch failed */
     AMP_ENOMEM = -5,  /* device allocation in amp_tensor_list_create failed */

@@ -82,6 +82,13 @@ const char *amp_last_error(void) { return g_err; }
 
 int amp_abi_version(void) { return 6; }
 
+// A [rows, cols] shape the launch arithmetic can hold: non-negative, each side
+// below 2^48 and rows * cols without int64 overflow.
+static bool bad_shape(int64_t rows, int64_t cols) {
+    const int64_t lim = int64_t(1) << 48;
+    return rows < 0 || cols < 0 || rows >= lim || cols >= lim || (cols > 0 && rows > INT64_MAX / cols);
+}
+
 amp_status amp_tensor_list_create(int n, void *const *dev_ptrs, const int64_t *rows,
                                   const int64_t *cols, amp_dtype dtype, amp_stream_t stream,
                                   amp_tensor_list *out) {
@@ -101,9 +108,9 @@ amp_status amp_tensor_list_create(int n, void *const *dev_ptrs, const int64_t *r
     std::vector<uint2> chunks, tiles;
     for (int i = 0; i < n; ++i) {
         const int64_t r = rows[i], c = cols ? cols[i] : 1;
-        if (r < 0 || c < 0) {
+        if (bad_shape(r, c)) {
             delete L;
-            return fail(AMP_EINVAL, "amp_tensor_list_create: negative size at tensor %d", i);
+            return fail(AMP_EINVAL, "amp_tensor_list_create: negative or too large size at tensor %d", i);
         }
         const int64_t ne = r * c;
         if (ne > 0 && dev_ptrs[i] == nullptr) {
@@ -431,7 +438,7 @@ amp_status fp8_quant_tensorwise(const void *x, amp_dtype x_dtype, int64_t rows, 
                                 amp_dtype fp8_dtype, double eps, void *out, void *out_t,
                                 float *inv_scale_dev, float *amax_dev, int amax_given,
                                 const int32_t *skip_if_dev, amp_stream_t stream) {
-    if (rows < 0 || cols < 0) return fail(AMP_EINVAL, "fp8_quant_tensorwise: negative size");
+    if (bad_shape(rows, cols)) return fail(AMP_EINVAL, "fp8_quant_tensorwise: negative or too large size");
     if (!inv_scale_dev || !amax_dev) return fail(AMP_EINVAL, "fp8_quant_tensorwise: NULL inv_scale/amax");
     if (rows * cols > 0 && (!x || !out)) return fail(AMP_EINVAL, "fp8_quant_tensorwise: NULL x/out");
     if (!(eps > 0.0)) return fail(AMP_EINVAL, "fp8_quant_tensorwise: eps must be > 0");
@@ -455,7 +462,7 @@ amp_status fp8_quant_rowwise(const void *x, amp_dtype x_dtype, int64_t rows, int
                              float *amax_col, float *scale_col, float *inv_scale_col,
                              const int32_t *skip_if_dev, amp_stream_t stream) {
     const char *fn = "fp8_quant_rowwise";
-    if (rows < 0 || cols < 0) return fail(AMP_EINVAL, "%s: negative size", fn);
+    if (bad_shape(rows, cols)) return fail(AMP_EINVAL, "%s: negative or too large size", fn);
     if (rows * cols > 0 && (!x || !out || !amax_row || !scale_row || !inv_scale_row))
         return fail(AMP_EINVAL, "%s: NULL x / out / row outputs", fn);
     if (out_t && rows * cols > 0 && (!amax_col || !scale_col || !inv_scale_col))
@@ -492,7 +499,9 @@ amp_status fp8_quant_tensorwise_list(amp_tensor_list x, amp_tensor_list out, amp
         return fail(AMP_EINVAL, "fp8_quant_tensorwise_list: out shapes differ from x");
     if (out_t && (out_t->n != x->n || out_t->rows != x->cols || out_t->cols != x->rows))
         return fail(AMP_EINVAL, "fp8_quant_tensorwise_list: out_t shapes are not x transposed");
-    cudaError_t e = amp::launch_fp8_quant_list(x->view, x->n_tiles, xc, out->view,
+    const bool any_empty =
+        std::any_of(x->numel.begin(), x->numel.end(), [](int64_t k) { return k == 0; });
+    cudaError_t e = amp::launch_fp8_quant_list(x->view, x->n_tiles, any_empty, xc, out->view,
                                                out_t ? &out_t->view : nullptr, fc, eps, amax_dev,
                                                inv_scale_dev, skip_if_dev,
                                                reinterpret_cast<cudaStream_t>(stream));

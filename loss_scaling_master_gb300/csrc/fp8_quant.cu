@@ -144,6 +144,20 @@ __global__ void __launch_bounds__(kThreads) quant_list_kernel(ListView X, ListVi
                        tr * kTile, tc * kTile, &s_scale, sm);
 }
 
+// Tensors of a list with no elements have no tiles, so quant_list_kernel never
+// visits them; their inv_scale still follows from their amax like any other's.
+template <int FT>
+__global__ void quant_list_empty_kernel(ListView X, const float *amax, float *inv_scale,
+                                        double eps, const int32_t *skip_if) {
+    if (skip_if && *skip_if) return;
+    for (int t = threadIdx.x; t < X.n; t += blockDim.x) {
+        if (X.numel[t] != 0) continue;
+        float s32, inv;
+        tensor_scale(amax[t], eps, fp8_max<FT>(), s32, inv);
+        inv_scale[t] = inv;
+    }
+}
+
 // amax is an output: it starts from +0 (unless the call is skipped).
 __global__ void amax_zero_kernel(float *amax, const int32_t *skip_if) {
     if (!(skip_if && *skip_if)) *amax = 0.0f;
@@ -252,10 +266,16 @@ cudaError_t launch_fp8_quant(const void *x, int xelem, int64_t rows, int64_t col
 #undef AMP_Q1
 }
 
-cudaError_t launch_fp8_quant_list(const ListView &x, int64_t n_tiles, int xelem,
+cudaError_t launch_fp8_quant_list(const ListView &x, int64_t n_tiles, bool any_empty, int xelem,
                                   const ListView &out, const ListView *out_t, int fp8,
                                   double eps, const float *amax, float *inv_scale,
                                   const int32_t *skip_if, cudaStream_t s) {
+    if (any_empty) {
+        if (fp8 == kE4M3) quant_list_empty_kernel<kE4M3><<<1, kThreads, 0, s>>>(x, amax, inv_scale, eps, skip_if);
+        else quant_list_empty_kernel<kE5M2><<<1, kThreads, 0, s>>>(x, amax, inv_scale, eps, skip_if);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     if (n_tiles == 0) return cudaSuccess;
     const ListView ot = out_t ? *out_t : ListView{};
     const int has_t = out_t != nullptr;

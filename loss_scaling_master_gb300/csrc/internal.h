@@ -112,7 +112,7 @@ cudaError_t launch_fp8_quant_rowwise(const void *x, int xelem, int64_t rows, int
                                      float *scale_col, float *inv_col, const int32_t *skip_if,
                                      int device, cudaStream_t s);
 
-cudaError_t launch_fp8_quant_list(const ListView &x, int64_t n_tiles, int xelem,
+cudaError_t launch_fp8_quant_list(const ListView &x, int64_t n_tiles, bool any_empty, int xelem,
                                   const ListView &out, const ListView *out_t, int fp8,
                                   double eps, const float *amax, float *inv_scale,
                                   const int32_t *skip_if, cudaStream_t s);

@@ -68,5 +68,17 @@ def test_invalid_arguments_return_status(lib):
     one = (ctypes.c_int64 * 1)(7)
     assert lib.amp_tensor_list_create(1, ptrs, neg, None, DT["f32"], None, ctypes.byref(out)) == EINVAL
     assert lib.amp_tensor_list_create(1, ptrs, one, None, DT["f32"], None, ctypes.byref(out)) == EINVAL
+    # shapes past the launch arithmetic: a side >= 2^48, rows * cols past int64
+    big = (ctypes.c_int64 * 1)(1 << 48)
+    huge = (ctypes.c_int64 * 1)((1 << 40) + 1)
+    assert lib.amp_tensor_list_create(1, (P * 1)(dummy), big, None, DT["f32"], None,
+                                      ctypes.byref(out)) == EINVAL
+    assert lib.amp_tensor_list_create(1, (P * 1)(dummy), huge, huge, DT["f32"], None,
+                                      ctypes.byref(out)) == EINVAL
+    assert b"too large" in lib.amp_last_error()
+    assert lib.fp8_quant_tensorwise(dummy, DT["bf16"], (1 << 40) + 1, (1 << 40) + 1, DT["e4m3fn"],
+                                    1e-12, dummy, None, dummy, dummy, 0, None, None) == EINVAL
+    assert lib.fp8_quant_rowwise(dummy, DT["bf16"], 0, 1 << 48, DT["e4m3fn"], 1e-12, dummy, None,
+                                 dummy, dummy, dummy, None, None, None, None, None) == EINVAL
     assert lib.amp_tensor_list_create(1, ptrs, one, None, 99, None, ctypes.byref(out)) == EDTYPE
     assert not out.value

@@ -783,3 +783,85 @@ def test_list_check_ok_after_steps(A, dev):
     A.amp_tensor_list_check(st.L_master)
     st.check()
     st.close()
+
+
+# ------------------------------------------------------ empty tensors and lists
+@pytest.mark.parametrize("fp8_scaling", ["dynamic", "delayed"])
+def test_empty_tensors_in_the_step(A, dev, fp8_scaling):
+    """Tensors with no elements among the parameters, including empty FP8
+    weights of shape [0, 128] and [128, 0]: the step runs, every non-empty
+    tensor matches the oracle bit for bit, and the empty FP8 weights get the
+    inv_scale of amax 0 (the EPS floor of [FP8] §2)."""
+    from loss_scaling_master_gb300 import AmpOptimizerStep
+    rng = np.random.default_rng(41)
+    shapes = [(0,), (96, 256), (0, 128), (300,), (128, 0), (0,), (128, 136)]
+    fp8_shapes = [s if len(s) == 2 else None for s in shapes]
+    sizes = [int(np.prod(s)) for s in shapes]
+    master = [(rng.standard_normal(n) * 0.02).astype(np.float32) for n in sizes]
+    G = [torch.empty(n, dtype=torch.float16, device=dev) for n in sizes]
+    hyper = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+    st = AmpOptimizerStep([torch.from_numpy(m.copy()).to(dev) for m in master], G,
+                          init_scale=65536.0, growth_interval=2, fp8_shapes=fp8_shapes,
+                          fp8_scaling=fp8_scaling, **hyper)
+    orc = O.AmpStepOracle(master, "f16", hyper["lr"], hyper["beta1"], hyper["beta2"],
+                          hyper["eps"], hyper["weight_decay"], 65536.0, 2.0, 0.5, 2,
+                          fp8_shapes=fp8_shapes, fp8_scaling=fp8_scaling)
+    for k in range(1, 6):
+        gh = [(rng.standard_normal(n) * 1e-4 * orc.scale).astype(np.float16).view(np.uint16)
+              for n in sizes]
+        if k == 3:
+            gh[3][299] = 0x7C00
+        for t, h in zip(G, gh):
+            t.copy_(to_device(h, "f16", dev))
+        st.step()
+        orc.run(gh)
+        s = st.state()
+        assert (s["scale"], s["growth_tracker"], s["step"], s["found_inf"]) == \
+            (orc.scale, orc.tracker, orc.step, 0), k
+    st.check()
+    for i, n in enumerate(sizes):
+        assert np.array_equal(to_host_bits(st.master[i]).view(np.uint32),
+                              orc.master[i].view(np.uint32)), i
+        assert np.array_equal(to_host_bits(st.bf16[i]), orc.bf16[i]), i
+    inv = to_host_bits(st.inv_scale)
+    j = 0
+    for i, sh in enumerate(fp8_shapes):
+        if sh is None:
+            continue
+        assert np.array_equal(to_host_bits(st.fp8[j].view(torch.uint8)).ravel(), orc.fp8[i])
+        assert np.array_equal(to_host_bits(st.fp8_t[j].view(torch.uint8)).ravel(), orc.fp8_t[i])
+        assert inv[j].view(np.uint32) == np.float32(orc.inv_scale[orc.slots[i]]).view(np.uint32), (i, inv[j])
+        if sizes[i] == 0:
+            assert inv[j] == np.float32(1e-12 / 448.0)
+        j += 1
+    st.close()
+
+
+def test_lists_with_no_tensors(A, dev):
+    """Every list entry point accepts a list of no tensors: the check leaves
+    found_inf alone, the norm is 0, and the AdamW step (nothing to update)
+    still advances the step counter unless skipped, as the oracle does."""
+    E = [A.amp_tensor_list_create([], dtype=d) for d in ("f32", "f32", "f32", "f16", "bf16")]
+    X8 = A.amp_tensor_list_create([], two_d=True, dtype="bf16")
+    Q8 = A.amp_tensor_list_create([], two_d=True, dtype="e4m3fn")
+    QT = A.amp_tensor_list_create([], two_d=True, dtype="e4m3fn")
+    scale = torch.tensor([1024.0], device=dev)
+    fi = torch.zeros(1, dtype=torch.int32, device=dev)
+    step = torch.zeros(1, dtype=torch.int32, device=dev)
+    sumsq = torch.full((1,), -1.0, dtype=torch.float64, device=dev)
+    A.amp_unscale_check(E[3], scale, fi)
+    A.amp_unscale_check_norm(E[3], scale, fi, sumsq)
+    A.amp_adamw_master_step(*E, scale, fi, step, 1e-3, 0.9, 0.999, 1e-8, 0.01)
+    fi.fill_(1)
+    A.amp_adamw_master_step(*E, scale, fi, step, 1e-3, 0.9, 0.999, 1e-8, 0.01)
+    amax = torch.zeros(1, device=dev)
+    inv = torch.zeros(1, device=dev)
+    A.fp8_quant_tensorwise_list(X8, Q8, QT, "e4m3fn", amax, inv)
+    torch.cuda.synchronize()
+    rstep = O.adamw_master_step([], [], [], [], "f16", None, 1024.0, 0, 0, 1e-3, 0.9, 0.999, 1e-8, 0.01)
+    rstep = O.adamw_master_step([], [], [], [], "f16", None, 1024.0, 1, rstep, 1e-3, 0.9, 0.999, 1e-8, 0.01)
+    assert int(step.item()) == rstep == 1
+    assert float(sumsq.item()) == 0.0
+    A.amp_tensor_list_check(E[0])
+    for L in E + [X8, Q8, QT]:
+        L.close()
