@@ -125,6 +125,22 @@ amp_status amp_selftest_bounded_wait(int32_t *err_dev, double limit_seconds, amp
  * device like any cudaFree).  NULL is accepted. */
 amp_status amp_tensor_list_destroy(amp_tensor_list list);
 
+/* Feed and read back a list from host memory.  The pages have no counterpart
+ * (they run on framework tensors); these let a caller with host buffers drive
+ * the step through this ABI alone.
+ *   host_ptrs  n host pointers; host_ptrs[i] holds numel[i] elements of the
+ *              list dtype (may be NULL for an empty tensor)
+ * One cudaMemcpyAsync per non-empty tensor, in list order, on `stream`.  With
+ * page-locked host memory (cudaHostAlloc / cudaHostRegister) the copies are
+ * asynchronous; with pageable memory CUDA stages them and the call may return
+ * only after they are done.  All pointers are checked before the first copy
+ * (AMP_EINVAL, nothing enqueued); a copy that fails to enqueue returns
+ * AMP_ECUDA with the earlier copies already enqueued. */
+amp_status amp_tensor_list_copy_from_host(amp_tensor_list list, const void *const *host_ptrs,
+                                          amp_stream_t stream);
+amp_status amp_tensor_list_copy_to_host(amp_tensor_list list, void *const *host_ptrs,
+                                        amp_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* A1: unscale + non-finite check.  [CH20] §20.2.2, [MP] "Gradient 和 Loss    */
 /* Scaling", [NOTES] §4 steps 3-4: before the optimizer the scaled gradients  */

@@ -27,6 +27,7 @@ _TORCH_DT = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16",
 # every symbol include/ampfp8.h declares
 EXPORTS = ("amp_tensor_list_create", "amp_tensor_list_set_amax_slots", "amp_tensor_list_destroy",
            "amp_tensor_list_check", "amp_selftest_bounded_wait",
+           "amp_tensor_list_copy_from_host", "amp_tensor_list_copy_to_host",
            "amp_unscale_check", "amp_unscale_check_norm", "amp_adamw_master_step",
            "amp_adamw_master_step_clip", "amp_adamw_master_step_sr",
            "amp_adamw_master_step_noalloc", "amp_noalloc_check",
@@ -68,6 +69,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.amp_tensor_list_destroy.argtypes = [P]
         L.amp_unscale_check.argtypes = [P, P, P, i32, P]
         L.amp_tensor_list_check.argtypes = [P, P]
+        L.amp_tensor_list_copy_from_host.argtypes = [P, P, P]
+        L.amp_tensor_list_copy_to_host.argtypes = [P, P, P]
         L.amp_noalloc_check.argtypes = [P]
         L.amp_selftest_bounded_wait.argtypes = [P, dbl, P]
         L.amp_adamw_master_step.argtypes = [P, P, P, P, P, P, P, P,
@@ -181,6 +184,38 @@ def amp_tensor_list_destroy(lst: TensorList):
 def amp_tensor_list_check(lst: TensorList, stream=None):
     """Raise AmpError(AMP_ETIMEOUT) if a kernel's bounded wait gave up (synchronises)."""
     _check("amp_tensor_list_check", load().amp_tensor_list_check(lst.handle, _stream(stream)))
+
+
+def _host_ptrs(items, n: int):
+    """Host addresses of numpy arrays / CPU tensors / ints (None for empty tensors)."""
+    items = list(items)
+    if len(items) != n:
+        raise ValueError(f"{len(items)} host buffers for a list of {n} tensors")
+    vals = []
+    for x in items:
+        if x is None or isinstance(x, int):
+            vals.append(x)
+        elif hasattr(x, "ctypes"):
+            vals.append(x.ctypes.data)
+        else:
+            if x.is_cuda:
+                raise ValueError("host buffers must be in host memory")
+            vals.append(x.data_ptr())
+    return (P * max(n, 1))(*vals)
+
+
+def amp_tensor_list_copy_from_host(lst: TensorList, host, stream=None):
+    """One H2D cudaMemcpyAsync per tensor from the host buffers (kept alive by
+    the caller until the copies are done)."""
+    _check("amp_tensor_list_copy_from_host",
+           load().amp_tensor_list_copy_from_host(lst.handle, _host_ptrs(host, len(lst)),
+                                                 _stream(stream)))
+
+
+def amp_tensor_list_copy_to_host(lst: TensorList, host, stream=None):
+    _check("amp_tensor_list_copy_to_host",
+           load().amp_tensor_list_copy_to_host(lst.handle, _host_ptrs(host, len(lst)),
+                                               _stream(stream)))
 
 
 def amp_noalloc_check(stream=None):

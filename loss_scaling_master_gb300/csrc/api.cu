@@ -80,7 +80,7 @@ extern "C" {
 
 const char *amp_last_error(void) { return g_err; }
 
-int amp_abi_version(void) { return 6; }
+int amp_abi_version(void) { return 7; }
 
 // A [rows, cols] shape the launch arithmetic can hold: non-negative, each side
 // below 2^48 and rows * cols without int64 overflow.
@@ -219,6 +219,37 @@ amp_status amp_tensor_list_destroy(amp_tensor_list list) {
     cudaError_t e = list->block ? cudaFree(list->block) : cudaSuccess;
     delete list;
     return e == cudaSuccess ? AMP_OK : cuda_fail(e, "amp_tensor_list_destroy");
+}
+
+static amp_status list_copy_host(amp_tensor_list list, void *const *host_ptrs, bool to_host,
+                                 amp_stream_t stream) {
+    const char *fn = to_host ? "amp_tensor_list_copy_to_host" : "amp_tensor_list_copy_from_host";
+    if (!list) return fail(AMP_EINVAL, "%s: NULL list", fn);
+    if (list->n > 0 && !host_ptrs) return fail(AMP_EINVAL, "%s: host_ptrs is NULL", fn);
+    for (int i = 0; i < list->n; ++i)
+        if (list->numel[i] > 0 && !host_ptrs[i])
+            return fail(AMP_EINVAL, "%s: NULL host pointer of non-empty tensor %d", fn, i);
+    const size_t es = elem_size(list->dtype);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    for (int i = 0; i < list->n; ++i) {
+        if (list->numel[i] == 0) continue;
+        const size_t bytes = size_t(list->numel[i]) * es;
+        cudaError_t e = to_host
+            ? cudaMemcpyAsync(host_ptrs[i], list->ptrs[i], bytes, cudaMemcpyDeviceToHost, s)
+            : cudaMemcpyAsync(list->ptrs[i], host_ptrs[i], bytes, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, fn);
+    }
+    return AMP_OK;
+}
+
+amp_status amp_tensor_list_copy_from_host(amp_tensor_list list, const void *const *host_ptrs,
+                                          amp_stream_t stream) {
+    return list_copy_host(list, const_cast<void *const *>(host_ptrs), false, stream);
+}
+
+amp_status amp_tensor_list_copy_to_host(amp_tensor_list list, void *const *host_ptrs,
+                                        amp_stream_t stream) {
+    return list_copy_host(list, host_ptrs, true, stream);
 }
 
 amp_status amp_tensor_list_check(amp_tensor_list list, amp_stream_t stream) {

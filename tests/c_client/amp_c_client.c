@@ -72,14 +72,23 @@ int main(int argc, char **argv) {
         v[i] = dmalloc(numel[i] * 4);
         g[i] = dmalloc(numel[i] * 2);
         b[i] = dmalloc(numel[i] * 2);
-        float *h = malloc(numel[i] * 4);
-        rd(h, numel[i] * 4, in);
-        CU(cudaMemcpy(p[i], h, numel[i] * 4, cudaMemcpyHostToDevice));
-        free(h);
         slots[i] = cols[i] ? n8++ : -1;
     }
     amp_tensor_list Lp, Lm, Lv, Lg, Lb, Lx, Lq, Lqt;
     CK(amp_tensor_list_create(n, p, numel, NULL, AMP_DT_F32, NULL, &Lp));
+    /* host buffers, one per tensor, fed and read back through the ABI */
+    void **hp = malloc(n * sizeof(void *)), **hm = malloc(n * sizeof(void *)),
+         **hv = malloc(n * sizeof(void *)), **hg = malloc(n * sizeof(void *)),
+         **hb = malloc(n * sizeof(void *));
+    for (int i = 0; i < n; ++i) {
+        hp[i] = malloc(numel[i] * 4 + 4);
+        hm[i] = malloc(numel[i] * 4 + 4);
+        hv[i] = malloc(numel[i] * 4 + 4);
+        hg[i] = malloc(numel[i] * 2 + 2);
+        hb[i] = malloc(numel[i] * 2 + 2);
+        rd(hp[i], numel[i] * 4, in);
+    }
+    CK(amp_tensor_list_copy_from_host(Lp, (const void *const *)hp, NULL));
     CK(amp_tensor_list_create(n, m, numel, NULL, AMP_DT_F32, NULL, &Lm));
     CK(amp_tensor_list_create(n, v, numel, NULL, AMP_DT_F32, NULL, &Lv));
     CK(amp_tensor_list_create(n, g, numel, NULL, AMP_DT_F16, NULL, &Lg));
@@ -108,12 +117,8 @@ int main(int argc, char **argv) {
     const amp_adamw_hyper hy = {1e-3, 0.9, 0.999, 1e-8, 0.01};
     int32_t *fi_log = malloc(steps * 4);
     for (int k = 0; k < steps; ++k) {
-        for (int i = 0; i < n; ++i) {
-            uint16_t *h = malloc(numel[i] * 2);
-            rd(h, numel[i] * 2, in);
-            CU(cudaMemcpy(g[i], h, numel[i] * 2, cudaMemcpyHostToDevice));
-            free(h);
-        }
+        for (int i = 0; i < n; ++i) rd(hg[i], numel[i] * 2, in);
+        CK(amp_tensor_list_copy_from_host(Lg, (const void *const *)hg, NULL));
         CK(amp_unscale_check(Lg, scale, found, 0, NULL));
         CU(cudaMemcpy(&fi_log[k], found, 4, cudaMemcpyDeviceToHost));   /* for the log only */
         CK(amp_adamw_master_step(Lp, Lm, Lv, Lg, Lb, scale, found, stepc, &hy, amax, NULL));
@@ -133,16 +138,21 @@ int main(int argc, char **argv) {
     fwrite(&s, 4, 1, out);
     fwrite(&t, 4, 1, out);
     fwrite(&st, 4, 1, out);
+    CK(amp_tensor_list_copy_to_host(Lp, hp, NULL));
+    CK(amp_tensor_list_copy_to_host(Lm, hm, NULL));
+    CK(amp_tensor_list_copy_to_host(Lv, hv, NULL));
+    CK(amp_tensor_list_copy_to_host(Lb, hb, NULL));
+    CU(cudaDeviceSynchronize());
     for (int i = 0; i < n; ++i) {
-        void *h = malloc(numel[i] * 4);
-        void *bufs[3] = {p[i], m[i], v[i]};
-        for (int q = 0; q < 3; ++q) {
-            CU(cudaMemcpy(h, bufs[q], numel[i] * 4, cudaMemcpyDeviceToHost));
-            fwrite(h, 4, numel[i], out);
-        }
-        CU(cudaMemcpy(h, b[i], numel[i] * 2, cudaMemcpyDeviceToHost));
-        fwrite(h, 2, numel[i], out);
-        free(h);
+        fwrite(hp[i], 4, numel[i], out);
+        fwrite(hm[i], 4, numel[i], out);
+        fwrite(hv[i], 4, numel[i], out);
+        fwrite(hb[i], 2, numel[i], out);
+        free(hp[i]);
+        free(hm[i]);
+        free(hv[i]);
+        free(hg[i]);
+        free(hb[i]);
     }
     float *hinv = malloc(4 * (n8 + 1));
     CU(cudaMemcpy(hinv, inv, 4 * (n8 + 1), cudaMemcpyDeviceToHost));

@@ -865,3 +865,28 @@ def test_lists_with_no_tensors(A, dev):
     A.amp_tensor_list_check(E[0])
     for L in E + [X8, Q8, QT]:
         L.close()
+
+
+def test_list_host_copies_round_trip(A, dev):
+    """amp_tensor_list_copy_from_host / _to_host move every tensor of a list
+    (empty ones included) byte for byte, from pageable and page-locked memory."""
+    rng = np.random.default_rng(42)
+    sizes = [0, 1, 7, 16385, 0, 100003]
+    for pinned in (False, True):
+        D = [torch.empty(n, dtype=torch.float16, device=dev) for n in sizes]
+        L = A.amp_tensor_list_create(D)
+        src = [torch.from_numpy(rng.integers(0, 1 << 16, n, dtype=np.uint16).view(np.int16).copy())
+               for n in sizes]
+        dst = [torch.full((n,), -1, dtype=torch.int16) for n in sizes]
+        if pinned:
+            src = [t.pin_memory() for t in src]
+            dst = [t.pin_memory() for t in dst]
+        A.amp_tensor_list_copy_from_host(L, [t if t.numel() else None for t in src])
+        torch.cuda.synchronize()
+        for d, s in zip(D, src):
+            assert torch.equal(d.cpu().view(torch.int16), s)
+        A.amp_tensor_list_copy_to_host(L, dst)
+        torch.cuda.synchronize()
+        for d, s in zip(dst, src):
+            assert torch.equal(d, s)
+        L.close()
