@@ -370,6 +370,25 @@ def test_quant_vs_torch_ops(fmt, tdt, shape):
     assert np.array_equal(qt.reshape(shape[1], shape[0]), ref.T)
 
 
+@pytest.mark.parametrize("fmt,tdt", [("e4m3fn", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)])
+def test_quant_amax_propagates_nan(fmt, tdt):
+    """[FP8] §2 takes amax = x.abs().max(), which propagates NaN: one NaN makes
+    the amax, the scale and so every output NaN, as torch's own ops give."""
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((9, 20)).astype(F32)
+    x[4, 13] = np.nan
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    bits = xb.view(torch.int16).numpy().view(np.uint16).ravel()
+    q, qt, inv, amax = O.fp8_quant_tensorwise(bits, "bf16", 9, 20, fmt)
+    mx = float(torch.finfo(tdt).max)
+    am = xb.float().abs().max()
+    sc = mx / am.double().clamp(min=1e-12)
+    ref = (xb.float() * sc).clamp(-mx, mx).to(tdt).float().numpy()
+    assert np.isnan(am.item()) and np.isnan(amax) and np.isnan(inv)
+    assert np.isnan(ref).all()
+    assert np.isnan(O.decode(fmt, q)).all() and np.isnan(O.decode(fmt, qt)).all()
+
+
 def test_quant_dequant_error_bound():
     """RNE error: |deq - x| <= half the fp8 spacing at |x*scale|, mapped back."""
     rng = np.random.default_rng(5)
@@ -581,6 +600,31 @@ def test_stochastic_rounding_is_unbiased_and_on_grid():
     # negative values mirror positive ones (rounding away from zero is "up")
     q = O.bf16_stochastic(-p[:1000], 1234, 1, 0)
     assert np.array_equal(q & 0x7FFF, b[:1000])
+
+
+def test_stochastic_rounding_probability_is_exact():
+    """Over all 2^16 values of the 16 random bits, the fraction that rounds
+    away from zero is exactly (|p| - |lo|) / (|hi| - |lo|), lo and hi the
+    neighbouring bf16 values, computed here in fp64 from their decoded values;
+    values on the bf16 grid never move."""
+    u = np.arange(1 << 16, dtype=np.uint32)
+    for pv in [1.0 + 1e-3, 1.25, -3.3e-5, 3.0e38, 1.0e-40, -7.77e5, 2.0 ** -133]:
+        p = np.float32(pv)
+        out = np.array([O.lib().orc_bf16_stochastic(float(p), int(k)) for k in u], np.uint16)
+        mag = abs(float(p))
+        # bf16 values next to |p|: decode every bf16 magnitude and bracket |p|
+        grid = O.decode("bf16", np.arange(0x7F80, dtype=np.uint16)).astype(np.float64)
+        j = np.searchsorted(grid, mag, side="right") - 1
+        lo = grid[j]
+        hi = grid[j + 1] if j + 1 < grid.size else np.inf
+        vals = np.abs(O.decode("bf16", out).astype(np.float64))
+        assert set(np.unique(vals)) <= {lo, hi}, pv
+        n_up = int(np.sum(vals == hi))
+        if mag == lo:
+            assert n_up == 0, pv
+        else:
+            assert n_up == (mag - lo) / (hi - lo) * 65536, pv
+        assert np.all(np.signbit(O.decode("bf16", out)) == np.signbit(p)), pv
 
 
 def test_adamw_with_stochastic_rounding_keeps_master_and_rounds_copy():
