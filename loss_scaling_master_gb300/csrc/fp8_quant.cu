@@ -175,8 +175,7 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const void *x, int64_t n
         constexpr int per = XT == kF32 ? 4 : 8;
         const int64_t nv = n / per;
         const char *b = static_cast<const char *>(x);
-        for (int64_t i = gtid; i < nv; i += gstride) {
-            const uint4 w = ld16(b + i * 16);
+        auto fold = [&](const uint4 &w) {
             if (XT == kF32) {
                 mx = max(mx, max(max(w.x & 0x7FFFFFFFu, w.y & 0x7FFFFFFFu),
                                  max(w.z & 0x7FFFFFFFu, w.w & 0x7FFFFFFFu)));
@@ -184,7 +183,17 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const void *x, int64_t n
                 mx = __vmaxu2(mx, __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
                                            __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu)));
             }
+        };
+        // four 16-byte loads in flight per thread, then the grid-stride tail
+        int64_t i = gtid;
+        for (; i + 3 * gstride < nv; i += 4 * gstride) {
+            uint4 w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) w[u] = ld16(b + (i + u * gstride) * 16);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) fold(w[u]);
         }
+        for (; i < nv; i += gstride) fold(ld16(b + i * 16));
         if (XT != kF32) mx = max(mx & 0xFFFFu, mx >> 16);
         for (int64_t k = nv * per + gtid; k < n; k += gstride) {
             mx = max(mx, XT == kF32 ? (static_cast<const uint32_t *>(x)[k] & 0x7FFFFFFFu)
@@ -202,8 +211,16 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const void *x, int64_t n
     if (XT == kF32) f = mx;
     else if (XT == kBF16) f = mx << 16;
     else f = __float_as_uint(f16_bits_to_f32(mx));
+    // one atomic per CTA: every CTA hits the same word, so per-warp atomics
+    // would queue up at one L2 slice
+    __shared__ uint32_t wmax[kThreads / 32];
     f = warp_max_u32(f);
-    if ((threadIdx.x & 31) == 0 && f != 0) atomicMax(amax_bits, f);
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = f;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        f = warp_max_u32(threadIdx.x < kThreads / 32 ? wmax[threadIdx.x] : 0u);
+        if (threadIdx.x == 0 && f != 0) atomicMax(amax_bits, f);
+    }
 }
 
 __global__ void quant_empty_kernel(float *amax, int amax_given, float *inv_scale, double eps,

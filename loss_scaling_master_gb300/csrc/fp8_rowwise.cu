@@ -33,17 +33,16 @@ __device__ __forceinline__ uint32_t abs_f32_bits(const void *x, int64_t k) {
     return XT == kBF16 ? (h << 16) : __float_as_uint(f16_bits_to_f32(h));
 }
 
+// |x| bit patterns (as abs_f32_bits) of 8 consecutive elements held in one
+// (16-bit types) or two (fp32) 16-byte words
 template <int XT>
-__device__ __forceinline__ void load8_abs(const void *x, int64_t e, uint32_t (&a)[8]) {
+__device__ __forceinline__ void raw_abs(const uint4 *u, uint32_t (&a)[8]) {
     if (XT == kF32) {
-        const char *p = static_cast<const char *>(x) + e * 4;
-        const uint4 u = ld16(p), v = ld16(p + 16);
-        const uint32_t w[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
+        const uint32_t w[8] = {u[0].x, u[0].y, u[0].z, u[0].w, u[1].x, u[1].y, u[1].z, u[1].w};
 #pragma unroll
         for (int j = 0; j < 8; ++j) a[j] = w[j] & 0x7FFFFFFFu;
     } else {
-        const uint4 u = ld16(static_cast<const char *>(x) + e * 2);
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        const uint32_t w[4] = {u[0].x, u[0].y, u[0].z, u[0].w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const uint32_t lo = w[j] & 0x7FFFu, hi = (w[j] >> 16) & 0x7FFFu;
@@ -58,17 +57,16 @@ __device__ __forceinline__ void load8_abs(const void *x, int64_t e, uint32_t (&a
     }
 }
 
+// 8 consecutive elements as fp32, from the one (16-bit types) or two (fp32)
+// 16-byte words that hold them
 template <int XT>
-__device__ __forceinline__ void load8_f32(const void *x, int64_t e, float (&y)[8]) {
+__device__ __forceinline__ void raw_to_f32(const uint4 *u, float (&y)[8]) {
     if (XT == kF32) {
-        const char *p = static_cast<const char *>(x) + e * 4;
-        const uint4 u = ld16(p), v = ld16(p + 16);
-        const uint32_t w[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
+        const uint32_t w[8] = {u[0].x, u[0].y, u[0].z, u[0].w, u[1].x, u[1].y, u[1].z, u[1].w};
 #pragma unroll
         for (int j = 0; j < 8; ++j) y[j] = __uint_as_float(w[j]);
     } else {
-        const uint4 u = ld16(static_cast<const char *>(x) + e * 2);
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        const uint32_t w[4] = {u[0].x, u[0].y, u[0].z, u[0].w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             y[2 * j] = lowp_to_f32<XT>(w[j] & 0xFFFFu);
@@ -106,9 +104,20 @@ __global__ void __launch_bounds__(kThreads) rowcol_amax_kernel(const void *x, in
     if (tile_fast(x, rows, cols, r0, c0)) {
         const int c8 = threadIdx.x & 15, rb = threadIdx.x >> 4;
         uint32_t cm[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        // all eight rows' loads in flight first: the row atomics below are
+        // memory operations the compiler would not move loads across
+        constexpr int nw = XT == kF32 ? 2 : 1;
+        uint4 raw[8][nw];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const char *p = static_cast<const char *>(x) +
+                            ((r0 + rb + 16 * k) * cols + c0 + 8 * c8) * (XT == kF32 ? 4 : 2);
+            raw[k][0] = ld16(p);
+            if (nw == 2) raw[k][nw - 1] = ld16(p + 16);
+        }
         uint32_t a[8][8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) load8_abs<XT>(x, (r0 + rb + 16 * k) * cols + c0 + 8 * c8, a[k]);
+        for (int k = 0; k < 8; ++k) raw_abs<XT>(raw[k], a[k]);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             uint32_t rm = 0;
@@ -187,13 +196,26 @@ __global__ void __launch_bounds__(kThreads) rowcol_cast_kernel(const void *x, in
         float sc[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) sc[j] = out_t ? scale_col[c0 + 8 * c8 + j] : 0.0f;
-#pragma unroll 2
+        // all eight rows' loads in flight before any store (x and out may
+        // alias as far as the compiler knows, so it would not hoist them)
+        constexpr int nw = XT == kF32 ? 2 : 1;
+        uint4 raw[8][nw];
+        float srow[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const char *p = static_cast<const char *>(x) +
+                            ((r0 + rb + 16 * k) * cols + c0 + 8 * c8) * (XT == kF32 ? 4 : 2);
+            raw[k][0] = ld16(p);
+            if (nw == 2) raw[k][nw - 1] = ld16(p + 16);
+            srow[k] = scale_row[r0 + rb + 16 * k];
+        }
+#pragma unroll
         for (int k = 0; k < 8; ++k) {
             const int r = rb + 16 * k;
             const int64_t e = (r0 + r) * cols + c0 + 8 * c8;
             float y[8];
-            load8_f32<XT>(x, e, y);
-            const float sr = scale_row[r0 + r];
+            raw_to_f32<XT>(raw[k], y);
+            const float sr = srow[k];
             uint32_t h[4], g[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
