@@ -24,6 +24,7 @@
 
 #include "fp8_tile.cuh"
 #include "internal.h"
+#include "pdl.cuh"
 
 namespace amp {
 namespace {
@@ -106,6 +107,8 @@ __global__ void __launch_bounds__(kThreads) quant_single_kernel(const void *x, i
                                                                 uint8_t *out_t, const float *amax,
                                                                 float *inv_scale, double eps,
                                                                 const int32_t *skip_if) {
+    pdl_wait();
+    pdl_trigger();
     if (skip_if && *skip_if) return;
     __shared__ __align__(16) uint32_t sm[kTile * 32];
     __shared__ float s_scale;
@@ -125,6 +128,8 @@ __global__ void __launch_bounds__(kThreads) quant_list_kernel(ListView X, ListVi
                                                               int has_t, const float *amax,
                                                               float *inv_scale, double eps,
                                                               const int32_t *skip_if) {
+    pdl_wait();
+    pdl_trigger();
     if (skip_if && *skip_if) return;
     __shared__ __align__(16) uint32_t sm[kTile * 32];
     __shared__ float s_scale;
@@ -149,6 +154,8 @@ __global__ void __launch_bounds__(kThreads) quant_list_kernel(ListView X, ListVi
 template <int FT>
 __global__ void quant_list_empty_kernel(ListView X, const float *amax, float *inv_scale,
                                         double eps, const int32_t *skip_if) {
+    pdl_wait();
+    pdl_trigger();
     if (skip_if && *skip_if) return;
     for (int t = threadIdx.x; t < X.n; t += blockDim.x) {
         if (X.numel[t] != 0) continue;
@@ -160,6 +167,8 @@ __global__ void quant_list_empty_kernel(ListView X, const float *amax, float *in
 
 // amax is an output: it starts from +0 (unless the call is skipped).
 __global__ void amax_zero_kernel(float *amax, const int32_t *skip_if) {
+    pdl_wait();
+    pdl_trigger();
     if (!(skip_if && *skip_if)) *amax = 0.0f;
 }
 
@@ -167,6 +176,8 @@ template <int XT>
 __global__ void __launch_bounds__(kThreads) amax_kernel(const void *x, int64_t n,
                                                         unsigned int *amax_bits,
                                                         const int32_t *skip_if) {
+    pdl_wait();
+    pdl_trigger();
     if (skip_if && *skip_if) return;
     const int64_t gtid = int64_t(blockIdx.x) * kThreads + threadIdx.x;
     const int64_t gstride = int64_t(gridDim.x) * kThreads;
@@ -225,6 +236,8 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const void *x, int64_t n
 
 __global__ void quant_empty_kernel(float *amax, int amax_given, float *inv_scale, double eps,
                                    float fmax, const int32_t *skip_if) {
+    pdl_wait();
+    pdl_trigger();
     if (skip_if && *skip_if) return;
     if (!amax_given) *amax = 0.0f;
     float s32, inv;
@@ -238,23 +251,20 @@ cudaError_t launch_single(const void *x, int64_t rows, int64_t cols, uint8_t *ou
                           const int32_t *skip_if, int device, cudaStream_t s) {
     const int64_t n = rows * cols;
     if (!amax_given) {
-        amax_zero_kernel<<<1, 1, 0, s>>>(amax, skip_if);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_pdl(amax_zero_kernel, dim3(1), dim3(1), 0, s, amax, skip_if);
         if (e != cudaSuccess) return e;
         const int64_t per = XT == kF32 ? 4 : 8;
         const int64_t want = (n / per + kThreads - 1) / kThreads;
         const int64_t cap = int64_t(sm_count(device)) * 8;
         const unsigned grid = (unsigned)std::max<int64_t>(1, std::min(want, cap));
-        amax_kernel<XT><<<grid, kThreads, 0, s>>>(x, n, reinterpret_cast<unsigned int *>(amax),
-                                                   skip_if);
-        e = cudaGetLastError();
+        e = launch_pdl(amax_kernel<XT>, dim3(grid), dim3(kThreads), 0, s, x, n,
+                       reinterpret_cast<unsigned int *>(amax), skip_if);
         if (e != cudaSuccess) return e;
     }
     const int64_t tiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
-    quant_single_kernel<XT, FT><<<unsigned(tiles), kThreads, 0, s>>>(x, rows, cols, out, out_t,
-                                                                      amax, inv_scale, eps,
-                                                                      skip_if);
-    return cudaGetLastError();
+    return launch_pdl(quant_single_kernel<XT, FT>, dim3(unsigned(tiles)), dim3(kThreads), 0, s, x,
+                      rows, cols, out, out_t, static_cast<const float *>(amax), inv_scale, eps,
+                      skip_if);
 }
 
 }  // namespace
@@ -264,10 +274,8 @@ cudaError_t launch_fp8_quant(const void *x, int xelem, int64_t rows, int64_t col
                              float *amax, int amax_given, const int32_t *skip_if, int device,
                              cudaStream_t s) {
     if (rows * cols == 0) {
-        quant_empty_kernel<<<1, 1, 0, s>>>(amax, amax_given, inv_scale, eps,
-                                           fp8 == kE4M3 ? fp8_max<kE4M3>() : fp8_max<kE5M2>(),
-                                           skip_if);
-        return cudaGetLastError();
+        return launch_pdl(quant_empty_kernel, dim3(1), dim3(1), 0, s, amax, amax_given, inv_scale,
+                          eps, fp8 == kE4M3 ? fp8_max<kE4M3>() : fp8_max<kE5M2>(), skip_if);
     }
 #define AMP_Q1(XT, FT) \
     launch_single<XT, FT>(x, rows, cols, out, out_t, inv_scale, amax, amax_given, eps, skip_if, \
@@ -288,8 +296,10 @@ cudaError_t launch_fp8_quant_list(const ListView &x, int64_t n_tiles, bool any_e
                                   double eps, const float *amax, float *inv_scale,
                                   const int32_t *skip_if, cudaStream_t s) {
     if (any_empty) {
-        if (fp8 == kE4M3) quant_list_empty_kernel<kE4M3><<<1, kThreads, 0, s>>>(x, amax, inv_scale, eps, skip_if);
-        else quant_list_empty_kernel<kE5M2><<<1, kThreads, 0, s>>>(x, amax, inv_scale, eps, skip_if);
+        if (fp8 == kE4M3) launch_pdl(quant_list_empty_kernel<kE4M3>, dim3(1), dim3(kThreads), 0, s,
+                                     x, amax, inv_scale, eps, skip_if);
+        else launch_pdl(quant_list_empty_kernel<kE5M2>, dim3(1), dim3(kThreads), 0, s, x, amax,
+                        inv_scale, eps, skip_if);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -297,8 +307,9 @@ cudaError_t launch_fp8_quant_list(const ListView &x, int64_t n_tiles, bool any_e
     const ListView ot = out_t ? *out_t : ListView{};
     const int has_t = out_t != nullptr;
     const dim3 grid((unsigned)n_tiles), block(kThreads);
-#define AMP_QL(XT, FT) \
-    quant_list_kernel<XT, FT><<<grid, block, 0, s>>>(x, out, ot, has_t, amax, inv_scale, eps, skip_if)
+#define AMP_QL(XT, FT)                                                                    \
+    launch_pdl(quant_list_kernel<XT, FT>, grid, block, 0, s, x, out, ot, has_t, amax, inv_scale, \
+               eps, skip_if)
     if (fp8 == kE4M3) {
         if (xelem == kBF16) AMP_QL(kBF16, kE4M3);
         else if (xelem == kF16) AMP_QL(kF16, kE4M3);

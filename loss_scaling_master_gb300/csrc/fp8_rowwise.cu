@@ -20,6 +20,7 @@
 
 #include "fp8_tile.cuh"
 #include "internal.h"
+#include "pdl.cuh"
 
 namespace amp {
 namespace {
@@ -82,6 +83,8 @@ __device__ __forceinline__ bool tile_fast(const void *x, int64_t rows, int64_t c
 
 __global__ void rowcol_zero_kernel(float *amax_row, int64_t rows, float *amax_col, int64_t cols,
                                    const int32_t *skip_if) {
+    pdl_wait();
+    pdl_trigger();
     if (skip_if && *skip_if) return;
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < rows + cols;
          i += int64_t(gridDim.x) * blockDim.x) {
@@ -95,6 +98,8 @@ __global__ void __launch_bounds__(kThreads) rowcol_amax_kernel(const void *x, in
                                                                int64_t cols, unsigned *amax_row,
                                                                unsigned *amax_col,
                                                                const int32_t *skip_if) {
+    pdl_wait();
+    pdl_trigger();
     if (skip_if && *skip_if) return;
     __shared__ uint32_t colmax[16][kTile];
     __shared__ uint32_t s_row[kTile], s_col[kTile];
@@ -164,6 +169,8 @@ __global__ void rowcol_scale_kernel(const float *amax_row, float *scale_row, flo
                                     int64_t rows, const float *amax_col, float *scale_col,
                                     float *inv_col, int64_t cols, double eps, float fmax,
                                     const int32_t *skip_if) {
+    pdl_wait();
+    pdl_trigger();
     if (skip_if && *skip_if) return;
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < rows + cols;
          i += int64_t(gridDim.x) * blockDim.x) {
@@ -183,6 +190,8 @@ __global__ void __launch_bounds__(kThreads) rowcol_cast_kernel(const void *x, in
                                                                const float *scale_row,
                                                                const float *scale_col,
                                                                const int32_t *skip_if) {
+    pdl_wait();
+    pdl_trigger();
     if (skip_if && *skip_if) return;
     __shared__ __align__(16) uint32_t sm[kTile * 32];
     const int64_t tiles_c = (cols + kTile - 1) / kTile;
@@ -254,22 +263,23 @@ cudaError_t launch_rowwise_t(const void *x, int64_t rows, int64_t cols, uint8_t 
     const unsigned small_grid =
         (unsigned)std::max<int64_t>(1, std::min<int64_t>((n_rc + 255) / 256, sm_count(device) * 4));
     float *acol = out_t ? amax_col : nullptr;
-    rowcol_zero_kernel<<<small_grid, 256, 0, s>>>(amax_row, rows, acol, out_t ? cols : 0, skip_if);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(rowcol_zero_kernel, dim3(small_grid), dim3(256), 0, s, amax_row,
+                               rows, acol, int64_t(out_t ? cols : 0), skip_if);
     if (e != cudaSuccess) return e;
     const int64_t tiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
     if (tiles == 0) return cudaSuccess;
-    rowcol_amax_kernel<XT><<<(unsigned)tiles, kThreads, 0, s>>>(
-        x, rows, cols, reinterpret_cast<unsigned *>(amax_row), reinterpret_cast<unsigned *>(acol),
-        skip_if);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    rowcol_scale_kernel<<<small_grid, 256, 0, s>>>(amax_row, scale_row, inv_row, rows, acol,
-                                                   scale_col, inv_col, out_t ? cols : 0, eps,
-                                                   fp8_max<FT>(), skip_if);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    rowcol_cast_kernel<XT, FT><<<(unsigned)tiles, kThreads, 0, s>>>(x, rows, cols, out, out_t,
-                                                                     scale_row, scale_col, skip_if);
-    return cudaGetLastError();
+    e = launch_pdl(rowcol_amax_kernel<XT>, dim3((unsigned)tiles), dim3(kThreads), 0, s, x, rows,
+                   cols, reinterpret_cast<unsigned *>(amax_row), reinterpret_cast<unsigned *>(acol),
+                   skip_if);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(rowcol_scale_kernel, dim3(small_grid), dim3(256), 0, s,
+                   static_cast<const float *>(amax_row), scale_row, inv_row, rows,
+                   static_cast<const float *>(acol), scale_col, inv_col,
+                   int64_t(out_t ? cols : 0), eps, fp8_max<FT>(), skip_if);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(rowcol_cast_kernel<XT, FT>, dim3((unsigned)tiles), dim3(kThreads), 0, s, x,
+                      rows, cols, out, out_t, static_cast<const float *>(scale_row),
+                      static_cast<const float *>(scale_col), skip_if);
 }
 
 }  // namespace

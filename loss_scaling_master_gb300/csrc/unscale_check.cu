@@ -11,6 +11,7 @@
 // two 16-bit gradients - and does one multiply per warp at the end.  Bytes
 // moved: 2 per 16-bit gradient.
 #include "internal.h"
+#include "pdl.cuh"
 
 namespace amp {
 namespace {
@@ -117,6 +118,8 @@ __device__ __forceinline__ void sq_add_vec(SqSum &q, const uint4 &w) {
 template <int ET, bool NORM>
 __global__ void __launch_bounds__(kThreads) check_kernel(ListView g, const float *scale,
                                                          int32_t *found_inf) {
+    pdl_wait();
+    pdl_trigger();
     using T = GradTraits<ET>;
     constexpr int esz = ET == kF32 ? 4 : 2;
     const uint2 ch = g.chunks[blockIdx.x];
@@ -190,6 +193,8 @@ __global__ void __launch_bounds__(kThreads) check_kernel(ListView g, const float
 template <int ET>
 __global__ void __launch_bounds__(kThreads) unscale_inplace_kernel(ListView g, const float *scale,
                                                                    int32_t *found_inf) {
+    pdl_wait();
+    pdl_trigger();
     const uint2 ch = g.chunks[blockIdx.x];
     const int64_t start = int64_t(ch.y) * kChunk;
     const int64_t n = min(int64_t(kChunk), g.numel[ch.x] - start);
@@ -217,6 +222,8 @@ __global__ void __launch_bounds__(kThreads) unscale_inplace_kernel(ListView g, c
 // strided subset, then a fixed shared-memory tree.
 __global__ void __launch_bounds__(1024) norm_reduce_kernel(const double *partials, int64_t n,
                                                            double *out) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ double sm[1024];
     double v = 0.0;
     for (int64_t i = threadIdx.x; i < n; i += 1024) v += partials[i];
@@ -235,13 +242,16 @@ cudaError_t launch_check_norm(const ListView &g, int64_t n_chunks, int elem, con
                               int32_t *found_inf, double *sumsq, cudaStream_t s) {
     if (n_chunks > 0) {
         const dim3 grid((unsigned)n_chunks), block(kThreads);
-        if (elem == kF32) check_kernel<kF32, true><<<grid, block, 0, s>>>(g, scale, found_inf);
-        else if (elem == kF16) check_kernel<kF16, true><<<grid, block, 0, s>>>(g, scale, found_inf);
-        else check_kernel<kBF16, true><<<grid, block, 0, s>>>(g, scale, found_inf);
+        if (elem == kF32) launch_pdl(check_kernel<kF32, true>, dim3(grid), dim3(block), 0, s, g,
+                                     scale, found_inf);
+        else if (elem == kF16) launch_pdl(check_kernel<kF16, true>, dim3(grid), dim3(block), 0, s,
+                                          g, scale, found_inf);
+        else launch_pdl(check_kernel<kBF16, true>, dim3(grid), dim3(block), 0, s, g, scale,
+                        found_inf);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    norm_reduce_kernel<<<1, 1024, 0, s>>>(g.partials, n_chunks, sumsq);
+    launch_pdl(norm_reduce_kernel, dim3(1), dim3(1024), 0, s, g.partials, n_chunks, sumsq);
     return cudaGetLastError();
 }
 
@@ -250,13 +260,19 @@ cudaError_t launch_unscale_check(const ListView &g, int64_t n_chunks, int elem, 
     if (n_chunks == 0) return cudaSuccess;
     const dim3 grid((unsigned)n_chunks), block(kThreads);
     if (inplace) {
-        if (elem == kF32) unscale_inplace_kernel<kF32><<<grid, block, 0, s>>>(g, scale, found_inf);
-        else if (elem == kF16) unscale_inplace_kernel<kF16><<<grid, block, 0, s>>>(g, scale, found_inf);
-        else unscale_inplace_kernel<kBF16><<<grid, block, 0, s>>>(g, scale, found_inf);
+        if (elem == kF32) launch_pdl(unscale_inplace_kernel<kF32>, dim3(grid), dim3(block), 0, s, g,
+                                     scale, found_inf);
+        else if (elem == kF16) launch_pdl(unscale_inplace_kernel<kF16>, dim3(grid), dim3(block), 0,
+                                          s, g, scale, found_inf);
+        else launch_pdl(unscale_inplace_kernel<kBF16>, dim3(grid), dim3(block), 0, s, g, scale,
+                        found_inf);
     } else {
-        if (elem == kF32) check_kernel<kF32, false><<<grid, block, 0, s>>>(g, scale, found_inf);
-        else if (elem == kF16) check_kernel<kF16, false><<<grid, block, 0, s>>>(g, scale, found_inf);
-        else check_kernel<kBF16, false><<<grid, block, 0, s>>>(g, scale, found_inf);
+        if (elem == kF32) launch_pdl(check_kernel<kF32, false>, dim3(grid), dim3(block), 0, s, g,
+                                     scale, found_inf);
+        else if (elem == kF16) launch_pdl(check_kernel<kF16, false>, dim3(grid), dim3(block), 0, s,
+                                          g, scale, found_inf);
+        else launch_pdl(check_kernel<kBF16, false>, dim3(grid), dim3(block), 0, s, g, scale,
+                        found_inf);
     }
     return cudaGetLastError();
 }

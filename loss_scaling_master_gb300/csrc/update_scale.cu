@@ -5,6 +5,7 @@
 // clears found_inf and the per-tensor amax slots for the next step, so the
 // host never reads the state back.
 #include "internal.h"
+#include "pdl.cuh"
 
 namespace amp {
 namespace {
@@ -12,6 +13,8 @@ namespace {
 __global__ void update_scale_kernel(float *scale, int32_t *tracker, int32_t *found_inf,
                                     float growth, float backoff, int32_t interval, float *amax,
                                     int n_amax) {
+    pdl_wait();
+    pdl_trigger();
     if (threadIdx.x == 0) {
         const int32_t fi = *found_inf;
         float s = *scale;
@@ -40,6 +43,8 @@ __global__ void update_scale_kernel(float *scale, int32_t *tracker, int32_t *fou
 __global__ void update_scale_hist_kernel(float *scale, int32_t *tracker, int32_t *found_inf,
                                          float growth, float backoff, int32_t interval,
                                          float *amax, float *hist, int n, int hist_len) {
+    pdl_wait();
+    pdl_trigger();
     const int32_t fi = *found_inf;
     __syncthreads();  // every thread has read the flag before thread 0 clears it
     if (threadIdx.x == 0) {
@@ -75,16 +80,16 @@ __global__ void update_scale_hist_kernel(float *scale, int32_t *tracker, int32_t
 cudaError_t launch_update_scale_hist(float *scale, int32_t *tracker, int32_t *found_inf,
                                      float growth, float backoff, int32_t interval, float *amax,
                                      float *hist, int n, int hist_len, cudaStream_t s) {
-    update_scale_hist_kernel<<<1, 256, 0, s>>>(scale, tracker, found_inf, growth, backoff,
-                                               interval, amax, hist, n, hist_len);
+    launch_pdl(update_scale_hist_kernel, dim3(1), dim3(256), 0, s, scale, tracker, found_inf,
+               growth, backoff, interval, amax, hist, n, hist_len);
     return cudaGetLastError();
 }
 
 cudaError_t launch_update_scale(float *scale, int32_t *tracker, int32_t *found_inf, float growth,
                                 float backoff, int32_t interval, float *amax, int n_amax,
                                 cudaStream_t s) {
-    update_scale_kernel<<<1, 256, 0, s>>>(scale, tracker, found_inf, growth, backoff, interval,
-                                          amax, n_amax);
+    launch_pdl(update_scale_kernel, dim3(1), dim3(256), 0, s, scale, tracker, found_inf, growth,
+               backoff, interval, amax, n_amax);
     return cudaGetLastError();
 }
 
