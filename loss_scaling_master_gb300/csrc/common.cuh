@@ -83,18 +83,49 @@ __device__ __forceinline__ uint16_t f32_to_f16(float x) {
 // Two fp32 -> packed fp8x2 (lo in bits 0..7), round-to-nearest-even with
 // saturation to the largest finite value (the same bytes as clamping to
 // +-fp8_max first), NaN -> canonical code.
+// Two fp32 -> two fp8 bytes (lo in bits 0-7, hi in bits 8-15), round to
+// nearest even with saturation to the largest finite value; NaN bytes are
+// whatever the conversion gives (see fp8x4_canonical_nan).
 template <int FT>
-__device__ __forceinline__ uint32_t f32x2_to_fp8x2(float lo, float hi) {
+__device__ __forceinline__ uint32_t f32x2_to_fp8x2_raw(float lo, float hi) {
     unsigned short r;
     if (FT == kE4M3)
         asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
     else
         asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    uint32_t v = r;
-    const uint32_t nan = FT == kE4M3 ? kE4M3NaN : kE5M2NaN;
-    if (lo != lo) v = (v & 0xFF00u) | nan;
-    if (hi != hi) v = (v & 0x00FFu) | (nan << 8);
-    return v;
+    return r;
+}
+
+// Every NaN byte of four fp8 bytes -> the positive canonical NaN (e4m3fn 0x7F,
+// e5m2 0x7E).  With saturation, finite and infinite inputs never convert to a
+// NaN pattern (the largest outputs are e4m3fn 0x7E and e5m2 0x7B), so the
+// NaN bytes are exactly those of NaN inputs.
+template <int FT>
+__device__ __forceinline__ uint32_t fp8x4_canonical_nan(uint32_t v) {
+    if (FT == kE4M3) {
+        const uint32_t m = __vcmpeq4(v | 0x80808080u, 0xFFFFFFFFu);  // bytes S.1111.111
+        return v & ~(m & 0x80808080u);
+    }
+    const uint32_t m = __vcmpgtu4(v & 0x7F7F7F7Fu, 0x7C7C7C7Cu);  // bytes S.11111.xx, xx != 0
+    return (v & ~m) | (kE5M2NaN * 0x01010101u & m);
+}
+
+template <int FT>
+__device__ __forceinline__ uint32_t f32x2_to_fp8x2(float lo, float hi) {
+    return fp8x4_canonical_nan<FT>(f32x2_to_fp8x2_raw<FT>(lo, hi));
+}
+
+// (a0 * b0, a1 * b1), each lane an IEEE fp32 multiply rounded to nearest even,
+// as one packed instruction.
+__device__ __forceinline__ void mul2_rn(float a0, float a1, float b0, float b1, float &o0,
+                                        float &o1) {
+    asm("{\n\t.reg .b64 pa, pb, pc;\n\t"
+        "mov.b64 pa, {%2, %3};\n\t"
+        "mov.b64 pb, {%4, %5};\n\t"
+        "mul.rn.f32x2 pc, pa, pb;\n\t"
+        "mov.b64 {%0, %1}, pc;\n\t}"
+        : "=f"(o0), "=f"(o1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
 template <int FT>

@@ -76,10 +76,12 @@ __device__ __forceinline__ void quant_tile(const void *x, int64_t rows, int64_t 
                 }
             }
 #pragma unroll
-            for (int j = 0; j < 8; ++j) y[j] = __fmul_rn(y[j], s32);
+            for (int j = 0; j < 8; j += 2) mul2_rn(y[j], y[j + 1], s32, s32, y[j], y[j + 1]);
             uint2 q;
-            q.x = f32x2_to_fp8x2<FT>(y[0], y[1]) | (f32x2_to_fp8x2<FT>(y[2], y[3]) << 16);
-            q.y = f32x2_to_fp8x2<FT>(y[4], y[5]) | (f32x2_to_fp8x2<FT>(y[6], y[7]) << 16);
+            q.x = fp8x4_canonical_nan<FT>(f32x2_to_fp8x2_raw<FT>(y[0], y[1]) |
+                                          (f32x2_to_fp8x2_raw<FT>(y[2], y[3]) << 16));
+            q.y = fp8x4_canonical_nan<FT>(f32x2_to_fp8x2_raw<FT>(y[4], y[5]) |
+                                          (f32x2_to_fp8x2_raw<FT>(y[6], y[7]) << 16));
             const int r = rb + 16 * k;
             *reinterpret_cast<uint2 *>(out + (r0 + r) * cols + c0 + 8 * c8) = q;
             if (out_t) *reinterpret_cast<uint2 *>(sm + swz(r, 2 * c8)) = q;

@@ -228,14 +228,19 @@ __global__ void __launch_bounds__(kThreads) rowcol_cast_kernel(const void *x, in
             uint32_t h[4], g[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                h[j] = f32x2_to_fp8x2<FT>(__fmul_rn(y[2 * j], sr), __fmul_rn(y[2 * j + 1], sr));
-                g[j] = f32x2_to_fp8x2<FT>(__fmul_rn(y[2 * j], sc[2 * j]),
-                                          __fmul_rn(y[2 * j + 1], sc[2 * j + 1]));
+                float a0, a1, b0, b1;
+                mul2_rn(y[2 * j], y[2 * j + 1], sr, sr, a0, a1);
+                mul2_rn(y[2 * j], y[2 * j + 1], sc[2 * j], sc[2 * j + 1], b0, b1);
+                h[j] = f32x2_to_fp8x2_raw<FT>(a0, a1);
+                g[j] = f32x2_to_fp8x2_raw<FT>(b0, b1);
             }
-            *reinterpret_cast<uint2 *>(out + e) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+            *reinterpret_cast<uint2 *>(out + e) =
+                make_uint2(fp8x4_canonical_nan<FT>(h[0] | (h[1] << 16)),
+                           fp8x4_canonical_nan<FT>(h[2] | (h[3] << 16)));
             if (out_t)
                 *reinterpret_cast<uint2 *>(sm + swz(r, 2 * c8)) =
-                    make_uint2(g[0] | (g[1] << 16), g[2] | (g[3] << 16));
+                    make_uint2(fp8x4_canonical_nan<FT>(g[0] | (g[1] << 16)),
+                               fp8x4_canonical_nan<FT>(g[2] | (g[3] << 16)));
         }
         if (out_t) {
             __syncthreads();

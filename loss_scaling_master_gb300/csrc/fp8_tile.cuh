@@ -30,11 +30,12 @@ __device__ __forceinline__ uint2 bf16x8_to_fp8x8(const uint4 &b, float s32) {
     uint32_t h[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const float lo = __fmul_rn(bf16_bits_to_f32(w[j] & 0xFFFFu), s32);
-        const float hi = __fmul_rn(bf16_bits_to_f32(w[j] >> 16), s32);
-        h[j] = f32x2_to_fp8x2<FT>(lo, hi);
+        float lo, hi;
+        mul2_rn(bf16_bits_to_f32(w[j] & 0xFFFFu), bf16_bits_to_f32(w[j] >> 16), s32, s32, lo, hi);
+        h[j] = f32x2_to_fp8x2_raw<FT>(lo, hi);
     }
-    return make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+    return make_uint2(fp8x4_canonical_nan<FT>(h[0] | (h[1] << 16)),
+                      fp8x4_canonical_nan<FT>(h[2] | (h[3] << 16)));
 }
 
 // 4-byte word (row r, word w) of a 128x128 byte tile in shared memory,
