@@ -17,6 +17,7 @@
 //          transposed bytes) and writes both (1 + 1 B/elt), the transposed
 //          tile through the swizzled shared-memory transpose.
 #include <algorithm>
+#include <atomic>
 
 #include "fp8_tile.cuh"
 #include "internal.h"
@@ -93,6 +94,15 @@ __global__ void rowcol_zero_kernel(float *amax_row, int64_t rows, float *amax_co
     }
 }
 
+// Row and column maxima of |x|.  The grid is a fixed number of CTAs; CTA b
+// walks the tiles [b T / G, (b+1) T / G) of the column-major tile order, so it
+// moves down one or two 128-column strips.  Per tile, each thread holds 8 rows
+// x 8 columns: row maxima are combined across the 16 lanes sharing a row and
+// sent with one atomicMax per row; column maxima stay in registers for the
+// whole strip and are combined through shared memory once, when the CTA leaves
+// the strip.  The next tile's loads are issued before the current tile is
+// reduced.  Tiles on a ragged edge, or with sizes/addresses that break 16-byte
+// access, take an element path through shared memory.
 template <int XT>
 __global__ void __launch_bounds__(kThreads) rowcol_amax_kernel(const void *x, int64_t rows,
                                                                int64_t cols, unsigned *amax_row,
@@ -101,68 +111,108 @@ __global__ void __launch_bounds__(kThreads) rowcol_amax_kernel(const void *x, in
     pdl_wait();
     pdl_trigger();
     if (skip_if && *skip_if) return;
-    __shared__ uint32_t colmax[16][kTile];
+    __shared__ __align__(16) uint32_t colmax[kThreads / 32][kTile];
     __shared__ uint32_t s_row[kTile], s_col[kTile];
-    const int64_t tiles_c = (cols + kTile - 1) / kTile;
-    const int64_t r0 = int64_t(blockIdx.x / tiles_c) * kTile;
-    const int64_t c0 = int64_t(blockIdx.x % tiles_c) * kTile;
-    if (tile_fast(x, rows, cols, r0, c0)) {
-        const int c8 = threadIdx.x & 15, rb = threadIdx.x >> 4;
-        uint32_t cm[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        // all eight rows' loads in flight first: the row atomics below are
-        // memory operations the compiler would not move loads across
-        constexpr int nw = XT == kF32 ? 2 : 1;
-        uint4 raw[8][nw];
+    constexpr int nw = XT == kF32 ? 2 : 1;
+    constexpr int esz = XT == kF32 ? 4 : 2;
+    const int64_t tiles_r = (rows + kTile - 1) / kTile, tiles_c = (cols + kTile - 1) / kTile;
+    const int64_t tiles = tiles_r * tiles_c;
+    const int64_t t0 = int64_t(blockIdx.x) * tiles / gridDim.x;
+    const int64_t t1 = int64_t(blockIdx.x + 1) * tiles / gridDim.x;
+    const int c8 = threadIdx.x & 15, rb = threadIdx.x >> 4;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t cm[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    uint4 raw[8][nw];
+    auto load = [&](int64_t r0, int64_t c0) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            const char *p = static_cast<const char *>(x) +
-                            ((r0 + rb + 16 * k) * cols + c0 + 8 * c8) * (XT == kF32 ? 4 : 2);
+            const char *p = static_cast<const char *>(x) + ((r0 + rb + 16 * k) * cols + c0 + 8 * c8) * esz;
             raw[k][0] = ld16(p);
             if (nw == 2) raw[k][nw - 1] = ld16(p + 16);
         }
-        uint32_t a[8][8];
+    };
+    // column maxima gathered in registers for strip tc -> one atomicMax per column
+    auto flush = [&](int64_t tc) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) raw_abs<XT>(raw[k], a[k]);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            uint32_t rm = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                rm = max(rm, a[k][j]);
-                cm[j] = max(cm[j], a[k][j]);
-            }
-            // the 16 lanes holding this row: lanes 0-15 or 16-31 of the warp
-#pragma unroll
-            for (int off = 8; off > 0; off >>= 1) rm = max(rm, __shfl_xor_sync(0xFFFFFFFFu, rm, off));
-            if (c8 == 0 && rm != 0) atomicMax(amax_row + r0 + rb + 16 * k, rm);
+        for (int j = 0; j < 8; ++j) cm[j] = max(cm[j], __shfl_xor_sync(0xFFFFFFFFu, cm[j], 16));
+        if (lane < 16) {
+            uint4 *d = reinterpret_cast<uint4 *>(&colmax[warp][8 * c8]);
+            d[0] = make_uint4(cm[0], cm[1], cm[2], cm[3]);
+            d[1] = make_uint4(cm[4], cm[5], cm[6], cm[7]);
         }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) colmax[rb][8 * c8 + j] = cm[j];
         __syncthreads();
         if (threadIdx.x < kTile) {
             uint32_t m = 0;
 #pragma unroll
-            for (int r = 0; r < 16; ++r) m = max(m, colmax[r][threadIdx.x]);
-            if (amax_col && m != 0) atomicMax(amax_col + c0 + threadIdx.x, m);
+            for (int w = 0; w < kThreads / 32; ++w) m = max(m, colmax[w][threadIdx.x]);
+            const int64_t c = tc * kTile + threadIdx.x;
+            if (amax_col && c < cols && m != 0) atomicMax(amax_col + c, m);
         }
-    } else {
-        if (threadIdx.x < kTile) s_row[threadIdx.x] = s_col[threadIdx.x] = 0u;
         __syncthreads();
-        for (int idx = threadIdx.x; idx < kTile * kTile; idx += kThreads) {
-            const int64_t i = r0 + (idx >> 7), j = c0 + (idx & (kTile - 1));
-            if (i < rows && j < cols) {
-                const uint32_t v = abs_f32_bits<XT>(x, i * cols + j);
-                atomicMax(&s_row[idx >> 7], v);
-                atomicMax(&s_col[idx & (kTile - 1)], v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) cm[j] = 0;
+    };
+    auto coords = [&](int64_t t, int64_t &r0, int64_t &c0) {
+        r0 = (t % tiles_r) * kTile;
+        c0 = (t / tiles_r) * kTile;
+    };
+    int64_t strip = -1;
+    if (t0 < t1) {
+        int64_t r0, c0;
+        coords(t0, r0, c0);
+        if (tile_fast(x, rows, cols, r0, c0)) load(r0, c0);
+    }
+    for (int64_t t = t0; t < t1; ++t) {
+        int64_t r0, c0, nr0 = 0, nc0 = 0;
+        coords(t, r0, c0);
+        const bool has_next = t + 1 < t1;
+        if (has_next) coords(t + 1, nr0, nc0);
+        const int64_t tc = c0 / kTile;
+        if (tc != strip) {
+            if (strip >= 0) flush(strip);
+            strip = tc;
+        }
+        if (tile_fast(x, rows, cols, r0, c0)) {
+            uint32_t a[8][8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) raw_abs<XT>(raw[k], a[k]);
+            if (has_next && tile_fast(x, rows, cols, nr0, nc0)) load(nr0, nc0);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                uint32_t rm = 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    rm = max(rm, a[k][j]);
+                    cm[j] = max(cm[j], a[k][j]);
+                }
+                // the 16 lanes holding this row: lanes 0-15 or 16-31 of the warp
+#pragma unroll
+                for (int off = 8; off > 0; off >>= 1)
+                    rm = max(rm, __shfl_xor_sync(0xFFFFFFFFu, rm, off));
+                if (c8 == 0 && rm != 0) atomicMax(amax_row + r0 + rb + 16 * k, rm);
             }
-        }
-        __syncthreads();
-        if (threadIdx.x < kTile) {
-            const int t = threadIdx.x;
-            if (r0 + t < rows && s_row[t] != 0) atomicMax(amax_row + r0 + t, s_row[t]);
-            if (amax_col && c0 + t < cols && s_col[t] != 0) atomicMax(amax_col + c0 + t, s_col[t]);
+        } else {
+            if (threadIdx.x < kTile) s_row[threadIdx.x] = s_col[threadIdx.x] = 0u;
+            __syncthreads();
+            for (int idx = threadIdx.x; idx < kTile * kTile; idx += kThreads) {
+                const int64_t i = r0 + (idx >> 7), j = c0 + (idx & (kTile - 1));
+                if (i < rows && j < cols) {
+                    const uint32_t v = abs_f32_bits<XT>(x, i * cols + j);
+                    atomicMax(&s_row[idx >> 7], v);
+                    atomicMax(&s_col[idx & (kTile - 1)], v);
+                }
+            }
+            __syncthreads();
+            if (threadIdx.x < kTile) {
+                const int u = threadIdx.x;
+                if (r0 + u < rows && s_row[u] != 0) atomicMax(amax_row + r0 + u, s_row[u]);
+                if (amax_col && c0 + u < cols && s_col[u] != 0) atomicMax(amax_col + c0 + u, s_col[u]);
+            }
+            __syncthreads();
+            if (has_next && tile_fast(x, rows, cols, nr0, nc0)) load(nr0, nc0);
         }
     }
+    if (strip >= 0) flush(strip);
 }
 
 __global__ void rowcol_scale_kernel(const float *amax_row, float *scale_row, float *inv_row,
@@ -273,7 +323,18 @@ cudaError_t launch_rowwise_t(const void *x, int64_t rows, int64_t cols, uint8_t 
     if (e != cudaSuccess) return e;
     const int64_t tiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
     if (tiles == 0) return cudaSuccess;
-    e = launch_pdl(rowcol_amax_kernel<XT>, dim3((unsigned)tiles), dim3(kThreads), 0, s, x, rows,
+    // as many CTAs as fit on the GPU at once (each walks a run of tiles)
+    static std::atomic<int> per_sm{0};
+    if (per_sm.load(std::memory_order_relaxed) == 0) {
+        int k = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&k, rowcol_amax_kernel<XT>, kThreads, 0) !=
+                cudaSuccess || k < 1)
+            k = 1;
+        per_sm.store(k, std::memory_order_relaxed);
+    }
+    const unsigned amax_grid = (unsigned)std::min<int64_t>(
+        tiles, int64_t(sm_count(device)) * per_sm.load(std::memory_order_relaxed));
+    e = launch_pdl(rowcol_amax_kernel<XT>, dim3(amax_grid), dim3(kThreads), 0, s, x, rows,
                    cols, reinterpret_cast<unsigned *>(amax_row), reinterpret_cast<unsigned *>(acol),
                    skip_if);
     if (e != cudaSuccess) return e;
