@@ -368,8 +368,7 @@ def run_e2e(args, step, info, stream, world):
     hbuf = pinned_empty(bufs[0].numel(), bufs[0].dtype)
     host = hbuf.tensor
     host.copy_(bufs[0])      # finite gradients of the workload's recipe
-    state_host = torch.empty(4, dtype=torch.int32, pin_memory=True)
-    packed = torch.empty(4, dtype=torch.int32, device=step.scale.device)
+    state_host = torch.empty(4, dtype=torch.int32, pin_memory=True)   # an amp_scaler_state
     copy_stream = torch.cuda.Stream(device=step.scale.device)
     ready = [torch.cuda.Event(), torch.cuda.Event()]
     free = [torch.cuda.Event(), torch.cuda.Event()]
@@ -399,12 +398,8 @@ def run_e2e(args, step, info, stream, world):
         stream.wait_event(ready[b])
         step.step(stream=stream, grad_buffer=(0 if b == 0 else b1))
         free[b].record(stream)
-        with torch.cuda.stream(stream):
-            packed[0:1].copy_(step.scale.view(torch.int32))
-            packed[1:2].copy_(step.growth_tracker)
-            packed[2:3].copy_(step.step_count)
-            packed[3:4].copy_(step.found_inf)
-            state_host.copy_(packed, non_blocking=True)
+        A.amp_read_state(step.scale, step.growth_tracker, step.step_count, step.found_inf,
+                         state_host.data_ptr(), stream=stream)
 
     for k in range(max(2, args.warmup // 2)):
         e2e_step(k)
@@ -431,7 +426,7 @@ def run_e2e(args, step, info, stream, world):
             "h2d_gbs_best": nbytes / copy_ms[0] / 1e6,
             "api": "amp_tensor_list_copy_from_host (one H2D copy per tensor from pinned huge-page "
                    "host memory, on a copy stream, double-buffered) + AmpOptimizerStep.step() "
-                   "(C-ABI calls) + D2H of {scale, tracker, step, found_inf}",
+                   "(C-ABI calls) + amp_read_state (D2H of {scale, tracker, step, found_inf})",
             "host_huge_pages": hbuf.huge_pages}
 
 

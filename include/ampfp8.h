@@ -414,6 +414,39 @@ amp_status amp_update_scale_fp8_history(float *scale_dev, int32_t *growth_tracke
                                         float *amax_dev, float *amax_history, int n_fp8,
                                         int hist_len, amp_stream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* Monitoring.  The pages watch the loss scale (scaler.get_scale()) and fall  */
+/* back to bf16 when it keeps halving ([CH20] §20.2.2 and "06 · 混合精度"      */
+/* §四); these two calls serve that outside the step, and have no other       */
+/* counterpart on the pages.                                                  */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    float scale;
+    int32_t growth_tracker;
+    int32_t step;
+    int32_t found_inf;
+} amp_scaler_state;
+
+/* Enqueue on `stream` a device-to-host copy of the scaler and step state into
+ * *host_out (one 4-byte cudaMemcpyAsync per non-NULL pointer; the fields of
+ * NULL pointers are left alone).  host_out should be page-locked for the
+ * copies to be asynchronous; read it after synchronising `stream`.
+ * Errors: AMP_EINVAL (host_out NULL), AMP_ECUDA. */
+amp_status amp_read_state(const float *scale_dev, const int32_t *growth_tracker_dev,
+                          const int32_t *step_dev, const int32_t *found_inf_dev,
+                          amp_scaler_state *host_out, amp_stream_t stream);
+
+/* Sticky health word of the loss scale, one thread on `stream`:
+ *   *health_dev |= 1 if *scale_dev is not finite,
+ *   *health_dev |= 2 if it is finite and below min_scale (it kept halving).
+ * Bits are only ever set; the caller clears the word.  health_dev may point to
+ * device memory or to page-locked host memory the device can address (memory
+ * from cudaHostAlloc, or registered), so the host can poll it without
+ * synchronising.  Errors: AMP_EINVAL (NULL pointer, min_scale < 0 or NaN). */
+amp_status amp_scale_health(const float *scale_dev, float min_scale, int32_t *health_dev,
+                            amp_stream_t stream);
+
 /* Message describing the last non-OK status returned on this thread. */
 const char *amp_last_error(void);
 

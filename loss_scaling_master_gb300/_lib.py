@@ -28,6 +28,7 @@ _TORCH_DT = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16",
 EXPORTS = ("amp_tensor_list_create", "amp_tensor_list_set_amax_slots", "amp_tensor_list_destroy",
            "amp_tensor_list_check", "amp_selftest_bounded_wait",
            "amp_tensor_list_copy_from_host", "amp_tensor_list_copy_to_host",
+           "amp_read_state", "amp_scale_health",
            "amp_unscale_check", "amp_unscale_check_norm", "amp_adamw_master_step",
            "amp_adamw_master_step_clip", "amp_adamw_master_step_sr",
            "amp_adamw_master_step_noalloc", "amp_noalloc_check",
@@ -71,6 +72,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.amp_tensor_list_check.argtypes = [P, P]
         L.amp_tensor_list_copy_from_host.argtypes = [P, P, P]
         L.amp_tensor_list_copy_to_host.argtypes = [P, P, P]
+        L.amp_read_state.argtypes = [P, P, P, P, P, P]
+        L.amp_scale_health.argtypes = [P, flt, P, P]
         L.amp_noalloc_check.argtypes = [P]
         L.amp_selftest_bounded_wait.argtypes = [P, dbl, P]
         L.amp_adamw_master_step.argtypes = [P, P, P, P, P, P, P, P,
@@ -216,6 +219,27 @@ def amp_tensor_list_copy_to_host(lst: TensorList, host, stream=None):
     _check("amp_tensor_list_copy_to_host",
            load().amp_tensor_list_copy_to_host(lst.handle, _host_ptrs(host, len(lst)),
                                                _stream(stream)))
+
+
+class ScalerState(ctypes.Structure):
+    """amp_scaler_state: the scaler and step state read back by amp_read_state."""
+    _fields_ = [("scale", ctypes.c_float), ("growth_tracker", ctypes.c_int32),
+                ("step", ctypes.c_int32), ("found_inf", ctypes.c_int32)]
+
+
+def amp_read_state(scale, growth_tracker, step, found_inf, host_out, stream=None):
+    """Enqueue the D2H copy of {scale, tracker, step, found_inf} into host_out:
+    a ScalerState, or the address of one (page-locked for asynchrony)."""
+    out = host_out if isinstance(host_out, int) else ctypes.addressof(host_out)
+    _check("amp_read_state",
+           load().amp_read_state(_dptr(scale), _dptr(growth_tracker), _dptr(step),
+                                 _dptr(found_inf), out, _stream(stream)))
+
+
+def amp_scale_health(scale, min_scale: float, health, stream=None):
+    """Sticky health bits of the loss scale into health (device or page-locked host int32)."""
+    _check("amp_scale_health",
+           load().amp_scale_health(_dptr(scale), float(min_scale), _dptr(health), _stream(stream)))
 
 
 def amp_noalloc_check(stream=None):

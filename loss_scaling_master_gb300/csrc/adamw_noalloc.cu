@@ -88,6 +88,7 @@ extern "C" amp_status amp_adamw_master_step_noalloc(
     const int64_t *numel, const int32_t *amax_slots, const float *scale_dev,
     const int32_t *found_inf_dev, int32_t *step_dev, const amp_adamw_hyper *hyper,
     float *amax_dev, amp_stream_t stream) {
+    AMP_TRACE("amp_adamw_master_step_noalloc");
     const char *fn = "amp_adamw_master_step_noalloc";
     if (n < 0 || (n > 0 && (!master || !exp_avg || !exp_avg_sq || !grads || !numel)) ||
         !step_dev || !hyper)
@@ -185,6 +186,7 @@ extern "C" amp_status amp_adamw_master_step_noalloc(
 }
 
 extern "C" amp_status amp_noalloc_check(amp_stream_t stream) {
+    AMP_TRACE("amp_noalloc_check");
     const char *fn = "amp_noalloc_check";
     unsigned char *base = nullptr;
     cudaError_t e = scratch_on_current_device(&base);

@@ -80,7 +80,7 @@ extern "C" {
 
 const char *amp_last_error(void) { return g_err; }
 
-int amp_abi_version(void) { return 7; }
+int amp_abi_version(void) { return 8; }
 
 // A [rows, cols] shape the launch arithmetic can hold: non-negative, each side
 // below 2^48 and rows * cols without int64 overflow.
@@ -92,6 +92,7 @@ static bool bad_shape(int64_t rows, int64_t cols) {
 amp_status amp_tensor_list_create(int n, void *const *dev_ptrs, const int64_t *rows,
                                   const int64_t *cols, amp_dtype dtype, amp_stream_t stream,
                                   amp_tensor_list *out) {
+    AMP_TRACE("amp_tensor_list_create");
     if (!out) return fail(AMP_EINVAL, "amp_tensor_list_create: out is NULL");
     if (n < 0) return fail(AMP_EINVAL, "amp_tensor_list_create: n < 0");
     if (n > 0 && (!dev_ptrs || !rows))
@@ -199,6 +200,7 @@ amp_status amp_tensor_list_create(int n, void *const *dev_ptrs, const int64_t *r
 
 amp_status amp_tensor_list_set_amax_slots(amp_tensor_list list, const int32_t *slots,
                                           amp_stream_t stream) {
+    AMP_TRACE("amp_tensor_list_set_amax_slots");
     if (!list || (list->n > 0 && !slots))
         return fail(AMP_EINVAL, "amp_tensor_list_set_amax_slots: NULL argument");
     if (list->n == 0) return AMP_OK;
@@ -215,6 +217,7 @@ amp_status amp_tensor_list_set_amax_slots(amp_tensor_list list, const int32_t *s
 }
 
 amp_status amp_tensor_list_destroy(amp_tensor_list list) {
+    AMP_TRACE("amp_tensor_list_destroy");
     if (!list) return AMP_OK;
     cudaError_t e = list->block ? cudaFree(list->block) : cudaSuccess;
     delete list;
@@ -244,15 +247,18 @@ static amp_status list_copy_host(amp_tensor_list list, void *const *host_ptrs, b
 
 amp_status amp_tensor_list_copy_from_host(amp_tensor_list list, const void *const *host_ptrs,
                                           amp_stream_t stream) {
+    AMP_TRACE("amp_tensor_list_copy_from_host");
     return list_copy_host(list, const_cast<void *const *>(host_ptrs), false, stream);
 }
 
 amp_status amp_tensor_list_copy_to_host(amp_tensor_list list, void *const *host_ptrs,
                                         amp_stream_t stream) {
+    AMP_TRACE("amp_tensor_list_copy_to_host");
     return list_copy_host(list, host_ptrs, true, stream);
 }
 
 amp_status amp_tensor_list_check(amp_tensor_list list, amp_stream_t stream) {
+    AMP_TRACE("amp_tensor_list_check");
     if (!list) return fail(AMP_EINVAL, "amp_tensor_list_check: NULL list");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int32_t *word = reinterpret_cast<int32_t *>(list->scratch) + amp::kErrWordOffset;
@@ -272,6 +278,7 @@ amp_status amp_tensor_list_check(amp_tensor_list list, amp_stream_t stream) {
 }
 
 amp_status amp_selftest_bounded_wait(int32_t *err_dev, double limit_seconds, amp_stream_t stream) {
+    AMP_TRACE("amp_selftest_bounded_wait");
     if (!err_dev || !(limit_seconds > 0.0) || limit_seconds > 10.0)
         return fail(AMP_EINVAL, "amp_selftest_bounded_wait: err_dev NULL or limit not in (0, 10] s");
     cudaError_t e = amp::launch_bounded_wait_selftest(err_dev, limit_seconds,
@@ -281,6 +288,7 @@ amp_status amp_selftest_bounded_wait(int32_t *err_dev, double limit_seconds, amp
 
 amp_status amp_unscale_check(amp_tensor_list grads, const float *scale_dev, int32_t *found_inf_dev,
                              int inplace, amp_stream_t stream) {
+    AMP_TRACE("amp_unscale_check");
     if (!grads || !found_inf_dev) return fail(AMP_EINVAL, "amp_unscale_check: NULL argument");
     const int ec = elem_code(grads->dtype);
     if (ec < 0) return fail(AMP_EDTYPE, "amp_unscale_check: gradients must be f32/f16/bf16");
@@ -337,6 +345,7 @@ amp_status amp_adamw_master_step_sr(amp_tensor_list master, amp_tensor_list exp_
                                     const int32_t *found_inf_dev, int32_t *step_dev,
                                     const amp_adamw_hyper *hyper, float *amax_dev, uint64_t seed,
                                     amp_stream_t stream) {
+    AMP_TRACE("amp_adamw_master_step_sr");
     if (!bf16_out) return fail(AMP_EINVAL, "amp_adamw_master_step_sr: bf16_out is NULL");
     return adamw_entry(master, exp_avg, exp_avg_sq, grads, bf16_out, scale_dev, found_inf_dev,
                        step_dev, hyper, amax_dev, nullptr, 0.0, stream, true, seed);
@@ -348,6 +357,7 @@ amp_status amp_adamw_master_step(amp_tensor_list master, amp_tensor_list exp_avg
                                  const int32_t *found_inf_dev, int32_t *step_dev,
                                  const amp_adamw_hyper *hyper, float *amax_dev,
                                  amp_stream_t stream) {
+    AMP_TRACE("amp_adamw_master_step");
     return adamw_entry(master, exp_avg, exp_avg_sq, grads, bf16_out, scale_dev, found_inf_dev,
                        step_dev, hyper, amax_dev, nullptr, 0.0, stream);
 }
@@ -359,6 +369,7 @@ amp_status amp_adamw_master_step_clip(amp_tensor_list master, amp_tensor_list ex
                                       const amp_adamw_hyper *hyper, float *amax_dev,
                                       const double *grad_sumsq_dev, double max_norm,
                                       amp_stream_t stream) {
+    AMP_TRACE("amp_adamw_master_step_clip");
     if (!grad_sumsq_dev) return fail(AMP_EINVAL, "amp_adamw_master_step_clip: grad_sumsq_dev is NULL");
     if (!(max_norm > 0.0) || max_norm > 1e300)
         return fail(AMP_EINVAL, "amp_adamw_master_step_clip: max_norm must be finite and > 0");
@@ -374,6 +385,7 @@ amp_status amp_adamw_master_step_fp8_delayed(
     amp_dtype fp8_dtype, double eps, const float *amax_history, int hist_len, float *amax_dev,
     float *inv_scale_dev, const float *scale_dev, const int32_t *found_inf_dev, int32_t *step_dev,
     const amp_adamw_hyper *hyper, amp_stream_t stream) {
+    AMP_TRACE("amp_adamw_master_step_fp8_delayed");
     const char *fn = "amp_adamw_master_step_fp8_delayed";
     if (!master || !exp_avg || !exp_avg_sq || !grads || !bf16_out || !master8 || !exp_avg8 ||
         !exp_avg_sq8 || !grads8 || !bf16_out8 || !fp8_out || !amax_history || !amax_dev ||
@@ -439,6 +451,7 @@ amp_status amp_update_scale_fp8_history(float *scale_dev, int32_t *growth_tracke
                                         float backoff_factor, int32_t growth_interval,
                                         float *amax_dev, float *amax_history, int n_fp8,
                                         int hist_len, amp_stream_t stream) {
+    AMP_TRACE("amp_update_scale_fp8_history");
     const char *fn = "amp_update_scale_fp8_history";
     if (!scale_dev || !growth_tracker_dev || !found_inf_dev)
         return fail(AMP_EINVAL, "%s: NULL state pointer", fn);
@@ -455,6 +468,7 @@ amp_status amp_update_scale_fp8_history(float *scale_dev, int32_t *growth_tracke
 amp_status amp_unscale_check_norm(amp_tensor_list grads, const float *scale_dev,
                                   int32_t *found_inf_dev, double *grad_sumsq_dev,
                                   amp_stream_t stream) {
+    AMP_TRACE("amp_unscale_check_norm");
     if (!grads || !found_inf_dev || !grad_sumsq_dev)
         return fail(AMP_EINVAL, "amp_unscale_check_norm: NULL argument");
     const int ec = elem_code(grads->dtype);
@@ -469,6 +483,7 @@ amp_status fp8_quant_tensorwise(const void *x, amp_dtype x_dtype, int64_t rows, 
                                 amp_dtype fp8_dtype, double eps, void *out, void *out_t,
                                 float *inv_scale_dev, float *amax_dev, int amax_given,
                                 const int32_t *skip_if_dev, amp_stream_t stream) {
+    AMP_TRACE("fp8_quant_tensorwise");
     if (bad_shape(rows, cols)) return fail(AMP_EINVAL, "fp8_quant_tensorwise: negative or too large size");
     if (!inv_scale_dev || !amax_dev) return fail(AMP_EINVAL, "fp8_quant_tensorwise: NULL inv_scale/amax");
     if (rows * cols > 0 && (!x || !out)) return fail(AMP_EINVAL, "fp8_quant_tensorwise: NULL x/out");
@@ -492,6 +507,7 @@ amp_status fp8_quant_rowwise(const void *x, amp_dtype x_dtype, int64_t rows, int
                              float *amax_row, float *scale_row, float *inv_scale_row,
                              float *amax_col, float *scale_col, float *inv_scale_col,
                              const int32_t *skip_if_dev, amp_stream_t stream) {
+    AMP_TRACE("fp8_quant_rowwise");
     const char *fn = "fp8_quant_rowwise";
     if (bad_shape(rows, cols)) return fail(AMP_EINVAL, "%s: negative or too large size", fn);
     if (rows * cols > 0 && (!x || !out || !amax_row || !scale_row || !inv_scale_row))
@@ -518,6 +534,7 @@ amp_status fp8_quant_tensorwise_list(amp_tensor_list x, amp_tensor_list out, amp
                                      amp_dtype fp8_dtype, double eps, const float *amax_dev,
                                      float *inv_scale_dev, const int32_t *skip_if_dev,
                                      amp_stream_t stream) {
+    AMP_TRACE("fp8_quant_tensorwise_list");
     if (!x || !out || !amax_dev || !inv_scale_dev)
         return fail(AMP_EINVAL, "fp8_quant_tensorwise_list: NULL argument");
     if (!x->two_d || !out->two_d || (out_t && !out_t->two_d))
@@ -542,6 +559,7 @@ amp_status fp8_quant_tensorwise_list(amp_tensor_list x, amp_tensor_list out, amp
 amp_status amp_update_scale(float *scale_dev, int32_t *growth_tracker_dev, int32_t *found_inf_dev,
                             float growth_factor, float backoff_factor, int32_t growth_interval,
                             float *amax_dev, int n_amax, amp_stream_t stream) {
+    AMP_TRACE("amp_update_scale");
     if (!scale_dev || !growth_tracker_dev || !found_inf_dev)
         return fail(AMP_EINVAL, "amp_update_scale: NULL state pointer");
     if (growth_interval < 1) return fail(AMP_EINVAL, "amp_update_scale: growth_interval < 1");
@@ -552,6 +570,33 @@ amp_status amp_update_scale(float *scale_dev, int32_t *growth_tracker_dev, int32
                                              amax_dev, n_amax,
                                              reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? AMP_OK : cuda_fail(e, "amp_update_scale");
+}
+
+amp_status amp_read_state(const float *scale_dev, const int32_t *growth_tracker_dev,
+                          const int32_t *step_dev, const int32_t *found_inf_dev,
+                          amp_scaler_state *host_out, amp_stream_t stream) {
+    AMP_TRACE("amp_read_state");
+    if (!host_out) return fail(AMP_EINVAL, "amp_read_state: host_out is NULL");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const void *src[4] = {scale_dev, growth_tracker_dev, step_dev, found_inf_dev};
+    void *dst[4] = {&host_out->scale, &host_out->growth_tracker, &host_out->step,
+                    &host_out->found_inf};
+    for (int i = 0; i < 4; ++i) {
+        if (!src[i]) continue;
+        cudaError_t e = cudaMemcpyAsync(dst[i], src[i], 4, cudaMemcpyDeviceToHost, s);
+        if (e != cudaSuccess) return cuda_fail(e, "amp_read_state");
+    }
+    return AMP_OK;
+}
+
+amp_status amp_scale_health(const float *scale_dev, float min_scale, int32_t *health_dev,
+                            amp_stream_t stream) {
+    AMP_TRACE("amp_scale_health");
+    if (!scale_dev || !health_dev) return fail(AMP_EINVAL, "amp_scale_health: NULL pointer");
+    if (!(min_scale >= 0.0f)) return fail(AMP_EINVAL, "amp_scale_health: min_scale must be >= 0");
+    cudaError_t e = amp::launch_scale_health(scale_dev, min_scale, health_dev,
+                                             reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AMP_OK : cuda_fail(e, "amp_scale_health");
 }
 
 }  // extern "C"

@@ -7,8 +7,21 @@
 
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "ampfp8.h"
 #include "common.cuh"
+
+// An NVTX range around one ABI call, named after the entry point: visible to
+// profilers that record NVTX ranges (ncu --nvtx, Nsight Systems); without an
+// attached tool each push/pop is a call through an empty hook.
+struct AmpTraceRange {
+    explicit AmpTraceRange(const char *name) { nvtxRangePushA(name); }
+    ~AmpTraceRange() { nvtxRangePop(); }
+    AmpTraceRange(const AmpTraceRange &) = delete;
+    AmpTraceRange &operator=(const AmpTraceRange &) = delete;
+};
+#define AMP_TRACE(name) AmpTraceRange amp_trace_range_(name)
 
 struct amp_tensor_list_s {
     int n = 0;
@@ -92,6 +105,7 @@ cudaError_t launch_adamw_fp8_delayed(const Fp8DelayedLists &L, int gelem, int fp
                                      float *inv_scale, cudaStream_t s);
 
 cudaError_t launch_bounded_wait_selftest(int32_t *err, double limit_s, cudaStream_t s);
+cudaError_t launch_scale_health(const float *scale, float min_scale, int32_t *health, cudaStream_t s);
 
 cudaError_t launch_update_scale_hist(float *scale, int32_t *tracker, int32_t *found_inf,
                                      float growth, float backoff, int32_t interval, float *amax,

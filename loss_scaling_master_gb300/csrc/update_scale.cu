@@ -93,4 +93,28 @@ cudaError_t launch_update_scale(float *scale, int32_t *tracker, int32_t *found_i
     return cudaGetLastError();
 }
 
+namespace {
+
+// Health of the loss scale: "第20章 量化与混合精度训练" and "06 · 混合精度" watch
+// the scale (scaler.get_scale()) and switch to bf16 when it keeps halving.
+// bit 0: the scale is not finite; bit 1: it fell below min_scale.  Bits are
+// only ever set.
+__global__ void scale_health_kernel(const float *scale, float min_scale, int32_t *health) {
+    pdl_wait();
+    pdl_trigger();
+    const float s = *scale;
+    const int32_t h = !isfinite(s) ? 1 : (s < min_scale ? 2 : 0);
+    if (h) {
+        volatile int32_t *p = health;
+        *p = *p | h;
+        __threadfence_system();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_scale_health(const float *scale, float min_scale, int32_t *health, cudaStream_t s) {
+    return launch_pdl(scale_health_kernel, dim3(1), dim3(1), 0, s, scale, min_scale, health);
+}
+
 }  // namespace amp

@@ -29,7 +29,7 @@ class AmpOptimizerStep:
                  init_scale=65536.0, growth_factor=2.0, backoff_factor=0.5,
                  growth_interval=2000, emit_bf16=True, fp8_shapes=None, fp8_eps=1e-12,
                  max_norm=None, fp8_scaling="dynamic", amax_history_len=1, sr_seed=None,
-                 stream=None):
+                 min_scale=None, stream=None):
         """master: fp32 device tensors (updated in place); grads: device
         tensors (f16/bf16/f32) the caller fills with scaled gradients before
         each step.  fp8_shapes: per tensor (rows, cols) for weights that get
@@ -39,7 +39,10 @@ class AmpOptimizerStep:
         "delayed" (the max of the last amax_history_len steps' amax, cast in
         the update pass; the history starts from the initial bf16 copy).
         sr_seed: round the bf16 copy stochastically with this 64-bit seed
-        (None: round to nearest-even)."""
+        (None: round to nearest-even).  min_scale: after every step, set the
+        sticky health bits of amp_scale_health in page-locked host memory when
+        the loss scale is not finite (1) or below min_scale (2); health()
+        reads them without synchronising (None: no check)."""
         dev = master[0].device
         self.stream = stream
         self.master = list(master)
@@ -55,6 +58,10 @@ class AmpOptimizerStep:
         self.step_count = torch.zeros(1, dtype=torch.int32, device=dev)
         self.found_inf = torch.zeros(1, dtype=torch.int32, device=dev)
         self.max_norm = max_norm
+        self.min_scale = min_scale
+        self.health_word = torch.zeros(1, dtype=torch.int32).pin_memory() \
+            if min_scale is not None else None
+        self._state_host = A.ScalerState()
         self.grad_sumsq = torch.zeros(1, dtype=torch.float64, device=dev)
         self.fp8_eps = fp8_eps
         mk = lambda ts, two_d=False: A.amp_tensor_list_create(ts, two_d=two_d, stream=stream)
@@ -136,9 +143,10 @@ class AmpOptimizerStep:
     def launches_per_step(self) -> int:
         """Kernels one step enqueues (check [+ norm reduce], AdamW prologue + main,
         [quant], update; delayed FP8: check, prologue, plain + FP8 mains, update)."""
+        health = 1 if self.min_scale is not None else 0
         if self.fp8_scaling == "delayed":
-            return 5
-        return 4 + (1 if self.n_fp8 else 0) + (1 if self.max_norm is not None else 0)
+            return 5 + health
+        return 4 + (1 if self.n_fp8 else 0) + (1 if self.max_norm is not None else 0) + health
 
     def add_grad_buffer(self, grads) -> int:
         """Register another set of gradient buffers (same shapes and dtype) and
@@ -192,6 +200,7 @@ class AmpOptimizerStep:
                                            self.growth, self.backoff, self.interval, self.amax,
                                            self.amax_history, self.n_fp8, self.hist_len,
                                            stream=s)
+            self._health(s)
             return
         if self.sr_seed is not None:
             A.amp_unscale_check(L_g, self.scale, self.found_inf, stream=s)
@@ -215,6 +224,15 @@ class AmpOptimizerStep:
         A.amp_update_scale(self.scale, self.growth_tracker, self.found_inf, self.growth,
                            self.backoff, self.interval, amax=self.amax if self.n_fp8 else None,
                            n_amax=self.n_fp8, stream=s)
+        self._health(s)
+
+    def _health(self, s):
+        if self.min_scale is not None:
+            A.amp_scale_health(self.scale, self.min_scale, self.health_word, stream=s)
+
+    def health(self) -> int:
+        """Sticky health bits of the loss scale (0 when min_scale is None); no sync."""
+        return 0 if self.health_word is None else int(self.health_word[0])
 
     def check(self, stream=None):
         """Raise AmpError(AMP_ETIMEOUT) if an AdamW kernel's bounded wait on its
@@ -222,10 +240,20 @@ class AmpOptimizerStep:
         holder = self.L_q if self.fp8_scaling == "delayed" else self.L_master
         A.amp_tensor_list_check(holder, stream=stream if stream is not None else self.stream)
 
-    def state(self) -> dict:
-        """Host copy of the scaler/optimizer counters (synchronises)."""
-        return {"scale": float(self.scale.item()), "growth_tracker": int(self.growth_tracker.item()),
-                "step": int(self.step_count.item()), "found_inf": int(self.found_inf.item())}
+    def state(self, stream=None) -> dict:
+        """Host copy of the scaler/optimizer counters (amp_read_state), read on
+        `stream` (default: the object's stream, else the current one), which it
+        synchronises: pass the stream the steps ran on."""
+        s = stream if stream is not None else self.stream
+        st = self._state_host
+        A.amp_read_state(self.scale, self.growth_tracker, self.step_count, self.found_inf, st,
+                         stream=s)
+        if s is None:
+            torch.cuda.current_stream(self.scale.device).synchronize()
+        else:
+            s.synchronize()
+        return {"scale": float(st.scale), "growth_tracker": int(st.growth_tracker),
+                "step": int(st.step), "found_inf": int(st.found_inf)}
 
     def state_dict(self) -> dict:
         """Host copies of everything a resumed run needs: master, m, v, the

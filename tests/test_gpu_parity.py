@@ -890,3 +890,33 @@ def test_list_host_copies_round_trip(A, dev):
         for d, s in zip(dst, src):
             assert torch.equal(d, s)
         L.close()
+
+
+# ------------------------------------------------------ monitoring
+def test_read_state_and_scale_health(A, dev):
+    """amp_read_state copies the scaler state to host memory; amp_scale_health
+    sets bit 2 once the scale has halved below min_scale and bit 1 for a
+    non-finite scale, into page-locked host memory the host polls."""
+    from loss_scaling_master_gb300 import AmpOptimizerStep
+    n = 3000
+    G = [torch.zeros(n, dtype=torch.float16, device=dev)]
+    st = AmpOptimizerStep([torch.zeros(n, device=dev)], G, lr=1e-3, beta1=0.9, beta2=0.999,
+                          eps=1e-8, weight_decay=0.0, init_scale=8.0, growth_interval=1000,
+                          min_scale=1.0)
+    G[0][17] = float("inf")                       # every step overflows: S halves each time
+    seen = []
+    for k in range(5):
+        st.step()
+        torch.cuda.synchronize()
+        seen.append(st.health())
+    assert seen == [0, 0, 0, 2, 2]                # 4, 2, 1, 0.5, 0.25
+    s = st.state()
+    assert s == {"scale": 0.25, "growth_tracker": 0, "step": 0, "found_inf": 0}
+    out = A.ScalerState()
+    bad = torch.tensor([float("nan")], device=dev)
+    A.amp_read_state(bad, st.growth_tracker, None, None, out)
+    health = torch.zeros(1, dtype=torch.int32).pin_memory()
+    A.amp_scale_health(bad, 1.0, health)
+    torch.cuda.synchronize()
+    assert np.isnan(out.scale) and out.growth_tracker == 0 and int(health[0]) == 1
+    st.close()
