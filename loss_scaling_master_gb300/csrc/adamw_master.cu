@@ -11,11 +11,13 @@
 //   prologue  one thread: reads found_inf and the step counter, forms the
 //             bias-corrected scalars in fp64 once, advances the counter when
 //             the step is not skipped, and leaves {skip, step_size, c2} in a
-//             16-byte block of the master list's device block;
-//   main      one CTA per chunk of 16384 elements; a skipped step returns at
-//             once, otherwise every thread streams groups of 8 elements with
-//             16-byte loads/stores: 14 bytes read + 14 bytes written per
-//             parameter (fp16/bf16 grads, bf16 emission).
+//             block of the master list's device block;
+//   main      adamw_bulk_kernel, one CTA per chunk of 16384 elements; a
+//             skipped step returns at once, otherwise the chunk streams
+//             through shared memory with TMA bulk copies: 14 bytes read + 14
+//             bytes written per parameter (fp16/bf16 grads, bf16 emission).
+// The delayed-FP8 form adds adamw_fp8_tile_kernel, which updates the FP8
+// weights by 128x128 tile and casts them in the same pass.
 #include "bulk_copy.cuh"
 #include "fp8_tile.cuh"
 #include "internal.h"
