@@ -7,7 +7,7 @@ handles, and enqueues, per step:
 
 1. ``amp_unscale_check``      scaled grads -> found_inf
 2. ``amp_adamw_master_step``  skip or update master/m/v, emit bf16 (+ amax)
-3. ``fp8_quant_tensorwise_list``  e4m3fn copies (+ transposed) of the FP8
+3. ``fp8_quant_tensorwise_list``  FP8 copies (+ transposed) of the FP8
    weights, skipped on inf (only when FP8 weights are configured)
 4. ``amp_update_scale``       scale state machine; clears found_inf and amax
 
@@ -29,11 +29,11 @@ class AmpOptimizerStep:
                  init_scale=65536.0, growth_factor=2.0, backoff_factor=0.5,
                  growth_interval=2000, emit_bf16=True, fp8_shapes=None, fp8_eps=1e-12,
                  max_norm=None, fp8_scaling="dynamic", amax_history_len=1, sr_seed=None,
-                 min_scale=None, stream=None):
+                 min_scale=None, fp8_format="e4m3fn", stream=None):
         """master: fp32 device tensors (updated in place); grads: device
         tensors (f16/bf16/f32) the caller fills with scaled gradients before
         each step.  fp8_shapes: per tensor (rows, cols) for weights that get
-        e4m3fn copies, None for the others (requires emit_bf16).  max_norm:
+        FP8 copies, None for the others (requires emit_bf16).  max_norm:
         clip the unscaled gradients to this global L2 norm (None: no clipping).
         fp8_scaling: "dynamic" (this step's amax, a separate cast pass) or
         "delayed" (the max of the last amax_history_len steps' amax, cast in
@@ -42,7 +42,9 @@ class AmpOptimizerStep:
         (None: round to nearest-even).  min_scale: after every step, set the
         sticky health bits of amp_scale_health in page-locked host memory when
         the loss scale is not finite (1) or below min_scale (2); health()
-        reads them without synchronising (None: no check)."""
+        reads them without synchronising (None: no check).  fp8_format: the
+        format of the FP8 weight copies, "e4m3fn" (the pages' choice for
+        weights) or "e5m2"."""
         dev = master[0].device
         self.stream = stream
         self.master = list(master)
@@ -59,6 +61,10 @@ class AmpOptimizerStep:
         self.found_inf = torch.zeros(1, dtype=torch.int32, device=dev)
         self.max_norm = max_norm
         self.min_scale = min_scale
+        if fp8_format not in ("e4m3fn", "e5m2"):
+            raise ValueError(fp8_format)
+        self.fp8_format = fp8_format
+        fp8_tdt = torch.float8_e4m3fn if fp8_format == "e4m3fn" else torch.float8_e5m2
         self.health_word = torch.zeros(1, dtype=torch.int32).pin_memory() \
             if min_scale is not None else None
         self._state_host = A.ScalerState()
@@ -82,8 +88,8 @@ class AmpOptimizerStep:
                 slots.append(self.n_fp8)
                 self.n_fp8 += 1
                 xs.append(self.bf16[i].view(sh[0], sh[1]))
-                self.fp8.append(torch.empty(sh, dtype=torch.float8_e4m3fn, device=dev))
-                self.fp8_t.append(torch.empty((sh[1], sh[0]), dtype=torch.float8_e4m3fn,
+                self.fp8.append(torch.empty(sh, dtype=fp8_tdt, device=dev))
+                self.fp8_t.append(torch.empty((sh[1], sh[0]), dtype=fp8_tdt,
                                               device=dev))
             A.amp_tensor_list_set_amax_slots(self.L_b, slots, stream=stream)
             self.L_x8 = mk(xs, True)
@@ -131,8 +137,8 @@ class AmpOptimizerStep:
             if sh is None:
                 continue
             self.bf16[i].copy_(self.master[i])
-            A.fp8_quant_tensorwise(self.bf16[i].view(*sh), "e4m3fn", self.fp8[j], self.fp8_t[j],
-                                   self.inv_scale[j:j + 1], self.amax[j:j + 1],
+            A.fp8_quant_tensorwise(self.bf16[i].view(*sh), self.fp8_format, self.fp8[j],
+                                   self.fp8_t[j], self.inv_scale[j:j + 1], self.amax[j:j + 1],
                                    eps=self.fp8_eps, stream=stream)
             j += 1
         with torch.cuda.stream(stream) if stream is not None else _nullctx():
@@ -191,7 +197,7 @@ class AmpOptimizerStep:
         if self.fp8_scaling == "delayed":
             P, F = self.delayed_groups[grad_buffer]
             A.amp_unscale_check(L_g, self.scale, self.found_inf, stream=s)
-            A.amp_adamw_master_step_fp8_delayed(P, F, self.L_q, self.L_qt, "e4m3fn",
+            A.amp_adamw_master_step_fp8_delayed(P, F, self.L_q, self.L_qt, self.fp8_format,
                                                 self.amax_history, self.hist_len, self.amax,
                                                 self.inv_scale, self.scale, self.found_inf,
                                                 self.step_count, *self.hyper,
@@ -218,7 +224,7 @@ class AmpOptimizerStep:
                                          self.scale, self.found_inf, self.step_count, *self.hyper,
                                          self.grad_sumsq, self.max_norm, amax=amax, stream=s)
         if self.n_fp8:
-            A.fp8_quant_tensorwise_list(self.L_x8, self.L_q, self.L_qt, "e4m3fn", self.amax,
+            A.fp8_quant_tensorwise_list(self.L_x8, self.L_q, self.L_qt, self.fp8_format, self.amax,
                                         self.inv_scale, eps=self.fp8_eps, skip_if=self.found_inf,
                                         stream=s)
         A.amp_update_scale(self.scale, self.growth_tracker, self.found_inf, self.growth,

@@ -248,7 +248,7 @@ class AmpStepOracle:
     def __init__(self, master, grad_dtype, lr, beta1, beta2, eps, weight_decay,
                  init_scale, growth_factor, backoff_factor, growth_interval,
                  emit_bf16=True, fp8_shapes=None, fp8_eps=1e-12, max_norm=None,
-                 fp8_scaling="dynamic", hist_len=1):
+                 fp8_scaling="dynamic", hist_len=1, fp8_format="e4m3fn"):
         self.master = [np.array(m, np.float32, copy=True) for m in master]
         self.exp_avg = [np.zeros_like(m) for m in self.master]
         self.exp_avg_sq = [np.zeros_like(m) for m in self.master]
@@ -261,6 +261,9 @@ class AmpStepOracle:
         self.fp8_shapes = fp8_shapes
         self.slots = None
         self.fp8_eps = fp8_eps
+        # format of the FP8 weight copies ("FP8训练：量化、自动微分、Torchao" §3:
+        # e4m3fn for weights and activations, e5m2 for gradients; both offered)
+        self.fp8_format = fp8_format
         self.max_norm = max_norm
         self.grad_norm = None
         if fp8_shapes is not None:
@@ -289,7 +292,7 @@ class AmpStepOracle:
                     continue
                 self.bf16[i] = encode("bf16", self.master[i])
                 q, qt, inv, am = fp8_quant_tensorwise(self.bf16[i], "bf16", sh[0], sh[1],
-                                                      "e4m3fn", self.fp8_eps, True)
+                                                      self.fp8_format, self.fp8_eps, True)
                 s_ = self.slots[i]
                 self.fp8[i], self.fp8_t[i], self.inv_scale[s_] = q, qt, inv
                 self.hist[s_, 0] = am
@@ -318,7 +321,7 @@ class AmpStepOracle:
                 else:
                     a = float(self.amax[s])
                 q, qt, inv, _ = fp8_quant_tensorwise(self.bf16[i], "bf16", sh[0], sh[1],
-                                                     "e4m3fn", self.fp8_eps, True, amax=a)
+                                                     self.fp8_format, self.fp8_eps, True, amax=a)
                 self.fp8[i], self.fp8_t[i], self.inv_scale[s] = q, qt, inv
         if self.fp8_scaling == "delayed" and not fi:
             self.hist[:, 1:] = self.hist[:, :-1].copy()

@@ -353,13 +353,15 @@ def test_fp8_cast_rounding_classes(A, dev, fmt):
     assert np.array_equal(qt, rqt)
 
 
-def test_fp8_quant_list_parity(A, dev):
+@pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
+def test_fp8_quant_list_parity(A, dev, fmt):
+    tdt = torch.float8_e4m3fn if fmt == "e4m3fn" else torch.float8_e5m2
     rng = np.random.default_rng(32)
     shapes = [(128, 256), (1024, 512), (127, 129), (384, 128), (64, 4096)]
     xs_h = [_x_host(rng, r, c, "bf16") for r, c in shapes]
     X = [to_device(h, "bf16", dev).view(r, c) for h, (r, c) in zip(xs_h, shapes)]
-    Q = [torch.empty((r, c), dtype=torch.float8_e4m3fn, device=dev) for r, c in shapes]
-    QT = [torch.empty((c, r), dtype=torch.float8_e4m3fn, device=dev) for r, c in shapes]
+    Q = [torch.empty((r, c), dtype=tdt, device=dev) for r, c in shapes]
+    QT = [torch.empty((c, r), dtype=tdt, device=dev) for r, c in shapes]
     LX, LQ, LQT = (A.amp_tensor_list_create(t, two_d=True) for t in (X, Q, QT))
     amax_h = np.array([np.abs(O.decode("bf16", h)).max() for h in xs_h], np.float32)
     amax_h[1] *= 0.5     # a given amax below the data: saturation path
@@ -367,11 +369,11 @@ def test_fp8_quant_list_parity(A, dev):
     inv = torch.zeros(len(shapes), device=dev)
     for skip in (1, 0):
         fi = torch.tensor([skip], dtype=torch.int32, device=dev)
-        A.fp8_quant_tensorwise_list(LX, LQ, LQT, "e4m3fn", amax, inv, skip_if=fi)
+        A.fp8_quant_tensorwise_list(LX, LQ, LQT, fmt, amax, inv, skip_if=fi)
         if skip:
             assert not inv.any()
     for i, (r, c) in enumerate(shapes):
-        rq, rqt, rinv, _ = O.fp8_quant_tensorwise(xs_h[i], "bf16", r, c, "e4m3fn",
+        rq, rqt, rinv, _ = O.fp8_quant_tensorwise(xs_h[i], "bf16", r, c, fmt,
                                                   amax=float(amax_h[i]))
         assert np.array_equal(to_host_bits(Q[i].view(torch.uint8)).ravel(), rq), i
         assert np.array_equal(to_host_bits(QT[i].view(torch.uint8)).ravel(), rqt), i
@@ -381,7 +383,8 @@ def test_fp8_quant_list_parity(A, dev):
 
 
 # ------------------------------------------------------------ composition
-def test_amp_step_composition_with_fp8(A, dev):
+@pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
+def test_amp_step_composition_with_fp8(A, dev, fmt):
     """The four calls of a step, with FP8 weights and an inf at step 3,
     against the oracle's step in the pages' order."""
     from loss_scaling_master_gb300 import AmpOptimizerStep
@@ -393,10 +396,11 @@ def test_amp_step_composition_with_fp8(A, dev):
     G = [torch.empty(n, dtype=torch.float16, device=dev) for n in sizes]
     hyper = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
     st = AmpOptimizerStep([torch.from_numpy(m.copy()).to(dev) for m in master], G,
-                          init_scale=65536.0, growth_interval=2, fp8_shapes=fp8_shapes, **hyper)
+                          init_scale=65536.0, growth_interval=2, fp8_shapes=fp8_shapes,
+                          fp8_format=fmt, **hyper)
     orc = O.AmpStepOracle(master, "f16", hyper["lr"], hyper["beta1"], hyper["beta2"],
                           hyper["eps"], hyper["weight_decay"], 65536.0, 2.0, 0.5, 2,
-                          fp8_shapes=fp8_shapes)
+                          fp8_shapes=fp8_shapes, fp8_format=fmt)
     for k in range(1, 8):
         gh = [(rng.standard_normal(n) * 1e-4 * orc.scale).astype(np.float16).view(np.uint16)
               for n in sizes]
@@ -530,9 +534,9 @@ def test_clipped_step_composition(A, dev):
 
 
 # ------------------------------------------------------ delayed FP8 scaling
-@pytest.mark.parametrize("hist_len", [1, 3])
+@pytest.mark.parametrize("hist_len,fmt", [(1, "e4m3fn"), (3, "e4m3fn"), (3, "e5m2")])
 @pytest.mark.parametrize("gdt", ["f16", "bf16"])
-def test_delayed_fp8_step_composition(A, dev, hist_len, gdt):
+def test_delayed_fp8_step_composition(A, dev, hist_len, gdt, fmt):
     """AdamW + bf16 + FP8 in one pass with the delayed scale vs the oracle's
     step: full tiles (vector path), ragged edge tiles and a tensor whose
     column count breaks 16-byte rows (element path), a skipped step."""
@@ -547,10 +551,11 @@ def test_delayed_fp8_step_composition(A, dev, hist_len, gdt):
     st = AmpOptimizerStep([torch.from_numpy(m.copy()).to(dev) for m in master],
                           [torch.empty(n, dtype=tdt, device=dev) for n in sizes],
                           init_scale=4096.0, growth_interval=3, fp8_shapes=fp8_shapes,
-                          fp8_scaling="delayed", amax_history_len=hist_len, **hyper)
+                          fp8_scaling="delayed", amax_history_len=hist_len, fp8_format=fmt,
+                          **hyper)
     orc = O.AmpStepOracle(master, gdt, hyper["lr"], hyper["beta1"], hyper["beta2"], hyper["eps"],
                           hyper["weight_decay"], 4096.0, 2.0, 0.5, 3, fp8_shapes=fp8_shapes,
-                          fp8_scaling="delayed", hist_len=hist_len)
+                          fp8_scaling="delayed", hist_len=hist_len, fp8_format=fmt)
 
     def check_fp8():
         j = 0
