@@ -925,3 +925,57 @@ def test_read_state_and_scale_health(A, dev):
     torch.cuda.synchronize()
     assert np.isnan(out.scale) and out.growth_tracker == 0 and int(health[0]) == 1
     st.close()
+
+
+# ------------------------------------------------------ every AdamW instantiation
+@pytest.mark.parametrize("gdt", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("emit", ["none", "rne", "sr"])
+def test_adamw_every_grad_dtype_and_copy_mode(A, dev, gdt, emit):
+    """Each (grad dtype) x (no copy, RNE bf16 copy, stochastic bf16 copy) form
+    of the update, aligned and misaligned, over chunk-spanning ragged sizes
+    with a skipped step: master, m, v and the copy bit-identical to the oracle."""
+    rng = np.random.default_rng(100 + len(gdt) + len(emit))
+    sizes = [1, 9, 2047, 2049, 16383, 16385, 3 * 16384 + 5]
+    seed = 0xC0FFEE
+    for misalign in (False, True):
+        master_h = [(rng.standard_normal(k) * 0.02).astype(np.float32) for k in sizes]
+        P = _device_views(master_h, "f32", dev, misalign)
+        M = _device_views([np.zeros(k, np.float32) for k in sizes], "f32", dev, misalign)
+        V = _device_views([np.zeros(k, np.float32) for k in sizes], "f32", dev, misalign)
+        G = _device_views(_grads_host(rng, sizes, gdt), gdt, dev, misalign)
+        B = _device_views([np.zeros(k, np.uint16) for k in sizes], "bf16", dev, misalign) \
+            if emit != "none" else None
+        LP, LM, LV, LG = (A.amp_tensor_list_create(x) for x in (P, M, V, G))
+        LB = A.amp_tensor_list_create(B) if B is not None else None
+        step = torch.zeros(1, dtype=torch.int32, device=dev)
+        fi = torch.zeros(1, dtype=torch.int32, device=dev)
+        rp, rm, rv = [x.copy() for x in master_h], [np.zeros(k, np.float32) for k in sizes], \
+            [np.zeros(k, np.float32) for k in sizes]
+        rb = [np.zeros(k, np.uint16) for k in sizes] if B is not None else None
+        rstep = 0
+        S = 512.0
+        for k in range(3):
+            gh = _grads_host(rng, sizes, gdt, sigma=1e-3 * S)
+            for t, h in zip(G, gh):
+                t.copy_(to_device(h, gdt, dev))
+            skip = int(k == 1)
+            fi.fill_(skip)
+            sd = torch.tensor([S], device=dev)
+            hyper = (1e-3, 0.9, 0.999, 1e-8, 0.01)
+            if emit == "sr":
+                A.amp_adamw_master_step_sr(LP, LM, LV, LG, LB, sd, fi, step, *hyper, seed)
+            else:
+                A.amp_adamw_master_step(LP, LM, LV, LG, LB, sd, fi, step, *hyper)
+            rstep = O.adamw_master_step(rp, rm, rv, gh, gdt, rb, S, skip, rstep, *hyper,
+                                        sr_seed=seed if emit == "sr" else None)
+            assert int(step.item()) == rstep
+        for i in range(len(sizes)):
+            key = (gdt, emit, misalign, sizes[i])
+            assert np.array_equal(to_host_bits(P[i]).view(np.uint32), rp[i].view(np.uint32)), key
+            assert np.array_equal(to_host_bits(M[i]).view(np.uint32), rm[i].view(np.uint32)), key
+            assert np.array_equal(to_host_bits(V[i]).view(np.uint32), rv[i].view(np.uint32)), key
+            if B is not None:
+                assert np.array_equal(to_host_bits(B[i]), rb[i]), key
+        for L in (LP, LM, LV, LG, LB):
+            if L is not None:
+                L.close()
