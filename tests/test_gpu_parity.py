@@ -354,16 +354,18 @@ def test_fp8_cast_rounding_classes(A, dev, fmt):
 
 
 @pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
-def test_fp8_quant_list_parity(A, dev, fmt):
+@pytest.mark.parametrize("xdt", ["bf16", "f16", "f32"])
+def test_fp8_quant_list_parity(A, dev, fmt, xdt):
     tdt = torch.float8_e4m3fn if fmt == "e4m3fn" else torch.float8_e5m2
     rng = np.random.default_rng(32)
     shapes = [(128, 256), (1024, 512), (127, 129), (384, 128), (64, 4096)]
-    xs_h = [_x_host(rng, r, c, "bf16") for r, c in shapes]
-    X = [to_device(h, "bf16", dev).view(r, c) for h, (r, c) in zip(xs_h, shapes)]
+    xs_h = [_x_host(rng, r, c, xdt) for r, c in shapes]
+    X = [to_device(h, xdt, dev).view(r, c) for h, (r, c) in zip(xs_h, shapes)]
     Q = [torch.empty((r, c), dtype=tdt, device=dev) for r, c in shapes]
     QT = [torch.empty((c, r), dtype=tdt, device=dev) for r, c in shapes]
     LX, LQ, LQT = (A.amp_tensor_list_create(t, two_d=True) for t in (X, Q, QT))
-    amax_h = np.array([np.abs(O.decode("bf16", h)).max() for h in xs_h], np.float32)
+    dec = (lambda h: h) if xdt == "f32" else (lambda h: O.decode(xdt, h))
+    amax_h = np.array([np.abs(dec(h)).max() for h in xs_h], np.float32)
     amax_h[1] *= 0.5     # a given amax below the data: saturation path
     amax = torch.from_numpy(amax_h).to(dev)
     inv = torch.zeros(len(shapes), device=dev)
@@ -373,7 +375,7 @@ def test_fp8_quant_list_parity(A, dev, fmt):
         if skip:
             assert not inv.any()
     for i, (r, c) in enumerate(shapes):
-        rq, rqt, rinv, _ = O.fp8_quant_tensorwise(xs_h[i], "bf16", r, c, fmt,
+        rq, rqt, rinv, _ = O.fp8_quant_tensorwise(xs_h[i], xdt, r, c, fmt,
                                                   amax=float(amax_h[i]))
         assert np.array_equal(to_host_bits(Q[i].view(torch.uint8)).ravel(), rq), i
         assert np.array_equal(to_host_bits(QT[i].view(torch.uint8)).ravel(), rqt), i
@@ -535,7 +537,7 @@ def test_clipped_step_composition(A, dev):
 
 # ------------------------------------------------------ delayed FP8 scaling
 @pytest.mark.parametrize("hist_len,fmt", [(1, "e4m3fn"), (3, "e4m3fn"), (3, "e5m2")])
-@pytest.mark.parametrize("gdt", ["f16", "bf16"])
+@pytest.mark.parametrize("gdt", ["f16", "bf16", "f32"])
 def test_delayed_fp8_step_composition(A, dev, hist_len, gdt, fmt):
     """AdamW + bf16 + FP8 in one pass with the delayed scale vs the oracle's
     step: full tiles (vector path), ragged edge tiles and a tensor whose
@@ -547,7 +549,7 @@ def test_delayed_fp8_step_composition(A, dev, hist_len, gdt, fmt):
     sizes = [int(np.prod(s)) for s in shapes]
     master = [(rng.standard_normal(n) * 0.02).astype(np.float32) for n in sizes]
     hyper = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
-    tdt = torch.float16 if gdt == "f16" else torch.bfloat16
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[gdt]
     st = AmpOptimizerStep([torch.from_numpy(m.copy()).to(dev) for m in master],
                           [torch.empty(n, dtype=tdt, device=dev) for n in sizes],
                           init_scale=4096.0, growth_interval=3, fp8_shapes=fp8_shapes,
@@ -573,8 +575,8 @@ def test_delayed_fp8_step_composition(A, dev, hist_len, gdt, fmt):
     for k in range(6):
         sigma = 1e-3 * orc.scale
         gh = [(rng.standard_normal(n) * sigma).astype(np.float32) for n in sizes]
-        gh = [g.astype(np.float16).view(np.uint16) if gdt == "f16" else O.encode("bf16", g)
-              for g in gh]
+        gh = [g.astype(np.float16).view(np.uint16) if gdt == "f16" else
+              (O.encode("bf16", g) if gdt == "bf16" else g) for g in gh]
         if k == 3:
             gh[3][17] = _inf_bits(gdt, np.inf)
         for t, h in zip(st.grads, gh):
