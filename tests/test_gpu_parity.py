@@ -501,26 +501,35 @@ def test_grad_norm_parity_and_determinism(A, dev, dt, misalign):
         Lb.close()
 
 
-def test_clipped_step_composition(A, dev):
+@pytest.mark.parametrize("gdt,with_fp8", [("f16", False), ("bf16", False), ("f32", False),
+                                          ("f16", True)])
+def test_clipped_step_composition(A, dev, gdt, with_fp8):
     """AmpOptimizerStep with max_norm vs the oracle's step with clipping, over
-    steps where the factor is < 1, = 1 and a skipped step."""
+    steps where the factor is < 1, = 1 and a skipped step; every grad dtype,
+    and once with FP8 weights cast after the clipped update."""
     from loss_scaling_master_gb300 import AmpOptimizerStep
     rng = np.random.default_rng(51)
     sizes = [1000, 4096, 257, 40000]
+    fp8_shapes = [None, (64, 64), None, (200, 200)] if with_fp8 else None
     master = [(rng.standard_normal(n) * 0.02).astype(np.float32) for n in sizes]
     hyper = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[gdt]
     st = AmpOptimizerStep([torch.from_numpy(m.copy()).to(dev) for m in master],
-                          [torch.empty(n, dtype=torch.float16, device=dev) for n in sizes],
-                          init_scale=65536.0, growth_interval=3, max_norm=0.5, **hyper)
-    orc = O.AmpStepOracle(master, "f16", hyper["lr"], hyper["beta1"], hyper["beta2"], hyper["eps"],
-                          hyper["weight_decay"], 65536.0, 2.0, 0.5, 3, max_norm=0.5)
+                          [torch.empty(n, dtype=tdt, device=dev) for n in sizes],
+                          init_scale=65536.0, growth_interval=3, max_norm=0.5,
+                          fp8_shapes=fp8_shapes, **hyper)
+    orc = O.AmpStepOracle(master, gdt, hyper["lr"], hyper["beta1"], hyper["beta2"], hyper["eps"],
+                          hyper["weight_decay"], 65536.0, 2.0, 0.5, 3, max_norm=0.5,
+                          fp8_shapes=fp8_shapes)
     for k in range(6):
         sigma = (1e-2 if k % 2 == 0 else 1e-5) * orc.scale      # clipped, then unclipped
-        gh = [(rng.standard_normal(n) * sigma).astype(np.float16).view(np.uint16) for n in sizes]
+        gh = [(rng.standard_normal(n) * sigma).astype(np.float32) for n in sizes]
+        gh = [g.astype(np.float16).view(np.uint16) if gdt == "f16" else
+              (O.encode("bf16", g) if gdt == "bf16" else g) for g in gh]
         if k == 3:
-            gh[2][100] = 0x7C00
+            gh[2][100] = _inf_bits(gdt, np.inf)
         for t, h in zip(st.grads, gh):
-            t.copy_(to_device(h, "f16", dev))
+            t.copy_(to_device(h, gdt, dev))
         st.step()
         orc.run(gh)
         s = st.state()
@@ -532,6 +541,17 @@ def test_clipped_step_composition(A, dev):
         assert_state_close(to_host_bits(st.exp_avg[i]), orc.exp_avg[i], f"exp_avg[{i}]")
         assert_state_close(to_host_bits(st.exp_avg_sq[i]), orc.exp_avg_sq[i], f"exp_avg_sq[{i}]")
         assert_bf16_close(to_host_bits(st.bf16[i]), orc.bf16[i], f"bf16[{i}]")
+    if with_fp8:
+        # the cast is exact given the copy and amax: compare where the copies agree
+        j = 0
+        for i, sh in enumerate(fp8_shapes):
+            if sh is None:
+                continue
+            if np.array_equal(to_host_bits(st.bf16[i]), orc.bf16[i]):
+                assert np.array_equal(to_host_bits(st.fp8[j].view(torch.uint8)).ravel(), orc.fp8[i])
+                assert np.array_equal(to_host_bits(st.fp8_t[j].view(torch.uint8)).ravel(),
+                                      orc.fp8_t[i])
+            j += 1
     st.close()
 
 
