@@ -1001,3 +1001,59 @@ def test_adamw_every_grad_dtype_and_copy_mode(A, dev, gdt, emit):
         for L in (LP, LM, LV, LG, LB):
             if L is not None:
                 L.close()
+
+
+def test_two_steps_on_two_streams_concurrently(A, dev):
+    """Two independent optimizer steps (own lists, own scaler state), each on
+    its own stream, enqueued alternately with no host sync in between: both
+    end bit-identical to the oracle (per-list scratch, stream-ordered launches)."""
+    from loss_scaling_master_gb300 import AmpOptimizerStep
+    rng = np.random.default_rng(110)
+    streams = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
+    cases = []
+    for c in range(2):
+        shapes = [(96, 256), (3000,), (200, 136)] if c == 0 else [(50000,), (128, 128)]
+        fp8_shapes = [s if len(s) == 2 else None for s in shapes]
+        sizes = [int(np.prod(s)) for s in shapes]
+        master = [(rng.standard_normal(n) * 0.02).astype(np.float32) for n in sizes]
+        hyper = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+        with torch.cuda.stream(streams[c]):
+            st = AmpOptimizerStep([torch.from_numpy(m.copy()).to(dev) for m in master],
+                                  [torch.zeros(n, dtype=torch.float16, device=dev) for n in sizes],
+                                  init_scale=1024.0, growth_interval=2, fp8_shapes=fp8_shapes,
+                                  fp8_scaling="delayed" if c == 1 else "dynamic",
+                                  stream=streams[c], **hyper)
+        orc = O.AmpStepOracle(master, "f16", hyper["lr"], hyper["beta1"], hyper["beta2"],
+                              hyper["eps"], hyper["weight_decay"], 1024.0, 2.0, 0.5, 2,
+                              fp8_shapes=fp8_shapes,
+                              fp8_scaling="delayed" if c == 1 else "dynamic")
+        cases.append((st, orc, sizes, fp8_shapes))
+    torch.cuda.synchronize()
+    grads = [[[(rng.standard_normal(n) * 1e-3 * 1024).astype(np.float16).view(np.uint16)
+               for n in sizes] for _ in range(4)] for (_, _, sizes, _) in cases]
+    dev_grads = [[[to_device(h, "f16", dev) for h in g] for g in per] for per in grads]
+    torch.cuda.synchronize()
+    for k in range(4):
+        for c, (st, orc, sizes, _) in enumerate(cases):
+            with torch.cuda.stream(streams[c]):
+                for t, h in zip(st.grads, dev_grads[c][k]):
+                    t.copy_(h)
+            st.step(stream=streams[c])
+    torch.cuda.synchronize()
+    for c, (st, orc, sizes, fp8_shapes) in enumerate(cases):
+        for k in range(4):
+            orc.run(grads[c][k])
+        s = st.state()
+        assert (s["scale"], s["growth_tracker"], s["step"]) == (orc.scale, orc.tracker, orc.step)
+        for i in range(len(sizes)):
+            assert np.array_equal(to_host_bits(st.master[i]).view(np.uint32),
+                                  orc.master[i].view(np.uint32)), (c, i)
+            assert np.array_equal(to_host_bits(st.bf16[i]), orc.bf16[i]), (c, i)
+        j = 0
+        for i, sh in enumerate(fp8_shapes):
+            if sh is None:
+                continue
+            assert np.array_equal(to_host_bits(st.fp8[j].view(torch.uint8)).ravel(), orc.fp8[i])
+            assert np.array_equal(to_host_bits(st.fp8_t[j].view(torch.uint8)).ravel(), orc.fp8_t[i])
+            j += 1
+        st.close()
