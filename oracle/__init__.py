@@ -75,6 +75,8 @@ def lib():
                                                    ctypes.c_int32, ctypes.c_int32]
             L.orc_fp8_quant_rowwise.argtypes = [P, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                                                 ctypes.c_int, ctypes.c_double] + [P] * 8
+            L.orc_fp8_quant_groupwise.argtypes = [P, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                                  ctypes.c_int64, ctypes.c_int, ctypes.c_double] + [P] * 8
             L.orc_fp8_quant_tensorwise.argtypes = [P, ctypes.c_int, ctypes.c_int64,
                                                    ctypes.c_int64, ctypes.c_int,
                                                    ctypes.c_double, P, P, P, P, ctypes.c_int]
@@ -214,6 +216,28 @@ def fp8_quant_tensorwise(x: np.ndarray, xdt: str, rows: int, cols: int, fp8: str
                                    _ptr(out), _ptr(out_t) if out_t is not None else None,
                                    _ptr(inv), _ptr(am), int(amax is not None))
     return out, out_t, float(inv[0]), float(am[0])
+
+
+def fp8_quant_groupwise(x: np.ndarray, xdt: str, rows: int, cols: int, fp8: str, group: int,
+                        eps: float = 1e-12, transposed: bool = True):
+    """One scale per `group` consecutive elements of a row for the row-major
+    bytes, per `group` consecutive rows of a column for the transposed copy.
+    Returns a dict of q, amax/scale/inv per row group ([rows, ceil(cols/group)])
+    and, transposed, q_t and amax/scale/inv per column group
+    ([cols, ceil(rows/group)])."""
+    x = np.ascontiguousarray(x)
+    assert x.size == rows * cols and group >= 1
+    ngc, ngr = -(-cols // group), -(-rows // group)
+    r = {"q": np.empty(rows * cols, np.uint8), "amax_rg": np.empty(rows * ngc, np.float32),
+         "scale_rg": np.empty(rows * ngc, np.float32), "inv_rg": np.empty(rows * ngc, np.float32)}
+    if transposed:
+        r.update(q_t=np.empty(rows * cols, np.uint8), amax_cg=np.empty(cols * ngr, np.float32),
+                 scale_cg=np.empty(cols * ngr, np.float32), inv_cg=np.empty(cols * ngr, np.float32))
+    g = lambda k: _ptr(r[k]) if k in r else None
+    lib().orc_fp8_quant_groupwise(_ptr(x), _CODES[xdt], rows, cols, group, _CODES[fp8], eps,
+                                  g("q"), g("q_t"), g("amax_rg"), g("scale_rg"), g("inv_rg"),
+                                  g("amax_cg"), g("scale_cg"), g("inv_cg"))
+    return r
 
 
 def fp8_quant_rowwise(x: np.ndarray, xdt: str, rows: int, cols: int, fp8: str,

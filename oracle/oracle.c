@@ -494,6 +494,57 @@ void orc_fp8_quant_rowwise(const void *x, int xdtype, int64_t rows, int64_t cols
 }
 
 /* ------------------------------------------------------------------------ */
+/* Group-wise FP8 scaling.  "第20章 量化与混合精度训练" §20.5.18: a weight     */
+/* [out, in] is cut into groups of `group` consecutive elements along in, each */
+/* with its own scale (g128: scales of shape [out, in / 128]).  Reading: §2's  */
+/* recipe of "FP8训练：量化、自动微分、Torchao" per group - amax of the group,  */
+/* scale_d = fp8_max / max(double(amax), EPS), clamp and RNE cast.  The        */
+/* column-major copy out_t ([cols, rows], §4) feeds the backward GEMM, whose   */
+/* reduction runs along the rows of x, so its groups are `group` consecutive   */
+/* rows within one column (scales of shape [cols, rows / group]).  The last    */
+/* group of a row (column) holds the remaining cols % group (rows % group).    */
+/*   *_rg: [rows, ceil(cols / group)] row-major; *_cg: [cols, ceil(rows /     */
+/*   group)] row-major.                                                       */
+/* ------------------------------------------------------------------------ */
+void orc_fp8_quant_groupwise(const void *x, int xdtype, int64_t rows, int64_t cols, int64_t group,
+                             int fp8_dtype, double eps, uint8_t *out, uint8_t *out_t,
+                             float *amax_rg, float *scale_rg, float *inv_rg, float *amax_cg,
+                             float *scale_cg, float *inv_cg)
+{
+    const orc_fmt *f = fmt_of(fp8_dtype);
+    double fmax = fmt_max(f);
+    int64_t ngc = (cols + group - 1) / group, ngr = (rows + group - 1) / group;
+    for (int64_t i = 0; i < rows; ++i) {
+        for (int64_t g = 0; g < ngc; ++g) {
+            int64_t j0 = g * group, j1 = j0 + group < cols ? j0 + group : cols;
+            double a = 0.0;
+            for (int64_t j = j0; j < j1; ++j)
+                a = nan_max_abs_update(a, load_as_f32(xdtype, x, i * cols + j));
+            int64_t k = i * ngc + g;
+            amax_rg[k] = (float)a;
+            scale_of(fmax, eps, amax_rg[k], &scale_rg[k], &inv_rg[k]);
+            for (int64_t j = j0; j < j1; ++j)
+                out[i * cols + j] = cast_scaled(f, load_as_f32(xdtype, x, i * cols + j), scale_rg[k]);
+        }
+    }
+    if (!out_t)
+        return;
+    for (int64_t j = 0; j < cols; ++j) {
+        for (int64_t g = 0; g < ngr; ++g) {
+            int64_t i0 = g * group, i1 = i0 + group < rows ? i0 + group : rows;
+            double a = 0.0;
+            for (int64_t i = i0; i < i1; ++i)
+                a = nan_max_abs_update(a, load_as_f32(xdtype, x, i * cols + j));
+            int64_t k = j * ngr + g;
+            amax_cg[k] = (float)a;
+            scale_of(fmax, eps, amax_cg[k], &scale_cg[k], &inv_cg[k]);
+            for (int64_t i = i0; i < i1; ++i)
+                out_t[j * rows + i] = cast_scaled(f, load_as_f32(xdtype, x, i * cols + j), scale_cg[k]);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Stochastic rounding of the bf16 working copy.  "第20章 量化与混合精度训练"  */
 /* §20.5.14: instead of round-to-nearest, round down or up with probability   */
 /* proportional to the distance, so the expected value is the input.  For a  */

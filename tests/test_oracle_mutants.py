@@ -82,6 +82,13 @@ MUTANTS = [
     ("rowwise_copy_uses_row_scale", C,
      "out_t[j * rows + i] = cast_scaled(f, load_as_f32(xdtype, x, i * cols + j), scale_col[j]);",
      "out_t[j * rows + i] = cast_scaled(f, load_as_f32(xdtype, x, i * cols + j), scale_row[i < cols ? i : 0]);"),
+    # group-wise FP8
+    ("groupwise_group_one_short", C,
+     "int64_t j0 = g * group, j1 = j0 + group < cols ? j0 + group : cols;",
+     "int64_t j0 = g * group, j1 = j0 + group - 1 < cols ? j0 + group - 1 : cols;"),
+    ("groupwise_copy_groups_by_row_scale", C,
+     "out_t[j * rows + i] = cast_scaled(f, load_as_f32(xdtype, x, i * cols + j), scale_cg[k]);",
+     "out_t[j * rows + i] = cast_scaled(f, load_as_f32(xdtype, x, i * cols + j), scale_rg[i * ((cols + group - 1) / group) + j / group]);"),
     # Philox / stochastic rounding
     ("philox_nine_rounds", C, "for (int r = 0; r < 10; ++r) {", "for (int r = 0; r < 9; ++r) {"),
     ("philox_key_weyl_swapped", C, "        k1 += 0xBB67AE85u;", "        k1 += 0x9E3779B9u;"),

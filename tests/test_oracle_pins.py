@@ -570,6 +570,60 @@ def test_rowwise_vs_torch_ops(fmt, tdt):
         assert np.array_equal(r["amax_" + key], am.numpy().ravel())
 
 
+# --------------------------------------------------------- group-wise FP8
+@pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
+@pytest.mark.parametrize("rows,cols", [(5, 7), (33, 64)])
+def test_groupwise_with_one_group_is_rowwise(fmt, rows, cols):
+    """A group at least as long as a row (a column) is the whole row (column):
+    the group-wise quantizer then reduces to the row-wise one."""
+    rng = np.random.default_rng(83)
+    x = (rng.standard_normal(rows * cols) * 2).astype(F32)
+    g = O.fp8_quant_groupwise(x, "f32", rows, cols, fmt, group=max(rows, cols) + 3)
+    r = O.fp8_quant_rowwise(x, "f32", rows, cols, fmt)
+    assert np.array_equal(g["q"], r["q"]) and np.array_equal(g["q_t"], r["q_t"])
+    for a, b in (("amax_rg", "amax_row"), ("scale_rg", "scale_row"), ("inv_rg", "inv_row"),
+                 ("amax_cg", "amax_col"), ("scale_cg", "scale_col"), ("inv_cg", "inv_col")):
+        assert np.array_equal(g[a].view(np.uint32), r[b].view(np.uint32)), a
+
+
+@pytest.mark.parametrize("fmt,tdt", [("e4m3fn", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)])
+@pytest.mark.parametrize("group", [4, 32, 128])
+def test_groupwise_vs_torch_ops(fmt, tdt, group):
+    """Each group of `group` elements (the last one ragged) through torch CPU
+    ops: abs-max, fp64 scale with the EPS floor, fp32 multiply by the scale
+    rounded to fp32, clamp, library fp8 cast; rows for the row-major bytes,
+    columns for the transposed copy ("第20章" §20.5.18 g128 layout)."""
+    rng = np.random.default_rng(84)
+    rows, cols = 70, 150
+    x = rng.standard_normal((rows, cols)) * 10 ** rng.uniform(-2, 2, size=(rows, 1))
+    x[3, :] = 0.0                                   # an all-zero row: its groups clamp to EPS
+    xb = torch.from_numpy(x.astype(F32)).to(torch.bfloat16)
+    bits = xb.view(torch.int16).numpy().view(np.uint16).ravel()
+    r = O.fp8_quant_groupwise(bits, "bf16", rows, cols, fmt, group=group)
+    mx = float(torch.finfo(tdt).max)
+    xf = xb.float()
+
+    def ref(m):               # m: [n, L] -> bytes, amax, inv per group along dim 1
+        q = torch.empty(m.shape, dtype=torch.uint8)
+        am, inv = [], []
+        for i in range(m.shape[0]):
+            for j0 in range(0, m.shape[1], group):
+                seg = m[i, j0:j0 + group]
+                a = seg.abs().max()
+                sc = mx / a.double().clamp(min=1e-12)
+                q[i, j0:j0 + group] = (seg * sc.float()).clamp(-mx, mx).to(tdt).view(torch.uint8)
+                am.append(a.item())
+                inv.append(sc.reciprocal().float().item())
+        return q.numpy().ravel(), np.array(am, F32), np.array(inv, F32)
+
+    q, am, inv = ref(xf)
+    assert np.array_equal(r["q"], q)
+    assert np.array_equal(r["amax_rg"], am) and np.array_equal(r["inv_rg"], inv)
+    qt, amt, invt = ref(xf.T.contiguous())
+    assert np.array_equal(r["q_t"], qt)
+    assert np.array_equal(r["amax_cg"], amt) and np.array_equal(r["inv_cg"], invt)
+
+
 # ---------------------------------------------------- stochastic rounding
 def test_philox_known_answers():
     """Philox4x32-10 known-answer vectors of its authors' reference release
