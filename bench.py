@@ -455,6 +455,14 @@ def run_fp8_sweep(args, rank, world, device):
     stream = torch.cuda.Stream(device=device)
     fmts = ["e4m3fn", "e5m2"]
     rowwise = args.fp8_granularity == "rowwise"
+    groupwise = args.fp8_granularity == "groupwise"
+    if groupwise:
+        G = 128
+        gw = [{k: torch.empty(n, device=device) for k, n in
+               (("ar", x.shape[0] * -(-x.shape[1] // G)), ("sr", x.shape[0] * -(-x.shape[1] // G)),
+                ("ir", x.shape[0] * -(-x.shape[1] // G)), ("ac", x.shape[1] * -(-x.shape[0] // G)),
+                ("sc", x.shape[1] * -(-x.shape[0] // G)), ("ic", x.shape[1] * -(-x.shape[0] // G)))}
+              for x in mats]
     if rowwise:
         rc = [{k: torch.empty(n, device=device) for k, n in
                (("ar", x.shape[0]), ("sr", x.shape[0]), ("ir", x.shape[0]),
@@ -463,7 +471,11 @@ def run_fp8_sweep(args, rank, world, device):
     def one(ev=None):
         for f in fmts:
             for i, x in enumerate(mats):
-                if rowwise:
+                if groupwise:
+                    d = gw[i]
+                    A.fp8_quant_groupwise(x, f, G, outs[i][0], outs[i][1], d["ar"], d["sr"],
+                                          d["ir"], d["ac"], d["sc"], d["ic"], stream=stream)
+                elif rowwise:
                     d = rc[i]
                     A.fp8_quant_rowwise(x, f, outs[i][0], outs[i][1], d["ar"], d["sr"], d["ir"],
                                         d["ac"], d["sc"], d["ic"], stream=stream)
@@ -489,10 +501,14 @@ def run_fp8_sweep(args, rank, world, device):
     ms = statistics.mean(times)
     elems = sum(x.numel() for x in mats) * len(fmts)
     peak, kind = measured_peaks()
-    gbs = 6 * elems / (ms * 1e-3) / 1e9
+    # algorithmic bytes: two passes (amax, then cast) read x twice; the
+    # group-wise cast reads it once (its groups lie inside one tile)
+    per_elt = 4 if groupwise else 6
+    gbs = per_elt * elems / (ms * 1e-3) / 1e9
     if rank != 0:
         return None
-    gran = "rowwise (per-row / per-column scales)" if rowwise else "tensorwise"
+    gran = ("rowwise (per-row / per-column scales)" if rowwise else
+            "group-wise (g128 along rows / along columns for the copy)" if groupwise else "tensorwise")
     return {"metric": f"FP8 {gran} quant GB/s (amax + e4m3fn/e5m2 cast + transposed copy)",
             "value": gbs * world, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -503,7 +519,8 @@ def run_fp8_sweep(args, rank, world, device):
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                          "frac": gbs / peak, "peak_kind": kind, "traffic": None},
             "clocks": clk.summary(),
-            "gpu_launches": args.steps * len(mats) * len(fmts) * (4 if rowwise else 3)}
+            "bytes_per_elt": per_elt,
+            "gpu_launches": args.steps * len(mats) * len(fmts) * (4 if rowwise else 1 if groupwise else 3)}
 
 
 # ------------------------------------------------------------ CPU baseline
@@ -594,7 +611,8 @@ def main():
     ap.add_argument("--fp8-scaling", default="dynamic", choices=["dynamic", "delayed"],
                     help="FP8 weight scaling: this step's amax (a separate cast pass) or the "
                          "previous step's (cast fused into the AdamW pass)")
-    ap.add_argument("--fp8-granularity", default="tensorwise", choices=["tensorwise", "rowwise"],
+    ap.add_argument("--fp8-granularity", default="tensorwise",
+                    choices=["tensorwise", "rowwise", "groupwise"],
                     help="scale granularity of the fp8_sweep workload")
     ap.add_argument("--sr-seed", type=int, default=None,
                     help="round the bf16 copy stochastically (Philox4x32-10 with this seed)")

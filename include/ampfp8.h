@@ -313,6 +313,30 @@ amp_status fp8_quant_tensorwise(const void *x, amp_dtype x_dtype, int64_t rows, 
                                 float *inv_scale_dev, float *amax_dev, int amax_given,
                                 const int32_t *skip_if_dev, amp_stream_t stream);
 
+/* Group-wise scaling ("第20章 量化与混合精度训练" §20.5.18: a weight [out, in]
+ * cut into groups of `group` consecutive elements along in, one scale per
+ * group; g128 is the usual size).  x is [rows, cols] row-major (bf16, f16,
+ * f32); group is 32, 64 or 128.  With ngc = ceil(cols / group), for every row
+ * i and group g (columns g*group .. min((g+1)*group, cols) - 1), §2 of
+ * "FP8训练：量化、自动微分、Torchao" on that group alone:
+ *     amax_rg[i*ngc+g]  = max |x[i,j]| over the group  (fp32, NaN propagating)
+ *     scale_d           = fp8_max / max(double(amax), eps)               (fp64)
+ *     scale_rg[i*ngc+g] = float(scale_d), inv_rg[i*ngc+g] = float(1/scale_d)
+ *     out[i,j]          = fp8(clamp(float(x[i,j]) * scale_rg, +-fp8_max)), RNE
+ * If out_t is non-NULL it is the column-major copy ([cols, rows], §4) for the
+ * GEMMs that reduce along the rows of x, so its groups are `group` consecutive
+ * rows of one column: with ngr = ceil(rows / group), amax_cg / scale_cg /
+ * inv_cg[j*ngr+g] and out_t[j,i] = fp8(clamp(float(x[i,j]) * scale_cg, ...)).
+ * One launch, one CTA per 128x128 tile, 2 bytes read + 1 (+1) written per
+ * element.  A set *skip_if_dev writes nothing.  Empty tensors return at once.
+ * Errors: AMP_EINVAL (group not 32/64/128, NULL outputs, negative size,
+ * eps <= 0), AMP_EDTYPE. */
+amp_status fp8_quant_groupwise(const void *x, amp_dtype x_dtype, int64_t rows, int64_t cols,
+                               int64_t group, amp_dtype fp8_dtype, double eps, void *out,
+                               void *out_t, float *amax_rg, float *scale_rg, float *inv_rg,
+                               float *amax_cg, float *scale_cg, float *inv_cg,
+                               const int32_t *skip_if_dev, amp_stream_t stream);
+
 /* Rowwise scaling ("FP8训练：量化、自动微分、Torchao" §1: one scale per row
  * instead of one per tensor).  x is [rows, cols] row-major (bf16, f16, f32).
  * For every row i, §2's recipe on that row alone:

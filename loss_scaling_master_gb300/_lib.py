@@ -28,7 +28,7 @@ _TORCH_DT = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16",
 EXPORTS = ("amp_tensor_list_create", "amp_tensor_list_set_amax_slots", "amp_tensor_list_destroy",
            "amp_tensor_list_check", "amp_selftest_bounded_wait",
            "amp_tensor_list_copy_from_host", "amp_tensor_list_copy_to_host",
-           "amp_read_state", "amp_scale_health",
+           "amp_read_state", "amp_scale_health", "fp8_quant_groupwise",
            "amp_unscale_check", "amp_unscale_check_norm", "amp_adamw_master_step",
            "amp_adamw_master_step_clip", "amp_adamw_master_step_sr",
            "amp_adamw_master_step_noalloc", "amp_noalloc_check",
@@ -74,6 +74,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.amp_tensor_list_copy_to_host.argtypes = [P, P, P]
         L.amp_read_state.argtypes = [P, P, P, P, P, P]
         L.amp_scale_health.argtypes = [P, flt, P, P]
+        L.fp8_quant_groupwise.argtypes = [P, i32, i64, i64, i64, i32, dbl] + [P] * 10
         L.amp_noalloc_check.argtypes = [P]
         L.amp_selftest_bounded_wait.argtypes = [P, dbl, P]
         L.amp_adamw_master_step.argtypes = [P, P, P, P, P, P, P, P,
@@ -374,6 +375,20 @@ def fp8_quant_rowwise(x: torch.Tensor, fp8_dtype: str, out, out_t, amax_row, sca
                                     _dptr(out), _dptr(out_t), _dptr(amax_row), _dptr(scale_row),
                                     _dptr(inv_scale_row), _dptr(amax_col), _dptr(scale_col),
                                     _dptr(inv_scale_col), _dptr(skip_if), _stream(stream)))
+
+
+def fp8_quant_groupwise(x: torch.Tensor, fp8_dtype: str, group: int, out, out_t, amax_rg,
+                        scale_rg, inv_rg, amax_cg=None, scale_cg=None, inv_cg=None,
+                        eps: float = 1e-12, skip_if=None, stream=None):
+    """x is [rows, cols]; one scale per `group` elements of a row for out, per
+    `group` rows of a column for out_t ([cols, rows])."""
+    rows, cols = x.shape
+    _check("fp8_quant_groupwise",
+           load().fp8_quant_groupwise(_dptr(x), DT[dtype_name(x)], rows, cols, int(group),
+                                      DT[fp8_dtype], eps, _dptr(out), _dptr(out_t),
+                                      _dptr(amax_rg), _dptr(scale_rg), _dptr(inv_rg),
+                                      _dptr(amax_cg), _dptr(scale_cg), _dptr(inv_cg),
+                                      _dptr(skip_if), _stream(stream)))
 
 
 def fp8_quant_tensorwise_list(x: TensorList, out: TensorList, out_t: TensorList | None,

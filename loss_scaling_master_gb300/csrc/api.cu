@@ -80,7 +80,7 @@ extern "C" {
 
 const char *amp_last_error(void) { return g_err; }
 
-int amp_abi_version(void) { return 8; }
+int amp_abi_version(void) { return 9; }
 
 // A [rows, cols] shape the launch arithmetic can hold: non-negative, each side
 // below 2^48 and rows * cols without int64 overflow.
@@ -527,6 +527,33 @@ amp_status fp8_quant_rowwise(const void *x, amp_dtype x_dtype, int64_t rows, int
                                       static_cast<uint8_t *>(out_t), amax_row, scale_row,
                                       inv_scale_row, amax_col, scale_col, inv_scale_col,
                                       skip_if_dev, dev, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AMP_OK : cuda_fail(e, fn);
+}
+
+amp_status fp8_quant_groupwise(const void *x, amp_dtype x_dtype, int64_t rows, int64_t cols,
+                               int64_t group, amp_dtype fp8_dtype, double eps, void *out,
+                               void *out_t, float *amax_rg, float *scale_rg, float *inv_rg,
+                               float *amax_cg, float *scale_cg, float *inv_cg,
+                               const int32_t *skip_if_dev, amp_stream_t stream) {
+    AMP_TRACE("fp8_quant_groupwise");
+    const char *fn = "fp8_quant_groupwise";
+    if (bad_shape(rows, cols)) return fail(AMP_EINVAL, "%s: negative or too large size", fn);
+    if (group != 32 && group != 64 && group != 128)
+        return fail(AMP_EINVAL, "%s: group must be 32, 64 or 128", fn);
+    if (rows * cols > 0 && (!x || !out || !amax_rg || !scale_rg || !inv_rg))
+        return fail(AMP_EINVAL, "%s: NULL x / out / row-group outputs", fn);
+    if (out_t && rows * cols > 0 && (!amax_cg || !scale_cg || !inv_cg))
+        return fail(AMP_EINVAL, "%s: out_t needs the column-group outputs", fn);
+    if (!(eps > 0.0)) return fail(AMP_EINVAL, "%s: eps must be > 0", fn);
+    const int xc = elem_code(x_dtype), fc = fp8_code(fp8_dtype);
+    if (xc < 0 || fc < 0) return fail(AMP_EDTYPE, "%s: unsupported dtype", fn);
+    const int64_t tiles = ((rows + amp::kTile - 1) / amp::kTile) * ((cols + amp::kTile - 1) / amp::kTile);
+    if (tiles > int64_t(INT32_MAX)) return fail(AMP_EINVAL, "%s: tensor too large", fn);
+    if (rows * cols == 0) return AMP_OK;
+    cudaError_t e = amp::launch_fp8_quant_groupwise(
+        x, xc, rows, cols, group, fc, eps, static_cast<uint8_t *>(out),
+        static_cast<uint8_t *>(out_t), amax_rg, scale_rg, inv_rg, amax_cg, scale_cg, inv_cg,
+        skip_if_dev, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? AMP_OK : cuda_fail(e, fn);
 }
 

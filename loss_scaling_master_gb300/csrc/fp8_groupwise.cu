@@ -1,0 +1,352 @@
+// fp8_groupwise.cu - group-wise FP8 scaling in one pass.
+//
+// "第20章 量化与混合精度训练" §20.5.18: a weight [out, in] is cut into groups
+// of G consecutive elements along `in`, each with its own scale (g128: scales
+// [out, in / 128]).  Each group follows §2 of "FP8训练：量化、自动微分、
+// Torchao" (amax, scale_d = fp8_max / max(double(amax), EPS), clamp, RNE
+// cast).  The column-major copy (§4) feeds the backward GEMM, whose reduction
+// runs along the rows of x, so its groups are G consecutive rows of a column
+// (scales [cols, rows / G]).
+//
+// With G dividing the 128x128 tile, every group lies inside one tile, so one
+// CTA per tile reads x once and finishes everything: group maxima along rows
+// (lane shuffles) and along columns (registers, then shared memory), the
+// scales, the row-major bytes and the transposed bytes (through the swizzled
+// shared tile).  2 bytes read + 1 + 1 written per element, one launch.
+//
+// Scales in fp32.  For a finite amax >= max(EPS, smallest normal) the
+// quotient fp8_max / amax of two fp32 values rounded to fp64 and then to fp32
+// equals its correctly rounded fp32 quotient (double rounding is innocuous
+// for division when the wider format has at least 2p + 2 bits, 53 >= 50), and
+// 1 / scale_d rounded to fp32 equals amax / fp8_max correctly rounded (fp8_max
+// is 7 * 2^k, so amax / fp8_max lies at least 1/14 ulp from any rounding
+// boundary, far beyond the fp64 errors).  Both come from IEEE fp32 divisions;
+// the EPS floor, infinity and NaN go through the fp64 formula.
+#include <algorithm>
+
+#include "fp8_tile.cuh"
+#include "internal.h"
+#include "pdl.cuh"
+
+namespace amp {
+namespace {
+
+// scale and inverse of one group from its amax (see the header comment)
+__device__ __forceinline__ void group_scale(float amax, double eps, float fmax, float &s32,
+                                            float &inv) {
+    if (amax >= 1.17549435e-38f && double(amax) >= eps && amax <= 3.40282347e38f) {
+        s32 = __fdiv_rn(fmax, amax);
+        inv = __fdiv_rn(amax, fmax);
+    } else {
+        tensor_scale(amax, eps, fmax, s32, inv);
+    }
+}
+
+template <int XT>
+__device__ __forceinline__ float elem_f32(const void *x, int64_t k) {
+    if (XT == kF32) return static_cast<const float *>(x)[k];
+    return lowp_to_f32<XT>(static_cast<const uint16_t *>(x)[k]);
+}
+
+template <int XT>
+__device__ __forceinline__ uint32_t elem_abs_bits(const void *x, int64_t k) {
+    return __float_as_uint(elem_f32<XT>(x, k)) & 0x7FFFFFFFu;
+}
+
+// 8 consecutive elements held in one (16-bit) or two (fp32) 16-byte words
+template <int XT>
+__device__ __forceinline__ void words_to_f32(const uint4 *u, float (&y)[8]) {
+    if (XT == kF32) {
+        const uint32_t w[8] = {u[0].x, u[0].y, u[0].z, u[0].w, u[1].x, u[1].y, u[1].z, u[1].w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) y[j] = __uint_as_float(w[j]);
+    } else {
+        const uint32_t w[4] = {u[0].x, u[0].y, u[0].z, u[0].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            y[2 * j] = lowp_to_f32<XT>(w[j] & 0xFFFFu);
+            y[2 * j + 1] = lowp_to_f32<XT>(w[j] >> 16);
+        }
+    }
+}
+
+struct GroupOut {
+    uint8_t *out, *out_t;
+    float *amax_rg, *scale_rg, *inv_rg;  // [rows, ngc]
+    float *amax_cg, *scale_cg, *inv_cg;  // [cols, ngr]
+};
+
+// shared memory of one CTA besides the staging buffers
+template <int G>
+struct GroupSmem {
+    static constexpr int NG = kTile / G;
+    uint32_t sm[kTile * 32];                    // fp8 tile for the transpose
+    uint32_t colmax[kThreads / 32][NG][kTile];  // per-warp column-group maxima
+    uint32_t s_rmax[kTile][NG];                 // row-group maxima (bit patterns)
+    float s_rsc[kTile][NG];                     // row-group multipliers
+    float s_csc[NG][kTile];                     // column-group multipliers
+};
+
+// Whether a tile takes the vector path: full, 16-byte rows, aligned outputs.
+__device__ __forceinline__ bool group_tile_fast(const void *x, int64_t rows, int64_t cols,
+                                                int64_t r0, int64_t c0, const GroupOut &o) {
+    return r0 + kTile <= rows && c0 + kTile <= cols && (cols & 7) == 0 && aligned16(x) &&
+           (reinterpret_cast<uintptr_t>(o.out) & 7) == 0 &&
+           (o.out_t == nullptr || ((rows & 15) == 0 && aligned16(o.out_t)));
+}
+
+// One 128x128 tile (one CTA): the vector path, or the element path for tiles
+// on a ragged edge or with sizes/addresses that break 16-byte access.
+template <int XT, int FT, int G>
+__device__ __forceinline__ void group_tile(const void *x, int64_t rows, int64_t cols, int64_t r0,
+                                           int64_t c0, const GroupOut &o, double eps, bool fast,
+                                           GroupSmem<G> &S) {
+    constexpr int NG = kTile / G;  // groups per tile edge
+    constexpr int nw = XT == kF32 ? 2 : 1;
+    uint32_t *sm = S.sm;
+    auto &colmax = S.colmax;
+    auto &s_rmax = S.s_rmax;
+    auto &s_rsc = S.s_rsc;
+    auto &s_csc = S.s_csc;
+    const float fmax = fp8_max<FT>();
+    const int64_t ngc = (cols + G - 1) / G, ngr = (rows + G - 1) / G;
+    const int64_t gc0 = c0 / G, gr0 = r0 / G;  // first group of this tile in each direction
+    uint8_t *out = o.out, *out_t = o.out_t;
+    if (fast) {
+        constexpr int esz = XT == kF32 ? 4 : 2;
+        const int c8 = threadIdx.x & 15, rb = threadIdx.x >> 4;
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        uint4 raw[8][nw];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const char *p = static_cast<const char *>(x) + ((r0 + rb + 16 * k) * cols + c0 + 8 * c8) * esz;
+            raw[k][0] = ld16(p);
+            if (nw == 2) raw[k][nw - 1] = ld16(p + 16);
+        }
+        // |x| bit patterns (an unsigned max of them is the NaN-propagating fp32
+        // max); colg[q][j]: column 8 c8 + j over this thread's rows of group q
+        uint32_t colg[NG][8];
+#pragma unroll
+        for (int q = 0; q < NG; ++q)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) colg[q][j] = 0u;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            float y[8];
+            words_to_f32<XT>(raw[k], y);
+            uint32_t rm = 0;
+            const int q = (16 * k) / G;  // column group of row rb + 16k (rb < 16 <= G)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t a = __float_as_uint(y[j]) & 0x7FFFFFFFu;
+                rm = max(rm, a);
+                colg[q][j] = max(colg[q][j], a);
+            }
+            // the G / 8 lanes holding this row's group of G columns
+#pragma unroll
+            for (int off = G / 16; off > 0; off >>= 1)
+                rm = max(rm, __shfl_xor_sync(0xFFFFFFFFu, rm, off));
+            if ((c8 & (G / 8 - 1)) == 0) s_rmax[rb + 16 * k][(8 * c8) / G] = rm;
+        }
+        if (out_t) {
+            // lanes l and l ^ 16 hold the same columns (row groups 2w and 2w + 1)
+#pragma unroll
+            for (int q = 0; q < NG; ++q)
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    colg[q][j] = max(colg[q][j], __shfl_xor_sync(0xFFFFFFFFu, colg[q][j], 16));
+            if (lane < 16) {
+#pragma unroll
+                for (int q = 0; q < NG; ++q) {
+                    uint4 *d = reinterpret_cast<uint4 *>(&colmax[warp][q][8 * c8]);
+                    d[0] = make_uint4(colg[q][0], colg[q][1], colg[q][2], colg[q][3]);
+                    d[1] = make_uint4(colg[q][4], colg[q][5], colg[q][6], colg[q][7]);
+                }
+            }
+        }
+        __syncthreads();
+        // scales: 128 x NG row groups, and (with the copy) NG x 128 column groups
+        for (int idx = threadIdx.x; idx < kTile * NG; idx += kThreads) {
+            const int r = idx / NG, q = idx % NG;
+            const float a = __uint_as_float(s_rmax[r][q]);
+            float s32, inv;
+            group_scale(a, eps, fmax, s32, inv);
+            s_rsc[r][q] = s32;
+            const int64_t k = (r0 + r) * ngc + gc0 + q;
+            o.amax_rg[k] = a;
+            o.scale_rg[k] = s32;
+            o.inv_rg[k] = inv;
+        }
+        if (out_t) {
+            for (int idx = threadIdx.x; idx < kTile * NG; idx += kThreads) {
+                const int q = idx / kTile, c = idx % kTile;
+                uint32_t m = 0;
+#pragma unroll
+                for (int w = 0; w < kThreads / 32; ++w) m = max(m, colmax[w][q][c]);
+                const float a = __uint_as_float(m);
+                float s32, inv;
+                group_scale(a, eps, fmax, s32, inv);
+                s_csc[q][c] = s32;
+                const int64_t k = (c0 + c) * ngr + gr0 + q;
+                o.amax_cg[k] = a;
+                o.scale_cg[k] = s32;
+                o.inv_cg[k] = inv;
+            }
+        }
+        __syncthreads();
+        const int qc = (8 * c8) / G;  // this thread's row group
+        // the column multipliers of this thread's 8 columns, per column group
+        float csc[NG][8];
+        if (out_t) {
+#pragma unroll
+            for (int q = 0; q < NG; ++q) {
+                const float4 a = *reinterpret_cast<const float4 *>(&s_csc[q][8 * c8]);
+                const float4 b = *reinterpret_cast<const float4 *>(&s_csc[q][8 * c8 + 4]);
+                csc[q][0] = a.x; csc[q][1] = a.y; csc[q][2] = a.z; csc[q][3] = a.w;
+                csc[q][4] = b.x; csc[q][5] = b.y; csc[q][6] = b.z; csc[q][7] = b.w;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int r = rb + 16 * k;
+            float y[8];
+            words_to_f32<XT>(raw[k], y);
+            const float sr = s_rsc[r][qc];
+            uint32_t h[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float a0, a1;
+                mul2_rn(y[2 * j], y[2 * j + 1], sr, sr, a0, a1);
+                h[j] = f32x2_to_fp8x2_raw<FT>(a0, a1);
+            }
+            *reinterpret_cast<uint2 *>(out + (r0 + r) * cols + c0 + 8 * c8) =
+                make_uint2(fp8x4_canonical_nan<FT>(h[0] | (h[1] << 16)),
+                           fp8x4_canonical_nan<FT>(h[2] | (h[3] << 16)));
+            if (out_t) {
+                const int q = (16 * k) / G;
+                uint32_t g[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float b0, b1;
+                    mul2_rn(y[2 * j], y[2 * j + 1], csc[q][2 * j], csc[q][2 * j + 1], b0, b1);
+                    g[j] = f32x2_to_fp8x2_raw<FT>(b0, b1);
+                }
+                *reinterpret_cast<uint2 *>(sm + swz(r, 2 * c8)) =
+                    make_uint2(fp8x4_canonical_nan<FT>(g[0] | (g[1] << 16)),
+                               fp8x4_canonical_nan<FT>(g[2] | (g[3] << 16)));
+            }
+        }
+        if (out_t) {
+            __syncthreads();
+            store_transposed_tile(sm, out_t, rows, r0, c0);
+        }
+    } else {
+        // element path (ragged edge, or sizes/addresses that break 16-byte
+        // access): group maxima through shared-memory atomics, then the cast
+        uint32_t(&rmax)[kTile][NG] = s_rmax;
+        uint32_t *cmax = &colmax[0][0][0];  // [NG][kTile]
+        for (int i = threadIdx.x; i < kTile * NG; i += kThreads) {
+            (&rmax[0][0])[i] = 0u;
+            cmax[i] = 0u;
+        }
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < kTile * kTile; idx += kThreads) {
+            const int ri = idx >> 7, cj = idx & (kTile - 1);
+            const int64_t i = r0 + ri, j = c0 + cj;
+            if (i < rows && j < cols) {
+                const uint32_t v = elem_abs_bits<XT>(x, i * cols + j);
+                atomicMax(&rmax[ri][cj / G], v);
+                atomicMax(&cmax[(ri / G) * kTile + cj], v);
+            }
+        }
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < kTile * NG; idx += kThreads) {
+            const int r = idx / NG, q = idx % NG;
+            if (r0 + r < rows && c0 + q * G < cols) {
+                const float a = __uint_as_float(rmax[r][q]);
+                float s32, inv;
+                group_scale(a, eps, fmax, s32, inv);
+                s_rsc[r][q] = s32;
+                const int64_t k = (r0 + r) * ngc + gc0 + q;
+                o.amax_rg[k] = a;
+                o.scale_rg[k] = s32;
+                o.inv_rg[k] = inv;
+            }
+            const int q2 = idx / kTile, c = idx % kTile;
+            if (out_t && c0 + c < cols && r0 + q2 * G < rows) {
+                const float a = __uint_as_float(cmax[q2 * kTile + c]);
+                float s32, inv;
+                group_scale(a, eps, fmax, s32, inv);
+                s_csc[q2][c] = s32;
+                const int64_t k = (c0 + c) * ngr + gr0 + q2;
+                o.amax_cg[k] = a;
+                o.scale_cg[k] = s32;
+                o.inv_cg[k] = inv;
+            }
+        }
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < kTile * kTile; idx += kThreads) {
+            const int ri = idx >> 7, cj = idx & (kTile - 1);
+            const int64_t i = r0 + ri, j = c0 + cj;
+            if (i < rows && j < cols) {
+                const float v = elem_f32<XT>(x, i * cols + j);
+                out[i * cols + j] = quant1<FT>(v, s_rsc[ri][cj / G]);
+                if (out_t) out_t[j * rows + i] = quant1<FT>(v, s_csc[ri / G][cj]);
+            }
+        }
+    }
+}
+
+template <int XT, int FT, int G>
+__global__ void __launch_bounds__(kThreads) groupwise_kernel(const void *x, int64_t rows,
+                                                             int64_t cols, GroupOut o, double eps,
+                                                             const int32_t *skip_if) {
+    pdl_wait();
+    pdl_trigger();
+    if (skip_if && *skip_if) return;
+    __shared__ __align__(16) GroupSmem<G> S;
+    const int64_t tiles_c = (cols + kTile - 1) / kTile;
+    const int64_t r0 = int64_t(blockIdx.x / tiles_c) * kTile;
+    const int64_t c0 = int64_t(blockIdx.x % tiles_c) * kTile;
+    group_tile<XT, FT, G>(x, rows, cols, r0, c0, o, eps,
+                          group_tile_fast(x, rows, cols, r0, c0, o), S);
+}
+
+template <int XT, int FT, int G>
+cudaError_t launch_group_t(const void *x, int64_t rows, int64_t cols, const GroupOut &o,
+                           double eps, const int32_t *skip_if, cudaStream_t s) {
+    const int64_t tiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
+    if (tiles == 0) return cudaSuccess;
+    return launch_pdl(groupwise_kernel<XT, FT, G>, dim3((unsigned)tiles), dim3(kThreads), 0, s, x,
+                      rows, cols, o, eps, skip_if);
+}
+
+template <int XT, int FT>
+cudaError_t launch_group_g(int64_t group, const void *x, int64_t rows, int64_t cols,
+                           const GroupOut &o, double eps, const int32_t *skip_if, cudaStream_t s) {
+    if (group == 32) return launch_group_t<XT, FT, 32>(x, rows, cols, o, eps, skip_if, s);
+    if (group == 64) return launch_group_t<XT, FT, 64>(x, rows, cols, o, eps, skip_if, s);
+    return launch_group_t<XT, FT, 128>(x, rows, cols, o, eps, skip_if, s);
+}
+
+}  // namespace
+
+cudaError_t launch_fp8_quant_groupwise(const void *x, int xelem, int64_t rows, int64_t cols,
+                                       int64_t group, int fp8, double eps, uint8_t *out,
+                                       uint8_t *out_t, float *amax_rg, float *scale_rg,
+                                       float *inv_rg, float *amax_cg, float *scale_cg,
+                                       float *inv_cg, const int32_t *skip_if, cudaStream_t s) {
+    GroupOut o{out, out_t, amax_rg, scale_rg, inv_rg, amax_cg, scale_cg, inv_cg};
+#define AMP_GW(XT, FT) launch_group_g<XT, FT>(group, x, rows, cols, o, eps, skip_if, s)
+    if (fp8 == kE4M3) {
+        if (xelem == kBF16) return AMP_GW(kBF16, kE4M3);
+        if (xelem == kF16) return AMP_GW(kF16, kE4M3);
+        return AMP_GW(kF32, kE4M3);
+    }
+    if (xelem == kBF16) return AMP_GW(kBF16, kE5M2);
+    if (xelem == kF16) return AMP_GW(kF16, kE5M2);
+    return AMP_GW(kF32, kE5M2);
+#undef AMP_GW
+}
+
+}  // namespace amp

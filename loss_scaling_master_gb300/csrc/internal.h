@@ -105,6 +105,11 @@ cudaError_t launch_adamw_fp8_delayed(const Fp8DelayedLists &L, int gelem, int fp
                                      float *inv_scale, cudaStream_t s);
 
 cudaError_t launch_bounded_wait_selftest(int32_t *err, double limit_s, cudaStream_t s);
+cudaError_t launch_fp8_quant_groupwise(const void *x, int xelem, int64_t rows, int64_t cols,
+                                       int64_t group, int fp8, double eps, uint8_t *out,
+                                       uint8_t *out_t, float *amax_rg, float *scale_rg,
+                                       float *inv_rg, float *amax_cg, float *scale_cg,
+                                       float *inv_cg, const int32_t *skip_if, cudaStream_t s);
 cudaError_t launch_scale_health(const float *scale, float min_scale, int32_t *health, cudaStream_t s);
 
 cudaError_t launch_update_scale_hist(float *scale, int32_t *tracker, int32_t *found_inf,

@@ -1057,3 +1057,75 @@ def test_two_steps_on_two_streams_concurrently(A, dev):
             assert np.array_equal(to_host_bits(st.fp8_t[j].view(torch.uint8)).ravel(), orc.fp8_t[i])
             j += 1
         st.close()
+
+
+# ----------------------------------------------------------- group-wise FP8
+def _run_groupwise(A, dev, xh, xdt, rows, cols, fmt, group, with_t, skip=None, misalign=False):
+    x = _device_views([xh], xdt, dev, misalign)[0].view(rows, cols)
+    ngc, ngr = -(-cols // group), -(-rows // group)
+    o = {"q": torch.full((rows * cols,), 0xA5, dtype=torch.uint8, device=dev)}
+    o.update({k: torch.full((rows * ngc,), -1.0, device=dev) for k in ("amax_rg", "scale_rg", "inv_rg")})
+    if with_t:
+        o["q_t"] = torch.full((rows * cols,), 0x5A, dtype=torch.uint8, device=dev)
+        o.update({k: torch.full((cols * ngr,), -1.0, device=dev) for k in ("amax_cg", "scale_cg", "inv_cg")})
+    sk = None if skip is None else torch.tensor([skip], dtype=torch.int32, device=dev)
+    A.fp8_quant_groupwise(x, fmt, group, o["q"], o.get("q_t"), o["amax_rg"], o["scale_rg"],
+                          o["inv_rg"], o.get("amax_cg"), o.get("scale_cg"), o.get("inv_cg"),
+                          skip_if=sk)
+    return {k: to_host_bits(v) for k, v in o.items()}
+
+
+def _assert_same(got, ref, key):
+    for k in ref:
+        if ref[k].dtype == np.float32:
+            assert np.array_equal(got[k].view(np.uint32), ref[k].view(np.uint32)), (k, key)
+        else:
+            assert np.array_equal(got[k], ref[k]), (k, key)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
+@pytest.mark.parametrize("xdt", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("group", [32, 64, 128])
+def test_fp8_groupwise_parity(A, dev, fmt, xdt, group):
+    rng = np.random.default_rng(120 + group)
+    for rows, cols in FP8_SHAPES:
+        xh = _x_host(rng, rows, cols, xdt)
+        if rows > 3:                       # a zero row: its groups clamp to EPS
+            xh.reshape(rows, cols)[2] = 0
+        for with_t in (True, False):
+            for misalign in ((False, True) if rows * cols > 8 else (False,)):
+                got = _run_groupwise(A, dev, xh, xdt, rows, cols, fmt, group, with_t,
+                                     misalign=misalign)
+                ref = O.fp8_quant_groupwise(xh, xdt, rows, cols, fmt, group, transposed=with_t)
+                _assert_same(got, ref, (rows, cols, with_t, misalign))
+
+
+@pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
+def test_fp8_groupwise_scale_over_many_amax_values(A, dev, fmt):
+    """The kernel forms group scales with fp32 divisions (equal to the fp64
+    recipe rounded to fp32, see its header); check that against the oracle's
+    fp64 formula for 2^16 group maxima spread over every fp32 exponent,
+    subnormals, values around EPS, zero, inf and NaN: each row group of a
+    [2^16, 128] fp32 matrix holds one such value, all else zero."""
+    rng = np.random.default_rng(130)
+    n = 1 << 16
+    bits = rng.integers(0, 0x7F800000, n, dtype=np.uint32)
+    bits[:64] = [0, 1, 0x00400000, 0x007FFFFF, 0x00800000, 0x7F7FFFFF, 0x7F800000, 0x7FC00000] * 8
+    eps = 1e-12
+    near = np.float32(eps).view(np.uint32)
+    bits[64:96] = near + np.arange(-16, 16, dtype=np.int64).astype(np.uint32)
+    vals = bits.view(np.float32)
+    x = np.zeros((n, 128), np.float32)
+    x[np.arange(n), rng.integers(0, 128, n)] = vals * np.where(rng.random(n) < 0.5, -1, 1).astype(np.float32)
+    xh = x.ravel()
+    got = _run_groupwise(A, dev, xh, "f32", n, 128, fmt, 128, True)
+    ref = O.fp8_quant_groupwise(xh, "f32", n, 128, fmt, 128, eps=eps)
+    _assert_same(got, ref, "amax sweep")
+
+
+def test_fp8_groupwise_skip_writes_nothing(A, dev):
+    rng = np.random.default_rng(131)
+    xh = _x_host(rng, 256, 384, "bf16")
+    got = _run_groupwise(A, dev, xh, "bf16", 256, 384, "e4m3fn", 128, True, skip=1)
+    assert np.all(got["q"] == 0xA5) and np.all(got["q_t"] == 0x5A)
+    assert np.all(got["amax_rg"] == -1.0) and np.all(got["inv_cg"] == -1.0)
