@@ -313,7 +313,8 @@ def run_ours(args, rank, world, device):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32 (master/m/v), f16 grads, bf16 + e4m3fn outputs",
+        "dtype": "f32",
+        "storage": "f32 master/m/v, f16 grads in, bf16 + e4m3fn copies out",
         "data": "synthetic (seeded N(0,0.02) masters, N(0,sigma*S) fp16 grads; no trained weights)",
         "config": dict(workload_config(args.workload, world), per_step_bytes=total_bytes),
         "hbm_gbs_step": total_bytes / (ms_step * 1e-3) / 1e9,
@@ -512,7 +513,8 @@ def run_fp8_sweep(args, rank, world, device):
     return {"metric": f"FP8 {gran} quant GB/s (amax + e4m3fn/e5m2 cast + transposed copy)",
             "value": gbs * world, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, fp8 out",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "storage": "bf16 in, e4m3fn/e5m2 out",
             "data": "synthetic N(0,1) bf16 + one all-zero matrix",
             "config": {"workload": "fp8_sweep [4096,4096],[8192,8192],[16384,5120],zero[4096,4096] "
                                    "x {e4m3fn,e5m2}", "l2": "flushed between steps"},
@@ -587,7 +589,8 @@ def run_reference(args, rank, world):
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "params/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32 (master/m/v), f16 grads, bf16 + e4m3fn outputs",
+            "vs_baseline": None, "dtype": "f32",
+            "storage": "f32 master/m/v, f16 grads in, bf16 + e4m3fn copies out",
             "data": "synthetic", "config": workload_config(args.workload, world),
             "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
