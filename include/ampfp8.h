@@ -38,6 +38,12 @@
  *   - Pointers need no particular alignment: tensors whose addresses allow
  *     16-byte vector access take the vector path, others a scalar path that
  *     gives the same bits.
+ *   - Kernels are launched as programmatic dependent launches: a kernel may
+ *     be scheduled while the one before it in the stream drains, but waits
+ *     (griddepcontrol.wait) for that kernel to complete before it touches
+ *     memory, so results are those of plain stream order.  Other work on the
+ *     stream, before or after, runs in plain stream order.
+ *   - Every call opens an NVTX range named after itself, for profilers.
  */
 #ifndef AMPFP8_H
 #define AMPFP8_H
