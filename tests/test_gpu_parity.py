@@ -1129,3 +1129,67 @@ def test_fp8_groupwise_skip_writes_nothing(A, dev):
     got = _run_groupwise(A, dev, xh, "bf16", 256, 384, "e4m3fn", 128, True, skip=1)
     assert np.all(got["q"] == 0xA5) and np.all(got["q_t"] == 0x5A)
     assert np.all(got["amax_rg"] == -1.0) and np.all(got["inv_cg"] == -1.0)
+
+
+def test_many_tensors_in_one_list(A, dev):
+    """3000 tensors (sizes 0..40 plus a few over a chunk) in one list through
+    the check and the AdamW step: the per-list tables of a large ragged list."""
+    rng = np.random.default_rng(140)
+    sizes = list(rng.integers(0, 41, 3000))
+    sizes[100], sizes[2000] = 16385, 40001
+    master_h = [(rng.standard_normal(k) * 0.02).astype(np.float32) for k in sizes]
+    P = _device_views(master_h, "f32", dev, True)
+    M = _device_views([np.zeros(k, np.float32) for k in sizes], "f32", dev, True)
+    V = _device_views([np.zeros(k, np.float32) for k in sizes], "f32", dev, True)
+    gh = _grads_host(rng, sizes, "bf16", sigma=1e-3)
+    G = _device_views(gh, "bf16", dev, True)
+    B = _device_views([np.zeros(k, np.uint16) for k in sizes], "bf16", dev, True)
+    Ls = [A.amp_tensor_list_create(x) for x in (P, M, V, G, B)]
+    fi = torch.zeros(1, dtype=torch.int32, device=dev)
+    step = torch.zeros(1, dtype=torch.int32, device=dev)
+    A.amp_unscale_check(Ls[3], None, fi)
+    assert int(fi.item()) == O.unscale_check([h.copy() for h in gh], "bf16", 1.0) == 0
+    A.amp_adamw_master_step(*Ls, None, fi, step, 1e-3, 0.9, 0.95, 1e-8, 0.1)
+    rp = [x.copy() for x in master_h]
+    rm = [np.zeros(k, np.float32) for k in sizes]
+    rv = [np.zeros(k, np.float32) for k in sizes]
+    rb = [np.zeros(k, np.uint16) for k in sizes]
+    O.adamw_master_step(rp, rm, rv, gh, "bf16", rb, None, 0, 0, 1e-3, 0.9, 0.95, 1e-8, 0.1)
+    torch.cuda.synchronize()
+    for i in range(len(sizes)):
+        assert np.array_equal(to_host_bits(P[i]).view(np.uint32), rp[i].view(np.uint32)), i
+        assert np.array_equal(to_host_bits(B[i]), rb[i]), i
+    for L in Ls:
+        L.close()
+
+
+def test_amax_fold_propagates_nan_and_inf(A, dev):
+    """The amax the AdamW pass folds from the bf16 copy: a NaN master makes the
+    slot NaN, an infinite one makes it inf, as the oracle's max does."""
+    sizes = [5000, 5000, 5000]
+    master_h = [np.full(k, 0.5, np.float32) for k in sizes]
+    master_h[0][1234] = np.nan
+    master_h[1][4999] = np.inf
+    P = _device_views(master_h, "f32", dev, False)
+    M = _device_views([np.zeros(k, np.float32) for k in sizes], "f32", dev, False)
+    V = _device_views([np.zeros(k, np.float32) for k in sizes], "f32", dev, False)
+    gh = [np.zeros(k, np.uint16) for k in sizes]
+    G = _device_views(gh, "f16", dev, False)
+    B = _device_views([np.zeros(k, np.uint16) for k in sizes], "bf16", dev, False)
+    Ls = [A.amp_tensor_list_create(x) for x in (P, M, V, G, B)]
+    A.amp_tensor_list_set_amax_slots(Ls[4], [0, 1, 2])
+    amax = torch.zeros(3, device=dev)
+    step = torch.zeros(1, dtype=torch.int32, device=dev)
+    A.amp_adamw_master_step(*Ls, None, None, step, 1e-3, 0.9, 0.999, 1e-8, 0.0, amax=amax)
+    ram = np.zeros(3, np.float32)
+    rp = [x.copy() for x in master_h]
+    O.adamw_master_step(rp, [np.zeros(k, np.float32) for k in sizes],
+                        [np.zeros(k, np.float32) for k in sizes], gh, "f16",
+                        [np.zeros(k, np.uint16) for k in sizes], None, 0, 0, 1e-3, 0.9, 0.999,
+                        1e-8, 0.0, amax_slot=[0, 1, 2], amax=ram)
+    got = to_host_bits(amax)
+    assert np.isnan(got[0]) and np.isnan(ram[0])
+    assert got[1] == ram[1] == np.inf
+    assert got[2] == ram[2]
+    for L in Ls:
+        L.close()
