@@ -403,7 +403,7 @@ struct Fp8StepParams {
 // FP8 tensors' scales from their amax histories (NaN propagating max).
 __global__ void adamw_fp8_prologue_kernel(const int32_t *found_inf, int32_t *step, double lr,
                                           double beta1, double beta2, AdamwStepScalars *out,
-                                          const float *hist, int hist_len, int n8, double eps,
+                                          const float *hist, int hist_len, int n8, EpsFloor ef,
                                           float fmax, float *tscale, float *inv_scale) {
     pdl_wait();
     pdl_trigger();
@@ -416,7 +416,7 @@ __global__ void adamw_fp8_prologue_kernel(const int32_t *found_inf, int32_t *ste
         float a = h[0];
         for (int k = 1; k < hist_len; ++k) a = (a != a || h[k] != h[k]) ? __int_as_float(0x7FC00000) : fmaxf(a, h[k]);
         float s32, inv;
-        tensor_scale(a, eps, fmax, s32, inv);
+        tensor_scale(a, ef, fmax, s32, inv);
         tscale[j] = s32;
         inv_scale[j] = inv;
     }
@@ -589,7 +589,8 @@ cudaError_t launch_adamw_fp8_delayed(const Fp8DelayedLists &L, int gelem, int fp
                                      float *inv_scale, cudaStream_t s) {
     const float fmax = fp8 == kE4M3 ? fp8_max<kE4M3>() : fp8_max<kE5M2>();
     launch_pdl(adamw_fp8_prologue_kernel, dim3(1), dim3(256), 0, s, found_inf, step, c.lr, c.beta1,
-               c.beta2, scal, hist, hist_len, L.n8, eps, fmax, L.tscale, inv_scale);
+               c.beta2, scal, hist, hist_len, L.n8, make_eps_floor(eps, fmax), fmax, L.tscale,
+               inv_scale);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (L.n_plain_chunks > 0) {

@@ -14,17 +14,9 @@
 // scales, the row-major bytes and the transposed bytes (through the swizzled
 // shared tile).  2 bytes read + 1 + 1 written per element, one launch.
 //
-// Scales in fp32.  For amax >= EPS the quotient fp8_max / amax of two fp32
-// values rounded to fp64 and then to fp32 equals its correctly rounded fp32
-// quotient (double rounding is innocuous for division when the wider format
-// has at least 2p + 2 bits, 53 >= 50), and 1 / scale_d rounded to fp32 equals
-// amax / fp8_max correctly rounded (fp8_max is 7 * 2^k, so amax / fp8_max lies
-// at least 1/14 ulp from any rounding boundary, far beyond the fp64 errors).
-// Both come from IEEE fp32 divisions (inf and NaN included; a NaN result is
-// the division's NaN); the EPS floor's two values are formed once on the host
-// in fp64, so no fp64 arithmetic runs on the device.
+// The scales come from tensor_scale (fp8_tile.cuh): fp32 divisions equal to
+// §2's fp64 formula rounded to fp32.
 #include <algorithm>
-#include <cmath>
 
 #include "fp8_tile.cuh"
 #include "internal.h"
@@ -32,26 +24,6 @@
 
 namespace amp {
 namespace {
-
-// The EPS floor, prepared on the host: eps32 is the smallest fp32 value not
-// below eps (so amax < eps32 exactly when double(amax) < eps); s_eps and
-// inv_eps are float(fp8_max / eps) and float(1 / (fp8_max / eps)) from fp64.
-struct EpsFloor {
-    float eps32, s_eps, inv_eps;
-};
-
-// scale and inverse of one group from its amax (see the header comment):
-// IEEE fp32 divisions, or the EPS floor; inf gives 0 and inf, NaN gives NaN
-__device__ __forceinline__ void group_scale(float amax, const EpsFloor &e, float fmax, float &s32,
-                                            float &inv) {
-    if (amax < e.eps32) {
-        s32 = e.s_eps;
-        inv = e.inv_eps;
-    } else {
-        s32 = __fdiv_rn(fmax, amax);
-        inv = __fdiv_rn(amax, fmax);
-    }
-}
 
 template <int XT>
 __device__ __forceinline__ float elem_f32(const void *x, int64_t k) {
@@ -181,7 +153,7 @@ __device__ __forceinline__ void group_tile(const void *x, int64_t rows, int64_t 
             const int r = idx / NG, q = idx % NG;
             const float a = __uint_as_float(s_rmax[r][q]);
             float s32, inv;
-            group_scale(a, ef, fmax, s32, inv);
+            tensor_scale(a, ef, fmax, s32, inv);
             s_rsc[r][q] = s32;
             const int64_t k = (r0 + r) * ngc + gc0 + q;
             o.amax_rg[k] = a;
@@ -196,7 +168,7 @@ __device__ __forceinline__ void group_tile(const void *x, int64_t rows, int64_t 
                 for (int w = 0; w < kThreads / 32; ++w) m = max(m, colmax[w][q][c]);
                 const float a = __uint_as_float(m);
                 float s32, inv;
-                group_scale(a, ef, fmax, s32, inv);
+                tensor_scale(a, ef, fmax, s32, inv);
                 s_csc[q][c] = s32;
                 const int64_t k = (c0 + c) * ngr + gr0 + q;
                 o.amax_cg[k] = a;
@@ -276,7 +248,7 @@ __device__ __forceinline__ void group_tile(const void *x, int64_t rows, int64_t 
             if (r0 + r < rows && c0 + q * G < cols) {
                 const float a = __uint_as_float(rmax[r][q]);
                 float s32, inv;
-                group_scale(a, ef, fmax, s32, inv);
+                tensor_scale(a, ef, fmax, s32, inv);
                 s_rsc[r][q] = s32;
                 const int64_t k = (r0 + r) * ngc + gc0 + q;
                 o.amax_rg[k] = a;
@@ -287,7 +259,7 @@ __device__ __forceinline__ void group_tile(const void *x, int64_t rows, int64_t 
             if (out_t && c0 + c < cols && r0 + q2 * G < rows) {
                 const float a = __uint_as_float(cmax[q2 * kTile + c]);
                 float s32, inv;
-                group_scale(a, ef, fmax, s32, inv);
+                tensor_scale(a, ef, fmax, s32, inv);
                 s_csc[q2][c] = s32;
                 const int64_t k = (c0 + c) * ngr + gr0 + q2;
                 o.amax_cg[k] = a;
@@ -328,12 +300,7 @@ cudaError_t launch_group_t(const void *x, int64_t rows, int64_t cols, const Grou
                            double eps, const int32_t *skip_if, cudaStream_t s) {
     const int64_t tiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
     if (tiles == 0) return cudaSuccess;
-    EpsFloor ef;
-    ef.eps32 = float(eps);
-    if (double(ef.eps32) < eps) ef.eps32 = std::nextafter(ef.eps32, INFINITY);
-    const double sd = double(fp8_max<FT>()) / eps;
-    ef.s_eps = float(sd);
-    ef.inv_eps = float(1.0 / sd);
+    const EpsFloor ef = make_eps_floor(eps, fp8_max<FT>());
     return launch_pdl(groupwise_kernel<XT, FT, G>, dim3((unsigned)tiles), dim3(kThreads), 0, s, x,
                       rows, cols, o, ef, skip_if);
 }

@@ -107,7 +107,7 @@ template <int XT, int FT>
 __global__ void __launch_bounds__(kThreads) quant_single_kernel(const void *x, int64_t rows,
                                                                 int64_t cols, uint8_t *out,
                                                                 uint8_t *out_t, const float *amax,
-                                                                float *inv_scale, double eps,
+                                                                float *inv_scale, EpsFloor ef,
                                                                 const int32_t *skip_if) {
     pdl_wait();
     pdl_trigger();
@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(kThreads) quant_single_kernel(const void *x, i
     const int64_t tr = blockIdx.x / tiles_c, tc = blockIdx.x % tiles_c;
     if (threadIdx.x == 0) {
         float s32, inv;
-        tensor_scale(*amax, eps, fp8_max<FT>(), s32, inv);
+        tensor_scale(*amax, ef, fp8_max<FT>(), s32, inv);
         s_scale = s32;
         if (blockIdx.x == 0) *inv_scale = inv;
     }
@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(kThreads) quant_single_kernel(const void *x, i
 template <int XT, int FT>
 __global__ void __launch_bounds__(kThreads) quant_list_kernel(ListView X, ListView O, ListView OT,
                                                               int has_t, const float *amax,
-                                                              float *inv_scale, double eps,
+                                                              float *inv_scale, EpsFloor ef,
                                                               const int32_t *skip_if) {
     pdl_wait();
     pdl_trigger();
@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kThreads) quant_list_kernel(ListView X, ListVi
     const int64_t tr = tl.y / tiles_c, tc = tl.y % tiles_c;
     if (threadIdx.x == 0) {
         float s32, inv;
-        tensor_scale(amax[t], eps, fp8_max<FT>(), s32, inv);
+        tensor_scale(amax[t], ef, fp8_max<FT>(), s32, inv);
         s_scale = s32;
         if (tl.y == 0) inv_scale[t] = inv;
     }
@@ -155,14 +155,14 @@ __global__ void __launch_bounds__(kThreads) quant_list_kernel(ListView X, ListVi
 // visits them; their inv_scale still follows from their amax like any other's.
 template <int FT>
 __global__ void quant_list_empty_kernel(ListView X, const float *amax, float *inv_scale,
-                                        double eps, const int32_t *skip_if) {
+                                        EpsFloor ef, const int32_t *skip_if) {
     pdl_wait();
     pdl_trigger();
     if (skip_if && *skip_if) return;
     for (int t = threadIdx.x; t < X.n; t += blockDim.x) {
         if (X.numel[t] != 0) continue;
         float s32, inv;
-        tensor_scale(amax[t], eps, fp8_max<FT>(), s32, inv);
+        tensor_scale(amax[t], ef, fp8_max<FT>(), s32, inv);
         inv_scale[t] = inv;
     }
 }
@@ -236,14 +236,14 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const void *x, int64_t n
     }
 }
 
-__global__ void quant_empty_kernel(float *amax, int amax_given, float *inv_scale, double eps,
+__global__ void quant_empty_kernel(float *amax, int amax_given, float *inv_scale, EpsFloor ef,
                                    float fmax, const int32_t *skip_if) {
     pdl_wait();
     pdl_trigger();
     if (skip_if && *skip_if) return;
     if (!amax_given) *amax = 0.0f;
     float s32, inv;
-    tensor_scale(*amax, eps, fmax, s32, inv);
+    tensor_scale(*amax, ef, fmax, s32, inv);
     *inv_scale = inv;
 }
 
@@ -265,8 +265,8 @@ cudaError_t launch_single(const void *x, int64_t rows, int64_t cols, uint8_t *ou
     }
     const int64_t tiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
     return launch_pdl(quant_single_kernel<XT, FT>, dim3(unsigned(tiles)), dim3(kThreads), 0, s, x,
-                      rows, cols, out, out_t, static_cast<const float *>(amax), inv_scale, eps,
-                      skip_if);
+                      rows, cols, out, out_t, static_cast<const float *>(amax), inv_scale,
+                      make_eps_floor(eps, fp8_max<FT>()), skip_if);
 }
 
 }  // namespace
@@ -276,8 +276,9 @@ cudaError_t launch_fp8_quant(const void *x, int xelem, int64_t rows, int64_t col
                              float *amax, int amax_given, const int32_t *skip_if, int device,
                              cudaStream_t s) {
     if (rows * cols == 0) {
+        const float fmax = fp8 == kE4M3 ? fp8_max<kE4M3>() : fp8_max<kE5M2>();
         return launch_pdl(quant_empty_kernel, dim3(1), dim3(1), 0, s, amax, amax_given, inv_scale,
-                          eps, fp8 == kE4M3 ? fp8_max<kE4M3>() : fp8_max<kE5M2>(), skip_if);
+                          make_eps_floor(eps, fmax), fmax, skip_if);
     }
 #define AMP_Q1(XT, FT) \
     launch_single<XT, FT>(x, rows, cols, out, out_t, inv_scale, amax, amax_given, eps, skip_if, \
@@ -299,9 +300,10 @@ cudaError_t launch_fp8_quant_list(const ListView &x, int64_t n_tiles, bool any_e
                                   const int32_t *skip_if, cudaStream_t s) {
     if (any_empty) {
         if (fp8 == kE4M3) launch_pdl(quant_list_empty_kernel<kE4M3>, dim3(1), dim3(kThreads), 0, s,
-                                     x, amax, inv_scale, eps, skip_if);
+                                     x, amax, inv_scale, make_eps_floor(eps, fp8_max<kE4M3>()),
+                                     skip_if);
         else launch_pdl(quant_list_empty_kernel<kE5M2>, dim3(1), dim3(kThreads), 0, s, x, amax,
-                        inv_scale, eps, skip_if);
+                        inv_scale, make_eps_floor(eps, fp8_max<kE5M2>()), skip_if);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -309,9 +311,10 @@ cudaError_t launch_fp8_quant_list(const ListView &x, int64_t n_tiles, bool any_e
     const ListView ot = out_t ? *out_t : ListView{};
     const int has_t = out_t != nullptr;
     const dim3 grid((unsigned)n_tiles), block(kThreads);
+    const EpsFloor ef = make_eps_floor(eps, fp8 == kE4M3 ? fp8_max<kE4M3>() : fp8_max<kE5M2>());
 #define AMP_QL(XT, FT)                                                                    \
     launch_pdl(quant_list_kernel<XT, FT>, grid, block, 0, s, x, out, ot, has_t, amax, inv_scale, \
-               eps, skip_if)
+               ef, skip_if)
     if (fp8 == kE4M3) {
         if (xelem == kBF16) AMP_QL(kBF16, kE4M3);
         else if (xelem == kF16) AMP_QL(kF16, kE4M3);

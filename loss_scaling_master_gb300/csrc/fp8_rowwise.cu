@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kThreads) rowcol_amax_kernel(const void *x, in
 
 __global__ void rowcol_scale_kernel(const float *amax_row, float *scale_row, float *inv_row,
                                     int64_t rows, const float *amax_col, float *scale_col,
-                                    float *inv_col, int64_t cols, double eps, float fmax,
+                                    float *inv_col, int64_t cols, EpsFloor ef, float fmax,
                                     const int32_t *skip_if) {
     pdl_wait();
     pdl_trigger();
@@ -225,10 +225,10 @@ __global__ void rowcol_scale_kernel(const float *amax_row, float *scale_row, flo
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < rows + cols;
          i += int64_t(gridDim.x) * blockDim.x) {
         if (i < rows) {
-            tensor_scale(amax_row[i], eps, fmax, scale_row[i], inv_row[i]);
+            tensor_scale(amax_row[i], ef, fmax, scale_row[i], inv_row[i]);
         } else if (amax_col) {
             const int64_t j = i - rows;
-            tensor_scale(amax_col[j], eps, fmax, scale_col[j], inv_col[j]);
+            tensor_scale(amax_col[j], ef, fmax, scale_col[j], inv_col[j]);
         }
     }
 }
@@ -341,7 +341,8 @@ cudaError_t launch_rowwise_t(const void *x, int64_t rows, int64_t cols, uint8_t 
     e = launch_pdl(rowcol_scale_kernel, dim3(small_grid), dim3(256), 0, s,
                    static_cast<const float *>(amax_row), scale_row, inv_row, rows,
                    static_cast<const float *>(acol), scale_col, inv_col,
-                   int64_t(out_t ? cols : 0), eps, fp8_max<FT>(), skip_if);
+                   int64_t(out_t ? cols : 0), make_eps_floor(eps, fp8_max<FT>()), fp8_max<FT>(),
+                   skip_if);
     if (e != cudaSuccess) return e;
     return launch_pdl(rowcol_cast_kernel<XT, FT>, dim3((unsigned)tiles), dim3(kThreads), 0, s, x,
                       rows, cols, out, out_t, static_cast<const float *>(scale_row),

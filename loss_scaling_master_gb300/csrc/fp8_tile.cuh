@@ -3,19 +3,50 @@
 // §2 scale and cast, §4 column-major copy).
 #pragma once
 
+#include <cmath>
+
 #include "common.cuh"
 
 namespace amp {
 
-// scale_d = fp8_max / max(double(amax), eps), NaN propagating; the cast uses
-// scale_d rounded to fp32, inv_scale is 1/scale_d rounded to fp32.
-__device__ __forceinline__ void tensor_scale(float amax, double eps, float fmax, float &s32,
+// §2's scale: scale_d = fp8_max / max(double(amax), eps) in fp64, NaN
+// propagating; the cast uses scale_d rounded to fp32 and inv_scale is
+// 1 / scale_d rounded to fp32.  Both are formed with IEEE fp32 divisions,
+// which give the same values:
+//   - for amax >= eps, fp8_max / amax rounded to fp64 and then to fp32 equals
+//     the correctly rounded fp32 quotient (double rounding is innocuous for
+//     division when the wider format has at least 2p + 2 bits: 53 >= 50);
+//   - 1 / scale_d rounded to fp32 equals amax / fp8_max correctly rounded:
+//     fp8_max = 7 * 2^k, so amax / fp8_max lies at least 1/14 ulp from any
+//     fp32 rounding boundary, far beyond the two fp64 rounding errors;
+//   - amax = inf gives 0 and inf, NaN gives NaN (a NaN's payload is open).
+// The EPS floor (amax < eps) takes two constants formed once on the host in
+// fp64, so no fp64 arithmetic runs on the device.
+struct EpsFloor {
+    float eps32;   // the smallest fp32 value not below eps: amax < eps32 <=> double(amax) < eps
+    float s_eps;   // float(fp8_max / eps)
+    float inv_eps; // float(1 / (fp8_max / eps))
+};
+
+inline EpsFloor make_eps_floor(double eps, float fmax) {
+    EpsFloor e;
+    e.eps32 = float(eps);
+    if (double(e.eps32) < eps) e.eps32 = std::nextafter(e.eps32, INFINITY);
+    const double sd = double(fmax) / eps;
+    e.s_eps = float(sd);
+    e.inv_eps = float(1.0 / sd);
+    return e;
+}
+
+__device__ __forceinline__ void tensor_scale(float amax, const EpsFloor &e, float fmax, float &s32,
                                              float &inv) {
-    const double a = double(amax);
-    const double cl = (a != a) ? a : (a < eps ? eps : a);
-    const double sd = double(fmax) / cl;
-    s32 = float(sd);
-    inv = float(1.0 / sd);
+    if (amax < e.eps32) {
+        s32 = e.s_eps;
+        inv = e.inv_eps;
+    } else {
+        s32 = __fdiv_rn(fmax, amax);
+        inv = __fdiv_rn(amax, fmax);
+    }
 }
 
 template <int FT>
