@@ -430,9 +430,11 @@ def test_amp_step_composition_with_fp8(A, dev, fmt):
     st.close()
 
 
-def test_graph_replay_matches_eager(A, dev):
-    """The step captured once in a CUDA graph and replayed gives the same
-    bits as the eager calls, including a skipped step."""
+@pytest.mark.parametrize("mode", ["dynamic", "delayed", "clip", "sr", "health"])
+def test_graph_replay_matches_eager(A, dev, mode):
+    """The step captured once in a CUDA graph (with its programmatic launch
+    edges) and replayed gives the same bits as the eager calls, including a
+    skipped step, for every form of the step."""
     from loss_scaling_master_gb300 import AmpOptimizerStep
     rng = np.random.default_rng(41)
     shapes = [(128, 256), (777,), (256, 384)]
@@ -440,10 +442,14 @@ def test_graph_replay_matches_eager(A, dev):
     sizes = [int(np.prod(s)) for s in shapes]
     master = [(rng.standard_normal(n) * 0.02).astype(np.float32) for n in sizes]
     hyper = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+    opts = {"dynamic": {}, "delayed": {"fp8_scaling": "delayed", "amax_history_len": 2},
+            "clip": {"max_norm": 0.05}, "sr": {"sr_seed": 77, "fp8_shapes": None},
+            "health": {"min_scale": 600.0}}[mode]
+    kw = dict(fp8_shapes=fp8_shapes)
+    kw.update(opts)
     mk = lambda: AmpOptimizerStep([torch.from_numpy(m.copy()).to(dev) for m in master],
                                   [torch.empty(n, dtype=torch.float16, device=dev) for n in sizes],
-                                  init_scale=1024.0, growth_interval=3, fp8_shapes=fp8_shapes,
-                                  **hyper)
+                                  init_scale=1024.0, growth_interval=3, **kw, **hyper)
     eager, graphed = mk(), mk()
     graphed.capture_graph()
     for k in range(6):
@@ -463,7 +469,10 @@ def test_graph_replay_matches_eager(A, dev):
                            b.view(torch.int16 if b.element_size() == 2 else torch.int32))
     for a, b in zip(eager.fp8 + eager.fp8_t, graphed.fp8 + graphed.fp8_t):
         assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
-    assert torch.equal(eager.inv_scale, graphed.inv_scale)
+    if eager.n_fp8:
+        assert torch.equal(eager.inv_scale, graphed.inv_scale)
+    if mode == "health":
+        assert eager.health() == graphed.health() == 2       # 1024 halved below 600 at the skip
     eager.close()
     graphed.close()
 
