@@ -83,7 +83,7 @@ __device__ __forceinline__ bool group_tile_fast(const void *x, int64_t rows, int
 template <int XT, int FT, int G>
 __device__ __forceinline__ void group_tile(const void *x, int64_t rows, int64_t cols, int64_t r0,
                                            int64_t c0, const GroupOut &o, const EpsFloor &ef,
-                                           bool fast, GroupSmem<G> &S) {
+                                           bool fast, GroupSmem<G> &S, uint4 *stage) {
     constexpr int NG = kTile / G;  // groups per tile edge
     constexpr int nw = XT == kF32 ? 2 : 1;
     uint32_t *sm = S.sm;
@@ -99,13 +99,22 @@ __device__ __forceinline__ void group_tile(const void *x, int64_t rows, int64_t 
         constexpr int esz = XT == kF32 ? 4 : 2;
         const int c8 = threadIdx.x & 15, rb = threadIdx.x >> 4;
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-        uint4 raw[8][nw];
+        // the tile goes to this thread's own staging slots with asynchronous
+        // copies, so no registers are held while the loads are in flight and
+        // the cast pass reads the data again from shared memory
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const char *p = static_cast<const char *>(x) + ((r0 + rb + 16 * k) * cols + c0 + 8 * c8) * esz;
-            raw[k][0] = ld16(p);
-            if (nw == 2) raw[k][nw - 1] = ld16(p + 16);
+#pragma unroll
+            for (int u = 0; u < nw; ++u) {
+                const uint32_t d = static_cast<uint32_t>(
+                    __cvta_generic_to_shared(stage + (k * kThreads + threadIdx.x) * nw + u));
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(p + 16 * u)
+                             : "memory");
+            }
         }
+        asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+        auto raw = [&](int k) { return stage + (k * kThreads + threadIdx.x) * nw; };
         // |x| bit patterns (an unsigned max of them is the NaN-propagating fp32
         // max); colg[q][j]: column 8 c8 + j over this thread's rows of group q
         uint32_t colg[NG][8];
@@ -116,7 +125,7 @@ __device__ __forceinline__ void group_tile(const void *x, int64_t rows, int64_t 
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             float y[8];
-            words_to_f32<XT>(raw[k], y);
+            words_to_f32<XT>(raw(k), y);
             uint32_t rm = 0;
             const int q = (16 * k) / G;  // column group of row rb + 16k (rb < 16 <= G)
 #pragma unroll
@@ -193,7 +202,7 @@ __device__ __forceinline__ void group_tile(const void *x, int64_t rows, int64_t 
         for (int k = 0; k < 8; ++k) {
             const int r = rb + 16 * k;
             float y[8];
-            words_to_f32<XT>(raw[k], y);
+            words_to_f32<XT>(raw(k), y);
             const float sr = s_rsc[r][qc];
             uint32_t h[4];
 #pragma unroll
@@ -288,11 +297,12 @@ __global__ void __launch_bounds__(kThreads) groupwise_kernel(const void *x, int6
     pdl_trigger();
     if (skip_if && *skip_if) return;
     __shared__ __align__(16) GroupSmem<G> S;
+    extern __shared__ __align__(16) uint4 stage[];  // the tile of x: 128 x 128 elements
     const int64_t tiles_c = (cols + kTile - 1) / kTile;
     const int64_t r0 = int64_t(blockIdx.x / tiles_c) * kTile;
     const int64_t c0 = int64_t(blockIdx.x % tiles_c) * kTile;
     group_tile<XT, FT, G>(x, rows, cols, r0, c0, o, ef,
-                          group_tile_fast(x, rows, cols, r0, c0, o), S);
+                          group_tile_fast(x, rows, cols, r0, c0, o), S, stage);
 }
 
 template <int XT, int FT, int G>
@@ -301,8 +311,11 @@ cudaError_t launch_group_t(const void *x, int64_t rows, int64_t cols, const Grou
     const int64_t tiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
     if (tiles == 0) return cudaSuccess;
     const EpsFloor ef = make_eps_floor(eps, fp8_max<FT>());
-    return launch_pdl(groupwise_kernel<XT, FT, G>, dim3((unsigned)tiles), dim3(kThreads), 0, s, x,
-                      rows, cols, o, ef, skip_if);
+    constexpr int smem = kTile * kTile * (XT == kF32 ? 4 : 2);
+    cudaFuncSetAttribute(groupwise_kernel<XT, FT, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         smem);
+    return launch_pdl(groupwise_kernel<XT, FT, G>, dim3((unsigned)tiles), dim3(kThreads), smem, s,
+                      x, rows, cols, o, ef, skip_if);
 }
 
 template <int XT, int FT>
