@@ -77,7 +77,13 @@ typedef enum {
 } amp_dtype;
 
 /* ------------------------------------------------------------------------ */
-/* Tensor lists                                                              */
+/* Tensor lists.  The pages run every step over the list of a model's        */
+/* parameters or gradients ([CH20] §20.2.2: the scaler unscales "all"        */
+/* gradients; [NOTES] §4 and [MP06] §四 per-tensor loops); a handle is that   */
+/* list on the device.  Its layout has no counterpart on the pages.           */
+/* Sources: [CH20] "第20章 量化与混合精度训练", [FP8] "FP8训练：量化、自动微分、 */
+/* Torchao", [MP] "从 AMP 到 Mixed Precision：训练和推理为什么不使用同一种精度", */
+/* [NOTES] "AMP：Automatic Mixed Precision 技术笔记", [MP06] "06 · 混合精度".    */
 /* ------------------------------------------------------------------------ */
 
 /* Opaque handle describing a ragged list of n contiguous device tensors of
@@ -477,10 +483,12 @@ amp_status amp_read_state(const float *scale_dev, const int32_t *growth_tracker_
 amp_status amp_scale_health(const float *scale_dev, float min_scale, int32_t *health_dev,
                             amp_stream_t stream);
 
-/* Message describing the last non-OK status returned on this thread. */
+/* Message describing the last non-OK status returned on this thread (no
+ * counterpart on the pages; error reporting of this ABI). */
 const char *amp_last_error(void);
 
-/* ABI version of this header (incremented on incompatible changes). */
+/* ABI version of this header (incremented on incompatible changes; no
+ * counterpart on the pages). */
 int amp_abi_version(void);
 
 #ifdef __cplusplus
