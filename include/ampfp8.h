@@ -77,13 +77,9 @@ typedef enum {
 } amp_dtype;
 
 /* ------------------------------------------------------------------------ */
-/* Tensor lists.  The pages run every step over the list of a model's        */
-/* parameters or gradients ([CH20] §20.2.2: the scaler unscales "all"        */
-/* gradients; [NOTES] §4 and [MP06] §四 per-tensor loops); a handle is that   */
-/* list on the device.  Its layout has no counterpart on the pages.           */
-/* Sources: [CH20] "第20章 量化与混合精度训练", [FP8] "FP8训练：量化、自动微分、 */
-/* Torchao", [MP] "从 AMP 到 Mixed Precision：训练和推理为什么不使用同一种精度", */
-/* [NOTES] "AMP：Automatic Mixed Precision 技术笔记", [MP06] "06 · 混合精度".    */
+/* Tensor lists.  Every step of the pages runs over all of a model's          */
+/* parameters or gradients ([CH20] §20.2.2, [NOTES] §4, [MP06] §四); a handle */
+/* is that list on the device.  Its layout has no counterpart on the pages.   */
 /* ------------------------------------------------------------------------ */
 
 /* Opaque handle describing a ragged list of n contiguous device tensors of
