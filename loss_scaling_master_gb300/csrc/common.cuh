@@ -115,6 +115,13 @@ __device__ __forceinline__ uint32_t f32x2_to_fp8x2(float lo, float hi) {
     return fp8x4_canonical_nan<FT>(f32x2_to_fp8x2_raw<FT>(lo, hi));
 }
 
+// Lane-wise unsigned maximum of two pairs of 16-bit values.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 // (a0 * b0, a1 * b1), each lane an IEEE fp32 multiply rounded to nearest even,
 // as one packed instruction.
 __device__ __forceinline__ void mul2_rn(float a0, float a1, float b0, float b1, float &o0,

@@ -11,12 +11,19 @@
 // With G dividing the 128x128 tile, every group lies inside one tile, so one
 // CTA per tile reads x once and finishes everything: group maxima along rows
 // (lane shuffles) and along columns (registers, then shared memory), the
-// scales, the row-major bytes and the transposed bytes (through the swizzled
-// shared tile).  2 bytes read + 1 + 1 written per element, one launch.
+// scales, the row-major bytes and the transposed bytes (through a swizzled
+// byte tile that reuses the staging buffer as its rows are consumed).  2 bytes
+// read + 1 + 1 written per element, one launch.
+//
+// Instruction count is what bounds this pass after the loads, so: 16-bit x
+// takes its maxima on packed pairs of 16-bit magnitudes, and the fp8 bytes
+// skip the NaN canonicalisation in tiles whose scales all lie in (0, inf),
+// where no NaN byte can arise.
 //
 // The scales come from tensor_scale (fp8_tile.cuh): fp32 divisions equal to
 // §2's fp64 formula rounded to fp32.
 #include <algorithm>
+#include <type_traits>
 
 #include "fp8_tile.cuh"
 #include "internal.h"
@@ -59,15 +66,16 @@ struct GroupOut {
     float *amax_cg, *scale_cg, *inv_cg;  // [cols, ngr]
 };
 
-// shared memory of one CTA besides the staging buffers
+// shared memory of one CTA besides the staging buffer (which also takes the
+// fp8 tile for the transpose, row by row as its x rows are consumed)
 template <int G>
 struct GroupSmem {
     static constexpr int NG = kTile / G;
-    uint32_t sm[kTile * 32];                    // fp8 tile for the transpose
     uint32_t colmax[kThreads / 32][NG][kTile];  // per-warp column-group maxima
     uint32_t s_rmax[kTile][NG];                 // row-group maxima (bit patterns)
     float s_rsc[kTile][NG];                     // row-group multipliers
     float s_csc[NG][kTile];                     // column-group multipliers
+    int canon;  // some scale of the tile is not in (0, inf): NaN bytes possible
 };
 
 // Whether a tile takes the vector path: full, 16-byte rows, aligned outputs.
@@ -86,7 +94,10 @@ __device__ __forceinline__ void group_tile(const void *x, int64_t rows, int64_t 
                                            bool fast, GroupSmem<G> &S, uint4 *stage) {
     constexpr int NG = kTile / G;  // groups per tile edge
     constexpr int nw = XT == kF32 ? 2 : 1;
-    uint32_t *sm = S.sm;
+    // row r of x fills stage bytes [r * 256 nw, (r + 1) * 256 nw); its 128 fp8
+    // bytes for the transpose go to the start of that span once it is read
+    constexpr int kRowWords = 64 * nw;
+    uint32_t *sm = reinterpret_cast<uint32_t *>(stage);
     auto &colmax = S.colmax;
     auto &s_rmax = S.s_rmax;
     auto &s_rsc = S.s_rsc;
@@ -115,44 +126,104 @@ __device__ __forceinline__ void group_tile(const void *x, int64_t rows, int64_t 
         }
         asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
         auto raw = [&](int k) { return stage + (k * kThreads + threadIdx.x) * nw; };
-        // |x| bit patterns (an unsigned max of them is the NaN-propagating fp32
-        // max); colg[q][j]: column 8 c8 + j over this thread's rows of group q
-        uint32_t colg[NG][8];
-#pragma unroll
-        for (int q = 0; q < NG; ++q)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) colg[q][j] = 0u;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            float y[8];
-            words_to_f32<XT>(raw(k), y);
-            uint32_t rm = 0;
-            const int q = (16 * k) / G;  // column group of row rb + 16k (rb < 16 <= G)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t a = __float_as_uint(y[j]) & 0x7FFFFFFFu;
-                rm = max(rm, a);
-                colg[q][j] = max(colg[q][j], a);
-            }
-            // the G / 8 lanes holding this row's group of G columns
-#pragma unroll
-            for (int off = G / 16; off > 0; off >>= 1)
-                rm = max(rm, __shfl_xor_sync(0xFFFFFFFFu, rm, off));
-            if ((c8 & (G / 8 - 1)) == 0) s_rmax[rb + 16 * k][(8 * c8) / G] = rm;
-        }
-        if (out_t) {
-            // lanes l and l ^ 16 hold the same columns (row groups 2w and 2w + 1)
+        if (threadIdx.x == 0) S.canon = 0;
+        if constexpr (XT == kF32) {
+            // |x| bit patterns (an unsigned max of them is the NaN-propagating
+            // fp32 max); colg[q][j]: column 8 c8 + j over this thread's rows of
+            // group q
+            uint32_t colg[NG][8];
 #pragma unroll
             for (int q = 0; q < NG; ++q)
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    colg[q][j] = max(colg[q][j], __shfl_xor_sync(0xFFFFFFFFu, colg[q][j], 16));
-            if (lane < 16) {
+                for (int j = 0; j < 8; ++j) colg[q][j] = 0u;
 #pragma unroll
-                for (int q = 0; q < NG; ++q) {
-                    uint4 *d = reinterpret_cast<uint4 *>(&colmax[warp][q][8 * c8]);
-                    d[0] = make_uint4(colg[q][0], colg[q][1], colg[q][2], colg[q][3]);
-                    d[1] = make_uint4(colg[q][4], colg[q][5], colg[q][6], colg[q][7]);
+            for (int k = 0; k < 8; ++k) {
+                float y[8];
+                words_to_f32<XT>(raw(k), y);
+                uint32_t rm = 0;
+                const int q = (16 * k) / G;  // column group of row rb + 16k (rb < 16 <= G)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t a = __float_as_uint(y[j]) & 0x7FFFFFFFu;
+                    rm = max(rm, a);
+                    colg[q][j] = max(colg[q][j], a);
+                }
+                // the G / 8 lanes holding this row's group of G columns
+#pragma unroll
+                for (int off = G / 16; off > 0; off >>= 1)
+                    rm = max(rm, __shfl_xor_sync(0xFFFFFFFFu, rm, off));
+                if ((c8 & (G / 8 - 1)) == 0) s_rmax[rb + 16 * k][(8 * c8) / G] = rm;
+            }
+            if (out_t) {
+                // lanes l and l ^ 16 hold the same columns (row groups 2w, 2w + 1)
+#pragma unroll
+                for (int q = 0; q < NG; ++q)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        colg[q][j] = max(colg[q][j], __shfl_xor_sync(0xFFFFFFFFu, colg[q][j], 16));
+                if (lane < 16) {
+#pragma unroll
+                    for (int q = 0; q < NG; ++q) {
+                        uint4 *d = reinterpret_cast<uint4 *>(&colmax[warp][q][8 * c8]);
+                        d[0] = make_uint4(colg[q][0], colg[q][1], colg[q][2], colg[q][3]);
+                        d[1] = make_uint4(colg[q][4], colg[q][5], colg[q][6], colg[q][7]);
+                    }
+                }
+            }
+        } else {
+            // 16-bit x: |x| as 16-bit patterns, whose unsigned order is the
+            // order of magnitudes (NaN above inf), so the maxima are taken on
+            // packed pairs and widened to fp32 bit patterns at the end.
+            // colg[q][j]: columns 8 c8 + 2j, 8 c8 + 2j + 1 over this thread's
+            // rows of group q; rpair[i]: rows rb + 32i and rb + 32i + 16.
+            auto widen = [](uint32_t h) {
+                return __float_as_uint(lowp_to_f32<XT>(h & 0xFFFFu)) & 0x7FFFFFFFu;
+            };
+            uint32_t colg[NG][4], rpair[4];
+#pragma unroll
+            for (int q = 0; q < NG; ++q)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) colg[q][j] = 0u;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint4 u = *raw(k);
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                const int q = (16 * k) / G;
+                uint32_t m2 = 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t a = w[j] & 0x7FFF7FFFu;
+                    m2 = max_u16x2(m2, a);
+                    colg[q][j] = max_u16x2(colg[q][j], a);
+                }
+                const uint32_t rm16 = max(m2 & 0xFFFFu, m2 >> 16);
+                rpair[k >> 1] = (k & 1) ? (rpair[k >> 1] | (rm16 << 16)) : rm16;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+#pragma unroll
+                for (int off = G / 16; off > 0; off >>= 1)
+                    rpair[i] = max_u16x2(rpair[i], __shfl_xor_sync(0xFFFFFFFFu, rpair[i], off));
+                if ((c8 & (G / 8 - 1)) == 0) {
+                    s_rmax[rb + 32 * i][(8 * c8) / G] = widen(rpair[i]);
+                    s_rmax[rb + 32 * i + 16][(8 * c8) / G] = widen(rpair[i] >> 16);
+                }
+            }
+            if (out_t) {
+#pragma unroll
+                for (int q = 0; q < NG; ++q)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        colg[q][j] = max_u16x2(colg[q][j], __shfl_xor_sync(0xFFFFFFFFu, colg[q][j], 16));
+                if (lane < 16) {
+#pragma unroll
+                    for (int q = 0; q < NG; ++q) {
+                        uint4 *d = reinterpret_cast<uint4 *>(&colmax[warp][q][8 * c8]);
+                        d[0] = make_uint4(widen(colg[q][0]), widen(colg[q][0] >> 16),
+                                          widen(colg[q][1]), widen(colg[q][1] >> 16));
+                        d[1] = make_uint4(widen(colg[q][2]), widen(colg[q][2] >> 16),
+                                          widen(colg[q][3]), widen(colg[q][3] >> 16));
+                    }
                 }
             }
         }
@@ -163,6 +234,7 @@ __device__ __forceinline__ void group_tile(const void *x, int64_t rows, int64_t 
             const float a = __uint_as_float(s_rmax[r][q]);
             float s32, inv;
             tensor_scale(a, ef, fmax, s32, inv);
+            if (!scale_keeps_finite(s32)) S.canon = 1;
             s_rsc[r][q] = s32;
             const int64_t k = (r0 + r) * ngc + gc0 + q;
             o.amax_rg[k] = a;
@@ -178,6 +250,7 @@ __device__ __forceinline__ void group_tile(const void *x, int64_t rows, int64_t 
                 const float a = __uint_as_float(m);
                 float s32, inv;
                 tensor_scale(a, ef, fmax, s32, inv);
+                if (!scale_keeps_finite(s32)) S.canon = 1;
                 s_csc[q][c] = s32;
                 const int64_t k = (c0 + c) * ngr + gr0 + q;
                 o.amax_cg[k] = a;
@@ -198,39 +271,50 @@ __device__ __forceinline__ void group_tile(const void *x, int64_t rows, int64_t 
                 csc[q][4] = b.x; csc[q][5] = b.y; csc[q][6] = b.z; csc[q][7] = b.w;
             }
         }
+        // NaN bytes can only come from a scale outside (0, inf): tiles without
+        // one skip the canonicalisation (a branch uniform over the CTA)
+        auto cast_pass = [&](auto canon_tag) {
+            constexpr bool kCanon = decltype(canon_tag)::value;
+            auto fix = [](uint32_t v) { return kCanon ? fp8x4_canonical_nan<FT>(v) : v; };
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int r = rb + 16 * k;
-            float y[8];
-            words_to_f32<XT>(raw(k), y);
-            const float sr = s_rsc[r][qc];
-            uint32_t h[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float a0, a1;
-                mul2_rn(y[2 * j], y[2 * j + 1], sr, sr, a0, a1);
-                h[j] = f32x2_to_fp8x2_raw<FT>(a0, a1);
-            }
-            *reinterpret_cast<uint2 *>(out + (r0 + r) * cols + c0 + 8 * c8) =
-                make_uint2(fp8x4_canonical_nan<FT>(h[0] | (h[1] << 16)),
-                           fp8x4_canonical_nan<FT>(h[2] | (h[3] << 16)));
-            if (out_t) {
-                const int q = (16 * k) / G;
-                uint32_t g[4];
+            for (int k = 0; k < 8; ++k) {
+                const int r = rb + 16 * k;
+                float y[8];
+                words_to_f32<XT>(raw(k), y);
+                // row r is read by this half-warp alone (lanes with this rb), in
+                // this iteration: once all 16 have it, its span takes the fp8 bytes
+                __syncwarp();
+                const float sr = s_rsc[r][qc];
+                uint32_t h[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    float b0, b1;
-                    mul2_rn(y[2 * j], y[2 * j + 1], csc[q][2 * j], csc[q][2 * j + 1], b0, b1);
-                    g[j] = f32x2_to_fp8x2_raw<FT>(b0, b1);
+                    float a0, a1;
+                    mul2_rn(y[2 * j], y[2 * j + 1], sr, sr, a0, a1);
+                    h[j] = f32x2_to_fp8x2_raw<FT>(a0, a1);
                 }
-                *reinterpret_cast<uint2 *>(sm + swz(r, 2 * c8)) =
-                    make_uint2(fp8x4_canonical_nan<FT>(g[0] | (g[1] << 16)),
-                               fp8x4_canonical_nan<FT>(g[2] | (g[3] << 16)));
+                *reinterpret_cast<uint2 *>(out + (r0 + r) * cols + c0 + 8 * c8) =
+                    make_uint2(fix(h[0] | (h[1] << 16)), fix(h[2] | (h[3] << 16)));
+                if (out_t) {
+                    const int q = (16 * k) / G;
+                    uint32_t g[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        float b0, b1;
+                        mul2_rn(y[2 * j], y[2 * j + 1], csc[q][2 * j], csc[q][2 * j + 1], b0, b1);
+                        g[j] = f32x2_to_fp8x2_raw<FT>(b0, b1);
+                    }
+                    *reinterpret_cast<uint2 *>(sm + swz<kRowWords>(r, 2 * c8)) =
+                        make_uint2(fix(g[0] | (g[1] << 16)), fix(g[2] | (g[3] << 16)));
+                }
             }
-        }
+        };
+        if (S.canon)
+            cast_pass(std::true_type{});
+        else
+            cast_pass(std::false_type{});
         if (out_t) {
             __syncthreads();
-            store_transposed_tile(sm, out_t, rows, r0, c0);
+            store_transposed_tile<kRowWords>(sm, out_t, rows, r0, c0);
         }
     } else {
         // element path (ragged edge, or sizes/addresses that break 16-byte

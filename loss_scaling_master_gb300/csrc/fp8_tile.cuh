@@ -49,6 +49,15 @@ __device__ __forceinline__ void tensor_scale(float amax, const EpsFloor &e, floa
     }
 }
 
+// Whether every product x * s32 of the elements that s32 was formed from is a
+// number: true when 0 < s32 < inf.  Then no element of the group is NaN or
+// infinite (a NaN amax gives a NaN scale, an infinite one the scale 0), and a
+// finite x times a finite positive s32 saturates instead of turning NaN, so
+// the raw conversion yields no NaN byte and needs no canonicalisation.
+__device__ __forceinline__ bool scale_keeps_finite(float s32) {
+    return s32 > 0.0f && s32 < __int_as_float(0x7F800000);
+}
+
 template <int FT>
 __device__ __forceinline__ uint8_t quant1(float x, float s32) {
     return uint8_t(f32x2_to_fp8x2<FT>(__fmul_rn(x, s32), 0.0f) & 0xFFu);
@@ -71,7 +80,13 @@ __device__ __forceinline__ uint2 bf16x8_to_fp8x8(const uint4 &b, float s32) {
 
 // 4-byte word (row r, word w) of a 128x128 byte tile in shared memory,
 // XOR-swizzled by 16-row band so the transposed read hits 32 distinct banks.
-__device__ __forceinline__ int swz(int r, int w) { return r * 32 + (w ^ (((r >> 4) & 7) << 2)); }
+// RowWords is the row pitch in words: 32 for a dense tile, more when the tile
+// sits in a wider buffer (any multiple of 32 keeps the banks distinct).
+template <int RowWords = 32>
+__device__ __forceinline__ int swz(int r, int w) {
+    static_assert(RowWords % 32 == 0, "row pitch must be a multiple of the 32 banks");
+    return r * RowWords + (w ^ (((r >> 4) & 7) << 2));
+}
 
 // Write the transposed copy of a full 128x128 byte tile held in `sm` (filled
 // through swz) to out_t, which is [cols, rows] row-major: tile element
@@ -79,14 +94,15 @@ __device__ __forceinline__ int swz(int r, int w) { return r * 32 + (w ^ (((r >> 
 // words of one word-column (conflict-free), transposes 4x4 byte blocks with
 // byte permutes and writes four 16-byte stores; 8 lanes cover one 128-byte
 // segment of a transposed row.  Requires rows % 16 == 0 and a 16-byte aligned
-// out_t.
+// out_t.  RowWords: the row pitch the tile was written with (swz<RowWords>).
+template <int RowWords = 32>
 __device__ __forceinline__ void store_transposed_tile(const uint32_t *sm, uint8_t *out_t,
                                                       int64_t rows, int64_t r0, int64_t c0) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int rg = lane & 7, wq = (lane >> 3) + 4 * warp;
     uint32_t wv[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) wv[i] = sm[(16 * rg + i) * 32 + (wq ^ (rg << 2))];
+    for (int i = 0; i < 16; ++i) wv[i] = sm[swz<RowWords>(16 * rg + i, wq)];
     uint32_t col[4][4];  // col[j][blk]: rows 4blk..4blk+3 of column 4wq+j
 #pragma unroll
     for (int blk = 0; blk < 4; ++blk) {

@@ -1137,6 +1137,36 @@ def test_fp8_groupwise_scale_over_many_amax_values(A, dev, fmt):
     _assert_same(got, ref, "amax sweep")
 
 
+@pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
+@pytest.mark.parametrize("xdt", ["bf16", "f16"])
+@pytest.mark.parametrize("group", [32, 128])
+def test_fp8_groupwise_nonfinite_16bit(A, dev, fmt, xdt, group):
+    """16-bit x with NaNs of both signs and several payloads, +-inf,
+    subnormals and -0 planted in some full tiles, the others left finite:
+    group maxima (NaN above inf), the NaN / zero scales they give, and the NaN
+    bytes (canonical) in both layouts."""
+    rng = np.random.default_rng(140 + group)
+    rows, cols = 384, 512
+    xh = _x_host(rng, rows, cols, xdt).reshape(rows, cols).copy()
+    if xdt == "bf16":
+        specials = [0x7FC0, 0xFFC0, 0x7F81, 0xFFFF, 0x7F80, 0xFF80, 0x0001, 0x807F, 0x8000]
+    else:
+        specials = [0x7E00, 0xFE00, 0x7C01, 0xFFFF, 0x7C00, 0xFC00, 0x0001, 0x83FF, 0x8000]
+    # tiles (0, 0), (1, 2) and (2, 3) get specials; tile (1, 1) holds only
+    # subnormals and -0; the rest stays finite
+    for (tr, tc) in ((0, 0), (1, 2), (2, 3)):
+        for v in specials:
+            i, j = rng.integers(0, 128, 2)
+            xh[128 * tr + i, 128 * tc + j] = v
+    xh[128:256, 128:256] = np.where(rng.random((128, 128)) < 0.5, specials[6], specials[7])
+    xh[130, 130] = specials[8]
+    xh = xh.ravel()
+    for with_t in (True, False):
+        got = _run_groupwise(A, dev, xh, xdt, rows, cols, fmt, group, with_t)
+        ref = O.fp8_quant_groupwise(xh, xdt, rows, cols, fmt, group, transposed=with_t)
+        _assert_same(got, ref, ("nonfinite", with_t))
+
+
 def test_fp8_groupwise_skip_writes_nothing(A, dev):
     rng = np.random.default_rng(131)
     xh = _x_host(rng, 256, 384, "bf16")
