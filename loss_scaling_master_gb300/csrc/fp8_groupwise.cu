@@ -12,8 +12,10 @@
 // CTA per tile reads x once and finishes everything: group maxima along rows
 // (lane shuffles) and along columns (registers, then shared memory), the
 // scales, the row-major bytes and the transposed bytes (through a swizzled
-// byte tile that reuses the staging buffer as its rows are consumed).  2 bytes
-// read + 1 + 1 written per element, one launch.
+// byte tile).  2 bytes read + 1 + 1 written per element, one launch.  The
+// tile of x sits in registers (16-bit x, G >= 64) or is staged in shared
+// memory with cp.async (fp32 x, G = 32), where the byte tile then reuses the
+// staging rows as they are consumed.
 //
 // Instruction count is what bounds this pass after the loads, so: 16-bit x
 // takes its maxima on packed pairs of 16-bit magnitudes, and the fp8 bytes
@@ -78,6 +80,13 @@ struct GroupSmem {
     int canon;  // some scale of the tile is not in (0, inf): NaN bytes possible
 };
 
+// Where the vector path keeps its tile of x: in registers for 16-bit x and
+// G >= 64 (measured a few per cent faster), in shared memory for fp32 x (64
+// registers of data) and for G = 32, whose four column groups' maxima would
+// push the register count to ~90.
+template <int XT, int G>
+constexpr bool kGroupRegs = XT != kF32 && G >= 64;
+
 // Whether a tile takes the vector path: full, 16-byte rows, aligned outputs.
 __device__ __forceinline__ bool group_tile_fast(const void *x, int64_t rows, int64_t cols,
                                                 int64_t r0, int64_t c0, const GroupOut &o) {
@@ -94,9 +103,13 @@ __device__ __forceinline__ void group_tile(const void *x, int64_t rows, int64_t 
                                            bool fast, GroupSmem<G> &S, uint4 *stage) {
     constexpr int NG = kTile / G;  // groups per tile edge
     constexpr int nw = XT == kF32 ? 2 : 1;
-    // row r of x fills stage bytes [r * 256 nw, (r + 1) * 256 nw); its 128 fp8
-    // bytes for the transpose go to the start of that span once it is read
-    constexpr int kRowWords = 64 * nw;
+    // With kGroupRegs, x stays in registers (8 x 16 B a thread) and `stage`
+    // holds only the 16 KB fp8 tile for the transpose.  Otherwise x is staged
+    // in shared memory: row r fills stage bytes [r * 256 nw, (r + 1) * 256 nw),
+    // and its 128 fp8 bytes for the transpose go to the start of that span
+    // once it is read.
+    constexpr bool kRegs = kGroupRegs<XT, G>;
+    constexpr int kRowWords = kRegs ? 32 : 64 * nw;
     uint32_t *sm = reinterpret_cast<uint32_t *>(stage);
     auto &colmax = S.colmax;
     auto &s_rmax = S.s_rmax;
@@ -110,22 +123,35 @@ __device__ __forceinline__ void group_tile(const void *x, int64_t rows, int64_t 
         constexpr int esz = XT == kF32 ? 4 : 2;
         const int c8 = threadIdx.x & 15, rb = threadIdx.x >> 4;
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-        // the tile goes to this thread's own staging slots with asynchronous
-        // copies, so no registers are held while the loads are in flight and
-        // the cast pass reads the data again from shared memory
+        uint4 xr[kRegs ? 8 : 1];
+        if constexpr (kRegs) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const char *p = static_cast<const char *>(x) + ((r0 + rb + 16 * k) * cols + c0 + 8 * c8) * esz;
+            for (int k = 0; k < 8; ++k)
+                xr[k] = ld16(static_cast<const char *>(x) +
+                             ((r0 + rb + 16 * k) * cols + c0 + 8 * c8) * esz);
+        } else {
+            // the tile goes to this thread's own staging slots with
+            // asynchronous copies, so no registers are held while the loads
+            // are in flight and the cast pass reads the data again
 #pragma unroll
-            for (int u = 0; u < nw; ++u) {
-                const uint32_t d = static_cast<uint32_t>(
-                    __cvta_generic_to_shared(stage + (k * kThreads + threadIdx.x) * nw + u));
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(p + 16 * u)
-                             : "memory");
+            for (int k = 0; k < 8; ++k) {
+                const char *p =
+                    static_cast<const char *>(x) + ((r0 + rb + 16 * k) * cols + c0 + 8 * c8) * esz;
+#pragma unroll
+                for (int u = 0; u < nw; ++u) {
+                    const uint32_t d = static_cast<uint32_t>(
+                        __cvta_generic_to_shared(stage + (k * kThreads + threadIdx.x) * nw + u));
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d),
+                                 "l"(p + 16 * u)
+                                 : "memory");
+                }
             }
+            asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
         }
-        asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-        auto raw = [&](int k) { return stage + (k * kThreads + threadIdx.x) * nw; };
+        auto raw = [&](int k) -> const uint4 * {
+            if constexpr (kRegs) return &xr[k];
+            else return stage + (k * kThreads + threadIdx.x) * nw;
+        };
         if (threadIdx.x == 0) S.canon = 0;
         if constexpr (XT == kF32) {
             // |x| bit patterns (an unsigned max of them is the NaN-propagating
@@ -395,7 +421,7 @@ cudaError_t launch_group_t(const void *x, int64_t rows, int64_t cols, const Grou
     const int64_t tiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
     if (tiles == 0) return cudaSuccess;
     const EpsFloor ef = make_eps_floor(eps, fp8_max<FT>());
-    constexpr int smem = kTile * kTile * (XT == kF32 ? 4 : 2);
+    constexpr int smem = kGroupRegs<XT, G> ? kTile * kTile : kTile * kTile * (XT == kF32 ? 4 : 2);
     cudaFuncSetAttribute(groupwise_kernel<XT, FT, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          smem);
     return launch_pdl(groupwise_kernel<XT, FT, G>, dim3((unsigned)tiles), dim3(kThreads), smem, s,
