@@ -1139,7 +1139,7 @@ def test_fp8_groupwise_scale_over_many_amax_values(A, dev, fmt):
 
 @pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
 @pytest.mark.parametrize("xdt", ["bf16", "f16"])
-@pytest.mark.parametrize("group", [32, 128])
+@pytest.mark.parametrize("group", [32, 64, 128])
 def test_fp8_groupwise_nonfinite_16bit(A, dev, fmt, xdt, group):
     """16-bit x with NaNs of both signs and several payloads, +-inf,
     subnormals and -0 planted in some full tiles, the others left finite:
