@@ -5,7 +5,9 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <memory>
 #include <mutex>
+#include <new>
 #include <vector>
 
 #include "internal.h"
@@ -89,16 +91,18 @@ static bool bad_shape(int64_t rows, int64_t cols) {
     return rows < 0 || cols < 0 || rows >= lim || cols >= lim || (cols > 0 && rows > INT64_MAX / cols);
 }
 
-amp_status amp_tensor_list_create(int n, void *const *dev_ptrs, const int64_t *rows,
-                                  const int64_t *cols, amp_dtype dtype, amp_stream_t stream,
-                                  amp_tensor_list *out) {
-    AMP_TRACE("amp_tensor_list_create");
+// The body of amp_tensor_list_create; host allocations may throw
+// std::bad_alloc, which the entry point turns into AMP_ENOMEM.
+static amp_status list_create(int n, void *const *dev_ptrs, const int64_t *rows,
+                              const int64_t *cols, amp_dtype dtype, amp_stream_t stream,
+                              amp_tensor_list *out) {
     if (!out) return fail(AMP_EINVAL, "amp_tensor_list_create: out is NULL");
     if (n < 0) return fail(AMP_EINVAL, "amp_tensor_list_create: n < 0");
     if (n > 0 && (!dev_ptrs || !rows))
         return fail(AMP_EINVAL, "amp_tensor_list_create: dev_ptrs / rows is NULL");
     if (elem_size(dtype) == 0) return fail(AMP_EDTYPE, "amp_tensor_list_create: unknown dtype");
-    auto *L = new amp_tensor_list_s();
+    auto owner = std::make_unique<amp_tensor_list_s>();
+    amp_tensor_list_s *L = owner.get();
     L->n = n;
     L->dtype = dtype;
     L->two_d = cols != nullptr;
@@ -110,31 +114,27 @@ amp_status amp_tensor_list_create(int n, void *const *dev_ptrs, const int64_t *r
     for (int i = 0; i < n; ++i) {
         const int64_t r = rows[i], c = cols ? cols[i] : 1;
         if (bad_shape(r, c)) {
-            delete L;
             return fail(AMP_EINVAL, "amp_tensor_list_create: negative or too large size at tensor %d", i);
         }
         const int64_t ne = r * c;
         if (ne > 0 && dev_ptrs[i] == nullptr) {
-            delete L;
             return fail(AMP_EINVAL, "amp_tensor_list_create: NULL pointer of non-empty tensor %d", i);
         }
-        if ((ne + amp::kChunk - 1) / amp::kChunk > int64_t(UINT32_MAX)) {
-            delete L;
+        // the tables are bounded before they grow, so an absurd shape fails
+        // here instead of exhausting host memory
+        const int64_t nc = (ne + amp::kChunk - 1) / amp::kChunk;
+        const int64_t nt =
+            cols ? ((r + amp::kTile - 1) / amp::kTile) * ((c + amp::kTile - 1) / amp::kTile) : 0;
+        if (nc > int64_t(INT32_MAX) - int64_t(chunks.size()) ||
+            nt > int64_t(INT32_MAX) - int64_t(tiles.size())) {
             return fail(AMP_EINVAL, "amp_tensor_list_create: tensor %d too large", i);
         }
         L->ptrs[i] = dev_ptrs[i];
         L->numel[i] = ne;
         L->rows[i] = r;
         L->cols[i] = c;
-        for (int64_t k = 0; k * amp::kChunk < ne; ++k) chunks.push_back(make_uint2(i, uint32_t(k)));
-        if (cols) {
-            const int64_t nt = ((r + amp::kTile - 1) / amp::kTile) * ((c + amp::kTile - 1) / amp::kTile);
-            for (int64_t k = 0; k < nt; ++k) tiles.push_back(make_uint2(i, uint32_t(k)));
-        }
-    }
-    if (chunks.size() > size_t(INT32_MAX) || tiles.size() > size_t(INT32_MAX)) {
-        delete L;
-        return fail(AMP_EINVAL, "amp_tensor_list_create: list too large");
+        for (int64_t k = 0; k < nc; ++k) chunks.push_back(make_uint2(i, uint32_t(k)));
+        for (int64_t k = 0; k < nt; ++k) tiles.push_back(make_uint2(i, uint32_t(k)));
     }
     L->n_chunks = int64_t(chunks.size());
     L->n_tiles = int64_t(tiles.size());
@@ -164,12 +164,10 @@ amp_status amp_tensor_list_create(int n, void *const *dev_ptrs, const int64_t *r
 
     cudaError_t e = cudaGetDevice(&L->device);
     if (e != cudaSuccess) {
-        delete L;
         return cuda_fail(e, "amp_tensor_list_create: cudaGetDevice");
     }
     e = cudaMalloc(&L->block, total);
     if (e != cudaSuccess) {
-        delete L;
         return fail(AMP_ENOMEM, "amp_tensor_list_create: cudaMalloc(%zu): %s", total,
                     cudaGetErrorString(e));
     }
@@ -179,7 +177,6 @@ amp_status amp_tensor_list_create(int n, void *const *dev_ptrs, const int64_t *r
     if (e == cudaSuccess) e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
         cudaFree(L->block);
-        delete L;
         return cuda_fail(e, "amp_tensor_list_create: upload");
     }
     char *b = static_cast<char *>(L->block);
@@ -194,8 +191,19 @@ amp_status amp_tensor_list_create(int n, void *const *dev_ptrs, const int64_t *r
     L->view.n = n;
     L->scratch = b + o_scratch;
     L->tscale = reinterpret_cast<float *>(b + o_tscale);
-    *out = L;
+    *out = owner.release();
     return AMP_OK;
+}
+
+amp_status amp_tensor_list_create(int n, void *const *dev_ptrs, const int64_t *rows,
+                                  const int64_t *cols, amp_dtype dtype, amp_stream_t stream,
+                                  amp_tensor_list *out) {
+    AMP_TRACE("amp_tensor_list_create");
+    try {
+        return list_create(n, dev_ptrs, rows, cols, dtype, stream, out);
+    } catch (const std::bad_alloc &) {
+        return fail(AMP_ENOMEM, "amp_tensor_list_create: host allocation failed");
+    }
 }
 
 amp_status amp_tensor_list_set_amax_slots(amp_tensor_list list, const int32_t *slots,

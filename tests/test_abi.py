@@ -76,6 +76,12 @@ def test_invalid_arguments_return_status(lib):
     assert lib.amp_tensor_list_create(1, (P * 1)(dummy), huge, huge, DT["f32"], None,
                                       ctypes.byref(out)) == EINVAL
     assert b"too large" in lib.amp_last_error()
+    # a shape that passes those limits but whose chunk table would pass 2^31
+    # entries fails before the table grows (no host allocation of it)
+    vast = (ctypes.c_int64 * 1)(1 << 45)
+    assert lib.amp_tensor_list_create(1, (P * 1)(dummy), vast, None, DT["f32"], None,
+                                      ctypes.byref(out)) == EINVAL
+    assert b"too large" in lib.amp_last_error()
     assert lib.fp8_quant_tensorwise(dummy, DT["bf16"], (1 << 40) + 1, (1 << 40) + 1, DT["e4m3fn"],
                                     1e-12, dummy, None, dummy, dummy, 0, None, None) == EINVAL
     assert lib.fp8_quant_rowwise(dummy, DT["bf16"], 0, 1 << 48, DT["e4m3fn"], 1e-12, dummy, None,
