@@ -22,7 +22,7 @@
  *   [NOTES] "AMP：Automatic Mixed Precision 技术笔记": §4 GradScaler.
  *   [MP06]  "06 · 混合精度": §一 五种数字格式, §三 主权重副本, §四 Loss Scaling.
  *
- * Readings of points the pages leave open (each also listed in the design doc):
+ * Readings of points the pages leave open:
  *   - AdamW is named but never written out on the pages; the oracle takes
  *     the published decoupled-weight-decay AdamW (Loshchilov & Hutter) with
  *     Adam's bias correction, in the parametrisation of torch.optim.AdamW
