@@ -65,6 +65,15 @@ def workload_config(workload: str, world: int) -> dict:
             "l2": "inputs larger than L2 (no flush needed)"}
 
 
+def storage_desc(workload: str) -> str:
+    """What the step reads and writes, from the workload's own recipe."""
+    from workloads import amp_config
+    cfg = amp_config(workload)
+    fp8 = cfg.fp8_weights and any(s.fp8 for s in cfg.specs)
+    return (f"f32 master/m/v, {cfg.grad_dtype} grads in, bf16"
+            + (" + e4m3fn (+ transposed) copies out" if fp8 else " copy out"))
+
+
 def adamw_traffic(delayed: bool, n_params: int, n_fp8: int):
     """DRAM bytes of the AdamW call from the committed captures: the chunked
     kernel for every parameter, or (delayed FP8) the chunked kernel for the
@@ -314,8 +323,9 @@ def run_ours(args, rank, world, device):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32",
-        "storage": "f32 master/m/v, f16 grads in, bf16 + e4m3fn copies out",
-        "data": "synthetic (seeded N(0,0.02) masters, N(0,sigma*S) fp16 grads; no trained weights)",
+        "storage": storage_desc(args.workload),
+        "data": "synthetic (seeded N(0,0.02) masters and seeded gradients of the workload's "
+                "recipe; no trained weights)",
         "config": dict(workload_config(args.workload, world), per_step_bytes=total_bytes),
         "hbm_gbs_step": total_bytes / (ms_step * 1e-3) / 1e9,
         "grad_clip": args.clip,
@@ -590,7 +600,7 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32",
-            "storage": "f32 master/m/v, f16 grads in, bf16 + e4m3fn copies out",
+            "storage": storage_desc(args.workload),
             "data": "synthetic", "config": workload_config(args.workload, world),
             "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
