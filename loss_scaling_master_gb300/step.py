@@ -79,7 +79,8 @@ class AmpOptimizerStep:
         self.n_fp8 = 0
         self.fp8, self.fp8_t = [], []
         if fp8_shapes is not None:
-            assert emit_bf16, "FP8 weight copies are cast from the bf16 copy"
+            if not emit_bf16:
+                raise ValueError("FP8 weight copies are cast from the bf16 copy (emit_bf16=True)")
             slots, xs = [], []
             for i, sh in enumerate(fp8_shapes):
                 if sh is None:
