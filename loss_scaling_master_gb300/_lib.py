@@ -117,8 +117,33 @@ def _stream(stream):
     return P(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
-def _dptr(t):
-    return None if t is None else P(t.data_ptr())
+def _buf(t, what: str, dtype=None, numel: int = 1, itemsize: int | None = None,
+         host_ok: bool = False):
+    """Pointer of a buffer the library reads or writes, after checking that it
+    is a contiguous CUDA tensor (or page-locked host memory where host_ok) of
+    the expected dtype (or item size) with at least `numel` elements, so a
+    wrong buffer fails here instead of faulting on the device."""
+    if t is None:
+        return None
+    if not t.is_contiguous() or not (t.is_cuda or (host_ok and t.is_pinned())):
+        raise ValueError(f"{what}: needs a contiguous "
+                         + ("CUDA or page-locked host" if host_ok else "CUDA") + " tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{what}: dtype {t.dtype}, expected {dtype}")
+    if itemsize is not None and t.element_size() != itemsize:
+        raise ValueError(f"{what}: {t.element_size()}-byte elements, expected {itemsize}")
+    if t.numel() < numel:
+        raise ValueError(f"{what}: {t.numel()} elements, at least {numel} needed")
+    return P(t.data_ptr())
+
+
+_F32, _F64, _I32 = torch.float32, torch.float64, torch.int32
+
+
+def _step_bufs(scale, found_inf, step):
+    """scale (fp32, may be None for S = 1), found_inf and the step counter (int32)."""
+    return (_buf(scale, "scale", _F32), _buf(found_inf, "found_inf", _I32),
+            _buf(step, "step", _I32))
 
 
 def dtype_name(t: torch.Tensor) -> str:
@@ -157,8 +182,8 @@ def amp_tensor_list_create(tensors, two_d: bool = False, dtype: str | None = Non
         dtype = dtype_name(tensors[0])
     n = len(tensors)
     for t in tensors:
-        if not t.is_contiguous() or dtype_name(t) != dtype:
-            raise ValueError("every tensor must be contiguous and of the list dtype")
+        if not t.is_cuda or not t.is_contiguous() or dtype_name(t) != dtype:
+            raise ValueError("every tensor must be a contiguous CUDA tensor of the list dtype")
         if two_d and t.dim() != 2:
             raise ValueError("2-D list needs 2-D tensors")
     ptrs = (P * max(n, 1))(*[t.data_ptr() for t in tensors])
@@ -233,14 +258,16 @@ def amp_read_state(scale, growth_tracker, step, found_inf, host_out, stream=None
     a ScalerState, or the address of one (page-locked for asynchrony)."""
     out = host_out if isinstance(host_out, int) else ctypes.addressof(host_out)
     _check("amp_read_state",
-           load().amp_read_state(_dptr(scale), _dptr(growth_tracker), _dptr(step),
-                                 _dptr(found_inf), out, _stream(stream)))
+           load().amp_read_state(_buf(scale, "scale", _F32), _buf(growth_tracker, "growth_tracker", _I32),
+                                 _buf(step, "step", _I32), _buf(found_inf, "found_inf", _I32), out,
+                                 _stream(stream)))
 
 
 def amp_scale_health(scale, min_scale: float, health, stream=None):
     """Sticky health bits of the loss scale into health (device or page-locked host int32)."""
     _check("amp_scale_health",
-           load().amp_scale_health(_dptr(scale), float(min_scale), _dptr(health), _stream(stream)))
+           load().amp_scale_health(_buf(scale, "scale", _F32), float(min_scale),
+                                   _buf(health, "health", _I32, host_ok=True), _stream(stream)))
 
 
 def amp_noalloc_check(stream=None):
@@ -250,12 +277,14 @@ def amp_noalloc_check(stream=None):
 
 def amp_selftest_bounded_wait(err, limit_seconds: float = 0.05, stream=None):
     _check("amp_selftest_bounded_wait",
-           load().amp_selftest_bounded_wait(_dptr(err), float(limit_seconds), _stream(stream)))
+           load().amp_selftest_bounded_wait(_buf(err, "err", _I32), float(limit_seconds),
+                                            _stream(stream)))
 
 
 def amp_unscale_check(grads: TensorList, scale, found_inf, inplace: bool = False, stream=None):
     _check("amp_unscale_check",
-           load().amp_unscale_check(grads.handle, _dptr(scale), _dptr(found_inf), int(inplace),
+           load().amp_unscale_check(grads.handle, _buf(scale, "scale", _F32),
+                                    _buf(found_inf, "found_inf", _I32), int(inplace),
                                     _stream(stream)))
 
 
@@ -263,8 +292,9 @@ def amp_unscale_check_norm(grads: TensorList, scale, found_inf, grad_sumsq, stre
     """As amp_unscale_check, and grad_sumsq (fp64 device scalar) = sum of
     squared unscaled gradients."""
     _check("amp_unscale_check_norm",
-           load().amp_unscale_check_norm(grads.handle, _dptr(scale), _dptr(found_inf),
-                                         _dptr(grad_sumsq), _stream(stream)))
+           load().amp_unscale_check_norm(grads.handle, _buf(scale, "scale", _F32),
+                                         _buf(found_inf, "found_inf", _I32),
+                                         _buf(grad_sumsq, "grad_sumsq", _F64), _stream(stream)))
 
 
 def amp_adamw_master_step_clip(master: TensorList, exp_avg: TensorList, exp_avg_sq: TensorList,
@@ -276,8 +306,9 @@ def amp_adamw_master_step_clip(master: TensorList, exp_avg: TensorList, exp_avg_
     _check("amp_adamw_master_step_clip",
            load().amp_adamw_master_step_clip(master.handle, exp_avg.handle, exp_avg_sq.handle,
                                              grads.handle, bf16_out.handle if bf16_out else None,
-                                             _dptr(scale), _dptr(found_inf), _dptr(step),
-                                             ctypes.byref(h), _dptr(amax), _dptr(grad_sumsq),
+                                             *_step_bufs(scale, found_inf, step),
+                                             ctypes.byref(h), _buf(amax, "amax", _F32),
+                                             _buf(grad_sumsq, "grad_sumsq", _F64),
                                              float(max_norm), _stream(stream)))
 
 
@@ -288,9 +319,10 @@ def amp_adamw_master_step_sr(master: TensorList, exp_avg: TensorList, exp_avg_sq
     h = amp_adamw_hyper(lr, beta1, beta2, eps, weight_decay)
     _check("amp_adamw_master_step_sr",
            load().amp_adamw_master_step_sr(master.handle, exp_avg.handle, exp_avg_sq.handle,
-                                           grads.handle, bf16_out.handle, _dptr(scale),
-                                           _dptr(found_inf), _dptr(step), ctypes.byref(h),
-                                           _dptr(amax), ctypes.c_uint64(seed), _stream(stream)))
+                                           grads.handle, bf16_out.handle,
+                                           *_step_bufs(scale, found_inf, step), ctypes.byref(h),
+                                           _buf(amax, "amax", _F32), ctypes.c_uint64(seed),
+                                           _stream(stream)))
 
 
 def amp_adamw_master_step(master: TensorList, exp_avg: TensorList, exp_avg_sq: TensorList,
@@ -301,8 +333,9 @@ def amp_adamw_master_step(master: TensorList, exp_avg: TensorList, exp_avg_sq: T
     _check("amp_adamw_master_step",
            load().amp_adamw_master_step(master.handle, exp_avg.handle, exp_avg_sq.handle,
                                         grads.handle, bf16_out.handle if bf16_out else None,
-                                        _dptr(scale), _dptr(found_inf), _dptr(step),
-                                        ctypes.byref(h), _dptr(amax), _stream(stream)))
+                                        *_step_bufs(scale, found_inf, step),
+                                        ctypes.byref(h), _buf(amax, "amax", _F32),
+                                        _stream(stream)))
 
 
 def amp_adamw_master_step_noalloc(master, exp_avg, exp_avg_sq, grads, bf16_out, scale,
@@ -312,7 +345,13 @@ def amp_adamw_master_step_noalloc(master, exp_avg, exp_avg_sq, grads, bf16_out, 
     """Allocation-free AdamW step over plain lists of contiguous device tensors
     (no list handles); see include/ampfp8.h for its limits."""
     n = len(master)
-    arr = lambda ts: (P * max(n, 1))(*[t.data_ptr() for t in ts])
+
+    def arr(ts):
+        ts = list(ts)
+        if len(ts) != n or any(not t.is_cuda or not t.is_contiguous() for t in ts):
+            raise ValueError("every list needs one contiguous CUDA tensor per parameter")
+        return (P * max(n, 1))(*[t.data_ptr() for t in ts])
+
     numel = (ctypes.c_int64 * max(n, 1))(*[t.numel() for t in master])
     slots = None if amax_slots is None else (ctypes.c_int32 * max(n, 1))(*amax_slots)
     h = amp_adamw_hyper(lr, beta1, beta2, eps, weight_decay)
@@ -320,8 +359,9 @@ def amp_adamw_master_step_noalloc(master, exp_avg, exp_avg_sq, grads, bf16_out, 
            load().amp_adamw_master_step_noalloc(
                n, arr(master), arr(exp_avg), arr(exp_avg_sq), arr(grads),
                DT[dtype_name(grads[0])] if n else DT["f32"],
-               arr(bf16_out) if bf16_out is not None else None, numel, slots, _dptr(scale),
-               _dptr(found_inf), _dptr(step), ctypes.byref(h), _dptr(amax), _stream(stream)))
+               arr(bf16_out) if bf16_out is not None else None, numel, slots,
+               *_step_bufs(scale, found_inf, step), ctypes.byref(h), _buf(amax, "amax", _F32),
+               _stream(stream)))
 
 
 def amp_adamw_master_step_fp8_delayed(plain, fp8_group, fp8_out: TensorList,
@@ -337,19 +377,24 @@ def amp_adamw_master_step_fp8_delayed(plain, fp8_group, fp8_out: TensorList,
            load().amp_adamw_master_step_fp8_delayed(
                *[x.handle for x in plain], *[x.handle for x in fp8_group], fp8_out.handle,
                fp8_t_out.handle if fp8_t_out else None, DT[fp8_dtype], fp8_eps,
-               _dptr(amax_history), int(hist_len), _dptr(amax), _dptr(inv_scale), _dptr(scale),
-               _dptr(found_inf), _dptr(step), ctypes.byref(h), _stream(stream)))
+               _buf(amax_history, "amax_history", _F32, len(fp8_out) * int(hist_len)),
+               int(hist_len), _buf(amax, "amax", _F32, len(fp8_out)),
+               _buf(inv_scale, "inv_scale", _F32, len(fp8_out)),
+               *_step_bufs(scale, found_inf, step), ctypes.byref(h), _stream(stream)))
 
 
 def amp_update_scale_fp8_history(scale, growth_tracker, found_inf, growth_factor: float,
                                  backoff_factor: float, growth_interval: int, amax,
                                  amax_history, n_fp8: int, hist_len: int, stream=None):
     _check("amp_update_scale_fp8_history",
-           load().amp_update_scale_fp8_history(_dptr(scale), _dptr(growth_tracker),
-                                               _dptr(found_inf), growth_factor, backoff_factor,
-                                               int(growth_interval), _dptr(amax),
-                                               _dptr(amax_history), int(n_fp8), int(hist_len),
-                                               _stream(stream)))
+           load().amp_update_scale_fp8_history(_buf(scale, "scale", _F32),
+                                               _buf(growth_tracker, "growth_tracker", _I32),
+                                               _buf(found_inf, "found_inf", _I32), growth_factor,
+                                               backoff_factor, int(growth_interval),
+                                               _buf(amax, "amax", _F32, int(n_fp8)),
+                                               _buf(amax_history, "amax_history", _F32,
+                                                    int(n_fp8) * int(hist_len)),
+                                               int(n_fp8), int(hist_len), _stream(stream)))
 
 
 def fp8_quant_tensorwise(x: torch.Tensor, fp8_dtype: str, out: torch.Tensor, out_t, inv_scale,
@@ -359,9 +404,13 @@ def fp8_quant_tensorwise(x: torch.Tensor, fp8_dtype: str, out: torch.Tensor, out
     if rows is None:
         rows, cols = (x.shape[0], x.shape[1]) if x.dim() == 2 else (1, x.numel())
     _check("fp8_quant_tensorwise",
-           load().fp8_quant_tensorwise(_dptr(x), DT[dtype_name(x)], rows, cols, DT[fp8_dtype],
-                                       eps, _dptr(out), _dptr(out_t), _dptr(inv_scale),
-                                       _dptr(amax), int(amax_given), _dptr(skip_if),
+           load().fp8_quant_tensorwise(_buf(x, "x", numel=rows * cols), DT[dtype_name(x)], rows,
+                                       cols, DT[fp8_dtype], eps,
+                                       _buf(out, "out", itemsize=1, numel=rows * cols),
+                                       _buf(out_t, "out_t", itemsize=1, numel=rows * cols),
+                                       _buf(inv_scale, "inv_scale", _F32),
+                                       _buf(amax, "amax", _F32), int(amax_given),
+                                       _buf(skip_if, "skip_if", _I32),
                                        _stream(stream)))
 
 
@@ -371,10 +420,17 @@ def fp8_quant_rowwise(x: torch.Tensor, fp8_dtype: str, out, out_t, amax_row, sca
     """x is [rows, cols]; per-row scales for out, per-column scales for out_t."""
     rows, cols = x.shape
     _check("fp8_quant_rowwise",
-           load().fp8_quant_rowwise(_dptr(x), DT[dtype_name(x)], rows, cols, DT[fp8_dtype], eps,
-                                    _dptr(out), _dptr(out_t), _dptr(amax_row), _dptr(scale_row),
-                                    _dptr(inv_scale_row), _dptr(amax_col), _dptr(scale_col),
-                                    _dptr(inv_scale_col), _dptr(skip_if), _stream(stream)))
+           load().fp8_quant_rowwise(_buf(x, "x", numel=rows * cols), DT[dtype_name(x)], rows, cols,
+                                    DT[fp8_dtype], eps,
+                                    _buf(out, "out", itemsize=1, numel=rows * cols),
+                                    _buf(out_t, "out_t", itemsize=1, numel=rows * cols),
+                                    *[_buf(t, n, _F32, rows) for t, n in
+                                      ((amax_row, "amax_row"), (scale_row, "scale_row"),
+                                       (inv_scale_row, "inv_scale_row"))],
+                                    *[_buf(t, n, _F32, cols) for t, n in
+                                      ((amax_col, "amax_col"), (scale_col, "scale_col"),
+                                       (inv_scale_col, "inv_scale_col"))],
+                                    _buf(skip_if, "skip_if", _I32), _stream(stream)))
 
 
 def fp8_quant_groupwise(x: torch.Tensor, fp8_dtype: str, group: int, out, out_t, amax_rg,
@@ -383,12 +439,20 @@ def fp8_quant_groupwise(x: torch.Tensor, fp8_dtype: str, group: int, out, out_t,
     """x is [rows, cols]; one scale per `group` elements of a row for out, per
     `group` rows of a column for out_t ([cols, rows])."""
     rows, cols = x.shape
+    g = max(int(group), 1)
+    n_rg, n_cg = rows * -(-cols // g), cols * -(-rows // g)
     _check("fp8_quant_groupwise",
-           load().fp8_quant_groupwise(_dptr(x), DT[dtype_name(x)], rows, cols, int(group),
-                                      DT[fp8_dtype], eps, _dptr(out), _dptr(out_t),
-                                      _dptr(amax_rg), _dptr(scale_rg), _dptr(inv_rg),
-                                      _dptr(amax_cg), _dptr(scale_cg), _dptr(inv_cg),
-                                      _dptr(skip_if), _stream(stream)))
+           load().fp8_quant_groupwise(_buf(x, "x", numel=rows * cols), DT[dtype_name(x)], rows,
+                                      cols, int(group), DT[fp8_dtype], eps,
+                                      _buf(out, "out", itemsize=1, numel=rows * cols),
+                                      _buf(out_t, "out_t", itemsize=1, numel=rows * cols),
+                                      *[_buf(t, n, _F32, n_rg) for t, n in
+                                        ((amax_rg, "amax_rg"), (scale_rg, "scale_rg"),
+                                         (inv_rg, "inv_rg"))],
+                                      *[_buf(t, n, _F32, n_cg) for t, n in
+                                        ((amax_cg, "amax_cg"), (scale_cg, "scale_cg"),
+                                         (inv_cg, "inv_cg"))],
+                                      _buf(skip_if, "skip_if", _I32), _stream(stream)))
 
 
 def fp8_quant_tensorwise_list(x: TensorList, out: TensorList, out_t: TensorList | None,
@@ -396,17 +460,21 @@ def fp8_quant_tensorwise_list(x: TensorList, out: TensorList, out_t: TensorList 
                               stream=None):
     _check("fp8_quant_tensorwise_list",
            load().fp8_quant_tensorwise_list(x.handle, out.handle, out_t.handle if out_t else None,
-                                            DT[fp8_dtype], eps, _dptr(amax), _dptr(inv_scale),
-                                            _dptr(skip_if), _stream(stream)))
+                                            DT[fp8_dtype], eps, _buf(amax, "amax", _F32, len(x)),
+                                            _buf(inv_scale, "inv_scale", _F32, len(x)),
+                                            _buf(skip_if, "skip_if", _I32), _stream(stream)))
 
 
 def amp_update_scale(scale, growth_tracker, found_inf, growth_factor: float,
                      backoff_factor: float, growth_interval: int, amax=None, n_amax: int = 0,
                      stream=None):
     _check("amp_update_scale",
-           load().amp_update_scale(_dptr(scale), _dptr(growth_tracker), _dptr(found_inf),
+           load().amp_update_scale(_buf(scale, "scale", _F32),
+                                   _buf(growth_tracker, "growth_tracker", _I32),
+                                   _buf(found_inf, "found_inf", _I32),
                                    growth_factor, backoff_factor, int(growth_interval),
-                                   _dptr(amax), int(n_amax), _stream(stream)))
+                                   _buf(amax, "amax", _F32, int(n_amax)), int(n_amax),
+                                   _stream(stream)))
 
 
 def amp_last_error() -> str:

@@ -88,3 +88,24 @@ def test_invalid_arguments_return_status(lib):
                                  dummy, dummy, dummy, None, None, None, None, None) == EINVAL
     assert lib.amp_tensor_list_create(1, ptrs, one, None, 99, None, ctypes.byref(out)) == EDTYPE
     assert not out.value
+
+
+def test_binding_rejects_host_tensors_and_bad_buffers():
+    """The Python binding checks every buffer it hands to the library (device,
+    contiguity, dtype, size) and raises before any call reaches the GPU."""
+    import torch
+
+    import loss_scaling_master_gb300 as A
+    x = torch.zeros(4, 4, dtype=torch.bfloat16)          # host memory
+    q = torch.empty(16, dtype=torch.uint8)
+    f = torch.empty(1, dtype=torch.float32)
+    with pytest.raises(ValueError, match="CUDA"):
+        A.fp8_quant_tensorwise(x, "e4m3fn", q, None, f, f)
+    with pytest.raises(ValueError, match="CUDA"):
+        A.amp_tensor_list_create([torch.zeros(3)])
+    with pytest.raises(ValueError, match="CUDA"):
+        A.amp_update_scale(f, torch.zeros(1, dtype=torch.int32), torch.zeros(1, dtype=torch.int32),
+                           2.0, 0.5, 10)
+    with pytest.raises(ValueError, match="contiguous"):
+        A.fp8_quant_rowwise(torch.zeros(4, 8, dtype=torch.bfloat16)[:, ::2], "e4m3fn", q, None,
+                            f, f, f)

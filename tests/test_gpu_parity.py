@@ -1167,6 +1167,30 @@ def test_fp8_groupwise_nonfinite_16bit(A, dev, fmt, xdt, group):
         _assert_same(got, ref, ("nonfinite", with_t))
 
 
+def test_binding_rejects_short_or_mistyped_buffers(A, dev):
+    """Undersized outputs and wrongly typed scalars raise in the binding, before
+    a launch could write past them."""
+    x = torch.zeros(256, 256, dtype=torch.bfloat16, device=dev)
+    q = torch.empty(256 * 256, dtype=torch.uint8, device=dev)
+    short = torch.empty(256 * 256 - 1, dtype=torch.uint8, device=dev)
+    f = torch.empty(1, device=dev)
+    with pytest.raises(ValueError, match="out_t"):
+        A.fp8_quant_tensorwise(x, "e4m3fn", q, short, f, f)
+    with pytest.raises(ValueError, match="amax"):
+        A.fp8_quant_tensorwise(x, "e4m3fn", q, None, f, torch.empty(1, dtype=torch.float64,
+                                                                     device=dev))
+    r = torch.empty(256, device=dev)
+    with pytest.raises(ValueError, match="scale_col"):
+        A.fp8_quant_rowwise(x, "e4m3fn", q, q, r, r, r, r, r[:255], r)
+    g = torch.empty(256 * 2, device=dev)
+    with pytest.raises(ValueError, match="inv_rg"):
+        A.fp8_quant_groupwise(x, "e4m3fn", 128, q, None, g, g, g[:511])
+    with pytest.raises(ValueError, match="found_inf"):
+        A.amp_update_scale(f, torch.zeros(1, dtype=torch.int32, device=dev),
+                           torch.zeros(1, dtype=torch.int64, device=dev), 2.0, 0.5, 10)
+    torch.cuda.synchronize()
+
+
 def test_fp8_groupwise_skip_writes_nothing(A, dev):
     rng = np.random.default_rng(131)
     xh = _x_host(rng, 256, 384, "bf16")
