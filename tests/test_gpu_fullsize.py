@@ -10,8 +10,8 @@ times (AmpOptimizerStep over the whole parameter set).
   is element-wise once found_inf is known.
 * FP8 sweep (bf16 [4096,4096], [8192,8192], [16384,5120] and an all-zero
   [4096,4096], e4m3fn and e5m2): every byte of both layouts; the same matrices
-  with per-row / per-column scales and with 128-wide group scales, every byte
-  and every scale.
+  with per-row / per-column scales and with 128-wide group scales (bf16, and
+  widened to fp32), every byte and every scale.
 * 8B Llama-3 set, the bench's own state (flat buffers, FP8 weights), with
   dynamic and with delayed FP8 scaling: 3 steps; two FP8 weights and a norm
   vector in full through the oracle (bf16, amax or amax history, inv_scale,
@@ -233,15 +233,19 @@ def test_fp8_sweep_rowwise_full_parity(A):
         del x, o
 
 
+@pytest.mark.parametrize("xdt", ["bf16", "f32"])
 @pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
-def test_fp8_sweep_groupwise_full_parity(A, fmt):
+def test_fp8_sweep_groupwise_full_parity(A, fmt, xdt):
     """The sweep matrices with g128 group scales (the bench's group size),
-    every byte and scale, both directions."""
+    every byte and scale, both directions; as bf16 (tiles held in registers)
+    and widened exactly to fp32 (tiles staged in shared memory)."""
     dev = torch.device("cuda:0")
     G = 128
     for j, (r, c) in enumerate(FP8_SWEEP_SHAPES + [FP8_SWEEP_ZERO_SHAPE]):
         xh = fp8_sweep_host(r, c, seed=0, zero=(j == len(FP8_SWEEP_SHAPES)))
-        x = to_device(xh, "bf16", dev).view(r, c)
+        if xdt == "f32":
+            xh = (xh.astype(np.uint32) << 16).view(np.float32)
+        x = to_device(xh, xdt, dev).view(r, c)
         ngc, ngr = -(-c // G), -(-r // G)
         o = {"q": torch.empty(r * c, dtype=torch.uint8, device=dev),
              "q_t": torch.empty(r * c, dtype=torch.uint8, device=dev)}
@@ -249,7 +253,7 @@ def test_fp8_sweep_groupwise_full_parity(A, fmt):
         o.update({k: torch.empty(c * ngr, device=dev) for k in ("amax_cg", "scale_cg", "inv_cg")})
         A.fp8_quant_groupwise(x, fmt, G, o["q"], o["q_t"], o["amax_rg"], o["scale_rg"],
                               o["inv_rg"], o["amax_cg"], o["scale_cg"], o["inv_cg"])
-        ref = O.fp8_quant_groupwise(xh, "bf16", r, c, fmt, G)
+        ref = O.fp8_quant_groupwise(xh, xdt, r, c, fmt, G)
         for k in ref:
             g = to_host_bits(o[k])
             assert np.array_equal(g.view(np.uint8) if g.dtype == np.uint8 else g.view(np.uint32),
