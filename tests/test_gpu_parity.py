@@ -678,6 +678,30 @@ def test_fp8_rowwise_degenerate(A, dev, fmt):
     assert np.all(skipped["amax_row"] == -1.0) and np.all(skipped["inv_col"] == -1.0)
 
 
+@pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
+@pytest.mark.parametrize("xdt", ["bf16", "f16"])
+def test_fp8_rowwise_nonfinite_16bit(A, dev, fmt, xdt):
+    """16-bit x with NaNs of both signs and several payloads, +-inf,
+    subnormals and -0: the rows and columns they touch get NaN or zero scales
+    and (canonical) NaN bytes; every other row and column is unaffected."""
+    rng = np.random.default_rng(150)
+    rows, cols = 384, 512
+    xh = _x_host(rng, rows, cols, xdt).reshape(rows, cols).copy()
+    if xdt == "bf16":
+        specials = [0x7FC0, 0xFFC0, 0x7F81, 0xFFFF, 0x7F80, 0xFF80, 0x0001, 0x807F, 0x8000]
+    else:
+        specials = [0x7E00, 0xFE00, 0x7C01, 0xFFFF, 0x7C00, 0xFC00, 0x0001, 0x83FF, 0x8000]
+    for v in specials:
+        i, j = rng.integers(0, rows), rng.integers(0, cols)
+        xh[i, j] = v
+    xh[200, :] = specials[6]            # a row of subnormals only
+    xh[:, 300] = specials[8]            # a column of -0 only
+    xh = xh.ravel()
+    got = _run_rowwise(A, dev, xh, xdt, rows, cols, fmt, True)
+    ref = O.fp8_quant_rowwise(xh, xdt, rows, cols, fmt)
+    _assert_same(got, ref, "rowwise nonfinite")
+
+
 # ------------------------------------------------------ stochastic rounding
 @pytest.mark.parametrize("misalign", [False, True])
 def test_adamw_stochastic_rounding_parity(A, dev, misalign):
