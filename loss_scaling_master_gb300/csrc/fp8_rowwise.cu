@@ -5,13 +5,16 @@
 //
 // Four launches, 6 bytes per element as for the tensorwise cast:
 //   zero   amax_row[rows], amax_col[cols] <- +0 (skipped calls write nothing)
-//   amax   one CTA per 128x128 tile reads it once (2 B/elt): every thread holds
-//          8 rows x 8 columns; row maxima are combined across the 16 lanes
-//          sharing a row, column maxima through 8 KB of shared memory; one
-//          atomicMax per row and per column of the tile (fp32 bit patterns of
-//          |x|: an unsigned max that propagates NaN)
-//   scale  per row and per column, scale_d in fp64, fp32 multiplier and
-//          inverse written once
+//   amax   one wave of CTAs reads x once (2 B/elt), each walking a run of
+//          128x128 tiles down a column strip; every thread holds 8 rows x 8
+//          columns of a tile; row maxima are combined across the 16 lanes
+//          sharing a row (one atomicMax per row and tile), column maxima stay
+//          in registers for the strip (one atomicMax per column when the CTA
+//          leaves it); fp32 bit patterns of |x|: an unsigned max that
+//          propagates NaN
+//   scale  per row and per column, fp32 multiplier and inverse written once,
+//          by fp32 divisions equal to the fp64 formula rounded to fp32
+//          (tensor_scale in fp8_tile.cuh)
 //   cast   one CTA per tile reads it again (2 B/elt), casts each element twice
 //          (row multiplier for the row-major bytes, column multiplier for the
 //          transposed bytes) and writes both (1 + 1 B/elt), the transposed
