@@ -7,9 +7,9 @@
 //   activations, e5m2 (57344) for gradients; §4: the backward GEMMs need
 //   column-major copies, i.e. the same bytes laid out [cols, rows].
 //
-// amax pass (single tensor, when not given): grid-stride 16-byte loads, SIMD
-//   integer max of |x| bit patterns, one atomicMax per warp - 2 bytes read
-//   per bf16 element.
+// amax pass (single tensor, when not given): grid-stride 16-byte loads, four
+//   in flight per thread, SIMD integer max of |x| bit patterns, a block-level
+//   max and one atomicMax per CTA - 2 bytes read per bf16 element.
 // quant pass: one CTA per 128x128 tile.  Each thread loads 8 rows x 8
 //   columns with 16-byte coalesced loads, converts pairs with the hardware
 //   RNE+satfinite cvt, stores its 8 row-major bytes, and parks them in a
