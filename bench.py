@@ -211,10 +211,13 @@ def run_ours(args, rank, world, device):
     stream = torch.cuda.Stream(device=device)
     comb = None
     if world > 1:
-        from loss_scaling_master_gb300.sharded import combine_found_inf
+        from loss_scaling_master_gb300.sharded import combine_found_inf, combine_grad_sumsq
+        step.data_parallel = True      # the e2e leg's step() exchanges the same values
 
         def comb():
             combine_found_inf(step.found_inf)
+            if args.clip is not None:
+                combine_grad_sumsq(step.grad_sumsq)
 
     def one_step(ev=None):
         if ev is not None:

@@ -5,7 +5,8 @@ the bf16 working copy, the optional FP8 copies, and the scaler state
 {scale, growth_tracker, step, found_inf, amax[], inv_scale[]}) and the list
 handles, and enqueues, per step:
 
-1. ``amp_unscale_check``      scaled grads -> found_inf
+1. ``amp_unscale_check``      scaled grads -> found_inf (data-parallel:
+   then an all-reduce(MAX) of found_inf across the ranks)
 2. ``amp_adamw_master_step``  skip or update master/m/v, emit bf16 (+ amax)
 3. ``fp8_quant_tensorwise_list``  FP8 copies (+ transposed) of the FP8
    weights, skipped on inf (only when FP8 weights are configured)
@@ -29,7 +30,8 @@ class AmpOptimizerStep:
                  init_scale=65536.0, growth_factor=2.0, backoff_factor=0.5,
                  growth_interval=2000, emit_bf16=True, fp8_shapes=None, fp8_eps=1e-12,
                  max_norm=None, fp8_scaling="dynamic", amax_history_len=1, sr_seed=None,
-                 min_scale=None, fp8_format="e4m3fn", stream=None):
+                 min_scale=None, fp8_format="e4m3fn", data_parallel=False, dp_group=None,
+                 stream=None):
         """master: fp32 device tensors (updated in place); grads: device
         tensors (f16/bf16/f32) the caller fills with scaled gradients before
         each step.  fp8_shapes: per tensor (rows, cols) for weights that get
@@ -44,7 +46,13 @@ class AmpOptimizerStep:
         the loss scale is not finite (1) or below min_scale (2); health()
         reads them without synchronising (None: no check).  fp8_format: the
         format of the FP8 weight copies, "e4m3fn" (the pages' choice for
-        weights) or "e5m2"."""
+        weights) or "e5m2".  data_parallel: this object steps one rank's shard
+        of a data-parallel parameter set; after the non-finite check, found_inf
+        is all-reduced (MAX) over dp_group (None: the default group of
+        torch.distributed) on the step's stream, so every rank skips together,
+        and with max_norm the fp64 sum of squares is all-reduced (SUM) too, so
+        every rank clips by the global norm.  Whole tensors belong to one rank,
+        so nothing else is exchanged."""
         dev = master[0].device
         self.stream = stream
         self.master = list(master)
@@ -61,6 +69,7 @@ class AmpOptimizerStep:
         self.found_inf = torch.zeros(1, dtype=torch.int32, device=dev)
         self.max_norm = max_norm
         self.min_scale = min_scale
+        self.data_parallel, self.dp_group = bool(data_parallel), dp_group
         if fp8_format not in ("e4m3fn", "e5m2"):
             raise ValueError(fp8_format)
         self.fp8_format = fp8_format
@@ -198,6 +207,7 @@ class AmpOptimizerStep:
         if self.fp8_scaling == "delayed":
             P, F = self.delayed_groups[grad_buffer]
             A.amp_unscale_check(L_g, self.scale, self.found_inf, stream=s)
+            self._combine(s)
             A.amp_adamw_master_step_fp8_delayed(P, F, self.L_q, self.L_qt, self.fp8_format,
                                                 self.amax_history, self.hist_len, self.amax,
                                                 self.inv_scale, self.scale, self.found_inf,
@@ -211,16 +221,19 @@ class AmpOptimizerStep:
             return
         if self.sr_seed is not None:
             A.amp_unscale_check(L_g, self.scale, self.found_inf, stream=s)
+            self._combine(s)
             A.amp_adamw_master_step_sr(self.L_master, self.L_m, self.L_v, L_g, self.L_b,
                                        self.scale, self.found_inf, self.step_count, *self.hyper,
                                        self.sr_seed, amax=amax, stream=s)
         elif self.max_norm is None:
             A.amp_unscale_check(L_g, self.scale, self.found_inf, stream=s)
+            self._combine(s)
             A.amp_adamw_master_step(self.L_master, self.L_m, self.L_v, L_g, self.L_b, self.scale,
                                     self.found_inf, self.step_count, *self.hyper, amax=amax,
                                     stream=s)
         else:
             A.amp_unscale_check_norm(L_g, self.scale, self.found_inf, self.grad_sumsq, stream=s)
+            self._combine(s, norm=True)
             A.amp_adamw_master_step_clip(self.L_master, self.L_m, self.L_v, L_g, self.L_b,
                                          self.scale, self.found_inf, self.step_count, *self.hyper,
                                          self.grad_sumsq, self.max_norm, amax=amax, stream=s)
@@ -232,6 +245,17 @@ class AmpOptimizerStep:
                            self.backoff, self.interval, amax=self.amax if self.n_fp8 else None,
                            n_amax=self.n_fp8, stream=s)
         self._health(s)
+
+    def _combine(self, s, norm: bool = False):
+        """All-reduce(MAX) of found_inf over the data-parallel group, and with
+        norm the all-reduce(SUM) of grad_sumsq, on stream s."""
+        if not self.data_parallel:
+            return
+        from .sharded import combine_found_inf, combine_grad_sumsq
+        with torch.cuda.stream(s) if s is not None else _nullctx():
+            combine_found_inf(self.found_inf, self.dp_group)
+            if norm:
+                combine_grad_sumsq(self.grad_sumsq, self.dp_group)
 
     def _health(self, s):
         if self.min_scale is not None:

@@ -1,0 +1,108 @@
+"""AmpOptimizerStep(data_parallel=True) on the GPU: two ranks (processes on the
+one visible GPU, exchanging over gloo through the host, so no kernel waits on
+another rank's kernel) each step the tensors they own.  The non-finite flag
+and, with clipping, the sum of squares are all-reduced between the check and
+the update; the union of the shards must equal the unsharded oracle step, and
+an inf in one rank's gradients must make both ranks skip."""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch.multiprocessing as mp
+
+pytestmark = pytest.mark.gpu
+
+SIZES = [1000, 4096, 257, 3000, 17, 640]
+HYPER = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+MAX_NORM = 1e-4          # the global norm of these gradients is ~9.5e-4
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _inputs():
+    rng = np.random.default_rng(321)
+    master = [(rng.standard_normal(n) * 0.02).astype(np.float32) for n in SIZES]
+    grads = []
+    for step in range(4):
+        g = [(rng.standard_normal(n) * 1e-5 * 65536).astype(np.float16).view(np.uint16)
+             for n in SIZES]
+        if step == 1:
+            g[2][256] = 0x7C00          # +inf in tensor 2 only
+        grads.append(g)
+    return master, grads
+
+
+def _rank(rank, world, port, clip, q):
+    import torch
+    import torch.distributed as dist
+
+    import loss_scaling_master_gb300 as A
+    from loss_scaling_master_gb300.sharded import partition_tensors
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    dev = torch.device("cuda:0")
+    mine = partition_tensors(SIZES, world)[rank]
+    master, grads = _inputs()
+    P = [torch.from_numpy(master[i].copy()).to(dev) for i in mine]
+    G = [torch.empty(SIZES[i], dtype=torch.float16, device=dev) for i in mine]
+    st = A.AmpOptimizerStep(P, G, **HYPER, init_scale=65536.0, growth_interval=2,
+                            max_norm=MAX_NORM if clip else None, data_parallel=True)
+    states = []
+    for g in grads:
+        for t, i in zip(G, mine):
+            t.copy_(torch.from_numpy(g[i].view(np.int16).copy()).view(torch.float16))
+        st.step()
+        states.append(st.state())
+    out = ([p.cpu().numpy() for p in P], [m.cpu().numpy() for m in st.exp_avg],
+           [v.cpu().numpy() for v in st.exp_avg_sq])
+    st.check()
+    st.close()
+    q.put((rank, mine, states, out))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("clip", [False, True])
+def test_two_ranks_on_one_gpu_match_the_unsharded_step(clip):
+    import oracle as O
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank, args=(r, world, port, clip, q)) for r in range(world)]
+    for pr in procs:
+        pr.start()
+    res = [q.get(timeout=300) for _ in range(world)]
+    for pr in procs:
+        pr.join(timeout=120)
+        assert pr.exitcode == 0
+    master, grads = _inputs()
+    p = [x.copy() for x in master]
+    m = [np.zeros_like(x) for x in p]
+    v = [np.zeros_like(x) for x in p]
+    scale, tracker, step, trace = 65536.0, 0, 0, []
+    for g in grads:
+        fi = O.unscale_check([x.copy() for x in g], "f16", scale)
+        c = O.clip_coef(O.grad_sumsq([x.copy() for x in g], "f16", scale), MAX_NORM) \
+            if clip else None
+        step = O.adamw_master_step(p, m, v, [x.copy() for x in g], "f16", None, scale, fi, step,
+                                   HYPER["lr"], HYPER["beta1"], HYPER["beta2"], HYPER["eps"],
+                                   HYPER["weight_decay"], clip=c)
+        scale, tracker, _ = O.update_scale(scale, tracker, fi, 2.0, 0.5, 2)
+        trace.append((scale, tracker, step))
+    assert trace[1] == (32768.0, 0, 1)                      # the inf step is skipped
+    for rank, mine, states, (pr, mr, vr) in res:
+        assert [(s["scale"], s["growth_tracker"], s["step"]) for s in states] == trace
+        for k, i in enumerate(mine):
+            for got, ref in ((pr[k], p[i]), (mr[k], m[i]), (vr[k], v[i])):
+                if clip:    # the global sum of squares adds the ranks' partial sums
+                    rms = np.sqrt(np.mean(ref.astype(np.float64) ** 2))
+                    np.testing.assert_allclose(got, ref, rtol=1e-6, atol=1e-6 * rms)
+                else:
+                    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
