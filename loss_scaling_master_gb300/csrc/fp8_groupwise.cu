@@ -15,7 +15,11 @@
 // byte tile).  2 bytes read + 1 + 1 written per element, one launch.  The
 // tile of x sits in registers (16-bit x, G >= 64) or is staged in shared
 // memory with cp.async (fp32 x, G = 32), where the byte tile then reuses the
-// staging rows as they are consumed.
+// staging rows as they are consumed.  With the tile in registers, the lanes of
+// a row group form its scales right after the row maxima and cast the
+// row-major bytes in the same pass, so only the column scales and the
+// transposed bytes wait for the CTA's barriers (and without the copy there
+// are none).
 //
 // Instruction count is what bounds this pass after the loads, so: 16-bit x
 // takes its maxima on packed pairs of 16-bit magnitudes, and the fp8 bytes
@@ -83,7 +87,8 @@ struct GroupSmem {
 // Where the vector path keeps its tile of x: in registers for 16-bit x and
 // G >= 64 (measured a few per cent faster), in shared memory for fp32 x (64
 // registers of data) and for G = 32, whose four column groups' maxima would
-// push the register count to ~90.
+// push the register count to ~90.  The kernel's register cap keeps as many
+// CTAs per SM as its shared memory allows: 4 for 16-bit x, 3 for fp32 x.
 template <int XT, int G>
 constexpr bool kGroupRegs = XT != kF32 && G >= 64;
 
@@ -230,10 +235,57 @@ __device__ __forceinline__ void group_tile(const void *x, int64_t rows, int64_t 
 #pragma unroll
                 for (int off = G / 16; off > 0; off >>= 1)
                     rpair[i] = max_u16x2(rpair[i], __shfl_xor_sync(0xFFFFFFFFu, rpair[i], off));
-                if ((c8 & (G / 8 - 1)) == 0) {
+                if (!kRegs && (c8 & (G / 8 - 1)) == 0) {
                     s_rmax[rb + 32 * i][(8 * c8) / G] = widen(rpair[i]);
                     s_rmax[rb + 32 * i + 16][(8 * c8) / G] = widen(rpair[i] >> 16);
                 }
+            }
+            if constexpr (kRegs) {
+                // Every lane of a row group now holds the maxima of its 8 rows.
+                // Lane gl < 8 of the group forms the scale of row rb + 16 gl
+                // and writes that row group's outputs; the row-major bytes are
+                // cast here, each row's multiplier taken from its lane.
+                const int gl = c8 & (G / 8 - 1);
+                const int base = lane & ~(G / 8 - 1);
+                float s32 = 0.0f;
+                bool odd = false;
+                if (gl < 8) {
+                    const uint32_t pr = gl < 2 ? rpair[0] : gl < 4 ? rpair[1]
+                                      : gl < 6 ? rpair[2] : rpair[3];
+                    const float a = __uint_as_float(widen((gl & 1) ? pr >> 16 : pr));
+                    float inv;
+                    tensor_scale(a, ef, fmax, s32, inv);
+                    odd = !scale_keeps_finite(s32);
+                    const int64_t k = (r0 + rb + 16 * gl) * ngc + gc0 + (8 * c8) / G;
+                    o.amax_rg[k] = a;
+                    o.scale_rg[k] = s32;
+                    o.inv_rg[k] = inv;
+                }
+                // NaN bytes need a scale outside (0, inf): warps whose rows have
+                // none skip the canonicalisation (a branch uniform over the warp)
+                auto cast_rows = [&](auto canon_tag) {
+                    constexpr bool kCanon = decltype(canon_tag)::value;
+                    auto fix = [](uint32_t v) { return kCanon ? fp8x4_canonical_nan<FT>(v) : v; };
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const float sr = __shfl_sync(0xFFFFFFFFu, s32, base + k);
+                        float y[8];
+                        words_to_f32<XT>(raw(k), y);
+                        uint32_t h[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            float a0, a1;
+                            mul2_rn(y[2 * j], y[2 * j + 1], sr, sr, a0, a1);
+                            h[j] = f32x2_to_fp8x2_raw<FT>(a0, a1);
+                        }
+                        *reinterpret_cast<uint2 *>(out + (r0 + rb + 16 * k) * cols + c0 + 8 * c8) =
+                            make_uint2(fix(h[0] | (h[1] << 16)), fix(h[2] | (h[3] << 16)));
+                    }
+                };
+                if (__any_sync(0xFFFFFFFFu, odd))
+                    cast_rows(std::true_type{});
+                else
+                    cast_rows(std::false_type{});
             }
             if (out_t) {
 #pragma unroll
@@ -253,19 +305,23 @@ __device__ __forceinline__ void group_tile(const void *x, int64_t rows, int64_t 
                 }
             }
         }
+        if (kRegs && out_t == nullptr) return;  // the row-major bytes are done
         __syncthreads();
-        // scales: 128 x NG row groups, and (with the copy) NG x 128 column groups
-        for (int idx = threadIdx.x; idx < kTile * NG; idx += kThreads) {
-            const int r = idx / NG, q = idx % NG;
-            const float a = __uint_as_float(s_rmax[r][q]);
-            float s32, inv;
-            tensor_scale(a, ef, fmax, s32, inv);
-            if (!scale_keeps_finite(s32)) S.canon = 1;
-            s_rsc[r][q] = s32;
-            const int64_t k = (r0 + r) * ngc + gc0 + q;
-            o.amax_rg[k] = a;
-            o.scale_rg[k] = s32;
-            o.inv_rg[k] = inv;
+        // scales: 128 x NG row groups (staged path; the register path formed
+        // them in pass 1), and (with the copy) NG x 128 column groups
+        if constexpr (!kRegs) {
+            for (int idx = threadIdx.x; idx < kTile * NG; idx += kThreads) {
+                const int r = idx / NG, q = idx % NG;
+                const float a = __uint_as_float(s_rmax[r][q]);
+                float s32, inv;
+                tensor_scale(a, ef, fmax, s32, inv);
+                if (!scale_keeps_finite(s32)) S.canon = 1;
+                s_rsc[r][q] = s32;
+                const int64_t k = (r0 + r) * ngc + gc0 + q;
+                o.amax_rg[k] = a;
+                o.scale_rg[k] = s32;
+                o.inv_rg[k] = inv;
+            }
         }
         if (out_t) {
             for (int idx = threadIdx.x; idx < kTile * NG; idx += kThreads) {
@@ -285,7 +341,7 @@ __device__ __forceinline__ void group_tile(const void *x, int64_t rows, int64_t 
             }
         }
         __syncthreads();
-        const int qc = (8 * c8) / G;  // this thread's row group
+        [[maybe_unused]] const int qc = (8 * c8) / G;  // this thread's row group
         // the column multipliers of this thread's 8 columns, per column group
         float csc[NG][8];
         if (out_t) {
@@ -310,16 +366,18 @@ __device__ __forceinline__ void group_tile(const void *x, int64_t rows, int64_t 
                 // row r is read by this half-warp alone (lanes with this rb), in
                 // this iteration: once all 16 have it, its span takes the fp8 bytes
                 __syncwarp();
-                const float sr = s_rsc[r][qc];
-                uint32_t h[4];
+                if constexpr (!kRegs) {
+                    const float sr = s_rsc[r][qc];
+                    uint32_t h[4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    float a0, a1;
-                    mul2_rn(y[2 * j], y[2 * j + 1], sr, sr, a0, a1);
-                    h[j] = f32x2_to_fp8x2_raw<FT>(a0, a1);
+                    for (int j = 0; j < 4; ++j) {
+                        float a0, a1;
+                        mul2_rn(y[2 * j], y[2 * j + 1], sr, sr, a0, a1);
+                        h[j] = f32x2_to_fp8x2_raw<FT>(a0, a1);
+                    }
+                    *reinterpret_cast<uint2 *>(out + (r0 + r) * cols + c0 + 8 * c8) =
+                        make_uint2(fix(h[0] | (h[1] << 16)), fix(h[2] | (h[3] << 16)));
                 }
-                *reinterpret_cast<uint2 *>(out + (r0 + r) * cols + c0 + 8 * c8) =
-                    make_uint2(fix(h[0] | (h[1] << 16)), fix(h[2] | (h[3] << 16)));
                 if (out_t) {
                     const int q = (16 * k) / G;
                     uint32_t g[4];
@@ -400,19 +458,37 @@ __device__ __forceinline__ void group_tile(const void *x, int64_t rows, int64_t 
 }
 
 template <int XT, int FT, int G>
-__global__ void __launch_bounds__(kThreads) groupwise_kernel(const void *x, int64_t rows,
-                                                             int64_t cols, GroupOut o, EpsFloor ef,
-                                                             const int32_t *skip_if) {
+__device__ __forceinline__ void groupwise_body(const void *x, int64_t rows, int64_t cols,
+                                               const GroupOut &o, const EpsFloor &ef,
+                                               const int32_t *skip_if) {
     pdl_wait();
     pdl_trigger();
     if (skip_if && *skip_if) return;
     __shared__ __align__(16) GroupSmem<G> S;
-    extern __shared__ __align__(16) uint4 stage[];  // the tile of x: 128 x 128 elements
+    extern __shared__ __align__(16) uint4 stage[];  // the tile of x, or the fp8 tile
     const int64_t tiles_c = (cols + kTile - 1) / kTile;
     const int64_t r0 = int64_t(blockIdx.x / tiles_c) * kTile;
     const int64_t c0 = int64_t(blockIdx.x % tiles_c) * kTile;
     group_tile<XT, FT, G>(x, rows, cols, r0, c0, o, ef,
                           group_tile_fast(x, rows, cols, r0, c0, o), S, stage);
+}
+
+// Tiles held in registers: capped at 64 registers, so 4 CTAs share an SM.
+template <int XT, int FT, int G>
+__global__ void __launch_bounds__(kThreads, 4) groupwise_kernel(const void *x, int64_t rows,
+                                                                int64_t cols, GroupOut o,
+                                                                EpsFloor ef,
+                                                                const int32_t *skip_if) {
+    groupwise_body<XT, FT, G>(x, rows, cols, o, ef, skip_if);
+}
+
+// Tiles staged in shared memory (fp32 x, G = 32): the compiler's own choice.
+template <int XT, int FT, int G>
+__global__ void __launch_bounds__(kThreads) groupwise_staged_kernel(const void *x, int64_t rows,
+                                                                    int64_t cols, GroupOut o,
+                                                                    EpsFloor ef,
+                                                                    const int32_t *skip_if) {
+    groupwise_body<XT, FT, G>(x, rows, cols, o, ef, skip_if);
 }
 
 template <int XT, int FT, int G>
@@ -421,11 +497,16 @@ cudaError_t launch_group_t(const void *x, int64_t rows, int64_t cols, const Grou
     const int64_t tiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
     if (tiles == 0) return cudaSuccess;
     const EpsFloor ef = make_eps_floor(eps, fp8_max<FT>());
-    constexpr int smem = kGroupRegs<XT, G> ? kTile * kTile : kTile * kTile * (XT == kF32 ? 4 : 2);
-    cudaFuncSetAttribute(groupwise_kernel<XT, FT, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         smem);
-    return launch_pdl(groupwise_kernel<XT, FT, G>, dim3((unsigned)tiles), dim3(kThreads), smem, s,
-                      x, rows, cols, o, ef, skip_if);
+    auto launch = [&](auto kern, int smem) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        return launch_pdl(kern, dim3((unsigned)tiles), dim3(kThreads), smem, s, x, rows, cols, o,
+                          ef, skip_if);
+    };
+    if constexpr (kGroupRegs<XT, G>)
+        return launch(groupwise_kernel<XT, FT, G>, kTile * kTile);  // the fp8 tile only
+    else
+        return launch(groupwise_staged_kernel<XT, FT, G>, kTile * kTile * (XT == kF32 ? 4 : 2));
 }
 
 template <int XT, int FT>
