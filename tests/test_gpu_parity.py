@@ -952,6 +952,36 @@ def test_list_host_copies_round_trip(A, dev):
         L.close()
 
 
+def test_huge_page_host_buffer_feeds_a_list(A, dev):
+    """pinned_empty (huge-page mapping registered with CUDA) as the host side of
+    amp_tensor_list_copy_from_host: one buffer viewed per tensor, as the e2e
+    feed uses it; every byte arrives, and the buffer closes cleanly."""
+    from loss_scaling_master_gb300.hostmem import pinned_empty
+    rng = np.random.default_rng(43)
+    sizes = [1, 1000, 0, (1 << 21) + 5, 8]
+    buf = pinned_empty(sum(sizes), torch.float16)
+    host = buf.tensor
+    assert host.numel() == sum(sizes) and host.dtype == torch.float16
+    host.view(torch.int16).copy_(torch.from_numpy(
+        rng.integers(0, 1 << 16, sum(sizes), dtype=np.uint16).view(np.int16)))
+    D = [torch.empty(n, dtype=torch.float16, device=dev) for n in sizes]
+    L = A.amp_tensor_list_create(D)
+    ptrs, off = [], 0
+    for n in sizes:
+        ptrs.append(host.data_ptr() + 2 * off if n else None)
+        off += n
+    A.amp_tensor_list_copy_from_host(L, ptrs)
+    torch.cuda.synchronize()
+    off = 0
+    for d, n in zip(D, sizes):
+        assert torch.equal(d.cpu().view(torch.int16), host[off:off + n].view(torch.int16))
+        off += n
+    L.close()
+    del host
+    buf.close()
+    assert buf.tensor is None
+
+
 # ------------------------------------------------------ monitoring
 def test_read_state_and_scale_health(A, dev):
     """amp_read_state copies the scaler state to host memory; amp_scale_health
