@@ -228,6 +228,24 @@ amp_status amp_adamw_master_step(amp_tensor_list master, amp_tensor_list exp_avg
                                  const amp_adamw_hyper *hyper, float *amax_dev,
                                  amp_stream_t stream);
 
+/* A5 on its own ("从 AMP 到 Mixed Precision" sections "为什么需要 FP32 Master
+ * Weights" and "PyTorch AMP 与 FP32 Master Weights", mode B: the model's bf16
+ * parameters are the fp32 master rounded to bf16).  The AdamW entry points
+ * emit this copy after every step; this call makes it before the first one,
+ * for the first forward pass and, with amax slots, for the first amax of the
+ * FP8 weights (the opening entry of a delayed-scaling history):
+ *     bf16_out = RNE(master)   (NaN -> 0x7FC0)
+ *     amax_dev[slot] = max(amax_dev[slot], |bf16|) for tensors with a slot
+ *                   (amp_tensor_list_set_amax_slots on bf16_out; fp32 bits,
+ *                   NaN propagating; the caller zeroes amax_dev first)
+ *   master    AMP_DT_F32 list (read only)
+ *   bf16_out  AMP_DT_BF16 list with master's tensor count and sizes
+ * 6 bytes per element, one launch.
+ * Errors: AMP_EINVAL (NULL / mismatched lists, slots without amax_dev),
+ * AMP_EDTYPE (wrong list dtypes). */
+amp_status amp_emit_bf16(amp_tensor_list master, amp_tensor_list bf16_out, float *amax_dev,
+                         amp_stream_t stream);
+
 /* amp_adamw_master_step with gradient-norm clipping: the per-step scalar
  *     clip = min(1, max_norm / (sqrt(*grad_sumsq_dev) + 1e-6))
  * is formed once in fp64 (NaN propagates) and rounded to fp32, and every

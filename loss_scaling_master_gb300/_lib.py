@@ -29,7 +29,7 @@ EXPORTS = ("amp_tensor_list_create", "amp_tensor_list_set_amax_slots", "amp_tens
            "amp_tensor_list_check", "amp_selftest_bounded_wait",
            "amp_tensor_list_copy_from_host", "amp_tensor_list_copy_to_host",
            "amp_read_state", "amp_scale_health", "fp8_quant_groupwise",
-           "amp_unscale_check", "amp_unscale_check_norm", "amp_adamw_master_step",
+           "amp_unscale_check", "amp_unscale_check_norm", "amp_adamw_master_step", "amp_emit_bf16",
            "amp_adamw_master_step_clip", "amp_adamw_master_step_sr",
            "amp_adamw_master_step_noalloc", "amp_noalloc_check",
            "amp_adamw_master_step_fp8_delayed", "amp_update_scale_fp8_history",
@@ -80,6 +80,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.amp_adamw_master_step.argtypes = [P, P, P, P, P, P, P, P,
                                             ctypes.POINTER(amp_adamw_hyper), P, P]
         L.amp_unscale_check_norm.argtypes = [P, P, P, P, P]
+        L.amp_emit_bf16.argtypes = [P, P, P, P]
         L.amp_adamw_master_step_clip.argtypes = [P, P, P, P, P, P, P, P,
                                                  ctypes.POINTER(amp_adamw_hyper), P, P, dbl, P]
         L.amp_adamw_master_step_sr.argtypes = [P, P, P, P, P, P, P, P,
@@ -338,28 +339,72 @@ def amp_adamw_master_step(master: TensorList, exp_avg: TensorList, exp_avg_sq: T
                                         _stream(stream)))
 
 
+def amp_emit_bf16(master: TensorList, bf16_out: TensorList, amax=None, stream=None):
+    """bf16_out = RNE(master), folding max|bf16| into amax[slot] for tensors
+    with an amax slot."""
+    if len(master) != len(bf16_out):
+        raise ValueError("master and bf16_out differ in tensor count")
+    _check("amp_emit_bf16",
+           load().amp_emit_bf16(master.handle, bf16_out.handle, _buf(amax, "amax", _F32),
+                                _stream(stream)))
+
+
 def amp_adamw_master_step_noalloc(master, exp_avg, exp_avg_sq, grads, bf16_out, scale,
                                   found_inf, step, lr: float, beta1: float, beta2: float,
                                   eps: float, weight_decay: float, amax_slots=None, amax=None,
                                   stream=None):
     """Allocation-free AdamW step over plain lists of contiguous device tensors
-    (no list handles); see include/ampfp8.h for its limits."""
+    (no list handles); see include/ampfp8.h for its limits.  Every list must
+    hold one tensor per parameter with master's element counts: master, m, v
+    fp32, bf16_out bf16, the gradients one dtype among f32/f16/bf16; amax
+    must hold every slot named.  A mismatch raises ValueError before the call,
+    since the library sees only pointers and would write out of bounds."""
+    master = list(master)
     n = len(master)
+    lists = {"master": master, "exp_avg": list(exp_avg), "exp_avg_sq": list(exp_avg_sq),
+             "grads": list(grads)}
+    if bf16_out is not None:
+        lists["bf16_out"] = list(bf16_out)
+    sizes = [t.numel() for t in master]
+    for name, ts in lists.items():
+        if len(ts) != n:
+            raise ValueError(f"{name}: {len(ts)} tensors, master has {n}")
+        for i, t in enumerate(ts):
+            if t.numel() != sizes[i]:
+                raise ValueError(f"{name}[{i}]: {t.numel()} elements, master[{i}] has {sizes[i]}")
+    want = {"master": (torch.float32,), "exp_avg": (torch.float32,),
+            "exp_avg_sq": (torch.float32,), "bf16_out": (torch.bfloat16,),
+            "grads": (torch.float32, torch.float16, torch.bfloat16)}
+    for name, ts in lists.items():
+        for i, t in enumerate(ts):
+            if t.dtype not in want[name]:
+                raise ValueError(f"{name}[{i}]: dtype {t.dtype}, expected one of {want[name]}")
+    gdts = {t.dtype for t in lists["grads"]}
+    if len(gdts) > 1:
+        raise ValueError(f"grads: mixed dtypes {sorted(map(str, gdts))}; one dtype is needed")
+    if amax_slots is not None:
+        amax_slots = [int(x) for x in amax_slots]
+        if len(amax_slots) != n:
+            raise ValueError(f"amax_slots: {len(amax_slots)} entries for {n} tensors")
+        top = max(amax_slots, default=-1)
+        if top >= 0 and bf16_out is not None and (amax is None or top >= amax.numel()):
+            raise ValueError(f"amax_slots name slot {top}; amax holds "
+                             f"{0 if amax is None else amax.numel()}")
+    for name, ts in lists.items():
+        if any(not t.is_cuda or not t.is_contiguous() for t in ts):
+            raise ValueError(f"{name}: every tensor must be a contiguous CUDA tensor")
 
     def arr(ts):
-        ts = list(ts)
-        if len(ts) != n or any(not t.is_cuda or not t.is_contiguous() for t in ts):
-            raise ValueError("every list needs one contiguous CUDA tensor per parameter")
         return (P * max(n, 1))(*[t.data_ptr() for t in ts])
 
-    numel = (ctypes.c_int64 * max(n, 1))(*[t.numel() for t in master])
+    numel = (ctypes.c_int64 * max(n, 1))(*sizes)
     slots = None if amax_slots is None else (ctypes.c_int32 * max(n, 1))(*amax_slots)
     h = amp_adamw_hyper(lr, beta1, beta2, eps, weight_decay)
     _check("amp_adamw_master_step_noalloc",
            load().amp_adamw_master_step_noalloc(
-               n, arr(master), arr(exp_avg), arr(exp_avg_sq), arr(grads),
-               DT[dtype_name(grads[0])] if n else DT["f32"],
-               arr(bf16_out) if bf16_out is not None else None, numel, slots,
+               n, arr(master), arr(lists["exp_avg"]), arr(lists["exp_avg_sq"]),
+               arr(lists["grads"]), DT[dtype_name(lists["grads"][0])] if n else DT["f32"],
+               arr(lists["bf16_out"]) if bf16_out is not None else None, numel, slots,
                *_step_bufs(scale, found_inf, step), ctypes.byref(h), _buf(amax, "amax", _F32),
                _stream(stream)))
 

@@ -18,7 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libampfp8.so")
-SOURCES = ["api.cu", "unscale_check.cu", "adamw_master.cu", "adamw_noalloc.cu", "fp8_quant.cu",
+SOURCES = ["api.cu", "unscale_check.cu", "adamw_master.cu", "adamw_noalloc.cu", "emit_bf16.cu",
+           "fp8_quant.cu",
            "fp8_rowwise.cu", "fp8_groupwise.cu", "update_scale.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # --fmad=false: no multiply-add is fused behind the code's back; the kernels

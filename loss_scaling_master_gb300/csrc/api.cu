@@ -82,7 +82,7 @@ extern "C" {
 
 const char *amp_last_error(void) { return g_err; }
 
-int amp_abi_version(void) { return 9; }
+int amp_abi_version(void) { return 10; }
 
 // A [rows, cols] shape the launch arithmetic can hold: non-negative, each side
 // below 2^48 and rows * cols without int64 overflow.
@@ -345,6 +345,23 @@ static amp_status adamw_entry(amp_tensor_list master, amp_tensor_list exp_avg,
         step_dev, c, reinterpret_cast<amp::AdamwStepScalars *>(master->scratch), amax_dev, slots,
         reinterpret_cast<cudaStream_t>(stream), clip_sumsq, max_norm, stochastic, seed);
     return e == cudaSuccess ? AMP_OK : cuda_fail(e, "amp_adamw_master_step");
+}
+
+amp_status amp_emit_bf16(amp_tensor_list master, amp_tensor_list bf16_out, float *amax_dev,
+                         amp_stream_t stream) {
+    AMP_TRACE("amp_emit_bf16");
+    const char *fn = "amp_emit_bf16";
+    if (!master || !bf16_out) return fail(AMP_EINVAL, "%s: NULL list", fn);
+    if (master->dtype != AMP_DT_F32 || bf16_out->dtype != AMP_DT_BF16)
+        return fail(AMP_EDTYPE, "%s: master must be f32 and bf16_out bf16", fn);
+    if (!same_shapes(master, bf16_out))
+        return fail(AMP_EINVAL, "%s: lists differ in tensor count or sizes", fn);
+    const bool slots = bf16_out->has_slots;
+    if (slots && !amax_dev)
+        return fail(AMP_EINVAL, "%s: bf16_out has amax slots but amax_dev is NULL", fn);
+    cudaError_t e = amp::launch_emit_bf16(master->view, bf16_out->view, master->n_chunks,
+                                          amax_dev, slots, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AMP_OK : cuda_fail(e, fn);
 }
 
 amp_status amp_adamw_master_step_sr(amp_tensor_list master, amp_tensor_list exp_avg,

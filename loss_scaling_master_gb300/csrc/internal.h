@@ -104,6 +104,9 @@ cudaError_t launch_adamw_fp8_delayed(const Fp8DelayedLists &L, int gelem, int fp
                                      const float *hist, int hist_len, double eps, float *amax,
                                      float *inv_scale, cudaStream_t s);
 
+cudaError_t launch_emit_bf16(const ListView &p, const ListView &b, int64_t n_chunks, float *amax,
+                             bool use_slots, cudaStream_t s);
+
 cudaError_t launch_bounded_wait_selftest(int32_t *err, double limit_s, cudaStream_t s);
 cudaError_t launch_fp8_quant_groupwise(const void *x, int xelem, int64_t rows, int64_t cols,
                                        int64_t group, int fp8, double eps, uint8_t *out,

@@ -119,6 +119,8 @@ class AmpOptimizerStep:
             self._setup_delayed(fp8_shapes, stream)
         elif fp8_scaling != "dynamic":
             raise ValueError(fp8_scaling)
+        else:
+            self._emit_working_copies(stream)
 
     def _groups(self, grads):
         """1-D lists of the plain tensors and 2-D lists of the FP8 weights."""
@@ -141,18 +143,25 @@ class AmpOptimizerStep:
         self.amax_history = torch.zeros((self.n_fp8, self.hist_len), dtype=torch.float32,
                                         device=dev)
         self.delayed_groups = [self._groups(self.grads)]
-        # seed: bf16 = RNE(master), then one dynamic cast whose amax opens the history
-        j = 0
-        for i, sh in enumerate(self.fp8_shapes):
-            if sh is None:
-                continue
-            self.bf16[i].copy_(self.master[i])
-            A.fp8_quant_tensorwise(self.bf16[i].view(*sh), self.fp8_format, self.fp8[j],
-                                   self.fp8_t[j], self.inv_scale[j:j + 1], self.amax[j:j + 1],
-                                   eps=self.fp8_eps, stream=stream)
-            j += 1
+        # the first working copies; their amax opens the history
+        self._emit_working_copies(stream)
+
+    def _emit_working_copies(self, stream):
+        """The working copies before the first step, for the first forward
+        pass: bf16 = RNE(master) (amp_emit_bf16, which folds the FP8 weights'
+        amax) and the FP8 copies cast dynamically from that amax.  With
+        delayed scaling that amax is the first entry of each history.  amax is
+        left zeroed for the first step's fold."""
+        if self.bf16 is None:
+            return
+        A.amp_emit_bf16(self.L_master, self.L_b, self.amax if self.n_fp8 else None, stream=stream)
+        if not self.n_fp8:
+            return
+        A.fp8_quant_tensorwise_list(self.L_x8, self.L_q, self.L_qt, self.fp8_format, self.amax,
+                                    self.inv_scale, eps=self.fp8_eps, stream=stream)
         with torch.cuda.stream(stream) if stream is not None else _nullctx():
-            self.amax_history[:, 0].copy_(self.amax[:self.n_fp8])
+            if self.fp8_scaling == "delayed":
+                self.amax_history[:, 0].copy_(self.amax[:self.n_fp8])
             self.amax.zero_()
 
     @property

@@ -301,25 +301,34 @@ class AmpStepOracle:
             self.inv_scale = np.zeros(max(k, 1), np.float32)
         else:
             self.amax = None
+        # The working copies exist before the first step: the model's bf16
+        # parameters are the master rounded to bf16 ("从 AMP 到 Mixed
+        # Precision", "PyTorch AMP 与 FP32 Master Weights", mode B), and the
+        # FP8 weights are cast from that copy with its own amax
+        # ("FP8训练：量化、自动微分、Torchao" §2).
         # Delayed scaling ("第20章 量化与混合精度训练" §20.5.9): each FP8 weight
         # keeps the amax of its last hist_len steps (newest first) and is cast
         # with the scale of their maximum.  At construction there is no
-        # previous step, so the history starts from the amax of the initial
-        # bf16 copy, cast dynamically.
+        # previous step, so the history starts from the amax of that first
+        # bf16 copy.
         self.fp8_scaling = fp8_scaling
         self.hist_len = hist_len
         if fp8_scaling == "delayed":
             assert fp8_shapes is not None and emit_bf16
             self.hist = np.zeros((max(k, 1), hist_len), np.float32)
+        if emit_bf16:
+            for i in range(len(self.master)):
+                self.bf16[i] = encode("bf16", self.master[i])
+        if fp8_shapes is not None:
             for i, sh in enumerate(fp8_shapes):
                 if sh is None:
                     continue
-                self.bf16[i] = encode("bf16", self.master[i])
                 q, qt, inv, am = fp8_quant_tensorwise(self.bf16[i], "bf16", sh[0], sh[1],
                                                       self.fp8_format, self.fp8_eps, True)
                 s_ = self.slots[i]
                 self.fp8[i], self.fp8_t[i], self.inv_scale[s_] = q, qt, inv
-                self.hist[s_, 0] = am
+                if fp8_scaling == "delayed":
+                    self.hist[s_, 0] = am
 
     def run(self, grads):
         """Apply one step with the given scaled gradients; returns found_inf."""

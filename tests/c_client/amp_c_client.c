@@ -1,10 +1,17 @@
 /*
  * amp_c_client.c - a plain C caller of libampfp8.so: no Python, no torch.
  *
- * Reads a binary input file, runs `steps` mixed-precision optimizer steps
- * through the C ABI (amp_unscale_check, amp_adamw_master_step with bf16
- * emission and an amax slot, fp8_quant_tensorwise_list, amp_update_scale)
- * on the legacy default stream, and writes the final state to an output file.
+ * Reads a binary input file, opens the run with the first working copies
+ * (amp_emit_bf16 with the FP8 weights' amax, then fp8_quant_tensorwise_list),
+ * runs `steps` mixed-precision optimizer steps through the C ABI on the legacy
+ * default stream, and writes the final state to an output file.  Per step:
+ *   dynamic (default)  amp_unscale_check, amp_adamw_master_step with bf16
+ *                      emission and amax slots, fp8_quant_tensorwise_list,
+ *                      amp_update_scale;
+ *   delayed (argv[3])  amp_unscale_check, amp_adamw_master_step_fp8_delayed
+ *                      over the plain tensors and the FP8 weights with an
+ *                      amax history of one step (opened from the first
+ *                      copy's amax), amp_update_scale_fp8_history.
  *
  * Input  (little-endian): int32 n_tensors, int32 steps, then per tensor int64
  *        numel, int64 rows, int64 cols (cols == 0: no FP8 copy), then the
@@ -52,7 +59,11 @@ static void rd(void *p, size_t n, FILE *f) {
 }
 
 int main(int argc, char **argv) {
-    if (argc != 3) { fprintf(stderr, "usage: %s in.bin out.bin\n", argv[0]); return 2; }
+    if (argc != 3 && argc != 4) {
+        fprintf(stderr, "usage: %s in.bin out.bin [delayed]\n", argv[0]);
+        return 2;
+    }
+    const int delayed = argc == 4;
     FILE *in = fopen(argv[1], "rb");
     if (!in) return 2;
     int32_t n, steps;
@@ -111,19 +122,70 @@ int main(int argc, char **argv) {
     CK(amp_tensor_list_create(n8, qts, c8, r8, AMP_DT_E4M3FN, NULL, &Lqt));
 
     float *scale = dmalloc(4), *amax = dmalloc(4 * (n8 + 1)), *inv = dmalloc(4 * (n8 + 1));
+    float *hist = dmalloc(4 * (n8 + 1));                        /* amax history, one step */
     int32_t *tracker = dmalloc(4), *found = dmalloc(4), *stepc = dmalloc(4);
     const float s0 = 65536.0f;
     CU(cudaMemcpy(scale, &s0, 4, cudaMemcpyHostToDevice));
     const amp_adamw_hyper hy = {1e-3, 0.9, 0.999, 1e-8, 0.01};
+
+    /* the first working copies: bf16 = RNE(master) with the FP8 weights' amax,
+     * their FP8 copies; with delayed scaling that amax opens the history */
+    CK(amp_emit_bf16(Lp, Lb, amax, NULL));
+    CK(fp8_quant_tensorwise_list(Lx, Lq, Lqt, AMP_DT_E4M3FN, 1e-12, amax, inv, NULL, NULL));
+    if (delayed) CU(cudaMemcpy(hist, amax, 4 * (size_t)n8, cudaMemcpyDeviceToDevice));
+    CU(cudaMemset(amax, 0, 4 * (size_t)(n8 + 1)));
+
+    /* delayed scaling steps the plain tensors (1-D lists) and the FP8 weights
+     * (2-D lists over the same buffers) in one call */
+    amp_tensor_list Pp = NULL, Pm = NULL, Pv = NULL, Pg = NULL, Pb = NULL;
+    amp_tensor_list Fp = NULL, Fm = NULL, Fv = NULL, Fg = NULL;
+    if (delayed) {
+        int np_ = n - n8;
+        void **lp = malloc((np_ + 1) * sizeof(void *)), **lm = malloc((np_ + 1) * sizeof(void *)),
+             **lv = malloc((np_ + 1) * sizeof(void *)), **lg = malloc((np_ + 1) * sizeof(void *)),
+             **lb = malloc((np_ + 1) * sizeof(void *));
+        void **fp = malloc((n8 + 1) * sizeof(void *)), **fm = malloc((n8 + 1) * sizeof(void *)),
+             **fv = malloc((n8 + 1) * sizeof(void *)), **fg = malloc((n8 + 1) * sizeof(void *));
+        int64_t *ln = malloc((np_ + 1) * 8);
+        for (int i = 0, a = 0, c = 0; i < n; ++i) {
+            if (cols[i]) {
+                fp[c] = p[i]; fm[c] = m[i]; fv[c] = v[i]; fg[c] = g[i]; ++c;
+            } else {
+                lp[a] = p[i]; lm[a] = m[i]; lv[a] = v[i]; lg[a] = g[i]; lb[a] = b[i];
+                ln[a] = numel[i]; ++a;
+            }
+        }
+        CK(amp_tensor_list_create(np_, lp, ln, NULL, AMP_DT_F32, NULL, &Pp));
+        CK(amp_tensor_list_create(np_, lm, ln, NULL, AMP_DT_F32, NULL, &Pm));
+        CK(amp_tensor_list_create(np_, lv, ln, NULL, AMP_DT_F32, NULL, &Pv));
+        CK(amp_tensor_list_create(np_, lg, ln, NULL, AMP_DT_F16, NULL, &Pg));
+        CK(amp_tensor_list_create(np_, lb, ln, NULL, AMP_DT_BF16, NULL, &Pb));
+        CK(amp_tensor_list_create(n8, fp, r8, c8, AMP_DT_F32, NULL, &Fp));
+        CK(amp_tensor_list_create(n8, fm, r8, c8, AMP_DT_F32, NULL, &Fm));
+        CK(amp_tensor_list_create(n8, fv, r8, c8, AMP_DT_F32, NULL, &Fv));
+        CK(amp_tensor_list_create(n8, fg, r8, c8, AMP_DT_F16, NULL, &Fg));
+        free(lp); free(lm); free(lv); free(lg); free(lb); free(ln);
+        free(fp); free(fm); free(fv); free(fg);
+    }
+
     int32_t *fi_log = malloc(steps * 4);
     for (int k = 0; k < steps; ++k) {
         for (int i = 0; i < n; ++i) rd(hg[i], numel[i] * 2, in);
         CK(amp_tensor_list_copy_from_host(Lg, (const void *const *)hg, NULL));
         CK(amp_unscale_check(Lg, scale, found, 0, NULL));
         CU(cudaMemcpy(&fi_log[k], found, 4, cudaMemcpyDeviceToHost));   /* for the log only */
-        CK(amp_adamw_master_step(Lp, Lm, Lv, Lg, Lb, scale, found, stepc, &hy, amax, NULL));
-        CK(fp8_quant_tensorwise_list(Lx, Lq, Lqt, AMP_DT_E4M3FN, 1e-12, amax, inv, found, NULL));
-        CK(amp_update_scale(scale, tracker, found, 2.0f, 0.5f, 2, amax, n8, NULL));
+        if (delayed) {
+            CK(amp_adamw_master_step_fp8_delayed(Pp, Pm, Pv, Pg, Pb, Fp, Fm, Fv, Fg, Lx, Lq, Lqt,
+                                                 AMP_DT_E4M3FN, 1e-12, hist, 1, amax, inv, scale,
+                                                 found, stepc, &hy, NULL));
+            CK(amp_update_scale_fp8_history(scale, tracker, found, 2.0f, 0.5f, 2, amax, hist, n8,
+                                            1, NULL));
+        } else {
+            CK(amp_adamw_master_step(Lp, Lm, Lv, Lg, Lb, scale, found, stepc, &hy, amax, NULL));
+            CK(fp8_quant_tensorwise_list(Lx, Lq, Lqt, AMP_DT_E4M3FN, 1e-12, amax, inv, found,
+                                         NULL));
+            CK(amp_update_scale(scale, tracker, found, 2.0f, 0.5f, 2, amax, n8, NULL));
+        }
     }
     CU(cudaDeviceSynchronize());
     fclose(in);
@@ -168,8 +230,8 @@ int main(int argc, char **argv) {
         ++j;
     }
     fclose(out);
-    amp_tensor_list all[8] = {Lp, Lm, Lv, Lg, Lb, Lx, Lq, Lqt};
-    for (int i = 0; i < 8; ++i) CK(amp_tensor_list_destroy(all[i]));
+    amp_tensor_list all[17] = {Lp, Lm, Lv, Lg, Lb, Lx, Lq, Lqt, Pp, Pm, Pv, Pg, Pb, Fp, Fm, Fv, Fg};
+    for (int i = 0; i < 17; ++i) CK(amp_tensor_list_destroy(all[i]));   /* NULL is accepted */
     printf("ok %d steps\n", steps);
     return 0;
 }

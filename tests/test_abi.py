@@ -26,7 +26,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
-    assert len(names) == 25, names
+    assert len(names) == 26, names
     from loss_scaling_master_gb300._lib import EXPORTS
     assert sorted(EXPORTS) == names
     for n in names:
@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version(lib):
-    assert lib.amp_abi_version() == 9
+    assert lib.amp_abi_version() == 10
 
 
 def test_invalid_arguments_return_status(lib):
@@ -47,6 +47,7 @@ def test_invalid_arguments_return_status(lib):
     assert lib.amp_adamw_master_step(None, None, None, None, None, None, None, None,
                                      ctypes.byref(h), None, None) == EINVAL
     assert lib.amp_update_scale(None, None, None, 2.0, 0.5, 10, None, 0, None) == EINVAL
+    assert lib.amp_emit_bf16(None, None, None, None) == EINVAL
     dummy = P(16)
     assert lib.amp_update_scale(dummy, dummy, dummy, 2.0, 0.5, 0, None, 0, None) == EINVAL
     assert lib.amp_update_scale(dummy, dummy, dummy, 2.0, 0.5, 1, None, 3, None) == EINVAL
@@ -109,3 +110,48 @@ def test_binding_rejects_host_tensors_and_bad_buffers():
     with pytest.raises(ValueError, match="contiguous"):
         A.fp8_quant_rowwise(torch.zeros(4, 8, dtype=torch.bfloat16)[:, ::2], "e4m3fn", q, None,
                             f, f, f)
+
+
+def test_noalloc_binding_rejects_mismatched_lists():
+    """The allocation-free AdamW binding hands the library bare pointers, so it
+    checks every list against master (count, element counts, dtypes), one
+    gradient dtype, and that amax holds every named slot, before any call."""
+    import torch
+
+    import loss_scaling_master_gb300 as A
+    sizes = [5, 17]
+    f32 = lambda: [torch.zeros(k) for k in sizes]
+    g16 = [torch.zeros(k, dtype=torch.float16) for k in sizes]
+    b16 = [torch.zeros(k, dtype=torch.bfloat16) for k in sizes]
+    hyper = (1e-3, 0.9, 0.999, 1e-8, 0.0)
+    i32 = torch.zeros(1, dtype=torch.int32)
+
+    def call(master=None, m=None, v=None, g=None, b="default", **kw):
+        A.amp_adamw_master_step_noalloc(master or f32(), m or f32(), v or f32(), g or g16,
+                                        b16 if b == "default" else b, None, i32, i32, *hyper,
+                                        **kw)
+
+    with pytest.raises(ValueError, match="exp_avg: 1 tensors"):
+        call(m=[torch.zeros(5)])
+    with pytest.raises(ValueError, match=r"exp_avg_sq\[1\]: 16 elements"):
+        call(v=[torch.zeros(5), torch.zeros(16)])
+    with pytest.raises(ValueError, match=r"grads\[0\]: 4 elements"):
+        call(g=[torch.zeros(4, dtype=torch.float16), g16[1]])
+    with pytest.raises(ValueError, match=r"bf16_out\[1\]: 3 elements"):
+        call(b=[b16[0], torch.zeros(3, dtype=torch.bfloat16)])
+    with pytest.raises(ValueError, match=r"exp_avg\[0\]: dtype"):
+        call(m=[torch.zeros(5, dtype=torch.float64), torch.zeros(17)])
+    with pytest.raises(ValueError, match=r"bf16_out\[0\]: dtype"):
+        call(b=[torch.zeros(5, dtype=torch.float16), b16[1]])
+    with pytest.raises(ValueError, match=r"grads\[1\]: dtype"):
+        call(g=[g16[0], torch.zeros(17, dtype=torch.int16)])
+    with pytest.raises(ValueError, match="mixed dtypes"):
+        call(g=[g16[0], torch.zeros(17, dtype=torch.bfloat16)])
+    with pytest.raises(ValueError, match="amax_slots: 1 entries"):
+        call(amax_slots=[0], amax=torch.zeros(2))
+    with pytest.raises(ValueError, match="slot 2; amax holds 2"):
+        call(amax_slots=[0, 2], amax=torch.zeros(2))
+    with pytest.raises(ValueError, match="slot 0; amax holds 0"):
+        call(amax_slots=[0, -1])
+    with pytest.raises(ValueError, match="CUDA"):        # well-formed lists, host memory
+        call(amax_slots=[0, 1], amax=torch.zeros(2))

@@ -1,7 +1,8 @@
 """The C ABI used from plain C: a C program (tests/c_client/amp_c_client.c,
 built with gcc against include/ampfp8.h and libampfp8.so) runs the tiny
-configuration with an FP8 weight; its outputs must equal the oracle's bit
-for bit."""
+configuration with an FP8 weight, with dynamic FP8 scaling and, from the
+first working copies it emits itself, with delayed scaling; its outputs must
+equal the oracle's bit for bit."""
 import os
 import shutil
 import subprocess
@@ -16,7 +17,8 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def test_plain_c_client_matches_oracle(tmp_path):
+@pytest.mark.parametrize("mode", ["dynamic", "delayed"])
+def test_plain_c_client_matches_oracle(tmp_path, mode):
     from loss_scaling_master_gb300 import build as B
     lib = B.build()
     cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
@@ -32,7 +34,7 @@ def test_plain_c_client_matches_oracle(tmp_path):
     masters = host_master(cfg)
     orc = O.AmpStepOracle(masters, "f16", cfg.lr, cfg.beta1, cfg.beta2, cfg.eps, cfg.weight_decay,
                           cfg.init_scale, cfg.growth_factor, cfg.backoff_factor,
-                          cfg.growth_interval, fp8_shapes=shapes)
+                          cfg.growth_interval, fp8_shapes=shapes, fp8_scaling=mode, hist_len=1)
     grads, fi = [], []
     for k in range(1, cfg.steps + 1):
         g = host_grads(cfg, k, orc.scale)
@@ -47,7 +49,8 @@ def test_plain_c_client_matches_oracle(tmp_path):
         for g in grads:
             for t in g:
                 f.write(t.tobytes())
-    out = subprocess.run([exe, str(tmp_path / "in.bin"), str(tmp_path / "out.bin")],
+    out = subprocess.run([exe, str(tmp_path / "in.bin"), str(tmp_path / "out.bin")]
+                         + (["delayed"] if mode == "delayed" else []),
                          capture_output=True, text=True)
     assert out.returncode == 0, out.stderr
     raw = open(tmp_path / "out.bin", "rb").read()

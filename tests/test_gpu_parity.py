@@ -243,6 +243,50 @@ def test_adamw_bf16_emission_exhaustive_rounding_classes(A, dev):
         L.close()
 
 
+@pytest.mark.parametrize("misalign", [False, True])
+def test_emit_bf16_parity(A, dev, misalign):
+    """amp_emit_bf16: the bf16 working copy of the masters (the rounding-class
+    sweep in one tensor, ragged sizes around the chunk, specials at tails)
+    equals the oracle's RNE encoder, and the amax folded for slot tensors is
+    max|bf16| by the oracle's decoder, NaN propagating."""
+    rng = np.random.default_rng(23)
+    hi = np.arange(1 << 16, dtype=np.uint64) << 16
+    lows = np.array([0, 1, 0x7FFF, 0x8000, 0x8001, 0xFFFF], np.uint64)
+    sweep = (hi[:, None] | lows[None, :]).astype(np.uint32).ravel().view(np.float32)
+    sweep = sweep[np.isfinite(sweep)]
+    sizes = RAGGED + [3 * 16384 + 5]
+    master_h = [(rng.standard_normal(k) * 0.02).astype(np.float32) for k in sizes] + [sweep]
+    master_h[9][256] = np.inf           # +inf in a tail element
+    master_h[12][16382] = -np.inf
+    master_h[13][0] = np.nan            # NaN: its slot's amax is NaN
+    master_h[5][3] = 3.0e38             # rounds to bf16 inf
+    slots = [-1] * len(master_h)
+    for j, i in enumerate((4, 9, 13, 15, len(master_h) - 1)):
+        slots[i] = j
+    P = _device_views(master_h, "f32", dev, misalign)
+    B = _device_views([np.zeros(h.size, np.uint16) for h in master_h], "bf16", dev, misalign)
+    LP, LB = A.amp_tensor_list_create(P), A.amp_tensor_list_create(B)
+    A.amp_tensor_list_set_amax_slots(LB, slots)
+    amax = torch.zeros(5, device=dev)
+    A.amp_emit_bf16(LP, LB, amax)
+    got_amax = to_host_bits(amax).view(np.uint32)
+    for i, h in enumerate(master_h):
+        ref = O.encode("bf16", h)
+        assert np.array_equal(to_host_bits(B[i]), ref), i
+        assert np.array_equal(to_host_bits(P[i]).view(np.uint32), h.view(np.uint32)), i
+        if slots[i] >= 0:
+            mag = np.abs(O.decode("bf16", ref))
+            want = np.float32(np.nan) if np.isnan(mag).any() else np.float32(mag.max())
+            if np.isnan(want):
+                assert np.isnan(got_amax.view(np.float32)[slots[i]]), i
+            else:
+                assert got_amax[slots[i]] == want.view(np.uint32), i
+    with pytest.raises(A.AmpError):               # slots but no amax buffer
+        A.amp_emit_bf16(LP, LB, None)
+    LP.close()
+    LB.close()
+
+
 # -------------------------------------------------------------------- FP8
 FP8_SHAPES = [(1, 1), (3, 5), (17, 31), (128, 128), (127, 129), (256, 384), (129, 136),
               (300, 520), (64, 4096), (384, 256)]
@@ -403,6 +447,14 @@ def test_amp_step_composition_with_fp8(A, dev, fmt):
     orc = O.AmpStepOracle(master, "f16", hyper["lr"], hyper["beta1"], hyper["beta2"],
                           hyper["eps"], hyper["weight_decay"], 65536.0, 2.0, 0.5, 2,
                           fp8_shapes=fp8_shapes, fp8_format=fmt)
+    for i, sh in enumerate(fp8_shapes):              # the first working copies
+        assert np.array_equal(to_host_bits(st.bf16[i]), orc.bf16[i]), i
+        if sh is not None:
+            j = orc.slots[i]
+            assert np.array_equal(to_host_bits(st.fp8[j].view(torch.uint8)).ravel(), orc.fp8[i])
+            assert np.array_equal(to_host_bits(st.fp8_t[j].view(torch.uint8)).ravel(), orc.fp8_t[i])
+            assert to_host_bits(st.inv_scale)[j] == orc.inv_scale[j]
+    assert not to_host_bits(st.amax).any()
     for k in range(1, 8):
         gh = [(rng.standard_normal(n) * 1e-4 * orc.scale).astype(np.float16).view(np.uint16)
               for n in sizes]
@@ -512,11 +564,28 @@ def test_grad_norm_parity_and_determinism(A, dev, dt, misalign):
 
 @pytest.mark.parametrize("gdt,with_fp8", [("f16", False), ("bf16", False), ("f32", False),
                                           ("f16", True)])
-def test_clipped_step_composition(A, dev, gdt, with_fp8):
+def test_clipped_step_composition(A, dev, gdt, with_fp8, monkeypatch):
     """AmpOptimizerStep with max_norm vs the oracle's step with clipping, over
     steps where the factor is < 1, = 1 and a skipped step; every grad dtype,
-    and once with FP8 weights cast after the clipped update."""
+    and once with FP8 weights cast after the clipped update.
+
+    The clip factor comes from a sum of squares that matches the oracle within
+    a tolerance, so the GPU's bf16 copy may differ from the oracle's by the
+    allowed 1 ulp.  The FP8 cast after it is exact given its input, so on
+    every step that is not skipped the FP8 bytes, the transposed bytes and
+    inv_scale are compared with the oracle's quantizer run on the GPU's own
+    bf16 copy, and the GPU's folded amax with max|bf16| of that copy."""
     from loss_scaling_master_gb300 import AmpOptimizerStep
+    from loss_scaling_master_gb300 import step as step_mod
+    snap = {}
+    real_update = step_mod.A.amp_update_scale
+
+    def spy_update(*args, amax=None, **kw):
+        if amax is not None:
+            snap["amax"] = amax.clone()      # enqueued on the step's stream, before the clear
+        return real_update(*args, amax=amax, **kw)
+
+    monkeypatch.setattr(step_mod.A, "amp_update_scale", spy_update)
     rng = np.random.default_rng(51)
     sizes = [1000, 4096, 257, 40000]
     fp8_shapes = [None, (64, 64), None, (200, 200)] if with_fp8 else None
@@ -545,22 +614,31 @@ def test_clipped_step_composition(A, dev, gdt, with_fp8):
         assert (s["scale"], s["growth_tracker"], s["step"]) == (orc.scale, orc.tracker, orc.step)
         if k != 3:
             assert abs(np.sqrt(st.grad_sumsq.item()) - orc.grad_norm) <= 1e-6 * orc.grad_norm
+        if with_fp8 and k != 3:
+            gpu_amax = to_host_bits(snap["amax"])
+            n_cmp, j = 0, 0
+            for i, sh in enumerate(fp8_shapes):
+                if sh is None:
+                    continue
+                gb = to_host_bits(st.bf16[i])
+                assert_bf16_close(gb, orc.bf16[i], f"bf16[{i}] step {k}")
+                mag = np.abs(O.decode("bf16", gb))
+                ref_amax = np.float32(np.nan) if np.isnan(mag).any() else mag.max()
+                assert gpu_amax[j].view(np.uint32) == np.float32(ref_amax).view(np.uint32), (k, i)
+                q, qt, inv, _ = O.fp8_quant_tensorwise(gb, "bf16", sh[0], sh[1], "e4m3fn",
+                                                       1e-12, True, amax=float(gpu_amax[j]))
+                assert np.array_equal(to_host_bits(st.fp8[j].view(torch.uint8)).ravel(), q), (k, i)
+                assert np.array_equal(to_host_bits(st.fp8_t[j].view(torch.uint8)).ravel(), qt), (k, i)
+                assert to_host_bits(st.inv_scale)[j].view(np.uint32) == \
+                    np.float32(inv).view(np.uint32), (k, i)
+                n_cmp += 1
+                j += 1
+            assert n_cmp == 2
     for i in range(len(sizes)):
         assert_state_close(to_host_bits(st.master[i]), orc.master[i], f"master[{i}]")
         assert_state_close(to_host_bits(st.exp_avg[i]), orc.exp_avg[i], f"exp_avg[{i}]")
         assert_state_close(to_host_bits(st.exp_avg_sq[i]), orc.exp_avg_sq[i], f"exp_avg_sq[{i}]")
         assert_bf16_close(to_host_bits(st.bf16[i]), orc.bf16[i], f"bf16[{i}]")
-    if with_fp8:
-        # the cast is exact given the copy and amax: compare where the copies agree
-        j = 0
-        for i, sh in enumerate(fp8_shapes):
-            if sh is None:
-                continue
-            if np.array_equal(to_host_bits(st.bf16[i]), orc.bf16[i]):
-                assert np.array_equal(to_host_bits(st.fp8[j].view(torch.uint8)).ravel(), orc.fp8[i])
-                assert np.array_equal(to_host_bits(st.fp8_t[j].view(torch.uint8)).ravel(),
-                                      orc.fp8_t[i])
-            j += 1
     st.close()
 
 
@@ -600,6 +678,8 @@ def test_delayed_fp8_step_composition(A, dev, hist_len, gdt, fmt):
         assert np.array_equal(to_host_bits(st.amax_history), orc.hist)
 
     torch.cuda.synchronize()
+    for i in range(len(shapes)):                     # the first working copies (amp_emit_bf16)
+        assert np.array_equal(to_host_bits(st.bf16[i]), orc.bf16[i]), i
     check_fp8()                                      # the seeding cast
     for k in range(6):
         sigma = 1e-3 * orc.scale
