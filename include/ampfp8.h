@@ -295,10 +295,17 @@ amp_status amp_adamw_master_step_sr(amp_tensor_list master, amp_tensor_list exp_
  * elements in total; larger calls return AMP_EINVAL with a message.
  *   - No cudaMalloc/cudaFree or other allocating routine is called.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress) with that device current.
+ *   - The tables are uploaded with one cudaMemcpyAsync from pageable host
+ *     memory.  CUDA stages such a copy itself and may first wait for the
+ *     stream, so, unlike the handle-based entry points, a call can block the
+ *     host until the work already enqueued on `stream` has drained.
+ *   - It cannot be captured into a CUDA graph: on a capturing stream it
+ *     returns AMP_EINVAL and enqueues nothing (a captured copy would replay
+ *     from host memory freed when the call returns).
  *   - Every call shares the array: calls whose work can overlap on the GPU
- *     (unordered streams) race; order them on one stream. */
+ *     (unordered streams) race; order them on one stream.
+ *   - Host allocation failure of the tables returns AMP_ENOMEM. */
 amp_status amp_adamw_master_step_noalloc(int n, float *const *master, float *const *exp_avg,
                                          float *const *exp_avg_sq, const void *const *grads,
                                          amp_dtype grad_dtype, uint16_t *const *bf16_out,

@@ -20,15 +20,27 @@
 // chunks of 16384 elements (8,589,934,592 elements in all); larger calls are
 // rejected with AMP_EINVAL.
 //
-// Every call shares the array and it keeps the last call's contents.  Nothing
-// in it needs to start at zero: each call rewrites the tables it reads, and
-// the prologue writes the scalar block before the main kernel reads it.
+// Every call shares the array and it keeps the last call's contents.  Each
+// call rewrites the tables it reads, and the prologue writes the step scalars
+// before the main kernel reads them, so none of those need to start at zero.
+// The one word that does is the sticky error word next to the step scalars:
+// it relies on the array's static zero-initialisation, is set only by a
+// bounded wait that gives up, and is cleared only by amp_noalloc_check.
 // Calls whose work overlaps on the GPU (different streams without ordering)
 // race on the array; order them on one stream.
+//
+// The tables travel with one cudaMemcpyAsync from a pageable host vector
+// (pinning it would be an allocation).  CUDA stages a pageable copy through
+// its own buffers and may wait for the stream to drain before it returns, so
+// a call can block the host until earlier work on `stream` is done.  A copy
+// from pageable memory cannot be recorded into a CUDA graph, and a recorded
+// one would replay from a vector freed on return, so a call on a capturing
+// stream is refused with AMP_EINVAL before anything is enqueued.
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <new>
 #include <vector>
 
 #include "internal.h"
@@ -80,15 +92,14 @@ amp_status noalloc_fail(amp_status st, const char *fmt, ...) {
     return st;
 }
 
-}  // namespace
-
-extern "C" amp_status amp_adamw_master_step_noalloc(
-    int n, float *const *master, float *const *exp_avg, float *const *exp_avg_sq,
-    const void *const *grads, amp_dtype grad_dtype, uint16_t *const *bf16_out,
-    const int64_t *numel, const int32_t *amax_slots, const float *scale_dev,
-    const int32_t *found_inf_dev, int32_t *step_dev, const amp_adamw_hyper *hyper,
-    float *amax_dev, amp_stream_t stream) {
-    AMP_TRACE("amp_adamw_master_step_noalloc");
+// The body of amp_adamw_master_step_noalloc; its host vectors may throw
+// std::bad_alloc, which the entry point reports as AMP_ENOMEM.
+amp_status noalloc_step(int n, float *const *master, float *const *exp_avg,
+                        float *const *exp_avg_sq, const void *const *grads, amp_dtype grad_dtype,
+                        uint16_t *const *bf16_out, const int64_t *numel,
+                        const int32_t *amax_slots, const float *scale_dev,
+                        const int32_t *found_inf_dev, int32_t *step_dev,
+                        const amp_adamw_hyper *hyper, float *amax_dev, amp_stream_t stream) {
     const char *fn = "amp_adamw_master_step_noalloc";
     if (n < 0 || (n > 0 && (!master || !exp_avg || !exp_avg_sq || !grads || !numel)) ||
         !step_dev || !hyper)
@@ -108,7 +119,9 @@ extern "C" amp_status amp_adamw_master_step_noalloc(
         if (numel[i] > 0 && (!master[i] || !exp_avg[i] || !exp_avg_sq[i] || !grads[i] ||
                              (bf16_out && !bf16_out[i])))
             return noalloc_fail(AMP_EINVAL, "%s: NULL pointer of non-empty tensor %d", fn, i);
-        n_chunks += (numel[i] + amp::kChunk - 1) / amp::kChunk;
+        // ceil without forming numel + kChunk - 1, which could pass INT64_MAX;
+        // each term is below 2^50 and there are at most 1024 of them
+        n_chunks += numel[i] / amp::kChunk + (numel[i] % amp::kChunk != 0);
         if (amax_slots && bf16_out && amax_slots[i] >= 0) any_slot = true;
     }
     if (n_chunks > kNoallocMaxChunks)
@@ -118,8 +131,18 @@ extern "C" amp_status amp_adamw_master_step_noalloc(
     if (any_slot && !amax_dev)
         return noalloc_fail(AMP_EINVAL, "%s: amax slots given but amax_dev is NULL", fn);
 
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cap);
+    if (e != cudaSuccess)
+        return noalloc_fail(AMP_ECUDA, "%s: cudaStreamIsCapturing: %s", fn, cudaGetErrorString(e));
+    if (cap != cudaStreamCaptureStatusNone)
+        return noalloc_fail(AMP_EINVAL,
+                            "%s: the stream is capturing a CUDA graph; this entry point uploads "
+                            "its tables from pageable host memory and cannot be captured", fn);
+
     unsigned char *base = nullptr;
-    cudaError_t e = scratch_on_current_device(&base);
+    e = scratch_on_current_device(&base);
     if (e != cudaSuccess)
         return noalloc_fail(AMP_ECUDA, "%s: cudaGetSymbolAddress: %s", fn, cudaGetErrorString(e));
 
@@ -151,9 +174,9 @@ extern "C" amp_status amp_adamw_master_step_noalloc(
         for (int64_t k = 0; k * amp::kChunk < numel[i]; ++k) chunks.push_back(make_uint2(i, uint32_t(k)));
     put(o_chunks, chunks.data(), chunks.size() * sizeof(uint2));
 
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // Pageable source: the runtime stages it before returning, so `host` may
-    // go out of scope; the copy is ordered before the kernels on `s`.
+    // Pageable source: the runtime stages it before returning (waiting for the
+    // stream if it must), so `host` may go out of scope; the copy is ordered
+    // before the kernels on `s`.
     e = cudaMemcpyAsync(base + kAlign, host.data(), host.size(), cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess)
         return noalloc_fail(AMP_ECUDA, "%s: table upload: %s", fn, cudaGetErrorString(e));
@@ -183,6 +206,25 @@ extern "C" amp_status amp_adamw_master_step_noalloc(
                           reinterpret_cast<amp::AdamwStepScalars *>(base), amax_dev, any_slot, s);
     if (e != cudaSuccess) return noalloc_fail(AMP_ECUDA, "%s: %s", fn, cudaGetErrorString(e));
     return AMP_OK;
+}
+
+}  // namespace
+
+extern "C" amp_status amp_adamw_master_step_noalloc(
+    int n, float *const *master, float *const *exp_avg, float *const *exp_avg_sq,
+    const void *const *grads, amp_dtype grad_dtype, uint16_t *const *bf16_out,
+    const int64_t *numel, const int32_t *amax_slots, const float *scale_dev,
+    const int32_t *found_inf_dev, int32_t *step_dev, const amp_adamw_hyper *hyper,
+    float *amax_dev, amp_stream_t stream) {
+    AMP_TRACE("amp_adamw_master_step_noalloc");
+    try {
+        return noalloc_step(n, master, exp_avg, exp_avg_sq, grads, grad_dtype, bf16_out, numel,
+                            amax_slots, scale_dev, found_inf_dev, step_dev, hyper, amax_dev,
+                            stream);
+    } catch (const std::bad_alloc &) {
+        return noalloc_fail(AMP_ENOMEM,
+                            "amp_adamw_master_step_noalloc: host allocation of the tables failed");
+    }
 }
 
 extern "C" amp_status amp_noalloc_check(amp_stream_t stream) {
