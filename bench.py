@@ -9,8 +9,12 @@ AdamW (+bf16, +amax) -> FP8 quantization -> scale update, all resident in HBM.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload llama3_8b|llama_1b|gpt2_small|fp8_sweep] [--no-e2e]
+                    [--no-configs]
 
-Prints one JSON line.  Under torchrun (N > 1) every rank holds its own
+Prints one JSON line.  At N = 1 the default run also times, after freeing the
+8B state, the GPT-2-small and 1B Llama sets and the FP8 quantizer sweep
+(tensorwise, rowwise, g128), each under "configs" with its own roofline
+fraction and CPU-oracle baseline; the headline keys stay on the 8B step.  Under torchrun (N > 1) every rank holds its own
 parameter shard of the same size (weak scaling) and the per-step non-finite
 flag is combined across ranks with an all-reduce(MAX) before the update.
 """
@@ -92,6 +96,30 @@ def measured_peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return HBM_FALLBACK_GBS, "fallback"
+
+
+def host_facts() -> dict:
+    """nproc and CPU model of the host the CPU baseline runs on."""
+    import platform
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for ln in f:
+                    if ln.lower().startswith("model name"):
+                        model = ln.split(":", 1)[1].strip()
+                        break
+        except Exception:
+            pass
+    return {"host_nproc": os.cpu_count(), "cpu_model": model or platform.machine()}
 
 
 # ------------------------------------------------------------------ clocks
@@ -429,15 +457,21 @@ def run_e2e(args, step, info, stream, world):
     t1.record(stream)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
+    # Each copy's events bracket only its copies: the start event follows the
+    # wait for its buffer on the copy stream, so it completes once that wait
+    # is satisfied.  The copies run back to back on one stream inside the
+    # timed region, so their mean (the copy stream's busy time per step)
+    # cannot exceed ms_per_step.
     copy_ms = sorted(a.elapsed_time(b) for a, b in copy_ev)
+    busy = sum(copy_ms) / len(copy_ms)
     del host, bufs
     hbuf.close()
     return {"value": info["params"] * args.steps * world / (ms * 1e-3), "unit": "params/s",
             "ms_per_step": ms / args.steps, "h2d_bytes_per_step": nbytes,
             "d2h_bytes_per_step": 16,
-            "h2d_copy_ms": {"min": copy_ms[0], "median": copy_ms[len(copy_ms) // 2],
-                            "max": copy_ms[-1]},
+            "h2d_copy_ms": {"min": copy_ms[0], "mean_busy": busy, "max": copy_ms[-1]},
             "h2d_gbs_best": nbytes / copy_ms[0] / 1e6,
+            "h2d_gbs_mean": nbytes / busy / 1e6,
             "api": "amp_tensor_list_copy_from_host (one H2D copy per tensor from pinned huge-page "
                    "host memory, on a copy stream, double-buffered) + AmpOptimizerStep.step() "
                    "(C-ABI calls) + amp_read_state (D2H of {scale, tracker, step, found_inf})",
@@ -449,7 +483,8 @@ def run_fp8_sweep(args, rank, world, device):
     import torch
 
     import loss_scaling_master_gb300 as A
-    from workloads import FP8_SWEEP_SHAPES, FP8_SWEEP_ZERO_SHAPE, device_generator
+    from workloads import (FP8_SWEEP_SHAPES, FP8_SWEEP_ZERO_SHAPE, device_fill_sweep,
+                           device_generator)
 
     gen = device_generator(device, 99 + rank, 4)
     mats = []
@@ -458,7 +493,7 @@ def run_fp8_sweep(args, rank, world, device):
         if (r, c) == FP8_SWEEP_ZERO_SHAPE and len(mats) == len(FP8_SWEEP_SHAPES):
             x.zero_()
         else:
-            x.normal_(0.0, 1.0, generator=gen)
+            device_fill_sweep(x, gen)
         mats.append(x)
     outs = [(torch.empty(x.shape, dtype=torch.uint8, device=device),
              torch.empty((x.shape[1], x.shape[0]), dtype=torch.uint8, device=device))
@@ -528,7 +563,7 @@ def run_fp8_sweep(args, rank, world, device):
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "storage": "bf16 in, e4m3fn/e5m2 out",
-            "data": "synthetic N(0,1) bf16 + one all-zero matrix",
+            "data": "synthetic N(0,1) bf16 with 0.1 % of positions x100, + one all-zero matrix",
             "config": {"workload": "fp8_sweep [4096,4096],[8192,8192],[16384,5120],zero[4096,4096] "
                                    "x {e4m3fn,e5m2}", "l2": "flushed between steps"},
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
@@ -536,6 +571,48 @@ def run_fp8_sweep(args, rank, world, device):
             "clocks": clk.summary(),
             "bytes_per_elt": per_elt,
             "gpu_launches": args.steps * len(mats) * len(fmts) * (4 if rowwise else 1 if groupwise else 3)}
+
+
+# ------------------------------------------------- the other configs, 1 GPU
+def _condense(line: dict) -> dict:
+    keep = ("metric", "value", "unit", "steps", "warmup", "ms_per_step", "hbm_gbs_step",
+            "kernels_ms", "adamw_gbs", "bytes_per_elt", "roofline", "clocks", "gpu_launches",
+            "cpu_baseline", "storage")
+    d = {k: line[k] for k in keep if k in line}
+    d["workload"] = line["config"]["workload"]
+    if "per_step_bytes" in line["config"]:
+        d["per_step_bytes"] = line["config"]["per_step_bytes"]
+    return d
+
+
+def run_configs(args, device) -> dict:
+    """The configurations besides the 8B set, timed on one GPU in the same
+    process after the 8B state is freed: the GPT-2-small and 1B Llama
+    parameter sets (each its own device-timed step line; every timed step
+    updates, none is skipped) and the FP8 quantizer sweep at tensorwise,
+    rowwise and group-wise (g128) granularity.  Each carries its roofline
+    fraction and a CPU-oracle baseline."""
+    import gc
+
+    import torch
+    out = {}
+    for wl, steps in (("gpt2_small", 10), ("llama_1b", 50)):
+        gc.collect()
+        torch.cuda.empty_cache()
+        a = argparse.Namespace(**vars(args))
+        a.workload, a.steps, a.warmup = wl, steps, 3
+        a.no_e2e, a.clip, a.sr_seed, a.fp8_scaling = True, None, None, "dynamic"
+        a.cpu_seconds = min(args.cpu_seconds, 4.0)
+        out[wl] = _condense(run_ours(a, 0, 1, device))
+    for gran in ("tensorwise", "rowwise", "groupwise"):
+        gc.collect()
+        torch.cuda.empty_cache()
+        a = argparse.Namespace(**vars(args))
+        a.workload, a.fp8_granularity, a.steps, a.warmup = "fp8_sweep", gran, 20, 3
+        out[f"fp8_sweep_{gran}"] = _condense(run_fp8_sweep(a, 0, 1, device))
+    if not args.no_cpu_baseline:
+        out["fp8_sweep_tensorwise"]["cpu_baseline"] = cpu_baseline_sweep(min(args.cpu_seconds, 4.0))
+    return out
 
 
 # ------------------------------------------------------------ CPU baseline
@@ -576,9 +653,32 @@ def cpu_baseline(workload: str, seconds: float):
         el = time.perf_counter() - t0
         if el >= seconds or steps >= 50:
             break
-    return {"value": n * steps / el, "unit": "params/s", "cores": 1, "kind": "oracle",
-            "sample": f"{len(specs)} tensors of {cfg.name} layer 0 ({n:,} params, {n8:,} "
-                      f"FP8-emitted), {steps} full step(s) in {el:.1f} s, single-threaded C oracle"}
+    return dict({"value": n * steps / el, "unit": "params/s", "cores": 1, "kind": "oracle",
+                 "sample": f"{len(specs)} tensors of {cfg.name} layer 0 ({n:,} params, {n8:,} "
+                           f"FP8-emitted), {steps} full step(s) in {el:.1f} s, single-threaded "
+                           f"C oracle"}, **host_facts())
+
+
+def cpu_baseline_sweep(seconds: float):
+    """The oracle's tensorwise quantizer (amax, fp64 scale, e4m3fn cast,
+    transposed copy) on the sweep's [4096, 4096] matrix, single-threaded,
+    repeated until ~`seconds` have passed; GB/s at 6 bytes per element."""
+    import oracle as O
+    from workloads import fp8_sweep_host
+    r, c = 4096, 4096
+    x = fp8_sweep_host(r, c, seed=0)
+    calls, t0 = 0, time.perf_counter()
+    while True:
+        O.fp8_quant_tensorwise(x, "bf16", r, c, "e4m3fn", 1e-12, True)
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or calls >= 50:
+            break
+    return dict({"value": 6 * r * c * calls / el / 1e9, "unit": "GB/s", "cores": 1,
+                 "kind": "oracle",
+                 "sample": f"{calls} tensorwise e4m3fn quantizations (with the transposed copy) "
+                           f"of one [4096, 4096] bf16 matrix in {el:.1f} s, single-threaded "
+                           f"C oracle"}, **host_facts())
 
 
 def run_reference(args, rank, world):
@@ -605,8 +705,8 @@ def run_reference(args, rank, world):
             "vs_baseline": None, "dtype": "f32",
             "storage": storage_desc(args.workload),
             "data": "synthetic", "config": workload_config(args.workload, world),
-            "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": dict({"value": value, "unit": "params/s", "cores": 1,
+                                  "kind": "oracle", "sample": sample}, **host_facts()),
             "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "note": "the pages ship no runnable code; the reference arm is the CPU oracle"}
@@ -623,6 +723,9 @@ def main():
                              "llama3_8b_2layers"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="time only --workload (by default the 8B run also times the GPT-2, 1B "
+                         "and FP8-sweep configurations on one GPU, under 'configs')")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--fp8-scaling", default="dynamic", choices=["dynamic", "delayed"],
                     help="FP8 weight scaling: this step's amax (a separate cast pass) or the "
@@ -648,6 +751,9 @@ def main():
             import torch.distributed as dist
             dist.init_process_group("nccl", device_id=torch.device("cuda", local))
         line = run_ours(args, rank, world, torch.device("cuda", local))
+        if (world == 1 and args.workload == "llama3_8b" and not args.no_configs
+                and line is not None):
+            line["configs"] = run_configs(args, torch.device("cuda", local))
         if world > 1:
             import torch.distributed as dist
             dist.destroy_process_group()

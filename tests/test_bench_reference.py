@@ -31,6 +31,7 @@ def test_reference_arm_json_line():
     assert "bf16 grads" in d["storage"]
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == d["value"]
+    assert cb["host_nproc"] >= 1 and cb["cpu_model"]
     e = d["e2e"]
     assert e["value"] == d["value"] and e["unit"] == d["unit"]
     assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0

@@ -42,8 +42,12 @@ def test_step_bench_json_line():
     e = d["e2e"]
     assert e["value"] > 0 and e["unit"] == d["unit"]
     assert e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+    # copies run back to back inside the timed region: their busy time per
+    # step cannot exceed the step
+    assert e["h2d_copy_ms"]["mean_busy"] <= e["ms_per_step"] * (1 + 1e-6)
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0
+    assert cb["host_nproc"] >= 1 and cb["cpu_model"]
 
 
 def test_sweep_bench_json_line():

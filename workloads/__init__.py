@@ -231,3 +231,17 @@ def device_fill_normal(t, sigma: float, gen):
         tmp.normal_(0.0, sigma, generator=gen)
         flat[s:e].copy_(tmp)
     return t
+
+
+def device_fill_sweep(x, gen, outlier_frac: float = 1e-3, outlier_mult: float = 100.0):
+    """The sweep's matrix on the device: N(0,1) drawn in fp32, a seeded
+    fraction of positions (0.1 %, sign kept) multiplied by 100, then rounded
+    to x's dtype, as fp8_sweep_host does on the host."""
+    import torch
+    tmp = torch.empty(x.numel(), dtype=torch.float32, device=x.device)
+    tmp.normal_(0.0, 1.0, generator=gen)
+    k = max(1, int(round(outlier_frac * tmp.numel())))
+    idx = torch.randint(0, tmp.numel(), (k,), generator=gen, device=x.device).unique()
+    tmp[idx] *= outlier_mult
+    x.view(-1).copy_(tmp)
+    return x
