@@ -520,6 +520,8 @@ def run_fp8_sweep(args, rank, world, device):
     def one(ev=None):
         for f in fmts:
             for i, x in enumerate(mats):
+                if ev is not None:
+                    ev[(f, i)][0].record(stream)
                 if groupwise:
                     d = gw[i]
                     A.fp8_quant_groupwise(x, f, G, outs[i][0], outs[i][1], d["ar"], d["sr"],
@@ -531,11 +533,14 @@ def run_fp8_sweep(args, rank, world, device):
                 else:
                     A.fp8_quant_tensorwise(x, f, outs[i][0], outs[i][1], inv[i:i + 1],
                                            amax[i:i + 1], stream=stream)
+                if ev is not None:
+                    ev[(f, i)][1].record(stream)
 
     for _ in range(args.warmup):
         one()
     torch.cuda.synchronize()
     times = []
+    per_call = {(f, i): [] for f in fmts for i in range(len(mats))}
     with ClockSampler(torch.cuda.current_device()) as clk:
         for _ in range(args.steps):
             with torch.cuda.stream(stream):
@@ -547,6 +552,18 @@ def run_fp8_sweep(args, rank, world, device):
             b.record(stream)
             torch.cuda.synchronize()
             times.append(a.elapsed_time(b))
+    # the per-call breakdown comes from separate steps: events between the
+    # calls end each call's overlap with the next one's launch, so they are
+    # kept out of the timed steps above
+    for _ in range(max(3, args.steps // 2)):
+        with torch.cuda.stream(stream):
+            flush.fill_(1)
+        ev = {key: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for key in per_call}
+        one(ev)
+        torch.cuda.synchronize()
+        for key, (e0, e1) in ev.items():
+            per_call[key].append(e0.elapsed_time(e1))
     ms = statistics.mean(times)
     elems = sum(x.numel() for x in mats) * len(fmts)
     peak, kind = measured_peaks()
@@ -570,14 +587,22 @@ def run_fp8_sweep(args, rank, world, device):
                          "frac": gbs / peak, "peak_kind": kind, "traffic": None},
             "clocks": clk.summary(),
             "bytes_per_elt": per_elt,
+            # each call's own time (CUDA events around it, in extra steps
+            # after the timed ones; the first call of a step follows the L2
+            # flush) and its algorithmic rate
+            "per_call": {f"{'zero ' if i == len(mats) - 1 else ''}{mats[i].shape[0]}x"
+                         f"{mats[i].shape[1]} {f}": {
+                             "us": 1e3 * statistics.mean(v),
+                             "gbs": per_elt * mats[i].numel() / (statistics.mean(v) * 1e-3) / 1e9}
+                         for (f, i), v in per_call.items()},
             "gpu_launches": args.steps * len(mats) * len(fmts) * (4 if rowwise else 1 if groupwise else 3)}
 
 
 # ------------------------------------------------- the other configs, 1 GPU
 def _condense(line: dict) -> dict:
     keep = ("metric", "value", "unit", "steps", "warmup", "ms_per_step", "hbm_gbs_step",
-            "kernels_ms", "adamw_gbs", "bytes_per_elt", "roofline", "clocks", "gpu_launches",
-            "cpu_baseline", "storage")
+            "kernels_ms", "adamw_gbs", "bytes_per_elt", "per_call", "roofline", "clocks",
+            "gpu_launches", "cpu_baseline", "storage")
     d = {k: line[k] for k in keep if k in line}
     d["workload"] = line["config"]["workload"]
     if "per_step_bytes" in line["config"]:

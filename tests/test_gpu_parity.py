@@ -1249,6 +1249,20 @@ def test_fp8_groupwise_parity(A, dev, fmt, xdt, group):
 
 
 @pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
+@pytest.mark.parametrize("xdt,group", [("bf16", 128), ("f16", 64)])
+def test_fp8_groupwise_many_tiles_per_cta(A, dev, fmt, xdt, group):
+    """More tiles than one wave of CTAs, full tiles and ragged edge tiles
+    mixed, twice in a row on one matrix."""
+    rng = np.random.default_rng(150)
+    rows, cols = 4096 + 80, 2048 + 8               # 33 x 17 tiles, a ragged row and column
+    xh = _x_host(rng, rows, cols, xdt)
+    ref = O.fp8_quant_groupwise(xh, xdt, rows, cols, fmt, group, transposed=True)
+    for _ in range(2):
+        got = _run_groupwise(A, dev, xh, xdt, rows, cols, fmt, group, True)
+        _assert_same(got, ref, (rows, cols))
+
+
+@pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
 def test_fp8_groupwise_scale_over_many_amax_values(A, dev, fmt):
     """The kernel forms group scales with fp32 divisions (equal to the fp64
     recipe rounded to fp32, see its header); check that against the oracle's
