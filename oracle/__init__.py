@@ -80,6 +80,20 @@ def lib():
             L.orc_fp8_quant_tensorwise.argtypes = [P, ctypes.c_int, ctypes.c_int64,
                                                    ctypes.c_int64, ctypes.c_int,
                                                    ctypes.c_double, P, P, P, P, ctypes.c_int]
+            L.orc_fp8_quant_tensorwise_sr.argtypes = [P, ctypes.c_int, ctypes.c_int64,
+                                                      ctypes.c_int64, ctypes.c_int,
+                                                      ctypes.c_double, P, P, P, P, ctypes.c_int,
+                                                      ctypes.c_uint64, ctypes.c_int32,
+                                                      ctypes.c_int32]
+            L.orc_fp8_stochastic.restype = ctypes.c_uint8
+            L.orc_fp8_stochastic.argtypes = [ctypes.c_int, ctypes.c_float, ctypes.c_uint32]
+            L.orc_fp8_stochastic_list.argtypes = [ctypes.c_int, P, P, P, ctypes.c_int64]
+            L.orc_sr8_bits_list.argtypes = [ctypes.c_uint64, ctypes.c_int32, ctypes.c_int32,
+                                            ctypes.c_int64, ctypes.c_int64, P]
+            L.orc_adamw_master_step_ids.argtypes = (
+                [ctypes.c_int, P, P, P, P, ctypes.c_int, P, I64P, P, ctypes.c_int32, P]
+                + [ctypes.c_double] * 5 + [P, P, ctypes.c_float, ctypes.c_int, ctypes.c_uint64,
+                                           P])
             _lib = L
     return _lib
 
@@ -162,10 +176,13 @@ def clip_coef(sumsq: float, max_norm: float) -> float:
 def adamw_master_step(master, exp_avg, exp_avg_sq, grads, gdt: str, bf16_out, scale,
                       found_inf: int, step: int, lr, beta1, beta2, eps, wd,
                       amax_slot=None, amax: np.ndarray | None = None,
-                      clip: float | None = None, sr_seed: int | None = None) -> int:
+                      clip: float | None = None, sr_seed: int | None = None,
+                      sr_ids=None) -> int:
     """FP32-master AdamW over a tensor list (in place); returns the new step count.
     ``scale`` None means S = 1. ``bf16_out`` is a list of uint16 arrays or None.
-    ``clip`` is the fp32 gradient clipping factor (None: no clipping)."""
+    ``clip`` is the fp32 gradient clipping factor (None: no clipping).
+    ``sr_seed``: round the bf16 copy stochastically; ``sr_ids`` the tensor
+    word of each tensor's random counter (None: its list index)."""
     n = len(master)
     sc = None if scale is None else np.array([scale], np.float32)
     st = np.array([step], np.int32)
@@ -177,8 +194,10 @@ def adamw_master_step(master, exp_avg, exp_avg_sq, grads, gdt: str, bf16_out, sc
             _ptr(slots) if slots is not None else None,
             _ptr(amax) if amax is not None else None]
     if sr_seed is not None:
-        lib().orc_adamw_master_step_ex(*args, ctypes.c_float(1.0 if clip is None else clip), 1,
-                                       ctypes.c_uint64(sr_seed))
+        ids = None if sr_ids is None else np.ascontiguousarray(sr_ids, np.int32)
+        lib().orc_adamw_master_step_ids(*args, ctypes.c_float(1.0 if clip is None else clip), 1,
+                                        ctypes.c_uint64(sr_seed),
+                                        _ptr(ids) if ids is not None else None)
     elif clip is None:
         lib().orc_adamw_master_step(*args)
     else:
@@ -215,6 +234,42 @@ def fp8_quant_tensorwise(x: np.ndarray, xdt: str, rows: int, cols: int, fp8: str
     lib().orc_fp8_quant_tensorwise(_ptr(x), _CODES[xdt], rows, cols, _CODES[fp8], eps,
                                    _ptr(out), _ptr(out_t) if out_t is not None else None,
                                    _ptr(inv), _ptr(am), int(amax is not None))
+    return out, out_t, float(inv[0]), float(am[0])
+
+
+def fp8_stochastic(fp8: str, y: np.ndarray, u: np.ndarray) -> np.ndarray:
+    """Stochastic rounding of fp32 values y (already scaled) to FP8 bytes with
+    32 random bits each (hi exactly when u < floor(2^32 * distance ratio))."""
+    y = np.ascontiguousarray(y, np.float32)
+    u = np.ascontiguousarray(u, np.uint32)
+    assert y.shape == u.shape
+    out = np.empty(y.shape, np.uint8)
+    lib().orc_fp8_stochastic_list(_CODES[fp8], _ptr(y), _ptr(u), _ptr(out), y.size)
+    return out
+
+
+def sr8_bits(seed: int, step: int, tensor: int, k0: int, n: int) -> np.ndarray:
+    """The 32 random bits of elements k0 .. k0+n-1 of FP8 tensor `tensor` at `step`."""
+    out = np.empty(n, np.uint32)
+    lib().orc_sr8_bits_list(ctypes.c_uint64(seed), step, tensor, k0, n, _ptr(out))
+    return out
+
+
+def fp8_quant_tensorwise_sr(x: np.ndarray, xdt: str, rows: int, cols: int, fp8: str,
+                            seed: int, step: int, tensor: int, eps: float = 1e-12,
+                            transposed: bool = True, amax: float | None = None):
+    """fp8_quant_tensorwise with the stochastic cast (same amax / inv_scale).
+    Returns (q, q_t or None, inv_scale, amax)."""
+    x = np.ascontiguousarray(x)
+    assert x.size == rows * cols
+    out = np.empty(rows * cols, np.uint8)
+    out_t = np.empty(rows * cols, np.uint8) if transposed else None
+    inv = np.zeros(1, np.float32)
+    am = np.array([0.0 if amax is None else amax], np.float32)
+    lib().orc_fp8_quant_tensorwise_sr(_ptr(x), _CODES[xdt], rows, cols, _CODES[fp8], eps,
+                                      _ptr(out), _ptr(out_t) if out_t is not None else None,
+                                      _ptr(inv), _ptr(am), int(amax is not None),
+                                      ctypes.c_uint64(seed), step, tensor)
     return out, out_t, float(inv[0]), float(am[0])
 
 
@@ -272,7 +327,7 @@ class AmpStepOracle:
     def __init__(self, master, grad_dtype, lr, beta1, beta2, eps, weight_decay,
                  init_scale, growth_factor, backoff_factor, growth_interval,
                  emit_bf16=True, fp8_shapes=None, fp8_eps=1e-12, max_norm=None,
-                 fp8_scaling="dynamic", hist_len=1, fp8_format="e4m3fn"):
+                 fp8_scaling="dynamic", hist_len=1, fp8_format="e4m3fn", sr_seed=None):
         self.master = [np.array(m, np.float32, copy=True) for m in master]
         self.exp_avg = [np.zeros_like(m) for m in self.master]
         self.exp_avg_sq = [np.zeros_like(m) for m in self.master]
@@ -290,6 +345,10 @@ class AmpStepOracle:
         self.fp8_format = fp8_format
         self.max_norm = max_norm
         self.grad_norm = None
+        # Stochastic rounding ("第20章 量化与混合精度训练" §20.5.14) of the copies
+        # each step emits: the bf16 copy and the FP8 weights cast from it.  The
+        # first working copies, made before any step, keep round-to-nearest.
+        self.sr_seed = sr_seed
         if fp8_shapes is not None:
             self.slots, k = [], 0
             for sh in fp8_shapes:
@@ -339,10 +398,21 @@ class AmpStepOracle:
             ss = grad_sumsq(grads, self.gdt, self.scale)
             self.grad_norm = float(np.sqrt(ss))
             clip = clip_coef(ss, self.max_norm)
+        sr_ids = None
+        if self.sr_seed is not None and self.fp8_scaling == "delayed":
+            # the delayed step walks the plain tensors and the FP8 weights as
+            # two lists: plain tensor p draws as p, FP8 weight j as j | 2^30
+            sr_ids, p_idx = [], 0
+            for sh, sl in zip(self.fp8_shapes, self.slots):
+                if sh is None:
+                    sr_ids.append(p_idx)
+                    p_idx += 1
+                else:
+                    sr_ids.append(sl | (1 << 30))
         self.step = adamw_master_step(self.master, self.exp_avg, self.exp_avg_sq, grads,
                                       self.gdt, self.bf16, self.scale, fi, self.step,
                                       *self.hyper, amax_slot=self.slots, amax=self.amax,
-                                      clip=clip)
+                                      clip=clip, sr_seed=self.sr_seed, sr_ids=sr_ids)
         if self.fp8_shapes is not None and not fi:
             for i, sh in enumerate(self.fp8_shapes):
                 if sh is None:
@@ -353,8 +423,15 @@ class AmpStepOracle:
                     a = float("nan") if np.isnan(h).any() else float(h.max())
                 else:
                     a = float(self.amax[s])
-                q, qt, inv, _ = fp8_quant_tensorwise(self.bf16[i], "bf16", sh[0], sh[1],
-                                                     self.fp8_format, self.fp8_eps, True, amax=a)
+                if self.sr_seed is None:
+                    q, qt, inv, _ = fp8_quant_tensorwise(self.bf16[i], "bf16", sh[0], sh[1],
+                                                         self.fp8_format, self.fp8_eps, True,
+                                                         amax=a)
+                else:
+                    q, qt, inv, _ = fp8_quant_tensorwise_sr(self.bf16[i], "bf16", sh[0], sh[1],
+                                                            self.fp8_format, self.sr_seed,
+                                                            self.step, s, self.fp8_eps, True,
+                                                            amax=a)
                 self.fp8[i], self.fp8_t[i], self.inv_scale[s] = q, qt, inv
         if self.fp8_scaling == "delayed" and not fi:
             self.hist[:, 1:] = self.hist[:, :-1].copy()

@@ -323,6 +323,18 @@ void orc_adamw_master_step_clip(int n_tensors, float *const *master, float *cons
 /* As above; with stochastic != 0 the bf16 copy is rounded stochastically
  * (orc_bf16_stochastic, random bits of element k of tensor i at the new step
  * count t from sr_bits(seed, t, i, k)) instead of to nearest-even. */
+/* As orc_adamw_master_step_ex; sr_ids[i] (when not NULL) replaces i as the
+ * tensor word of the bf16 copy's random counter.  The delayed FP8 step walks
+ * its plain tensors and its FP8 weights as two lists: plain tensor p uses p,
+ * FP8 weight j uses j | 2^30. */
+void orc_adamw_master_step_ids(int n_tensors, float *const *master, float *const *exp_avg,
+                               float *const *exp_avg_sq, void *const *grads, int gdtype,
+                               uint16_t *const *bf16_out, const int64_t *numel,
+                               const float *scale, int32_t found_inf, int32_t *step,
+                               double lr, double beta1, double beta2, double eps, double wd,
+                               const int32_t *amax_slot, float *amax, float clip_coef,
+                               int stochastic, uint64_t seed, const int32_t *sr_ids);
+
 void orc_adamw_master_step_ex(int n_tensors, float *const *master, float *const *exp_avg,
                               float *const *exp_avg_sq, void *const *grads, int gdtype,
                               uint16_t *const *bf16_out, const int64_t *numel,
@@ -330,6 +342,19 @@ void orc_adamw_master_step_ex(int n_tensors, float *const *master, float *const 
                               double lr, double beta1, double beta2, double eps, double wd,
                               const int32_t *amax_slot, float *amax, float clip_coef,
                               int stochastic, uint64_t seed)
+{
+    orc_adamw_master_step_ids(n_tensors, master, exp_avg, exp_avg_sq, grads, gdtype, bf16_out,
+                              numel, scale, found_inf, step, lr, beta1, beta2, eps, wd, amax_slot,
+                              amax, clip_coef, stochastic, seed, NULL);
+}
+
+void orc_adamw_master_step_ids(int n_tensors, float *const *master, float *const *exp_avg,
+                               float *const *exp_avg_sq, void *const *grads, int gdtype,
+                               uint16_t *const *bf16_out, const int64_t *numel,
+                               const float *scale, int32_t found_inf, int32_t *step,
+                               double lr, double beta1, double beta2, double eps, double wd,
+                               const int32_t *amax_slot, float *amax, float clip_coef,
+                               int stochastic, uint64_t seed, const int32_t *sr_ids)
 {
     if (found_inf)
         return; /* skipped step: no state, output or counter changes */
@@ -360,7 +385,8 @@ void orc_adamw_master_step_ex(int n_tensors, float *const *master, float *const 
             exp_avg[i][k] = m;
             exp_avg_sq[i][k] = v;
             if (bf16_out && bf16_out[i]) {
-                uint16_t b = stochastic ? orc_bf16_stochastic(p, sr_bits(seed, t, i, k))
+                int32_t id = sr_ids ? sr_ids[i] : i;
+                uint16_t b = stochastic ? orc_bf16_stochastic(p, sr_bits(seed, t, id, k))
                                         : (uint16_t)fmt_encode(&FMT_BF16, (double)p);
                 bf16_out[i][k] = b;
                 if (slot >= 0) {
@@ -612,4 +638,137 @@ void orc_bf16_stochastic_list(const float *p, uint16_t *out, int64_t n, uint64_t
 {
     for (int64_t k = 0; k < n; ++k)
         out[k] = orc_bf16_stochastic(p[k], sr_bits(seed, step, tensor, k));
+}
+
+/* ------------------------------------------------------------------------ */
+/* Stochastic rounding of the FP8 weight copies.  "第20章 量化与混合精度训练"  */
+/* §20.5.14 rounds down or up with probability proportional to the distance  */
+/* (so the expected value is the input) and says it matters most the lower   */
+/* the precision, FP8 and FP4 included.  Reading: [FP8] §2's quantizer with   */
+/* its round-to-nearest cast replaced by that rule:                           */
+/*   y = x_f32 * scale (fp32), clamped to +-fp8_max, NaN propagating;         */
+/*   lo <= |y| < hi: the neighbouring FP8 magnitudes (|y| = fp8_max or on the */
+/*   grid: the result is |y| itself);                                        */
+/*   result = sign(y) * hi with probability                                   */
+/*       floor(2^32 * (|y| - lo) / (hi - lo)) / 2^32,                         */
+/*   else sign(y) * lo; NaN gives the canonical NaN.                          */
+/* With 32 random bits u the result is hi exactly when u is below that       */
+/* numerator.  The ratio is exact whenever it has at most 32 fractional      */
+/* bits, which holds for every |y| in the normal range of both formats (the  */
+/* fp32 significand keeps 21 bits below an E5M2 quantum, 20 below an E4M3FN  */
+/* one); below it, where fp32 keeps finer bits, the probability is the ratio */
+/* truncated to a multiple of 2^-32.                                         */
+/* Random bits: Philox4x32-10 (above) with counter {k/4 low, k/4 high, step, */
+/* tensor | 2^31} and key = seed; element k (row-major index within its     */
+/* tensor) takes output word k % 4.  Bit 31 of the last counter word keeps   */
+/* these draws apart from the bf16 copy's.  The transposed copy holds the    */
+/* same bytes as the row-major one (one draw per element).                   */
+/* ------------------------------------------------------------------------ */
+
+/* ascending finite non-negative magnitudes of an FP8 format (at most 128) */
+static int fp8_grid(const orc_fmt *f, double *g)
+{
+    int n = 0;
+    uint32_t codes = 1u << (f->ebits + f->mbits);   /* codes with sign bit clear */
+    for (uint32_t c = 0; c < codes; ++c) {
+        double v = fmt_decode(f, c);
+        if (isfinite(v))
+            g[n++] = v;                              /* decode is monotone in c */
+    }
+    return n;
+}
+
+uint8_t orc_fp8_stochastic(int fp8_dtype, float y, uint32_t u)
+{
+    const orc_fmt *f = fmt_of(fp8_dtype);
+    if (isnan(y))
+        return (uint8_t)f->nan_code;
+    double grid[256];
+    int n = fp8_grid(f, grid);
+    double a = fabs((double)y), fmax = fmt_max(f);
+    if (a > fmax)
+        a = fmax;
+    int i = 0;                                       /* largest grid[i] <= a */
+    while (i + 1 < n && grid[i + 1] <= a)
+        ++i;
+    double r = grid[i];
+    if (r < a) {
+        double ratio = (a - grid[i]) / (grid[i + 1] - grid[i]);   /* exact: the gap is 2^k */
+        double num = floor(ratio * 4294967296.0);
+        if ((double)u < num)
+            r = grid[i + 1];
+    }
+    return (uint8_t)fmt_encode(f, signbit(y) ? -r : r);
+}
+
+static uint32_t sr8_bits(uint64_t seed, int32_t step, int32_t tensor, int64_t k)
+{
+    uint64_t grp = (uint64_t)k >> 2;
+    uint32_t ctr[4] = {(uint32_t)grp, (uint32_t)(grp >> 32), (uint32_t)step,
+                       (uint32_t)tensor | 0x80000000u};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t o[4];
+    orc_philox4x32_10(ctr, key, o);
+    return o[k & 3];
+}
+
+/* orc_fp8_quant_tensorwise with the stochastic cast: the same amax, scale and
+ * inv_scale; element k of tensor `tensor` at optimizer step `step` rounds
+ * with sr8_bits(seed, step, tensor, k). */
+void orc_fp8_quant_tensorwise_sr(const void *x, int xdtype, int64_t rows, int64_t cols,
+                                 int fp8_dtype, double eps, uint8_t *out, uint8_t *out_t,
+                                 float *inv_scale, float *amax, int amax_given, uint64_t seed,
+                                 int32_t step, int32_t tensor)
+{
+    const orc_fmt *f = fmt_of(fp8_dtype);
+    int64_t n = rows * cols;
+    float a = 0.0f;
+    if (amax_given) {
+        a = *amax;
+    } else {
+        for (int64_t k = 0; k < n; ++k) {
+            float v = fabsf(load_as_f32(xdtype, x, k));
+            if (isnan(v) || isnan(a))
+                a = NAN;
+            else if (v > a)
+                a = v;
+        }
+        *amax = a;
+    }
+    double fmax = fmt_max(f);
+    double ad = (double)a;
+    double clamped = isnan(ad) ? ad : (ad < eps ? eps : ad);
+    double scale_d = fmax / clamped;
+    float s32 = (float)scale_d;
+    *inv_scale = (float)(1.0 / scale_d);
+    for (int64_t i = 0; i < rows; ++i) {
+        for (int64_t j = 0; j < cols; ++j) {
+            int64_t k = i * cols + j;
+            float y = load_as_f32(xdtype, x, k) * s32;
+            uint8_t q = orc_fp8_stochastic(fp8_dtype, y, sr8_bits(seed, step, tensor, k));
+            out[k] = q;
+            if (out_t)
+                out_t[j * rows + i] = q;
+        }
+    }
+}
+
+/* the 32 random bits of element k (exported for the pin tests) */
+uint32_t orc_sr8_bits(uint64_t seed, int32_t step, int32_t tensor, int64_t k)
+{
+    return sr8_bits(seed, step, tensor, k);
+}
+
+void orc_fp8_stochastic_list(int fp8_dtype, const float *y, const uint32_t *u, uint8_t *out,
+                             int64_t n)
+{
+    for (int64_t k = 0; k < n; ++k)
+        out[k] = orc_fp8_stochastic(fp8_dtype, y[k], u[k]);
+}
+
+void orc_sr8_bits_list(uint64_t seed, int32_t step, int32_t tensor, int64_t k0, int64_t n,
+                       uint32_t *out)
+{
+    for (int64_t k = 0; k < n; ++k)
+        out[k] = sr8_bits(seed, step, tensor, k0 + k);
 }

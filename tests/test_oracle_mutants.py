@@ -94,6 +94,16 @@ MUTANTS = [
     ("philox_key_weyl_swapped", C, "        k1 += 0xBB67AE85u;", "        k1 += 0x9E3779B9u;"),
     ("sr_rounds_up_on_grid", C, "uint32_t r = lo + ((u & 0xFFFFu) < frac ? 1u : 0u);",
      "uint32_t r = lo + ((u & 0xFFFFu) <= frac ? 1u : 0u);"),
+    # stochastic rounding of the FP8 copies
+    ("fp8_sr_rounds_up_at_the_threshold", C, "        if ((double)u < num)",
+     "        if ((double)u <= num)"),
+    ("fp8_sr_ratio_of_hi_not_gap", C,
+     "double ratio = (a - grid[i]) / (grid[i + 1] - grid[i]);",
+     "double ratio = (a - grid[i]) / grid[i + 1];"),
+    ("fp8_sr_sign_dropped", C, "    return (uint8_t)fmt_encode(f, signbit(y) ? -r : r);",
+     "    return (uint8_t)fmt_encode(f, r);"),
+    ("fp8_sr_stream_not_marked", C, "(uint32_t)tensor | 0x80000000u};", "(uint32_t)tensor};"),
+    ("fp8_sr_word_of_k_over_two", C, "    return o[k & 3];", "    return o[(k >> 1) & 3];"),
     # delayed scaling (the composed step, in Python)
     ("delayed_uses_current_amax", PY,
      '                if self.fp8_scaling == "delayed":\n                    h = self.hist[s]',

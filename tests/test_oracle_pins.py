@@ -701,3 +701,129 @@ def test_adamw_with_stochastic_rounding_keeps_master_and_rounds_copy():
 def bf16_ulp_steps(a, b):
     key = lambda x: np.where(x & 0x8000, -(x.astype(np.int64) & 0x7FFF), x.astype(np.int64) & 0x7FFF)
     return np.abs(key(a) - key(b))
+
+
+# --------------------------------------------- stochastic rounding of FP8
+def _torch_fp8_grid(tdt):
+    """Ascending finite non-negative magnitudes of an FP8 format, decoded by
+    torch's own casts (independent of the oracle's decoder)."""
+    v = torch.arange(128, dtype=torch.uint8).view(tdt).float().numpy().astype(np.float64)
+    return np.unique(v[np.isfinite(v)])
+
+
+FP8_SR_VALUES = {
+    # normal range, binade edges, the largest gap, ties, the subnormal range
+    "e4m3fn": [1.0 + 1e-3, 1.0625, 1.1, 255.9, 447.0, 300.1, 0.015625 + 1e-6, 0.0017, 2.0 ** -9 * 0.7,
+               -3.3, -0.123, 1.0e-30],
+    "e5m2": [1.0 + 1e-3, 1.125, 1.3, 57000.0, 40000.5, 0.000061, 2.0 ** -16 * 0.3, -7.7, -1.0e-6,
+             3.0e-20],
+}
+
+
+@pytest.mark.parametrize("fmt,tdt", [("e4m3fn", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)])
+def test_fp8_stochastic_probability_is_exact(fmt, tdt):
+    """'第20章 量化与混合精度训练' §20.5.14: round to the neighbour away from
+    zero with probability equal to the distance ratio.  For y between FP8
+    neighbours lo < |y| < hi (torch's decode), the result is hi exactly for
+    u < N and lo for u >= N, with N / 2^32 = (|y| - lo) / (hi - lo) computed
+    here in fp64; so over all 2^32 random words the fraction that rounds away
+    is that ratio (exact where the ratio has <= 32 fractional bits, i.e. every
+    value of the normal range; below it the ratio truncated to 2^-32)."""
+    grid = _torch_fp8_grid(tdt)
+    for yv in FP8_SR_VALUES[fmt]:
+        y = np.float32(yv)
+        a = abs(float(y))
+        j = np.searchsorted(grid, a, side="right") - 1
+        lo, hi = grid[j], grid[j + 1]
+        ratio = (a - lo) / (hi - lo)
+        n = int(np.floor(ratio * 2.0 ** 32))
+        probe = [0, max(n - 1, 0), n, min(n + 1, 2 ** 32 - 1), 2 ** 32 - 1]
+        out = O.fp8_stochastic(fmt, np.full(len(probe), y), np.array(probe, np.uint32))
+        dec = torch.from_numpy(out).view(tdt).float().numpy().astype(np.float64)
+        want = [hi if u < n else lo for u in probe]
+        assert np.array_equal(np.abs(dec), want), (yv, probe, dec, lo, hi, n)
+        assert np.all(np.signbit(dec) == np.signbit(y)) or lo == 0.0, yv
+    # normal range: the ratio has at most 21 fractional bits, so it is exact
+    y = np.float32(1.0 + 3 * 2.0 ** -23)
+    j = np.searchsorted(grid, float(y), side="right") - 1
+    ratio = (float(y) - grid[j]) / (grid[j + 1] - grid[j])
+    assert ratio * 2.0 ** 32 == np.floor(ratio * 2.0 ** 32)
+
+
+@pytest.mark.parametrize("fmt,tdt", [("e4m3fn", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)])
+def test_fp8_stochastic_is_unbiased_and_keeps_grid(fmt, tdt):
+    """The mean of many draws is the input (within 5 sigma); grid values,
+    zeros and the saturation of [FP8] §2's clamp are as the RNE cast gives
+    them for every random word; NaN is the canonical NaN."""
+    rng = np.random.default_rng(7)
+    grid = _torch_fp8_grid(tdt)
+    for yv in (1.0 + 1e-3, 3.14159, -0.0123, 0.7 * grid[1]):
+        y = np.float32(yv)
+        u = rng.integers(0, 2 ** 32, 400000, dtype=np.uint64).astype(np.uint32)
+        out = O.fp8_stochastic(fmt, np.full(u.size, y), u)
+        dec = torch.from_numpy(out).view(tdt).float().numpy().astype(np.float64)
+        a = abs(float(y))
+        j = np.searchsorted(grid, a, side="right") - 1
+        lo, hi = grid[j], grid[j + 1]
+        assert set(np.unique(np.abs(dec))) <= {lo, hi}, yv
+        p = (a - lo) / (hi - lo)
+        sd = (hi - lo) * np.sqrt(p * (1 - p) / u.size)
+        assert abs(dec.mean() - float(y)) <= 5 * sd + 1e-12, yv
+    fmax = O.fmt_max(fmt)
+    special = np.array([grid[5], -grid[40], grid[-1], 0.0, -0.0, fmax * 1.5, -np.inf, np.inf,
+                        np.nan], np.float32)
+    want = O.encode(fmt, np.clip(special, -fmax, fmax))                 # RNE of the clamp
+    for u in (0, 1, 2 ** 31, 2 ** 32 - 1):
+        got = O.fp8_stochastic(fmt, special, np.full(special.size, u, np.uint32))
+        assert np.array_equal(got, want), u
+    # torch's cast agrees on the saturated and on-grid values (NaN: canonical code)
+    tq = torch.from_numpy(np.clip(special[:-1], -fmax, fmax)).to(tdt).view(torch.uint8).numpy()
+    assert np.array_equal(want[:-1], tq)
+    assert want[-1] == {"e4m3fn": 0x7F, "e5m2": 0x7E}[fmt]
+
+
+@pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
+def test_fp8_quant_sr_reduces_to_rne_on_grid(fmt):
+    """With amax = fp8_max the scale is exactly 1, so x on the FP8 grid stays
+    on it: the stochastic quantizer then equals the RNE one byte for byte, for
+    any seed; its amax and inv_scale equal the RNE quantizer's for any x."""
+    codes = np.arange(256, dtype=np.uint8)
+    vals = O.decode(fmt, codes)
+    vals = vals[np.isfinite(vals)]
+    x = O.encode("bf16", vals)                    # every FP8 value is exact in bf16
+    rows, cols = 1, x.size
+    fmax = O.fmt_max(fmt)
+    q0, qt0, inv0, _ = O.fp8_quant_tensorwise(x, "bf16", rows, cols, fmt, amax=fmax)
+    for seed in (1, 99):
+        q1, qt1, inv1, _ = O.fp8_quant_tensorwise_sr(x, "bf16", rows, cols, fmt, seed, 3, 0,
+                                                     amax=fmax)
+        assert np.array_equal(q0, q1) and np.array_equal(qt0, qt1) and inv0 == inv1
+    rng = np.random.default_rng(8)
+    y = O.encode("bf16", rng.standard_normal(40 * 24).astype(F32))
+    a0 = O.fp8_quant_tensorwise(y, "bf16", 40, 24, fmt)
+    a1 = O.fp8_quant_tensorwise_sr(y, "bf16", 40, 24, fmt, 5, 2, 1)
+    assert a0[2] == a1[2] and a0[3] == a1[3]
+    # out_t holds the same bytes transposed (one draw per element)
+    assert np.array_equal(a1[1].reshape(24, 40).T.ravel(), a1[0])
+    # each byte is the RNE byte or the neighbour on the other side of the
+    # scaled value x * s32 (fp32 product, s32 = fp8_max / amax rounded to fp32)
+    s32 = np.float32(O.fmt_max(fmt) / np.float64(a0[3]))
+    exact = (O.decode("bf16", y) * s32).astype(np.float64)
+    d0 = O.decode(fmt, a0[0]).astype(np.float64)
+    d1 = O.decode(fmt, a1[0]).astype(np.float64)
+    assert np.all((d1 == d0) | (np.sign(d1 - exact) == -np.sign(d0 - exact)))
+    assert np.any(d1 != d0)
+
+
+def test_fp8_random_stream_is_apart_from_bf16_stream():
+    """The FP8 draws of element k use Philox output word k % 4 at counter
+    {k/4, step, tensor | 2^31}; the bf16 copy's draws use counter
+    {k/8, step, tensor}: no counter of one stream is a counter of the other."""
+    seed, step, tensor = 0x0123456789ABCDEF, 9, 4
+    bits = O.sr8_bits(seed, step, tensor, 0, 12)
+    key = [seed & 0xFFFFFFFF, seed >> 32]
+    for g in range(3):
+        w = O.philox4x32_10([g, 0, step, tensor | 0x80000000], key)
+        assert bits[4 * g:4 * g + 4].tolist() == w.tolist()
+    b16 = O.philox4x32_10([0, 0, step, tensor], key)
+    assert bits[:4].tolist() != b16.tolist()
