@@ -230,8 +230,7 @@ def run_ours(args, rank, world, device):
     delayed = step.fp8_scaling == "delayed"
     if delayed and args.clip is not None:
         raise SystemExit("--clip with --fp8-scaling delayed is not supported")
-    if args.sr_seed is not None and (delayed or args.clip is not None):
-        raise SystemExit("--sr-seed goes with the plain dynamic step")
+    sr = args.sr_seed is not None
     if delayed:
         info["bytes_adamw"] += 2 * info["fp8_params"]       # fp8 + fp8T written in the same pass
         info["bytes_quant"] = 0
@@ -263,19 +262,33 @@ def run_ours(args, rank, world, device):
         amax = step.amax if step.n_fp8 else None
         if delayed:
             P, F = step.delayed_groups[0]
-            A.amp_adamw_master_step_fp8_delayed(P, F, step.L_q, step.L_qt, "e4m3fn",
-                                                step.amax_history, step.hist_len, step.amax,
-                                                step.inv_scale, step.scale, step.found_inf,
-                                                step.step_count, *step.hyper,
-                                                fp8_eps=step.fp8_eps, stream=stream)
-        elif args.sr_seed is not None:
-            A.amp_adamw_master_step_sr(step.L_master, step.L_m, step.L_v, step.L_g, step.L_b,
-                                       step.scale, step.found_inf, step.step_count, *step.hyper,
-                                       args.sr_seed, amax=amax, stream=stream)
+            if sr:
+                A.amp_adamw_master_step_fp8_delayed_sr(P, F, step.L_q, step.L_qt, "e4m3fn",
+                                                       step.amax_history, step.hist_len,
+                                                       step.amax, step.inv_scale, step.scale,
+                                                       step.found_inf, step.step_count,
+                                                       *step.hyper, args.sr_seed,
+                                                       fp8_eps=step.fp8_eps, stream=stream)
+            else:
+                A.amp_adamw_master_step_fp8_delayed(P, F, step.L_q, step.L_qt, "e4m3fn",
+                                                    step.amax_history, step.hist_len, step.amax,
+                                                    step.inv_scale, step.scale, step.found_inf,
+                                                    step.step_count, *step.hyper,
+                                                    fp8_eps=step.fp8_eps, stream=stream)
         elif args.clip is None:
-            A.amp_adamw_master_step(step.L_master, step.L_m, step.L_v, step.L_g, step.L_b,
-                                    step.scale, step.found_inf, step.step_count, *step.hyper,
-                                    amax=amax, stream=stream)
+            if sr:
+                A.amp_adamw_master_step_sr(step.L_master, step.L_m, step.L_v, step.L_g, step.L_b,
+                                           step.scale, step.found_inf, step.step_count,
+                                           *step.hyper, args.sr_seed, amax=amax, stream=stream)
+            else:
+                A.amp_adamw_master_step(step.L_master, step.L_m, step.L_v, step.L_g, step.L_b,
+                                        step.scale, step.found_inf, step.step_count, *step.hyper,
+                                        amax=amax, stream=stream)
+        elif sr:
+            A.amp_adamw_master_step_clip_sr(step.L_master, step.L_m, step.L_v, step.L_g,
+                                            step.L_b, step.scale, step.found_inf,
+                                            step.step_count, *step.hyper, step.grad_sumsq,
+                                            args.clip, args.sr_seed, amax=amax, stream=stream)
         else:
             A.amp_adamw_master_step_clip(step.L_master, step.L_m, step.L_v, step.L_g, step.L_b,
                                          step.scale, step.found_inf, step.step_count,
@@ -284,9 +297,15 @@ def run_ours(args, rank, world, device):
         if ev is not None:
             ev[2].record(stream)
         if step.n_fp8 and not delayed:
-            A.fp8_quant_tensorwise_list(step.L_x8, step.L_q, step.L_qt, "e4m3fn", step.amax,
-                                        step.inv_scale, eps=step.fp8_eps,
-                                        skip_if=step.found_inf, stream=stream)
+            if sr:
+                A.fp8_quant_tensorwise_list_sr(step.L_x8, step.L_q, step.L_qt, "e4m3fn",
+                                               step.amax, step.inv_scale, args.sr_seed,
+                                               step.step_count, eps=step.fp8_eps,
+                                               skip_if=step.found_inf, stream=stream)
+            else:
+                A.fp8_quant_tensorwise_list(step.L_x8, step.L_q, step.L_qt, "e4m3fn", step.amax,
+                                            step.inv_scale, eps=step.fp8_eps,
+                                            skip_if=step.found_inf, stream=stream)
         if ev is not None:
             ev[3].record(stream)
         if delayed:
@@ -360,7 +379,8 @@ def run_ours(args, rank, world, device):
         "config": dict(workload_config(args.workload, world), per_step_bytes=total_bytes),
         "hbm_gbs_step": total_bytes / (ms_step * 1e-3) / 1e9,
         "grad_clip": args.clip,
-        "bf16_rounding": "stochastic" if args.sr_seed is not None else "nearest-even",
+        "rounding": ("stochastic (bf16 and FP8 copies)" if args.sr_seed is not None
+                     else "nearest-even"),
         "fp8_scaling": step.fp8_scaling,
         "kernels_ms": {"unscale_check": statistics.mean(k_check),
                        "adamw_master_step": adamw_ms,
@@ -759,7 +779,8 @@ def main():
                     choices=["tensorwise", "rowwise", "groupwise"],
                     help="scale granularity of the fp8_sweep workload")
     ap.add_argument("--sr-seed", type=int, default=None,
-                    help="round the bf16 copy stochastically (Philox4x32-10 with this seed)")
+                    help="round the bf16 and FP8 copies stochastically (Philox4x32-10 with this "
+                         "seed)")
     ap.add_argument("--clip", type=float, default=None,
                     help="also clip the unscaled gradients to this global L2 norm")
     args = ap.parse_args()

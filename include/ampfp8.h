@@ -281,6 +281,18 @@ amp_status amp_adamw_master_step_sr(amp_tensor_list master, amp_tensor_list exp_
                                     const amp_adamw_hyper *hyper, float *amax_dev, uint64_t seed,
                                     amp_stream_t stream);
 
+/* amp_adamw_master_step_clip with the bf16 copy rounded stochastically as in
+ * amp_adamw_master_step_sr (same random counters); the clip factor as in
+ * amp_adamw_master_step_clip.
+ * Errors: as amp_adamw_master_step_clip, and AMP_EINVAL for a NULL bf16_out. */
+amp_status amp_adamw_master_step_clip_sr(amp_tensor_list master, amp_tensor_list exp_avg,
+                                         amp_tensor_list exp_avg_sq, amp_tensor_list grads,
+                                         amp_tensor_list bf16_out, const float *scale_dev,
+                                         const int32_t *found_inf_dev, int32_t *step_dev,
+                                         const amp_adamw_hyper *hyper, float *amax_dev,
+                                         const double *grad_sumsq_dev, double max_norm,
+                                         uint64_t seed, amp_stream_t stream);
+
 /* Allocation-free form of amp_adamw_master_step.  The pages have no
  * counterpart: it exists for callers that cannot allocate device memory -
  * runtimes that serve all device memory from their own arena, loops that must
@@ -403,6 +415,30 @@ amp_status fp8_quant_tensorwise_list(amp_tensor_list x, amp_tensor_list out,
                                      const float *amax_dev, float *inv_scale_dev,
                                      const int32_t *skip_if_dev, amp_stream_t stream);
 
+/* fp8_quant_tensorwise_list with the FP8 bytes rounded stochastically
+ * ("第20章 量化与混合精度训练" §20.5.14: round down or up with probability
+ * proportional to the distance; the lower the precision, FP8 included, the
+ * more it matters).  The same amax, scale and inv_scale; each element's
+ * y = float(x) * float(scale_d), clamped to +-fp8_max, becomes the FP8 value
+ * away from zero with probability
+ *     floor(2^16 * (|y| - lo) / (hi - lo)) / 2^16
+ * (lo <= |y| < hi the neighbouring FP8 magnitudes: the distance ratio,
+ * truncated to a multiple of 2^-16, so the mean is low by less than 2^-16 of
+ * an FP8 quantum), else the one toward zero, with y's sign; values on the
+ * grid stay, NaN gives 0x7F / 0x7E.  Random bits: 16 per element from
+ * Philox4x32-10 (Salmon et al., SC 2011), key = seed, counter {k/8 (low,
+ * high 32 bits), t, j | 2^31} for row-major element k of tensor j of the
+ * list, t = *step_dev (the step count after this step's update); element k
+ * takes the 16-bit half (k%8)%2 (low first) of output word (k%8)/2, the
+ * layout of the bf16 copy's draws.  The transposed copy holds the same bytes.
+ * Errors: as fp8_quant_tensorwise_list, and AMP_EINVAL for a NULL step_dev or
+ * a list of 2^30 tensors or more. */
+amp_status fp8_quant_tensorwise_list_sr(amp_tensor_list x, amp_tensor_list out,
+                                        amp_tensor_list out_t, amp_dtype fp8_dtype, double eps,
+                                        const float *amax_dev, float *inv_scale_dev,
+                                        const int32_t *skip_if_dev, uint64_t seed,
+                                        const int32_t *step_dev, amp_stream_t stream);
+
 /* Delayed FP8 scaling fused into the update ("第20章 量化与混合精度训练"
  * §20.5.9: each FP8 op keeps an amax history and casts with the scale of the
  * previous steps' amax; §20.5.31 ScalingStrategy.DELAYED).  The pages have no
@@ -440,6 +476,23 @@ amp_status amp_adamw_master_step_fp8_delayed(
     amp_dtype fp8_dtype, double eps, const float *amax_history, int hist_len, float *amax_dev,
     float *inv_scale_dev, const float *scale_dev, const int32_t *found_inf_dev,
     int32_t *step_dev, const amp_adamw_hyper *hyper, amp_stream_t stream);
+
+/* amp_adamw_master_step_fp8_delayed with both copies rounded stochastically
+ * ("第20章 量化与混合精度训练" §20.5.14): the bf16 copy as in
+ * amp_adamw_master_step_sr, whose counter takes, as its tensor word, the list
+ * index p for plain tensors and j | 2^30 for FP8 weight j; the FP8 bytes cast
+ * from that copy with the delayed scale as in fp8_quant_tensorwise_list_sr
+ * (tensor word j | 2^31); t is the step count after this step.
+ * Errors: as amp_adamw_master_step_fp8_delayed, and AMP_EINVAL for a list of
+ * 2^30 tensors or more. */
+amp_status amp_adamw_master_step_fp8_delayed_sr(
+    amp_tensor_list master, amp_tensor_list exp_avg, amp_tensor_list exp_avg_sq,
+    amp_tensor_list grads, amp_tensor_list bf16_out, amp_tensor_list master8,
+    amp_tensor_list exp_avg8, amp_tensor_list exp_avg_sq8, amp_tensor_list grads8,
+    amp_tensor_list bf16_out8, amp_tensor_list fp8_out, amp_tensor_list fp8_t_out,
+    amp_dtype fp8_dtype, double eps, const float *amax_history, int hist_len, float *amax_dev,
+    float *inv_scale_dev, const float *scale_dev, const int32_t *found_inf_dev,
+    int32_t *step_dev, const amp_adamw_hyper *hyper, uint64_t seed, amp_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* A3: dynamic loss-scale state machine.  [CH20] §20.5.33, [MP06] §四.        */

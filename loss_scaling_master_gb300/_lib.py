@@ -31,6 +31,8 @@ EXPORTS = ("amp_tensor_list_create", "amp_tensor_list_set_amax_slots", "amp_tens
            "amp_read_state", "amp_scale_health", "fp8_quant_groupwise",
            "amp_unscale_check", "amp_unscale_check_norm", "amp_adamw_master_step", "amp_emit_bf16",
            "amp_adamw_master_step_clip", "amp_adamw_master_step_sr",
+           "amp_adamw_master_step_clip_sr", "amp_adamw_master_step_fp8_delayed_sr",
+           "fp8_quant_tensorwise_list_sr",
            "amp_adamw_master_step_noalloc", "amp_noalloc_check",
            "amp_adamw_master_step_fp8_delayed", "amp_update_scale_fp8_history",
            "fp8_quant_tensorwise", "fp8_quant_tensorwise_list", "fp8_quant_rowwise",
@@ -86,6 +88,14 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.amp_adamw_master_step_sr.argtypes = [P, P, P, P, P, P, P, P,
                                                ctypes.POINTER(amp_adamw_hyper), P,
                                                ctypes.c_uint64, P]
+        L.amp_adamw_master_step_clip_sr.argtypes = [P, P, P, P, P, P, P, P,
+                                                    ctypes.POINTER(amp_adamw_hyper), P, P, dbl,
+                                                    ctypes.c_uint64, P]
+        L.amp_adamw_master_step_fp8_delayed_sr.argtypes = (
+            [P] * 12 + [i32, dbl, P, i32, P, P, P, P, P, ctypes.POINTER(amp_adamw_hyper),
+                        ctypes.c_uint64, P])
+        L.fp8_quant_tensorwise_list_sr.argtypes = [P, P, P, i32, dbl, P, P, P, ctypes.c_uint64,
+                                                   P, P]
         L.amp_adamw_master_step_noalloc.argtypes = [i32, P, P, P, P, i32, P, P, P, P, P, P,
                                                     ctypes.POINTER(amp_adamw_hyper), P, P]
         L.amp_adamw_master_step_fp8_delayed.argtypes = [P] * 12 + [i32, dbl, P, i32, P, P, P, P,
@@ -313,6 +323,22 @@ def amp_adamw_master_step_clip(master: TensorList, exp_avg: TensorList, exp_avg_
                                              float(max_norm), _stream(stream)))
 
 
+def amp_adamw_master_step_clip_sr(master: TensorList, exp_avg: TensorList,
+                                  exp_avg_sq: TensorList, grads: TensorList, bf16_out: TensorList,
+                                  scale, found_inf, step, lr: float, beta1: float, beta2: float,
+                                  eps: float, weight_decay: float, grad_sumsq, max_norm: float,
+                                  seed: int, amax=None, stream=None):
+    h = amp_adamw_hyper(lr, beta1, beta2, eps, weight_decay)
+    _check("amp_adamw_master_step_clip_sr",
+           load().amp_adamw_master_step_clip_sr(master.handle, exp_avg.handle, exp_avg_sq.handle,
+                                                grads.handle, bf16_out.handle,
+                                                *_step_bufs(scale, found_inf, step),
+                                                ctypes.byref(h), _buf(amax, "amax", _F32),
+                                                _buf(grad_sumsq, "grad_sumsq", _F64),
+                                                float(max_norm), ctypes.c_uint64(seed),
+                                                _stream(stream)))
+
+
 def amp_adamw_master_step_sr(master: TensorList, exp_avg: TensorList, exp_avg_sq: TensorList,
                              grads: TensorList, bf16_out: TensorList, scale, found_inf, step,
                              lr: float, beta1: float, beta2: float, eps: float,
@@ -428,6 +454,26 @@ def amp_adamw_master_step_fp8_delayed(plain, fp8_group, fp8_out: TensorList,
                *_step_bufs(scale, found_inf, step), ctypes.byref(h), _stream(stream)))
 
 
+def amp_adamw_master_step_fp8_delayed_sr(plain, fp8_group, fp8_out: TensorList,
+                                         fp8_t_out: TensorList | None, fp8_dtype: str,
+                                         amax_history, hist_len: int, amax, inv_scale, scale,
+                                         found_inf, step, lr: float, beta1: float, beta2: float,
+                                         eps: float, weight_decay: float, seed: int,
+                                         fp8_eps: float = 1e-12, stream=None):
+    """amp_adamw_master_step_fp8_delayed with the bf16 and FP8 copies rounded
+    stochastically (Philox4x32-10 with this 64-bit seed)."""
+    h = amp_adamw_hyper(lr, beta1, beta2, eps, weight_decay)
+    _check("amp_adamw_master_step_fp8_delayed_sr",
+           load().amp_adamw_master_step_fp8_delayed_sr(
+               *[x.handle for x in plain], *[x.handle for x in fp8_group], fp8_out.handle,
+               fp8_t_out.handle if fp8_t_out else None, DT[fp8_dtype], fp8_eps,
+               _buf(amax_history, "amax_history", _F32, len(fp8_out) * int(hist_len)),
+               int(hist_len), _buf(amax, "amax", _F32, len(fp8_out)),
+               _buf(inv_scale, "inv_scale", _F32, len(fp8_out)),
+               *_step_bufs(scale, found_inf, step), ctypes.byref(h), ctypes.c_uint64(seed),
+               _stream(stream)))
+
+
 def amp_update_scale_fp8_history(scale, growth_tracker, found_inf, growth_factor: float,
                                  backoff_factor: float, growth_interval: int, amax,
                                  amax_history, n_fp8: int, hist_len: int, stream=None):
@@ -508,6 +554,21 @@ def fp8_quant_tensorwise_list(x: TensorList, out: TensorList, out_t: TensorList 
                                             DT[fp8_dtype], eps, _buf(amax, "amax", _F32, len(x)),
                                             _buf(inv_scale, "inv_scale", _F32, len(x)),
                                             _buf(skip_if, "skip_if", _I32), _stream(stream)))
+
+
+def fp8_quant_tensorwise_list_sr(x: TensorList, out: TensorList, out_t: TensorList | None,
+                                 fp8_dtype: str, amax, inv_scale, seed: int, step,
+                                 eps: float = 1e-12, skip_if=None, stream=None):
+    """fp8_quant_tensorwise_list with stochastically rounded FP8 bytes; step is
+    the device step counter whose value keys the random draws."""
+    _check("fp8_quant_tensorwise_list_sr",
+           load().fp8_quant_tensorwise_list_sr(x.handle, out.handle,
+                                               out_t.handle if out_t else None, DT[fp8_dtype],
+                                               eps, _buf(amax, "amax", _F32, len(x)),
+                                               _buf(inv_scale, "inv_scale", _F32, len(x)),
+                                               _buf(skip_if, "skip_if", _I32),
+                                               ctypes.c_uint64(seed), _buf(step, "step", _I32),
+                                               _stream(stream)))
 
 
 def amp_update_scale(scale, growth_tracker, found_inf, growth_factor: float,

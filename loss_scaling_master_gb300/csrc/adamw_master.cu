@@ -397,7 +397,26 @@ struct Fp8StepParams {
     const float *tscale;  // per tensor: the fp32 cast scale from the history
     float *amax;          // per tensor: max|bf16| of this step, for the history
     float decay, b1, omb1, b2, omb2, eps;
+    uint64_t sr_seed;     // stochastic rounding of the bf16 and FP8 copies
 };
+
+// Tensor word of the bf16 copy's random counter for FP8 weight t of the
+// delayed step (its plain tensors use their own list index, below 2^30).
+constexpr uint32_t kSrFp8GroupBit = 0x40000000u;
+
+// Eight bf16 values (a 16-byte word group of elements k0 .. k0+7 of FP8
+// weight `tensor`) -> eight stochastically rounded fp8 bytes of x * s32.
+template <int FT>
+__device__ __forceinline__ uint2 bf16x8_to_fp8x8_sr(const uint4 &b, float s32, uint64_t seed,
+                                                    int32_t step, int tensor, int64_t k0) {
+    const uint32_t w[4] = {b.x, b.y, b.z, b.w};
+    float y[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        mul2_rn(bf16_bits_to_f32(w[j] & 0xFFFFu), bf16_bits_to_f32(w[j] >> 16), s32, s32,
+                y[2 * j], y[2 * j + 1]);
+    return fp8x8_stochastic<FT>(y, seed, step, tensor, k0);
+}
 
 // One CTA: thread 0 the step scalars; every thread a strided share of the
 // FP8 tensors' scales from their amax histories (NaN propagating max).
@@ -422,8 +441,8 @@ __global__ void adamw_fp8_prologue_kernel(const int32_t *found_inf, int32_t *ste
     }
 }
 
-template <int GT, int FT>
-__global__ void __launch_bounds__(kThreads) adamw_fp8_tile_kernel(Fp8StepParams P) {
+template <int GT, int FT, bool SR>
+__device__ __forceinline__ void adamw_fp8_tile(const Fp8StepParams &P) {
     pdl_wait();
     pdl_trigger();
     const AdamwStepScalars sc = *P.scal;
@@ -470,10 +489,23 @@ __global__ void __launch_bounds__(kThreads) adamw_fp8_tile_kernel(Fp8StepParams 
             Group<GT> a, b;
             load_group<GT>(a, pp, mp, vp, gp, ea);
             load_group<GT>(b, pp, mp, vp, gp, eb);
-            const uint4 oa = compute_store_group<GT, true>(a, pp, mp, vp, bp, ea, s, amax2);
-            const uint4 ob = compute_store_group<GT, true>(b, pp, mp, vp, bp, eb, s, amax2);
-            const uint2 qa = bf16x8_to_fp8x8<FT>(oa, s32);
-            const uint2 qb = bf16x8_to_fp8x8<FT>(ob, s32);
+            uint2 qa, qb;
+            if constexpr (SR) {
+                const int32_t bid = int32_t(uint32_t(t) | kSrFp8GroupBit);
+                const uint4 ra = sr_random8(P.sr_seed, sc.t, bid, ea >> 3);
+                const uint4 rbv = sr_random8(P.sr_seed, sc.t, bid, eb >> 3);
+                const uint4 oa = compute_store_group<GT, true, true>(a, pp, mp, vp, bp, ea, s,
+                                                                     amax2, &ra);
+                const uint4 ob = compute_store_group<GT, true, true>(b, pp, mp, vp, bp, eb, s,
+                                                                     amax2, &rbv);
+                qa = bf16x8_to_fp8x8_sr<FT>(oa, s32, P.sr_seed, sc.t, t, ea);
+                qb = bf16x8_to_fp8x8_sr<FT>(ob, s32, P.sr_seed, sc.t, t, eb);
+            } else {
+                const uint4 oa = compute_store_group<GT, true>(a, pp, mp, vp, bp, ea, s, amax2);
+                const uint4 ob = compute_store_group<GT, true>(b, pp, mp, vp, bp, eb, s, amax2);
+                qa = bf16x8_to_fp8x8<FT>(oa, s32);
+                qb = bf16x8_to_fp8x8<FT>(ob, s32);
+            }
             *reinterpret_cast<uint2 *>(qp + ea) = qa;
             *reinterpret_cast<uint2 *>(qp + eb) = qb;
             if (qtp) {
@@ -490,8 +522,18 @@ __global__ void __launch_bounds__(kThreads) adamw_fp8_tile_kernel(Fp8StepParams 
             const int64_t i = r0 + (idx >> 7), j = c0 + (idx & (kTile - 1));
             if (i < rows && j < cols) {
                 const int64_t e = i * cols + j;
-                const uint16_t bv = scalar_elem<GT, true>(pp, mp, vp, gp, bp, e, s, amax1);
-                const uint8_t q8 = quant1<FT>(bf16_bits_to_f32(bv), s32);
+                uint16_t bv;
+                uint8_t q8;
+                if constexpr (SR) {
+                    bv = scalar_elem<GT, true, true>(
+                        pp, mp, vp, gp, bp, e, s, amax1,
+                        sr_u16(P.sr_seed, sc.t, int(uint32_t(t) | kSrFp8GroupBit), e));
+                    q8 = uint8_t(fp8_stochastic<FT>(__fmul_rn(bf16_bits_to_f32(bv), s32),
+                                                    sr8_word(P.sr_seed, sc.t, t, e)));
+                } else {
+                    bv = scalar_elem<GT, true>(pp, mp, vp, gp, bp, e, s, amax1);
+                    q8 = quant1<FT>(bf16_bits_to_f32(bv), s32);
+                }
                 qp[e] = q8;
                 if (qtp) qtp[j * rows + i] = q8;
             }
@@ -501,6 +543,18 @@ __global__ void __launch_bounds__(kThreads) adamw_fp8_tile_kernel(Fp8StepParams 
     a = warp_max_u32(a);
     if ((threadIdx.x & 31) == 0 && a != 0)
         atomicMax(reinterpret_cast<unsigned int *>(P.amax) + t, a << 16);
+}
+
+template <int GT, int FT>
+__global__ void __launch_bounds__(kThreads) adamw_fp8_tile_kernel(Fp8StepParams P) {
+    adamw_fp8_tile<GT, FT, false>(P);
+}
+
+// The stochastic form is held to 128 registers, so two CTAs share an SM as
+// with the plain form (left to itself it took 143).
+template <int GT, int FT>
+__global__ void __launch_bounds__(kThreads, 2) adamw_fp8_tile_sr_kernel(Fp8StepParams P) {
+    adamw_fp8_tile<GT, FT, true>(P);
 }
 
 // Self-test of the bounded wait: a barrier that nothing completes (one
@@ -586,7 +640,8 @@ cudaError_t launch_adamw_fp8_delayed(const Fp8DelayedLists &L, int gelem, int fp
                                      const float *scale, const int32_t *found_inf, int32_t *step,
                                      const AdamwConsts &c, AdamwStepScalars *scal,
                                      const float *hist, int hist_len, double eps, float *amax,
-                                     float *inv_scale, cudaStream_t s) {
+                                     float *inv_scale, cudaStream_t s, bool stochastic,
+                                     uint64_t seed) {
     const float fmax = fp8 == kE4M3 ? fp8_max<kE4M3>() : fp8_max<kE5M2>();
     launch_pdl(adamw_fp8_prologue_kernel, dim3(1), dim3(256), 0, s, found_inf, step, c.lr, c.beta1,
                c.beta2, scal, hist, hist_len, L.n8, make_eps_floor(eps, fmax), fmax, L.tscale,
@@ -595,7 +650,7 @@ cudaError_t launch_adamw_fp8_delayed(const Fp8DelayedLists &L, int gelem, int fp
     if (e != cudaSuccess) return e;
     if (L.n_plain_chunks > 0) {
         e = launch_adamw_main(L.p, L.m, L.v, L.g, &L.b, L.n_plain_chunks, gelem, scale, c, scal,
-                              nullptr, false, s);
+                              nullptr, false, s, stochastic, seed);
         if (e != cudaSuccess) return e;
     }
     if (L.n_tiles == 0) return cudaSuccess;
@@ -618,14 +673,20 @@ cudaError_t launch_adamw_fp8_delayed(const Fp8DelayedLists &L, int gelem, int fp
     P.b2 = c.b2;
     P.omb2 = c.omb2;
     P.eps = c.eps;
+    P.sr_seed = seed;
     const dim3 grid((unsigned)L.n_tiles), block(kThreads);
     // A plain launch: with programmatic dependent launch this kernel ran 6 %
     // slower on GB300 (30.7 -> 32.5 ms on the 8B set), while the chunked pass
     // before it gained nothing from the overlap.
-#define AMP_FP8_LAUNCH(GT)                                                            \
-    do {                                                                              \
-        if (fp8 == kE4M3) adamw_fp8_tile_kernel<GT, kE4M3><<<grid, block, 0, s>>>(P); \
-        else adamw_fp8_tile_kernel<GT, kE5M2><<<grid, block, 0, s>>>(P);              \
+#define AMP_FP8_LAUNCH(GT)                                                                  \
+    do {                                                                                    \
+        if (stochastic) {                                                                   \
+            if (fp8 == kE4M3) adamw_fp8_tile_sr_kernel<GT, kE4M3><<<grid, block, 0, s>>>(P);   \
+            else adamw_fp8_tile_sr_kernel<GT, kE5M2><<<grid, block, 0, s>>>(P);              \
+        } else {                                                                            \
+            if (fp8 == kE4M3) adamw_fp8_tile_kernel<GT, kE4M3><<<grid, block, 0, s>>>(P);   \
+            else adamw_fp8_tile_kernel<GT, kE5M2><<<grid, block, 0, s>>>(P);                \
+        }                                                                                   \
     } while (0)
     if (gelem == kF32) AMP_FP8_LAUNCH(kF32);
     else if (gelem == kF16) AMP_FP8_LAUNCH(kF16);

@@ -82,7 +82,7 @@ extern "C" {
 
 const char *amp_last_error(void) { return g_err; }
 
-int amp_abi_version(void) { return 10; }
+int amp_abi_version(void) { return 11; }
 
 // A [rows, cols] shape the launch arithmetic can hold: non-negative, each side
 // below 2^48 and rows * cols without int64 overflow.
@@ -402,16 +402,14 @@ amp_status amp_adamw_master_step_clip(amp_tensor_list master, amp_tensor_list ex
                        step_dev, hyper, amax_dev, grad_sumsq_dev, max_norm, stream);
 }
 
-amp_status amp_adamw_master_step_fp8_delayed(
-    amp_tensor_list master, amp_tensor_list exp_avg, amp_tensor_list exp_avg_sq,
+static amp_status delayed_entry(
+    const char *fn, amp_tensor_list master, amp_tensor_list exp_avg, amp_tensor_list exp_avg_sq,
     amp_tensor_list grads, amp_tensor_list bf16_out, amp_tensor_list master8,
     amp_tensor_list exp_avg8, amp_tensor_list exp_avg_sq8, amp_tensor_list grads8,
     amp_tensor_list bf16_out8, amp_tensor_list fp8_out, amp_tensor_list fp8_t_out,
     amp_dtype fp8_dtype, double eps, const float *amax_history, int hist_len, float *amax_dev,
     float *inv_scale_dev, const float *scale_dev, const int32_t *found_inf_dev, int32_t *step_dev,
-    const amp_adamw_hyper *hyper, amp_stream_t stream) {
-    AMP_TRACE("amp_adamw_master_step_fp8_delayed");
-    const char *fn = "amp_adamw_master_step_fp8_delayed";
+    const amp_adamw_hyper *hyper, amp_stream_t stream, bool stochastic, uint64_t seed) {
     if (!master || !exp_avg || !exp_avg_sq || !grads || !bf16_out || !master8 || !exp_avg8 ||
         !exp_avg_sq8 || !grads8 || !bf16_out8 || !fp8_out || !amax_history || !amax_dev ||
         !inv_scale_dev || !step_dev || !hyper)
@@ -464,11 +462,62 @@ amp_status amp_adamw_master_step_fp8_delayed(
     L.n_tiles = master8->n_tiles;
     L.n8 = fp8_out->n;
     L.tscale = fp8_out->tscale;
+    if (stochastic && (master->n >= (1 << 30) || fp8_out->n >= (1 << 30)))
+        return fail(AMP_EINVAL, "%s: 2^30 tensors or more per list", fn);
     cudaError_t e = amp::launch_adamw_fp8_delayed(
         L, gc, fc, scale_dev, found_inf_dev, step_dev, c,
         reinterpret_cast<amp::AdamwStepScalars *>(fp8_out->scratch), amax_history, hist_len, eps,
-        amax_dev, inv_scale_dev, reinterpret_cast<cudaStream_t>(stream));
+        amax_dev, inv_scale_dev, reinterpret_cast<cudaStream_t>(stream), stochastic, seed);
     return e == cudaSuccess ? AMP_OK : cuda_fail(e, fn);
+}
+
+amp_status amp_adamw_master_step_clip_sr(amp_tensor_list master, amp_tensor_list exp_avg,
+                                         amp_tensor_list exp_avg_sq, amp_tensor_list grads,
+                                         amp_tensor_list bf16_out, const float *scale_dev,
+                                         const int32_t *found_inf_dev, int32_t *step_dev,
+                                         const amp_adamw_hyper *hyper, float *amax_dev,
+                                         const double *grad_sumsq_dev, double max_norm,
+                                         uint64_t seed, amp_stream_t stream) {
+    AMP_TRACE("amp_adamw_master_step_clip_sr");
+    const char *fn = "amp_adamw_master_step_clip_sr";
+    if (!grad_sumsq_dev) return fail(AMP_EINVAL, "%s: grad_sumsq_dev is NULL", fn);
+    if (!(max_norm > 0.0) || max_norm > 1e300)
+        return fail(AMP_EINVAL, "%s: max_norm must be finite and > 0", fn);
+    if (!bf16_out) return fail(AMP_EINVAL, "%s: bf16_out is NULL", fn);
+    return adamw_entry(master, exp_avg, exp_avg_sq, grads, bf16_out, scale_dev, found_inf_dev,
+                       step_dev, hyper, amax_dev, grad_sumsq_dev, max_norm, stream, true, seed);
+}
+
+amp_status amp_adamw_master_step_fp8_delayed(
+    amp_tensor_list master, amp_tensor_list exp_avg, amp_tensor_list exp_avg_sq,
+    amp_tensor_list grads, amp_tensor_list bf16_out, amp_tensor_list master8,
+    amp_tensor_list exp_avg8, amp_tensor_list exp_avg_sq8, amp_tensor_list grads8,
+    amp_tensor_list bf16_out8, amp_tensor_list fp8_out, amp_tensor_list fp8_t_out,
+    amp_dtype fp8_dtype, double eps, const float *amax_history, int hist_len, float *amax_dev,
+    float *inv_scale_dev, const float *scale_dev, const int32_t *found_inf_dev, int32_t *step_dev,
+    const amp_adamw_hyper *hyper, amp_stream_t stream) {
+    AMP_TRACE("amp_adamw_master_step_fp8_delayed");
+    return delayed_entry("amp_adamw_master_step_fp8_delayed", master, exp_avg, exp_avg_sq, grads,
+                         bf16_out, master8, exp_avg8, exp_avg_sq8, grads8, bf16_out8, fp8_out,
+                         fp8_t_out, fp8_dtype, eps, amax_history, hist_len, amax_dev,
+                         inv_scale_dev, scale_dev, found_inf_dev, step_dev, hyper, stream, false,
+                         0);
+}
+
+amp_status amp_adamw_master_step_fp8_delayed_sr(
+    amp_tensor_list master, amp_tensor_list exp_avg, amp_tensor_list exp_avg_sq,
+    amp_tensor_list grads, amp_tensor_list bf16_out, amp_tensor_list master8,
+    amp_tensor_list exp_avg8, amp_tensor_list exp_avg_sq8, amp_tensor_list grads8,
+    amp_tensor_list bf16_out8, amp_tensor_list fp8_out, amp_tensor_list fp8_t_out,
+    amp_dtype fp8_dtype, double eps, const float *amax_history, int hist_len, float *amax_dev,
+    float *inv_scale_dev, const float *scale_dev, const int32_t *found_inf_dev, int32_t *step_dev,
+    const amp_adamw_hyper *hyper, uint64_t seed, amp_stream_t stream) {
+    AMP_TRACE("amp_adamw_master_step_fp8_delayed_sr");
+    return delayed_entry("amp_adamw_master_step_fp8_delayed_sr", master, exp_avg, exp_avg_sq,
+                         grads, bf16_out, master8, exp_avg8, exp_avg_sq8, grads8, bf16_out8,
+                         fp8_out, fp8_t_out, fp8_dtype, eps, amax_history, hist_len, amax_dev,
+                         inv_scale_dev, scale_dev, found_inf_dev, step_dev, hyper, stream, true,
+                         seed);
 }
 
 amp_status amp_update_scale_fp8_history(float *scale_dev, int32_t *growth_tracker_dev,
@@ -582,11 +631,37 @@ amp_status fp8_quant_groupwise(const void *x, amp_dtype x_dtype, int64_t rows, i
     return e == cudaSuccess ? AMP_OK : cuda_fail(e, fn);
 }
 
+static amp_status quant_list_entry(amp_tensor_list x, amp_tensor_list out, amp_tensor_list out_t,
+                                   amp_dtype fp8_dtype, double eps, const float *amax_dev,
+                                   float *inv_scale_dev, const int32_t *skip_if_dev,
+                                   amp_stream_t stream, const int32_t *sr_step, uint64_t seed);
+
 amp_status fp8_quant_tensorwise_list(amp_tensor_list x, amp_tensor_list out, amp_tensor_list out_t,
                                      amp_dtype fp8_dtype, double eps, const float *amax_dev,
                                      float *inv_scale_dev, const int32_t *skip_if_dev,
                                      amp_stream_t stream) {
     AMP_TRACE("fp8_quant_tensorwise_list");
+    return quant_list_entry(x, out, out_t, fp8_dtype, eps, amax_dev, inv_scale_dev, skip_if_dev,
+                            stream, nullptr, 0);
+}
+
+amp_status fp8_quant_tensorwise_list_sr(amp_tensor_list x, amp_tensor_list out,
+                                        amp_tensor_list out_t, amp_dtype fp8_dtype, double eps,
+                                        const float *amax_dev, float *inv_scale_dev,
+                                        const int32_t *skip_if_dev, uint64_t seed,
+                                        const int32_t *step_dev, amp_stream_t stream) {
+    AMP_TRACE("fp8_quant_tensorwise_list_sr");
+    if (!step_dev) return fail(AMP_EINVAL, "fp8_quant_tensorwise_list_sr: step_dev is NULL");
+    if (x && x->n >= (1 << 30))
+        return fail(AMP_EINVAL, "fp8_quant_tensorwise_list_sr: 2^30 tensors or more");
+    return quant_list_entry(x, out, out_t, fp8_dtype, eps, amax_dev, inv_scale_dev, skip_if_dev,
+                            stream, step_dev, seed);
+}
+
+static amp_status quant_list_entry(amp_tensor_list x, amp_tensor_list out, amp_tensor_list out_t,
+                                   amp_dtype fp8_dtype, double eps, const float *amax_dev,
+                                   float *inv_scale_dev, const int32_t *skip_if_dev,
+                                   amp_stream_t stream, const int32_t *sr_step, uint64_t seed) {
     if (!x || !out || !amax_dev || !inv_scale_dev)
         return fail(AMP_EINVAL, "fp8_quant_tensorwise_list: NULL argument");
     if (!x->two_d || !out->two_d || (out_t && !out_t->two_d))
@@ -604,7 +679,8 @@ amp_status fp8_quant_tensorwise_list(amp_tensor_list x, amp_tensor_list out, amp
     cudaError_t e = amp::launch_fp8_quant_list(x->view, x->n_tiles, any_empty, xc, out->view,
                                                out_t ? &out_t->view : nullptr, fc, eps, amax_dev,
                                                inv_scale_dev, skip_if_dev,
-                                               reinterpret_cast<cudaStream_t>(stream));
+                                               reinterpret_cast<cudaStream_t>(stream), sr_step,
+                                               seed);
     return e == cudaSuccess ? AMP_OK : cuda_fail(e, "fp8_quant_tensorwise_list");
 }
 

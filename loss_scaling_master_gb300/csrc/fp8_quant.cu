@@ -20,11 +20,17 @@
 //   Bytes: 2 read + 1 + 1 written per element.
 // Tiles on a ragged edge, or with sizes/addresses that break 16-byte access,
 // take an element-wise path with the same arithmetic.
+// The list cast has a stochastic-rounding form for the FP8 weight copies
+// ("第20章 量化与混合精度训练" §20.5.14): the same scaled fp32 values, each
+// rounded by fp8_stochastic (philox.cuh) with 32 random bits drawn per
+// element from its row-major index, so the transposed copy holds the same
+// bytes.
 #include <algorithm>
 
 #include "fp8_tile.cuh"
 #include "internal.h"
 #include "pdl.cuh"
+#include "philox.cuh"
 
 namespace amp {
 namespace {
@@ -35,10 +41,19 @@ __device__ __forceinline__ float x_at(const void *x, int64_t k) {
     return lowp_to_f32<XT>(static_cast<const uint16_t *>(x)[k]);
 }
 
-template <int XT, int FT>
+// Random-bit source of the stochastic cast: element k of this tensor rounds
+// with sr8 bits of (seed, step, tensor, k).
+struct SrArgs {
+    uint64_t seed;
+    int32_t step;
+    int32_t tensor;
+};
+
+template <int XT, int FT, bool SR = false>
 __device__ __forceinline__ void quant_tile(const void *x, int64_t rows, int64_t cols, uint8_t *out,
                                            uint8_t *out_t, int64_t r0, int64_t c0,
-                                           const float *s_scale, uint32_t *sm) {
+                                           const float *s_scale, uint32_t *sm,
+                                           SrArgs sr = SrArgs{}) {
     constexpr int esz = XT == kF32 ? 4 : 2;
     constexpr int nv = XT == kF32 ? 2 : 1;  // 16-byte loads per 8 elements
     const bool fast = r0 + kTile <= rows && c0 + kTile <= cols && (cols & 7) == 0 &&
@@ -77,12 +92,17 @@ __device__ __forceinline__ void quant_tile(const void *x, int64_t rows, int64_t 
             }
 #pragma unroll
             for (int j = 0; j < 8; j += 2) mul2_rn(y[j], y[j + 1], s32, s32, y[j], y[j + 1]);
-            uint2 q;
-            q.x = fp8x4_canonical_nan<FT>(f32x2_to_fp8x2_raw<FT>(y[0], y[1]) |
-                                          (f32x2_to_fp8x2_raw<FT>(y[2], y[3]) << 16));
-            q.y = fp8x4_canonical_nan<FT>(f32x2_to_fp8x2_raw<FT>(y[4], y[5]) |
-                                          (f32x2_to_fp8x2_raw<FT>(y[6], y[7]) << 16));
             const int r = rb + 16 * k;
+            uint2 q;
+            if constexpr (SR) {
+                q = fp8x8_stochastic<FT>(y, sr.seed, sr.step, sr.tensor,
+                                         (r0 + r) * cols + c0 + 8 * c8);
+            } else {
+                q.x = fp8x4_canonical_nan<FT>(f32x2_to_fp8x2_raw<FT>(y[0], y[1]) |
+                                              (f32x2_to_fp8x2_raw<FT>(y[2], y[3]) << 16));
+                q.y = fp8x4_canonical_nan<FT>(f32x2_to_fp8x2_raw<FT>(y[4], y[5]) |
+                                              (f32x2_to_fp8x2_raw<FT>(y[6], y[7]) << 16));
+            }
             *reinterpret_cast<uint2 *>(out + (r0 + r) * cols + c0 + 8 * c8) = q;
             if (out_t) *reinterpret_cast<uint2 *>(sm + swz(r, 2 * c8)) = q;
         }
@@ -95,8 +115,14 @@ __device__ __forceinline__ void quant_tile(const void *x, int64_t rows, int64_t 
         for (int idx = threadIdx.x; idx < kTile * kTile; idx += kThreads) {
             const int64_t i = r0 + (idx >> 7), j = c0 + (idx & (kTile - 1));
             if (i < rows && j < cols) {
-                const uint8_t q = quant1<FT>(x_at<XT>(x, i * cols + j), s32);
-                out[i * cols + j] = q;
+                const int64_t k = i * cols + j;
+                uint8_t q;
+                if constexpr (SR)
+                    q = uint8_t(fp8_stochastic<FT>(__fmul_rn(x_at<XT>(x, k), s32),
+                                                   sr8_word(sr.seed, sr.step, sr.tensor, k)));
+                else
+                    q = quant1<FT>(x_at<XT>(x, k), s32);
+                out[k] = q;
                 if (out_t) out_t[j * rows + i] = q;
             }
         }
@@ -125,11 +151,12 @@ __global__ void __launch_bounds__(kThreads) quant_single_kernel(const void *x, i
     quant_tile<XT, FT>(x, rows, cols, out, out_t, tr * kTile, tc * kTile, &s_scale, sm);
 }
 
-template <int XT, int FT>
-__global__ void __launch_bounds__(kThreads) quant_list_kernel(ListView X, ListView O, ListView OT,
-                                                              int has_t, const float *amax,
-                                                              float *inv_scale, EpsFloor ef,
-                                                              const int32_t *skip_if) {
+template <int XT, int FT, bool SR>
+__device__ __forceinline__ void quant_list_body(const ListView &X, const ListView &O,
+                                                const ListView &OT, int has_t, const float *amax,
+                                                float *inv_scale, const EpsFloor &ef,
+                                                const int32_t *skip_if, uint64_t sr_seed,
+                                                const int32_t *sr_step) {
     pdl_wait();
     pdl_trigger();
     if (skip_if && *skip_if) return;
@@ -147,8 +174,26 @@ __global__ void __launch_bounds__(kThreads) quant_list_kernel(ListView X, ListVi
         if (tl.y == 0) inv_scale[t] = inv;
     }
     uint8_t *ot = has_t ? static_cast<uint8_t *>(OT.ptrs[t]) : nullptr;
-    quant_tile<XT, FT>(X.ptrs[t], rows, cols, static_cast<uint8_t *>(O.ptrs[t]), ot,
-                       tr * kTile, tc * kTile, &s_scale, sm);
+    SrArgs sr{};
+    if constexpr (SR) sr = SrArgs{sr_seed, *sr_step, t};
+    quant_tile<XT, FT, SR>(X.ptrs[t], rows, cols, static_cast<uint8_t *>(O.ptrs[t]), ot,
+                           tr * kTile, tc * kTile, &s_scale, sm, sr);
+}
+
+template <int XT, int FT>
+__global__ void __launch_bounds__(kThreads) quant_list_kernel(ListView X, ListView O, ListView OT,
+                                                              int has_t, const float *amax,
+                                                              float *inv_scale, EpsFloor ef,
+                                                              const int32_t *skip_if) {
+    quant_list_body<XT, FT, false>(X, O, OT, has_t, amax, inv_scale, ef, skip_if, 0, nullptr);
+}
+
+// The stochastic cast: the same tile walk with the rounding of philox.cuh.
+template <int XT, int FT>
+__global__ void __launch_bounds__(kThreads) quant_list_sr_kernel(
+    ListView X, ListView O, ListView OT, int has_t, const float *amax, float *inv_scale,
+    EpsFloor ef, const int32_t *skip_if, uint64_t sr_seed, const int32_t *sr_step) {
+    quant_list_body<XT, FT, true>(X, O, OT, has_t, amax, inv_scale, ef, skip_if, sr_seed, sr_step);
 }
 
 // Tensors of a list with no elements have no tiles, so quant_list_kernel never
@@ -297,7 +342,8 @@ cudaError_t launch_fp8_quant(const void *x, int xelem, int64_t rows, int64_t col
 cudaError_t launch_fp8_quant_list(const ListView &x, int64_t n_tiles, bool any_empty, int xelem,
                                   const ListView &out, const ListView *out_t, int fp8,
                                   double eps, const float *amax, float *inv_scale,
-                                  const int32_t *skip_if, cudaStream_t s) {
+                                  const int32_t *skip_if, cudaStream_t s, const int32_t *sr_step,
+                                  uint64_t sr_seed) {
     if (any_empty) {
         if (fp8 == kE4M3) launch_pdl(quant_list_empty_kernel<kE4M3>, dim3(1), dim3(kThreads), 0, s,
                                      x, amax, inv_scale, make_eps_floor(eps, fp8_max<kE4M3>()),
@@ -312,9 +358,11 @@ cudaError_t launch_fp8_quant_list(const ListView &x, int64_t n_tiles, bool any_e
     const int has_t = out_t != nullptr;
     const dim3 grid((unsigned)n_tiles), block(kThreads);
     const EpsFloor ef = make_eps_floor(eps, fp8 == kE4M3 ? fp8_max<kE4M3>() : fp8_max<kE5M2>());
-#define AMP_QL(XT, FT)                                                                    \
-    launch_pdl(quant_list_kernel<XT, FT>, grid, block, 0, s, x, out, ot, has_t, amax, inv_scale, \
-               ef, skip_if)
+#define AMP_QL(XT, FT)                                                                       \
+    (sr_step ? launch_pdl(quant_list_sr_kernel<XT, FT>, grid, block, 0, s, x, out, ot, has_t,     \
+                          amax, inv_scale, ef, skip_if, sr_seed, sr_step)                        \
+             : launch_pdl(quant_list_kernel<XT, FT>, grid, block, 0, s, x, out, ot, has_t, amax,  \
+                          inv_scale, ef, skip_if))
     if (fp8 == kE4M3) {
         if (xelem == kBF16) AMP_QL(kBF16, kE4M3);
         else if (xelem == kF16) AMP_QL(kF16, kE4M3);

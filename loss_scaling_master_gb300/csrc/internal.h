@@ -102,7 +102,8 @@ cudaError_t launch_adamw_fp8_delayed(const Fp8DelayedLists &L, int gelem, int fp
                                      const float *scale, const int32_t *found_inf, int32_t *step,
                                      const AdamwConsts &c, AdamwStepScalars *scal,
                                      const float *hist, int hist_len, double eps, float *amax,
-                                     float *inv_scale, cudaStream_t s);
+                                     float *inv_scale, cudaStream_t s, bool stochastic = false,
+                                     uint64_t seed = 0);
 
 cudaError_t launch_emit_bf16(const ListView &p, const ListView &b, int64_t n_chunks, float *amax,
                              bool use_slots, cudaStream_t s);
@@ -134,9 +135,12 @@ cudaError_t launch_fp8_quant_rowwise(const void *x, int xelem, int64_t rows, int
                                      float *scale_col, float *inv_col, const int32_t *skip_if,
                                      int device, cudaStream_t s);
 
+// sr_step non-NULL: the stochastic cast, random counters from the step count
+// *sr_step and sr_seed.
 cudaError_t launch_fp8_quant_list(const ListView &x, int64_t n_tiles, bool any_empty, int xelem,
                                   const ListView &out, const ListView *out_t, int fp8,
                                   double eps, const float *amax, float *inv_scale,
-                                  const int32_t *skip_if, cudaStream_t s);
+                                  const int32_t *skip_if, cudaStream_t s,
+                                  const int32_t *sr_step = nullptr, uint64_t sr_seed = 0);
 
 }  // namespace amp

@@ -40,8 +40,10 @@ class AmpOptimizerStep:
         fp8_scaling: "dynamic" (this step's amax, a separate cast pass) or
         "delayed" (the max of the last amax_history_len steps' amax, cast in
         the update pass; the history starts from the initial bf16 copy).
-        sr_seed: round the bf16 copy stochastically with this 64-bit seed
-        (None: round to nearest-even).  min_scale: after every step, set the
+        sr_seed: round the copies each step emits stochastically with this
+        64-bit seed - the bf16 copy and the FP8 weight copies cast from it, in
+        every form of the step (None: round to nearest-even).  The first
+        working copies, made before any step, round to nearest-even.  min_scale: after every step, set the
         sticky health bits of amp_scale_health in page-locked host memory when
         the loss scale is not finite (1) or below min_scale (2); health()
         reads them without synchronising (None: no check).  fp8_format: the
@@ -110,9 +112,8 @@ class AmpOptimizerStep:
         self.fp8_scaling = fp8_scaling
         self.hist_len = amax_history_len
         self.sr_seed = sr_seed
-        if sr_seed is not None and (max_norm is not None or fp8_scaling != "dynamic"
-                                    or not emit_bf16):
-            raise ValueError("stochastic rounding is offered with the plain AdamW step")
+        if sr_seed is not None and not emit_bf16:
+            raise ValueError("stochastic rounding applies to the emitted copies (emit_bf16=True)")
         if fp8_scaling == "delayed":
             if not self.n_fp8 or max_norm is not None:
                 raise ValueError("delayed FP8 scaling needs FP8 weights and no clipping")
@@ -217,39 +218,60 @@ class AmpOptimizerStep:
             P, F = self.delayed_groups[grad_buffer]
             A.amp_unscale_check(L_g, self.scale, self.found_inf, stream=s)
             self._combine(s)
-            A.amp_adamw_master_step_fp8_delayed(P, F, self.L_q, self.L_qt, self.fp8_format,
-                                                self.amax_history, self.hist_len, self.amax,
-                                                self.inv_scale, self.scale, self.found_inf,
-                                                self.step_count, *self.hyper,
-                                                fp8_eps=self.fp8_eps, stream=s)
+            if self.sr_seed is None:
+                A.amp_adamw_master_step_fp8_delayed(P, F, self.L_q, self.L_qt, self.fp8_format,
+                                                    self.amax_history, self.hist_len, self.amax,
+                                                    self.inv_scale, self.scale, self.found_inf,
+                                                    self.step_count, *self.hyper,
+                                                    fp8_eps=self.fp8_eps, stream=s)
+            else:
+                A.amp_adamw_master_step_fp8_delayed_sr(P, F, self.L_q, self.L_qt, self.fp8_format,
+                                                       self.amax_history, self.hist_len,
+                                                       self.amax, self.inv_scale, self.scale,
+                                                       self.found_inf, self.step_count,
+                                                       *self.hyper, self.sr_seed,
+                                                       fp8_eps=self.fp8_eps, stream=s)
             A.amp_update_scale_fp8_history(self.scale, self.growth_tracker, self.found_inf,
                                            self.growth, self.backoff, self.interval, self.amax,
                                            self.amax_history, self.n_fp8, self.hist_len,
                                            stream=s)
             self._health(s)
             return
-        if self.sr_seed is not None:
+        sr = self.sr_seed is not None
+        if self.max_norm is None:
             A.amp_unscale_check(L_g, self.scale, self.found_inf, stream=s)
             self._combine(s)
-            A.amp_adamw_master_step_sr(self.L_master, self.L_m, self.L_v, L_g, self.L_b,
-                                       self.scale, self.found_inf, self.step_count, *self.hyper,
-                                       self.sr_seed, amax=amax, stream=s)
-        elif self.max_norm is None:
-            A.amp_unscale_check(L_g, self.scale, self.found_inf, stream=s)
-            self._combine(s)
-            A.amp_adamw_master_step(self.L_master, self.L_m, self.L_v, L_g, self.L_b, self.scale,
-                                    self.found_inf, self.step_count, *self.hyper, amax=amax,
-                                    stream=s)
+            if sr:
+                A.amp_adamw_master_step_sr(self.L_master, self.L_m, self.L_v, L_g, self.L_b,
+                                           self.scale, self.found_inf, self.step_count,
+                                           *self.hyper, self.sr_seed, amax=amax, stream=s)
+            else:
+                A.amp_adamw_master_step(self.L_master, self.L_m, self.L_v, L_g, self.L_b,
+                                        self.scale, self.found_inf, self.step_count, *self.hyper,
+                                        amax=amax, stream=s)
         else:
             A.amp_unscale_check_norm(L_g, self.scale, self.found_inf, self.grad_sumsq, stream=s)
             self._combine(s, norm=True)
-            A.amp_adamw_master_step_clip(self.L_master, self.L_m, self.L_v, L_g, self.L_b,
-                                         self.scale, self.found_inf, self.step_count, *self.hyper,
-                                         self.grad_sumsq, self.max_norm, amax=amax, stream=s)
+            if sr:
+                A.amp_adamw_master_step_clip_sr(self.L_master, self.L_m, self.L_v, L_g, self.L_b,
+                                                self.scale, self.found_inf, self.step_count,
+                                                *self.hyper, self.grad_sumsq, self.max_norm,
+                                                self.sr_seed, amax=amax, stream=s)
+            else:
+                A.amp_adamw_master_step_clip(self.L_master, self.L_m, self.L_v, L_g, self.L_b,
+                                             self.scale, self.found_inf, self.step_count,
+                                             *self.hyper, self.grad_sumsq, self.max_norm,
+                                             amax=amax, stream=s)
         if self.n_fp8:
-            A.fp8_quant_tensorwise_list(self.L_x8, self.L_q, self.L_qt, self.fp8_format, self.amax,
-                                        self.inv_scale, eps=self.fp8_eps, skip_if=self.found_inf,
-                                        stream=s)
+            if sr:
+                A.fp8_quant_tensorwise_list_sr(self.L_x8, self.L_q, self.L_qt, self.fp8_format,
+                                               self.amax, self.inv_scale, self.sr_seed,
+                                               self.step_count, eps=self.fp8_eps,
+                                               skip_if=self.found_inf, stream=s)
+            else:
+                A.fp8_quant_tensorwise_list(self.L_x8, self.L_q, self.L_qt, self.fp8_format,
+                                            self.amax, self.inv_scale, eps=self.fp8_eps,
+                                            skip_if=self.found_inf, stream=s)
         A.amp_update_scale(self.scale, self.growth_tracker, self.found_inf, self.growth,
                            self.backoff, self.interval, amax=self.amax if self.n_fp8 else None,
                            n_amax=self.n_fp8, stream=s)

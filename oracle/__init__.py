@@ -239,7 +239,7 @@ def fp8_quant_tensorwise(x: np.ndarray, xdt: str, rows: int, cols: int, fp8: str
 
 def fp8_stochastic(fp8: str, y: np.ndarray, u: np.ndarray) -> np.ndarray:
     """Stochastic rounding of fp32 values y (already scaled) to FP8 bytes with
-    32 random bits each (hi exactly when u < floor(2^32 * distance ratio))."""
+    16 random bits each (hi exactly when u < floor(2^16 * distance ratio))."""
     y = np.ascontiguousarray(y, np.float32)
     u = np.ascontiguousarray(u, np.uint32)
     assert y.shape == u.shape
@@ -249,7 +249,7 @@ def fp8_stochastic(fp8: str, y: np.ndarray, u: np.ndarray) -> np.ndarray:
 
 
 def sr8_bits(seed: int, step: int, tensor: int, k0: int, n: int) -> np.ndarray:
-    """The 32 random bits of elements k0 .. k0+n-1 of FP8 tensor `tensor` at `step`."""
+    """The 16 random bits of elements k0 .. k0+n-1 of FP8 tensor `tensor` at `step`."""
     out = np.empty(n, np.uint32)
     lib().orc_sr8_bits_list(ctypes.c_uint64(seed), step, tensor, k0, n, _ptr(out))
     return out

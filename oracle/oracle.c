@@ -645,24 +645,27 @@ void orc_bf16_stochastic_list(const float *p, uint16_t *out, int64_t n, uint64_t
 /* §20.5.14 rounds down or up with probability proportional to the distance  */
 /* (so the expected value is the input) and says it matters most the lower   */
 /* the precision, FP8 and FP4 included.  Reading: [FP8] §2's quantizer with   */
-/* its round-to-nearest cast replaced by that rule:                           */
+/* its round-to-nearest cast replaced by that rule, drawn with 16 random bits */
+/* per element as for the bf16 copy:                                          */
 /*   y = x_f32 * scale (fp32), clamped to +-fp8_max, NaN propagating;         */
 /*   lo <= |y| < hi: the neighbouring FP8 magnitudes (|y| = fp8_max or on the */
 /*   grid: the result is |y| itself);                                        */
 /*   result = sign(y) * hi with probability                                   */
-/*       floor(2^32 * (|y| - lo) / (hi - lo)) / 2^32,                         */
+/*       floor(2^16 * (|y| - lo) / (hi - lo)) / 2^16,                         */
 /*   else sign(y) * lo; NaN gives the canonical NaN.                          */
-/* With 32 random bits u the result is hi exactly when u is below that       */
-/* numerator.  The ratio is exact whenever it has at most 32 fractional      */
-/* bits, which holds for every |y| in the normal range of both formats (the  */
-/* fp32 significand keeps 21 bits below an E5M2 quantum, 20 below an E4M3FN  */
-/* one); below it, where fp32 keeps finer bits, the probability is the ratio */
-/* truncated to a multiple of 2^-32.                                         */
-/* Random bits: Philox4x32-10 (above) with counter {k/4 low, k/4 high, step, */
-/* tensor | 2^31} and key = seed; element k (row-major index within its     */
-/* tensor) takes output word k % 4.  Bit 31 of the last counter word keeps   */
-/* these draws apart from the bf16 copy's.  The transposed copy holds the    */
-/* same bytes as the row-major one (one draw per element).                   */
+/* With 16 uniform random bits u the result is hi exactly when u is below    */
+/* that numerator.  The probability is the distance ratio itself whenever the */
+/* ratio is a multiple of 2^-16, else the ratio truncated to one: the mean is */
+/* then low by less than 2^-16 of a quantum.  (The bf16 copy's rule is exact, */
+/* since bf16 drops exactly 16 bits of an fp32 value; a scaled FP8 input      */
+/* keeps up to 21 bits below the FP8 quantum.)                                */
+/* Random bits: element k (row-major index within its tensor) takes the      */
+/* 16-bit draw that the bf16 copy's layout assigns it (sr_bits above: half    */
+/* (k%8)%2, low first, of Philox output word (k%8)/2 at counter {k/8 low,     */
+/* k/8 high, step, w}, key = seed) with w = tensor | 2^31; bit 31 keeps these */
+/* draws apart from the bf16 copy's, whose tensor words stay below 2^31.      */
+/* The transposed copy holds the same bytes as the row-major one (one draw    */
+/* per element).                                                              */
 /* ------------------------------------------------------------------------ */
 
 /* ascending finite non-negative magnitudes of an FP8 format (at most 128) */
@@ -694,8 +697,8 @@ uint8_t orc_fp8_stochastic(int fp8_dtype, float y, uint32_t u)
     double r = grid[i];
     if (r < a) {
         double ratio = (a - grid[i]) / (grid[i + 1] - grid[i]);   /* exact: the gap is 2^k */
-        double num = floor(ratio * 4294967296.0);
-        if ((double)u < num)
+        double num = floor(ratio * 65536.0);
+        if ((double)(u & 0xFFFFu) < num)
             r = grid[i + 1];
     }
     return (uint8_t)fmt_encode(f, signbit(y) ? -r : r);
@@ -703,13 +706,7 @@ uint8_t orc_fp8_stochastic(int fp8_dtype, float y, uint32_t u)
 
 static uint32_t sr8_bits(uint64_t seed, int32_t step, int32_t tensor, int64_t k)
 {
-    uint64_t grp = (uint64_t)k >> 2;
-    uint32_t ctr[4] = {(uint32_t)grp, (uint32_t)(grp >> 32), (uint32_t)step,
-                       (uint32_t)tensor | 0x80000000u};
-    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
-    uint32_t o[4];
-    orc_philox4x32_10(ctr, key, o);
-    return o[k & 3];
+    return sr_bits(seed, step, (int32_t)((uint32_t)tensor | 0x80000000u), k);
 }
 
 /* orc_fp8_quant_tensorwise with the stochastic cast: the same amax, scale and
@@ -753,7 +750,7 @@ void orc_fp8_quant_tensorwise_sr(const void *x, int xdtype, int64_t rows, int64_
     }
 }
 
-/* the 32 random bits of element k (exported for the pin tests) */
+/* the 16 random bits of element k (exported for the pin tests) */
 uint32_t orc_sr8_bits(uint64_t seed, int32_t step, int32_t tensor, int64_t k)
 {
     return sr8_bits(seed, step, tensor, k);

@@ -482,7 +482,8 @@ def test_amp_step_composition_with_fp8(A, dev, fmt):
     st.close()
 
 
-@pytest.mark.parametrize("mode", ["dynamic", "delayed", "clip", "sr", "health"])
+@pytest.mark.parametrize("mode", ["dynamic", "delayed", "clip", "sr", "health", "sr_fp8",
+                                  "sr_delayed", "sr_clip"])
 def test_graph_replay_matches_eager(A, dev, mode):
     """The step captured once in a CUDA graph (with its programmatic launch
     edges) and replayed gives the same bits as the eager calls, including a
@@ -496,7 +497,9 @@ def test_graph_replay_matches_eager(A, dev, mode):
     hyper = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
     opts = {"dynamic": {}, "delayed": {"fp8_scaling": "delayed", "amax_history_len": 2},
             "clip": {"max_norm": 0.05}, "sr": {"sr_seed": 77, "fp8_shapes": None},
-            "health": {"min_scale": 600.0}}[mode]
+            "health": {"min_scale": 600.0}, "sr_fp8": {"sr_seed": 78},
+            "sr_delayed": {"sr_seed": 79, "fp8_scaling": "delayed", "amax_history_len": 2},
+            "sr_clip": {"sr_seed": 80, "max_norm": 0.05}}[mode]
     kw = dict(fp8_shapes=fp8_shapes)
     kw.update(opts)
     mk = lambda: AmpOptimizerStep([torch.from_numpy(m.copy()).to(dev) for m in master],
@@ -849,6 +852,200 @@ def test_stochastic_rounding_unbiased_on_gpu(A, dev):
     assert abs(b.mean().item() - float(np.float32(1.0 + 1e-3))) < 5 * sigma
     for L in Ls:
         L.close()
+
+
+# ------------------------------------------- stochastic rounding of FP8 copies
+@pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
+@pytest.mark.parametrize("xdt", ["bf16", "f16", "f32"])
+def test_fp8_list_stochastic_parity(A, dev, fmt, xdt):
+    """fp8_quant_tensorwise_list_sr: every byte of both layouts and every
+    inv_scale equal to the oracle's stochastic quantizer (same published
+    generator, written separately), on full, ragged and misaligned-row tiles,
+    with NaN, inf, zeros and values in the FP8 subnormal range; a set skip flag
+    writes nothing; the tensor word of the random counter is the list index."""
+    rng = np.random.default_rng(160)
+    shapes = [(128, 128), (127, 129), (256, 384), (33, 40), (1, 1), (130, 52)]
+    seed, t = 0xDEADBEEF_0BADF00D, 13
+    xs, xh = [], []
+    for (r, c) in shapes:
+        h = _x_host(rng, r, c, xdt)
+        if r * c > 64:
+            flat = h.reshape(-1)
+            flat[3] = _inf_bits(xdt, np.inf)
+            flat[5] = _inf_bits(xdt, -np.inf) if r != 33 else flat[5]
+            flat[7] = _inf_bits(xdt, np.nan) if (r, c) == (256, 384) else flat[7]
+            if xdt == "f32":
+                flat[9] = np.float32(1e-30)
+        xh.append(h)
+        xs.append(to_device(h, xdt, dev).view(r, c))
+    LX = A.amp_tensor_list_create(xs, True)
+    tdt = torch.float8_e4m3fn if fmt == "e4m3fn" else torch.float8_e5m2
+    Q = [torch.full((r, c), 0x5A, dtype=torch.uint8, device=dev).view(tdt) for r, c in shapes]
+    QT = [torch.full((c, r), 0xA5, dtype=torch.uint8, device=dev).view(tdt) for r, c in shapes]
+    LQ, LQT = A.amp_tensor_list_create(Q, True), A.amp_tensor_list_create(QT, True)
+    # amax per tensor from the oracle's quantizer (the list takes it as given)
+    amax_h = np.array([O.fp8_quant_tensorwise(h, xdt, r, c, fmt)[3] for h, (r, c) in
+                       zip(xh, shapes)], np.float32)
+    amax_h[1] = 0.75 * amax_h[1]                        # a delayed amax: values saturate
+    amax = torch.from_numpy(amax_h).to(dev)
+    inv = torch.zeros(len(shapes), device=dev)
+    step = torch.tensor([t], dtype=torch.int32, device=dev)
+    skip = torch.ones(1, dtype=torch.int32, device=dev)
+    A.fp8_quant_tensorwise_list_sr(LX, LQ, LQT, fmt, amax, inv, seed, step, skip_if=skip)
+    torch.cuda.synchronize()
+    assert all(int(q.view(torch.uint8).unique().item()) == 0x5A for q in Q)
+    A.fp8_quant_tensorwise_list_sr(LX, LQ, LQT, fmt, amax, inv, seed, step)
+    for j, (h, (r, c)) in enumerate(zip(xh, shapes)):
+        q, qt, rinv, _ = O.fp8_quant_tensorwise_sr(h, xdt, r, c, fmt, seed, t, j,
+                                                   amax=float(amax_h[j]))
+        assert np.array_equal(to_host_bits(Q[j].view(torch.uint8)).ravel(), q), (j, r, c)
+        assert np.array_equal(to_host_bits(QT[j].view(torch.uint8)).ravel(), qt), (j, r, c)
+        gi = to_host_bits(inv)[j]
+        if np.isnan(rinv):                    # an fp32 NaN's payload is open: by position
+            assert np.isnan(gi), j
+        else:
+            assert gi.view(np.uint32) == np.float32(rinv).view(np.uint32), j
+    for L in (LX, LQ, LQT):
+        L.close()
+
+
+@pytest.mark.parametrize("mode,fmt", [("dynamic", "e4m3fn"), ("dynamic", "e5m2"),
+                                      ("delayed", "e4m3fn"), ("delayed", "e5m2")])
+def test_stochastic_step_composition(A, dev, mode, fmt):
+    """AmpOptimizerStep(sr_seed) with FP8 weights, dynamic or delayed scaling,
+    against the oracle's step with the same seed: master, m, v, the bf16 copy,
+    the FP8 bytes of both layouts and inv_scale bit-identical over several
+    steps with a skip."""
+    from loss_scaling_master_gb300 import AmpOptimizerStep
+    rng = np.random.default_rng(161)
+    shapes = [(256, 512), (300,), (96, 256), (128, 136), (1000,), (130, 52)]
+    fp8_shapes = [s if len(s) == 2 else None for s in shapes]
+    sizes = [int(np.prod(s)) for s in shapes]
+    master = [(rng.standard_normal(n) * 0.02).astype(np.float32) for n in sizes]
+    hyper = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+    seed = 0x5EED_0000_1234_5678
+    st = AmpOptimizerStep([torch.from_numpy(m.copy()).to(dev) for m in master],
+                          [torch.empty(n, dtype=torch.float16, device=dev) for n in sizes],
+                          init_scale=4096.0, growth_interval=3, fp8_shapes=fp8_shapes,
+                          fp8_scaling=mode, amax_history_len=2, fp8_format=fmt, sr_seed=seed,
+                          **hyper)
+    orc = O.AmpStepOracle(master, "f16", hyper["lr"], hyper["beta1"], hyper["beta2"], hyper["eps"],
+                          hyper["weight_decay"], 4096.0, 2.0, 0.5, 3, fp8_shapes=fp8_shapes,
+                          fp8_scaling=mode, hist_len=2, fp8_format=fmt, sr_seed=seed)
+    for k in range(5):
+        gh = [(rng.standard_normal(n) * 1e-3 * orc.scale).astype(np.float16).view(np.uint16)
+              for n in sizes]
+        if k == 2:
+            gh[3][17] = 0x7C00
+        for t, h in zip(st.grads, gh):
+            t.copy_(to_device(h, "f16", dev))
+        st.step()
+        orc.run(gh)
+        s = st.state()
+        assert (s["scale"], s["growth_tracker"], s["step"]) == (orc.scale, orc.tracker, orc.step)
+        for i, sh in enumerate(fp8_shapes):
+            assert np.array_equal(to_host_bits(st.bf16[i]), orc.bf16[i]), (k, i)
+            if sh is None:
+                continue
+            j = orc.slots[i]
+            assert np.array_equal(to_host_bits(st.fp8[j].view(torch.uint8)).ravel(), orc.fp8[i]), (k, i)
+            assert np.array_equal(to_host_bits(st.fp8_t[j].view(torch.uint8)).ravel(),
+                                  orc.fp8_t[i]), (k, i)
+            assert to_host_bits(st.inv_scale)[j] == orc.inv_scale[j], (k, i)
+    for i in range(len(shapes)):
+        assert np.array_equal(to_host_bits(st.master[i]).view(np.uint32), orc.master[i].view(np.uint32))
+        assert np.array_equal(to_host_bits(st.exp_avg_sq[i]).view(np.uint32),
+                              orc.exp_avg_sq[i].view(np.uint32))
+    st.close()
+
+
+def test_stochastic_step_with_clipping(A, dev, monkeypatch):
+    """AmpOptimizerStep(sr_seed, max_norm) with FP8 weights: the master state
+    within the clipped step's tolerance, the bf16 copy within 1 ulp of the
+    oracle's (its clip factor comes from a tolerance-checked sum of squares),
+    and on every step that is not skipped the FP8 bytes equal the oracle's
+    stochastic quantizer run on the GPU's own bf16 copy with the GPU's amax."""
+    from loss_scaling_master_gb300 import AmpOptimizerStep
+    from loss_scaling_master_gb300 import step as step_mod
+    snap = {}
+    real_update = step_mod.A.amp_update_scale
+
+    def spy_update(*args, amax=None, **kw):
+        if amax is not None:
+            snap["amax"] = amax.clone()
+        return real_update(*args, amax=amax, **kw)
+
+    monkeypatch.setattr(step_mod.A, "amp_update_scale", spy_update)
+    rng = np.random.default_rng(162)
+    sizes = [1000, 4096, 257, 40000]
+    fp8_shapes = [None, (64, 64), None, (200, 200)]
+    master = [(rng.standard_normal(n) * 0.02).astype(np.float32) for n in sizes]
+    hyper = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+    seed = 77
+    st = AmpOptimizerStep([torch.from_numpy(m.copy()).to(dev) for m in master],
+                          [torch.empty(n, dtype=torch.float16, device=dev) for n in sizes],
+                          init_scale=65536.0, growth_interval=3, max_norm=0.5,
+                          fp8_shapes=fp8_shapes, sr_seed=seed, **hyper)
+    orc = O.AmpStepOracle(master, "f16", hyper["lr"], hyper["beta1"], hyper["beta2"], hyper["eps"],
+                          hyper["weight_decay"], 65536.0, 2.0, 0.5, 3, max_norm=0.5,
+                          fp8_shapes=fp8_shapes, sr_seed=seed)
+    for k in range(5):
+        sigma = (1e-2 if k % 2 == 0 else 1e-5) * orc.scale
+        gh = [(rng.standard_normal(n) * sigma).astype(np.float16).view(np.uint16) for n in sizes]
+        if k == 3:
+            gh[2][100] = 0x7C00
+        for t, h in zip(st.grads, gh):
+            t.copy_(to_device(h, "f16", dev))
+        st.step()
+        orc.run(gh)
+        s = st.state()
+        assert (s["scale"], s["growth_tracker"], s["step"]) == (orc.scale, orc.tracker, orc.step)
+        if k == 3:
+            continue
+        gpu_amax = to_host_bits(snap["amax"])
+        for i, sh in enumerate(fp8_shapes):
+            gb = to_host_bits(st.bf16[i])
+            assert_bf16_close(gb, orc.bf16[i], f"bf16[{i}] step {k}")
+            if sh is None:
+                continue
+            j = orc.slots[i]
+            q, qt, inv, _ = O.fp8_quant_tensorwise_sr(gb, "bf16", sh[0], sh[1], "e4m3fn", seed,
+                                                      s["step"], j, amax=float(gpu_amax[j]))
+            assert np.array_equal(to_host_bits(st.fp8[j].view(torch.uint8)).ravel(), q), (k, i)
+            assert np.array_equal(to_host_bits(st.fp8_t[j].view(torch.uint8)).ravel(), qt), (k, i)
+    for i in range(len(sizes)):
+        assert_state_close(to_host_bits(st.master[i]), orc.master[i], f"master[{i}]")
+    st.close()
+
+
+@pytest.mark.parametrize("fmt,tdt", [("e4m3fn", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)])
+def test_fp8_stochastic_unbiased_on_gpu(A, dev, fmt, tdt):
+    """E[fp8_sr(y)] = y: a constant [2048, 2048] bf16 matrix whose scaled value
+    falls between two FP8 neighbours; the mean of the dequantized bytes over
+    its 4M elements sits within 5 sigma of the scaled value."""
+    n = 2048
+    xval = 0.3                                         # bf16 0.30078125; amax given as 1.0
+    x = torch.full((n, n), xval, dtype=torch.bfloat16, device=dev)
+    q = torch.empty((n, n), dtype=tdt, device=dev)
+    LX, LQ = A.amp_tensor_list_create([x], True), A.amp_tensor_list_create([q], True)
+    amax = torch.ones(1, device=dev)
+    inv = torch.zeros(1, device=dev)
+    step = torch.tensor([5], dtype=torch.int32, device=dev)
+    A.fp8_quant_tensorwise_list_sr(LX, LQ, None, fmt, amax, inv, 4242, step)
+    fmax = O.fmt_max(fmt)
+    y = float(np.float32(np.float32(x[0, 0].item()) * np.float32(fmax)))
+    d = q.float().double()
+    grid = torch.arange(128, dtype=torch.uint8).view(tdt).float().double().cpu().numpy()
+    grid = np.unique(grid[np.isfinite(grid)])
+    j = np.searchsorted(grid, y, side="right") - 1
+    lo, hi = grid[j], grid[j + 1]
+    assert set(torch.unique(d).tolist()) <= {lo, hi}
+    p = (y - lo) / (hi - lo)
+    sigma = (hi - lo) * np.sqrt(p * (1 - p) / d.numel())
+    assert 0.05 < p < 0.95
+    assert abs(d.mean().item() - y) < 5 * sigma
+    LX.close()
+    LQ.close()
 
 
 # --------------------------------------------------------- checkpoint / resume

@@ -95,15 +95,18 @@ MUTANTS = [
     ("sr_rounds_up_on_grid", C, "uint32_t r = lo + ((u & 0xFFFFu) < frac ? 1u : 0u);",
      "uint32_t r = lo + ((u & 0xFFFFu) <= frac ? 1u : 0u);"),
     # stochastic rounding of the FP8 copies
-    ("fp8_sr_rounds_up_at_the_threshold", C, "        if ((double)u < num)",
-     "        if ((double)u <= num)"),
+    ("fp8_sr_rounds_up_at_the_threshold", C, "        if ((double)(u & 0xFFFFu) < num)",
+     "        if ((double)(u & 0xFFFFu) <= num)"),
     ("fp8_sr_ratio_of_hi_not_gap", C,
      "double ratio = (a - grid[i]) / (grid[i + 1] - grid[i]);",
      "double ratio = (a - grid[i]) / grid[i + 1];"),
     ("fp8_sr_sign_dropped", C, "    return (uint8_t)fmt_encode(f, signbit(y) ? -r : r);",
      "    return (uint8_t)fmt_encode(f, r);"),
-    ("fp8_sr_stream_not_marked", C, "(uint32_t)tensor | 0x80000000u};", "(uint32_t)tensor};"),
-    ("fp8_sr_word_of_k_over_two", C, "    return o[k & 3];", "    return o[(k >> 1) & 3];"),
+    ("fp8_sr_stream_not_marked", C,
+     "    return sr_bits(seed, step, (int32_t)((uint32_t)tensor | 0x80000000u), k);",
+     "    return sr_bits(seed, step, tensor, k);"),
+    ("fp8_sr_threshold_of_32_bits", C, "        double num = floor(ratio * 65536.0);",
+     "        double num = floor(ratio * 4294967296.0) / 65536.0;"),
     # delayed scaling (the composed step, in Python)
     ("delayed_uses_current_amax", PY,
      '                if self.fp8_scaling == "delayed":\n                    h = self.hist[s]',

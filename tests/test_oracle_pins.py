@@ -723,31 +723,33 @@ FP8_SR_VALUES = {
 @pytest.mark.parametrize("fmt,tdt", [("e4m3fn", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)])
 def test_fp8_stochastic_probability_is_exact(fmt, tdt):
     """'第20章 量化与混合精度训练' §20.5.14: round to the neighbour away from
-    zero with probability equal to the distance ratio.  For y between FP8
-    neighbours lo < |y| < hi (torch's decode), the result is hi exactly for
-    u < N and lo for u >= N, with N / 2^32 = (|y| - lo) / (hi - lo) computed
-    here in fp64; so over all 2^32 random words the fraction that rounds away
-    is that ratio (exact where the ratio has <= 32 fractional bits, i.e. every
-    value of the normal range; below it the ratio truncated to 2^-32)."""
+    zero with probability equal to the distance ratio.  Over all 2^16 values
+    of the 16 random bits, the count that rounds to hi is floor(2^16 * (|y| -
+    lo) / (hi - lo)), with lo < |y| < hi the FP8 neighbours from torch's own
+    decode and the ratio computed here in fp64: the ratio itself when it is a
+    multiple of 2^-16 (checked on such values), else truncated."""
     grid = _torch_fp8_grid(tdt)
-    for yv in FP8_SR_VALUES[fmt]:
+    u = np.arange(1 << 16, dtype=np.uint32)
+    vals = list(FP8_SR_VALUES[fmt])
+    # values whose ratio is an exact multiple of 2^-16: lo + m * gap / 2^16
+    for j, m in ((20, 1), (40, 12345), (90, 65535), (100, 32768)):
+        vals.append(float(grid[j] + m * (grid[j + 1] - grid[j]) / 65536))
+    for yv in vals:
         y = np.float32(yv)
         a = abs(float(y))
         j = np.searchsorted(grid, a, side="right") - 1
         lo, hi = grid[j], grid[j + 1]
         ratio = (a - lo) / (hi - lo)
-        n = int(np.floor(ratio * 2.0 ** 32))
-        probe = [0, max(n - 1, 0), n, min(n + 1, 2 ** 32 - 1), 2 ** 32 - 1]
-        out = O.fp8_stochastic(fmt, np.full(len(probe), y), np.array(probe, np.uint32))
+        out = O.fp8_stochastic(fmt, np.full(u.size, y), u)
         dec = torch.from_numpy(out).view(tdt).float().numpy().astype(np.float64)
-        want = [hi if u < n else lo for u in probe]
-        assert np.array_equal(np.abs(dec), want), (yv, probe, dec, lo, hi, n)
+        assert set(np.unique(np.abs(dec))) <= {lo, hi}, yv
+        n_up = int(np.sum(np.abs(dec) == hi)) if hi != lo else 0
+        assert n_up == int(np.floor(ratio * 65536)), (yv, n_up, ratio)
+        if ratio * 65536 == np.floor(ratio * 65536):
+            assert n_up == ratio * 65536, yv                    # the exact probability
+        # hi exactly for the lowest n_up values of u
+        assert np.all(np.abs(dec[:n_up]) == hi) and np.all(np.abs(dec[n_up:]) == lo), yv
         assert np.all(np.signbit(dec) == np.signbit(y)) or lo == 0.0, yv
-    # normal range: the ratio has at most 21 fractional bits, so it is exact
-    y = np.float32(1.0 + 3 * 2.0 ** -23)
-    j = np.searchsorted(grid, float(y), side="right") - 1
-    ratio = (float(y) - grid[j]) / (grid[j + 1] - grid[j])
-    assert ratio * 2.0 ** 32 == np.floor(ratio * 2.0 ** 32)
 
 
 @pytest.mark.parametrize("fmt,tdt", [("e4m3fn", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)])
@@ -759,7 +761,7 @@ def test_fp8_stochastic_is_unbiased_and_keeps_grid(fmt, tdt):
     grid = _torch_fp8_grid(tdt)
     for yv in (1.0 + 1e-3, 3.14159, -0.0123, 0.7 * grid[1]):
         y = np.float32(yv)
-        u = rng.integers(0, 2 ** 32, 400000, dtype=np.uint64).astype(np.uint32)
+        u = rng.integers(0, 2 ** 16, 400000, dtype=np.uint64).astype(np.uint32)
         out = O.fp8_stochastic(fmt, np.full(u.size, y), u)
         dec = torch.from_numpy(out).view(tdt).float().numpy().astype(np.float64)
         a = abs(float(y))
@@ -768,12 +770,13 @@ def test_fp8_stochastic_is_unbiased_and_keeps_grid(fmt, tdt):
         assert set(np.unique(np.abs(dec))) <= {lo, hi}, yv
         p = (a - lo) / (hi - lo)
         sd = (hi - lo) * np.sqrt(p * (1 - p) / u.size)
-        assert abs(dec.mean() - float(y)) <= 5 * sd + 1e-12, yv
+        # the probability is truncated to a multiple of 2^-16: low by < 2^-16 * gap
+        assert abs(dec.mean() - float(y)) <= 5 * sd + (hi - lo) / 65536, yv
     fmax = O.fmt_max(fmt)
     special = np.array([grid[5], -grid[40], grid[-1], 0.0, -0.0, fmax * 1.5, -np.inf, np.inf,
                         np.nan], np.float32)
     want = O.encode(fmt, np.clip(special, -fmax, fmax))                 # RNE of the clamp
-    for u in (0, 1, 2 ** 31, 2 ** 32 - 1):
+    for u in (0, 1, 2 ** 15, 2 ** 16 - 1):
         got = O.fp8_stochastic(fmt, special, np.full(special.size, u, np.uint32))
         assert np.array_equal(got, want), u
     # torch's cast agrees on the saturated and on-grid values (NaN: canonical code)
@@ -816,14 +819,19 @@ def test_fp8_quant_sr_reduces_to_rne_on_grid(fmt):
 
 
 def test_fp8_random_stream_is_apart_from_bf16_stream():
-    """The FP8 draws of element k use Philox output word k % 4 at counter
-    {k/4, step, tensor | 2^31}; the bf16 copy's draws use counter
-    {k/8, step, tensor}: no counter of one stream is a counter of the other."""
+    """The FP8 draws of element k are the 16-bit half (k%8)%2 (low first) of
+    Philox output word (k%8)/2 at counter {k/8, step, tensor | 2^31}; the
+    bf16 copy's draws use the same layout at {k/8, step, tensor}, tensor
+    below 2^31: no counter of one stream is a counter of the other."""
     seed, step, tensor = 0x0123456789ABCDEF, 9, 4
-    bits = O.sr8_bits(seed, step, tensor, 0, 12)
+    bits = O.sr8_bits(seed, step, tensor, 0, 24)
     key = [seed & 0xFFFFFFFF, seed >> 32]
-    for g in range(3):
-        w = O.philox4x32_10([g, 0, step, tensor | 0x80000000], key)
-        assert bits[4 * g:4 * g + 4].tolist() == w.tolist()
-    b16 = O.philox4x32_10([0, 0, step, tensor], key)
-    assert bits[:4].tolist() != b16.tolist()
+
+    def halves(w):
+        out = []
+        for g in range(3):
+            for word in O.philox4x32_10([g, 0, step, w], key):
+                out += [int(word) & 0xFFFF, int(word) >> 16]
+        return np.array(out, np.uint32)
+    assert bits.tolist() == halves(tensor | 0x80000000).tolist()
+    assert not np.array_equal(bits, halves(tensor))
