@@ -106,10 +106,14 @@ amp_status amp_tensor_list_create(int n, void *const *dev_ptrs, const int64_t *r
                                   const int64_t *cols, amp_dtype dtype,
                                   amp_stream_t stream, amp_tensor_list *out);
 
-/* Per-tensor amax slots of a list used as the bf16 output of
- * amp_adamw_master_step: slots[i] >= 0 folds max|bf16| of tensor i into
- * amax_dev[slots[i]]; -1 (the default) does not.  Host array[n], copied to
- * the handle's device block on `stream` (waits for the copy: set-up call). */
+/* Per-tensor amax slots of a list.  On the bf16 output of
+ * amp_adamw_master_step (and amp_emit_bf16): slots[i] >= 0 folds max|bf16| of
+ * tensor i into amax_dev[slots[i]]; -1 (the default) does not.  On the x list
+ * of fp8_quant_tensorwise_list(_sr) (every slot >= 0): tensor i takes its
+ * amax from, and writes its inv_scale to, entry slots[i] instead of i - so
+ * the pieces of weights sharded over ranks can use the weights' global
+ * numbering.  Host array[n], copied to the handle's device block on `stream`
+ * (waits for the copy: set-up call). */
 amp_status amp_tensor_list_set_amax_slots(amp_tensor_list list, const int32_t *slots,
                                           amp_stream_t stream);
 
@@ -404,7 +408,8 @@ amp_status fp8_quant_rowwise(const void *x, amp_dtype x_dtype, int64_t rows, int
 
 /* The same over a list of 2-D tensors in one launch, with amax given per
  * tensor: tensor i uses amax_dev[i] (e.g. folded by amp_adamw_master_step
- * with slot i) and writes inv_scale_dev[i].
+ * with slot i) and writes inv_scale_dev[i]; if x has amax slots, entry
+ * slots[i] instead (amp_tensor_list_set_amax_slots).
  *   x      2-D list, AMP_DT_BF16 / AMP_DT_F16 / AMP_DT_F32
  *   out    2-D list of fp8_dtype with the shapes of x
  *   out_t  2-D list of fp8_dtype with the transposed shapes, or NULL

@@ -166,6 +166,7 @@ class TensorList:
 
     def __init__(self, handle, tensors, dtype: str, two_d: bool):
         self.handle, self.tensors, self.dtype, self.two_d = handle, tensors, dtype, two_d
+        self.slots = None   # amax slots, once set
 
     def __len__(self):
         return len(self.tensors)
@@ -212,9 +213,23 @@ def amp_tensor_list_create(tensors, two_d: bool = False, dtype: str | None = Non
 
 
 def amp_tensor_list_set_amax_slots(lst: TensorList, slots, stream=None):
-    arr = (ctypes.c_int32 * max(len(lst), 1))(*[int(s) for s in slots])
+    slots = [int(s) for s in slots]
+    if len(slots) != len(lst):
+        raise ValueError(f"{len(slots)} slots for a list of {len(lst)} tensors")
+    arr = (ctypes.c_int32 * max(len(lst), 1))(*slots)
     _check("amp_tensor_list_set_amax_slots",
            load().amp_tensor_list_set_amax_slots(lst.handle, arr, _stream(stream)))
+    lst.slots = slots
+
+
+def _n_entries(x: TensorList) -> int:
+    """amax / inv_scale entries a list cast reads and writes: one per tensor,
+    or up to the largest slot when x has slots."""
+    if x.slots is not None and any(s >= 0 for s in x.slots):
+        if min(x.slots) < 0:
+            raise ValueError("every tensor of a cast list with slots needs a slot >= 0")
+        return max(x.slots) + 1
+    return len(x)
 
 
 def amp_tensor_list_destroy(lst: TensorList):
@@ -551,8 +566,9 @@ def fp8_quant_tensorwise_list(x: TensorList, out: TensorList, out_t: TensorList 
                               stream=None):
     _check("fp8_quant_tensorwise_list",
            load().fp8_quant_tensorwise_list(x.handle, out.handle, out_t.handle if out_t else None,
-                                            DT[fp8_dtype], eps, _buf(amax, "amax", _F32, len(x)),
-                                            _buf(inv_scale, "inv_scale", _F32, len(x)),
+                                            DT[fp8_dtype], eps,
+                                            _buf(amax, "amax", _F32, _n_entries(x)),
+                                            _buf(inv_scale, "inv_scale", _F32, _n_entries(x)),
                                             _buf(skip_if, "skip_if", _I32), _stream(stream)))
 
 
@@ -564,8 +580,8 @@ def fp8_quant_tensorwise_list_sr(x: TensorList, out: TensorList, out_t: TensorLi
     _check("fp8_quant_tensorwise_list_sr",
            load().fp8_quant_tensorwise_list_sr(x.handle, out.handle,
                                                out_t.handle if out_t else None, DT[fp8_dtype],
-                                               eps, _buf(amax, "amax", _F32, len(x)),
-                                               _buf(inv_scale, "inv_scale", _F32, len(x)),
+                                               eps, _buf(amax, "amax", _F32, _n_entries(x)),
+                                               _buf(inv_scale, "inv_scale", _F32, _n_entries(x)),
                                                _buf(skip_if, "skip_if", _I32),
                                                ctypes.c_uint64(seed), _buf(step, "step", _I32),
                                                _stream(stream)))

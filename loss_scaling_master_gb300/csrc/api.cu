@@ -214,13 +214,18 @@ amp_status amp_tensor_list_set_amax_slots(amp_tensor_list list, const int32_t *s
     if (list->n == 0) return AMP_OK;
     std::vector<int32_t> h(slots, slots + list->n);
     bool any = false;
-    for (int32_t s : h) any |= s >= 0;
+    int32_t lo = INT32_MAX;
+    for (int32_t s : h) {
+        any |= s >= 0;
+        lo = std::min(lo, s);
+    }
     cudaError_t e = cudaMemcpyAsync(const_cast<int32_t *>(list->view.slots), h.data(),
                                     h.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
                                     reinterpret_cast<cudaStream_t>(stream));
     if (e == cudaSuccess) e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "amp_tensor_list_set_amax_slots");
     list->has_slots = any;
+    list->min_slot = lo;
     return AMP_OK;
 }
 
@@ -664,6 +669,9 @@ static amp_status quant_list_entry(amp_tensor_list x, amp_tensor_list out, amp_t
                                    amp_stream_t stream, const int32_t *sr_step, uint64_t seed) {
     if (!x || !out || !amax_dev || !inv_scale_dev)
         return fail(AMP_EINVAL, "fp8_quant_tensorwise_list: NULL argument");
+    if (x->has_slots && x->min_slot < 0)
+        return fail(AMP_EINVAL,
+                    "fp8_quant_tensorwise_list: x has amax slots, so every tensor needs one >= 0");
     if (!x->two_d || !out->two_d || (out_t && !out_t->two_d))
         return fail(AMP_EINVAL, "fp8_quant_tensorwise_list: lists must be 2-D");
     if (!(eps > 0.0)) return fail(AMP_EINVAL, "fp8_quant_tensorwise_list: eps must be > 0");
@@ -680,7 +688,7 @@ static amp_status quant_list_entry(amp_tensor_list x, amp_tensor_list out, amp_t
                                                out_t ? &out_t->view : nullptr, fc, eps, amax_dev,
                                                inv_scale_dev, skip_if_dev,
                                                reinterpret_cast<cudaStream_t>(stream), sr_step,
-                                               seed);
+                                               seed, x->has_slots);
     return e == cudaSuccess ? AMP_OK : cuda_fail(e, "fp8_quant_tensorwise_list");
 }
 

@@ -151,12 +151,14 @@ __global__ void __launch_bounds__(kThreads) quant_single_kernel(const void *x, i
     quant_tile<XT, FT>(x, rows, cols, out, out_t, tr * kTile, tc * kTile, &s_scale, sm);
 }
 
+// Tensor t of the list takes amax[a] and writes inv_scale[a] with a = its
+// slot in X (use_slots; the slots the bf16 list folded the amax into) or t.
 template <int XT, int FT, bool SR>
 __device__ __forceinline__ void quant_list_body(const ListView &X, const ListView &O,
-                                                const ListView &OT, int has_t, const float *amax,
-                                                float *inv_scale, const EpsFloor &ef,
-                                                const int32_t *skip_if, uint64_t sr_seed,
-                                                const int32_t *sr_step) {
+                                                const ListView &OT, int has_t, int use_slots,
+                                                const float *amax, float *inv_scale,
+                                                const EpsFloor &ef, const int32_t *skip_if,
+                                                uint64_t sr_seed, const int32_t *sr_step) {
     pdl_wait();
     pdl_trigger();
     if (skip_if && *skip_if) return;
@@ -167,48 +169,54 @@ __device__ __forceinline__ void quant_list_body(const ListView &X, const ListVie
     const int64_t rows = X.rows[t], cols = X.cols[t];
     const int64_t tiles_c = (cols + kTile - 1) / kTile;
     const int64_t tr = tl.y / tiles_c, tc = tl.y % tiles_c;
+    const int a = use_slots ? X.slots[t] : t;
     if (threadIdx.x == 0) {
         float s32, inv;
-        tensor_scale(amax[t], ef, fp8_max<FT>(), s32, inv);
+        tensor_scale(amax[a], ef, fp8_max<FT>(), s32, inv);
         s_scale = s32;
-        if (tl.y == 0) inv_scale[t] = inv;
+        if (tl.y == 0) inv_scale[a] = inv;
     }
     uint8_t *ot = has_t ? static_cast<uint8_t *>(OT.ptrs[t]) : nullptr;
     SrArgs sr{};
-    if constexpr (SR) sr = SrArgs{sr_seed, *sr_step, t};
+    if constexpr (SR) sr = SrArgs{sr_seed, *sr_step, a};
     quant_tile<XT, FT, SR>(X.ptrs[t], rows, cols, static_cast<uint8_t *>(O.ptrs[t]), ot,
                            tr * kTile, tc * kTile, &s_scale, sm, sr);
 }
 
 template <int XT, int FT>
 __global__ void __launch_bounds__(kThreads) quant_list_kernel(ListView X, ListView O, ListView OT,
-                                                              int has_t, const float *amax,
+                                                              int has_t, int use_slots,
+                                                              const float *amax,
                                                               float *inv_scale, EpsFloor ef,
                                                               const int32_t *skip_if) {
-    quant_list_body<XT, FT, false>(X, O, OT, has_t, amax, inv_scale, ef, skip_if, 0, nullptr);
+    quant_list_body<XT, FT, false>(X, O, OT, has_t, use_slots, amax, inv_scale, ef, skip_if, 0,
+                                   nullptr);
 }
 
 // The stochastic cast: the same tile walk with the rounding of philox.cuh.
 template <int XT, int FT>
 __global__ void __launch_bounds__(kThreads) quant_list_sr_kernel(
-    ListView X, ListView O, ListView OT, int has_t, const float *amax, float *inv_scale,
-    EpsFloor ef, const int32_t *skip_if, uint64_t sr_seed, const int32_t *sr_step) {
-    quant_list_body<XT, FT, true>(X, O, OT, has_t, amax, inv_scale, ef, skip_if, sr_seed, sr_step);
+    ListView X, ListView O, ListView OT, int has_t, int use_slots, const float *amax,
+    float *inv_scale, EpsFloor ef, const int32_t *skip_if, uint64_t sr_seed,
+    const int32_t *sr_step) {
+    quant_list_body<XT, FT, true>(X, O, OT, has_t, use_slots, amax, inv_scale, ef, skip_if,
+                                  sr_seed, sr_step);
 }
 
 // Tensors of a list with no elements have no tiles, so quant_list_kernel never
 // visits them; their inv_scale still follows from their amax like any other's.
 template <int FT>
-__global__ void quant_list_empty_kernel(ListView X, const float *amax, float *inv_scale,
-                                        EpsFloor ef, const int32_t *skip_if) {
+__global__ void quant_list_empty_kernel(ListView X, int use_slots, const float *amax,
+                                        float *inv_scale, EpsFloor ef, const int32_t *skip_if) {
     pdl_wait();
     pdl_trigger();
     if (skip_if && *skip_if) return;
     for (int t = threadIdx.x; t < X.n; t += blockDim.x) {
         if (X.numel[t] != 0) continue;
+        const int a = use_slots ? X.slots[t] : t;
         float s32, inv;
-        tensor_scale(amax[t], ef, fp8_max<FT>(), s32, inv);
-        inv_scale[t] = inv;
+        tensor_scale(amax[a], ef, fp8_max<FT>(), s32, inv);
+        inv_scale[a] = inv;
     }
 }
 
@@ -343,12 +351,13 @@ cudaError_t launch_fp8_quant_list(const ListView &x, int64_t n_tiles, bool any_e
                                   const ListView &out, const ListView *out_t, int fp8,
                                   double eps, const float *amax, float *inv_scale,
                                   const int32_t *skip_if, cudaStream_t s, const int32_t *sr_step,
-                                  uint64_t sr_seed) {
+                                  uint64_t sr_seed, bool use_slots) {
+    const int us = use_slots ? 1 : 0;
     if (any_empty) {
         if (fp8 == kE4M3) launch_pdl(quant_list_empty_kernel<kE4M3>, dim3(1), dim3(kThreads), 0, s,
-                                     x, amax, inv_scale, make_eps_floor(eps, fp8_max<kE4M3>()),
-                                     skip_if);
-        else launch_pdl(quant_list_empty_kernel<kE5M2>, dim3(1), dim3(kThreads), 0, s, x, amax,
+                                     x, us, amax, inv_scale,
+                                     make_eps_floor(eps, fp8_max<kE4M3>()), skip_if);
+        else launch_pdl(quant_list_empty_kernel<kE5M2>, dim3(1), dim3(kThreads), 0, s, x, us, amax,
                         inv_scale, make_eps_floor(eps, fp8_max<kE5M2>()), skip_if);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -359,10 +368,10 @@ cudaError_t launch_fp8_quant_list(const ListView &x, int64_t n_tiles, bool any_e
     const dim3 grid((unsigned)n_tiles), block(kThreads);
     const EpsFloor ef = make_eps_floor(eps, fp8 == kE4M3 ? fp8_max<kE4M3>() : fp8_max<kE5M2>());
 #define AMP_QL(XT, FT)                                                                       \
-    (sr_step ? launch_pdl(quant_list_sr_kernel<XT, FT>, grid, block, 0, s, x, out, ot, has_t,     \
+    (sr_step ? launch_pdl(quant_list_sr_kernel<XT, FT>, grid, block, 0, s, x, out, ot, has_t, us, \
                           amax, inv_scale, ef, skip_if, sr_seed, sr_step)                        \
-             : launch_pdl(quant_list_kernel<XT, FT>, grid, block, 0, s, x, out, ot, has_t, amax,  \
-                          inv_scale, ef, skip_if))
+             : launch_pdl(quant_list_kernel<XT, FT>, grid, block, 0, s, x, out, ot, has_t, us,    \
+                          amax, inv_scale, ef, skip_if))
     if (fp8 == kE4M3) {
         if (xelem == kBF16) AMP_QL(kBF16, kE4M3);
         else if (xelem == kF16) AMP_QL(kF16, kE4M3);

@@ -32,7 +32,8 @@ struct amp_tensor_list_s {
     std::vector<int64_t> numel, rows, cols;
     int64_t n_chunks = 0;
     int64_t n_tiles = 0;
-    bool has_slots = false;
+    bool has_slots = false;  // some slot >= 0
+    int32_t min_slot = -1;   // the smallest slot (a cast list needs every slot >= 0)
     void *block = nullptr;   // the single device allocation
     void *scratch = nullptr; // 256 bytes of it for per-call kernel scalars
     float *tscale = nullptr; // one float per tensor of it (per-call scratch)
@@ -136,11 +137,13 @@ cudaError_t launch_fp8_quant_rowwise(const void *x, int xelem, int64_t rows, int
                                      int device, cudaStream_t s);
 
 // sr_step non-NULL: the stochastic cast, random counters from the step count
-// *sr_step and sr_seed.
+// *sr_step and sr_seed.  use_slots: tensor t takes amax / inv_scale (and the
+// random counter's tensor word) at x.slots[t] instead of t.
 cudaError_t launch_fp8_quant_list(const ListView &x, int64_t n_tiles, bool any_empty, int xelem,
                                   const ListView &out, const ListView *out_t, int fp8,
                                   double eps, const float *amax, float *inv_scale,
                                   const int32_t *skip_if, cudaStream_t s,
-                                  const int32_t *sr_step = nullptr, uint64_t sr_seed = 0);
+                                  const int32_t *sr_step = nullptr, uint64_t sr_seed = 0,
+                                  bool use_slots = false);
 
 }  // namespace amp

@@ -31,7 +31,7 @@ class AmpOptimizerStep:
                  growth_interval=2000, emit_bf16=True, fp8_shapes=None, fp8_eps=1e-12,
                  max_norm=None, fp8_scaling="dynamic", amax_history_len=1, sr_seed=None,
                  min_scale=None, fp8_format="e4m3fn", data_parallel=False, dp_group=None,
-                 stream=None):
+                 fp8_slots=None, n_fp8_total=None, stream=None):
         """master: fp32 device tensors (updated in place); grads: device
         tensors (f16/bf16/f32) the caller fills with scaled gradients before
         each step.  fp8_shapes: per tensor (rows, cols) for weights that get
@@ -53,8 +53,16 @@ class AmpOptimizerStep:
         is all-reduced (MAX) over dp_group (None: the default group of
         torch.distributed) on the step's stream, so every rank skips together,
         and with max_norm the fp64 sum of squares is all-reduced (SUM) too, so
-        every rank clips by the global norm.  Whole tensors belong to one rank,
-        so nothing else is exchanged."""
+        every rank clips by the global norm.  fp8_slots / n_fp8_total: flat
+        (FSDP-style) shards, where a weight can span ranks (sharded.
+        partition_flat): per tensor of this rank the weight's index among all
+        n_fp8_total FP8 weights of the model (None for tensors without an FP8
+        copy), fp8_shapes giving the rank's band of rows of each.  amax and
+        inv_scale are then indexed by that global number, and with
+        data_parallel the amax array is all-reduced (MAX) after each update,
+        before the FP8 cast (dynamic scaling, round-to-nearest).  Without
+        fp8_slots whole tensors belong to one rank and the amax needs no
+        exchange."""
         dev = master[0].device
         self.stream = stream
         self.master = list(master)
@@ -89,6 +97,13 @@ class AmpOptimizerStep:
         self.L_b = mk(self.bf16) if emit_bf16 else None
         self.n_fp8 = 0
         self.fp8, self.fp8_t = [], []
+        self.flat = fp8_slots is not None
+        if self.flat and (fp8_shapes is None or n_fp8_total is None or
+                          len(fp8_slots) != len(self.master)):
+            raise ValueError("flat shards need fp8_shapes, fp8_slots per tensor and n_fp8_total")
+        if self.flat and (fp8_scaling != "dynamic" or sr_seed is not None):
+            raise ValueError("flat shards are offered with dynamic scaling and "
+                             "round-to-nearest copies")
         if fp8_shapes is not None:
             if not emit_bf16:
                 raise ValueError("FP8 weight copies are cast from the bf16 copy (emit_bf16=True)")
@@ -97,7 +112,13 @@ class AmpOptimizerStep:
                 if sh is None:
                     slots.append(-1)
                     continue
-                slots.append(self.n_fp8)
+                if self.flat:
+                    if fp8_slots[i] is None or not 0 <= fp8_slots[i] < n_fp8_total:
+                        raise ValueError(f"tensor {i}: FP8 slot {fp8_slots[i]} outside "
+                                         f"0..{n_fp8_total - 1}")
+                    slots.append(int(fp8_slots[i]))
+                else:
+                    slots.append(self.n_fp8)
                 self.n_fp8 += 1
                 xs.append(self.bf16[i].view(sh[0], sh[1]))
                 self.fp8.append(torch.empty(sh, dtype=fp8_tdt, device=dev))
@@ -105,10 +126,16 @@ class AmpOptimizerStep:
                                               device=dev))
             A.amp_tensor_list_set_amax_slots(self.L_b, slots, stream=stream)
             self.L_x8 = mk(xs, True)
+            if self.flat:
+                A.amp_tensor_list_set_amax_slots(self.L_x8, [x for x in slots if x >= 0],
+                                                 stream=stream)
             self.L_q = mk(self.fp8, True)
             self.L_qt = mk(self.fp8_t, True)
-        self.amax = torch.zeros(max(self.n_fp8, 1), dtype=torch.float32, device=dev)
-        self.inv_scale = torch.zeros(max(self.n_fp8, 1), dtype=torch.float32, device=dev)
+        # amax / inv_scale entries: one per FP8 weight of this object, or (flat
+        # shards) one per FP8 weight of the whole model
+        self.n_amax = int(n_fp8_total) if self.flat else self.n_fp8
+        self.amax = torch.zeros(max(self.n_amax, 1), dtype=torch.float32, device=dev)
+        self.inv_scale = torch.zeros(max(self.n_amax, 1), dtype=torch.float32, device=dev)
         self.fp8_scaling = fp8_scaling
         self.hist_len = amax_history_len
         self.sr_seed = sr_seed
@@ -156,7 +183,12 @@ class AmpOptimizerStep:
         if self.bf16 is None:
             return
         A.amp_emit_bf16(self.L_master, self.L_b, self.amax if self.n_fp8 else None, stream=stream)
+        if not self.n_fp8 and not self.flat:
+            return
+        self._combine_amax(stream)
         if not self.n_fp8:
+            with torch.cuda.stream(stream) if stream is not None else _nullctx():
+                self.amax.zero_()
             return
         A.fp8_quant_tensorwise_list(self.L_x8, self.L_q, self.L_qt, self.fp8_format, self.amax,
                                     self.inv_scale, eps=self.fp8_eps, stream=stream)
@@ -262,6 +294,7 @@ class AmpOptimizerStep:
                                              self.scale, self.found_inf, self.step_count,
                                              *self.hyper, self.grad_sumsq, self.max_norm,
                                              amax=amax, stream=s)
+        self._combine_amax(s)
         if self.n_fp8:
             if sr:
                 A.fp8_quant_tensorwise_list_sr(self.L_x8, self.L_q, self.L_qt, self.fp8_format,
@@ -273,8 +306,8 @@ class AmpOptimizerStep:
                                             self.amax, self.inv_scale, eps=self.fp8_eps,
                                             skip_if=self.found_inf, stream=s)
         A.amp_update_scale(self.scale, self.growth_tracker, self.found_inf, self.growth,
-                           self.backoff, self.interval, amax=self.amax if self.n_fp8 else None,
-                           n_amax=self.n_fp8, stream=s)
+                           self.backoff, self.interval, amax=self.amax if self.n_amax else None,
+                           n_amax=self.n_amax, stream=s)
         self._health(s)
 
     def _combine(self, s, norm: bool = False):
@@ -287,6 +320,15 @@ class AmpOptimizerStep:
             combine_found_inf(self.found_inf, self.dp_group)
             if norm:
                 combine_grad_sumsq(self.grad_sumsq, self.dp_group)
+
+    def _combine_amax(self, s):
+        """Flat data-parallel shards: all-reduce(MAX) of the amax array over the
+        group, so every rank casts its band with its weight's global amax."""
+        if not (self.flat and self.data_parallel):
+            return
+        from .sharded import combine_amax
+        with torch.cuda.stream(s) if s is not None else _nullctx():
+            combine_amax(self.amax, self.dp_group)
 
     def _health(self, s):
         if self.min_scale is not None:
@@ -354,7 +396,7 @@ class AmpOptimizerStep:
 
     def state_fp8(self) -> dict:
         """Host copies of the FP8 scaling state (synchronises)."""
-        d = {"amax": self.amax[:self.n_fp8].cpu(), "inv_scale": self.inv_scale[:self.n_fp8].cpu()}
+        d = {"amax": self.amax[:self.n_amax].cpu(), "inv_scale": self.inv_scale[:self.n_amax].cpu()}
         if self.fp8_scaling == "delayed":
             d["amax_history"] = self.amax_history.cpu()
         return d

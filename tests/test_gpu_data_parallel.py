@@ -106,3 +106,116 @@ def test_two_ranks_on_one_gpu_match_the_unsharded_step(clip):
                     np.testing.assert_allclose(got, ref, rtol=1e-6, atol=1e-6 * rms)
                 else:
                     assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+# ------------------------------------------------ flat (FSDP-style) shards
+FLAT_SHAPES = [(1000,), (64, 64), (257,), (200, 200), (17,), (640,)]
+FLAT_FP8 = [None, 0, None, 1, None, None]          # global FP8 index of each 2-D weight
+
+
+def _flat_inputs():
+    rng = np.random.default_rng(78)
+    sizes = [int(np.prod(s)) for s in FLAT_SHAPES]
+    master = [(rng.standard_normal(n) * 0.02).astype(np.float32) for n in sizes]
+    grads = []
+    for step in range(4):
+        g = [(rng.standard_normal(n) * 1e-5 * 65536).astype(np.float16).view(np.uint16)
+             for n in sizes]
+        if step == 1:
+            g[3][150 * 200 + 7] = 0x7C00     # +inf in the second rank's rows of the FP8 weight
+        grads.append(g)
+    return master, grads
+
+
+def _rank_flat(rank, world, port, q):
+    import torch
+    import torch.distributed as dist
+
+    import loss_scaling_master_gb300 as A
+    from loss_scaling_master_gb300.sharded import partition_flat
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    dev = torch.device("cuda:0")
+    pieces = partition_flat(FLAT_SHAPES, world)[rank]
+    master, grads = _flat_inputs()
+    P = [torch.from_numpy(master[t][b:e].copy()).to(dev) for t, b, e in pieces]
+    G = [torch.empty(e - b, dtype=torch.float16, device=dev) for t, b, e in pieces]
+    shapes = [((e - b) // FLAT_SHAPES[t][1], FLAT_SHAPES[t][1]) if FLAT_FP8[t] is not None
+              else None for t, b, e in pieces]
+    st = A.AmpOptimizerStep(P, G, **HYPER, init_scale=65536.0, growth_interval=2,
+                            fp8_shapes=shapes, fp8_slots=[FLAT_FP8[t] for t, _, _ in pieces],
+                            n_fp8_total=2, data_parallel=True)
+    first = [q_.view(torch.uint8).cpu().numpy().copy() for q_ in st.fp8]
+    states = []
+    for g in grads:
+        for tt, (t, b, e) in zip(G, pieces):
+            tt.copy_(torch.from_numpy(g[t][b:e].view(np.int16).copy()).view(torch.float16))
+        st.step()
+        states.append(st.state())
+    out = dict(p=[x.cpu().numpy() for x in P], bf=[x.view(torch.int16).cpu().numpy().view(np.uint16)
+                                                  for x in st.bf16],
+               q=[x.view(torch.uint8).cpu().numpy() for x in st.fp8],
+               qt=[x.view(torch.uint8).cpu().numpy() for x in st.fp8_t],
+               inv=st.inv_scale.cpu().numpy(), first=first)
+    st.check()
+    st.close()
+    q.put((rank, pieces, shapes, states, out))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_ranks_flat_shards_on_one_gpu_match_the_unsharded_step():
+    """Flat shards through AmpOptimizerStep(fp8_slots=..., data_parallel=True):
+    a weight with an FP8 copy spans both ranks; each rank's amax of its rows
+    is all-reduced (MAX) before the cast, from the first working copies on.
+    The union of the bands of FP8 rows, of the column slices of the
+    transposed copy, and of master and bf16 equals the unsharded oracle step
+    bit for bit; every rank holding rows of a weight has the whole weight's
+    inv_scale."""
+    import oracle as O
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank_flat, args=(r, world, port, q)) for r in range(world)]
+    for pr in procs:
+        pr.start()
+    res = [q.get(timeout=300) for _ in range(world)]
+    for pr in procs:
+        pr.join(timeout=120)
+        assert pr.exitcode == 0
+    master, grads = _flat_inputs()
+    fp8_shapes = [s if FLAT_FP8[i] is not None else None for i, s in enumerate(FLAT_SHAPES)]
+    orc = O.AmpStepOracle(master, "f16", HYPER["lr"], HYPER["beta1"], HYPER["beta2"],
+                          HYPER["eps"], HYPER["weight_decay"], 65536.0, 2.0, 0.5, 2,
+                          fp8_shapes=fp8_shapes)
+    first = {t: orc.fp8[t].copy() for t in (1, 3)}          # the first working copies
+    trace = []
+    for g in grads:
+        orc.run([x.copy() for x in g])
+        trace.append((orc.scale, orc.tracker, orc.step))
+    assert trace[1] == (32768.0, 0, 1)                       # the inf step is skipped
+    full = {t: np.zeros(FLAT_SHAPES[t], np.uint8) for t in (1, 3)}
+    full_t = {t: np.zeros(FLAT_SHAPES[t][::-1], np.uint8) for t in (1, 3)}
+    full0 = {t: np.zeros(FLAT_SHAPES[t], np.uint8) for t in (1, 3)}
+    owners = {}
+    for rank, pieces, shapes, states, out in res:
+        assert [(s["scale"], s["growth_tracker"], s["step"]) for s in states] == trace
+        j = 0
+        for k, (t, b, e) in enumerate(pieces):
+            assert np.array_equal(out["p"][k].view(np.uint32), orc.master[t][b:e].view(np.uint32))
+            assert np.array_equal(out["bf"][k], orc.bf16[t][b:e])
+            if shapes[k] is None:
+                continue
+            owners.setdefault(t, set()).add(rank)
+            r0, nr = b // FLAT_SHAPES[t][1], shapes[k][0]
+            full[t][r0:r0 + nr] = out["q"][j]
+            full_t[t][:, r0:r0 + nr] = out["qt"][j]
+            full0[t][r0:r0 + nr] = out["first"][j]
+            j += 1
+        for t in {t for (t, _, _), sh in zip(pieces, shapes) if sh is not None}:
+            assert out["inv"][FLAT_FP8[t]] == orc.inv_scale[FLAT_FP8[t]]   # the owners' bands
+    assert owners[3] == {0, 1}
+    for t in (1, 3):
+        assert np.array_equal(full[t].ravel(), orc.fp8[t])
+        assert np.array_equal(full_t[t].ravel(), orc.fp8_t[t])
+        assert np.array_equal(full0[t].ravel(), first[t])

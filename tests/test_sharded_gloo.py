@@ -179,3 +179,139 @@ def test_two_rank_gloo_clipped_step_uses_the_global_norm():
             for got, ref in ((pr[k], p[i]), (mr[k], m[i]), (vr[k], v[i])):
                 rms = np.sqrt(np.mean(ref.astype(np.float64) ** 2))
                 np.testing.assert_allclose(got, ref, rtol=1e-6, atol=1e-6 * rms)
+
+
+# ------------------------------------------------ flat (FSDP-style) shards
+FLAT_SHAPES = [(1000,), (64, 64), (257,), (200, 200), (17,), (640,)]
+FLAT_FP8 = [None, 0, None, 1, None, None]          # global FP8 index of each 2-D weight
+
+
+def test_partition_flat_covers_everything_once_on_row_and_vector_boundaries():
+    from loss_scaling_master_gb300.sharded import partition_flat
+    sizes = [int(np.prod(s)) for s in FLAT_SHAPES]
+    for world in (1, 2, 3, 4, 7):
+        parts = partition_flat(FLAT_SHAPES, world)
+        assert len(parts) == world
+        flat = [(t, b, e) for p in parts for (t, b, e) in p]
+        # in flat order, contiguous, each tensor covered exactly once
+        pos = 0
+        offs = np.concatenate([[0], np.cumsum(sizes)])
+        for t, b, e in flat:
+            assert offs[t] + b == pos and e > b
+            pos = offs[t] + e
+        assert pos == offs[-1]
+        for t, b, e in flat:
+            s = FLAT_SHAPES[t]
+            for x in (b, e):
+                if len(s) == 2:
+                    assert x % s[1] == 0 and ((x // s[1]) % 16 == 0 or x == sizes[t]), (t, x)
+                else:
+                    assert x % 8 == 0 or x == sizes[t], (t, x)
+        # balanced to within one cut unit of the even share
+        loads = [sum(e - b for _, b, e in p) for p in parts]
+        assert max(loads) - min(loads) <= 2 * 16 * 200 + 8
+
+
+def _flat_inputs():
+    rng = np.random.default_rng(77)
+    sizes = [int(np.prod(s)) for s in FLAT_SHAPES]
+    master = [(rng.standard_normal(n) * 0.02).astype(np.float32) for n in sizes]
+    grads = []
+    for step in range(4):
+        g = [(rng.standard_normal(n) * 1e-5 * 65536).astype(np.float16).view(np.uint16)
+             for n in sizes]
+        if step == 1:
+            g[3][150 * 200 + 7] = 0x7C00     # +inf in the second rank's rows of the FP8 weight
+        grads.append(g)
+    return master, grads
+
+
+def _rank_flat(rank, world, port, q):
+    import torch
+    import torch.distributed as dist
+
+    import oracle as O
+    from loss_scaling_master_gb300.sharded import (combine_amax, combine_found_inf,
+                                                   partition_flat)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    pieces = partition_flat(FLAT_SHAPES, world)[rank]
+    master, grads = _flat_inputs()
+    p = [master[t][b:e].copy() for t, b, e in pieces]
+    m = [np.zeros_like(x) for x in p]
+    v = [np.zeros_like(x) for x in p]
+    bf = [np.zeros(x.size, np.uint16) for x in p]
+    slots = [FLAT_FP8[t] if FLAT_FP8[t] is not None else -1 for t, _, _ in pieces]
+    scale, tracker, step = 65536.0, 0, 0
+    fp8 = {}
+    for g in grads:
+        gs = [g[t][b:e].copy() for t, b, e in pieces]
+        fi = torch.tensor([O.unscale_check(gs, "f16", scale)], dtype=torch.int32)
+        combine_found_inf(fi)
+        amax = np.zeros(2, np.float32)
+        step = O.adamw_master_step(p, m, v, gs, "f16", bf, scale, int(fi.item()), step, *HYPER,
+                                   amax_slot=slots, amax=amax)
+        at = torch.from_numpy(amax.copy())
+        combine_amax(at)                      # the global amax of every FP8 weight
+        if not int(fi.item()):
+            for k, (t, b, e) in enumerate(pieces):
+                if FLAT_FP8[t] is None:
+                    continue
+                cols = FLAT_SHAPES[t][1]
+                q_, qt, inv, _ = O.fp8_quant_tensorwise(bf[k], "bf16", (e - b) // cols, cols,
+                                                        "e4m3fn", amax=float(at[FLAT_FP8[t]]))
+                fp8[t] = (b // cols, q_, qt, inv)
+        scale, tracker, _ = O.update_scale(scale, tracker, int(fi.item()), 2.0, 0.5, 2)
+    q.put((rank, pieces, p, m, v, bf, fp8, scale, tracker, step))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_rank_gloo_flat_shards_match_unsharded():
+    """A weight with an FP8 copy spans both ranks.  Each rank updates its
+    flat slice, folds the amax of its rows, and the amax array is all-reduced
+    (MAX) before the cast: the union of the ranks' bands of FP8 rows, of their
+    column slices of the transposed copy, and of master, m, v and bf16 equals
+    the unsharded oracle step bit for bit, and an inf in one rank's rows makes
+    both skip."""
+    import oracle as O
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank_flat, args=(r, world, port, q)) for r in range(world)]
+    for pr in procs:
+        pr.start()
+    res = [q.get(timeout=120) for _ in range(world)]
+    for pr in procs:
+        pr.join(timeout=60)
+        assert pr.exitcode == 0
+    master, grads = _flat_inputs()
+    fp8_shapes = [s if FLAT_FP8[i] is not None else None for i, s in enumerate(FLAT_SHAPES)]
+    orc = O.AmpStepOracle(master, "f16", *HYPER, 65536.0, 2.0, 0.5, 2, fp8_shapes=fp8_shapes)
+    for g in grads:
+        orc.run([x.copy() for x in g])
+    assert orc.step == 3 and orc.scale == 65536.0
+    spans = {}
+    for rank, pieces, p, m, v, bf, fp8, sc, tr, st in res:
+        assert (sc, tr, st) == (orc.scale, orc.tracker, orc.step)
+        for k, (t, b, e) in enumerate(pieces):
+            spans.setdefault(t, []).append(rank)
+            assert np.array_equal(p[k].view(np.uint32), orc.master[t][b:e].view(np.uint32))
+            assert np.array_equal(m[k].view(np.uint32), orc.exp_avg[t][b:e].view(np.uint32))
+            assert np.array_equal(v[k].view(np.uint32), orc.exp_avg_sq[t][b:e].view(np.uint32))
+            assert np.array_equal(bf[k], orc.bf16[t][b:e])
+    assert sorted(spans[3]) == [0, 1]                      # the FP8 weight spans the ranks
+    for t, shp in enumerate(FLAT_SHAPES):
+        if FLAT_FP8[t] is None:
+            continue
+        rows, cols = shp
+        full, full_t = np.zeros((rows, cols), np.uint8), np.zeros((cols, rows), np.uint8)
+        for rank, _, _, _, _, _, fp8, *_ in res:
+            if t in fp8:
+                r0, q_, qt, inv = fp8[t]
+                nr = q_.size // cols
+                full[r0:r0 + nr] = q_.reshape(nr, cols)
+                full_t[:, r0:r0 + nr] = qt.reshape(cols, nr)
+                assert inv == orc.inv_scale[FLAT_FP8[t]]       # one scale for the whole weight
+        assert np.array_equal(full.ravel(), orc.fp8[t])
+        assert np.array_equal(full_t.ravel(), orc.fp8_t[t])
