@@ -1483,6 +1483,30 @@ def test_fp8_groupwise_scale_over_many_amax_values(A, dev, fmt):
 
 
 @pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
+def test_scale_formula_dense_where_it_is_tightest(A, dev, fmt):
+    """The kernels form scale = fp8_max / amax and inv_scale = amax / fp8_max
+    with IEEE fp32 divisions in place of the fp64 recipe rounded to fp32; the
+    argument for equality is tightest where amax / fp8_max is exact, i.e. where
+    amax's significand is a multiple of 7 (fp8_max = 7 * 2^k).  Every fp32
+    significand m with m % 7 in {0, 1, 2, 5, 6} (the multiples and their two
+    neighbours on each side) at the smallest normal exponent, at 2^-20, 2^0,
+    2^20 and 2^127, and every subnormal pattern with that residue (where the
+    EPS floor decides), as single-element rows of the per-row quantizer: amax,
+    scale, inv_scale and the byte equal the oracle's fp64 formula."""
+    m = np.arange(1 << 23, 1 << 24, dtype=np.uint32)
+    m = m[np.isin(m % 7, [0, 1, 2, 5, 6])] - np.uint32(1 << 23)
+    sub = np.arange(1, 1 << 23, dtype=np.uint32)
+    sub = sub[np.isin(sub % 7, [0, 1, 2, 5, 6])]
+    for e in (-126, -20, 0, 20, 127, None):
+        bits = sub if e is None else (np.uint32(e + 127) << np.uint32(23)) | m
+        x = bits.view(np.float32)
+        rows = x.size
+        got = _run_rowwise(A, dev, x, "f32", rows, 1, fmt, False)
+        ref = O.fp8_quant_rowwise(x, "f32", rows, 1, fmt, transposed=False)
+        _assert_same(got, ref, ("dense scale", e))
+
+
+@pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
 @pytest.mark.parametrize("xdt", ["bf16", "f16"])
 @pytest.mark.parametrize("group", [32, 64, 128])
 def test_fp8_groupwise_nonfinite_16bit(A, dev, fmt, xdt, group):
