@@ -132,13 +132,7 @@ __device__ __forceinline__ uint4 compute_store_group(Group<GT> &r, float *pp, fl
     if (BF16) {
         uint4 o;
         if constexpr (SR) {
-            const uint32_t w[4] = {rnd->x, rnd->y, rnd->z, rnd->w};
-            uint32_t h[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                h[j] = bf16_stochastic(p[2 * j], w[j] & 0xFFFFu) |
-                       (bf16_stochastic(p[2 * j + 1], w[j] >> 16) << 16);
-            o = make_uint4(h[0], h[1], h[2], h[3]);
+            o = bf16x8_stochastic(p, *rnd);
         } else {
             o.x = f32x2_to_bf16x2(p[0], p[1]);
             o.y = f32x2_to_bf16x2(p[2], p[3]);
@@ -479,7 +473,41 @@ __device__ __forceinline__ void adamw_fp8_tile(const Fp8StepParams &P) {
                       aligned16(pp) && aligned16(mp) && aligned16(vp) && aligned16(gp) &&
                       aligned16(bp) && (reinterpret_cast<uintptr_t>(qp) & 7) == 0 &&
                       (qtp == nullptr || ((rows & 15) == 0 && aligned16(qtp)));
-    if (fast) {
+    if (fast && SR) {
+        // The stochastic form loads the next two groups before it rounds the
+        // FP8 bytes of the current two, so that the generator draws and the
+        // roundings, which need no memory, run while those loads are in flight.
+        const int c8 = threadIdx.x & 15, rb = threadIdx.x >> 4;
+        const int32_t bid = int32_t(uint32_t(t) | kSrFp8GroupBit);
+        int64_t ea = (r0 + rb) * cols + c0 + 8 * c8, eb = ea + 16 * cols;
+        Group<GT> a, b;
+        load_group<GT>(a, pp, mp, vp, gp, ea);
+        load_group<GT>(b, pp, mp, vp, gp, eb);
+#pragma unroll 1
+        for (int k = 0; k < 8; k += 2) {
+            const uint4 rna = sr_random8(P.sr_seed, sc.t, bid, ea >> 3);
+            const uint4 rnb = sr_random8(P.sr_seed, sc.t, bid, eb >> 3);
+            const uint4 oa = compute_store_group<GT, true, true>(a, pp, mp, vp, bp, ea, s, amax2,
+                                                                 &rna);
+            const uint4 ob = compute_store_group<GT, true, true>(b, pp, mp, vp, bp, eb, s, amax2,
+                                                                 &rnb);
+            const int64_t ea0 = ea, eb0 = eb;
+            if (k + 2 < 8) {
+                ea += 32 * cols;
+                eb += 32 * cols;
+                load_group<GT>(a, pp, mp, vp, gp, ea);
+                load_group<GT>(b, pp, mp, vp, gp, eb);
+            }
+            const uint2 qa = bf16x8_to_fp8x8_sr<FT>(oa, s32, P.sr_seed, sc.t, t, ea0);
+            const uint2 qb = bf16x8_to_fp8x8_sr<FT>(ob, s32, P.sr_seed, sc.t, t, eb0);
+            *reinterpret_cast<uint2 *>(qp + ea0) = qa;
+            *reinterpret_cast<uint2 *>(qp + eb0) = qb;
+            if (qtp) {
+                *reinterpret_cast<uint2 *>(sm + swz(rb + 16 * k, 2 * c8)) = qa;
+                *reinterpret_cast<uint2 *>(sm + swz(rb + 16 * (k + 1), 2 * c8)) = qb;
+            }
+        }
+    } else if (fast) {
         const int c8 = threadIdx.x & 15, rb = threadIdx.x >> 4;
 #pragma unroll 1
         for (int k = 0; k < 8; k += 2) {
@@ -489,23 +517,10 @@ __device__ __forceinline__ void adamw_fp8_tile(const Fp8StepParams &P) {
             Group<GT> a, b;
             load_group<GT>(a, pp, mp, vp, gp, ea);
             load_group<GT>(b, pp, mp, vp, gp, eb);
-            uint2 qa, qb;
-            if constexpr (SR) {
-                const int32_t bid = int32_t(uint32_t(t) | kSrFp8GroupBit);
-                const uint4 ra = sr_random8(P.sr_seed, sc.t, bid, ea >> 3);
-                const uint4 rbv = sr_random8(P.sr_seed, sc.t, bid, eb >> 3);
-                const uint4 oa = compute_store_group<GT, true, true>(a, pp, mp, vp, bp, ea, s,
-                                                                     amax2, &ra);
-                const uint4 ob = compute_store_group<GT, true, true>(b, pp, mp, vp, bp, eb, s,
-                                                                     amax2, &rbv);
-                qa = bf16x8_to_fp8x8_sr<FT>(oa, s32, P.sr_seed, sc.t, t, ea);
-                qb = bf16x8_to_fp8x8_sr<FT>(ob, s32, P.sr_seed, sc.t, t, eb);
-            } else {
-                const uint4 oa = compute_store_group<GT, true>(a, pp, mp, vp, bp, ea, s, amax2);
-                const uint4 ob = compute_store_group<GT, true>(b, pp, mp, vp, bp, eb, s, amax2);
-                qa = bf16x8_to_fp8x8<FT>(oa, s32);
-                qb = bf16x8_to_fp8x8<FT>(ob, s32);
-            }
+            const uint4 oa = compute_store_group<GT, true>(a, pp, mp, vp, bp, ea, s, amax2);
+            const uint4 ob = compute_store_group<GT, true>(b, pp, mp, vp, bp, eb, s, amax2);
+            const uint2 qa = bf16x8_to_fp8x8<FT>(oa, s32);
+            const uint2 qb = bf16x8_to_fp8x8<FT>(ob, s32);
             *reinterpret_cast<uint2 *>(qp + ea) = qa;
             *reinterpret_cast<uint2 *>(qp + eb) = qb;
             if (qtp) {
@@ -513,11 +528,12 @@ __device__ __forceinline__ void adamw_fp8_tile(const Fp8StepParams &P) {
                 *reinterpret_cast<uint2 *>(sm + swz(rbb, 2 * c8)) = qb;
             }
         }
-        if (qtp) {
-            __syncthreads();
-            store_transposed_tile(sm, qtp, rows, r0, c0);
-        }
-    } else {
+    }
+    if (fast && qtp) {
+        __syncthreads();
+        store_transposed_tile(sm, qtp, rows, r0, c0);
+    }
+    if (!fast) {
         for (int idx = threadIdx.x; idx < kTile * kTile; idx += kThreads) {
             const int64_t i = r0 + (idx >> 7), j = c0 + (idx & (kTile - 1));
             if (i < rows && j < cols) {

@@ -22,7 +22,7 @@
 // take an element-wise path with the same arithmetic.
 // The list cast has a stochastic-rounding form for the FP8 weight copies
 // ("第20章 量化与混合精度训练" §20.5.14): the same scaled fp32 values, each
-// rounded by fp8_stochastic (philox.cuh) with 32 random bits drawn per
+// rounded by fp8_stochastic (philox.cuh) with 16 random bits drawn per
 // element from its row-major index, so the transposed copy holds the same
 // bytes.
 #include <algorithm>

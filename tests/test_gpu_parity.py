@@ -1048,6 +1048,43 @@ def test_fp8_stochastic_unbiased_on_gpu(A, dev, fmt, tdt):
     LQ.close()
 
 
+@pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
+def test_fp8_stochastic_rule_dense_over_fp32_patterns(A, dev, fmt):
+    """The stochastic FP8 rule on 4M fp32 bit patterns spread (odd stride, so
+    the low fraction bits vary) over every magnitude where the rounding has a
+    non-zero chance of going up: the FP8 subnormal range, the normal binades,
+    the clamp above fp8_max; every other pattern negative, and NaN and
+    infinities planted.  f32 input with amax = fp8_max gives a cast scale of
+    exactly 1, so the cast rounds these patterns themselves; every byte of
+    both layouts equals the oracle's."""
+    rows, cols = 2048, 2048
+    n = rows * cols
+    lo, hi = 0x2F000000, 0x47800000          # 2^-33 .. 2^16: past both formats' ranges
+    k = np.arange(n, dtype=np.uint64)
+    bits = (lo + (k * 97) % (hi - lo)).astype(np.uint32)
+    bits[1::2] |= np.uint32(0x80000000)
+    bits[[10, 11, 12]] = np.array([0x7F800000, 0xFF800000, 0x7FC00001], np.uint32)
+    x = bits.view(np.float32)
+    fmax = O.fmt_max(fmt)
+    tdt = torch.float8_e4m3fn if fmt == "e4m3fn" else torch.float8_e5m2
+    xd = torch.from_numpy(x.copy()).to(dev).view(rows, cols)
+    q = torch.empty((rows, cols), dtype=tdt, device=dev)
+    qt = torch.empty((cols, rows), dtype=tdt, device=dev)
+    LX, LQ, LQT = (A.amp_tensor_list_create([t], True) for t in (xd, q, qt))
+    amax = torch.tensor([fmax], dtype=torch.float32, device=dev)
+    inv = torch.zeros(1, device=dev)
+    seed, step = 0x0123456789ABCDEF, 77
+    A.fp8_quant_tensorwise_list_sr(LX, LQ, LQT, fmt, amax, inv, seed,
+                                   torch.tensor([step], dtype=torch.int32, device=dev))
+    rq, rqt, rinv, _ = O.fp8_quant_tensorwise_sr(x, "f32", rows, cols, fmt, seed, step, 0,
+                                                 amax=fmax)
+    assert rinv == 1.0 and to_host_bits(inv)[0] == 1.0
+    assert np.array_equal(to_host_bits(q.view(torch.uint8)).ravel(), rq)
+    assert np.array_equal(to_host_bits(qt.view(torch.uint8)).ravel(), rqt)
+    for L in (LX, LQ, LQT):
+        L.close()
+
+
 # --------------------------------------------------------- checkpoint / resume
 @pytest.mark.parametrize("fp8_scaling", ["dynamic", "delayed"])
 def test_checkpoint_resume_is_bit_identical(A, dev, fp8_scaling):
