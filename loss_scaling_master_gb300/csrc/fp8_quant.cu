@@ -140,8 +140,11 @@ __global__ void __launch_bounds__(kThreads) quant_single_kernel(const void *x, i
     if (skip_if && *skip_if) return;
     __shared__ __align__(16) uint32_t sm[kTile * 32];
     __shared__ float s_scale;
+    // Tiles in reverse row-major order: the maxima pass sweeps x from its
+    // start, so its last reads, still in L2, are the first ones here.
     const int64_t tiles_c = (cols + kTile - 1) / kTile;
-    const int64_t tr = blockIdx.x / tiles_c, tc = blockIdx.x % tiles_c;
+    const int64_t tile = int64_t(gridDim.x) - 1 - blockIdx.x;
+    const int64_t tr = tile / tiles_c, tc = tile % tiles_c;
     if (threadIdx.x == 0) {
         float s32, inv;
         tensor_scale(*amax, ef, fp8_max<FT>(), s32, inv);
