@@ -5,20 +5,22 @@
 //
 // Four launches, 6 bytes per element as for the tensorwise cast:
 //   zero   amax_row[rows], amax_col[cols] <- +0 (skipped calls write nothing)
-//   amax   one wave of CTAs reads x once (2 B/elt), each walking a run of
-//          128x128 tiles down a column strip; every thread holds 8 rows x 8
+//   amax   one wave of CTAs reads x once (2 B/elt), S CTAs per column strip,
+//          each taking every S-th 128x128 tile down its strip, so that the
+//          wave sweeps x from top to bottom; every thread holds 8 rows x 8
 //          columns of a tile; row maxima are combined across the 16 lanes
 //          sharing a row (one atomicMax per row and tile), column maxima stay
-//          in registers for the strip (one atomicMax per column when the CTA
-//          leaves it); fp32 bit patterns of |x|: an unsigned max that
-//          propagates NaN
+//          in registers for the strip (one atomicMax per column at the end);
+//          fp32 bit patterns of |x|: an unsigned max that propagates NaN
 //   scale  per row and per column, fp32 multiplier and inverse written once,
 //          by fp32 divisions equal to the fp64 formula rounded to fp32
 //          (tensor_scale in fp8_tile.cuh)
 //   cast   one CTA per tile reads it again (2 B/elt), casts each element twice
 //          (row multiplier for the row-major bytes, column multiplier for the
 //          transposed bytes) and writes both (1 + 1 B/elt), the transposed
-//          tile through the swizzled shared-memory transpose.
+//          tile through the swizzled shared-memory transpose.  The tiles go
+//          in reverse row-major order, the reverse of the maxima pass's
+//          sweep, so the first reads find x still in L2.
 #include <algorithm>
 #include <atomic>
 
@@ -97,19 +99,22 @@ __global__ void rowcol_zero_kernel(float *amax_row, int64_t rows, float *amax_co
     }
 }
 
-// Row and column maxima of |x|.  The grid is a fixed number of CTAs; CTA b
-// walks the tiles [b T / G, (b+1) T / G) of the column-major tile order, so it
-// moves down one or two 128-column strips.  Per tile, each thread holds 8 rows
-// x 8 columns: row maxima are combined across the 16 lanes sharing a row and
-// sent with one atomicMax per row; column maxima stay in registers for the
-// whole strip and are combined through shared memory once, when the CTA leaves
-// the strip.  The next tile's loads are issued before the current tile is
-// reduced.  Tiles on a ragged edge, or with sizes/addresses that break 16-byte
-// access, take an element path through shared memory.
+// Row and column maxima of |x|.  The grid is S CTAs per 128-column strip:
+// CTA b takes strip b mod C (C strips) and, in it, the tile rows b / C,
+// b / C + S, b / C + 2S, ...  At step m the CTAs together read tile rows
+// [m S, m S + S) of every strip, so the pass sweeps x from top to bottom (the
+// cast then walks the tiles in reverse and meets the last reads in L2).  Per
+// tile, each thread holds 8 rows x 8 columns: row maxima are combined across
+// the 16 lanes sharing a row and sent with one atomicMax per row; column
+// maxima stay in registers for the whole strip and are combined through
+// shared memory once, at the end.  The next tile's loads are issued before
+// the current tile is reduced.  Tiles on a ragged edge, or with sizes/
+// addresses that break 16-byte access, take an element path through shared
+// memory.
 template <int XT>
 __global__ void __launch_bounds__(kThreads) rowcol_amax_kernel(const void *x, int64_t rows,
                                                                int64_t cols, unsigned *amax_row,
-                                                               unsigned *amax_col,
+                                                               unsigned *amax_col, int per_strip,
                                                                const int32_t *skip_if) {
     pdl_wait();
     pdl_trigger();
@@ -119,9 +124,7 @@ __global__ void __launch_bounds__(kThreads) rowcol_amax_kernel(const void *x, in
     constexpr int nw = XT == kF32 ? 2 : 1;
     constexpr int esz = XT == kF32 ? 4 : 2;
     const int64_t tiles_r = (rows + kTile - 1) / kTile, tiles_c = (cols + kTile - 1) / kTile;
-    const int64_t tiles = tiles_r * tiles_c;
-    const int64_t t0 = int64_t(blockIdx.x) * tiles / gridDim.x;
-    const int64_t t1 = int64_t(blockIdx.x + 1) * tiles / gridDim.x;
+    const int64_t strip = blockIdx.x % tiles_c, tr0 = blockIdx.x / tiles_c;
     const int c8 = threadIdx.x & 15, rb = threadIdx.x >> 4;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t cm[8] = {0, 0, 0, 0, 0, 0, 0, 0};
@@ -134,8 +137,8 @@ __global__ void __launch_bounds__(kThreads) rowcol_amax_kernel(const void *x, in
             if (nw == 2) raw[k][nw - 1] = ld16(p + 16);
         }
     };
-    // column maxima gathered in registers for strip tc -> one atomicMax per column
-    auto flush = [&](int64_t tc) {
+    // column maxima gathered in registers for the strip -> one atomicMax per column
+    auto flush = [&]() {
 #pragma unroll
         for (int j = 0; j < 8; ++j) cm[j] = max(cm[j], __shfl_xor_sync(0xFFFFFFFFu, cm[j], 16));
         if (lane < 16) {
@@ -148,38 +151,20 @@ __global__ void __launch_bounds__(kThreads) rowcol_amax_kernel(const void *x, in
             uint32_t m = 0;
 #pragma unroll
             for (int w = 0; w < kThreads / 32; ++w) m = max(m, colmax[w][threadIdx.x]);
-            const int64_t c = tc * kTile + threadIdx.x;
+            const int64_t c = strip * kTile + threadIdx.x;
             if (amax_col && c < cols && m != 0) atomicMax(amax_col + c, m);
         }
-        __syncthreads();
-#pragma unroll
-        for (int j = 0; j < 8; ++j) cm[j] = 0;
     };
-    auto coords = [&](int64_t t, int64_t &r0, int64_t &c0) {
-        r0 = (t % tiles_r) * kTile;
-        c0 = (t / tiles_r) * kTile;
-    };
-    int64_t strip = -1;
-    if (t0 < t1) {
-        int64_t r0, c0;
-        coords(t0, r0, c0);
-        if (tile_fast(x, rows, cols, r0, c0)) load(r0, c0);
-    }
-    for (int64_t t = t0; t < t1; ++t) {
-        int64_t r0, c0, nr0 = 0, nc0 = 0;
-        coords(t, r0, c0);
-        const bool has_next = t + 1 < t1;
-        if (has_next) coords(t + 1, nr0, nc0);
-        const int64_t tc = c0 / kTile;
-        if (tc != strip) {
-            if (strip >= 0) flush(strip);
-            strip = tc;
-        }
+    const int64_t c0 = strip * kTile;
+    if (tr0 < tiles_r && tile_fast(x, rows, cols, tr0 * kTile, c0)) load(tr0 * kTile, c0);
+    for (int64_t tr = tr0; tr < tiles_r; tr += per_strip) {
+        const int64_t r0 = tr * kTile, nr0 = r0 + int64_t(per_strip) * kTile;
+        const bool has_next = tr + per_strip < tiles_r;
         if (tile_fast(x, rows, cols, r0, c0)) {
             uint32_t a[8][8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) raw_abs<XT>(raw[k], a[k]);
-            if (has_next && tile_fast(x, rows, cols, nr0, nc0)) load(nr0, nc0);
+            if (has_next && tile_fast(x, rows, cols, nr0, c0)) load(nr0, c0);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 uint32_t rm = 0;
@@ -212,10 +197,10 @@ __global__ void __launch_bounds__(kThreads) rowcol_amax_kernel(const void *x, in
                 if (amax_col && c0 + u < cols && s_col[u] != 0) atomicMax(amax_col + c0 + u, s_col[u]);
             }
             __syncthreads();
-            if (has_next && tile_fast(x, rows, cols, nr0, nc0)) load(nr0, nc0);
+            if (has_next && tile_fast(x, rows, cols, nr0, c0)) load(nr0, c0);
         }
     }
-    if (strip >= 0) flush(strip);
+    flush();
 }
 
 __global__ void rowcol_scale_kernel(const float *amax_row, float *scale_row, float *inv_row,
@@ -247,9 +232,11 @@ __global__ void __launch_bounds__(kThreads) rowcol_cast_kernel(const void *x, in
     pdl_trigger();
     if (skip_if && *skip_if) return;
     __shared__ __align__(16) uint32_t sm[kTile * 32];
+    // tiles in reverse row-major order: the maxima pass's last reads first
     const int64_t tiles_c = (cols + kTile - 1) / kTile;
-    const int64_t r0 = int64_t(blockIdx.x / tiles_c) * kTile;
-    const int64_t c0 = int64_t(blockIdx.x % tiles_c) * kTile;
+    const int64_t tile = int64_t(gridDim.x) - 1 - blockIdx.x;
+    const int64_t r0 = (tile / tiles_c) * kTile;
+    const int64_t c0 = (tile % tiles_c) * kTile;
     const bool fast = tile_fast(x, rows, cols, r0, c0) &&
                       (reinterpret_cast<uintptr_t>(out) & 7) == 0 &&
                       (out_t == nullptr || ((rows & 15) == 0 && aligned16(out_t)));
@@ -335,11 +322,14 @@ cudaError_t launch_rowwise_t(const void *x, int64_t rows, int64_t cols, uint8_t 
             k = 1;
         per_sm.store(k, std::memory_order_relaxed);
     }
-    const unsigned amax_grid = (unsigned)std::min<int64_t>(
-        tiles, int64_t(sm_count(device)) * per_sm.load(std::memory_order_relaxed));
-    e = launch_pdl(rowcol_amax_kernel<XT>, dim3(amax_grid), dim3(kThreads), 0, s, x, rows,
-                   cols, reinterpret_cast<unsigned *>(amax_row), reinterpret_cast<unsigned *>(acol),
-                   skip_if);
+    // S CTAs per column strip, so that the CTAs resident at once cover all
+    // strips (at least one CTA per strip; no more than the strip's tiles)
+    const int64_t tiles_r = (rows + kTile - 1) / kTile, tiles_c = (cols + kTile - 1) / kTile;
+    const int64_t resident = int64_t(sm_count(device)) * per_sm.load(std::memory_order_relaxed);
+    const int64_t per_strip = std::max<int64_t>(1, std::min<int64_t>(tiles_r, resident / tiles_c));
+    e = launch_pdl(rowcol_amax_kernel<XT>, dim3((unsigned)(tiles_c * per_strip)), dim3(kThreads),
+                   0, s, x, rows, cols, reinterpret_cast<unsigned *>(amax_row),
+                   reinterpret_cast<unsigned *>(acol), int(per_strip), skip_if);
     if (e != cudaSuccess) return e;
     e = launch_pdl(rowcol_scale_kernel, dim3(small_grid), dim3(256), 0, s,
                    static_cast<const float *>(amax_row), scale_row, inv_row, rows,
