@@ -35,6 +35,9 @@
  *     caller's next synchronisation, as for any CUDA work.
  *   - Calls that touch the same buffers must be ordered on one stream (or
  *     by events); the library takes no locks.
+ *   - Within one call, buffers that are only read (x, grads) must not
+ *     overlap buffers the call writes; only the buffers named as updated in
+ *     place (master, m, v) are both read and written.
  *   - Pointers need no particular alignment: tensors whose addresses allow
  *     16-byte vector access take the vector path, others a scalar path that
  *     gives the same bits.
