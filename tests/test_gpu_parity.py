@@ -742,6 +742,22 @@ def test_fp8_rowwise_parity(A, dev, fmt, xdt):
                         assert np.array_equal(got[k], ref[k]), (k, key)
 
 
+@pytest.mark.parametrize("xdt", ["bf16", "f32"])
+@pytest.mark.parametrize("rows,cols", [(8256, 2056), (16, 76800), (76800, 8)])
+def test_fp8_rowwise_strip_walks(A, dev, xdt, rows, cols):
+    """The maxima pass gives each column strip S CTAs, each taking every S-th
+    tile row of its strip: [8256, 2056] gives every CTA several tiles with a
+    ragged last tile row and a ragged last strip in the same walk; [16, 76800]
+    has more strips than CTAs fit at once (S = 1); [76800, 8] has one narrow
+    strip and hundreds of CTAs on it.  Every byte and scale equals the
+    oracle's."""
+    rng = np.random.default_rng(93)
+    xh = _x_host(rng, rows, cols, xdt)
+    got = _run_rowwise(A, dev, xh, xdt, rows, cols, "e4m3fn", True)
+    ref = O.fp8_quant_rowwise(xh, xdt, rows, cols, "e4m3fn")
+    _assert_same(got, ref, f"rowwise strips {rows}x{cols}")
+
+
 @pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
 def test_fp8_rowwise_degenerate(A, dev, fmt):
     rng = np.random.default_rng(91)
