@@ -1,9 +1,9 @@
-"""AmpOptimizerStep(data_parallel=True) on the GPU: two ranks (processes on the
-one visible GPU, exchanging over gloo through the host, so no kernel waits on
-another rank's kernel) each step the tensors they own.  The non-finite flag
+"""AmpOptimizerStep(data_parallel=True) on the GPU: two or four ranks
+(processes on the one visible GPU, exchanging over gloo through the host, so no
+kernel waits on another rank's kernel) each step the tensors they own.  The non-finite flag
 and, with clipping, the sum of squares are all-reduced between the check and
 the update; the union of the shards must equal the unsharded oracle step, and
-an inf in one rank's gradients must make both ranks skip."""
+an inf in one rank's gradients must make every rank skip."""
 import os
 import socket
 
@@ -69,10 +69,11 @@ def _rank(rank, world, port, clip, q):
     dist.destroy_process_group()
 
 
+@pytest.mark.parametrize("world", [2, 4])
 @pytest.mark.parametrize("clip", [False, True])
-def test_two_ranks_on_one_gpu_match_the_unsharded_step(clip):
+def test_ranks_on_one_gpu_match_the_unsharded_step(clip, world):
     import oracle as O
-    world, port = 2, _free_port()
+    port = _free_port()
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     procs = [ctx.Process(target=_rank, args=(r, world, port, clip, q)) for r in range(world)]
@@ -164,16 +165,17 @@ def _rank_flat(rank, world, port, q):
     dist.destroy_process_group()
 
 
-def test_two_ranks_flat_shards_on_one_gpu_match_the_unsharded_step():
+@pytest.mark.parametrize("world", [2, 4])
+def test_flat_shards_on_one_gpu_match_the_unsharded_step(world):
     """Flat shards through AmpOptimizerStep(fp8_slots=..., data_parallel=True):
-    a weight with an FP8 copy spans both ranks; each rank's amax of its rows
+    a weight with an FP8 copy spans every rank (bands of 16-row multiples); each rank's amax of its rows
     is all-reduced (MAX) before the cast, from the first working copies on.
     The union of the bands of FP8 rows, of the column slices of the
     transposed copy, and of master and bf16 equals the unsharded oracle step
     bit for bit; every rank holding rows of a weight has the whole weight's
     inv_scale."""
     import oracle as O
-    world, port = 2, _free_port()
+    port = _free_port()
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     procs = [ctx.Process(target=_rank_flat, args=(r, world, port, q)) for r in range(world)]
@@ -214,7 +216,7 @@ def test_two_ranks_flat_shards_on_one_gpu_match_the_unsharded_step():
             j += 1
         for t in {t for (t, _, _), sh in zip(pieces, shapes) if sh is not None}:
             assert out["inv"][FLAT_FP8[t]] == orc.inv_scale[FLAT_FP8[t]]   # the owners' bands
-    assert owners[3] == {0, 1}
+    assert owners[3] == set(range(world))
     for t in (1, 3):
         assert np.array_equal(full[t].ravel(), orc.fp8[t])
         assert np.array_equal(full_t[t].ravel(), orc.fp8_t[t])

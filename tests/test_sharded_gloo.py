@@ -1,7 +1,7 @@
-"""Sharded (2-rank, gloo, CPU) step: tensors partitioned across ranks, the
-non-finite flag combined with all-reduce(MAX), each rank updating its own
+"""Sharded (2- and 4-rank, gloo, CPU) step: tensors partitioned across ranks,
+the non-finite flag combined with all-reduce(MAX), each rank updating its own
 tensors with the oracle.  The union of the shards must equal the unsharded
-oracle step, and a non-finite gradient on one rank must make both skip."""
+oracle step, and a non-finite gradient on one rank must make all skip."""
 import os
 import socket
 
@@ -72,9 +72,10 @@ def test_partition_is_balanced_and_complete():
         assert max(loads) - min(loads) <= max(SIZES)
 
 
-def test_two_rank_gloo_step_matches_unsharded():
+@pytest.mark.parametrize("world", [2, 4])
+def test_gloo_step_matches_unsharded(world):
     import oracle as O
-    world, port = 2, _free_port()
+    port = _free_port()
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     procs = [ctx.Process(target=_rank, args=(r, world, port, q)) for r in range(world)]
@@ -139,14 +140,15 @@ def _rank_clip(rank, world, port, q):
     dist.destroy_process_group()
 
 
-def test_two_rank_gloo_clipped_step_uses_the_global_norm():
+@pytest.mark.parametrize("world", [2, 4])
+def test_gloo_clipped_step_uses_the_global_norm(world):
     """With clipping, the ranks' sums of squares are summed (all-reduce SUM):
-    both ranks see the global sum and clip by the global norm, and the union
+    every rank sees the global sum and clips by the global norm, and the union
     of the shards matches the unsharded clipped step.  The global sum adds
     the ranks' partial sums in another order than the unsharded sum, so it
     and the states are compared within rel 1e-12 and rel 1e-6."""
     import oracle as O
-    world, port = 2, _free_port()
+    port = _free_port()
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     procs = [ctx.Process(target=_rank_clip, args=(r, world, port, q)) for r in range(world)]
@@ -267,15 +269,16 @@ def _rank_flat(rank, world, port, q):
     dist.destroy_process_group()
 
 
-def test_two_rank_gloo_flat_shards_match_unsharded():
-    """A weight with an FP8 copy spans both ranks.  Each rank updates its
-    flat slice, folds the amax of its rows, and the amax array is all-reduced
-    (MAX) before the cast: the union of the ranks' bands of FP8 rows, of their
-    column slices of the transposed copy, and of master, m, v and bf16 equals
-    the unsharded oracle step bit for bit, and an inf in one rank's rows makes
-    both skip."""
+@pytest.mark.parametrize("world", [2, 4])
+def test_gloo_flat_shards_match_unsharded(world):
+    """A weight with an FP8 copy spans several ranks (two of two, four of
+    four).  Each rank updates its flat slice, folds the amax of its rows, and
+    the amax array is all-reduced (MAX) before the cast: the union of the
+    ranks' bands of FP8 rows, of their column slices of the transposed copy,
+    and of master, m, v and bf16 equals the unsharded oracle step bit for bit,
+    and an inf in one rank's rows makes all skip."""
     import oracle as O
-    world, port = 2, _free_port()
+    port = _free_port()
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     procs = [ctx.Process(target=_rank_flat, args=(r, world, port, q)) for r in range(world)]
@@ -300,7 +303,7 @@ def test_two_rank_gloo_flat_shards_match_unsharded():
             assert np.array_equal(m[k].view(np.uint32), orc.exp_avg[t][b:e].view(np.uint32))
             assert np.array_equal(v[k].view(np.uint32), orc.exp_avg_sq[t][b:e].view(np.uint32))
             assert np.array_equal(bf[k], orc.bf16[t][b:e])
-    assert sorted(spans[3]) == [0, 1]                      # the FP8 weight spans the ranks
+    assert sorted(spans[3]) == list(range(world))          # the FP8 weight spans the ranks
     for t, shp in enumerate(FLAT_SHAPES):
         if FLAT_FP8[t] is None:
             continue
