@@ -173,8 +173,9 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- workloads
-def build_step(workload: str, device, seed: int, fp8_scaling: str = "dynamic"):
-    """Allocate a workload's device state; returns (step_obj, info)."""
+def build_step(workload: str, device, seed: int, fp8_scaling: str = "dynamic", sr_seed=None):
+    """Allocate a workload's device state; returns (step_obj, info).  sr_seed:
+    the step object's own step() rounds both copies stochastically."""
     import torch
 
     from loss_scaling_master_gb300 import AmpOptimizerStep
@@ -203,7 +204,8 @@ def build_step(workload: str, device, seed: int, fp8_scaling: str = "dynamic"):
                             init_scale=cfg.init_scale, growth_factor=cfg.growth_factor,
                             backoff_factor=cfg.backoff_factor,
                             growth_interval=cfg.growth_interval, fp8_shapes=fp8_shapes,
-                            fp8_scaling=fp8_scaling if fp8_shapes is not None else "dynamic")
+                            fp8_scaling=fp8_scaling if fp8_shapes is not None else "dynamic",
+                            sr_seed=sr_seed)
     n = sum(s.numel for s in cfg.specs)
     n8 = sum(s.numel for s in cfg.specs if s.fp8) if cfg.fp8_weights else 0
     gbytes = {"f16": 2, "bf16": 2, "f32": 4}[cfg.grad_dtype]

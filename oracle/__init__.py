@@ -327,7 +327,8 @@ class AmpStepOracle:
     def __init__(self, master, grad_dtype, lr, beta1, beta2, eps, weight_decay,
                  init_scale, growth_factor, backoff_factor, growth_interval,
                  emit_bf16=True, fp8_shapes=None, fp8_eps=1e-12, max_norm=None,
-                 fp8_scaling="dynamic", hist_len=1, fp8_format="e4m3fn", sr_seed=None):
+                 fp8_scaling="dynamic", hist_len=1, fp8_format="e4m3fn", sr_seed=None,
+                 sr_tensor_ids=None, sr_fp8_ids=None):
         self.master = [np.array(m, np.float32, copy=True) for m in master]
         self.exp_avg = [np.zeros_like(m) for m in self.master]
         self.exp_avg_sq = [np.zeros_like(m) for m in self.master]
@@ -349,6 +350,13 @@ class AmpStepOracle:
         # each step emits: the bf16 copy and the FP8 weights cast from it.  The
         # first working copies, made before any step, keep round-to-nearest.
         self.sr_seed = sr_seed
+        # Tensor words of the random counters, for tensors that are a subset of
+        # a larger set: sr_tensor_ids per tensor for its bf16 copy (default:
+        # the list position; in the delayed step the plain-list position p, or
+        # j | 2^30 for FP8 weight j), sr_fp8_ids per FP8 slot for its FP8 copy
+        # (default: the slot).
+        self.sr_tensor_ids = None if sr_tensor_ids is None else list(sr_tensor_ids)
+        self.sr_fp8_ids = None if sr_fp8_ids is None else list(sr_fp8_ids)
         if fp8_shapes is not None:
             self.slots, k = [], 0
             for sh in fp8_shapes:
@@ -399,7 +407,9 @@ class AmpStepOracle:
             self.grad_norm = float(np.sqrt(ss))
             clip = clip_coef(ss, self.max_norm)
         sr_ids = None
-        if self.sr_seed is not None and self.fp8_scaling == "delayed":
+        if self.sr_seed is not None and self.sr_tensor_ids is not None:
+            sr_ids = self.sr_tensor_ids
+        elif self.sr_seed is not None and self.fp8_scaling == "delayed":
             # the delayed step walks the plain tensors and the FP8 weights as
             # two lists: plain tensor p draws as p, FP8 weight j as j | 2^30
             sr_ids, p_idx = [], 0
@@ -428,9 +438,10 @@ class AmpStepOracle:
                                                          self.fp8_format, self.fp8_eps, True,
                                                          amax=a)
                 else:
+                    w = s if self.sr_fp8_ids is None else self.sr_fp8_ids[s]
                     q, qt, inv, _ = fp8_quant_tensorwise_sr(self.bf16[i], "bf16", sh[0], sh[1],
                                                             self.fp8_format, self.sr_seed,
-                                                            self.step, s, self.fp8_eps, True,
+                                                            self.step, w, self.fp8_eps, True,
                                                             amax=a)
                 self.fp8[i], self.fp8_t[i], self.inv_scale[s] = q, qt, inv
         if self.fp8_scaling == "delayed" and not fi:

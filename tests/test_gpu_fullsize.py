@@ -213,6 +213,62 @@ def test_llama3_8b_bench_state_parity(A, fp8_scaling):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("fp8_scaling", ["dynamic", "delayed"])
+def test_llama3_8b_bench_state_stochastic_parity(A, fp8_scaling):
+    """The bench's 8B state with both copies rounded stochastically (its
+    --sr-seed line), 3 steps.  Two FP8 weights and a norm vector go whole
+    through the oracle, whose random counters take the tensor words the whole
+    set's lists give them: the bf16 copy the list position (delayed step: the
+    plain-list position, or FP8 index | 2^30), the FP8 copy the FP8 index.
+    master, m, v, bf16, both FP8 layouts and inv_scale equal the oracle's bit
+    for bit."""
+    import bench
+    dev = torch.device("cuda:0")
+    torch.cuda.empty_cache()
+    seed = 0x5EED0F5EED
+    st, info = bench.build_step("llama3_8b", dev, seed=1234, fp8_scaling=fp8_scaling,
+                                sr_seed=seed)
+    cfg = info["cfg"]
+    names = [s.name for s in cfg.specs]
+    full = [names.index(n) for n in ("l0.k", "l0.v", "l5.ffn_norm")]
+    plain = [i for i, s in enumerate(cfg.specs) if not s.fp8]
+    fp8 = [i for i, s in enumerate(cfg.specs) if s.fp8]
+    if fp8_scaling == "delayed":
+        ids = [fp8.index(i) | (1 << 30) if cfg.specs[i].fp8 else plain.index(i) for i in full]
+    else:
+        ids = list(full)
+    fp8_shapes = [(cfg.specs[i].rows, cfg.specs[i].cols) if cfg.specs[i].fp8 else None
+                  for i in full]
+    orc = O.AmpStepOracle([to_host_bits(st.master[i]) for i in full], cfg.grad_dtype, cfg.lr,
+                          cfg.beta1, cfg.beta2, cfg.eps, cfg.weight_decay, cfg.init_scale,
+                          cfg.growth_factor, cfg.backoff_factor, cfg.growth_interval,
+                          fp8_shapes=fp8_shapes, fp8_scaling=fp8_scaling, sr_seed=seed,
+                          sr_tensor_ids=ids,
+                          sr_fp8_ids=[fp8.index(i) for i in full if cfg.specs[i].fp8])
+    gh = [to_host_bits(st.grads[i]) for i in full]
+    for _ in range(3):
+        st.step()
+        assert orc.run(gh) == 0
+        s = st.state()
+        assert (s["scale"], s["growth_tracker"], s["step"]) == (orc.scale, orc.tracker, orc.step)
+    for pos, i in enumerate(full):
+        for got, ref in ((st.master[i], orc.master[pos]), (st.exp_avg[i], orc.exp_avg[pos]),
+                         (st.exp_avg_sq[i], orc.exp_avg_sq[pos])):
+            assert np.array_equal(to_host_bits(got).view(np.uint32), ref.view(np.uint32)), names[i]
+        assert np.array_equal(to_host_bits(st.bf16[i]), orc.bf16[pos]), names[i]
+        if cfg.specs[i].fp8:
+            j = fp8.index(i)
+            assert np.array_equal(to_host_bits(st.fp8[j].view(torch.uint8)).ravel(),
+                                  orc.fp8[pos]), names[i]
+            assert np.array_equal(to_host_bits(st.fp8_t[j].view(torch.uint8)).ravel(),
+                                  orc.fp8_t[pos]), names[i]
+            assert to_host_bits(st.inv_scale)[j] == orc.inv_scale[orc.slots[pos]]
+    st.check()
+    st.close()
+    del st, info
+    torch.cuda.empty_cache()
+
+
 def test_fp8_sweep_rowwise_full_parity(A):
     """The sweep matrices with per-row / per-column scales, every byte and scale."""
     dev = torch.device("cuda:0")

@@ -681,6 +681,40 @@ def test_stochastic_rounding_probability_is_exact():
         assert np.all(np.signbit(O.decode("bf16", out)) == np.signbit(p)), pv
 
 
+@pytest.mark.parametrize("fp8_scaling", ["dynamic", "delayed"])
+def test_step_oracle_stream_ids_are_only_labels(fp8_scaling):
+    """AmpStepOracle's explicit random-stream words (for a subset of a larger
+    set): given the words it would derive itself, the run is identical; given
+    other words, the stochastically rounded copies change while master, m and
+    v do not (the streams feed only the roundings)."""
+    rng = np.random.default_rng(5)
+    shapes = [(64, 96), None, (32, 48)]
+    master = [(rng.standard_normal(64 * 96) * 0.02).astype(np.float32),
+              (rng.standard_normal(300) * 0.02).astype(np.float32),
+              (rng.standard_normal(32 * 48) * 0.02).astype(np.float32)]
+    grads = [(rng.standard_normal(m.size) * 1e-3 * 1024).astype(np.float16).view(np.uint16)
+             for m in master]
+    hyper = (1e-3, 0.9, 0.999, 1e-8, 0.01, 1024.0, 2.0, 0.5, 10)
+    own = [0 | (1 << 30), 0, 1 | (1 << 30)] if fp8_scaling == "delayed" else [0, 1, 2]
+
+    def run(**kw):
+        o = O.AmpStepOracle(master, "f16", *hyper, fp8_shapes=shapes, fp8_scaling=fp8_scaling,
+                            sr_seed=99, **kw)
+        for _ in range(2):
+            o.run([g.copy() for g in grads])
+        return o
+
+    a, b = run(), run(sr_tensor_ids=own, sr_fp8_ids=[0, 1])
+    c = run(sr_tensor_ids=[x + 5 for x in own], sr_fp8_ids=[7, 8])
+    for i in range(3):
+        assert np.array_equal(a.bf16[i], b.bf16[i])
+        assert np.array_equal(a.master[i], c.master[i]) and np.array_equal(a.exp_avg_sq[i],
+                                                                           c.exp_avg_sq[i])
+    assert all(np.array_equal(a.fp8[i], b.fp8[i]) for i in (0, 2))
+    assert not np.array_equal(a.bf16[0], c.bf16[0])
+    assert not np.array_equal(a.fp8[2], c.fp8[2])
+
+
 def test_adamw_with_stochastic_rounding_keeps_master_and_rounds_copy():
     rng = np.random.default_rng(62)
     p0 = [rng.standard_normal(5000).astype(F32) * F32(0.02)]
