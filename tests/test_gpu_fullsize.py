@@ -15,7 +15,8 @@ times (AmpOptimizerStep over the whole parameter set).
 * 8B Llama-3 set, the bench's own state (flat buffers, FP8 weights), with
   dynamic and with delayed FP8 scaling: 3 steps; two FP8 weights and a norm
   vector in full through the oracle (bf16, amax or amax history, inv_scale,
-  row-major and transposed bytes), sampled elements elsewhere.
+  row-major and transposed bytes), sampled elements elsewhere.  The same
+  state with both copies rounded stochastically: three tensors in full.
 """
 import numpy as np
 import pytest
