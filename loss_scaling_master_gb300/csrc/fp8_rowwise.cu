@@ -40,6 +40,13 @@ __device__ __forceinline__ uint32_t abs_f32_bits(const void *x, int64_t k) {
     return XT == kBF16 ? (h << 16) : __float_as_uint(f16_bits_to_f32(h));
 }
 
+// A 16-bit magnitude pattern (sign clear) as the fp32 pattern of the same
+// value, as abs_f32_bits gives it; 0 stays 0.
+template <int XT>
+__device__ __forceinline__ uint32_t widen16(uint32_t h) {
+    return XT == kBF16 ? (h << 16) : __float_as_uint(f16_bits_to_f32(h));
+}
+
 // |x| bit patterns (as abs_f32_bits) of 8 consecutive elements held in one
 // (16-bit types) or two (fp32) 16-byte words
 template <int XT>
@@ -105,7 +112,9 @@ __global__ void rowcol_zero_kernel(float *amax_row, int64_t rows, float *amax_co
 // [m S, m S + S) of every strip, so the pass sweeps x from top to bottom (the
 // cast then walks the tiles in reverse and meets the last reads in L2).  Per
 // tile, each thread holds 8 rows x 8 columns: row maxima are combined across
-// the 16 lanes sharing a row and sent with one atomicMax per row; column
+// the 16 lanes sharing a row (16-bit x: on packed magnitudes, by a transposing
+// reduction of five shuffles that leaves each row in one lane pair) and sent
+// with one atomicMax per row; column
 // maxima stay in registers for the whole strip and are combined through
 // shared memory once, at the end.  The next tile's loads are issued before
 // the current tile is reduced.  Tiles on a ragged edge, or with sizes/
@@ -128,6 +137,7 @@ __global__ void __launch_bounds__(kThreads) rowcol_amax_kernel(const void *x, in
     const int c8 = threadIdx.x & 15, rb = threadIdx.x >> 4;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t cm[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    uint32_t cm2[4] = {0, 0, 0, 0};  // 16-bit x: packed column maxima of the fast tiles
     uint4 raw[8][nw];
     auto load = [&](int64_t r0, int64_t c0) {
 #pragma unroll
@@ -139,6 +149,13 @@ __global__ void __launch_bounds__(kThreads) rowcol_amax_kernel(const void *x, in
     };
     // column maxima gathered in registers for the strip -> one atomicMax per column
     auto flush = [&]() {
+        if constexpr (XT != kF32) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                cm[2 * j] = max(cm[2 * j], widen16<XT>(cm2[j] & 0xFFFFu));
+                cm[2 * j + 1] = max(cm[2 * j + 1], widen16<XT>(cm2[j] >> 16));
+            }
+        }
 #pragma unroll
         for (int j = 0; j < 8; ++j) cm[j] = max(cm[j], __shfl_xor_sync(0xFFFFFFFFu, cm[j], 16));
         if (lane < 16) {
@@ -160,7 +177,48 @@ __global__ void __launch_bounds__(kThreads) rowcol_amax_kernel(const void *x, in
     for (int64_t tr = tr0; tr < tiles_r; tr += per_strip) {
         const int64_t r0 = tr * kTile, nr0 = r0 + int64_t(per_strip) * kTile;
         const bool has_next = tr + per_strip < tiles_r;
-        if (tile_fast(x, rows, cols, r0, c0)) {
+        if (XT != kF32 && tile_fast(x, rows, cols, r0, c0)) {
+            // 16-bit x: packed magnitudes (unsigned order = order of |x|, NaN
+            // above inf), widened to fp32 patterns only for the atomics
+            uint32_t mg[8][4];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                mg[k][0] = raw[k][0].x & 0x7FFF7FFFu;
+                mg[k][1] = raw[k][0].y & 0x7FFF7FFFu;
+                mg[k][2] = raw[k][0].z & 0x7FFF7FFFu;
+                mg[k][3] = raw[k][0].w & 0x7FFF7FFFu;
+            }
+            if (has_next && tile_fast(x, rows, cols, nr0, c0)) load(nr0, c0);
+            // pk[i]: the maxima of rows rb + 32 i (low half) and rb + 32 i + 16
+            uint32_t pk[4];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) cm2[j] = __vmaxu2(cm2[j], mg[k][j]);
+                const uint32_t r2 = __vmaxu2(__vmaxu2(mg[k][0], mg[k][1]), __vmaxu2(mg[k][2], mg[k][3]));
+                const uint32_t r16 = max(r2 & 0xFFFFu, r2 >> 16);
+                if (k & 1) pk[k >> 1] |= r16 << 16;
+                else pk[k >> 1] = r16;
+            }
+            // transposing reduction over the 16 lanes of the row (c8 bits 3..0):
+            // each step hands half of the words to the partner and keeps the
+            // other half, so lane c8 ends with pk[2 b3 + b2] over all 16 lanes
+            const bool b3 = c8 & 8, b2 = c8 & 4;
+            const uint32_t k0 = b3 ? pk[2] : pk[0], k1 = b3 ? pk[3] : pk[1];
+            const uint32_t s0 = b3 ? pk[0] : pk[2], s1 = b3 ? pk[1] : pk[3];
+            const uint32_t q0 = __vmaxu2(k0, __shfl_xor_sync(0xFFFFFFFFu, s0, 8));
+            const uint32_t q1 = __vmaxu2(k1, __shfl_xor_sync(0xFFFFFFFFu, s1, 8));
+            uint32_t rr = __vmaxu2(b2 ? q1 : q0, __shfl_xor_sync(0xFFFFFFFFu, b2 ? q0 : q1, 4));
+            rr = __vmaxu2(rr, __shfl_xor_sync(0xFFFFFFFFu, rr, 2));
+            rr = __vmaxu2(rr, __shfl_xor_sync(0xFFFFFFFFu, rr, 1));
+            // lanes with c8 & 3 == 0 / 1 send the low / high row of pk[2 b3 + b2]
+            if ((c8 & 2) == 0) {
+                const int i = (b3 ? 2 : 0) + (b2 ? 1 : 0);
+                const uint32_t h = (c8 & 1) ? (rr >> 16) : (rr & 0xFFFFu);
+                const uint32_t v = widen16<XT>(h);
+                if (v != 0) atomicMax(amax_row + r0 + rb + 32 * i + 16 * (c8 & 1), v);
+            }
+        } else if (tile_fast(x, rows, cols, r0, c0)) {
             uint32_t a[8][8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) raw_abs<XT>(raw[k], a[k]);
