@@ -230,15 +230,36 @@ __device__ __forceinline__ void group_tile(const void *x, int64_t rows, int64_t 
                 const uint32_t rm16 = max(m2 & 0xFFFFu, m2 >> 16);
                 rpair[k >> 1] = (k & 1) ? (rpair[k >> 1] | (rm16 << 16)) : rm16;
             }
+            // rrow: G >= 64, after a transposing reduction over the G / 8 lanes
+            // of the row group, lane gl = c8 mod (G / 8) holds (in the half gl
+            // & 1) the maximum of row rb + 16 (gl mod 8): the words are halved
+            // between partners on lane bits 2 and 1, then reduced whole over
+            // the remaining bits.  G = 32 reduces every word over its 4 lanes.
+            uint32_t rrow = 0;
+            if constexpr (G >= 64) {
+                const bool b2 = c8 & 4, b1 = c8 & 2;
+                const uint32_t q0 = max_u16x2(b2 ? rpair[2] : rpair[0],
+                                              __shfl_xor_sync(0xFFFFFFFFu, b2 ? rpair[0] : rpair[2], 4));
+                const uint32_t q1 = max_u16x2(b2 ? rpair[3] : rpair[1],
+                                              __shfl_xor_sync(0xFFFFFFFFu, b2 ? rpair[1] : rpair[3], 4));
+                rrow = max_u16x2(b1 ? q1 : q0, __shfl_xor_sync(0xFFFFFFFFu, b1 ? q0 : q1, 2));
+                rrow = max_u16x2(rrow, __shfl_xor_sync(0xFFFFFFFFu, rrow, 1));
+                if (G == 128) rrow = max_u16x2(rrow, __shfl_xor_sync(0xFFFFFFFFu, rrow, 8));
+            } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+                for (int i = 0; i < 4; ++i) {
 #pragma unroll
-                for (int off = G / 16; off > 0; off >>= 1)
-                    rpair[i] = max_u16x2(rpair[i], __shfl_xor_sync(0xFFFFFFFFu, rpair[i], off));
-                if (!kRegs && (c8 & (G / 8 - 1)) == 0) {
-                    s_rmax[rb + 32 * i][(8 * c8) / G] = widen(rpair[i]);
-                    s_rmax[rb + 32 * i + 16][(8 * c8) / G] = widen(rpair[i] >> 16);
+                    for (int off = G / 16; off > 0; off >>= 1)
+                        rpair[i] = max_u16x2(rpair[i], __shfl_xor_sync(0xFFFFFFFFu, rpair[i], off));
+                    if ((c8 & (G / 8 - 1)) == 0) {
+                        s_rmax[rb + 32 * i][(8 * c8) / G] = widen(rpair[i]);
+                        s_rmax[rb + 32 * i + 16][(8 * c8) / G] = widen(rpair[i] >> 16);
+                    }
                 }
+            }
+            if constexpr (!kRegs && G >= 64) {
+                const int gl = c8 & (G / 8 - 1);
+                if (gl < 8) s_rmax[rb + 16 * gl][(8 * c8) / G] = widen((gl & 1) ? rrow >> 16 : rrow);
             }
             if constexpr (kRegs) {
                 // Every lane of a row group now holds the maxima of its 8 rows.
@@ -250,9 +271,7 @@ __device__ __forceinline__ void group_tile(const void *x, int64_t rows, int64_t 
                 float s32 = 0.0f;
                 bool odd = false;
                 if (gl < 8) {
-                    const uint32_t pr = gl < 2 ? rpair[0] : gl < 4 ? rpair[1]
-                                      : gl < 6 ? rpair[2] : rpair[3];
-                    const float a = __uint_as_float(widen((gl & 1) ? pr >> 16 : pr));
+                    const float a = __uint_as_float(widen((gl & 1) ? rrow >> 16 : rrow));
                     float inv;
                     tensor_scale(a, ef, fmax, s32, inv);
                     odd = !scale_keeps_finite(s32);
