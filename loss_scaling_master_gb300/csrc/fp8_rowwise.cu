@@ -11,7 +11,8 @@
 //          columns of a tile; row maxima are combined across the 16 lanes
 //          sharing a row (one atomicMax per row and tile), column maxima stay
 //          in registers for the strip (one atomicMax per column at the end);
-//          fp32 bit patterns of |x|: an unsigned max that propagates NaN
+//          fp32 bit patterns of |x| (16-bit x: 16-bit patterns, widened for
+//          the atomics): an unsigned max that propagates NaN
 //   scale  per row and per column, fp32 multiplier and inverse written once,
 //          by fp32 divisions equal to the fp64 formula rounded to fp32
 //          (tensor_scale in fp8_tile.cuh)
@@ -111,15 +112,14 @@ __global__ void rowcol_zero_kernel(float *amax_row, int64_t rows, float *amax_co
 // b / C + S, b / C + 2S, ...  At step m the CTAs together read tile rows
 // [m S, m S + S) of every strip, so the pass sweeps x from top to bottom (the
 // cast then walks the tiles in reverse and meets the last reads in L2).  Per
-// tile, each thread holds 8 rows x 8 columns: row maxima are combined across
-// the 16 lanes sharing a row (16-bit x: on packed magnitudes, by a transposing
-// reduction of five shuffles that leaves each row in one lane pair) and sent
-// with one atomicMax per row; column
-// maxima stay in registers for the whole strip and are combined through
-// shared memory once, at the end.  The next tile's loads are issued before
-// the current tile is reduced.  Tiles on a ragged edge, or with sizes/
-// addresses that break 16-byte access, take an element path through shared
-// memory.
+// tile, each thread holds 8 rows x 8 columns.  Row maxima are combined across
+// the 16 lanes sharing a row and sent with one atomicMax per row; for 16-bit
+// x on packed magnitudes, by a transposing reduction of five shuffles that
+// leaves each row in one lane pair.  Column maxima stay in registers for the
+// whole strip and are combined through shared memory once, at the end.  The
+// next tile's loads are issued before the current tile is reduced.  Tiles on
+// a ragged edge, or with sizes/addresses that break 16-byte access, take an
+// element path through shared memory.
 template <int XT>
 __global__ void __launch_bounds__(kThreads) rowcol_amax_kernel(const void *x, int64_t rows,
                                                                int64_t cols, unsigned *amax_row,
