@@ -210,7 +210,7 @@ __device__ __forceinline__ void group_tile(const void *x, int64_t rows, int64_t 
             auto widen = [](uint32_t h) {
                 return __float_as_uint(lowp_to_f32<XT>(h & 0xFFFFu)) & 0x7FFFFFFFu;
             };
-            uint32_t colg[NG][4], rpair[4];
+            uint32_t colg[NG][4], rpair[4], m2[8];
 #pragma unroll
             for (int q = 0; q < NG; ++q)
 #pragma unroll
@@ -220,16 +220,19 @@ __device__ __forceinline__ void group_tile(const void *x, int64_t rows, int64_t 
                 const uint4 u = *raw(k);
                 const uint32_t w[4] = {u.x, u.y, u.z, u.w};
                 const int q = (16 * k) / G;
-                uint32_t m2 = 0;
+                m2[k] = 0;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const uint32_t a = w[j] & 0x7FFF7FFFu;
-                    m2 = max_u16x2(m2, a);
+                    m2[k] = max_u16x2(m2[k], a);
                     colg[q][j] = max_u16x2(colg[q][j], a);
                 }
-                const uint32_t rm16 = max(m2 & 0xFFFFu, m2 >> 16);
-                rpair[k >> 1] = (k & 1) ? (rpair[k >> 1] | (rm16 << 16)) : rm16;
             }
+            // rows k = 2i, 2i + 1: low halves side by side against high halves
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                rpair[i] = max_u16x2(__byte_perm(m2[2 * i], m2[2 * i + 1], 0x5410),
+                                     __byte_perm(m2[2 * i], m2[2 * i + 1], 0x7632));
             // rrow: G >= 64, after a transposing reduction over the G / 8 lanes
             // of the row group, lane gl = c8 mod (G / 8) holds (in the half gl
             // & 1) the maximum of row rb + 16 (gl mod 8): the words are halved

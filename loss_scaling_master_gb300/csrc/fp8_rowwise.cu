@@ -190,16 +190,19 @@ __global__ void __launch_bounds__(kThreads) rowcol_amax_kernel(const void *x, in
             }
             if (has_next && tile_fast(x, rows, cols, nr0, c0)) load(nr0, c0);
             // pk[i]: the maxima of rows rb + 32 i (low half) and rb + 32 i + 16
-            uint32_t pk[4];
+            uint32_t pk[4], r2[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) cm2[j] = __vmaxu2(cm2[j], mg[k][j]);
-                const uint32_t r2 = __vmaxu2(__vmaxu2(mg[k][0], mg[k][1]), __vmaxu2(mg[k][2], mg[k][3]));
-                const uint32_t r16 = max(r2 & 0xFFFFu, r2 >> 16);
-                if (k & 1) pk[k >> 1] |= r16 << 16;
-                else pk[k >> 1] = r16;
+                r2[k] = __vmaxu2(__vmaxu2(mg[k][0], mg[k][1]), __vmaxu2(mg[k][2], mg[k][3]));
             }
+            // rows 2i and 2i + 1: their low halves side by side against their
+            // high halves, one packed max
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                pk[i] = __vmaxu2(__byte_perm(r2[2 * i], r2[2 * i + 1], 0x5410),
+                                 __byte_perm(r2[2 * i], r2[2 * i + 1], 0x7632));
             // transposing reduction over the 16 lanes of the row (c8 bits 3..0):
             // each step hands half of the words to the partner and keeps the
             // other half, so lane c8 ends with pk[2 b3 + b2] over all 16 lanes
