@@ -655,7 +655,7 @@ def run_configs(args, device) -> dict:
         gc.collect()
         torch.cuda.empty_cache()
         a = argparse.Namespace(**vars(args))
-        a.workload, a.fp8_granularity, a.steps, a.warmup = "fp8_sweep", gran, 20, 3
+        a.workload, a.fp8_granularity, a.steps, a.warmup = "fp8_sweep", gran, 30, 5
         out[f"fp8_sweep_{gran}"] = _condense(run_fp8_sweep(a, 0, 1, device))
     if not args.no_cpu_baseline:
         out["fp8_sweep_tensorwise"]["cpu_baseline"] = cpu_baseline_sweep(min(args.cpu_seconds, 4.0))
