@@ -89,7 +89,8 @@ class AmpOptimizerStep:
         self._state_host = A.ScalerState()
         self.grad_sumsq = torch.zeros(1, dtype=torch.float64, device=dev)
         self.fp8_eps = fp8_eps
-        mk = lambda ts, two_d=False: A.amp_tensor_list_create(ts, two_d=two_d, stream=stream)
+        mk = lambda ts, two_d=False, dt=None: A.amp_tensor_list_create(ts, two_d=two_d, dtype=dt,
+                                                                        stream=stream)
         self.L_master, self.L_m, self.L_v = mk(self.master), mk(self.exp_avg), mk(self.exp_avg_sq)
         self.L_g = mk(self.grads)
         self.grad_lists = [self.L_g]
@@ -125,12 +126,14 @@ class AmpOptimizerStep:
                 self.fp8_t.append(torch.empty((sh[1], sh[0]), dtype=fp8_tdt,
                                               device=dev))
             A.amp_tensor_list_set_amax_slots(self.L_b, slots, stream=stream)
-            self.L_x8 = mk(xs, True)
+            # explicit dtypes: a flat shard may hold no FP8 weight at all, and
+            # still takes part in the amax exchange through empty lists
+            self.L_x8 = mk(xs, True, "bf16")
             if self.flat:
                 A.amp_tensor_list_set_amax_slots(self.L_x8, [x for x in slots if x >= 0],
                                                  stream=stream)
-            self.L_q = mk(self.fp8, True)
-            self.L_qt = mk(self.fp8_t, True)
+            self.L_q = mk(self.fp8, True, fp8_format)
+            self.L_qt = mk(self.fp8_t, True, fp8_format)
         # amax / inv_scale entries: one per FP8 weight of this object, or (flat
         # shards) one per FP8 weight of the whole model
         self.n_amax = int(n_fp8_total) if self.flat else self.n_fp8
