@@ -139,6 +139,11 @@ class AmpOptimizerStep:
         self.n_amax = int(n_fp8_total) if self.flat else self.n_fp8
         self.amax = torch.zeros(max(self.n_amax, 1), dtype=torch.float32, device=dev)
         self.inv_scale = torch.zeros(max(self.n_amax, 1), dtype=torch.float32, device=dev)
+        if fp8_scaling == "delayed" and fp8_shapes is not None and not self.n_fp8:
+            # no FP8 weight in this set (a data-parallel shard can own none):
+            # nothing to cast and no history to keep, so the step is the plain
+            # one, with the same exchanges as the other ranks
+            fp8_scaling = "dynamic"
         self.fp8_scaling = fp8_scaling
         self.hist_len = amax_history_len
         self.sr_seed = sr_seed

@@ -1102,6 +1102,45 @@ def test_fp8_stochastic_rule_dense_over_fp32_patterns(A, dev, fmt):
 
 
 # --------------------------------------------------------- checkpoint / resume
+def test_delayed_scaling_without_fp8_weights_is_the_plain_step(A, dev):
+    """A set given fp8_shapes with no FP8 weight in it (a data-parallel shard
+    can own none) and delayed scaling steps exactly as the plain dynamic step:
+    nothing to cast, no history; master, m, v, bf16 and the scaler state equal
+    the plain step's bit for bit through a skipped step."""
+    from loss_scaling_master_gb300 import AmpOptimizerStep
+    rng = np.random.default_rng(111)
+    sizes = [1000, 4097, 300]
+    master = [(rng.standard_normal(n) * 0.02).astype(np.float32) for n in sizes]
+    grads = []
+    for k in range(3):
+        g = [(rng.standard_normal(n) * 1e-5 * 1024).astype(np.float16).view(np.uint16)
+             for n in sizes]
+        if k == 1:
+            g[2][7] = 0x7C00
+        grads.append(g)
+    runs = []
+    for kw in (dict(fp8_shapes=[None, None, None], fp8_scaling="delayed"), dict()):
+        P = [to_device(m, "f32", dev) for m in master]
+        G = [torch.empty(n, dtype=torch.float16, device=dev) for n in sizes]
+        st = AmpOptimizerStep(P, G, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8,
+                              weight_decay=0.01, init_scale=1024.0, growth_interval=2, **kw)
+        assert st.fp8_scaling == "dynamic" and st.n_fp8 == 0
+        trace = []
+        for g in grads:
+            for t, h in zip(G, g):
+                t.copy_(to_device(h, "f16", dev))
+            st.step()
+            s = st.state()
+            trace.append((s["scale"], s["growth_tracker"], s["step"]))
+        runs.append((trace, [to_host_bits(x) for x in st.master + st.exp_avg + st.exp_avg_sq],
+                     [to_host_bits(x) for x in st.bf16]))
+        st.check()
+        st.close()
+    assert runs[0][0] == runs[1][0] and runs[0][0][1][2] == runs[0][0][0][2]
+    for a, b in zip(runs[0][1] + runs[0][2], runs[1][1] + runs[1][2]):
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+
+
 @pytest.mark.parametrize("fp8_scaling", ["dynamic", "delayed"])
 def test_checkpoint_resume_is_bit_identical(A, dev, fp8_scaling):
     """Save the state after 3 steps, restore it into a fresh step object and
