@@ -63,7 +63,9 @@ class AmpOptimizerStep:
         before the FP8 cast (dynamic scaling, round-to-nearest).  Without
         fp8_slots whole tensors belong to one rank and the amax needs no
         exchange."""
-        dev = master[0].device
+        # a data-parallel shard may hold no tensor at all (partition_flat can
+        # give a rank an empty slice); it still takes part in every exchange
+        dev = master[0].device if len(master) else torch.device("cuda", torch.cuda.current_device())
         self.stream = stream
         self.master = list(master)
         self.grads = list(grads)
@@ -91,11 +93,15 @@ class AmpOptimizerStep:
         self.fp8_eps = fp8_eps
         mk = lambda ts, two_d=False, dt=None: A.amp_tensor_list_create(ts, two_d=two_d, dtype=dt,
                                                                         stream=stream)
-        self.L_master, self.L_m, self.L_v = mk(self.master), mk(self.exp_avg), mk(self.exp_avg_sq)
-        self.L_g = mk(self.grads)
+        # empty lists take their dtype explicitly; others take it from their tensors
+        e = lambda ts, dt: None if len(ts) else dt
+        self.L_master = mk(self.master, dt=e(self.master, "f32"))
+        self.L_m = mk(self.exp_avg, dt=e(self.exp_avg, "f32"))
+        self.L_v = mk(self.exp_avg_sq, dt=e(self.exp_avg_sq, "f32"))
+        self.L_g = mk(self.grads, dt=e(self.grads, "f16"))
         self.grad_lists = [self.L_g]
         self.graphs = {}
-        self.L_b = mk(self.bf16) if emit_bf16 else None
+        self.L_b = mk(self.bf16, dt=e(self.bf16, "bf16")) if emit_bf16 else None
         self.n_fp8 = 0
         self.fp8, self.fp8_t = [], []
         self.flat = fp8_slots is not None
@@ -222,7 +228,8 @@ class AmpOptimizerStep:
         if [g.numel() for g in grads] != [g.numel() for g in self.grads] or \
                 any(a.dtype != b.dtype for a, b in zip(grads, self.grads)):
             raise ValueError("gradient buffers must match the first set in sizes and dtype")
-        self.grad_lists.append(A.amp_tensor_list_create(grads, stream=self.stream))
+        self.grad_lists.append(A.amp_tensor_list_create(
+            grads, dtype=None if grads else self.L_g.dtype, stream=self.stream))
         if self.fp8_scaling == "delayed":
             self.delayed_groups.append(self._groups(grads))
         return len(self.grad_lists) - 1

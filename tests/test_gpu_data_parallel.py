@@ -223,43 +223,51 @@ def test_flat_shards_on_one_gpu_match_the_unsharded_step(world):
         assert np.array_equal(full0[t].ravel(), first[t])
 
 
-# --------------------------- flat shards: ranks that hold no FP8 weight at all
-PLAIN_SHAPES = [(64, 64), (128, 64), (20000,), (20000,)]
-PLAIN_FP8 = [0, 1, None, None]          # both FP8 weights fall inside rank 0's slice
+# ------------------- flat shards: ranks with no FP8 weight, and an empty rank
+# case: (shapes, global FP8 index per tensor, world, (tensor, element, step) of a +inf)
+CASES = {
+    # both FP8 weights fall inside rank 0's slice; ranks 1-3 hold plain tensors only
+    "no_fp8": ([(64, 64), (128, 64), (20000,), (20000,)], [0, 1, None, None], 4, (3, 15000, 2)),
+    # the 32-row weight is cut in two 16-row bands; rank 1's slice is empty
+    "empty_rank": ([(32, 64), (16,)], [0, None], 3, (1, 5, 2)),
+}
 
 
-def _plain_inputs():
+def _case_inputs(case):
+    shapes, _, _, (ti, ei, si) = CASES[case]
     rng = np.random.default_rng(79)
-    sizes = [int(np.prod(s)) for s in PLAIN_SHAPES]
+    sizes = [int(np.prod(s)) for s in shapes]
     master = [(rng.standard_normal(n) * 0.02).astype(np.float32) for n in sizes]
     grads = []
     for step in range(4):
         g = [(rng.standard_normal(n) * 1e-5 * 65536).astype(np.float16).view(np.uint16)
              for n in sizes]
-        if step == 2:
-            g[3][15000] = 0x7C00     # +inf in the last rank's plain slice
+        if step == si:
+            g[ti][ei] = 0x7C00
         grads.append(g)
     return master, grads
 
 
-def _rank_plain(rank, world, port, q):
+def _rank_case(rank, world, port, q, case):
     import torch
     import torch.distributed as dist
 
     import loss_scaling_master_gb300 as A
     from loss_scaling_master_gb300.sharded import partition_flat
+    shapes_all, fp8_all, _, _ = CASES[case]
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
+    torch.cuda.set_device(0)
     dev = torch.device("cuda:0")
-    pieces = partition_flat(PLAIN_SHAPES, world)[rank]
-    master, grads = _plain_inputs()
+    pieces = partition_flat(shapes_all, world)[rank]
+    master, grads = _case_inputs(case)
     P = [torch.from_numpy(master[t][b:e].copy()).to(dev) for t, b, e in pieces]
     G = [torch.empty(e - b, dtype=torch.float16, device=dev) for t, b, e in pieces]
-    shapes = [((e - b) // PLAIN_SHAPES[t][1], PLAIN_SHAPES[t][1]) if PLAIN_FP8[t] is not None
+    shapes = [((e - b) // shapes_all[t][1], shapes_all[t][1]) if fp8_all[t] is not None
               else None for t, b, e in pieces]
     st = A.AmpOptimizerStep(P, G, **HYPER, init_scale=65536.0, growth_interval=2,
-                            fp8_shapes=shapes, fp8_slots=[PLAIN_FP8[t] for t, _, _ in pieces],
-                            n_fp8_total=2, data_parallel=True)
+                            fp8_shapes=shapes, fp8_slots=[fp8_all[t] for t, _, _ in pieces],
+                            n_fp8_total=sum(x is not None for x in fp8_all), data_parallel=True)
     states = []
     for g in grads:
         for tt, (t, b, e) in zip(G, pieces):
@@ -278,25 +286,29 @@ def _rank_plain(rank, world, port, q):
     dist.destroy_process_group()
 
 
-def test_flat_shards_with_ranks_holding_no_fp8_weight():
-    """Four ranks, of which three hold only plain tensors: they still join the
-    amax all-reduce (at the first working copies and every step), so no
-    collective waits for them; an inf in the last rank's slice makes every rank
-    skip; every piece equals the unsharded oracle step bit for bit, and rank
-    0's FP8 copies and inv_scale too."""
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_flat_shards_with_ranks_holding_no_fp8_weight_or_nothing(case):
+    """Flat shards where some ranks hold no FP8 weight ("no_fp8": three of
+    four ranks hold plain tensors only) or nothing at all ("empty_rank": the
+    middle one of three slices is empty).  Every rank still takes part in the
+    found_inf and amax exchanges, from the first working copies on, so no
+    collective waits for it; an inf on one rank makes every rank skip; every
+    piece equals the unsharded oracle step bit for bit, the FP8 bands, their
+    transposed slices and the owners' inv_scale too."""
     import oracle as O
-    world, port = 4, _free_port()
+    shapes_all, fp8_all, world, _ = CASES[case]
+    port = _free_port()
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
-    procs = [ctx.Process(target=_rank_plain, args=(r, world, port, q)) for r in range(world)]
+    procs = [ctx.Process(target=_rank_case, args=(r, world, port, q, case)) for r in range(world)]
     for pr in procs:
         pr.start()
     res = [q.get(timeout=300) for _ in range(world)]
     for pr in procs:
         pr.join(timeout=120)
         assert pr.exitcode == 0
-    master, grads = _plain_inputs()
-    fp8_shapes = [s if PLAIN_FP8[i] is not None else None for i, s in enumerate(PLAIN_SHAPES)]
+    master, grads = _case_inputs(case)
+    fp8_shapes = [s if fp8_all[i] is not None else None for i, s in enumerate(shapes_all)]
     orc = O.AmpStepOracle(master, "f16", HYPER["lr"], HYPER["beta1"], HYPER["beta2"],
                           HYPER["eps"], HYPER["weight_decay"], 65536.0, 2.0, 0.5, 2,
                           fp8_shapes=fp8_shapes)
@@ -305,19 +317,29 @@ def test_flat_shards_with_ranks_holding_no_fp8_weight():
         orc.run([x.copy() for x in g])
         trace.append((orc.scale, orc.tracker, orc.step))
     assert trace[2][2] == trace[1][2]                         # the inf step is skipped
-    fp8_ranks = set()
+    full = {t: np.zeros(shapes_all[t], np.uint8) for t in range(len(shapes_all))
+            if fp8_all[t] is not None}
+    full_t = {t: np.zeros(shapes_all[t][::-1], np.uint8) for t in full}
+    holders = {t: set() for t in full}
     for rank, pieces, states, out in res:
         assert [(s["scale"], s["growth_tracker"], s["step"]) for s in states] == trace
         j = 0
         for k, (t, b, e) in enumerate(pieces):
             assert np.array_equal(out["p"][k].view(np.uint32), orc.master[t][b:e].view(np.uint32))
             assert np.array_equal(out["bf"][k], orc.bf16[t][b:e])
-            if PLAIN_FP8[t] is None:
+            if fp8_all[t] is None:
                 continue
-            fp8_ranks.add(rank)
-            assert (b, e) == (0, int(np.prod(PLAIN_SHAPES[t])))   # whole weights on rank 0
-            assert np.array_equal(out["q"][j].ravel(), orc.fp8[t])
-            assert np.array_equal(out["qt"][j].ravel(), orc.fp8_t[t])
-            assert out["inv"][PLAIN_FP8[t]] == orc.inv_scale[PLAIN_FP8[t]]
+            holders[t].add(rank)
+            cols = shapes_all[t][1]
+            r0, nr = b // cols, (e - b) // cols
+            full[t][r0:r0 + nr] = out["q"][j].reshape(nr, cols)
+            full_t[t][:, r0:r0 + nr] = out["qt"][j].reshape(cols, nr)
+            assert out["inv"][fp8_all[t]] == orc.inv_scale[fp8_all[t]]
             j += 1
-    assert fp8_ranks == {0}
+    for t in full:
+        assert np.array_equal(full[t].ravel(), orc.fp8[t])
+        assert np.array_equal(full_t[t].ravel(), orc.fp8_t[t])
+    if case == "no_fp8":
+        assert set().union(*holders.values()) == {0}
+    else:
+        assert holders[0] == {0, 2} and not [p for r, p, _, _ in res if r == 1][0]
