@@ -239,7 +239,9 @@ class AmpOptimizerStep:
         gradient buffer replay it.  Every call of the step is stream-ordered
         and allocation-free, so the graph is the same calls with the same
         device pointers; the caller keeps writing each step's gradients into
-        the same buffers."""
+        the same buffers.  With data_parallel over more than one rank the
+        exchanges are recorded too, which needs collectives that can be
+        captured (NCCL's; gloo's run on the host and cannot be)."""
         s = stream if stream is not None else (self.stream or torch.cuda.Stream())
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
